@@ -1,0 +1,59 @@
+"""Layer dimensions and the standard shapes.
+
+K3 figures: 7168-d residual, 3584-d latent, 896 routed experts, top-16,
+moe_intermediate_size 3072, MXFP4 group 32, SiTU-GLU beta 4 / beta_lin 25
+(kimi-k3-mlx README, "Architecture" table; K3_ARTIFACT_AUDIT section 4.3
+for the expert tensor shapes).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, replace
+
+
+@dataclass(frozen=True)
+class LayerDims:
+    hidden: int
+    latent: int
+    n_experts: int
+    top_k: int
+    inter: int
+    group: int = 32
+    beta: float = 4.0
+    beta_lin: float = 25.0
+    rms_eps: float = 1e-6
+    routed_scaling: float = 1.0
+    norm_topk: int = 1
+
+    def with_(self, **kw) -> "LayerDims":
+        return replace(self, **kw)
+
+    # --- storage figures (bytes) -------------------------------------------------
+    def expert_bytes(self) -> int:
+        """Packed nibbles + e8m0 scales of one expert's w1, w3 and w2."""
+        gate_up = 2 * (self.inter * self.latent // 2 + self.inter * self.latent // self.group)
+        down = self.latent * self.inter // 2 + self.latent * self.inter // self.group
+        return gate_up + down
+
+    def expert_gate_up_bytes(self) -> int:
+        return 2 * (self.inter * self.latent // 2 + self.inter * self.latent // self.group)
+
+    def expert_down_bytes(self) -> int:
+        return self.latent * self.inter // 2 + self.latent * self.inter // self.group
+
+    def dense_bytes(self) -> int:
+        """Router weight + bias, down_proj, up_proj and the RMSNorm weight."""
+        return (self.n_experts * self.hidden * 2 + self.n_experts * 4 + self.latent * self.hidden * 2
+                + self.hidden * self.latent * 2 + self.latent * 2)
+
+    # --- work figures (multiply-adds counted as 2 FLOP) -------------------------
+    def expert_flop_per_token(self) -> int:
+        return self.top_k * (2 * self.latent * 2 * self.inter + 2 * self.inter * self.latent)
+
+    def flop_per_token(self) -> int:
+        router = 2 * self.n_experts * self.hidden
+        proj = 2 * 2 * self.latent * self.hidden
+        return router + proj + self.expert_flop_per_token()
+
+
+TINY = LayerDims(hidden=1024, latent=512, n_experts=64, top_k=8, inter=384)
+K3 = LayerDims(hidden=7168, latent=3584, n_experts=896, top_k=16, inter=3072)

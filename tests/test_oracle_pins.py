@@ -1,0 +1,397 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle.
+
+Each check is chosen so that a plausible slip in the oracle (a swapped
+nibble, a wrong exponent bias, a dropped term, a transposed operand, a
+bias used in the weights, a tie broken the wrong way) fails at least one:
+
+  * MXFP4 dequant: all 256 packed bytes x 256 e8m0 bytes against the
+    integer form v = (-1)^s * M[m] * 2^(S-128), M = {0,1,2,3,4,6,8,12}
+    (the OCP e2m1 table written as integers), and the low-nibble-first
+    order the pages state.
+  * bf16 rounding: against torch's float32->bfloat16 conversion and
+    hand-made ties.
+  * SiTU-GLU: closed-form limits, oddness in u, the SwiGLU limit.
+  * Router: sort-based top-k (numpy stable argsort), the pruning invariant
+    (-inf bias == expert removed), bias-shift invariance, the hot-expert
+    set, the sum of the weights.
+  * Whole layer: an independent numpy formulation that evaluates every
+    expert for every token with zero weight for unselected ones, and a
+    pure-Python brute force on a tiny layer.
+  * Work counts: the byte, parameter and PFLOP figures the pages print.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from mxfp4_routed_expert_k3_gb300 import synth
+from mxfp4_routed_expert_k3_gb300.dims import K3, TINY, LayerDims
+from oracle import oracle as ora
+
+E2M1_INT = [0, 1, 2, 3, 4, 6, 8, 12]  # e2m1 magnitudes times 2 (OCP MX FP4 table)
+
+
+# ----------------------------------------------------------------------------- helpers
+def exact_mxfp4(byte: int, hi: bool, S: int) -> float:
+    code = (byte >> 4) if hi else (byte & 0xF)
+    s, m = code >> 3, code & 7
+    if S == 255:
+        return math.nan
+    v = E2M1_INT[m] * 2.0 ** (S - 128)
+    return -v if s else v
+
+
+def bf16_rne_py(v: float) -> float:
+    """Round a float to bf16 (8 significant bits, exponent >= -126 normal,
+    subnormal spacing 2^-133, overflow to inf), written from the format."""
+    if math.isnan(v) or math.isinf(v) or v == 0.0:
+        return v
+    a = abs(v)
+    m, e = math.frexp(a)  # a = m 2^e, m in [0.5, 1)
+    E = max(e - 1, -126)
+    ulp = 2.0 ** (E - 7)
+    r = round(a / ulp) * ulp  # Python round: ties to even
+    if r >= 2.0 ** 128:
+        r = math.inf
+    return math.copysign(r, v)
+
+
+def bits_to_f64(bits):
+    return ora.bf16_to_float(bits)
+
+
+def f64_to_bits_torch(v: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.asarray(v, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+# ----------------------------------------------------------------------------- dequant
+def test_e2m1_table_is_ocp():
+    vals = [ora.e2m1_value(c) for c in range(16)]
+    expect = [0, .5, 1, 1.5, 2, 3, 4, 6, -0.0, -.5, -1, -1.5, -2, -3, -4, -6]
+    assert vals == expect
+    assert math.copysign(1.0, vals[8]) == -1.0  # code 0x8 is -0.0
+
+
+def test_e8m0_scale_values():
+    assert ora.e8m0_value(127) == 1.0
+    assert ora.e8m0_value(0) == 2.0 ** -127
+    assert ora.e8m0_value(254) == 2.0 ** 127
+    assert math.isnan(ora.e8m0_value(255))
+
+
+def test_low_nibble_first():
+    # byte 0x21 with scale 1.0: element 0 is the low nibble (code 1 = 0.5),
+    # element 1 the high nibble (code 2 = 1.0).
+    packed = np.zeros((1, 16), np.uint8)
+    packed[0, 0] = 0x21
+    scale = np.full((1, 1), 127, np.uint8)
+    out = bits_to_f64(ora.mxfp4_dequant_bf16(packed, scale))
+    assert out[0, 0] == 0.5 and out[0, 1] == 1.0 and np.all(out[0, 2:] == 0)
+
+
+def test_dequant_bruteforce_all_bytes_all_scales():
+    packed = np.tile(np.arange(256, dtype=np.uint8), (256, 1))  # row S, byte i
+    scale = np.repeat(np.arange(256, dtype=np.uint8)[:, None], 512 // 32, axis=1)
+    got = ora.mxfp4_dequant_bf16(packed, scale)
+    gotf = bits_to_f64(got)
+    for S in range(256):
+        for b in range(256):
+            for hi in (0, 1):
+                g = gotf[S, 2 * b + hi]
+                x = exact_mxfp4(b, bool(hi), S)
+                if math.isnan(x):
+                    assert math.isnan(g)
+                    continue
+                want = bf16_rne_py(x)
+                assert g == want or (math.isinf(want) and g == want), (S, b, hi, g, want)
+                if S <= 252:
+                    assert g == x  # exact: every product is a bf16 value
+                if x == 0.0:  # keep the sign of zero
+                    assert math.copysign(1.0, g) == math.copysign(1.0, x)
+
+
+def test_dequant_overflow_only_above_252():
+    packed = np.tile(np.arange(256, dtype=np.uint8), (256, 1))
+    scale = np.repeat(np.arange(256, dtype=np.uint8)[:, None], 16, axis=1)
+    f = bits_to_f64(ora.mxfp4_dequant_bf16(packed, scale))
+    assert np.all(np.isfinite(f[:253]))
+    assert np.any(np.isinf(f[253])) and np.any(np.isinf(f[254]))
+    assert np.all(np.isnan(f[255]))
+
+
+# ----------------------------------------------------------------------------- bf16
+def test_bf16_rounding_matches_torch_on_floats():
+    rng = np.random.default_rng(1)
+    vals = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32),
+        (rng.standard_normal(2000) * 1e-39).astype(np.float32),  # subnormal range
+        np.clip(rng.standard_normal(2000) * 3e38, -3.4e38, 3.4e38).astype(np.float32),
+        np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, 1 - 2 ** -9, 3.3895314e38, 2 ** -133, 2 ** -134], np.float32),
+    ])
+    ours = np.array([ora.bf16_from_double(float(v)) for v in vals], np.uint16)
+    ref = f64_to_bits_torch(vals)
+    assert np.array_equal(ours, ref)
+
+
+def test_bf16_rounding_ties_to_even_direct_from_double():
+    # 1 + 2^-8 is exactly halfway between 1 and 1 + 2^-7 -> even (1.0)
+    assert ora.bf16_from_double(1 + 2 ** -8) == 0x3F80
+    # a hair above the tie rounds up; a float detour would have lost the hair
+    assert ora.bf16_from_double(1 + 2 ** -8 + 2 ** -40) == 0x3F81
+    assert ora.bf16_from_double(1 + 3 * 2 ** -8) == 0x3F82
+    assert ora.bf16_from_double(-2.0) == 0xC000
+    assert ora.bf16_from_double(1e39) == 0x7F80
+
+
+# ----------------------------------------------------------------------------- SiTU-GLU
+def test_situ_limits():
+    for u in (-30.0, -3.0, -0.1, 0.0, 0.5, 7.0, 80.0):
+        # g -> +inf: sigmoid -> 1, tanh(g/4) -> 1
+        assert ora.situ_glu(60.0, u) == pytest.approx(4 * 25 * math.tanh(u / 25), rel=1e-12, abs=1e-12)
+        # g -> -inf: the gate closes
+        assert abs(ora.situ_glu(-60.0, u)) < 1e-20
+    # |h| < 4 * 25 everywhere
+    grid = np.linspace(-200, 200, 81)
+    assert max(abs(ora.situ_glu(g, u)) for g in grid for u in grid) < 100.0
+
+
+def test_situ_odd_in_u_and_swiglu_limit():
+    rng = np.random.default_rng(2)
+    for g, u in rng.standard_normal((50, 2)) * 5:
+        assert ora.situ_glu(g, -u) == -ora.situ_glu(g, u)
+    for g, u in rng.standard_normal((50, 2)) * 1e-3:
+        silu = g / (1 + math.exp(-g))
+        assert ora.situ_glu(g, u) == pytest.approx(silu * u, rel=1e-5)
+
+
+def test_situ_is_not_symmetric_in_g_and_u():
+    # beta = 4 on the gate, beta_lin = 25 on the linear branch: swapping fails
+    assert abs(ora.situ_glu(8.0, 2.0) - ora.situ_glu(2.0, 8.0)) > 1.0
+
+
+# ----------------------------------------------------------------------------- router
+def _keys_from_logits(logits, bias):
+    s = (1.0 / (1.0 + np.exp(-logits.astype(np.float64)))).astype(np.float32)
+    return s, (s + bias.astype(np.float32)).astype(np.float32)
+
+
+def test_router_topk_matches_sort():
+    d = TINY
+    rng = np.random.default_rng(3)
+    logits = rng.standard_normal((200, d.n_experts)).astype(np.float32)
+    bias = rng.uniform(-0.1, 0.1, d.n_experts).astype(np.float32)
+    idx, w = ora.route_from_logits(d, logits, bias)
+    s, key = _keys_from_logits(logits, bias)
+    for t in range(200):
+        order = np.argsort(-key[t], kind="stable")[: d.top_k]
+        assert np.array_equal(idx[t], order)
+        sel = s[t, order].astype(np.float64)
+        assert np.allclose(w[t], sel / sel.sum(), rtol=1e-6)
+        assert abs(float(w[t].astype(np.float64).sum()) - 1.0) < 1e-6
+        # the weights use the unbiased score, not the key
+        assert not np.allclose(w[t], key[t, order] / key[t, order].sum(), rtol=1e-6)
+
+
+def test_router_ties_go_to_lower_id():
+    d = LayerDims(hidden=64, latent=64, n_experts=8, top_k=3, inter=64)
+    logits = np.zeros((1, 8), np.float32)
+    bias = np.array([0, 0.5, 0.5, 0, 0.5, 0, 0.5, 0], np.float32)
+    idx, _ = ora.route_from_logits(d, logits, bias)
+    assert idx[0].tolist() == [1, 2, 4]
+
+
+def test_router_pruning_invariant_and_bias_shift():
+    d = TINY
+    rng = np.random.default_rng(4)
+    logits = rng.standard_normal((64, d.n_experts)).astype(np.float32)
+    bias = rng.uniform(-0.1, 0.1, d.n_experts).astype(np.float32)
+    pruned = bias.copy()
+    drop = [3, 17, 40]
+    pruned[drop] = -np.inf
+    idx_p, w_p = ora.route_from_logits(d, logits, pruned)
+    keep = np.array([e for e in range(d.n_experts) if e not in drop])
+    d_small = d.with_(n_experts=len(keep))
+    idx_s, w_s = ora.route_from_logits(d_small, np.ascontiguousarray(logits[:, keep]), bias[keep])
+    assert np.array_equal(idx_p, keep[idx_s])
+    assert np.array_equal(w_p, w_s)
+    # a constant shift of the bias (exact in fp32 here) never changes the selection
+    idx0, _ = ora.route_from_logits(d, logits, bias)
+    idx1, _ = ora.route_from_logits(d, logits, (bias + np.float32(0.25)).astype(np.float32))
+    assert np.array_equal(idx0, idx1)
+
+
+def test_router_hot_set_and_scaling_options():
+    d = TINY
+    w = synth.layer_weights(d, seed=7, n_hot=2 * d.top_k)
+    hot = synth.hot_experts(d, 7, 2 * d.top_k)
+    x = synth.token_rows(d, 70, 16)
+    idx, wts, logits = ora.route(d, x, w["router_w"], w["router_bias"])
+    assert np.isin(idx, hot).all()
+    d0 = d.with_(norm_topk=0, routed_scaling=2.5)
+    idx0, w0, _ = ora.route(d0, x, w["router_w"], w["router_bias"])
+    assert np.array_equal(idx, idx0)
+    s = (1.0 / (1.0 + np.exp(-np.take_along_axis(logits, idx, 1).astype(np.float64)))).astype(np.float32)
+    assert np.allclose(w0, s.astype(np.float64) * 2.5, rtol=1e-6)
+
+
+def test_router_logits_match_library_matmul():
+    d = TINY
+    w = synth.layer_weights(d, seed=1)
+    x = synth.token_rows(d, 11, 8)
+    _, _, logits = ora.route(d, x, w["router_w"], w["router_bias"])
+    ref = (bits_to_f64(x) @ bits_to_f64(w["router_w"]).T).astype(np.float32)
+    assert np.max(np.abs(logits.astype(np.float64) - ref) / np.maximum(np.abs(ref), 1e-30)) < 2e-7
+
+
+# ----------------------------------------------------------------------------- whole layer
+def np_dequant(packed, scale):
+    """Independent numpy dequant (integer table x 2^(S-128)) -> float64."""
+    lo = packed & 0xF
+    hi = packed >> 4
+    codes = np.stack([lo, hi], axis=-1).reshape(*packed.shape[:-1], packed.shape[-1] * 2)
+    mag = np.array(E2M1_INT, np.float64)[codes & 7] * np.where(codes >> 3, -1.0, 1.0)
+    sc = np.ldexp(1.0, scale.astype(np.int64) - 128)
+    return mag * np.repeat(sc, 32, axis=-1)
+
+
+def np_bf16(v):
+    return np.vectorize(bf16_rne_py, otypes=[np.float64])(v)
+
+
+def np_layer(d, w, x):
+    """Dense all-expert masked formulation of the layer in numpy fp64."""
+    xf = bits_to_f64(x)
+    logits = (xf @ bits_to_f64(w["router_w"]).T).astype(np.float32)
+    s, key = _keys_from_logits(logits, w["router_bias"])
+    T = x.shape[0]
+    gate = np.zeros((T, d.n_experts))
+    for t in range(T):
+        sel = np.argsort(-key[t], kind="stable")[: d.top_k]
+        wk = (s[t, sel].astype(np.float64) / s[t, sel].astype(np.float64).sum()).astype(np.float32)
+        gate[t, sel] = wk.astype(np.float64) * d.routed_scaling
+    lat = np_bf16(xf @ bits_to_f64(w["down_proj"]).T)
+    c = np.zeros((T, d.latent))
+    for e in range(d.n_experts):
+        W1 = np_dequant(w["w1_packed"][e], w["w1_scale"][e])
+        W3 = np_dequant(w["w3_packed"][e], w["w3_scale"][e])
+        W2 = np_dequant(w["w2_packed"][e], w["w2_scale"][e])
+        g, u = lat @ W1.T, lat @ W3.T
+        h = np_bf16(4 * np.tanh(g / 4) / (1 + np.exp(-g)) * 25 * np.tanh(u / 25))
+        c += gate[:, e:e + 1] * (h @ W2.T)
+    inv = 1.0 / np.sqrt((c * c).mean(axis=1, keepdims=True) + d.rms_eps)
+    n = np_bf16(c * inv * bits_to_f64(w["norm_w"]))
+    y = np_bf16(n @ bits_to_f64(w["up_proj"]).T)
+    return {"c": c, "lat": lat, "n": n, "y": y, "gate": gate}
+
+
+@pytest.fixture(scope="module")
+def tiny_case():
+    d = TINY
+    w = synth.layer_weights(d, seed=0)
+    x = synth.token_rows(d, 100, 12)
+    return d, w, x, ora.forward(d, w, x, probes=True)
+
+
+def test_layer_matches_dense_masked_numpy(tiny_case):
+    d, w, x, out = tiny_case
+    ref = np_layer(d, w, x)
+    assert np.array_equal(bits_to_f64(out["lat"]), ref["lat"])
+    rel = np.abs(out["c"] - ref["c"]).max() / np.sqrt((ref["c"] ** 2).mean())
+    assert rel < 1e-9
+    # n and y are bf16: identical except where fp64 reordering lands on a tie
+    assert np.mean(bits_to_f64(out["n"]) == ref["n"]) > 0.999
+    yo, yr = bits_to_f64(out["y"]), ref["y"]
+    assert np.mean(yo == yr) > 0.999
+    assert np.max(np.abs(yo - yr)) / np.sqrt((yr ** 2).mean()) < 1e-2
+    # selection and weights agree with the masked formulation
+    for t in range(x.shape[0]):
+        assert np.array_equal(np.sort(out["idx"][t]), np.flatnonzero(ref["gate"][t]))
+
+
+def test_layer_sparse_equals_c_dense_masked(tiny_case):
+    d, w, x, out = tiny_case
+    c_dense = ora.forward_dense_masked_c(d, w, x[:4])
+    assert np.allclose(out["c"][:4], c_dense, rtol=1e-12, atol=1e-12)
+
+
+def test_rmsnorm_removes_routing_weight_scale(tiny_case):
+    d, w, x, out = tiny_case
+    for dd in (d.with_(norm_topk=0), d.with_(routed_scaling=2.0)):
+        o2 = ora.forward(dd, w, x)
+        a, b = bits_to_f64(out["y"]), bits_to_f64(o2["y"])
+        assert np.array_equal(out["idx"], o2["idx"])
+        assert np.abs(a - b).mean() / np.abs(a).mean() < 2e-3
+
+
+def test_layer_tokens_independent(tiny_case):
+    d, w, x, out = tiny_case
+    part = ora.forward(d, w, x[5:7])
+    assert np.array_equal(part["y"], out["y"][5:7])
+
+
+def test_brute_force_tiny_layer_pure_python():
+    d = LayerDims(hidden=64, latent=64, n_experts=4, top_k=2, inter=64)
+    w = synth.layer_weights(d, seed=5)
+    x = synth.token_rows(d, 55, 2)
+    out = ora.forward(d, w, x, probes=True)
+    f = lambda b: float(bits_to_f64(np.uint16(b)))
+    for t in range(2):
+        xs = [f(v) for v in x[t]]
+        logits = []
+        for e in range(4):
+            acc = math.fsum(xs[j] * f(w["router_w"][e, j]) for j in range(64))
+            logits.append(float(np.float32(acc)))
+        s = [float(np.float32(1 / (1 + math.exp(-z)))) for z in logits]
+        key = [float(np.float32(np.float32(s[e]) + w["router_bias"][e])) for e in range(4)]
+        sel = sorted(range(4), key=lambda e: (-key[e], e))[:2]
+        assert list(out["idx"][t]) == sel
+        wk = [float(np.float32(s[e] / (s[sel[0]] + s[sel[1]]))) for e in sel]
+        lat = [bf16_rne_py(math.fsum(f(w["down_proj"][l, j]) * xs[j] for j in range(64))) for l in range(64)]
+        c = [0.0] * 64
+        for k, e in enumerate(sel):
+            def wv(P, Sc, r, j):
+                return exact_mxfp4(int(P[e, r, j // 2]), j % 2 == 1, int(Sc[e, r, j // 32]))
+            h = []
+            for j in range(64):
+                g = math.fsum(wv(w["w1_packed"], w["w1_scale"], j, l) * lat[l] for l in range(64))
+                u = math.fsum(wv(w["w3_packed"], w["w3_scale"], j, l) * lat[l] for l in range(64))
+                h.append(bf16_rne_py(4 * math.tanh(g / 4) / (1 + math.exp(-g)) * 25 * math.tanh(u / 25)))
+            assert [bits_to_f64(v) for v in out["h"][t, k]] == h
+            for l in range(64):
+                o = math.fsum(wv(w["w2_packed"], w["w2_scale"], l, j) * h[j] for j in range(64))
+                c[l] += wk[k] * o
+        assert np.allclose(out["c"][t], c, rtol=1e-12, atol=1e-14)
+        inv = 1 / math.sqrt(math.fsum(v * v for v in c) / 64 + 1e-6)
+        n = [bf16_rne_py(c[l] * inv * f(w["norm_w"][l])) for l in range(64)]
+        y = [bf16_rne_py(math.fsum(f(w["up_proj"][j, l]) * n[l] for l in range(64))) for j in range(64)]
+        assert np.mean(np.array(y) == bits_to_f64(out["y"][t])) > 0.98
+        assert np.allclose(bits_to_f64(out["y"][t]), y, rtol=1e-2, atol=1e-2)
+
+
+# ----------------------------------------------------------------------------- work counts
+def test_page_byte_figures(golden):
+    g = golden["expert_tensors"]
+    assert K3.expert_bytes() == g["bytes_per_expert"] == 17547264
+    assert K3.inter * K3.latent // 2 == g["w1_packed"]["bytes"]
+    assert K3.inter * (K3.latent // K3.group) == g["w1_scale"]["bytes"]
+    assert [K3.latent, K3.inter // 2] == g["w2_packed"]["shape"]
+    assert [K3.inter, K3.latent // 32] == g["w1_scale"]["shape"]
+    assert golden["tiers"]["mxfp4_expert_bpw"] == 4 + 8 / K3.group
+    assert round(K3.n_experts * K3.hidden * 2 / 1e6, 2) == golden["router"]["weight_mb"]
+
+
+def test_page_parameter_and_flop_figures(golden):
+    a = golden["architecture"]
+    layers = a["moe_layers"]
+    routed = layers * K3.n_experts * 3 * K3.inter * K3.latent
+    assert round(routed / 1e9, 1) == a["routed_expert_params_billion"]
+    assert round(layers * 2 * K3.hidden * K3.latent / 1e9, 1) == a["latent_up_down_params_billion"]
+    for row in golden["reap_compute"]["rows"]:
+        tokens = row["seqs"] * row["seqlen"]
+        pflop = K3.expert_flop_per_token() * tokens * layers / 1e15
+        assert round(pflop, 1) == row["pflop"]
+    # per-token routed expert traffic ~= 87 GB - 61 GB from the published builds
+    routed_gb = layers * K3.top_k * K3.expert_bytes() / 1e9
+    dt = golden["decode_traffic"]
+    assert abs(routed_gb - (dt["gb_read_per_token"] - dt["gb_non_expert_per_token"])) < 1.0
