@@ -1,0 +1,205 @@
+/*
+ * k3moe.h -- C ABI of the GB300 (sm_103a) Kimi-K3 Stable LatentMoE
+ * routed-expert layer.
+ *
+ * The layer, for each token x (7168-d, bf16) independently:
+ *   1. router    logit[e] = x . Wr[e] (fp32 accumulate); s = sigmoid(logit);
+ *                key = s + e_score_correction_bias[e] (selection only);
+ *                the top-K keys give topk_idx; topk_w = s / sum(s) * rsf.
+ *   2. down_proj lat = bf16(Wd . x), 7168 -> 3584.
+ *   3. experts   for each selected expert e: g = W1_e . lat, u = W3_e . lat,
+ *                h = bf16(beta tanh(g/beta) sigmoid(g) beta_lin tanh(u/beta_lin)),
+ *                o = W2_e . h; W1/W3/W2 are MXFP4 (e2m1 nibbles, low nibble
+ *                first, one e8m0 scale per 32 along the input dimension).
+ *   4. combine   c = sum_k topk_w[k] * o_k, in k order, fp32.
+ *   5. RMSNorm   n = bf16(c / sqrt(mean(c^2) + eps) * gamma).
+ *   6. up_proj   y = bf16(Wu . n), 3584 -> 7168.
+ * Passages defining these steps (page title, section):
+ *   kimi-k3-mlx README, "Architecture" table (896 routed experts, top-16,
+ *     sigmoid router + aux-loss-free e_score_correction_bias, Stable
+ *     LatentMoE down_proj -> experts -> RMSNorm -> up_proj in a 3584-d
+ *     latent, SiTU-GLU with beta = 4 and beta_lin = 25, MXFP4 source format
+ *     with group 32); "Porting notes" item 1 (SiTU-GLU in fp32); "Tiers"
+ *     (low-bits-first e2m1 codes, e8m0 scales); "REAP expert pruning"
+ *     closing caveat (RMSNorm on the combined expert output, before up_proj).
+ *   K3_ARTIFACT_AUDIT, section 4.3 (expert tensor shapes and the group of 32)
+ *     and section 6 (router weight [896,7168] bf16, fp32 correction bias).
+ * The renormalisation of the selected scores and the routed scaling factor
+ * are not fixed by the pages; they are configuration fields here.
+ *
+ * Conventions
+ *   - Every function returns K3MOE_OK (0) or a negative K3MOE_E* code; no
+ *     C++ exception crosses this boundary.  The message of the last failure
+ *     of a context is available from k3moe_last_error(); failures that
+ *     happen without a context (bad arguments to k3moe_create) are reported
+ *     by k3moe_last_error(NULL) on the calling thread.
+ *   - bf16 values are passed as uint16_t bit patterns (or void* to them).
+ *   - "device" pointers are CUDA device (or managed) memory on the context's
+ *     device; "host" pointers are ordinary CPU memory.  The library never
+ *     takes ownership of caller memory.
+ *   - Argument checks happen on the host before anything is launched.
+ */
+#ifndef K3MOE_H
+#define K3MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define K3MOE_OK 0
+#define K3MOE_EINVAL (-1)    /* bad argument or unsupported dimension */
+#define K3MOE_ENOMEM (-2)    /* device or host allocation failed */
+#define K3MOE_ECUDA (-3)     /* a CUDA runtime/driver call failed */
+#define K3MOE_ETIMEOUT (-4)  /* a bounded device-side wait gave up */
+#define K3MOE_EBADSCALE (-5) /* an e8m0 scale byte was 0xFF (NaN) */
+#define K3MOE_ESTATE (-6)    /* call out of order (e.g. forward before load_weights) */
+
+typedef struct k3moe_ctx k3moe_ctx; /* opaque; owned by the library */
+
+/* Layer configuration.  Dimensions must satisfy: hidden, latent and inter
+ * are multiples of 128; top_k <= 32 and top_k <= n_experts <= 2048;
+ * group == 32.  max_tokens bounds T in every forward call; the workspace
+ * is sized for it at create time and forward never allocates. */
+typedef struct {
+  int hidden;      /* H: 7168 for K3 */
+  int latent;      /* L: 3584 */
+  int n_experts;   /* E: 896 */
+  int top_k;       /* K: 16 */
+  int inter;       /* I: moe_intermediate_size, 3072 */
+  int group;       /* MXFP4 scale group along the input dimension: 32 */
+  float beta;      /* SiTU-GLU gate temperature: 4 */
+  float beta_lin;  /* SiTU-GLU linear-branch temperature: 25 */
+  float rms_eps;   /* RMSNorm epsilon: 1e-6 */
+  float routed_scaling; /* multiplies topk_w: 1.0 */
+  int norm_topk;   /* 1: topk_w = s / sum of the selected s; 0: topk_w = s */
+  int max_tokens;  /* largest T a forward call may pass */
+  int spin_timeout_ms; /* limit of any device-side wait; 0 selects 2000 ms */
+} k3moe_config;
+
+/* Host arrays in checkpoint layout, experts stacked along dim 0.  Row-major;
+ * packed MXFP4 rows hold element 2i in the low nibble of byte i. */
+typedef struct {
+  const uint16_t* router_w;    /* [E, H] bf16   (gate.weight)                 */
+  const float* router_bias;    /* [E]    f32    (e_score_correction_bias)     */
+  const uint16_t* down_proj;   /* [L, H] bf16                                 */
+  const uint8_t* w1_packed;    /* [E, I, L/2]   gate weight_packed            */
+  const uint8_t* w1_scale;     /* [E, I, L/32]  gate weight_scale (e8m0)      */
+  const uint8_t* w3_packed;    /* [E, I, L/2]   up                            */
+  const uint8_t* w3_scale;     /* [E, I, L/32]                                */
+  const uint8_t* w2_packed;    /* [E, L, I/2]   down                          */
+  const uint8_t* w2_scale;     /* [E, L, I/32]                                */
+  const uint16_t* norm_w;      /* [L]    bf16   RMSNorm weight (gamma)        */
+  const uint16_t* up_proj;     /* [H, L] bf16                                 */
+} k3moe_weights;
+
+/* Creates a context on `cuda_device` and allocates its device workspace for
+ * cfg->max_tokens tokens.  On success *out owns the context; release it
+ * with k3moe_destroy.  Errors: EINVAL (bad config or device), ECUDA,
+ * ENOMEM. */
+int k3moe_create(const k3moe_config* cfg, int cuda_device, k3moe_ctx** out);
+
+/* Copies the weights (host memory, checkpoint layout) to the device.  The
+ * MXFP4 tensors are re-laid into 128-row x 64-column tiles (packed nibbles
+ * followed by their scales) for the expert kernels; values are unchanged.
+ * Any scale byte equal to 0xFF is rejected with EBADSCALE before anything
+ * is copied.  May be called again to replace the weights.  Synchronous. */
+int k3moe_load_weights(k3moe_ctx* ctx, const k3moe_weights* w);
+
+/* One layer forward for T tokens, enqueued on `cuda_stream` (a
+ * cudaStream_t; NULL = the legacy default stream).  Asynchronous: returns
+ * after launching.  Device pointers:
+ *   x        [T, H] bf16 input
+ *   y        [T, H] bf16 output
+ *   topk_idx [T, K] int32 output: selected experts, descending key; ties
+ *            go to the lower expert id
+ *   topk_w   [T, K] fp32 output: routing weights in the same order
+ * T == 0 is a no-op.  T > max_tokens or T < 0 returns EINVAL.  Performs no
+ * allocation and no host synchronisation; a device-side timeout is
+ * reported by the next k3moe_status. */
+int k3moe_forward(k3moe_ctx* ctx, const void* x, int T, void* y, int32_t* topk_idx,
+                  float* topk_w, void* cuda_stream);
+
+/* The same forward with HOST buffers (x_host [T,H] bf16, y_host [T,H] bf16,
+ * idx_host [T,K], w_host [T,K]; any of the three outputs may be NULL):
+ * copies x to the device, runs the layer, copies the results back and
+ * synchronises the stream.  Pinned host memory gives the fastest copies. */
+int k3moe_forward_host(k3moe_ctx* ctx, const void* x_host, int T, void* y_host,
+                       int32_t* idx_host, float* w_host, void* cuda_stream);
+
+/* Synchronises the context's device, then reports and clears the device
+ * status word: K3MOE_OK, or K3MOE_ETIMEOUT if a bounded wait gave up, or
+ * ECUDA if a pending CUDA error was found. */
+int k3moe_status(k3moe_ctx* ctx);
+
+/* Message of the last failure on `ctx` (or, for NULL, of the last
+ * k3moe_create failure on this thread).  Never NULL; owned by the library,
+ * valid until the next call on the same context. */
+const char* k3moe_last_error(const k3moe_ctx* ctx);
+
+/* Frees the device memory of the context and the context itself.  NULL is
+ * a no-op. */
+void k3moe_destroy(k3moe_ctx* ctx);
+
+/* ---- step entry points (the hot path's steps, callable on their own) ---- */
+
+/* MXFP4 -> bf16 dequantisation of a [rows, cols] matrix in checkpoint
+ * layout (device pointers: packed [rows, cols/2] u8, scale [rows, cols/32]
+ * u8, out [rows, cols] bf16), using the same device decoding routines as
+ * the expert kernels.  kind 0: the bf16 tile producer of the tensor-core
+ * kernels (value = e2m1 * 2^(S-127), exact for scale bytes 0..252, IEEE
+ * overflow above); kind 1: the per-group decoding of the decode kernels,
+ * written as fp32 (out is then [rows, cols] float).  Requires cols % 64 == 0.
+ * Asynchronous on `cuda_stream`.  The decoding definition is the "Tiers"
+ * section of the kimi-k3-mlx README (same encoding, low bits first, e8m0
+ * scales) and K3_ARTIFACT_AUDIT section 4.3 (group 32). */
+int k3moe_mxfp4_dequant(const uint8_t* packed, const uint8_t* scale, int rows, int cols,
+                        void* out, int kind, void* cuda_stream);
+
+/* Router step on its own: logits = x . Wr^T into the caller's scratch
+ * `logits` [T, E] fp32 (device), then top-K selection and weights exactly
+ * as in k3moe_forward (same kernels).  Device pointers: x [T,H] bf16,
+ * router_w [E,H] bf16, bias [E] f32, topk_idx [T,K], topk_w [T,K].
+ * Requires H % 128 == 0, 1 <= K <= 32, K <= E <= 2048.  Asynchronous. */
+int k3moe_route(const void* x, int T, const void* router_w, const float* bias, int E, int H, int K,
+                int norm_topk, float routed_scaling, float* logits, int32_t* topk_idx, float* topk_w,
+                void* cuda_stream);
+
+/* ---- inspection (tests and tools) ---- */
+
+enum {
+  K3MOE_BUF_LOGITS = 0, /* [T, E] f32   router logits of the last forward       */
+  K3MOE_BUF_LAT = 1,    /* [T, L] bf16  latent after down_proj                   */
+  K3MOE_BUF_COUNTS = 2, /* [E]    i32   assignments per expert                   */
+  K3MOE_BUF_OFFSETS = 3,/* [E+1]  i32   exclusive prefix sum of COUNTS           */
+  K3MOE_BUF_PERM = 4,   /* [T*K]  i32   slot -> t*K + k, grouped by expert, stable */
+  K3MOE_BUF_SLOT = 5,   /* [T*K]  i32   t*K + k -> slot                          */
+  K3MOE_BUF_H = 6,      /* [T*K, I] bf16 SiTU-GLU output per slot                */
+  K3MOE_BUF_O = 7,      /* [T*K, L] f32 expert output per slot                   */
+  K3MOE_BUF_N = 8,      /* [T, L] bf16  RMSNorm output                           */
+  K3MOE_BUF_ACTIVE = 9  /* [E+1]  i32   number of experts with work, then their ids */
+};
+
+/* Copies `bytes` bytes of an internal buffer (K3MOE_BUF_*) of the last
+ * forward into host memory `dst` (synchronises the device).  EINVAL if
+ * `bytes` exceeds the buffer. */
+int k3moe_fetch(k3moe_ctx* ctx, int which, void* dst, size_t bytes);
+
+enum {
+  K3MOE_Q_WORKSPACE_BYTES = 0, /* device workspace bytes                       */
+  K3MOE_Q_WEIGHT_BYTES = 1,    /* device weight bytes                          */
+  K3MOE_Q_LAUNCHES_LAST = 2,   /* kernels launched by the last forward          */
+  K3MOE_Q_PATH_LAST = 3,       /* 0: decode kernels, 1: tensor-core kernels     */
+  K3MOE_Q_DEVICE = 4           /* CUDA device ordinal                          */
+};
+
+/* Reads a counter or size of the context into *value. */
+int k3moe_query(const k3moe_ctx* ctx, int what, long long* value);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* K3MOE_H */

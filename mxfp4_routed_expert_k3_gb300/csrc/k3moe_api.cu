@@ -1,0 +1,446 @@
+// k3moe_api.cu -- host implementation of the C ABI declared in
+// include/k3moe.h: context lifetime, weight loading (with the MXFP4 tile
+// re-layout), argument checks and the per-forward launch sequence.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "../../include/k3moe.h"
+#include "k3moe_device.cuh"
+#include "k3moe_internal.h"
+#include "k3moe_umma.h"
+
+namespace {
+
+thread_local std::string g_create_error = "no error";
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+struct k3moe_ctx {
+  k3moe_config cfg{};
+  int device = 0;
+  k3::Dims d{};
+  // device weights
+  uint16_t* wcat = nullptr;     // [E + L, H]: router rows, then down_proj rows
+  float* bias = nullptr;        // [E]
+  uint16_t* gamma = nullptr;    // [L]
+  uint16_t* wu = nullptr;       // [H, L]
+  uint8_t* gu_tiles = nullptr;  // [E][I/128][L/64][2][tile]
+  uint8_t* d_tiles = nullptr;   // [E][L/128][I/64][tile]
+  size_t weight_bytes = 0;
+  bool loaded = false;
+  // workspace
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  k3::Work w{};
+  size_t sz_logits = 0, sz_lat = 0, sz_counts = 0, sz_offsets = 0, sz_active = 0, sz_perm = 0, sz_h = 0, sz_o = 0,
+         sz_n = 0;
+  uint16_t* x_stage = nullptr;
+  uint16_t* y_stage = nullptr;
+  int32_t* idx_stage = nullptr;
+  float* w_stage = nullptr;
+  k3::UmmaPlan umma{};
+  long long launches_last = 0;
+  int path_last = 0;
+  std::string err = "no error";
+};
+
+namespace {
+
+int fail(k3moe_ctx* c, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  if (c)
+    c->err = buf;
+  else
+    g_create_error = buf;
+  return code;
+}
+
+int cuda_fail(k3moe_ctx* c, cudaError_t e, const char* what) {
+  return fail(c, e == cudaErrorMemoryAllocation ? K3MOE_ENOMEM : K3MOE_ECUDA, "%s: %s (%s)", what,
+              cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define K3_CUDA(c, call, what)                 \
+  do {                                         \
+    cudaError_t e_ = (call);                   \
+    if (e_ != cudaSuccess) return cuda_fail(c, e_, what); \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_config(const k3moe_config* c) {
+  if (!c) return fail(nullptr, K3MOE_EINVAL, "config is NULL");
+  if (c->hidden <= 0 || c->latent <= 0 || c->inter <= 0 || c->n_experts <= 0 || c->top_k <= 0)
+    return fail(nullptr, K3MOE_EINVAL, "dimensions must be positive");
+  if (c->hidden % 128 || c->latent % 128 || c->inter % 128)
+    return fail(nullptr, K3MOE_EINVAL, "hidden, latent and inter must be multiples of 128 (got %d, %d, %d)",
+                c->hidden, c->latent, c->inter);
+  if (c->group != 32) return fail(nullptr, K3MOE_EINVAL, "only MXFP4 group 32 is supported (got %d)", c->group);
+  if (c->top_k > 32 || c->top_k > c->n_experts || c->n_experts > 2048)
+    return fail(nullptr, K3MOE_EINVAL, "need top_k <= 32, top_k <= n_experts <= 2048");
+  if (c->max_tokens < 1 || c->max_tokens > (1 << 20))
+    return fail(nullptr, K3MOE_EINVAL, "max_tokens must be in [1, 2^20] (got %d)", c->max_tokens);
+  if (!(c->rms_eps >= 0.f) || !(c->beta > 0.f) || !(c->beta_lin > 0.f))
+    return fail(nullptr, K3MOE_EINVAL, "beta, beta_lin must be > 0 and rms_eps >= 0");
+  if (c->spin_timeout_ms < 0) return fail(nullptr, K3MOE_EINVAL, "spin_timeout_ms must be >= 0");
+  return K3MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int k3moe_create(const k3moe_config* cfg, int cuda_device, k3moe_ctx** out) {
+  if (!out) return fail(nullptr, K3MOE_EINVAL, "out is NULL");
+  *out = nullptr;
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  int ndev = 0;
+  cudaError_t e = cudaGetDeviceCount(&ndev);
+  if (e != cudaSuccess || ndev == 0)
+    return fail(nullptr, K3MOE_ECUDA, "no CUDA device available (%s)", cudaGetErrorString(e));
+  if (cuda_device < 0 || cuda_device >= ndev)
+    return fail(nullptr, K3MOE_EINVAL, "device %d out of range [0, %d)", cuda_device, ndev);
+  cudaDeviceProp prop;
+  if ((e = cudaGetDeviceProperties(&prop, cuda_device)) != cudaSuccess)
+    return fail(nullptr, K3MOE_ECUDA, "cudaGetDeviceProperties: %s", cudaGetErrorString(e));
+  if (prop.major != 10 || prop.minor != 3)
+    return fail(nullptr, K3MOE_EINVAL, "this library is built for sm_103a (GB300); device %d is sm_%d%d",
+                cuda_device, prop.major, prop.minor);
+  if ((e = cudaSetDevice(cuda_device)) != cudaSuccess)
+    return fail(nullptr, K3MOE_ECUDA, "cudaSetDevice: %s", cudaGetErrorString(e));
+
+  k3moe_ctx* c = new k3moe_ctx();
+  c->cfg = *cfg;
+  if (c->cfg.spin_timeout_ms == 0) c->cfg.spin_timeout_ms = 2000;
+  c->device = cuda_device;
+  c->d = k3::Dims{cfg->hidden, cfg->latent, cfg->n_experts, cfg->top_k, cfg->inter, cfg->beta, cfg->beta_lin,
+                  cfg->rms_eps, cfg->routed_scaling, cfg->norm_topk};
+  const size_t Tm = (size_t)cfg->max_tokens, H = cfg->hidden, L = cfg->latent, E = cfg->n_experts,
+               K = cfg->top_k, I = cfg->inter;
+  const size_t nblk = (Tm * K + k3::kPermChunk - 1) / k3::kPermChunk;
+  c->sz_logits = Tm * E * 4;
+  c->sz_lat = Tm * L * 2;
+  c->sz_counts = E * 4;
+  c->sz_offsets = (E + 1) * 4;
+  c->sz_active = (E + 1) * 4;
+  c->sz_perm = Tm * K * 4;
+  c->sz_h = Tm * K * I * 2;
+  c->sz_o = Tm * K * L * 4;
+  c->sz_n = Tm * L * 2;
+  c->umma = k3::umma_plan(c->d, (int)Tm);
+  const size_t parts[] = {c->sz_logits, c->sz_lat,   c->sz_counts, c->sz_offsets, c->sz_active, c->sz_perm,
+                          c->sz_perm,   nblk * E * 4, c->sz_h,     c->sz_o,       c->sz_n,      256,
+                          Tm * H * 2,   Tm * H * 2,   Tm * K * 4,  Tm * K * 4,    c->umma.ws_bytes};
+  size_t total = 0;
+  for (size_t p : parts) total += align_up(p, 256);
+  e = cudaMalloc(&c->ws, total);
+  if (e != cudaSuccess) {
+    fail(nullptr, K3MOE_ENOMEM, "workspace of %zu bytes for max_tokens=%d: %s", total, cfg->max_tokens,
+         cudaGetErrorString(e));
+    delete c;
+    return K3MOE_ENOMEM;
+  }
+  c->ws_bytes = total;
+  char* p = static_cast<char*>(c->ws);
+  auto take = [&](size_t n) {
+    char* r = p;
+    p += align_up(n, 256);
+    return r;
+  };
+  c->w.logits = (float*)take(parts[0]);
+  c->w.lat = (uint16_t*)take(parts[1]);
+  c->w.counts = (int*)take(parts[2]);
+  c->w.offsets = (int*)take(parts[3]);
+  c->w.active = (int*)take(parts[4]);
+  c->w.perm = (int*)take(parts[5]);
+  c->w.slot = (int*)take(parts[6]);
+  c->w.blk_hist = (int*)take(parts[7]);
+  c->w.h = (uint16_t*)take(parts[8]);
+  c->w.o = (float*)take(parts[9]);
+  c->w.n = (uint16_t*)take(parts[10]);
+  c->w.status = (unsigned*)take(parts[11]);
+  c->x_stage = (uint16_t*)take(parts[12]);
+  c->y_stage = (uint16_t*)take(parts[13]);
+  c->idx_stage = (int32_t*)take(parts[14]);
+  c->w_stage = (float*)take(parts[15]);
+  c->umma.ws = take(parts[16]);
+  e = cudaMemset(c->ws, 0, total);
+  if (e != cudaSuccess) {
+    fail(nullptr, K3MOE_ECUDA, "cudaMemset: %s", cudaGetErrorString(e));
+    cudaFree(c->ws);
+    delete c;
+    return K3MOE_ECUDA;
+  }
+  *out = c;
+  return K3MOE_OK;
+}
+
+void k3moe_destroy(k3moe_ctx* c) {
+  if (!c) return;
+  cudaSetDevice(c->device);
+  cudaDeviceSynchronize();
+  cudaFree(c->ws);
+  cudaFree(c->wcat);
+  cudaFree(c->bias);
+  cudaFree(c->gamma);
+  cudaFree(c->wu);
+  cudaFree(c->gu_tiles);
+  cudaFree(c->d_tiles);
+  delete c;
+}
+
+const char* k3moe_last_error(const k3moe_ctx* c) { return c ? c->err.c_str() : g_create_error.c_str(); }
+
+int k3moe_load_weights(k3moe_ctx* c, const k3moe_weights* wt) {
+  if (!c) return fail(nullptr, K3MOE_EINVAL, "ctx is NULL");
+  if (!wt) return fail(c, K3MOE_EINVAL, "weights is NULL");
+  const void* ptrs[] = {wt->router_w,  wt->router_bias, wt->down_proj, wt->w1_packed, wt->w1_scale, wt->w3_packed,
+                        wt->w3_scale,  wt->w2_packed,   wt->w2_scale,  wt->norm_w,    wt->up_proj};
+  for (const void* q : ptrs)
+    if (!q) return fail(c, K3MOE_EINVAL, "a weight pointer is NULL");
+  const size_t H = c->d.H, L = c->d.L, E = c->d.E, I = c->d.I;
+  const size_t n_gu_scale = E * I * (L / 32), n_d_scale = E * L * (I / 32);
+  const uint8_t* scales[] = {wt->w1_scale, wt->w3_scale, wt->w2_scale};
+  const size_t nscales[] = {n_gu_scale, n_gu_scale, n_d_scale};
+  const char* names[] = {"w1_scale", "w3_scale", "w2_scale"};
+  for (int i = 0; i < 3; ++i) {
+    const void* hit = memchr(scales[i], 0xFF, nscales[i]);
+    if (hit)
+      return fail(c, K3MOE_EBADSCALE, "%s holds the e8m0 NaN byte 0xFF at offset %zu", names[i],
+                  (size_t)((const uint8_t*)hit - scales[i]));
+  }
+  K3_CUDA(c, cudaSetDevice(c->device), "cudaSetDevice");
+  const size_t gu_bytes = E * (I / 128) * (L / 64) * 2 * (size_t)k3::kTileBytes;
+  const size_t d_bytes = E * (L / 128) * (I / 64) * (size_t)k3::kTileBytes;
+  if (!c->wcat) {
+    K3_CUDA(c, cudaMalloc(&c->wcat, (E + L) * H * 2), "cudaMalloc(router+down_proj)");
+    K3_CUDA(c, cudaMalloc(&c->bias, E * 4), "cudaMalloc(bias)");
+    K3_CUDA(c, cudaMalloc(&c->gamma, L * 2), "cudaMalloc(gamma)");
+    K3_CUDA(c, cudaMalloc(&c->wu, H * L * 2), "cudaMalloc(up_proj)");
+    K3_CUDA(c, cudaMalloc(&c->gu_tiles, gu_bytes), "cudaMalloc(gate/up tiles)");
+    K3_CUDA(c, cudaMalloc(&c->d_tiles, d_bytes), "cudaMalloc(down tiles)");
+    c->weight_bytes = (E + L) * H * 2 + E * 4 + L * 2 + H * L * 2 + gu_bytes + d_bytes;
+  }
+  c->loaded = false;
+  K3_CUDA(c, cudaMemcpy(c->wcat, wt->router_w, E * H * 2, cudaMemcpyHostToDevice), "copy router_w");
+  K3_CUDA(c, cudaMemcpy(c->wcat + E * H, wt->down_proj, L * H * 2, cudaMemcpyHostToDevice), "copy down_proj");
+  K3_CUDA(c, cudaMemcpy(c->bias, wt->router_bias, E * 4, cudaMemcpyHostToDevice), "copy bias");
+  K3_CUDA(c, cudaMemcpy(c->gamma, wt->norm_w, L * 2, cudaMemcpyHostToDevice), "copy norm_w");
+  K3_CUDA(c, cudaMemcpy(c->wu, wt->up_proj, H * L * 2, cudaMemcpyHostToDevice), "copy up_proj");
+
+  // Experts: stage a chunk of experts of one tensor, re-lay into tiles.
+  const size_t per_expert_packed = I * L / 2, per_expert_scale = I * L / 32;  // same for w1/w3/w2
+  size_t chunk = std::max<size_t>(1, (size_t)(256u << 20) / per_expert_packed);
+  chunk = std::min(chunk, E);
+  uint8_t *st_p = nullptr, *st_s = nullptr;
+  K3_CUDA(c, cudaMalloc(&st_p, chunk * per_expert_packed), "cudaMalloc(staging)");
+  cudaError_t e = cudaMalloc(&st_s, chunk * per_expert_scale);
+  if (e != cudaSuccess) {
+    cudaFree(st_p);
+    return cuda_fail(c, e, "cudaMalloc(staging)");
+  }
+  struct Job {
+    const uint8_t *p, *s;
+    int rows, cols;
+    uint8_t* tiles;
+    size_t mat_stride;
+    int step, offset;
+  } jobs[3] = {
+      {wt->w1_packed, wt->w1_scale, (int)I, (int)L, c->gu_tiles, (I / 128) * (L / 64) * 2, 2, 0},
+      {wt->w3_packed, wt->w3_scale, (int)I, (int)L, c->gu_tiles, (I / 128) * (L / 64) * 2, 2, 1},
+      {wt->w2_packed, wt->w2_scale, (int)L, (int)I, c->d_tiles, (L / 128) * (I / 64), 1, 0},
+  };
+  int rc = K3MOE_OK;
+  for (const Job& j : jobs) {
+    for (size_t e0 = 0; e0 < E && rc == K3MOE_OK; e0 += chunk) {
+      const size_t ne = std::min(chunk, E - e0);
+      if ((e = cudaMemcpy(st_p, j.p + e0 * per_expert_packed, ne * per_expert_packed, cudaMemcpyHostToDevice)) ||
+          (e = cudaMemcpy(st_s, j.s + e0 * per_expert_scale, ne * per_expert_scale, cudaMemcpyHostToDevice)) ||
+          (e = k3::launch_relayout(st_p, st_s, (int)ne, j.rows, j.cols,
+                                   j.tiles + e0 * j.mat_stride * (size_t)k3::kTileBytes, j.mat_stride, j.step,
+                                   j.offset, 0)) ||
+          (e = cudaDeviceSynchronize()))
+        rc = cuda_fail(c, e, "expert re-layout");
+    }
+  }
+  cudaFree(st_p);
+  cudaFree(st_s);
+  if (rc) return rc;
+  c->loaded = true;
+  return K3MOE_OK;
+}
+
+static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* idx, float* wts,
+                        cudaStream_t s) {
+  const k3::Dims& d = c->d;
+  k3::Work& w = c->w;
+  const bool big = k3::umma_path_enabled(c->umma, d, T);
+  c->path_last = big ? 1 : 0;
+  long long n = 0;
+  cudaError_t e;
+#define K3_LAUNCH(expr, count, what)        \
+  do {                                      \
+    if ((e = (expr)) != cudaSuccess) return cuda_fail(c, e, what); \
+    n += (count);                           \
+  } while (0)
+  if (big) {
+    K3_LAUNCH(k3::umma_dense(c->umma, c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, d.E, w.logits, w.lat, s),
+              k3::umma_dense_launches(), "router + down_proj (tensor cores)");
+  } else {
+    K3_LAUNCH(k3::launch_dense_gemv(c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, d.E, w.logits, w.lat, s), 1,
+              "router + down_proj");
+  }
+  K3_LAUNCH(k3::launch_topk(w.logits, T, d.E, d.E, c->bias, d.K, d.norm_topk, d.rsf, idx, wts, s), 1, "top-k");
+  K3_LAUNCH(k3::launch_permute(idx, T, d.K, d.E, w.blk_hist, w.counts, w.offsets, w.active, w.perm, w.slot, s), 3,
+            "permute");
+  const int max_active = std::min(d.E, T * d.K);
+  if (big) {
+    K3_LAUNCH(k3::umma_experts(c->umma, c->gu_tiles, c->d_tiles, w, T, d, s), k3::umma_expert_launches(),
+              "experts (tensor cores)");
+  } else {
+    K3_LAUNCH(k3::launch_gateup_gemv(c->gu_tiles, w.lat, w.active, w.offsets, w.perm, max_active, d, w.h, s), 1,
+              "gate/up");
+    K3_LAUNCH(k3::launch_down_gemv(c->d_tiles, w.h, w.active, w.offsets, max_active, d, w.o, s), 1, "down");
+  }
+  K3_LAUNCH(k3::launch_combine_rmsnorm(w.o, w.slot, wts, c->gamma, T, d, w.n, s), 1, "combine + RMSNorm");
+  if (big) {
+    K3_LAUNCH(k3::umma_dense(c->umma, c->wu, d.H, d.L, w.n, T, 0, nullptr, (uint16_t*)y, s),
+              k3::umma_dense_launches(), "up_proj (tensor cores)");
+  } else {
+    K3_LAUNCH(k3::launch_dense_gemv(c->wu, d.H, d.L, w.n, T, 0, nullptr, (uint16_t*)y, s), 1, "up_proj");
+  }
+#undef K3_LAUNCH
+  c->launches_last = n;
+  return K3MOE_OK;
+}
+
+int k3moe_forward(k3moe_ctx* c, const void* x, int T, void* y, int32_t* topk_idx, float* topk_w,
+                  void* cuda_stream) {
+  if (!c) return fail(nullptr, K3MOE_EINVAL, "ctx is NULL");
+  if (!c->loaded) return fail(c, K3MOE_ESTATE, "forward before load_weights");
+  if (T < 0 || T > c->cfg.max_tokens)
+    return fail(c, K3MOE_EINVAL, "T=%d outside [0, max_tokens=%d]", T, c->cfg.max_tokens);
+  if (T == 0) {
+    c->launches_last = 0;
+    return K3MOE_OK;
+  }
+  if (!x || !y || !topk_idx || !topk_w) return fail(c, K3MOE_EINVAL, "a device pointer is NULL");
+  if (!aligned16(x) || !aligned16(y) || !aligned16(topk_idx) || !aligned16(topk_w))
+    return fail(c, K3MOE_EINVAL, "x, y, topk_idx and topk_w must be 16-byte aligned");
+  K3_CUDA(c, cudaSetDevice(c->device), "cudaSetDevice");
+  return forward_impl(c, x, T, y, topk_idx, topk_w, (cudaStream_t)cuda_stream);
+}
+
+int k3moe_forward_host(k3moe_ctx* c, const void* x_host, int T, void* y_host, int32_t* idx_host, float* w_host,
+                       void* cuda_stream) {
+  if (!c) return fail(nullptr, K3MOE_EINVAL, "ctx is NULL");
+  if (!c->loaded) return fail(c, K3MOE_ESTATE, "forward before load_weights");
+  if (T < 0 || T > c->cfg.max_tokens)
+    return fail(c, K3MOE_EINVAL, "T=%d outside [0, max_tokens=%d]", T, c->cfg.max_tokens);
+  if (T == 0) return K3MOE_OK;
+  if (!x_host) return fail(c, K3MOE_EINVAL, "x_host is NULL");
+  K3_CUDA(c, cudaSetDevice(c->device), "cudaSetDevice");
+  cudaStream_t s = (cudaStream_t)cuda_stream;
+  const size_t H = c->d.H, K = c->d.K;
+  K3_CUDA(c, cudaMemcpyAsync(c->x_stage, x_host, (size_t)T * H * 2, cudaMemcpyHostToDevice, s), "copy x");
+  int rc = forward_impl(c, c->x_stage, T, c->y_stage, c->idx_stage, c->w_stage, s);
+  if (rc) return rc;
+  if (y_host)
+    K3_CUDA(c, cudaMemcpyAsync(y_host, c->y_stage, (size_t)T * H * 2, cudaMemcpyDeviceToHost, s), "copy y");
+  if (idx_host)
+    K3_CUDA(c, cudaMemcpyAsync(idx_host, c->idx_stage, (size_t)T * K * 4, cudaMemcpyDeviceToHost, s), "copy idx");
+  if (w_host)
+    K3_CUDA(c, cudaMemcpyAsync(w_host, c->w_stage, (size_t)T * K * 4, cudaMemcpyDeviceToHost, s), "copy w");
+  K3_CUDA(c, cudaStreamSynchronize(s), "cudaStreamSynchronize");
+  return K3MOE_OK;
+}
+
+int k3moe_status(k3moe_ctx* c) {
+  if (!c) return fail(nullptr, K3MOE_EINVAL, "ctx is NULL");
+  K3_CUDA(c, cudaSetDevice(c->device), "cudaSetDevice");
+  K3_CUDA(c, cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+  unsigned st = 0;
+  K3_CUDA(c, cudaMemcpy(&st, c->w.status, 4, cudaMemcpyDeviceToHost), "read status");
+  if (st) {
+    unsigned zero = 0;
+    K3_CUDA(c, cudaMemcpy(c->w.status, &zero, 4, cudaMemcpyHostToDevice), "clear status");
+    return fail(c, K3MOE_ETIMEOUT, "a device-side wait gave up (status word 0x%08x)", st);
+  }
+  return K3MOE_OK;
+}
+
+int k3moe_fetch(k3moe_ctx* c, int which, void* dst, size_t bytes) {
+  if (!c) return fail(nullptr, K3MOE_EINVAL, "ctx is NULL");
+  if (!dst && bytes) return fail(c, K3MOE_EINVAL, "dst is NULL");
+  const void* src = nullptr;
+  size_t cap = 0;
+  switch (which) {
+    case K3MOE_BUF_LOGITS: src = c->w.logits; cap = c->sz_logits; break;
+    case K3MOE_BUF_LAT: src = c->w.lat; cap = c->sz_lat; break;
+    case K3MOE_BUF_COUNTS: src = c->w.counts; cap = c->sz_counts; break;
+    case K3MOE_BUF_OFFSETS: src = c->w.offsets; cap = c->sz_offsets; break;
+    case K3MOE_BUF_PERM: src = c->w.perm; cap = c->sz_perm; break;
+    case K3MOE_BUF_SLOT: src = c->w.slot; cap = c->sz_perm; break;
+    case K3MOE_BUF_H: src = c->w.h; cap = c->sz_h; break;
+    case K3MOE_BUF_O: src = c->w.o; cap = c->sz_o; break;
+    case K3MOE_BUF_N: src = c->w.n; cap = c->sz_n; break;
+    case K3MOE_BUF_ACTIVE: src = c->w.active; cap = c->sz_active; break;
+    default: return fail(c, K3MOE_EINVAL, "unknown buffer %d", which);
+  }
+  if (bytes > cap) return fail(c, K3MOE_EINVAL, "buffer %d holds %zu bytes, %zu requested", which, cap, bytes);
+  K3_CUDA(c, cudaSetDevice(c->device), "cudaSetDevice");
+  K3_CUDA(c, cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+  K3_CUDA(c, cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost), "fetch");
+  return K3MOE_OK;
+}
+
+int k3moe_query(const k3moe_ctx* c, int what, long long* value) {
+  if (!c || !value) return fail(nullptr, K3MOE_EINVAL, "ctx or value is NULL");
+  switch (what) {
+    case K3MOE_Q_WORKSPACE_BYTES: *value = (long long)c->ws_bytes; return K3MOE_OK;
+    case K3MOE_Q_WEIGHT_BYTES: *value = (long long)c->weight_bytes; return K3MOE_OK;
+    case K3MOE_Q_LAUNCHES_LAST: *value = c->launches_last; return K3MOE_OK;
+    case K3MOE_Q_PATH_LAST: *value = c->path_last; return K3MOE_OK;
+    case K3MOE_Q_DEVICE: *value = c->device; return K3MOE_OK;
+    default: return fail(nullptr, K3MOE_EINVAL, "unknown query %d", what);
+  }
+}
+
+int k3moe_mxfp4_dequant(const uint8_t* packed, const uint8_t* scale, int rows, int cols, void* out, int kind,
+                        void* cuda_stream) {
+  if (!packed || !scale || !out) return fail(nullptr, K3MOE_EINVAL, "a pointer is NULL");
+  if (rows < 0 || cols < 0 || cols % 64) return fail(nullptr, K3MOE_EINVAL, "need rows >= 0 and cols %% 64 == 0");
+  if (kind != 0 && kind != 1) return fail(nullptr, K3MOE_EINVAL, "kind must be 0 (bf16) or 1 (fp32)");
+  if (!aligned16(out)) return fail(nullptr, K3MOE_EINVAL, "out must be 16-byte aligned");
+  cudaError_t e = k3::launch_dequant(packed, scale, rows, cols, out, kind, (cudaStream_t)cuda_stream);
+  if (e != cudaSuccess) return fail(nullptr, K3MOE_ECUDA, "dequant launch: %s", cudaGetErrorString(e));
+  return K3MOE_OK;
+}
+
+int k3moe_route(const void* x, int T, const void* router_w, const float* bias, int E, int H, int K, int norm_topk,
+                float routed_scaling, float* logits, int32_t* topk_idx, float* topk_w, void* cuda_stream) {
+  if (T < 0) return fail(nullptr, K3MOE_EINVAL, "T < 0");
+  if (T == 0) return K3MOE_OK;
+  if (!x || !router_w || !bias || !logits || !topk_idx || !topk_w)
+    return fail(nullptr, K3MOE_EINVAL, "a pointer is NULL");
+  if (H <= 0 || H % 128 || K < 1 || K > 32 || K > E || E > 2048)
+    return fail(nullptr, K3MOE_EINVAL, "need H %% 128 == 0, 1 <= K <= 32, K <= E <= 2048");
+  if (!aligned16(x) || !aligned16(router_w)) return fail(nullptr, K3MOE_EINVAL, "x and router_w must be 16-byte aligned");
+  cudaStream_t s = (cudaStream_t)cuda_stream;
+  cudaError_t e = k3::launch_dense_gemv((const uint16_t*)router_w, E, H, (const uint16_t*)x, T, E, logits, nullptr, s);
+  if (e == cudaSuccess) e = k3::launch_topk(logits, T, E, E, bias, K, norm_topk, routed_scaling, topk_idx, topk_w, s);
+  if (e != cudaSuccess) return fail(nullptr, K3MOE_ECUDA, "route launch: %s", cudaGetErrorString(e));
+  return K3MOE_OK;
+}
+
+}  // extern "C"

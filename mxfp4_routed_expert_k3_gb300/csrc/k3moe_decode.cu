@@ -1,0 +1,697 @@
+// k3moe_decode.cu -- the layer's CUDA-core kernels: dense GEMV for small
+// token counts, router top-K, the token->expert permutation, the grouped
+// MXFP4 expert GEMVs (gate/up with the SiTU-GLU epilogue, and down), the
+// weighted combine + RMSNorm, and the MXFP4 re-layout / dequant kernels.
+//
+// At decode sizes every one of these is bound by HBM bandwidth (the expert
+// kernels stream MXFP4 tiles once; per weight they issue about two
+// instructions), so they are written as streaming kernels: coalesced
+// 16-byte loads, work items sized so the grid covers the 152 SMs several
+// times, activations staged once per CTA in shared memory.
+#include <cfloat>
+#include <climits>
+
+#include "k3moe_device.cuh"
+#include "k3moe_internal.h"
+
+namespace k3 {
+
+// =====================================================================
+// Dense GEMV:  Y[t, m] = sum_k W[m, k] * X[t, k]
+//   W bf16 [M, K] row-major, X bf16 [T, K]; fp32 accumulation.
+//   rows m <  split -> out_f32 [t * split + m]            (router logits)
+//   rows m >= split -> out_bf16[t * (M - split) + m - split] (bf16, RNE)
+// One warp owns two rows; lanes stride over K in 16-byte vectors; tokens
+// are processed TG at a time (each pass re-reads the rows).
+// =====================================================================
+template <int TG>
+__global__ void __launch_bounds__(256) dense_gemv_kernel(const uint16_t* __restrict__ W, int M, int K,
+                                                         const uint16_t* __restrict__ X, int T, int split,
+                                                         float* __restrict__ out_f32,
+                                                         uint16_t* __restrict__ out_bf16) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = (blockIdx.x * 8 + warp) * 2;
+  if (m0 >= M) return;
+  const bool has1 = (m0 + 1) < M;
+  const uint4* w0 = reinterpret_cast<const uint4*>(W + (size_t)m0 * K);
+  const uint4* w1 = reinterpret_cast<const uint4*>(W + (size_t)(has1 ? m0 + 1 : m0) * K);
+  const int nvec = K >> 3;
+  for (int t0 = 0; t0 < T; t0 += TG) {
+    const int tn = min(TG, T - t0);
+    float acc0[TG], acc1[TG];
+#pragma unroll
+    for (int t = 0; t < TG; ++t) acc0[t] = acc1[t] = 0.f;
+    for (int v0 = lane; v0 < nvec; v0 += 32 * 4) {
+      uint4 a[4], b[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = v0 + 32 * u;
+        if (v < nvec) {
+          a[u] = __ldg(w0 + v);
+          b[u] = __ldg(w1 + v);
+        } else {
+          a[u] = b[u] = make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = v0 + 32 * u;
+        if (v >= nvec) break;
+        const uint32_t wa[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+        const uint32_t wb[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
+#pragma unroll
+        for (int t = 0; t < TG; ++t) {
+          if (t < tn) {
+            const uint4 xv = __ldg(reinterpret_cast<const uint4*>(X + (size_t)(t0 + t) * K) + v);
+            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 xf = unpack_bf16x2(xw[i]);
+              const float2 fa = unpack_bf16x2(wa[i]);
+              const float2 fb = unpack_bf16x2(wb[i]);
+              acc0[t] = fmaf(fa.x, xf.x, acc0[t]);
+              acc0[t] = fmaf(fa.y, xf.y, acc0[t]);
+              acc1[t] = fmaf(fb.x, xf.x, acc1[t]);
+              acc1[t] = fmaf(fb.y, xf.y, acc1[t]);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < TG; ++t) {
+      if (t >= tn) break;
+      const float s0 = warp_sum(acc0[t]);
+      const float s1 = warp_sum(acc1[t]);
+      if (lane == 0) {
+        const int tt = t0 + t;
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const int m = m0 + rr;
+          if (rr == 1 && !has1) break;
+          const float v = rr ? s1 : s0;
+          if (m < split)
+            out_f32[(size_t)tt * split + m] = v;
+          else
+            out_bf16[(size_t)tt * (M - split) + (m - split)] = f32_to_bf16(v);
+        }
+      }
+    }
+  }
+}
+
+cudaError_t launch_dense_gemv(const uint16_t* W, int M, int K, const uint16_t* X, int T, int split,
+                              float* out_f32, uint16_t* out_bf16, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  const int blocks = (M + 15) / 16;
+  if (T <= 1)
+    dense_gemv_kernel<1><<<blocks, 256, 0, s>>>(W, M, K, X, T, split, out_f32, out_bf16);
+  else if (T <= 2)
+    dense_gemv_kernel<2><<<blocks, 256, 0, s>>>(W, M, K, X, T, split, out_f32, out_bf16);
+  else if (T <= 4)
+    dense_gemv_kernel<4><<<blocks, 256, 0, s>>>(W, M, K, X, T, split, out_f32, out_bf16);
+  else
+    dense_gemv_kernel<8><<<blocks, 256, 0, s>>>(W, M, K, X, T, split, out_f32, out_bf16);
+  return cudaGetLastError();
+}
+
+// =====================================================================
+// Router top-K (one warp per token).
+//   s = sigmoid(logit) in fp32; key = s + bias (fp32); the K largest keys
+//   are taken one at a time, ties to the lower expert id; weights from the
+//   unbiased s, divided by their sum when norm_topk, times rsf.
+// =====================================================================
+template <int EPL>
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int T, int E, int ld,
+                                                   const float* __restrict__ bias, int K, int norm_topk, float rsf,
+                                                   int32_t* __restrict__ idx, float* __restrict__ w) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  float key[EPL], sc[EPL];
+  unsigned long long avail = 0;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      const float z = logits[(size_t)t * ld + e];
+      sc[i] = 1.0f / (1.0f + expf(-z));
+      key[i] = sc[i] + bias[e];
+      avail |= 1ull << i;
+    } else {
+      sc[i] = 0.f;
+      key[i] = -INFINITY;
+    }
+  }
+  float my_s = 0.f;
+  for (int k = 0; k < K; ++k) {
+    float bk = -INFINITY, bs = 0.f;
+    int be = INT_MAX;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      if (!((avail >> i) & 1ull)) continue;
+      const int e = lane + 32 * i;
+      if (key[i] > bk || (key[i] == bk && e < be)) {
+        bk = key[i];
+        be = e;
+        bs = sc[i];
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ok = __shfl_xor_sync(0xFFFFFFFFu, bk, off);
+      const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
+      const float os = __shfl_xor_sync(0xFFFFFFFFu, bs, off);
+      if (ok > bk || (ok == bk && oe < be)) {
+        bk = ok;
+        be = oe;
+        bs = os;
+      }
+    }
+    if (be != INT_MAX && (be & 31) == lane) avail &= ~(1ull << (be >> 5));
+    if (lane == k) my_s = bs;
+    if (lane == 0) idx[(size_t)t * K + k] = be;
+  }
+  float sum = 0.f;
+  // sum in k order (lane order) for a fixed, documented rounding sequence
+  for (int k = 0; k < K; ++k) sum += __shfl_sync(0xFFFFFFFFu, my_s, k);
+  if (lane < K) w[(size_t)t * K + lane] = (norm_topk ? my_s / sum : my_s) * rsf;
+}
+
+cudaError_t launch_topk(const float* logits, int T, int E, int ld, const float* bias, int K, int norm_topk,
+                        float rsf, int32_t* idx, float* w, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  const int blocks = (T + 7) / 8;
+  if (E <= 32 * 8)
+    topk_kernel<8><<<blocks, 256, 0, s>>>(logits, T, E, ld, bias, K, norm_topk, rsf, idx, w);
+  else if (E <= 32 * 32)
+    topk_kernel<32><<<blocks, 256, 0, s>>>(logits, T, E, ld, bias, K, norm_topk, rsf, idx, w);
+  else
+    topk_kernel<64><<<blocks, 256, 0, s>>>(logits, T, E, ld, bias, K, norm_topk, rsf, idx, w);
+  return cudaGetLastError();
+}
+
+// =====================================================================
+// Token -> expert permutation ("sort the (token, expert) pairs by expert",
+// kimi-k3-mlx README, REAP section): counts, offsets, a stable order of the
+// T*K assignments grouped by expert (slot -> t*K + k), its inverse, and the
+// list of experts that received work.  Three kernels; deterministic.
+// =====================================================================
+__global__ void __launch_bounds__(kPermChunk) perm_hist_kernel(const int32_t* __restrict__ idx, int TK, int E,
+                                                               int* __restrict__ blk_hist) {
+  extern __shared__ int hist[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int a = blockIdx.x * kPermChunk + threadIdx.x;
+  if (a < TK) atomicAdd(&hist[idx[a]], 1);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) blk_hist[(size_t)blockIdx.x * E + e] = hist[e];
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x == 1024).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int wv = warp_tot[lane];
+    int wi = wv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    warp_tot[lane] = wi - wv;
+    if (lane == 31) *total = wi;
+  }
+  __syncthreads();
+  const int r = warp_tot[warp] + incl - v;
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(1024) perm_scan_kernel(int* __restrict__ blk_hist, int nblk, int E, int TK,
+                                                         int* __restrict__ counts, int* __restrict__ offsets,
+                                                         int* __restrict__ active) {
+  __shared__ int warp_tot[32];
+  __shared__ int total_s, carry_off, carry_act;
+  if (threadIdx.x == 0) {
+    carry_off = 0;
+    carry_act = 0;
+  }
+  __syncthreads();
+  for (int e0 = 0; e0 < E; e0 += 1024) {
+    const int e = e0 + threadIdx.x;
+    int tot = 0;
+    if (e < E) {
+      // per-block prefix of this expert's count, in block order
+      for (int b = 0; b < nblk; ++b) {
+        const int c = blk_hist[(size_t)b * E + e];
+        blk_hist[(size_t)b * E + e] = tot;
+        tot += c;
+      }
+      counts[e] = tot;
+    }
+    const int ex = block_exclusive_scan(tot, warp_tot, &total_s);
+    const int add_off = carry_off;
+    if (e < E) offsets[e] = add_off + ex;
+    const int flag = (e < E && tot > 0) ? 1 : 0;
+    const int add_tot = total_s;
+    const int ax = block_exclusive_scan(flag, warp_tot, &total_s);
+    if (flag) active[1 + carry_act + ax] = e;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      carry_off += add_tot;
+      carry_act += total_s;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    offsets[E] = TK;
+    active[0] = carry_act;
+  }
+}
+
+__global__ void __launch_bounds__(kPermChunk) perm_scatter_kernel(const int32_t* __restrict__ idx, int TK, int E,
+                                                                  const int* __restrict__ blk_prefix,
+                                                                  const int* __restrict__ offsets,
+                                                                  int* __restrict__ perm, int* __restrict__ slot) {
+  extern __shared__ int run[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) run[e] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int a = blockIdx.x * kPermChunk + threadIdx.x;
+  const bool valid = a < TK;
+  const int e = valid ? idx[a] : -1;
+  const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  const bool leader = (__ffs(peers) - 1) == lane;
+  int base = 0;
+  for (int w = 0; w < kPermChunk / 32; ++w) {
+    if (warp == w && valid) {
+      base = run[e];
+      __syncwarp(peers);
+      if (leader) run[e] = base + __popc(peers);
+    }
+    __syncthreads();
+  }
+  if (valid) {
+    const int s = offsets[e] + blk_prefix[(size_t)blockIdx.x * E + e] + base + rank;
+    perm[s] = a;
+    slot[a] = s;
+  }
+}
+
+cudaError_t launch_permute(const int32_t* idx, int T, int K, int E, int* blk_hist, int* counts, int* offsets,
+                           int* active, int* perm, int* slot, cudaStream_t s) {
+  const int TK = T * K;
+  if (TK <= 0) return cudaSuccess;
+  const int nblk = (TK + kPermChunk - 1) / kPermChunk;
+  const size_t sm = sizeof(int) * (size_t)E;
+  perm_hist_kernel<<<nblk, kPermChunk, sm, s>>>(idx, TK, E, blk_hist);
+  perm_scan_kernel<<<1, 1024, 0, s>>>(blk_hist, nblk, E, TK, counts, offsets, active);
+  perm_scatter_kernel<<<nblk, kPermChunk, sm, s>>>(idx, TK, E, blk_hist, offsets, perm, slot);
+  return cudaGetLastError();
+}
+
+// =====================================================================
+// SiTU-GLU in fp32 (kimi-k3-mlx README, "Architecture" table and
+// "Porting notes" item 1): beta*tanh(g/beta)*sigmoid(g) * beta_lin*tanh(u/beta_lin).
+// =====================================================================
+__device__ __forceinline__ float situ_glu(float g, float u, float beta, float beta_lin) {
+  const float sig = 1.0f / (1.0f + expf(-g));
+  return beta * tanhf(g / beta) * sig * beta_lin * tanhf(u / beta_lin);
+}
+
+// Position, within each group of 8 staged activations, of column c (the
+// inverse of dec2_column_of).
+__device__ __forceinline__ int dec2_pos_of_column(int c) {
+  // columns 0..7 -> stream positions
+  const int pos[8] = {0, 4, 1, 5, 2, 6, 3, 7};
+  return pos[c];
+}
+
+// Accumulate sum_i w_i * x_i over one 32-column scale group held in the
+// 16-byte chunk q, for NT staged token rows (xs rows of `ld` floats,
+// starting at stream column x0).
+template <int NT>
+__device__ __forceinline__ void group_dot(const uint4& q, const float* __restrict__ xs, int ld, int x0, int nt,
+                                          float part[NT]) {
+  const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float2 f[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) f[b] = f16x2_to_f32x2(e2m1x2_to_f16x2((wd[j] >> (8 * b)) & 0xFFu));
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      if (t < nt) {
+        const float4 xa = *reinterpret_cast<const float4*>(xs + (size_t)t * ld + x0 + 8 * j);
+        const float4 xb = *reinterpret_cast<const float4*>(xs + (size_t)t * ld + x0 + 8 * j + 4);
+        unsigned long long acc = pack_f32x2(part[t], 0.f);
+        acc = ffma2(pack_f32x2(f[0].x, f[0].y), pack_f32x2(xa.x, xa.y), acc);
+        acc = ffma2(pack_f32x2(f[1].x, f[1].y), pack_f32x2(xa.z, xa.w), acc);
+        acc = ffma2(pack_f32x2(f[2].x, f[2].y), pack_f32x2(xb.x, xb.y), acc);
+        acc = ffma2(pack_f32x2(f[3].x, f[3].y), pack_f32x2(xb.z, xb.w), acc);
+        const float2 r = unpack_f32x2(acc);
+        part[t] = r.x + r.y;
+      }
+    }
+  }
+}
+
+// Stage nb token rows (bf16, length len, row index from `rows_of`) as fp32
+// in decoder-2 stream order.
+template <typename RowOf>
+__device__ __forceinline__ void stage_rows(float* xs, const uint16_t* __restrict__ src, int len, int nb,
+                                           RowOf rows_of) {
+  for (int i = threadIdx.x; i < nb * len; i += blockDim.x) {
+    const int j = i / len, c = i - j * len;
+    const size_t row = rows_of(j);
+    xs[(size_t)j * len + (c & ~7) + dec2_pos_of_column(c & 7)] = bf16_to_f32(src[row * len + c]);
+  }
+}
+
+// =====================================================================
+// Grouped MXFP4 gate/up GEMV + SiTU-GLU.  Work item (a, mt): active expert
+// a, output rows [128 mt, 128 mt + 128) of both w1 (gate) and w3 (up).
+// Threads 0..127 stream gate rows, 128..255 the matching up rows; each
+// thread's row tile is read once per pass of up to TB tokens.
+//   h[slot, j] = bf16(SiTU(W1_e[j] . lat[t], W3_e[j] . lat[t]))
+// =====================================================================
+template <int TB>
+__global__ void __launch_bounds__(256) gateup_gemv_kernel(const uint8_t* __restrict__ gu_tiles,
+                                                          const uint16_t* __restrict__ lat,
+                                                          const int* __restrict__ active,
+                                                          const int* __restrict__ offsets,
+                                                          const int* __restrict__ perm, int Ktop, int L, int I,
+                                                          float beta, float beta_lin, uint16_t* __restrict__ h) {
+  extern __shared__ float xs[];  // [TB, L] staged activations
+  __shared__ float ubuf[TB][128];
+  const int n_mt = I / kTileRows;
+  const int a = blockIdx.x / n_mt, mt = blockIdx.x - (blockIdx.x / n_mt) * n_mt;
+  if (a >= active[0]) return;
+  const int e = active[1 + a];
+  const int s0 = offsets[e], n = offsets[e + 1] - s0;
+  const int tid = threadIdx.x, r = tid & 127;
+  const bool is_up = tid >= 128;
+  const int KS = L / kTileCols;
+  const uint8_t* base =
+      gu_tiles + ((size_t)(e * n_mt + mt) * KS) * 2 * kTileBytes + (is_up ? kTileBytes : 0);
+  for (int p0 = 0; p0 < n; p0 += TB) {
+    const int nb = min(TB, n - p0);
+    __syncthreads();
+    stage_rows(xs, lat, L, nb, [&](int j) { return (size_t)(perm[s0 + p0 + j] / Ktop); });
+    __syncthreads();
+    float acc[TB];
+#pragma unroll
+    for (int t = 0; t < TB; ++t) acc[t] = 0.f;
+    const uint8_t* tile = base;
+    uint4 c0 = __ldg(reinterpret_cast<const uint4*>(tile) + r);
+    uint4 c1 = __ldg(reinterpret_cast<const uint4*>(tile) + 128 + r);
+    uint32_t sc = __ldg(reinterpret_cast<const uint16_t*>(tile + kTilePackedBytes) + r);
+    for (int ks = 0; ks < KS; ++ks) {
+      uint4 n0 = c0, n1 = c1;
+      uint32_t nsc = sc;
+      if (ks + 1 < KS) {
+        const uint8_t* nt = tile + 2 * kTileBytes;
+        n0 = __ldg(reinterpret_cast<const uint4*>(nt) + r);
+        n1 = __ldg(reinterpret_cast<const uint4*>(nt) + 128 + r);
+        nsc = __ldg(reinterpret_cast<const uint16_t*>(nt + kTilePackedBytes) + r);
+      }
+      float part[TB];
+#pragma unroll
+      for (int t = 0; t < TB; ++t) part[t] = 0.f;
+      group_dot<TB>(c0, xs, L, ks * kTileCols, nb, part);
+      const float sf0 = e8m0_to_f32(sc & 0xFFu);
+#pragma unroll
+      for (int t = 0; t < TB; ++t) {
+        acc[t] = fmaf(sf0, part[t], acc[t]);
+        part[t] = 0.f;
+      }
+      group_dot<TB>(c1, xs, L, ks * kTileCols + 32, nb, part);
+      const float sf1 = e8m0_to_f32(sc >> 8);
+#pragma unroll
+      for (int t = 0; t < TB; ++t) acc[t] = fmaf(sf1, part[t], acc[t]);
+      c0 = n0;
+      c1 = n1;
+      sc = nsc;
+      tile += 2 * kTileBytes;
+    }
+    if (is_up) {
+#pragma unroll
+      for (int t = 0; t < TB; ++t) ubuf[t][r] = acc[t];
+    }
+    __syncthreads();
+    if (!is_up) {
+#pragma unroll
+      for (int t = 0; t < TB; ++t) {
+        if (t < nb)
+          h[(size_t)(s0 + p0 + t) * I + mt * kTileRows + r] = f32_to_bf16(situ_glu(acc[t], ubuf[t][r], beta, beta_lin));
+      }
+    }
+  }
+}
+
+cudaError_t launch_gateup_gemv(const uint8_t* gu_tiles, const uint16_t* lat, const int* active,
+                               const int* offsets, const int* perm, int max_active, const Dims& d,
+                               uint16_t* h, cudaStream_t s) {
+  constexpr int TB = 4;
+  const int grid = max_active * (d.I / kTileRows);
+  if (grid <= 0) return cudaSuccess;
+  const size_t sm = sizeof(float) * (size_t)TB * d.L;
+  cudaFuncSetAttribute(gateup_gemv_kernel<TB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  gateup_gemv_kernel<TB><<<grid, 256, sm, s>>>(gu_tiles, lat, active, offsets, perm, d.K, d.L, d.I, d.beta,
+                                               d.beta_lin, h);
+  return cudaGetLastError();
+}
+
+// =====================================================================
+// Grouped MXFP4 down GEMV.  Work item (a, mt): active expert a, output rows
+// [128 mt, 128 mt + 128) of w2.  Threads t and t+128 take the two halves of
+// the input columns of row t; the halves are added in a fixed order.
+//   o[slot, l] = W2_e[l] . h[slot]   (fp32)
+// =====================================================================
+template <int TB>
+__global__ void __launch_bounds__(256) down_gemv_kernel(const uint8_t* __restrict__ d_tiles,
+                                                        const uint16_t* __restrict__ h,
+                                                        const int* __restrict__ active,
+                                                        const int* __restrict__ offsets, int L, int I,
+                                                        float* __restrict__ o) {
+  extern __shared__ float xs[];  // [TB, I]
+  __shared__ float half1[TB][128];
+  const int n_mt = L / kTileRows;
+  const int a = blockIdx.x / n_mt, mt = blockIdx.x - (blockIdx.x / n_mt) * n_mt;
+  if (a >= active[0]) return;
+  const int e = active[1 + a];
+  const int s0 = offsets[e], n = offsets[e + 1] - s0;
+  const int tid = threadIdx.x, r = tid & 127, hf = tid >> 7;
+  const int KS = I / kTileCols, ks_begin = hf * (KS / 2), ks_end = hf ? KS : KS / 2;
+  const uint8_t* base = d_tiles + ((size_t)(e * n_mt + mt) * KS) * kTileBytes;
+  for (int p0 = 0; p0 < n; p0 += TB) {
+    const int nb = min(TB, n - p0);
+    __syncthreads();
+    stage_rows(xs, h, I, nb, [&](int j) { return (size_t)(s0 + p0 + j); });
+    __syncthreads();
+    float acc[TB];
+#pragma unroll
+    for (int t = 0; t < TB; ++t) acc[t] = 0.f;
+    const uint8_t* tile = base + (size_t)ks_begin * kTileBytes;
+    uint4 c0 = __ldg(reinterpret_cast<const uint4*>(tile) + r);
+    uint4 c1 = __ldg(reinterpret_cast<const uint4*>(tile) + 128 + r);
+    uint32_t sc = __ldg(reinterpret_cast<const uint16_t*>(tile + kTilePackedBytes) + r);
+    for (int ks = ks_begin; ks < ks_end; ++ks) {
+      uint4 n0 = c0, n1 = c1;
+      uint32_t nsc = sc;
+      if (ks + 1 < ks_end) {
+        const uint8_t* nt = tile + kTileBytes;
+        n0 = __ldg(reinterpret_cast<const uint4*>(nt) + r);
+        n1 = __ldg(reinterpret_cast<const uint4*>(nt) + 128 + r);
+        nsc = __ldg(reinterpret_cast<const uint16_t*>(nt + kTilePackedBytes) + r);
+      }
+      float part[TB];
+#pragma unroll
+      for (int t = 0; t < TB; ++t) part[t] = 0.f;
+      group_dot<TB>(c0, xs, I, ks * kTileCols, nb, part);
+      const float sf0 = e8m0_to_f32(sc & 0xFFu);
+#pragma unroll
+      for (int t = 0; t < TB; ++t) {
+        acc[t] = fmaf(sf0, part[t], acc[t]);
+        part[t] = 0.f;
+      }
+      group_dot<TB>(c1, xs, I, ks * kTileCols + 32, nb, part);
+      const float sf1 = e8m0_to_f32(sc >> 8);
+#pragma unroll
+      for (int t = 0; t < TB; ++t) acc[t] = fmaf(sf1, part[t], acc[t]);
+      c0 = n0;
+      c1 = n1;
+      sc = nsc;
+      tile += kTileBytes;
+    }
+    if (hf) {
+#pragma unroll
+      for (int t = 0; t < TB; ++t) half1[t][r] = acc[t];
+    }
+    __syncthreads();
+    if (!hf) {
+#pragma unroll
+      for (int t = 0; t < TB; ++t)
+        if (t < nb) o[(size_t)(s0 + p0 + t) * L + mt * kTileRows + r] = acc[t] + half1[t][r];
+    }
+  }
+}
+
+cudaError_t launch_down_gemv(const uint8_t* d_tiles, const uint16_t* h, const int* active, const int* offsets,
+                             int max_active, const Dims& d, float* o, cudaStream_t s) {
+  constexpr int TB = 4;
+  const int grid = max_active * (d.L / kTileRows);
+  if (grid <= 0) return cudaSuccess;
+  const size_t sm = sizeof(float) * (size_t)TB * d.I;
+  cudaFuncSetAttribute(down_gemv_kernel<TB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  down_gemv_kernel<TB><<<grid, 256, sm, s>>>(d_tiles, h, active, offsets, d.L, d.I, o);
+  return cudaGetLastError();
+}
+
+// =====================================================================
+// Weighted combine (k order, fp32) + RMSNorm over the latent (kimi-k3-mlx
+// README, REAP section caveat: RMSNorm on the combined expert output,
+// before up_proj).  One CTA per token.
+// =====================================================================
+__global__ void __launch_bounds__(256) combine_rmsnorm_kernel(const float* __restrict__ o,
+                                                              const int* __restrict__ slot,
+                                                              const float* __restrict__ topk_w,
+                                                              const uint16_t* __restrict__ gamma, int K, int L,
+                                                              float eps, uint16_t* __restrict__ n) {
+  extern __shared__ float cs[];  // [L]
+  __shared__ int sl[32];
+  __shared__ float wk[32];
+  __shared__ float red[8];
+  const int t = blockIdx.x;
+  if (threadIdx.x < K) {
+    sl[threadIdx.x] = slot[(size_t)t * K + threadIdx.x];
+    wk[threadIdx.x] = topk_w[(size_t)t * K + threadIdx.x];
+  }
+  __syncthreads();
+  float ss = 0.f;
+  for (int l = threadIdx.x; l < L; l += blockDim.x) {
+    float c = 0.f;
+    for (int k = 0; k < K; ++k) c = fmaf(wk[k], o[(size_t)sl[k] * L + l], c);
+    cs[l] = c;
+    ss = fmaf(c, c, ss);
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += red[i];
+  const float inv = 1.0f / sqrtf(tot / (float)L + eps);
+  for (int l = threadIdx.x; l < L; l += blockDim.x)
+    n[(size_t)t * L + l] = f32_to_bf16(cs[l] * inv * bf16_to_f32(gamma[l]));
+}
+
+cudaError_t launch_combine_rmsnorm(const float* o, const int* slot, const float* topk_w, const uint16_t* gamma,
+                                   int T, const Dims& d, uint16_t* n, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  combine_rmsnorm_kernel<<<T, 256, sizeof(float) * d.L, s>>>(o, slot, topk_w, gamma, d.K, d.L, d.rms_eps, n);
+  return cudaGetLastError();
+}
+
+// =====================================================================
+// Checkpoint MXFP4 -> tile format.  n_mat matrices [rows, cols] (packed
+// [rows, cols/2], scale [rows, cols/32]); tile (m, mt, ks) goes to
+// tiles + ((m * mat_stride_tiles) + (mt * KS + ks) * tile_step + tile_offset) * kTileBytes.
+// One thread per 32-bit word of a tile (1024 packed words + 64 scale words).
+// =====================================================================
+__global__ void relayout_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scale, int n_mat,
+                                int rows, int cols, uint8_t* __restrict__ tiles, size_t mat_stride_tiles,
+                                int tile_step, int tile_offset) {
+  const int KS = cols / kTileCols, MT = rows / kTileRows;
+  const long long words_per_tile = kTileBytes / 4;  // 1088
+  const long long total = (long long)n_mat * MT * KS * words_per_tile;
+  for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < total;
+       g += (long long)gridDim.x * blockDim.x) {
+    const int w = (int)(g % words_per_tile);
+    const long long tile_lin = g / words_per_tile;
+    const int ks = (int)(tile_lin % KS);
+    const int mt = (int)((tile_lin / KS) % MT);
+    const int m = (int)(tile_lin / ((long long)KS * MT));
+    uint8_t* tile = tiles + ((size_t)m * mat_stride_tiles + ((size_t)mt * KS + ks) * tile_step + tile_offset) *
+                                (size_t)kTileBytes;
+    uint32_t word;
+    if (w < 1024) {
+      const int ch = w >> 2, j = w & 3;
+      const int c = ch >> 7, r = ch & 127;
+      const size_t row = (size_t)m * rows + (size_t)mt * kTileRows + r;
+      const int col0 = ks * kTileCols + c * 32 + j * 8;
+      const uint8_t* src = packed + row * (cols / 2) + col0 / 2;
+      word = tile_word_from_checkpoint(src[0], src[1], src[2], src[3]);
+    } else {
+      const int sw = w - 1024;  // bytes 4sw..4sw+3: rows 2sw, 2sw+1, groups 0 and 1
+      const size_t row0 = (size_t)m * rows + (size_t)mt * kTileRows + 2 * sw;
+      const uint8_t* s0 = scale + row0 * (cols / 32) + ks * 2;
+      const uint8_t* s1 = s0 + cols / 32;
+      word = (uint32_t)s0[0] | ((uint32_t)s0[1] << 8) | ((uint32_t)s1[0] << 16) | ((uint32_t)s1[1] << 24);
+    }
+    reinterpret_cast<uint32_t*>(tile)[w] = word;
+  }
+}
+
+cudaError_t launch_relayout(const uint8_t* packed, const uint8_t* scale, int n_mat, int rows, int cols,
+                            uint8_t* tiles, size_t mat_stride_tiles, int tile_step, int tile_offset,
+                            cudaStream_t s) {
+  relayout_kernel<<<152 * 8, 256, 0, s>>>(packed, scale, n_mat, rows, cols, tiles, mat_stride_tiles, tile_step,
+                                          tile_offset);
+  return cudaGetLastError();
+}
+
+// =====================================================================
+// Standalone dequant (checkpoint layout in, row-major out) through the same
+// tile-word re-layout and decoders as the expert kernels.
+//   kind 0: bf16 via decoder 1 (tensor-core tile producer)
+//   kind 1: fp32 via decoder 2 (decode GEMV), value = e2m1 * e8m0_to_f32(S)
+// One thread per 8 consecutive columns of a row.
+// =====================================================================
+__global__ void dequant_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scale, int rows,
+                               int cols, void* __restrict__ out, int kind) {
+  const long long total = (long long)rows * (cols / 8);
+  for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < total;
+       g += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(g / (cols / 8));
+    const int col0 = (int)(g % (cols / 8)) * 8;
+    const uint8_t* src = packed + (size_t)r * (cols / 2) + col0 / 2;
+    const uint32_t q = tile_word_from_checkpoint(src[0], src[1], src[2], src[3]);
+    const uint32_t S = scale[(size_t)r * (cols / 32) + col0 / 32];
+    if (kind == 0) {
+      uint32_t o4[4];
+      tile_word_to_bf16(q, scale_multipliers(S), o4);
+      *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + (size_t)r * cols + col0) =
+          make_uint4(o4[0], o4[1], o4[2], o4[3]);
+    } else {
+      const float sf = e8m0_to_f32(S);
+      float* dst = reinterpret_cast<float*>(out) + (size_t)r * cols + col0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const float2 f = f16x2_to_f32x2(e2m1x2_to_f16x2((q >> (8 * b)) & 0xFFu));
+        dst[dec2_column_of(2 * b)] = f.x * sf;
+        dst[dec2_column_of(2 * b + 1)] = f.y * sf;
+      }
+    }
+  }
+}
+
+cudaError_t launch_dequant(const uint8_t* packed, const uint8_t* scale, int rows, int cols, void* out,
+                           int kind, cudaStream_t s) {
+  const long long total = (long long)rows * (cols / 8);
+  if (total <= 0) return cudaSuccess;
+  const int blocks = (int)std::min<long long>((total + 255) / 256, 152LL * 16);
+  dequant_kernel<<<blocks, 256, 0, s>>>(packed, scale, rows, cols, out, kind);
+  return cudaGetLastError();
+}
+
+}  // namespace k3

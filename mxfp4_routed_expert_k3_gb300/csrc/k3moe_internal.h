@@ -1,0 +1,53 @@
+// k3moe_internal.h -- launchers shared between the library's translation
+// units (host side only; no torch types).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace k3 {
+
+struct Dims {
+  int H, L, E, K, I;
+  float beta, beta_lin, rms_eps, rsf;
+  int norm_topk;
+};
+
+// Workspace views for one forward call (all device memory).
+struct Work {
+  float* logits;      // [Tm, E]
+  uint16_t* lat;      // [Tm, L]
+  int* counts;        // [E]
+  int* offsets;       // [E + 1]
+  int* active;        // [E + 1]: n_active, then expert ids
+  int* perm;          // [Tm * K] slot -> t*K + k
+  int* slot;          // [Tm * K] t*K + k -> slot
+  int* blk_hist;      // [nblk_max, E]
+  uint16_t* h;        // [Tm * K, I]
+  float* o;           // [Tm * K, L]
+  uint16_t* n;        // [Tm, L]
+  unsigned* status;   // device status word
+};
+
+// ---- k3moe_decode.cu
+cudaError_t launch_dense_gemv(const uint16_t* W, int M, int K, const uint16_t* X, int T, int split,
+                              float* out_f32, uint16_t* out_bf16, cudaStream_t s);
+cudaError_t launch_topk(const float* logits, int T, int E, int ld, const float* bias, int K, int norm_topk,
+                        float rsf, int32_t* idx, float* w, cudaStream_t s);
+constexpr int kPermChunk = 1024;
+cudaError_t launch_permute(const int32_t* idx, int T, int K, int E, int* blk_hist, int* counts, int* offsets,
+                           int* active, int* perm, int* slot, cudaStream_t s);
+cudaError_t launch_gateup_gemv(const uint8_t* gu_tiles, const uint16_t* lat, const int* active,
+                               const int* offsets, const int* perm, int max_active, const Dims& d,
+                               uint16_t* h, cudaStream_t s);
+cudaError_t launch_down_gemv(const uint8_t* d_tiles, const uint16_t* h, const int* active, const int* offsets,
+                             int max_active, const Dims& d, float* o, cudaStream_t s);
+cudaError_t launch_combine_rmsnorm(const float* o, const int* slot, const float* topk_w, const uint16_t* gamma,
+                                   int T, const Dims& d, uint16_t* n, cudaStream_t s);
+cudaError_t launch_relayout(const uint8_t* packed, const uint8_t* scale, int n_mat, int rows, int cols,
+                            uint8_t* tiles, size_t mat_stride_tiles, int tile_step, int tile_offset,
+                            cudaStream_t s);
+cudaError_t launch_dequant(const uint8_t* packed, const uint8_t* scale, int rows, int cols, void* out,
+                           int kind, cudaStream_t s);
+
+}  // namespace k3

@@ -1,0 +1,29 @@
+// k3moe_umma.h -- the tensor-core (tcgen05 / TMEM / TMA) path used for
+// larger token counts: dense bf16 GEMMs (router + down_proj, up_proj) and
+// the grouped MXFP4 expert GEMMs.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "k3moe_internal.h"
+
+namespace k3 {
+
+struct UmmaPlan {
+  bool enabled = false;   // false: every forward uses the CUDA-core kernels
+  int min_tokens = 1 << 30;
+  size_t ws_bytes = 256;  // workspace this path needs (tile lists, B copies)
+  void* ws = nullptr;
+};
+
+UmmaPlan umma_plan(const Dims& d, int max_tokens);
+bool umma_path_enabled(const UmmaPlan& p, const Dims& d, int T);
+cudaError_t umma_dense(const UmmaPlan& p, const uint16_t* W, int M, int K, const uint16_t* X, int T, int split,
+                       float* out_f32, uint16_t* out_bf16, cudaStream_t s);
+int umma_dense_launches();
+cudaError_t umma_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8_t* d_tiles, const Work& w, int T,
+                         const Dims& d, cudaStream_t s);
+int umma_expert_launches();
+
+}  // namespace k3

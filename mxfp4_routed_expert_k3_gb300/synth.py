@@ -134,6 +134,12 @@ def token_rows(d: LayerDims, seed: int, T: int, attempts: np.ndarray | None = No
     return x
 
 
+def token_row_into(d: LayerDims, seed: int, t: int, attempt: int, out: np.ndarray) -> None:
+    """Row t of attempt `attempt` (the same values token_rows would give it)."""
+    assert out.dtype == np.uint16 and out.size == d.hidden and out.flags.c_contiguous
+    lib().k3s_fill_bf16_normal(seed, S_X + attempt, t * d.hidden, 0.0, 1.0, out.ctypes.data, d.hidden)
+
+
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
 

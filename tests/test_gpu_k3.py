@@ -1,0 +1,87 @@
+"""GPU parity at K3 dims (H=7168, L=3584, 896 experts, top-16, I=3072) in
+the launch configuration the benchmark times: decode T = 1, 8, 64 against
+the oracle on every token; prefill T = 8192 and the skewed T = 4096 case
+with the routing of every token checked bit for bit and the outputs on a
+seeded sample of tokens."""
+import numpy as np
+import pytest
+
+from mxfp4_routed_expert_k3_gb300 import k3moe, synth
+from mxfp4_routed_expert_k3_gb300.dims import K3
+from oracle import oracle as ora
+
+from _cases import assert_routing_equal, assert_y_close, gapped_tokens, y_metrics
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+MAXT = 8192
+
+
+@pytest.fixture(scope="module")
+def k3layer():
+    w = synth.layer_weights(K3, seed=1)
+    layer = k3moe.Layer(K3, w, max_tokens=MAXT)
+    yield w, layer
+    layer.close()
+
+
+def run(layer, x_np):
+    d = layer.d
+    T = x_np.shape[0]
+    x = torch.from_numpy(x_np.view(np.int16)).cuda()
+    y = torch.empty((T, d.hidden), dtype=torch.int16, device="cuda")
+    idx = torch.empty((T, d.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, d.top_k), dtype=torch.float32, device="cuda")
+    layer.forward(x, y, idx, w, stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    return y.cpu().numpy().view(np.uint16), idx.cpu().numpy(), w.cpu().numpy()
+
+
+@pytest.mark.parametrize("T", [1, 8, 64])
+def test_k3_decode_all_tokens(k3layer, T):
+    w, layer = k3layer
+    x = gapped_tokens(K3, w, seed=200 + T, T=T)
+    ref = ora.forward(K3, w, x)
+    y, idx, wts = run(layer, x)
+    assert_routing_equal(idx, wts, ref["idx"], ref["w"], f"decode T={T}")
+    m = assert_y_close(y, ref["y"], f"decode T={T}")
+    print(f"decode T={T} path={layer.query('path_last')}", m)
+
+
+def _sampled(layer, w, x, n_sample, seed, label):
+    T = x.shape[0]
+    idx_ref, w_ref, _ = ora.route(K3, x, w["router_w"], w["router_bias"])
+    y, idx, wts = run(layer, x)
+    assert_routing_equal(idx, wts, idx_ref, w_ref, label)
+    sample = np.sort(np.random.default_rng(seed).choice(T, n_sample, replace=False))
+    sample[-1] = T - 1  # always include the ragged tail
+    ref = ora.forward(K3, w, np.ascontiguousarray(x[sample]))
+    m = assert_y_close(y[sample], ref["y"], label)
+    # properties that hold for every token
+    yf = (y.astype(np.uint32) << 16).view(np.float32)
+    assert np.all(np.isfinite(yf))
+    assert np.allclose(wts.sum(1), K3.routed_scaling, rtol=1e-5)
+    print(label, f"path={layer.query('path_last')}", m)
+    return idx
+
+
+def test_k3_prefill_8192(k3layer):
+    w, layer = k3layer
+    x = gapped_tokens(K3, w, seed=300, T=8192)
+    _sampled(layer, w, x, 24, 1, "prefill T=8192")
+
+
+def test_k3_skewed_4096():
+    w = synth.layer_weights(K3, seed=3, n_hot=32)
+    hot = synth.hot_experts(K3, 3, 32)
+    layer = k3moe.Layer(K3, w, max_tokens=4096)
+    try:
+        x = gapped_tokens(K3, w, seed=301, T=4096)
+        idx = _sampled(layer, w, x, 16, 2, "skew T=4096")
+        assert np.isin(idx, hot).all()
+        counts = layer.fetch("counts", (K3.n_experts,), np.int32)
+        assert np.count_nonzero(counts) == 32 and counts.sum() == 4096 * 16
+    finally:
+        layer.close()
