@@ -1,0 +1,404 @@
+#!/usr/bin/env python3
+"""Benchmark of the K3 LatentMoE MXFP4 routed-expert layer on GB300.
+
+Default workload: one K3-dim routed layer at decode sizes (H=7168,
+L=3584, 896 experts top-16, I=3072, ~15.7 GB of MXFP4 expert weights); one
+step = one forward of a fresh T=1 batch, a fresh T=8 batch and a fresh
+T=64 batch (73 tokens).  Inputs and weights are seeded synthetic data and
+are resident in HBM before timing.  L2 is flushed (512 MB write) before
+every forward, outside the timed events.  Each forward is replayed from a
+CUDA graph captured from the library's C-ABI forward call.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on
+the host cores instead (a bounded sample of the same workload per step).
+Under torchrun every rank runs its own replica of the workload on its own
+GPU (tokens are independent: weak scaling, no data-path collective);
+timing is max over ranks and `value` sums the ranks' tokens.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DECODE_BATCHES = (1, 8, 64)
+METRIC = "LatentMoE MXFP4 layer tokens/s (K3 dims); decode HBM GB/s vs ~8 TB/s"
+FLUSH_BYTES = 512 << 20
+REASON_BITS = {
+    0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+    0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+    0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
+}
+
+
+def dist_info():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def reduce_max_over_ranks(value: float, world: int, device=None) -> float:
+    """max over ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,utilization.gpu")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], None, set()
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                clk, mx, util = float(parts[1]), float(parts[2]), float(parts[5])
+                act = int(parts[4], 16)
+            except ValueError:
+                continue
+            smax = mx
+            if util > 0:
+                sm.append(clk)
+                for bit, name in REASON_BITS.items():
+                    if act & bit and name != "gpu_idle":
+                        reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def source_sha(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel's
+    source is unchanged since it was taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(kernel)
+    if not rec or rec.get("workload") != workload:
+        return None
+    src = os.path.join(ROOT, "mxfp4_routed_expert_k3_gb300", "csrc", rec["source"])
+    if not os.path.exists(src) or source_sha(src) != rec.get("source_sha"):
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
+# ============================================================================ ours
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from mxfp4_routed_expert_k3_gb300 import k3moe, synth
+    from mxfp4_routed_expert_k3_gb300.dims import K3
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    d = K3
+    batches = DECODE_BATCHES
+    maxT = max(batches)
+    w = synth.layer_weights(d, seed=1)
+    layer = k3moe.Layer(d, w, max_tokens=maxT, device=local_rank)
+    stream = torch.cuda.Stream(device=dev)
+    pool = args.warmup + args.steps
+    # fresh token batches for every step, resident in HBM before timing
+    xs = {T: [torch.from_numpy(synth.token_rows(d, 5000 + 97 * rank + 13 * i + T, T).view(np.int16)).to(dev)
+              for i in range(pool)] for T in batches}
+    x_in = {T: torch.empty((T, d.hidden), dtype=torch.int16, device=dev) for T in batches}
+    y = {T: torch.empty((T, d.hidden), dtype=torch.int16, device=dev) for T in batches}
+    idx = {T: torch.empty((T, d.top_k), dtype=torch.int32, device=dev) for T in batches}
+    wt = {T: torch.empty((T, d.top_k), dtype=torch.float32, device=dev) for T in batches}
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    with torch.cuda.stream(stream):
+        for T in batches:  # eager warm-up before capture
+            x_in[T].copy_(xs[T][0])
+            layer.forward(x_in[T], y[T], idx[T], wt[T], stream=stream)
+    stream.synchronize()
+    k3moe.profile(layer.ctx, True)
+    graphs = {}
+    for T in batches:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            layer.forward(x_in[T], y[T], idx[T], wt[T], stream=stream)
+        graphs[T] = g
+    launches_per_forward = {}
+    for T in batches:
+        layer.forward(x_in[T], y[T], idx[T], wt[T], stream=stream)
+        launches_per_forward[T] = layer.query("launches_last")
+    stream.synchronize()
+
+    ev = {T: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(pool)]
+          for T in batches}
+    per_kernel = {T: [] for T in batches}
+    active_experts = {T: [] for T in batches}
+
+    def one_step(i, record):
+        for T in batches:
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                x_in[T].copy_(xs[T][i])
+                ev[T][i][0].record(stream)
+                graphs[T].replay()
+                ev[T][i][1].record(stream)
+            if record:
+                stream.synchronize()
+                per_kernel[T].append(k3moe.profile_read(layer.ctx))
+                act = np.empty(d.n_experts + 1, np.int32)
+                k3moe.fetch(layer.ctx, "active", act)
+                active_experts[T].append(int(act[0]))
+
+    for i in range(args.warmup):
+        one_step(i, False)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler(local_rank)
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for i in range(args.warmup, pool):
+        one_step(i, True)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    barrier(world)
+    clk = clocks.stop()
+    assert layer.status() == 0, k3moe.last_error(layer.ctx)
+
+    fwd_ms = {T: [ev[T][i][0].elapsed_time(ev[T][i][1]) for i in range(args.warmup, pool)] for T in batches}
+    step_ms = sum(statistics.mean(fwd_ms[T]) for T in batches)
+    tokens_per_step = sum(batches)
+    step_ms_max = reduce_max_over_ranks(step_ms, world, dev)
+    value = tokens_per_step * world / (step_ms_max / 1e3)
+
+    # ---- roofline of the dominant kernel (the grouped MXFP4 gate/up GEMV)
+    peaks, peak_kind = measured_peaks()
+    kname = "gate/up"
+    kern_ms, kern_bytes = 0.0, 0.0
+    group_ms = {}
+    for T in batches:
+        for step_prof, n_act in zip(per_kernel[T], active_experts[T]):
+            for name, ms in step_prof:
+                group_ms.setdefault(name, []).append(ms)
+                if name == kname:
+                    kern_ms += ms
+                    kern_bytes += n_act * d.expert_gate_up_bytes() + T * d.top_k * (d.latent + d.inter) * 2
+    launches = sum(len(per_kernel[T]) for T in batches)
+    achieved = kern_bytes / (kern_ms / 1e3) / 1e9 if kern_ms > 0 else None
+    traffic = recorded_traffic("gateup_gemv_kernel", "k3-decode-T64")
+    roofline = {"bound": "hbm", "kernel": "gateup_gemv_kernel (grouped MXFP4 gate/up GEMV + SiTU-GLU)",
+                "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": (achieved / peaks["hbm_gbs"]) if achieved else None,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
+                "traffic": traffic,
+                "algorithmic_bytes_per_launch": kern_bytes / max(launches, 1)}
+    # whole-layer HBM figure: all algorithmic bytes / forward time, per batch
+    sweep = {}
+    for T in batches:
+        nact = statistics.mean(active_experts[T])
+        alg = nact * d.expert_bytes() + d.dense_bytes() + T * d.hidden * 4
+        fms = statistics.mean(fwd_ms[T])
+        sweep[f"T={T}"] = {"forward_ms": fms, "tokens_per_s": T / (fms / 1e3), "active_experts": nact,
+                           "algorithmic_GB": alg / 1e9, "layer_GB_per_s": alg / (fms / 1e3) / 1e9,
+                           "launches": launches_per_forward[T]}
+
+    # ---- e2e: through the public C-ABI call with HOST buffers (pinned), copies timed
+    e2e = run_e2e(layer, d, batches, args, rank, dev, stream)
+    e2e_value = reduce_sum_over_ranks(e2e["tokens_per_s_rank"], world, dev)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(d, w, args.cpu_sample)
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "mxfp4(e2m1+e8m0) weights, bf16 activations, f32 accumulate",
+        "data": "synthetic (seeded generator: x~N(0,1) bf16, uniform MXFP4 bytes, e8m0 scales 118..124)",
+        "config": {"workload": "K3 LatentMoE routed layer, decode batches T=1,8,64 per step (73 tokens)",
+                   "hidden": d.hidden, "latent": d.latent, "experts": d.n_experts, "top_k": d.top_k,
+                   "moe_intermediate": d.inter, "global_batch": tokens_per_step * world,
+                   "l2": "flushed (512 MB write) before every forward, outside the timed events",
+                   "timing": "CUDA events around each CUDA-graph replay of the C-ABI forward; mean per batch size",
+                   "parallelism": f"replica x{world}" if world > 1 else "single GPU"},
+        "roofline": roofline,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": e2e["h2d"],
+                "d2h_bytes_per_step": e2e["d2h"], "how": "k3moe_forward_host (pinned host x -> y, idx, w)"},
+        "gpu_launches": sum(launches_per_forward[T] for T in batches) * args.steps,
+        "decode_sweep": sweep,
+        "kernel_ms_mean": {k: statistics.mean(v) for k, v in group_ms.items()},
+        "wall_s_timed_region": t_wall,
+    }
+    if clk is not None:
+        out["clocks"] = clk
+    if cpu is not None:
+        out["cpu_baseline"] = cpu
+    layer.close()
+    return out
+
+
+def run_e2e(layer, d, batches, args, rank, dev, stream):
+    import torch
+    from mxfp4_routed_expert_k3_gb300 import k3moe, synth
+    k3moe.profile(layer.ctx, False)
+    xs = {T: torch.from_numpy(synth.token_rows(d, 9000 + 31 * rank + T, T).view(np.int16)).pin_memory()
+          for T in batches}
+    ys = {T: torch.empty((T, d.hidden), dtype=torch.int16).pin_memory() for T in batches}
+    ids = {T: torch.empty((T, d.top_k), dtype=torch.int32).pin_memory() for T in batches}
+    ws = {T: torch.empty((T, d.top_k), dtype=torch.float32).pin_memory() for T in batches}
+    for T in batches:
+        k3moe.forward_host(layer.ctx, xs[T], T, ys[T], ids[T], ws[T], stream=stream)
+    n = max(3, args.steps // 2)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        for T in batches:
+            k3moe.forward_host(layer.ctx, xs[T], T, ys[T], ids[T], ws[T], stream=stream)
+    dt = (time.perf_counter() - t0) / n
+    tok = sum(batches)
+    h2d = sum(T * d.hidden * 2 for T in batches)
+    d2h = sum(T * (d.hidden * 2 + d.top_k * 8) for T in batches)
+    return {"tokens_per_s_rank": tok / dt, "h2d": h2d, "d2h": d2h}
+
+
+# ============================================================================ oracle (CPU)
+def cpu_baseline(d, w, n_tokens: int) -> dict:
+    """The oracle, as it stands, on a bounded sample: n_tokens decode tokens
+    through the whole layer on the host cores."""
+    from mxfp4_routed_expert_k3_gb300 import synth
+    from oracle import oracle as ora
+    x = synth.token_rows(d, 7777, n_tokens)
+    ora.forward(d, w, x[:1])  # load + page in
+    t0 = time.perf_counter()
+    ora.forward(d, w, x)
+    dt = time.perf_counter() - t0
+    return {"value": n_tokens / dt, "unit": "tokens/s", "cores": ora.num_threads(), "kind": "oracle",
+            "sample": f"{n_tokens} decode tokens of the K3 layer (full layer per token, fp64 oracle), "
+                      f"{dt:.1f} s wall"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    from mxfp4_routed_expert_k3_gb300 import synth
+    from mxfp4_routed_expert_k3_gb300.dims import K3
+    from oracle import oracle as ora
+    d = K3
+    w = synth.layer_weights(d, seed=1)
+    per_step = args.ref_tokens_per_step
+    xs = [synth.token_rows(d, 5000 + i, per_step) for i in range(args.warmup + args.steps)]
+    for i in range(args.warmup):
+        ora.forward(d, w, xs[i])
+    times = []
+    for i in range(args.warmup, args.warmup + args.steps):
+        t0 = time.perf_counter()
+        ora.forward(d, w, xs[i])
+        times.append(time.perf_counter() - t0)
+    ms = statistics.mean(times) * 1e3
+    value = per_step / (ms / 1e3)
+    return {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (same generator and seed as the GPU arm)",
+        "impl": "reference",
+        "config": {"workload": "K3 LatentMoE routed layer, decode tokens (bounded sample per step)",
+                   "tokens_per_step": per_step, "hidden": d.hidden, "latent": d.latent,
+                   "experts": d.n_experts, "top_k": d.top_k, "moe_intermediate": d.inter},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": ora.num_threads(), "kind": "oracle",
+                         "sample": f"{per_step} decode tokens per step through the fp64 CPU oracle"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-sample", type=int, default=16, help="tokens in the oracle CPU baseline sample")
+    ap.add_argument("--ref-tokens-per-step", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local_rank = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend=backend)
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        out = run_ours(args, rank, world, local_rank)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -77,6 +77,9 @@ typedef struct {
   int norm_topk;   /* 1: topk_w = s / sum of the selected s; 0: topk_w = s */
   int max_tokens;  /* largest T a forward call may pass */
   int spin_timeout_ms; /* limit of any device-side wait; 0 selects 2000 ms */
+  int force_path;  /* 0: by token count (CUDA-core kernels below 128 tokens,
+                      tensor-core kernels from 128); 1: always the CUDA-core
+                      kernels; 2: always the tensor-core kernels */
 } k3moe_config;
 
 /* Host arrays in checkpoint layout, experts stacked along dim 0.  Row-major;
@@ -197,6 +200,19 @@ enum {
 
 /* Reads a counter or size of the context into *value. */
 int k3moe_query(const k3moe_ctx* ctx, int what, long long* value);
+
+/* Per-step timing.  With profiling enabled, every later forward records a
+ * CUDA event on its stream before its first launch and after each launch
+ * group (router+down_proj, top-k, permute, gate/up, down, combine+RMSNorm,
+ * up_proj; the tensor-core path's expert group also contains its tile-list
+ * and gather kernels).  k3moe_profile_read waits for the events of the last
+ * forward and writes the elapsed milliseconds of each group to ms[0..max)
+ * and the number of groups to *count; k3moe_profile_name gives the group's
+ * name (a static string, "" out of range).  The events are also recorded
+ * inside a captured CUDA graph, so replays can be read the same way. */
+int k3moe_profile(k3moe_ctx* ctx, int enable);
+int k3moe_profile_read(k3moe_ctx* ctx, float* ms, int max_entries, int* count);
+const char* k3moe_profile_name(const k3moe_ctx* ctx, int i);
 
 #ifdef __cplusplus
 }

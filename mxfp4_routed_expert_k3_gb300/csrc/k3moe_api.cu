@@ -46,6 +46,12 @@ struct k3moe_ctx {
   k3::UmmaPlan umma{};
   long long launches_last = 0;
   int path_last = 0;
+  // optional per-step timing: events around each launch group of a forward
+  static constexpr int kMaxProf = 16;
+  bool prof = false;
+  int prof_n = 0;
+  cudaEvent_t prof_ev[kMaxProf + 1] = {};
+  const char* prof_name[kMaxProf] = {};
   std::string err = "no error";
 };
 
@@ -92,6 +98,7 @@ int check_config(const k3moe_config* c) {
   if (!(c->rms_eps >= 0.f) || !(c->beta > 0.f) || !(c->beta_lin > 0.f))
     return fail(nullptr, K3MOE_EINVAL, "beta, beta_lin must be > 0 and rms_eps >= 0");
   if (c->spin_timeout_ms < 0) return fail(nullptr, K3MOE_EINVAL, "spin_timeout_ms must be >= 0");
+  if (c->force_path < 0 || c->force_path > 2) return fail(nullptr, K3MOE_EINVAL, "force_path must be 0, 1 or 2");
   return K3MOE_OK;
 }
 
@@ -174,9 +181,13 @@ int k3moe_create(const k3moe_config* cfg, int cuda_device, k3moe_ctx** out) {
   c->idx_stage = (int32_t*)take(parts[14]);
   c->w_stage = (float*)take(parts[15]);
   c->umma.ws = take(parts[16]);
+  c->umma.status = c->w.status;
+  c->umma.limit_ns = (uint64_t)c->cfg.spin_timeout_ms * 1000000ull;
   e = cudaMemset(c->ws, 0, total);
+  if (e == cudaSuccess) e = k3::prepare_decode_kernels(c->d);
+  if (e == cudaSuccess) e = k3::prepare_umma_kernels();
   if (e != cudaSuccess) {
-    fail(nullptr, K3MOE_ECUDA, "cudaMemset: %s", cudaGetErrorString(e));
+    fail(nullptr, K3MOE_ECUDA, "workspace / kernel setup: %s", cudaGetErrorString(e));
     cudaFree(c->ws);
     delete c;
     return K3MOE_ECUDA;
@@ -196,6 +207,8 @@ void k3moe_destroy(k3moe_ctx* c) {
   cudaFree(c->wu);
   cudaFree(c->gu_tiles);
   cudaFree(c->d_tiles);
+  for (cudaEvent_t ev : c->prof_ev)
+    if (ev) cudaEventDestroy(ev);
   delete c;
 }
 
@@ -284,14 +297,21 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
                         cudaStream_t s) {
   const k3::Dims& d = c->d;
   k3::Work& w = c->w;
-  const bool big = k3::umma_path_enabled(c->umma, d, T);
+  const bool big = c->cfg.force_path == 2 || (c->cfg.force_path == 0 && k3::umma_path_enabled(c->umma, d, T));
   c->path_last = big ? 1 : 0;
   long long n = 0;
   cudaError_t e;
-#define K3_LAUNCH(expr, count, what)        \
-  do {                                      \
-    if ((e = (expr)) != cudaSuccess) return cuda_fail(c, e, what); \
-    n += (count);                           \
+  c->prof_n = 0;
+  if (c->prof && (e = cudaEventRecord(c->prof_ev[0], s)) != cudaSuccess) return cuda_fail(c, e, "profile event");
+#define K3_LAUNCH(expr, count, what)                                                    \
+  do {                                                                                  \
+    if ((e = (expr)) != cudaSuccess) return cuda_fail(c, e, what);                      \
+    n += (count);                                                                       \
+    if (c->prof && c->prof_n < k3moe_ctx::kMaxProf) {                                   \
+      c->prof_name[c->prof_n] = what;                                                   \
+      if ((e = cudaEventRecord(c->prof_ev[++c->prof_n], s)) != cudaSuccess)            \
+        return cuda_fail(c, e, "profile event");                                        \
+    }                                                                                   \
   } while (0)
   if (big) {
     K3_LAUNCH(k3::umma_dense(c->umma, c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, d.E, w.logits, w.lat, s),
@@ -414,6 +434,31 @@ int k3moe_query(const k3moe_ctx* c, int what, long long* value) {
     case K3MOE_Q_DEVICE: *value = c->device; return K3MOE_OK;
     default: return fail(nullptr, K3MOE_EINVAL, "unknown query %d", what);
   }
+}
+
+int k3moe_profile(k3moe_ctx* c, int enable) {
+  if (!c) return fail(nullptr, K3MOE_EINVAL, "ctx is NULL");
+  K3_CUDA(c, cudaSetDevice(c->device), "cudaSetDevice");
+  if (enable && !c->prof_ev[0])
+    for (cudaEvent_t& ev : c->prof_ev) K3_CUDA(c, cudaEventCreate(&ev), "cudaEventCreate");
+  c->prof = enable != 0;
+  c->prof_n = 0;
+  return K3MOE_OK;
+}
+
+int k3moe_profile_read(k3moe_ctx* c, float* ms, int max_entries, int* count) {
+  if (!c || !count) return fail(c, K3MOE_EINVAL, "ctx or count is NULL");
+  *count = c->prof_n;
+  for (int i = 0; i < c->prof_n && i < max_entries && ms; ++i) {
+    K3_CUDA(c, cudaEventSynchronize(c->prof_ev[i + 1]), "cudaEventSynchronize");
+    K3_CUDA(c, cudaEventElapsedTime(&ms[i], c->prof_ev[i], c->prof_ev[i + 1]), "cudaEventElapsedTime");
+  }
+  return K3MOE_OK;
+}
+
+const char* k3moe_profile_name(const k3moe_ctx* c, int i) {
+  if (!c || i < 0 || i >= c->prof_n) return "";
+  return c->prof_name[i];
 }
 
 int k3moe_mxfp4_dequant(const uint8_t* packed, const uint8_t* scale, int rows, int cols, void* out, int kind,

@@ -466,7 +466,6 @@ cudaError_t launch_gateup_gemv(const uint8_t* gu_tiles, const uint16_t* lat, con
   const int grid = max_active * (d.I / kTileRows);
   if (grid <= 0) return cudaSuccess;
   const size_t sm = sizeof(float) * (size_t)TB * d.L;
-  cudaFuncSetAttribute(gateup_gemv_kernel<TB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   gateup_gemv_kernel<TB><<<grid, 256, sm, s>>>(gu_tiles, lat, active, offsets, perm, d.K, d.L, d.I, d.beta,
                                                d.beta_lin, h);
   return cudaGetLastError();
@@ -553,7 +552,6 @@ cudaError_t launch_down_gemv(const uint8_t* d_tiles, const uint16_t* h, const in
   const int grid = max_active * (d.L / kTileRows);
   if (grid <= 0) return cudaSuccess;
   const size_t sm = sizeof(float) * (size_t)TB * d.I;
-  cudaFuncSetAttribute(down_gemv_kernel<TB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   down_gemv_kernel<TB><<<grid, 256, sm, s>>>(d_tiles, h, active, offsets, d.L, d.I, o);
   return cudaGetLastError();
 }
@@ -593,6 +591,20 @@ __global__ void __launch_bounds__(256) combine_rmsnorm_kernel(const float* __res
   const float inv = 1.0f / sqrtf(tot / (float)L + eps);
   for (int l = threadIdx.x; l < L; l += blockDim.x)
     n[(size_t)t * L + l] = f32_to_bf16(cs[l] * inv * bf16_to_f32(gamma[l]));
+}
+
+// One-time kernel attributes (dynamic shared memory above 48 KB), set when a
+// context is created so that forward calls stay capturable.
+cudaError_t prepare_decode_kernels(const Dims& d) {
+  cudaError_t e = cudaFuncSetAttribute(gateup_gemv_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)(sizeof(float) * 4 * d.L));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(down_gemv_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(sizeof(float) * 4 * d.I));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(combine_rmsnorm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(sizeof(float) * d.L));
+  return e;
 }
 
 cudaError_t launch_combine_rmsnorm(const float* o, const int* slot, const float* topk_w, const uint16_t* gamma,

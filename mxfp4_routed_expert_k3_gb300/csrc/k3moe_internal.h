@@ -42,6 +42,7 @@ cudaError_t launch_gateup_gemv(const uint8_t* gu_tiles, const uint16_t* lat, con
                                uint16_t* h, cudaStream_t s);
 cudaError_t launch_down_gemv(const uint8_t* d_tiles, const uint16_t* h, const int* active, const int* offsets,
                              int max_active, const Dims& d, float* o, cudaStream_t s);
+cudaError_t prepare_decode_kernels(const Dims& d);
 cudaError_t launch_combine_rmsnorm(const float* o, const int* slot, const float* topk_w, const uint16_t* gamma,
                                    int T, const Dims& d, uint16_t* n, cudaStream_t s);
 cudaError_t launch_relayout(const uint8_t* packed, const uint8_t* scale, int n_mat, int rows, int cols,

@@ -1,19 +1,618 @@
-// k3moe_umma.cu -- tensor-core path (tcgen05 + TMEM + TMA).
+// k3moe_umma.cu -- tensor-core path: tcgen05 MMA with fp32 accumulators in
+// tensor memory, operands staged in shared memory by TMA.
+//
+// One kernel template serves three GEMMs, all written "weights x tokens":
+// D[m, n] = sum_k A[m, k] * B[n, k], A = a 128-row tile of a weight matrix
+// (M side of the MMA), B = up to 256 token rows (N side), K = the weight's
+// input dimension, both operands K-major, bf16, D fp32 [128 lanes x N].
+//   DENSE  : A is bf16 (router + down_proj fused, or up_proj), loaded by a
+//            2-D TMA with 128-byte swizzle.  Epilogue: fp32 logits for rows
+//            below `split`, bf16 for the rest, written transposed [n, m].
+//   GATEUP : A is MXFP4 (w1 and w3 tiles of one expert, adjacent in memory),
+//            copied by a 1-D bulk TMA, decoded exactly to bf16 in shared
+//            memory by a warpgroup, two accumulators (gate, up); epilogue
+//            SiTU-GLU -> h (bf16) per expert slot.
+//   DOWN   : A is MXFP4 (w2 tile), one accumulator; epilogue o (fp32).
+// For the grouped GEMMs the token rows of an expert are contiguous (slot
+// order) and a device-built tile list gives, per tile, the expert, the first
+// row and the row count.
+//
+// Warp roles (192 threads): warp 0 issues the TMA copies, warp 1 (one lane)
+// issues the MMAs, warps 2..5 (a full warpgroup, so that warp w reads TMEM
+// lanes 32*(w%4)..+31) decode MXFP4 tiles and then run the epilogue.
+// Every wait on an mbarrier is bounded: past the limit the kernel records a
+// status bit, raises a shared abort flag that releases the other roles,
+// waits (bounded) for its own copies in flight, frees TMEM and returns.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cstdio>
+
+#include "k3moe_device.cuh"
 #include "k3moe_umma.h"
 
 namespace k3 {
 
-UmmaPlan umma_plan(const Dims&, int) { return UmmaPlan{}; }
+constexpr int kBM = 128;        // weight rows per tile (MMA M)
+constexpr int kBK = 64;         // input columns per stage (one 128-byte swizzle row of bf16)
+constexpr int kBNMax = 192;     // token rows per tile (MMA N, multiple of 16)
+constexpr int kThreads = 192;
+
+enum Mode { DENSE = 0, GATEUP = 1, DOWN = 2 };
+
+template <int MODE>
+struct Cfg {
+  static constexpr int kNumA = (MODE == GATEUP) ? 2 : 1;
+  static constexpr int kABytes = kBM * kBK * 2;                 // 16 KB per A tile
+  static constexpr int kBBytes = kBNMax * kBK * 2;              // 24 KB
+  static constexpr int kStageBytesRaw = (MODE == DENSE) ? 0 : kNumA * kTileBytes;
+  static constexpr int kStaging = (kStageBytesRaw + 1023) / 1024 * 1024;
+  static constexpr int kStageBytes = kNumA * kABytes + kBBytes + kStaging;
+  static constexpr int kStages = (MODE == GATEUP) ? 3 : 4;
+  static constexpr int kTmemCols = (MODE == GATEUP) ? 512 : 256;
+  static constexpr int kSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+struct Guard {
+  volatile int* abort;   // shared flag
+  unsigned* status;      // device status word
+  uint64_t limit_ns;
+};
+
+// Bounded wait; false if the wait gave up (or another role already did).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Guard& g, unsigned code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      if (*g.abort) return false;
+      if (global_ns() - t0 > g.limit_ns) {
+        *g.abort = 1;
+        atomicOr(g.status, code);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols));
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// UMMA shared-memory descriptor, K-major, 128-byte swizzle: rows of 128 bytes,
+// 8-row groups 1024 bytes apart (stride byte offset), leading offset unused.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1u << 16;                 // leading byte offset (unused for this layout)
+  d |= (uint64_t)(1024u >> 4) << 32;       // stride byte offset
+  d |= (uint64_t)1u << 46;                 // descriptor version
+  d |= (uint64_t)2u << 61;                 // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor: kind::f16, A = B = bf16, D = fp32, both K-major.
+__device__ __forceinline__ uint32_t umma_idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// SiTU-GLU in fp32 from the identities tanh(x/2) = (1 - e^-x)/(1 + e^-x)
+// and sigmoid(g) = 1/(1 + e^-g), one exponential per branch, written for
+// either sign without overflow:
+//   t = e^(-|g|/2):  g >= 0: beta tanh(g/beta) sigma(g) = 4 (1-t) / ((1+t)(1+t^2))   (beta = 4)
+//                    g <  0:                            = -4 (1-t) t^2 / ((1+t)(1+t^2))
+// The general-beta form uses t1 = e^(-2|g|/beta) for the tanh and e^(-|g|)
+// for the sigmoid.
+__device__ __forceinline__ float situ_fast(float g, float u, float beta, float beta_lin) {
+  const float ag = fabsf(g);
+  const float a = __expf(-2.0f * ag / beta);  // tanh(|g|/beta) = (1-a)/(1+a)
+  const float b = __expf(-ag);                 // sigmoid(|g|) = 1/(1+b), sigmoid(-|g|) = b/(1+b)
+  const float th = __fdividef(1.0f - a, 1.0f + a);
+  const float sg = g >= 0.f ? __fdividef(1.0f, 1.0f + b) : __fdividef(b, 1.0f + b);
+  const float gate = beta * copysignf(th, g) * sg;
+  const float au = fabsf(u);
+  const float c = __expf(-2.0f * au / beta_lin);
+  const float tu = copysignf(__fdividef(1.0f - c, 1.0f + c), u);
+  return gate * beta_lin * tu;
+}
+
+// Per-tile description for grouped GEMMs: x = expert, y = first row (slot),
+// z = valid rows, w = MMA N (rows rounded up to 16).
+struct TileList {
+  const int4* tiles;
+  const int* count;
+};
+
+struct Params {
+  // operand sources
+  const uint8_t* a_tiles;  // MXFP4 tiles (GATEUP / DOWN)
+  int MT;                  // weight row tiles per matrix
+  int KS;                  // K / 64
+  int M;                   // weight rows (DENSE edge masking)
+  // token tiling
+  TileList list;           // GATEUP / DOWN
+  int T, tn;               // DENSE: tokens and rows per tile
+  // epilogue
+  int split;               // DENSE: rows below -> fp32 out_f32, others -> bf16 out_bf16
+  float* out_f32;
+  uint16_t* out_bf16;
+  int ld_out;              // GATEUP: I, DOWN: L (row length of h / o)
+  float beta, beta_lin;
+  unsigned* status;
+  uint64_t limit_ns;
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
+                                                                const __grid_constant__ CUtensorMap map_b,
+                                                                const Params p) {
+  using C = Cfg<MODE>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  // bars: [0, S) full_tma, [S, 2S) full_a, [2S, 3S) empty, [3S] tmem_full
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * C::kStages + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = blockIdx.x;
+
+  // ---- which token tile
+  int e = 0, row0 = 0, rows = 0, n_mma = 0;
+  if (MODE == DENSE) {
+    row0 = blockIdx.y * p.tn;
+    rows = min(p.tn, p.T - row0);
+    n_mma = (rows + 15) & ~15;
+  } else {
+    if ((int)blockIdx.y >= *p.list.count) return;
+    const int4 t = p.list.tiles[blockIdx.y];
+    e = t.x;
+    row0 = t.y;
+    rows = t.z;
+    n_mma = t.w;
+  }
+  if (rows <= 0) return;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 3 * C::kStages + 1; ++s)
+      mbar_init(smem_u32(bars + s), (s >= C::kStages && s < 2 * C::kStages) ? 128u : 1u);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Guard g{abort_flag, p.status, p.limit_ns};
+  auto full_tma = [&](int s) { return smem_u32(bars + s); };
+  auto full_a = [&](int s) { return smem_u32(bars + C::kStages + s); };
+  auto empty = [&](int s) { return smem_u32(bars + 2 * C::kStages + s); };
+  const uint32_t tmem_full = smem_u32(bars + 3 * C::kStages);
+  auto stage_a = [&](int s, int i) { return smem + (size_t)s * C::kStageBytes + i * C::kABytes; };
+  auto stage_b = [&](int s) { return smem + (size_t)s * C::kStageBytes + C::kNumA * C::kABytes; };
+  auto stage_stg = [&](int s) { return smem + (size_t)s * C::kStageBytes + C::kNumA * C::kABytes + C::kBBytes; };
+
+  if (warp == 0) {
+    // ================= TMA producer
+    int issued = 0;
+    if (lane == 0) {
+      const uint32_t tx = C::kBBytes + (MODE == DENSE ? C::kABytes : C::kNumA * kTileBytes);
+      const uint8_t* a_src = (MODE == DENSE) ? nullptr
+                                             : p.a_tiles + ((size_t)(e * p.MT + mt) * p.KS) * C::kNumA * kTileBytes;
+      for (int ks = 0; ks < p.KS; ++ks) {
+        const int s = ks % C::kStages, u = ks / C::kStages;
+        if (u > 0 && !mbar_wait(empty(s), (u - 1) & 1, g, 1u)) break;
+        mbar_expect_tx(full_tma(s), tx);
+        tma_load_2d(smem_u32(stage_b(s)), &map_b, full_tma(s), ks * kBK, row0);
+        if (MODE == DENSE)
+          tma_load_2d(smem_u32(stage_a(s, 0)), &map_a, full_tma(s), ks * kBK, mt * kBM);
+        else
+          bulk_load(smem_u32(stage_stg(s)), a_src + (size_t)ks * C::kNumA * kTileBytes, C::kNumA * kTileBytes,
+                    full_tma(s));
+        ++issued;
+      }
+      if (*abort_flag) {
+        // let our own copies land before the CTA's shared memory goes away
+        for (int ks = max(0, issued - C::kStages); ks < issued; ++ks) {
+          const uint64_t t0 = global_ns();
+          while (!mbar_try_wait(full_tma(ks % C::kStages), (ks / C::kStages) & 1))
+            if (global_ns() - t0 > p.limit_ns) break;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================= MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = umma_idesc_bf16(kBM, n_mma);
+      bool ok = true;
+      for (int ks = 0; ks < p.KS && ok; ++ks) {
+        const int s = ks % C::kStages, par = (ks / C::kStages) & 1;
+        ok = mbar_wait(full_tma(s), par, g, 2u);
+        if (ok && MODE != DENSE) ok = mbar_wait(full_a(s), par, g, 4u);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t b0 = smem_u32(stage_b(s));
+#pragma unroll
+        for (int i = 0; i < C::kNumA; ++i) {
+          const uint32_t a0 = smem_u32(stage_a(s, i));
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_bf16(tmem + i * 256, umma_desc_sw128(a0 + kk * 32), umma_desc_sw128(b0 + kk * 32), idesc,
+                      (ks | kk) ? 1u : 0u);
+        }
+        umma_commit(empty(s));
+      }
+      umma_commit(tmem_full);
+      if (!ok) {
+        // the MMAs already issued must finish before TMEM is released
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(tmem_full, 0))
+          if (global_ns() - t0 > p.limit_ns) break;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ================= decode (MXFP4) + epilogue warpgroup
+    const int wg_t = threadIdx.x - 64;  // 0..127
+    if (MODE != DENSE) {
+      const int r = wg_t;  // row of the 128-row tile this thread decodes
+      for (int ks = 0; ks < p.KS; ++ks) {
+        const int s = ks % C::kStages, par = (ks / C::kStages) & 1;
+        if (!mbar_wait(full_tma(s), par, g, 8u)) break;
+        const uint8_t* stg = stage_stg(s);
+#pragma unroll
+        for (int i = 0; i < C::kNumA; ++i) {
+          const uint8_t* tile = stg + i * kTileBytes;
+          const uint4 c0 = *reinterpret_cast<const uint4*>(tile + (size_t)r * 16);
+          const uint4 c1 = *reinterpret_cast<const uint4*>(tile + (size_t)(128 + r) * 16);
+          const uint32_t sc = *reinterpret_cast<const uint16_t*>(tile + kTilePackedBytes + 2 * r);
+          const ScaleMul m0 = scale_multipliers(sc & 0xFFu), m1 = scale_multipliers(sc >> 8);
+          uint8_t* arow = stage_a(s, i) + (size_t)r * 128;
+          const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            uint32_t o[4];
+            tile_word_to_bf16(words[q], q < 4 ? m0 : m1, o);
+            *reinterpret_cast<uint4*>(arow + ((q ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(full_a(s));
+      }
+    }
+    // ---- epilogue
+    if (mbar_wait(tmem_full, 0, g, 16u) && !*abort_flag) {
+      tc_fence_after();
+      const int quarter = warp & 3;
+      const int m_local = quarter * 32 + lane;
+      const int m = mt * kBM + m_local;
+      const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+      for (int j0 = 0; j0 < n_mma; j0 += 32) {
+        float acc[32];
+        tmem_ld32(lane_addr + j0, acc);
+        if (MODE == GATEUP) {
+          float up[32];
+          tmem_ld32(lane_addr + 256 + j0, up);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j0 + j < rows)
+              p.out_bf16[(size_t)(row0 + j0 + j) * p.ld_out + m] =
+                  f32_to_bf16(situ_fast(acc[j], up[j], p.beta, p.beta_lin));
+        } else if (MODE == DOWN) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j0 + j < rows) p.out_f32[(size_t)(row0 + j0 + j) * p.ld_out + m] = acc[j];
+        } else {
+          if (m < p.M) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (j0 + j < rows) {
+                const size_t t = (size_t)(row0 + j0 + j);
+                if (m < p.split)
+                  p.out_f32[t * p.split + m] = acc[j];
+                else
+                  p.out_bf16[t * (p.M - p.split) + (m - p.split)] = f32_to_bf16(acc[j]);
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// ------------------------------------------------------------------ helpers
+// Gather the latent rows into slot order: lat_perm[s] = lat[perm[s] / K].
+__global__ void gather_rows_kernel(const uint16_t* __restrict__ lat, const int* __restrict__ perm, int TK, int K,
+                                   int L, uint16_t* __restrict__ out) {
+  const int vec = L / 8;
+  const long long total = (long long)TK * vec;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int s = (int)(i / vec), v = (int)(i - (long long)s * vec);
+    const int t = perm[s] / K;
+    reinterpret_cast<uint4*>(out)[(size_t)s * vec + v] = reinterpret_cast<const uint4*>(lat)[(size_t)t * vec + v];
+  }
+}
+
+// Tiles of at most kBNMax rows per active expert, rows split evenly and
+// rounded up to 16: tiles[i] = {expert, first slot, rows, MMA N}.
+__global__ void __launch_bounds__(1024) build_tiles_kernel(const int* __restrict__ active,
+                                                           const int* __restrict__ offsets, int4* __restrict__ tiles,
+                                                           int* __restrict__ count) {
+  __shared__ int warp_tot[32];
+  __shared__ int carry;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n_act = active[0];
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int a0 = 0; a0 < n_act; a0 += 1024) {
+    const int a = a0 + threadIdx.x;
+    int e = 0, c = 0, nsub = 0;
+    if (a < n_act) {
+      e = active[1 + a];
+      c = offsets[e + 1] - offsets[e];
+      nsub = (c + kBNMax - 1) / kBNMax;
+    }
+    // exclusive scan of nsub over the block
+    int incl = nsub;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int wv = warp_tot[lane];
+      int wi = wv;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+        if (lane >= o) wi += v;
+      }
+      warp_tot[lane] = wi - wv;
+    }
+    __syncthreads();
+    const int base = carry + warp_tot[warp] + incl - nsub;
+    if (a < n_act && nsub > 0) {
+      const int per = (c + nsub - 1) / nsub;
+      const int tn = (per + 15) & ~15;
+      for (int j = 0; j < nsub; ++j) {
+        const int r0 = j * tn;
+        const int rows = min(tn, c - r0);
+        tiles[base + j] = make_int4(e, offsets[e] + r0, rows, (rows + 15) & ~15);
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 1023) carry = base + nsub;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *count = carry;
+}
+
+// ------------------------------------------------------------------ host side
+namespace {
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D bf16 map of a row-major [rows, cols] matrix, box [box_rows, 64], 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, int rows, int cols, int box_rows) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct UmmaWs {
+  int4* tiles;
+  int* count;
+  uint16_t* lat_perm;
+};
+
+UmmaWs ws_view(const UmmaPlan& p, const Dims& d, int max_tokens) {
+  const size_t max_tiles = (size_t)max_tokens * d.K / kBNMax + d.E + 1;
+  uint8_t* b = static_cast<uint8_t*>(p.ws);
+  UmmaWs w;
+  w.tiles = reinterpret_cast<int4*>(b);
+  w.count = reinterpret_cast<int*>(b + max_tiles * sizeof(int4));
+  w.lat_perm = reinterpret_cast<uint16_t*>(b + ((max_tiles * sizeof(int4) + 16 + 255) / 256) * 256);
+  return w;
+}
+
+template <int MODE>
+cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const Params& prm, dim3 grid, cudaStream_t s) {
+  constexpr int smem = Cfg<MODE>::kSmem;
+  static_assert(smem <= 232448, "shared memory budget");
+  umma_gemm_kernel<MODE><<<grid, kThreads, smem, s>>>(ma, mb, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t prepare_umma_kernels() {
+  cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg<DENSE>::kSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(umma_gemm_kernel<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<GATEUP>::kSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(umma_gemm_kernel<DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<DOWN>::kSmem);
+  return e;
+}
+
+UmmaPlan umma_plan(const Dims& d, int max_tokens) {
+  UmmaPlan p;
+  p.max_tokens = max_tokens;
+  const size_t max_tiles = (size_t)max_tokens * d.K / kBNMax + d.E + 1;
+  p.ws_bytes = ((max_tiles * sizeof(int4) + 16 + 255) / 256) * 256 + (size_t)max_tokens * d.K * d.L * 2;
+  p.enabled = true;
+  p.min_tokens = 128;
+  return p;
+}
+
 bool umma_path_enabled(const UmmaPlan& p, const Dims&, int T) { return p.enabled && T >= p.min_tokens; }
-cudaError_t umma_dense(const UmmaPlan&, const uint16_t*, int, int, const uint16_t*, int, int, float*, uint16_t*,
-                       cudaStream_t) {
-  return cudaErrorNotSupported;
-}
+
 int umma_dense_launches() { return 1; }
-cudaError_t umma_experts(const UmmaPlan&, const uint8_t*, const uint8_t*, const Work&, int, const Dims&,
-                         cudaStream_t) {
-  return cudaErrorNotSupported;
+int umma_expert_launches() { return 4; }
+
+cudaError_t umma_dense(const UmmaPlan& p, const uint16_t* W, int M, int K, const uint16_t* X, int T, int split,
+                       float* out_f32, uint16_t* out_bf16, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, W, M, K, kBM) || !make_map(&mb, X, T, K, kBNMax)) return cudaErrorInvalidValue;
+  const int ntile = (T + kBNMax - 1) / kBNMax;
+  const int per = (T + ntile - 1) / ntile;
+  Params prm{};
+  prm.MT = (M + kBM - 1) / kBM;
+  prm.KS = K / kBK;
+  prm.M = M;
+  prm.T = T;
+  prm.tn = (per + 15) & ~15;
+  prm.split = split;
+  prm.out_f32 = out_f32;
+  prm.out_bf16 = out_bf16;
+  prm.status = p.status;
+  prm.limit_ns = p.limit_ns;
+  const int ny = (T + prm.tn - 1) / prm.tn;
+  return launch_gemm<DENSE>(ma, mb, prm, dim3(prm.MT, ny), s);
 }
-int umma_expert_launches() { return 2; }
+
+cudaError_t umma_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8_t* d_tiles, const Work& w, int T,
+                         const Dims& d, cudaStream_t s) {
+  const int TK = T * d.K;
+  if (TK <= 0) return cudaSuccess;
+  UmmaWs ws = ws_view(p, d, p.max_tokens);
+  const int max_tiles = TK / kBNMax + std::min(d.E, TK) + 1;
+  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, ws.tiles, ws.count);
+  gather_rows_kernel<<<152 * 8, 256, 0, s>>>(w.lat, w.perm, TK, d.K, d.L, ws.lat_perm);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap mb1, mb2;
+  if (!make_map(&mb1, ws.lat_perm, TK, d.L, kBNMax) || !make_map(&mb2, w.h, TK, d.I, kBNMax))
+    return cudaErrorInvalidValue;
+  Params g{};
+  g.a_tiles = gu_tiles;
+  g.MT = d.I / kBM;
+  g.KS = d.L / kBK;
+  g.M = d.I;
+  g.list = TileList{ws.tiles, ws.count};
+  g.out_bf16 = w.h;
+  g.ld_out = d.I;
+  g.beta = d.beta;
+  g.beta_lin = d.beta_lin;
+  g.status = p.status;
+  g.limit_ns = p.limit_ns;
+  e = launch_gemm<GATEUP>(mb1, mb1, g, dim3(g.MT, max_tiles), s);
+  if (e != cudaSuccess) return e;
+  Params dn = g;
+  dn.a_tiles = d_tiles;
+  dn.MT = d.L / kBM;
+  dn.KS = d.I / kBK;
+  dn.M = d.L;
+  dn.out_bf16 = nullptr;
+  dn.out_f32 = w.o;
+  dn.ld_out = d.L;
+  return launch_gemm<DOWN>(mb2, mb2, dn, dim3(dn.MT, max_tiles), s);
+}
 
 }  // namespace k3

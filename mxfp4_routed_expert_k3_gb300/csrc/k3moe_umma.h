@@ -13,10 +13,14 @@ namespace k3 {
 struct UmmaPlan {
   bool enabled = false;   // false: every forward uses the CUDA-core kernels
   int min_tokens = 1 << 30;
-  size_t ws_bytes = 256;  // workspace this path needs (tile lists, B copies)
+  int max_tokens = 0;
+  size_t ws_bytes = 256;  // workspace this path needs (tile list, slot-ordered latent rows)
   void* ws = nullptr;
+  unsigned* status = nullptr;  // device status word (bounded waits report here)
+  uint64_t limit_ns = 2000000000ull;
 };
 
+cudaError_t prepare_umma_kernels();
 UmmaPlan umma_plan(const Dims& d, int max_tokens);
 bool umma_path_enabled(const UmmaPlan& p, const Dims& d, int T);
 cudaError_t umma_dense(const UmmaPlan& p, const uint16_t* W, int M, int K, const uint16_t* X, int T, int split,

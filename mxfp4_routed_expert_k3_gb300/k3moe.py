@@ -20,7 +20,7 @@ BUF = dict(logits=0, lat=1, counts=2, offsets=3, perm=4, slot=5, h=6, o=7, n=8, 
 Q = dict(workspace_bytes=0, weight_bytes=1, launches_last=2, path_last=3, device=4)
 EXPORTS = ["k3moe_create", "k3moe_load_weights", "k3moe_forward", "k3moe_forward_host", "k3moe_status",
            "k3moe_last_error", "k3moe_destroy", "k3moe_mxfp4_dequant", "k3moe_route", "k3moe_fetch",
-           "k3moe_query"]
+           "k3moe_query", "k3moe_profile", "k3moe_profile_read", "k3moe_profile_name"]
 
 
 class K3Error(RuntimeError):
@@ -33,7 +33,7 @@ class Config(C.Structure):
     _fields_ = [("hidden", C.c_int), ("latent", C.c_int), ("n_experts", C.c_int), ("top_k", C.c_int),
                 ("inter", C.c_int), ("group", C.c_int), ("beta", C.c_float), ("beta_lin", C.c_float),
                 ("rms_eps", C.c_float), ("routed_scaling", C.c_float), ("norm_topk", C.c_int),
-                ("max_tokens", C.c_int), ("spin_timeout_ms", C.c_int)]
+                ("max_tokens", C.c_int), ("spin_timeout_ms", C.c_int), ("force_path", C.c_int)]
 
 
 class Weights(C.Structure):
@@ -65,11 +65,13 @@ def lib():
         L.k3moe_route.argtypes = [vp, i32, vp, vp, i32, i32, i32, i32, C.c_float, vp, vp, vp, vp]
         L.k3moe_fetch.argtypes = [vp, i32, vp, C.c_size_t]
         L.k3moe_query.argtypes = [vp, i32, C.POINTER(C.c_longlong)]
-        for f in EXPORTS:
-            if getattr(L, f).restype is None and f not in ("k3moe_destroy",):
-                pass
+        L.k3moe_profile.argtypes = [vp, i32]
+        L.k3moe_profile_read.argtypes = [vp, C.POINTER(C.c_float), i32, C.POINTER(C.c_int)]
+        L.k3moe_profile_name.argtypes = [vp, i32]
+        L.k3moe_profile_name.restype = C.c_char_p
         for f in ("k3moe_create", "k3moe_load_weights", "k3moe_forward", "k3moe_forward_host", "k3moe_status",
-                  "k3moe_mxfp4_dequant", "k3moe_route", "k3moe_fetch", "k3moe_query"):
+                  "k3moe_mxfp4_dequant", "k3moe_route", "k3moe_fetch", "k3moe_query", "k3moe_profile",
+                  "k3moe_profile_read"):
             getattr(L, f).restype = C.c_int
         _lib = L
     return _lib
@@ -102,9 +104,12 @@ def _check(rc: int, ctx=None):
         raise K3Error(rc, last_error(ctx))
 
 
-def make_config(d: LayerDims, max_tokens: int, spin_timeout_ms: int = 0) -> Config:
+PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE = 0, 1, 2
+
+
+def make_config(d: LayerDims, max_tokens: int, spin_timeout_ms: int = 0, force_path: int = 0) -> Config:
     return Config(d.hidden, d.latent, d.n_experts, d.top_k, d.inter, d.group, d.beta, d.beta_lin, d.rms_eps,
-                  d.routed_scaling, int(d.norm_topk), int(max_tokens), int(spin_timeout_ms))
+                  d.routed_scaling, int(d.norm_topk), int(max_tokens), int(spin_timeout_ms), int(force_path))
 
 
 # ------------------------------------------------------------------ raw calls
@@ -162,14 +167,27 @@ def query(ctx, what: str) -> int:
     return int(v.value)
 
 
+def profile(ctx, enable: bool = True):
+    _check(lib().k3moe_profile(ctx, int(enable)), ctx)
+
+
+def profile_read(ctx) -> list:
+    """[(group name, milliseconds)] of the last forward."""
+    buf = (C.c_float * 16)()
+    n = C.c_int()
+    _check(lib().k3moe_profile_read(ctx, buf, 16, C.byref(n)), ctx)
+    return [(lib().k3moe_profile_name(ctx, i).decode(), float(buf[i])) for i in range(min(n.value, 16))]
+
+
 # ------------------------------------------------------------------ convenience
 class Layer:
     """One context: create + load_weights on construction, destroy on close."""
 
-    def __init__(self, d: LayerDims, weights: dict, max_tokens: int, device: int = 0, spin_timeout_ms: int = 0):
+    def __init__(self, d: LayerDims, weights: dict, max_tokens: int, device: int = 0, spin_timeout_ms: int = 0,
+                 force_path: int = PATH_AUTO):
         self.d = d
         self.max_tokens = max_tokens
-        self.ctx = create(make_config(d, max_tokens, spin_timeout_ms), device)
+        self.ctx = create(make_config(d, max_tokens, spin_timeout_ms, force_path), device)
         try:
             load_weights(self.ctx, weights)
         except Exception:

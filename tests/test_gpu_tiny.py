@@ -14,14 +14,15 @@ from _cases import (assert_routing_equal, assert_y_close, bf16_f64, gapped_token
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-MAXT = 96
+MAXT = 320
 
 
-@pytest.fixture(scope="module")
-def tiny():
+@pytest.fixture(scope="module", params=[k3moe.PATH_AUTO, k3moe.PATH_CUDA_CORE, k3moe.PATH_TENSOR_CORE],
+                ids=["auto", "cudacore", "tensorcore"])
+def tiny(request):
     d = TINY
     w = synth.layer_weights(d, seed=0)
-    layer = k3moe.Layer(d, w, max_tokens=MAXT)
+    layer = k3moe.Layer(d, w, max_tokens=MAXT, force_path=request.param)
     yield d, w, layer
     layer.close()
 
@@ -39,7 +40,7 @@ def run(layer, x_np):
     return y.cpu().numpy().view(np.uint16), idx.cpu().numpy(), w.cpu().numpy()
 
 
-@pytest.mark.parametrize("T", [1, 3, 32, 77, MAXT])
+@pytest.mark.parametrize("T", [1, 3, 32, 77, 128, 200, MAXT])
 def test_tiny_layer_matches_oracle(tiny, T):
     d, w, layer = tiny
     x = gapped_tokens(d, w, seed=100 + T, T=T)
