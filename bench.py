@@ -155,7 +155,7 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    d = K3
+    d = K3 if args.experts == K3.n_experts else K3.with_(n_experts=args.experts)
     batches = DECODE_BATCHES
     maxT = max(batches)
     w = synth.layer_weights(d, seed=1)
@@ -274,7 +274,8 @@ def run_ours(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": step_ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "mxfp4(e2m1+e8m0) weights, bf16 activations, f32 accumulate",
         "data": "synthetic (seeded generator: x~N(0,1) bf16, uniform MXFP4 bytes, e8m0 scales 118..124)",
-        "config": {"workload": "K3 LatentMoE routed layer, decode batches T=1,8,64 per step (73 tokens)",
+        "config": {"workload": "K3 LatentMoE routed layer, decode batches T=1,8,64 per step (73 tokens)"
+                   + ("" if d.n_experts == K3.n_experts else f" [reduced to {d.n_experts} experts: profiling case]"),
                    "hidden": d.hidden, "latent": d.latent, "experts": d.n_experts, "top_k": d.top_k,
                    "moe_intermediate": d.inter, "global_batch": tokens_per_step * world,
                    "l2": "flushed (512 MB write) before every forward, outside the timed events",
@@ -378,6 +379,8 @@ def main():
     ap.add_argument("--cpu-sample", type=int, default=16, help="tokens in the oracle CPU baseline sample")
     ap.add_argument("--ref-tokens-per-step", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--experts", type=int, default=896,
+                    help="experts of the K3-dim layer (default 896; fewer only for small profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

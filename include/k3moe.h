@@ -79,7 +79,9 @@ typedef struct {
   int spin_timeout_ms; /* limit of any device-side wait; 0 selects 2000 ms */
   int force_path;  /* 0: by token count (CUDA-core kernels below 128 tokens,
                       tensor-core kernels from 128); 1: always the CUDA-core
-                      kernels; 2: always the tensor-core kernels */
+                      kernels; 2: always the tensor-core GEMM kernels;
+                      3: CUDA-core dense GEMVs with the streaming
+                      tensor-core expert kernels (decode-size batches) */
 } k3moe_config;
 
 /* Host arrays in checkpoint layout, experts stacked along dim 0.  Row-major;
@@ -194,7 +196,7 @@ enum {
   K3MOE_Q_WORKSPACE_BYTES = 0, /* device workspace bytes                       */
   K3MOE_Q_WEIGHT_BYTES = 1,    /* device weight bytes                          */
   K3MOE_Q_LAUNCHES_LAST = 2,   /* kernels launched by the last forward          */
-  K3MOE_Q_PATH_LAST = 3,       /* 0: decode kernels, 1: tensor-core kernels     */
+  K3MOE_Q_PATH_LAST = 3,       /* path of the last forward (force_path values 1..3) */
   K3MOE_Q_DEVICE = 4           /* CUDA device ordinal                          */
 };
 

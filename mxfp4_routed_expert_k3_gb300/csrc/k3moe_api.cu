@@ -98,7 +98,7 @@ int check_config(const k3moe_config* c) {
   if (!(c->rms_eps >= 0.f) || !(c->beta > 0.f) || !(c->beta_lin > 0.f))
     return fail(nullptr, K3MOE_EINVAL, "beta, beta_lin must be > 0 and rms_eps >= 0");
   if (c->spin_timeout_ms < 0) return fail(nullptr, K3MOE_EINVAL, "spin_timeout_ms must be >= 0");
-  if (c->force_path < 0 || c->force_path > 2) return fail(nullptr, K3MOE_EINVAL, "force_path must be 0, 1 or 2");
+  if (c->force_path < 0 || c->force_path > 3) return fail(nullptr, K3MOE_EINVAL, "force_path must be 0..3");
   return K3MOE_OK;
 }
 
@@ -182,6 +182,7 @@ int k3moe_create(const k3moe_config* cfg, int cuda_device, k3moe_ctx** out) {
   c->w_stage = (float*)take(parts[15]);
   c->umma.ws = take(parts[16]);
   c->umma.status = c->w.status;
+  c->umma.num_sms = prop.multiProcessorCount;
   c->umma.limit_ns = (uint64_t)c->cfg.spin_timeout_ms * 1000000ull;
   e = cudaMemset(c->ws, 0, total);
   if (e == cudaSuccess) e = k3::prepare_decode_kernels(c->d);
@@ -297,8 +298,11 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
                         cudaStream_t s) {
   const k3::Dims& d = c->d;
   k3::Work& w = c->w;
-  const bool big = c->cfg.force_path == 2 || (c->cfg.force_path == 0 && k3::umma_path_enabled(c->umma, d, T));
-  c->path_last = big ? 1 : 0;
+  // path: 1 CUDA-core kernels, 2 tensor-core GEMMs, 3 CUDA-core dense GEMVs + streaming tensor-core experts
+  int path = c->cfg.force_path;
+  if (path == 0) path = k3::umma_path_enabled(c->umma, d, T) ? 2 : 1;
+  const bool big = path == 2;
+  c->path_last = path;
   long long n = 0;
   cudaError_t e;
   c->prof_n = 0;
@@ -327,6 +331,9 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
   if (big) {
     K3_LAUNCH(k3::umma_experts(c->umma, c->gu_tiles, c->d_tiles, w, T, d, s), k3::umma_expert_launches(),
               "experts (tensor cores)");
+  } else if (path == 3) {
+    K3_LAUNCH(k3::umma_stream_experts(c->umma, c->gu_tiles, c->d_tiles, w, T, d, s), k3::umma_stream_launches(),
+              "experts (streaming tensor cores)");
   } else {
     K3_LAUNCH(k3::launch_gateup_gemv(c->gu_tiles, w.lat, w.active, w.offsets, w.perm, max_active, d, w.h, s), 1,
               "gate/up");

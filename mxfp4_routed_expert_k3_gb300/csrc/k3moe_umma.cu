@@ -400,6 +400,231 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
   if (warp == 0) tmem_dealloc(tmem, C::kTmemCols);
 }
 
+// =====================================================================
+// Streaming expert kernel for small token counts per expert (decode).
+// Persistent: each CTA walks the work items (tile, 128-row block) with
+// stride gridDim.x; the TMA ring runs across item boundaries, so every SM
+// keeps ~(kSStages-1) stages of weight bytes in flight.  The decoded bf16
+// weights go to TENSOR MEMORY (tcgen05.st) and the MMA reads A from there
+// (tcgen05.mma ... [d], [a_tmem], b_desc): the 4x-expanded weights never
+// touch shared memory, and the decode costs the same per weight whatever
+// the number of tokens (N = 16 or 32).  Tokens: up to kSNB rows of the
+// slot-ordered activation matrix per tile, one 2-D TMA box per stage.
+// TMEM (256 columns per CTA, two CTAs per SM):
+//   GATEUP: D gate [0, 32), D up [32, 64), A slots at 64 + 64 t (t < 3;
+//           gate half then up half, 32 columns each)
+//   DOWN  : D [0, 32), A slots at 32 + 32 t (t < 4)
+// A in TMEM for kind::f16, M = 128: row m in lane m, two consecutive bf16
+// (k even in the low half) per 32-bit column, 8 columns per K = 16.
+// =====================================================================
+constexpr int kSNB = 32;  // max token rows per streaming tile
+constexpr int kSThreads = 192;
+
+template <int MODE>
+struct SCfg {
+  static constexpr int kNumA = (MODE == GATEUP) ? 2 : 1;
+  static constexpr int kBBytes = kSNB * kBK * 2;  // 4 KB, 1024-aligned
+  static constexpr int kStg = (kNumA * kTileBytes + 1023) / 1024 * 1024;
+  static constexpr int kStageBytes = kBBytes + kStg;
+  static constexpr int kStages = (MODE == GATEUP) ? 7 : 9;
+  static constexpr int kSlots = (MODE == GATEUP) ? 3 : 4;
+  static constexpr int kSlotCols = kNumA * 32;
+  static constexpr int kDCols = kNumA * kSNB;
+  // padded so that at most two CTAs fit on an SM (two x 256 TMEM columns)
+  static constexpr int kSmem = 94 * 1024;
+  static_assert(kStages * kStageBytes + 1024 + 512 <= kSmem, "ring does not fit");
+  static_assert(kDCols + kSlots * kSlotCols <= 256, "TMEM budget");
+};
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t v[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                 uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kSThreads, 1) umma_stream_kernel(const __grid_constant__ CUtensorMap map_b,
+                                                                   const Params p) {
+  using C = SCfg<MODE>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  // bars: full[S], free[S], a_ready[NS], a_free[NS], tmem_full
+  const int NB = 2 * C::kStages + 2 * C::kSlots + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NB);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int n_items = *p.list.count * p.MT;
+  if ((int)blockIdx.x >= n_items) return;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NB; ++i) {
+      const bool is_ready = i >= 2 * C::kStages && i < 2 * C::kStages + C::kSlots;
+      mbar_init(smem_u32(bars + i), is_ready ? 128u : 1u);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Guard g{abort_flag, p.status, p.limit_ns};
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto sfree = [&](int s) { return smem_u32(bars + C::kStages + s); };
+  auto a_ready = [&](int t) { return smem_u32(bars + 2 * C::kStages + t); };
+  auto a_free = [&](int t) { return smem_u32(bars + 2 * C::kStages + C::kSlots + t); };
+  const uint32_t tmem_full = smem_u32(bars + 2 * C::kStages + 2 * C::kSlots);
+  auto stage_b = [&](int s) { return smem + (size_t)s * C::kStageBytes; };
+  auto stage_stg = [&](int s) { return smem + (size_t)s * C::kStageBytes + C::kBBytes; };
+  auto slot_col = [&](int t) { return (uint32_t)(C::kDCols + t * C::kSlotCols); };
+
+  if (warp == 0) {
+    // ================= TMA producer
+    if (lane == 0) {
+      const uint32_t tx = C::kBBytes + C::kNumA * kTileBytes;
+      int kg = 0, issued = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const int4 tile = p.list.tiles[item / p.MT];
+        const int mt = item - (item / p.MT) * p.MT;
+        const uint8_t* a_src = p.a_tiles + ((size_t)(tile.x * p.MT + mt) * p.KS) * C::kNumA * kTileBytes;
+        for (int ks = 0; ks < p.KS; ++ks, ++kg) {
+          const int s = kg % C::kStages, u = kg / C::kStages;
+          if (u > 0 && !mbar_wait(sfree(s), (u - 1) & 1, g, 1u)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(full(s), tx);
+          tma_load_2d(smem_u32(stage_b(s)), &map_b, full(s), ks * kBK, tile.y);
+          bulk_load(smem_u32(stage_stg(s)), a_src + (size_t)ks * C::kNumA * kTileBytes, C::kNumA * kTileBytes,
+                    full(s));
+          ++issued;
+        }
+      }
+      if (*abort_flag) {
+        for (int k = max(0, issued - C::kStages); k < issued; ++k) {
+          const uint64_t t0 = global_ns();
+          while (!mbar_try_wait(full(k % C::kStages), (k / C::kStages) & 1))
+            if (global_ns() - t0 > p.limit_ns) break;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================= MMA issuer
+    if (lane == 0) {
+      int kg = 0, done = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const int4 tile = p.list.tiles[item / p.MT];
+        const uint32_t idesc = umma_idesc_bf16(kBM, tile.w);
+        for (int ks = 0; ks < p.KS; ++ks, ++kg) {
+          const int s = kg % C::kStages, t = kg % C::kSlots;
+          ok = mbar_wait(full(s), (kg / C::kStages) & 1, g, 2u) &&
+               mbar_wait(a_ready(t), (kg / C::kSlots) & 1, g, 4u);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t b0 = smem_u32(stage_b(s));
+#pragma unroll
+          for (int i = 0; i < C::kNumA; ++i)
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              umma_bf16_tmem_a(tmem + i * kSNB, tmem + slot_col(t) + i * 32 + kk * 8,
+                               umma_desc_sw128(b0 + kk * 32), idesc, (ks | kk) ? 1u : 0u);
+          umma_commit(sfree(s));
+          umma_commit(a_free(t));
+        }
+        if (ok) {
+          umma_commit(tmem_full);
+          ++done;
+        }
+      }
+      if (!ok) {
+        // MMAs already issued must finish before TMEM is released
+        umma_commit(tmem_full);
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(tmem_full, done & 1))
+          if (global_ns() - t0 > p.limit_ns) break;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ================= decode to TMEM + epilogue (warps 2..5)
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // tile row == TMEM lane
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    int kg = 0, it = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
+      const int4 tile = p.list.tiles[item / p.MT];
+      const int mt = item - (item / p.MT) * p.MT;
+      for (int ks = 0; ks < p.KS; ++ks, ++kg) {
+        const int s = kg % C::kStages, t = kg % C::kSlots, ut = kg / C::kSlots;
+        ok = mbar_wait(full(s), (kg / C::kStages) & 1, g, 8u) && (ut == 0 || mbar_wait(a_free(t), (ut - 1) & 1, g, 32u));
+        if (!ok) break;
+        const uint8_t* stg = stage_stg(s);
+#pragma unroll
+        for (int i = 0; i < C::kNumA; ++i) {
+          const uint8_t* tl = stg + i * kTileBytes;
+          const uint4 c0 = *reinterpret_cast<const uint4*>(tl + (size_t)r * 16);
+          const uint4 c1 = *reinterpret_cast<const uint4*>(tl + (size_t)(128 + r) * 16);
+          const uint32_t sc = *reinterpret_cast<const uint16_t*>(tl + kTilePackedBytes + 2 * r);
+          const ScaleMul m0 = scale_multipliers(sc & 0xFFu), m1 = scale_multipliers(sc >> 8);
+          const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          uint32_t v[32];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) tile_word_to_bf16(words[q], q < 4 ? m0 : m1, v + 4 * q);
+          tmem_st32(lane_base + slot_col(t) + i * 32, v);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        mbar_arrive(a_ready(t));
+      }
+      if (!ok) break;
+      // epilogue of this item
+      ok = mbar_wait(tmem_full, it & 1, g, 16u) && !*abort_flag;
+      if (!ok) break;
+      tc_fence_after();
+      const int m = mt * kBM + r;
+      float acc[32];
+      tmem_ld32(lane_base + 0, acc);
+      if (MODE == GATEUP) {
+        float up[32];
+        tmem_ld32(lane_base + kSNB, up);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < tile.z)
+            p.out_bf16[(size_t)(tile.y + j) * p.ld_out + m] = f32_to_bf16(situ_fast(acc[j], up[j], p.beta, p.beta_lin));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < tile.z) p.out_f32[(size_t)(tile.y + j) * p.ld_out + m] = acc[j];
+      }
+      tc_fence_before();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
 // ------------------------------------------------------------------ helpers
 // Gather the latent rows into slot order: lat_perm[s] = lat[perm[s] / K].
 __global__ void gather_rows_kernel(const uint16_t* __restrict__ lat, const int* __restrict__ perm, int TK, int K,
@@ -414,11 +639,11 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ lat, const int* 
   }
 }
 
-// Tiles of at most kBNMax rows per active expert, rows split evenly and
+// Tiles of at most bn_max rows per active expert, rows split evenly and
 // rounded up to 16: tiles[i] = {expert, first slot, rows, MMA N}.
 __global__ void __launch_bounds__(1024) build_tiles_kernel(const int* __restrict__ active,
-                                                           const int* __restrict__ offsets, int4* __restrict__ tiles,
-                                                           int* __restrict__ count) {
+                                                           const int* __restrict__ offsets, int bn_max,
+                                                           int4* __restrict__ tiles, int* __restrict__ count) {
   __shared__ int warp_tot[32];
   __shared__ int carry;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -431,7 +656,7 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int* __restrict
     if (a < n_act) {
       e = active[1 + a];
       c = offsets[e + 1] - offsets[e];
-      nsub = (c + kBNMax - 1) / kBNMax;
+      nsub = (c + bn_max - 1) / bn_max;
     }
     // exclusive scan of nsub over the block
     int incl = nsub;
@@ -530,6 +755,12 @@ cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const Para
 }  // namespace
 
 cudaError_t prepare_umma_kernels() {
+  cudaError_t e0 = cudaFuncSetAttribute(umma_stream_kernel<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        SCfg<GATEUP>::kSmem);
+  if (e0 == cudaSuccess)
+    e0 = cudaFuncSetAttribute(umma_stream_kernel<DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              SCfg<DOWN>::kSmem);
+  if (e0 != cudaSuccess) return e0;
   cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg<DENSE>::kSmem);
   if (e == cudaSuccess)
@@ -554,6 +785,7 @@ bool umma_path_enabled(const UmmaPlan& p, const Dims&, int T) { return p.enabled
 
 int umma_dense_launches() { return 1; }
 int umma_expert_launches() { return 4; }
+int umma_stream_launches() { return 4; }
 
 cudaError_t umma_dense(const UmmaPlan& p, const uint16_t* W, int M, int K, const uint16_t* X, int T, int split,
                        float* out_f32, uint16_t* out_bf16, cudaStream_t s) {
@@ -583,7 +815,7 @@ cudaError_t umma_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8
   if (TK <= 0) return cudaSuccess;
   UmmaWs ws = ws_view(p, d, p.max_tokens);
   const int max_tiles = TK / kBNMax + std::min(d.E, TK) + 1;
-  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, ws.tiles, ws.count);
+  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, kBNMax, ws.tiles, ws.count);
   gather_rows_kernel<<<152 * 8, 256, 0, s>>>(w.lat, w.perm, TK, d.K, d.L, ws.lat_perm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -613,6 +845,47 @@ cudaError_t umma_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8
   dn.out_f32 = w.o;
   dn.ld_out = d.L;
   return launch_gemm<DOWN>(mb2, mb2, dn, dim3(dn.MT, max_tiles), s);
+}
+
+// Decode-size experts: tiles of at most kSNB rows, streamed by persistent
+// CTAs (two per SM) with the decoded weights in TMEM.
+cudaError_t umma_stream_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8_t* d_tiles, const Work& w,
+                                int T, const Dims& d, cudaStream_t s) {
+  const int TK = T * d.K;
+  if (TK <= 0) return cudaSuccess;
+  UmmaWs ws = ws_view(p, d, p.max_tokens);
+  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, kSNB, ws.tiles, ws.count);
+  gather_rows_kernel<<<152 * 2, 256, 0, s>>>(w.lat, w.perm, TK, d.K, d.L, ws.lat_perm);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap mb1, mb2;
+  if (!make_map(&mb1, ws.lat_perm, TK, d.L, kSNB) || !make_map(&mb2, w.h, TK, d.I, kSNB))
+    return cudaErrorInvalidValue;
+  Params g{};
+  g.a_tiles = gu_tiles;
+  g.MT = d.I / kBM;
+  g.KS = d.L / kBK;
+  g.M = d.I;
+  g.list = TileList{ws.tiles, ws.count};
+  g.out_bf16 = w.h;
+  g.ld_out = d.I;
+  g.beta = d.beta;
+  g.beta_lin = d.beta_lin;
+  g.status = p.status;
+  g.limit_ns = p.limit_ns;
+  const int grid = 2 * p.num_sms;
+  umma_stream_kernel<GATEUP><<<grid, kSThreads, SCfg<GATEUP>::kSmem, s>>>(mb1, g);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  Params dn = g;
+  dn.a_tiles = d_tiles;
+  dn.MT = d.L / kBM;
+  dn.KS = d.I / kBK;
+  dn.M = d.L;
+  dn.out_bf16 = nullptr;
+  dn.out_f32 = w.o;
+  dn.ld_out = d.L;
+  umma_stream_kernel<DOWN><<<grid, kSThreads, SCfg<DOWN>::kSmem, s>>>(mb2, dn);
+  return cudaGetLastError();
 }
 
 }  // namespace k3

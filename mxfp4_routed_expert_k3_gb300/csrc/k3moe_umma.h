@@ -17,6 +17,7 @@ struct UmmaPlan {
   size_t ws_bytes = 256;  // workspace this path needs (tile list, slot-ordered latent rows)
   void* ws = nullptr;
   unsigned* status = nullptr;  // device status word (bounded waits report here)
+  int num_sms = 152;
   uint64_t limit_ns = 2000000000ull;
 };
 
@@ -29,5 +30,8 @@ int umma_dense_launches();
 cudaError_t umma_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8_t* d_tiles, const Work& w, int T,
                          const Dims& d, cudaStream_t s);
 int umma_expert_launches();
+cudaError_t umma_stream_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8_t* d_tiles, const Work& w,
+                                int T, const Dims& d, cudaStream_t s);
+int umma_stream_launches();
 
 }  // namespace k3

@@ -104,7 +104,7 @@ def _check(rc: int, ctx=None):
         raise K3Error(rc, last_error(ctx))
 
 
-PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE = 0, 1, 2
+PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_STREAM = 0, 1, 2, 3
 
 
 def make_config(d: LayerDims, max_tokens: int, spin_timeout_ms: int = 0, force_path: int = 0) -> Config:

@@ -17,8 +17,9 @@ pytestmark = pytest.mark.gpu
 MAXT = 320
 
 
-@pytest.fixture(scope="module", params=[k3moe.PATH_AUTO, k3moe.PATH_CUDA_CORE, k3moe.PATH_TENSOR_CORE],
-                ids=["auto", "cudacore", "tensorcore"])
+@pytest.fixture(scope="module",
+                params=[k3moe.PATH_AUTO, k3moe.PATH_CUDA_CORE, k3moe.PATH_TENSOR_CORE, k3moe.PATH_STREAM],
+                ids=["auto", "cudacore", "tensorcore", "stream"])
 def tiny(request):
     d = TINY
     w = synth.layer_weights(d, seed=0)
