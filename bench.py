@@ -159,7 +159,7 @@ def run_ours(args, rank, world, local_rank):
     batches = DECODE_BATCHES
     maxT = max(batches)
     w = synth.layer_weights(d, seed=1)
-    layer = k3moe.Layer(d, w, max_tokens=maxT, device=local_rank)
+    layer = k3moe.Layer(d, w, max_tokens=maxT, device=local_rank, force_path=args.path)
     stream = torch.cuda.Stream(device=dev)
     pool = args.warmup + args.steps
     # fresh token batches for every step, resident in HBM before timing
@@ -245,8 +245,13 @@ def run_ours(args, rank, world, local_rank):
                     kern_bytes += n_act * d.expert_gate_up_bytes() + T * d.top_k * (d.latent + d.inter) * 2
     launches = sum(len(per_kernel[T]) for T in batches)
     achieved = kern_bytes / (kern_ms / 1e3) / 1e9 if kern_ms > 0 else None
-    traffic = recorded_traffic("gateup_gemv_kernel", "k3-decode-T64")
-    roofline = {"bound": "hbm", "kernel": "gateup_gemv_kernel (grouped MXFP4 gate/up GEMV + SiTU-GLU)",
+    path_used = layer.query("path_last")
+    kernel_id = {1: "gateup_gemv_kernel", 3: "umma_stream_kernel_gateup"}.get(path_used, "umma_gemm_kernel_gateup")
+    kernel_desc = {1: "gateup_gemv_kernel (CUDA-core grouped MXFP4 gate/up GEMV + SiTU-GLU)",
+                   3: "umma_stream_kernel<GATEUP> (tcgen05, decoded MXFP4 weights in TMEM, SiTU-GLU epilogue)"
+                   }.get(path_used, "umma_gemm_kernel<GATEUP> (tcgen05 grouped MXFP4 GEMM)")
+    traffic = recorded_traffic(kernel_id, "k3-decode")
+    roofline = {"bound": "hbm", "kernel": kernel_desc, "path": path_used,
                 "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": (achieved / peaks["hbm_gbs"]) if achieved else None,
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
@@ -379,6 +384,8 @@ def main():
     ap.add_argument("--cpu-sample", type=int, default=16, help="tokens in the oracle CPU baseline sample")
     ap.add_argument("--ref-tokens-per-step", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="kernel path (0 = the library's choice by token count; see k3moe_config.force_path)")
     ap.add_argument("--experts", type=int, default=896,
                     help="experts of the K3-dim layer (default 896; fewer only for small profiling captures)")
     args = ap.parse_args()

@@ -153,10 +153,11 @@ void k3moe_destroy(k3moe_ctx* ctx);
 /* MXFP4 -> bf16 dequantisation of a [rows, cols] matrix in checkpoint
  * layout (device pointers: packed [rows, cols/2] u8, scale [rows, cols/32]
  * u8, out [rows, cols] bf16), using the same device decoding routines as
- * the expert kernels.  kind 0: the bf16 tile producer of the tensor-core
- * kernels (value = e2m1 * 2^(S-127), exact for scale bytes 0..252, IEEE
- * overflow above); kind 1: the per-group decoding of the decode kernels,
- * written as fp32 (out is then [rows, cols] float).  Requires cols % 64 == 0.
+ * the expert kernels (checkpoint bytes -> tile word -> bf16).  kind 0: bf16
+ * out (value = e2m1 * 2^(S-127), exact for scale bytes 0..252, IEEE
+ * overflow above); kind 1: the same values widened to fp32 (out is then
+ * [rows, cols] float), as the CUDA-core kernels use them.  Requires
+ * cols % 64 == 0.
  * Asynchronous on `cuda_stream`.  The decoding definition is the "Tiers"
  * section of the kimi-k3-mlx README (same encoding, low bits first, e8m0
  * scales) and K3_ARTIFACT_AUDIT section 4.3 (group 32). */

@@ -332,8 +332,9 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
     K3_LAUNCH(k3::umma_experts(c->umma, c->gu_tiles, c->d_tiles, w, T, d, s), k3::umma_expert_launches(),
               "experts (tensor cores)");
   } else if (path == 3) {
-    K3_LAUNCH(k3::umma_stream_experts(c->umma, c->gu_tiles, c->d_tiles, w, T, d, s), k3::umma_stream_launches(),
-              "experts (streaming tensor cores)");
+    K3_LAUNCH(k3::umma_stream_prepare(c->umma, w, T, d, s), 2, "tile list + gather");
+    K3_LAUNCH(k3::umma_stream_gateup(c->umma, c->gu_tiles, w, T, d, s), 1, "gate/up");
+    K3_LAUNCH(k3::umma_stream_down(c->umma, c->d_tiles, w, T, d, s), 1, "down");
   } else {
     K3_LAUNCH(k3::launch_gateup_gemv(c->gu_tiles, w.lat, w.active, w.offsets, w.perm, max_active, d, w.h, s), 1,
               "gate/up");

@@ -329,36 +329,28 @@ __device__ __forceinline__ float situ_glu(float g, float u, float beta, float be
   return beta * tanhf(g / beta) * sig * beta_lin * tanhf(u / beta_lin);
 }
 
-// Position, within each group of 8 staged activations, of column c (the
-// inverse of dec2_column_of).
-__device__ __forceinline__ int dec2_pos_of_column(int c) {
-  // columns 0..7 -> stream positions
-  const int pos[8] = {0, 4, 1, 5, 2, 6, 3, 7};
-  return pos[c];
-}
-
 // Accumulate sum_i w_i * x_i over one 32-column scale group held in the
-// 16-byte chunk q, for NT staged token rows (xs rows of `ld` floats,
-// starting at stream column x0).
+// 16-byte chunk q (decoded exactly to bf16 with the group's scale, then
+// widened to fp32), for NT staged token rows (xs rows of `ld` floats,
+// starting at column x0).
 template <int NT>
-__device__ __forceinline__ void group_dot(const uint4& q, const float* __restrict__ xs, int ld, int x0, int nt,
-                                          float part[NT]) {
+__device__ __forceinline__ void group_dot(const uint4& q, const ScaleMul& sm, const float* __restrict__ xs, int ld,
+                                          int x0, int nt, float part[NT]) {
   const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    float2 f[4];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) f[b] = f16x2_to_f32x2(e2m1x2_to_f16x2((wd[j] >> (8 * b)) & 0xFFu));
+    uint32_t o[4];
+    tile_word_to_bf16(wd[j], sm, o);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       if (t < nt) {
         const float4 xa = *reinterpret_cast<const float4*>(xs + (size_t)t * ld + x0 + 8 * j);
         const float4 xb = *reinterpret_cast<const float4*>(xs + (size_t)t * ld + x0 + 8 * j + 4);
         unsigned long long acc = pack_f32x2(part[t], 0.f);
-        acc = ffma2(pack_f32x2(f[0].x, f[0].y), pack_f32x2(xa.x, xa.y), acc);
-        acc = ffma2(pack_f32x2(f[1].x, f[1].y), pack_f32x2(xa.z, xa.w), acc);
-        acc = ffma2(pack_f32x2(f[2].x, f[2].y), pack_f32x2(xb.x, xb.y), acc);
-        acc = ffma2(pack_f32x2(f[3].x, f[3].y), pack_f32x2(xb.z, xb.w), acc);
+        acc = ffma2(((unsigned long long)(o[0] & 0xFFFF0000u) << 32) | (o[0] << 16), pack_f32x2(xa.x, xa.y), acc);
+        acc = ffma2(((unsigned long long)(o[1] & 0xFFFF0000u) << 32) | (o[1] << 16), pack_f32x2(xa.z, xa.w), acc);
+        acc = ffma2(((unsigned long long)(o[2] & 0xFFFF0000u) << 32) | (o[2] << 16), pack_f32x2(xb.x, xb.y), acc);
+        acc = ffma2(((unsigned long long)(o[3] & 0xFFFF0000u) << 32) | (o[3] << 16), pack_f32x2(xb.z, xb.w), acc);
         const float2 r = unpack_f32x2(acc);
         part[t] = r.x + r.y;
       }
@@ -366,15 +358,13 @@ __device__ __forceinline__ void group_dot(const uint4& q, const float* __restric
   }
 }
 
-// Stage nb token rows (bf16, length len, row index from `rows_of`) as fp32
-// in decoder-2 stream order.
+// Stage nb token rows (bf16, length len, row index from `rows_of`) as fp32.
 template <typename RowOf>
 __device__ __forceinline__ void stage_rows(float* xs, const uint16_t* __restrict__ src, int len, int nb,
                                            RowOf rows_of) {
   for (int i = threadIdx.x; i < nb * len; i += blockDim.x) {
     const int j = i / len, c = i - j * len;
-    const size_t row = rows_of(j);
-    xs[(size_t)j * len + (c & ~7) + dec2_pos_of_column(c & 7)] = bf16_to_f32(src[row * len + c]);
+    xs[(size_t)j * len + c] = bf16_to_f32(src[rows_of(j) * len + c]);
   }
 }
 
@@ -425,20 +415,8 @@ __global__ void __launch_bounds__(256) gateup_gemv_kernel(const uint8_t* __restr
         n1 = __ldg(reinterpret_cast<const uint4*>(nt) + 128 + r);
         nsc = __ldg(reinterpret_cast<const uint16_t*>(nt + kTilePackedBytes) + r);
       }
-      float part[TB];
-#pragma unroll
-      for (int t = 0; t < TB; ++t) part[t] = 0.f;
-      group_dot<TB>(c0, xs, L, ks * kTileCols, nb, part);
-      const float sf0 = e8m0_to_f32(sc & 0xFFu);
-#pragma unroll
-      for (int t = 0; t < TB; ++t) {
-        acc[t] = fmaf(sf0, part[t], acc[t]);
-        part[t] = 0.f;
-      }
-      group_dot<TB>(c1, xs, L, ks * kTileCols + 32, nb, part);
-      const float sf1 = e8m0_to_f32(sc >> 8);
-#pragma unroll
-      for (int t = 0; t < TB; ++t) acc[t] = fmaf(sf1, part[t], acc[t]);
+      group_dot<TB>(c0, scale_multipliers(sc & 0xFFu), xs, L, ks * kTileCols, nb, acc);
+      group_dot<TB>(c1, scale_multipliers(sc >> 8), xs, L, ks * kTileCols + 32, nb, acc);
       c0 = n0;
       c1 = n1;
       sc = nsc;
@@ -514,20 +492,8 @@ __global__ void __launch_bounds__(256) down_gemv_kernel(const uint8_t* __restric
         n1 = __ldg(reinterpret_cast<const uint4*>(nt) + 128 + r);
         nsc = __ldg(reinterpret_cast<const uint16_t*>(nt + kTilePackedBytes) + r);
       }
-      float part[TB];
-#pragma unroll
-      for (int t = 0; t < TB; ++t) part[t] = 0.f;
-      group_dot<TB>(c0, xs, I, ks * kTileCols, nb, part);
-      const float sf0 = e8m0_to_f32(sc & 0xFFu);
-#pragma unroll
-      for (int t = 0; t < TB; ++t) {
-        acc[t] = fmaf(sf0, part[t], acc[t]);
-        part[t] = 0.f;
-      }
-      group_dot<TB>(c1, xs, I, ks * kTileCols + 32, nb, part);
-      const float sf1 = e8m0_to_f32(sc >> 8);
-#pragma unroll
-      for (int t = 0; t < TB; ++t) acc[t] = fmaf(sf1, part[t], acc[t]);
+      group_dot<TB>(c0, scale_multipliers(sc & 0xFFu), xs, I, ks * kTileCols, nb, acc);
+      group_dot<TB>(c1, scale_multipliers(sc >> 8), xs, I, ks * kTileCols + 32, nb, acc);
       c0 = n0;
       c1 = n1;
       sc = nsc;
@@ -665,8 +631,8 @@ cudaError_t launch_relayout(const uint8_t* packed, const uint8_t* scale, int n_m
 // =====================================================================
 // Standalone dequant (checkpoint layout in, row-major out) through the same
 // tile-word re-layout and decoders as the expert kernels.
-//   kind 0: bf16 via decoder 1 (tensor-core tile producer)
-//   kind 1: fp32 via decoder 2 (decode GEMV), value = e2m1 * e8m0_to_f32(S)
+//   kind 0: bf16 (the tensor-core tile producer's decoder)
+//   kind 1: the same values widened to fp32 (as the CUDA-core GEMVs use them)
 // One thread per 8 consecutive columns of a row.
 // =====================================================================
 __global__ void dequant_kernel(const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scale, int rows,
@@ -685,14 +651,13 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ packed, const uint8_t
       *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + (size_t)r * cols + col0) =
           make_uint4(o4[0], o4[1], o4[2], o4[3]);
     } else {
-      const float sf = e8m0_to_f32(S);
-      float* dst = reinterpret_cast<float*>(out) + (size_t)r * cols + col0;
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const float2 f = f16x2_to_f32x2(e2m1x2_to_f16x2((q >> (8 * b)) & 0xFFu));
-        dst[dec2_column_of(2 * b)] = f.x * sf;
-        dst[dec2_column_of(2 * b + 1)] = f.y * sf;
-      }
+      uint32_t o4[4];
+      tile_word_to_bf16(q, scale_multipliers(S), o4);
+      float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (size_t)r * cols + col0);
+      const float2 a = unpack_bf16x2(o4[0]), b = unpack_bf16x2(o4[1]), c = unpack_bf16x2(o4[2]),
+                   d = unpack_bf16x2(o4[3]);
+      dst[0] = make_float4(a.x, a.y, b.x, b.y);
+      dst[1] = make_float4(c.x, c.y, d.x, d.y);
     }
   }
 }

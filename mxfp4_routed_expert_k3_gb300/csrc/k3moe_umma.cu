@@ -785,7 +785,6 @@ bool umma_path_enabled(const UmmaPlan& p, const Dims&, int T) { return p.enabled
 
 int umma_dense_launches() { return 1; }
 int umma_expert_launches() { return 4; }
-int umma_stream_launches() { return 4; }
 
 cudaError_t umma_dense(const UmmaPlan& p, const uint16_t* W, int M, int K, const uint16_t* X, int T, int split,
                        float* out_f32, uint16_t* out_bf16, cudaStream_t s) {
@@ -848,43 +847,60 @@ cudaError_t umma_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8
 }
 
 // Decode-size experts: tiles of at most kSNB rows, streamed by persistent
-// CTAs (two per SM) with the decoded weights in TMEM.
-cudaError_t umma_stream_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8_t* d_tiles, const Work& w,
-                                int T, const Dims& d, cudaStream_t s) {
+// CTAs (two per SM) with the decoded weights in TMEM.  Three launch groups:
+// the tile list + slot-ordered latent rows, then gate/up, then down.
+cudaError_t umma_stream_prepare(const UmmaPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s) {
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
   UmmaWs ws = ws_view(p, d, p.max_tokens);
   build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, kSNB, ws.tiles, ws.count);
   gather_rows_kernel<<<152 * 2, 256, 0, s>>>(w.lat, w.perm, TK, d.K, d.L, ws.lat_perm);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  CUtensorMap mb1, mb2;
-  if (!make_map(&mb1, ws.lat_perm, TK, d.L, kSNB) || !make_map(&mb2, w.h, TK, d.I, kSNB))
-    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+static Params stream_params(const UmmaPlan& p, const Dims& d, const UmmaWs& ws) {
   Params g{};
-  g.a_tiles = gu_tiles;
-  g.MT = d.I / kBM;
-  g.KS = d.L / kBK;
-  g.M = d.I;
   g.list = TileList{ws.tiles, ws.count};
-  g.out_bf16 = w.h;
-  g.ld_out = d.I;
   g.beta = d.beta;
   g.beta_lin = d.beta_lin;
   g.status = p.status;
   g.limit_ns = p.limit_ns;
-  const int grid = 2 * p.num_sms;
-  umma_stream_kernel<GATEUP><<<grid, kSThreads, SCfg<GATEUP>::kSmem, s>>>(mb1, g);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  Params dn = g;
-  dn.a_tiles = d_tiles;
-  dn.MT = d.L / kBM;
-  dn.KS = d.I / kBK;
-  dn.M = d.L;
-  dn.out_bf16 = nullptr;
-  dn.out_f32 = w.o;
-  dn.ld_out = d.L;
-  umma_stream_kernel<DOWN><<<grid, kSThreads, SCfg<DOWN>::kSmem, s>>>(mb2, dn);
+  return g;
+}
+
+cudaError_t umma_stream_gateup(const UmmaPlan& p, const uint8_t* gu_tiles, const Work& w, int T, const Dims& d,
+                               cudaStream_t s) {
+  const int TK = T * d.K;
+  if (TK <= 0) return cudaSuccess;
+  UmmaWs ws = ws_view(p, d, p.max_tokens);
+  CUtensorMap mb;
+  if (!make_map(&mb, ws.lat_perm, TK, d.L, kSNB)) return cudaErrorInvalidValue;
+  Params g = stream_params(p, d, ws);
+  g.a_tiles = gu_tiles;
+  g.MT = d.I / kBM;
+  g.KS = d.L / kBK;
+  g.M = d.I;
+  g.out_bf16 = w.h;
+  g.ld_out = d.I;
+  umma_stream_kernel<GATEUP><<<2 * p.num_sms, kSThreads, SCfg<GATEUP>::kSmem, s>>>(mb, g);
+  return cudaGetLastError();
+}
+
+cudaError_t umma_stream_down(const UmmaPlan& p, const uint8_t* d_tiles, const Work& w, int T, const Dims& d,
+                             cudaStream_t s) {
+  const int TK = T * d.K;
+  if (TK <= 0) return cudaSuccess;
+  UmmaWs ws = ws_view(p, d, p.max_tokens);
+  CUtensorMap mb;
+  if (!make_map(&mb, w.h, TK, d.I, kSNB)) return cudaErrorInvalidValue;
+  Params g = stream_params(p, d, ws);
+  g.a_tiles = d_tiles;
+  g.MT = d.L / kBM;
+  g.KS = d.I / kBK;
+  g.M = d.L;
+  g.out_f32 = w.o;
+  g.ld_out = d.L;
+  umma_stream_kernel<DOWN><<<2 * p.num_sms, kSThreads, SCfg<DOWN>::kSmem, s>>>(mb, g);
   return cudaGetLastError();
 }
 

@@ -30,8 +30,10 @@ int umma_dense_launches();
 cudaError_t umma_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8_t* d_tiles, const Work& w, int T,
                          const Dims& d, cudaStream_t s);
 int umma_expert_launches();
-cudaError_t umma_stream_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8_t* d_tiles, const Work& w,
-                                int T, const Dims& d, cudaStream_t s);
-int umma_stream_launches();
+cudaError_t umma_stream_prepare(const UmmaPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s);
+cudaError_t umma_stream_gateup(const UmmaPlan& p, const uint8_t* gu_tiles, const Work& w, int T, const Dims& d,
+                               cudaStream_t s);
+cudaError_t umma_stream_down(const UmmaPlan& p, const uint8_t* d_tiles, const Work& w, int T, const Dims& d,
+                             cudaStream_t s);
 
 }  // namespace k3

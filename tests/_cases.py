@@ -40,6 +40,25 @@ def bf16_f64(bits) -> np.ndarray:
     return ora.bf16_to_float(np.asarray(bits).view(np.uint16) if np.asarray(bits).dtype != np.uint16 else bits)
 
 
+def bf16_round(v: np.ndarray) -> np.ndarray:
+    """float64 -> nearest bf16 value (as float64), through the oracle."""
+    flat = np.asarray(v, np.float64).reshape(-1)
+    bits = np.fromiter((ora.bf16_from_double(float(a)) for a in flat), dtype=np.uint16, count=flat.size)
+    return ora.bf16_to_float(bits).reshape(np.shape(v))
+
+
+_EXPERT_CACHE: dict = {}
+
+
+def expert_matrix(w: dict, name: str, e: int) -> np.ndarray:
+    """Expert e's w1 / w3 / w2 dequantised by the oracle, as float64."""
+    key = (id(w), name, int(e))
+    if key not in _EXPERT_CACHE or _EXPERT_CACHE[key][0] is not w:
+        _EXPERT_CACHE[key] = (w, ora.bf16_to_float(ora.mxfp4_dequant_bf16(w[name + "_packed"][e],
+                                                                          w[name + "_scale"][e])))
+    return _EXPERT_CACHE[key][1]
+
+
 def bf16_ulp(v: np.ndarray) -> np.ndarray:
     a = np.abs(v)
     e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))

@@ -19,10 +19,21 @@ MAXT = 8192
 
 
 @pytest.fixture(scope="module")
-def k3layer():
-    w = synth.layer_weights(K3, seed=1)
-    layer = k3moe.Layer(K3, w, max_tokens=MAXT)
-    yield w, layer
+def k3weights():
+    return synth.layer_weights(K3, seed=1)
+
+
+@pytest.fixture(scope="module")
+def k3layer(k3weights):
+    layer = k3moe.Layer(K3, k3weights, max_tokens=MAXT)
+    yield k3weights, layer
+    layer.close()
+
+
+@pytest.fixture(scope="module", params=[k3moe.PATH_CUDA_CORE, k3moe.PATH_STREAM], ids=["cudacore", "stream"])
+def k3decode(request, k3weights):
+    layer = k3moe.Layer(K3, k3weights, max_tokens=64, force_path=request.param)
+    yield k3weights, layer
     layer.close()
 
 
@@ -40,8 +51,8 @@ def run(layer, x_np):
 
 
 @pytest.mark.parametrize("T", [1, 8, 64])
-def test_k3_decode_all_tokens(k3layer, T):
-    w, layer = k3layer
+def test_k3_decode_all_tokens(k3decode, T):
+    w, layer = k3decode
     x = gapped_tokens(K3, w, seed=200 + T, T=T)
     ref = ora.forward(K3, w, x)
     y, idx, wts = run(layer, x)

@@ -1,0 +1,148 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case copies oracle/k3moe_oracle.c, plants one mistake in the copy (on
+the CPU, in a temporary directory), compiles it, and checks that the pin
+written for that part of the oracle rejects the mutant while the original
+passes.  The mistakes are the ones a reader could make from the pages:
+the wrong nibble first, the wrong exponent bias, swapped SiTU temperatures,
+the bias leaking into the weights, ties to the higher id, a dropped RMSNorm
+epsilon, a transposed down projection.
+"""
+import ctypes as C
+import math
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+from mxfp4_routed_expert_k3_gb300 import synth
+from mxfp4_routed_expert_k3_gb300.dims import LayerDims
+from oracle import oracle as ora
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "k3moe_oracle.c")
+E2M1_INT = [0, 1, 2, 3, 4, 6, 8, 12]
+
+MUTATIONS = {
+    "high_nibble_first": ("unsigned code = (j % 2 == 0) ? (byte & 0x0Fu) : (byte >> 4);",
+                          "unsigned code = (j % 2 == 0) ? (byte >> 4) : (byte & 0x0Fu);"),
+    "e2m1_bias_0": ("ldexp(1.0 + 0.5 * (double)m, (int)e - 1)", "ldexp(1.0 + 0.5 * (double)m, (int)e)"),
+    "e8m0_bias_128": ("return ldexp(1.0, (int)S - 127);", "return ldexp(1.0, (int)S - 128);"),
+    "situ_betas_swapped": ("return beta * tanh(g / beta) * ora_sigmoid(g) * beta_lin * tanh(u / beta_lin);",
+                           "return beta_lin * tanh(g / beta_lin) * ora_sigmoid(g) * beta * tanh(u / beta);"),
+    "bias_in_weights": ("for (int k = 0; k < K; ++k) sum += (double)s[idx[k]];",
+                        "for (int k = 0; k < K; ++k) sum += (double)key[idx[k]];"),
+    "ties_to_higher_id": ("if (best < 0 || key[e] > key[best]) best = e;",
+                          "if (best < 0 || key[e] >= key[best]) best = e;"),
+    "rmsnorm_no_eps": ("double inv = 1.0 / sqrt(ms + d->rms_eps);", "double inv = 1.0 / sqrt(ms);"),
+    "down_proj_transposed": ("acc += ora_bf16_to_double(W->down_proj[(size_t)l * H + j]) * ora_bf16_to_double(x[j]);",
+                             "acc += ora_bf16_to_double(W->down_proj[(size_t)j * L + l]) * ora_bf16_to_double(x[j]);"),
+}
+
+
+def build_variant(tmp, name):
+    src = open(SRC).read()
+    if name is not None:
+        old, new = MUTATIONS[name]
+        assert src.count(old) >= 1, name
+        src = src.replace(old, new, 1)
+    path = os.path.join(tmp, f"v_{name}.c")
+    open(path, "w").write(src)
+    so = path[:-2] + ".so"
+    subprocess.check_call(["gcc", *ora.GCC_FLAGS, path, "-o", so, "-lm"])
+    L = C.CDLL(so)
+    L.ora_bf16_to_double.restype = C.c_double
+    L.ora_bf16_to_double.argtypes = [C.c_uint16]
+    L.ora_situ_glu.restype = C.c_double
+    L.ora_situ_glu.argtypes = [C.c_double] * 4
+    L.ora_mxfp4_dequant_bf16.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p]
+    L.ora_route_from_logits.argtypes = [C.POINTER(ora.OraDims)] + [C.c_void_p] * 5
+    L.ora_forward.argtypes = [C.POINTER(ora.OraDims), C.POINTER(ora.OraWeights)] + [C.c_void_p, C.c_int] + \
+        [C.c_void_p] * 9
+    return L
+
+
+# ---- the pins, as functions of a compiled variant (True = pin passes)
+def pin_dequant(L):
+    packed = np.tile(np.arange(256, dtype=np.uint8), (256, 1))
+    scale = np.repeat(np.arange(256, dtype=np.uint8)[:, None], 16, axis=1)
+    out = np.empty((256, 512), np.uint16)
+    L.ora_mxfp4_dequant_bf16(packed.ctypes.data, scale.ctypes.data, 256, 512, out.ctypes.data)
+    f = ora.bf16_to_float(out)
+    for S in range(0, 253, 7):
+        for b in range(256):
+            for hi in (0, 1):
+                code = (b >> 4) if hi else (b & 0xF)
+                v = E2M1_INT[code & 7] * 2.0 ** (S - 128) * (-1 if code >> 3 else 1)
+                if f[S, 2 * b + hi] != v:
+                    return False
+    return True
+
+
+def pin_situ(L):
+    for u in (-3.0, 0.5, 7.0):
+        if abs(L.ora_situ_glu(60.0, u, 4.0, 25.0) - 100 * math.tanh(u / 25)) > 1e-9:
+            return False
+    return True
+
+
+def pin_router(L):
+    d = LayerDims(hidden=64, latent=64, n_experts=8, top_k=3, inter=64)
+    ds = ora.dims_struct(d)
+    logits = np.zeros(8, np.float32)
+    bias = np.array([0, 0.5, 0.5, 0, 0.5, 0, 0.5, 0], np.float32)
+    idx = np.empty(3, np.int32)
+    w = np.empty(3, np.float32)
+    L.ora_route_from_logits(C.byref(ds), logits.ctypes.data, bias.ctypes.data, idx.ctypes.data, w.ctypes.data, None)
+    if idx.tolist() != [1, 2, 4]:
+        return False
+    # the weights use the unbiased score: all selected scores are sigmoid(0)
+    return bool(np.allclose(w, 1 / 3, rtol=1e-6))
+
+
+def pin_layer(L):
+    """Against the independent numpy formulation in test_oracle_pins."""
+    from test_oracle_pins import np_layer
+    # eps of the order of mean(c^2), so that dropping it changes n visibly
+    d = LayerDims(hidden=128, latent=128, n_experts=8, top_k=2, inter=128, rms_eps=4.0)
+    w = synth.layer_weights(d, seed=12)
+    x = synth.token_rows(d, 13, 3)
+    ref = np_layer(d, w, x)
+    T = 3
+    y = np.empty((T, d.hidden), np.uint16)
+    idx = np.empty((T, d.top_k), np.int32)
+    wt = np.empty((T, d.top_k), np.float32)
+    c = np.empty((T, d.latent), np.float64)
+    n = np.empty((T, d.latent), np.uint16)
+    ds, ws = ora.dims_struct(d), ora.weights_struct(w)
+    L.ora_forward(C.byref(ds), C.byref(ws), x.ctypes.data, T, y.ctypes.data, idx.ctypes.data, wt.ctypes.data,
+                  None, None, None, None, c.ctypes.data, n.ctypes.data)
+    assert 0.1 < d.rms_eps / np.mean(ref["c"] ** 2) < 10
+    yf, nf = ora.bf16_to_float(y), ora.bf16_to_float(n)
+    return bool(np.abs(c - ref["c"]).max() < 1e-9 * np.abs(ref["c"]).max()
+                and np.abs(nf - ref["n"]).max() <= 2 ** -7 * np.abs(ref["n"]).max()
+                and np.abs(yf - ref["y"]).max() <= 2 ** -6 * np.abs(ref["y"]).max())
+
+
+PIN_OF = {
+    "high_nibble_first": pin_dequant, "e2m1_bias_0": pin_dequant, "e8m0_bias_128": pin_dequant,
+    "situ_betas_swapped": pin_situ, "bias_in_weights": pin_router, "ties_to_higher_id": pin_router,
+    "rmsnorm_no_eps": pin_layer, "down_proj_transposed": pin_layer,
+}
+
+
+@pytest.fixture(scope="module")
+def tmpdir_mod(tmp_path_factory):
+    return str(tmp_path_factory.mktemp("mutants"))
+
+
+def test_original_passes_every_pin(tmpdir_mod):
+    L = build_variant(tmpdir_mod, None)
+    for pin in set(PIN_OF.values()):
+        assert pin(L), pin.__name__
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pin_rejects_mutant(tmpdir_mod, name):
+    L = build_variant(tmpdir_mod, name)
+    assert not PIN_OF[name](L), f"mutation {name} was not caught by {PIN_OF[name].__name__}"
