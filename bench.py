@@ -263,9 +263,17 @@ def run_ours(args, rank, world, local_rank):
         nact = statistics.mean(active_experts[T])
         alg = nact * d.expert_bytes() + d.dense_bytes() + T * d.hidden * 4
         fms = statistics.mean(fwd_ms[T])
+        kms = {}
+        for step_prof in per_kernel[T]:
+            for name, ms in step_prof:
+                kms.setdefault(name, []).append(ms)
+        gu_ms = statistics.mean(kms.get(kname, [float("nan")]))
+        gu_bytes = nact * d.expert_gate_up_bytes() + T * d.top_k * (d.latent + d.inter) * 2
         sweep[f"T={T}"] = {"forward_ms": fms, "tokens_per_s": T / (fms / 1e3), "active_experts": nact,
                            "algorithmic_GB": alg / 1e9, "layer_GB_per_s": alg / (fms / 1e3) / 1e9,
-                           "launches": launches_per_forward[T]}
+                           "gate_up_GB_per_s": gu_bytes / (gu_ms / 1e3) / 1e9,
+                           "launches": launches_per_forward[T],
+                           "kernel_ms": {k: statistics.mean(v) for k, v in kms.items()}}
 
     # ---- e2e: through the public C-ABI call with HOST buffers (pinned), copies timed
     e2e = run_e2e(layer, d, batches, args, rank, dev, stream)
@@ -291,7 +299,6 @@ def run_ours(args, rank, world, local_rank):
                 "d2h_bytes_per_step": e2e["d2h"], "how": "k3moe_forward_host (pinned host x -> y, idx, w)"},
         "gpu_launches": sum(launches_per_forward[T] for T in batches) * args.steps,
         "decode_sweep": sweep,
-        "kernel_ms_mean": {k: statistics.mean(v) for k, v in group_ms.items()},
         "wall_s_timed_region": t_wall,
     }
     if clk is not None:

@@ -20,6 +20,10 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 }  // namespace
 
+namespace k3 {
+void set_thread_error(const char* msg) { g_create_error = msg; }
+}  // namespace k3
+
 struct k3moe_ctx {
   k3moe_config cfg{};
   int device = 0;
@@ -320,6 +324,9 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
   if (big) {
     K3_LAUNCH(k3::umma_dense(c->umma, c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, d.E, w.logits, w.lat, s),
               k3::umma_dense_launches(), "router + down_proj (tensor cores)");
+  } else if (path == 3 && T <= 64) {
+    K3_LAUNCH(k3::umma_dense_small(c->umma, c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, d.E, w.logits, w.lat, s),
+              2, "router + down_proj");
   } else {
     K3_LAUNCH(k3::launch_dense_gemv(c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, d.E, w.logits, w.lat, s), 1,
               "router + down_proj");
@@ -344,6 +351,8 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
   if (big) {
     K3_LAUNCH(k3::umma_dense(c->umma, c->wu, d.H, d.L, w.n, T, 0, nullptr, (uint16_t*)y, s),
               k3::umma_dense_launches(), "up_proj (tensor cores)");
+  } else if (path == 3 && T <= 64) {
+    K3_LAUNCH(k3::umma_dense_small(c->umma, c->wu, d.H, d.L, w.n, T, 0, nullptr, (uint16_t*)y, s), 2, "up_proj");
   } else {
     K3_LAUNCH(k3::launch_dense_gemv(c->wu, d.H, d.L, w.n, T, 0, nullptr, (uint16_t*)y, s), 1, "up_proj");
   }

@@ -29,6 +29,9 @@ struct Work {
   unsigned* status;   // device status word
 };
 
+// ---- k3moe_api.cu: the per-thread message returned by k3moe_last_error(NULL)
+void set_thread_error(const char* msg);
+
 // ---- k3moe_decode.cu
 cudaError_t launch_dense_gemv(const uint16_t* W, int M, int K, const uint16_t* X, int T, int split,
                               float* out_f32, uint16_t* out_bf16, cudaStream_t s);

@@ -625,6 +625,177 @@ __global__ void __launch_bounds__(kSThreads, 1) umma_stream_kernel(const __grid_
   if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
+// =====================================================================
+// Streaming dense GEMM for small T (decode): D = W . X^T with W bf16
+// [M, K] (the weights, M side) and X bf16 [T <= 64, K] (N side).  Work items
+// are (128-row tile, K chunk) so that every SM streams weights even though
+// M / 128 is small (35 tiles for router + down_proj); each item writes its
+// fp32 partial sums to part[chunk][t][m] and splitk_reduce_kernel adds the
+// chunks in order.  A and B come by 2-D TMA (128-byte swizzle); D is double
+// buffered in TMEM so the epilogue of one item overlaps the next item's MMAs.
+// =====================================================================
+constexpr int kDNB = 64;  // max tokens
+struct DCfg {
+  static constexpr int kABytes = kBM * kBK * 2;   // 16 KB
+  static constexpr int kBBytes = kDNB * kBK * 2;  // 8 KB
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = 4;
+  static constexpr int kSmem = kStages * kStageBytes + 1024 + 512;
+};
+
+struct DenseStreamParams {
+  int MT, KS, nkc, ks_per_chunk, M, T;
+  float* part;  // [nkc][T][M]
+  unsigned* status;
+  uint64_t limit_ns;
+};
+
+__global__ void __launch_bounds__(kSThreads, 1) umma_dense_stream_kernel(const __grid_constant__ CUtensorMap map_a,
+                                                                         const __grid_constant__ CUtensorMap map_b,
+                                                                         const DenseStreamParams p) {
+  using C = DCfg;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  // bars: full[S], free[S], tmem_full[2], tmem_empty[2]
+  const int NB = 2 * C::kStages + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NB);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = p.MT * p.nkc;
+  if ((int)blockIdx.x >= n_items) return;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NB; ++i) mbar_init(smem_u32(bars + i), i >= 2 * C::kStages + 2 ? 128u : 1u);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 128);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Guard g{abort_flag, p.status, p.limit_ns};
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto sfree = [&](int s) { return smem_u32(bars + C::kStages + s); };
+  auto tfull = [&](int b) { return smem_u32(bars + 2 * C::kStages + b); };
+  auto tempty = [&](int b) { return smem_u32(bars + 2 * C::kStages + 2 + b); };
+  auto stage_a = [&](int s) { return smem + (size_t)s * C::kStageBytes; };
+  auto stage_b = [&](int s) { return smem + (size_t)s * C::kStageBytes + C::kABytes; };
+  const int n_mma = (p.T + 15) & ~15;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int kg = 0, issued = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const int mt = item % p.MT, kc = item / p.MT;
+        const int k0 = kc * p.ks_per_chunk, k1 = min(p.KS, k0 + p.ks_per_chunk);
+        for (int ks = k0; ks < k1; ++ks, ++kg) {
+          const int s = kg % C::kStages, u = kg / C::kStages;
+          if (u > 0 && !mbar_wait(sfree(s), (u - 1) & 1, g, 1u)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(full(s), C::kABytes + C::kBBytes);
+          tma_load_2d(smem_u32(stage_a(s)), &map_a, full(s), ks * kBK, mt * kBM);
+          tma_load_2d(smem_u32(stage_b(s)), &map_b, full(s), ks * kBK, 0);
+          ++issued;
+        }
+      }
+      if (*abort_flag) {
+        for (int k = max(0, issued - C::kStages); k < issued; ++k) {
+          const uint64_t t0 = global_ns();
+          while (!mbar_try_wait(full(k % C::kStages), (k / C::kStages) & 1))
+            if (global_ns() - t0 > p.limit_ns) break;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = umma_idesc_bf16(kBM, n_mma);
+      int kg = 0, it = 0, done = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
+        const int kc = item / p.MT, buf = it & 1;
+        const int k0 = kc * p.ks_per_chunk, k1 = min(p.KS, k0 + p.ks_per_chunk);
+        // the epilogue must have drained this accumulator buffer (used two items ago)
+        if (it >= 2 && !mbar_wait(tempty(buf), ((it >> 1) - 1) & 1, g, 64u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int ks = k0; ks < k1; ++ks, ++kg) {
+          const int s = kg % C::kStages;
+          if (!(ok = mbar_wait(full(s), (kg / C::kStages) & 1, g, 2u))) break;
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(stage_a(s)), b0 = smem_u32(stage_b(s));
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_bf16(tmem + buf * kDNB, umma_desc_sw128(a0 + kk * 32), umma_desc_sw128(b0 + kk * 32), idesc,
+                      (ks > k0 || kk) ? 1u : 0u);
+          umma_commit(sfree(s));
+        }
+        if (ok) {
+          umma_commit(tfull(buf));
+          ++done;
+        }
+      }
+      if (!ok) {
+        umma_commit(tfull(0));
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(tfull(0), ((done + 1) >> 1) & 1))
+          if (global_ns() - t0 > p.limit_ns) break;
+      }
+    }
+    __syncwarp();
+  } else {
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    int it = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+      const int mt = item % p.MT, kc = item / p.MT, buf = it & 1;
+      if (!mbar_wait(tfull(buf), (it >> 1) & 1, g, 16u) || *abort_flag) break;
+      tc_fence_after();
+      const int m = mt * kBM + r;
+      float* dst = p.part + (size_t)kc * p.T * p.M + m;
+      for (int j0 = 0; j0 < n_mma; j0 += 32) {
+        float acc[32];
+        tmem_ld32(lane_base + buf * kDNB + j0, acc);
+        if (m < p.M) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j0 + j < p.T) dst[(size_t)(j0 + j) * p.M] = acc[j];
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty(buf));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+// out[t][m] = sum over chunks (in order) of part[kc][t][m]; rows m < split
+// to out_f32[t*split + m], the others to bf16 out_bf16[t*(M-split) + m-split].
+__global__ void splitk_reduce_kernel(const float* __restrict__ part, int nkc, int T, int M, int split,
+                                     float* __restrict__ out_f32, uint16_t* __restrict__ out_bf16) {
+  const long long total = (long long)T * M;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    float v = 0.f;
+    for (int kc = 0; kc < nkc; ++kc) v += part[(size_t)kc * total + i];
+    const int t = (int)(i / M), m = (int)(i - (long long)t * M);
+    if (m < split)
+      out_f32[(size_t)t * split + m] = v;
+    else
+      out_bf16[(size_t)t * (M - split) + (m - split)] = f32_to_bf16(v);
+  }
+}
+
 // ------------------------------------------------------------------ helpers
 // Gather the latent rows into slot order: lat_perm[s] = lat[perm[s] / K].
 __global__ void gather_rows_kernel(const uint16_t* __restrict__ lat, const int* __restrict__ perm, int TK, int K,
@@ -732,15 +903,38 @@ struct UmmaWs {
   int4* tiles;
   int* count;
   uint16_t* lat_perm;
+  float* part;
 };
 
+constexpr int kMaxChunks = 16;  // split-K chunks of the small-T dense GEMM
+
+// Workspace carve-up; sizes are bounds for any T <= max_tokens:
+//   tiles: at most T*K/kSNB + (experts with work) entries (kSNB is the
+//          smallest tile height used), lat_perm: T*K rows of L,
+//   part : kMaxChunks * kDNB * max(E + L, H) fp32 partial sums.
+struct WsLayout {
+  size_t tiles_off, count_off, lat_off, part_off, total;
+};
+WsLayout ws_layout(const Dims& d, int max_tokens) {
+  auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+  const size_t max_tiles = (size_t)max_tokens * d.K / kSNB + d.E + 1;
+  WsLayout l;
+  l.tiles_off = 0;
+  l.count_off = up(max_tiles * sizeof(int4));
+  l.lat_off = l.count_off + 256;
+  l.part_off = l.lat_off + up((size_t)max_tokens * d.K * d.L * 2);
+  l.total = l.part_off + up((size_t)kMaxChunks * kDNB * std::max(d.E + d.L, d.H) * sizeof(float));
+  return l;
+}
+
 UmmaWs ws_view(const UmmaPlan& p, const Dims& d, int max_tokens) {
-  const size_t max_tiles = (size_t)max_tokens * d.K / kBNMax + d.E + 1;
+  const WsLayout l = ws_layout(d, max_tokens);
   uint8_t* b = static_cast<uint8_t*>(p.ws);
   UmmaWs w;
-  w.tiles = reinterpret_cast<int4*>(b);
-  w.count = reinterpret_cast<int*>(b + max_tiles * sizeof(int4));
-  w.lat_perm = reinterpret_cast<uint16_t*>(b + ((max_tiles * sizeof(int4) + 16 + 255) / 256) * 256);
+  w.tiles = reinterpret_cast<int4*>(b + l.tiles_off);
+  w.count = reinterpret_cast<int*>(b + l.count_off);
+  w.lat_perm = reinterpret_cast<uint16_t*>(b + l.lat_off);
+  w.part = reinterpret_cast<float*>(b + l.part_off);
   return w;
 }
 
@@ -755,7 +949,10 @@ cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const Para
 }  // namespace
 
 cudaError_t prepare_umma_kernels() {
-  cudaError_t e0 = cudaFuncSetAttribute(umma_stream_kernel<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e0 = cudaFuncSetAttribute(umma_dense_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        DCfg::kSmem);
+  if (e0 != cudaSuccess) return e0;
+  e0 = cudaFuncSetAttribute(umma_stream_kernel<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         SCfg<GATEUP>::kSmem);
   if (e0 == cudaSuccess)
     e0 = cudaFuncSetAttribute(umma_stream_kernel<DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -774,8 +971,8 @@ cudaError_t prepare_umma_kernels() {
 UmmaPlan umma_plan(const Dims& d, int max_tokens) {
   UmmaPlan p;
   p.max_tokens = max_tokens;
-  const size_t max_tiles = (size_t)max_tokens * d.K / kBNMax + d.E + 1;
-  p.ws_bytes = ((max_tiles * sizeof(int4) + 16 + 255) / 256) * 256 + (size_t)max_tokens * d.K * d.L * 2;
+  p.dims = d;
+  p.ws_bytes = ws_layout(d, max_tokens).total;
   p.enabled = true;
   p.min_tokens = 128;
   return p;
@@ -812,7 +1009,7 @@ cudaError_t umma_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8
                          const Dims& d, cudaStream_t s) {
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
-  UmmaWs ws = ws_view(p, d, p.max_tokens);
+  UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
   const int max_tiles = TK / kBNMax + std::min(d.E, TK) + 1;
   build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, kBNMax, ws.tiles, ws.count);
   gather_rows_kernel<<<152 * 8, 256, 0, s>>>(w.lat, w.perm, TK, d.K, d.L, ws.lat_perm);
@@ -852,7 +1049,7 @@ cudaError_t umma_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8
 cudaError_t umma_stream_prepare(const UmmaPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s) {
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
-  UmmaWs ws = ws_view(p, d, p.max_tokens);
+  UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
   build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, kSNB, ws.tiles, ws.count);
   gather_rows_kernel<<<152 * 2, 256, 0, s>>>(w.lat, w.perm, TK, d.K, d.L, ws.lat_perm);
   return cudaGetLastError();
@@ -872,7 +1069,7 @@ cudaError_t umma_stream_gateup(const UmmaPlan& p, const uint8_t* gu_tiles, const
                                cudaStream_t s) {
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
-  UmmaWs ws = ws_view(p, d, p.max_tokens);
+  UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
   CUtensorMap mb;
   if (!make_map(&mb, ws.lat_perm, TK, d.L, kSNB)) return cudaErrorInvalidValue;
   Params g = stream_params(p, d, ws);
@@ -890,7 +1087,7 @@ cudaError_t umma_stream_down(const UmmaPlan& p, const uint8_t* d_tiles, const Wo
                              cudaStream_t s) {
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
-  UmmaWs ws = ws_view(p, d, p.max_tokens);
+  UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
   CUtensorMap mb;
   if (!make_map(&mb, w.h, TK, d.I, kSNB)) return cudaErrorInvalidValue;
   Params g = stream_params(p, d, ws);
@@ -901,6 +1098,36 @@ cudaError_t umma_stream_down(const UmmaPlan& p, const uint8_t* d_tiles, const Wo
   g.out_f32 = w.o;
   g.ld_out = d.L;
   umma_stream_kernel<DOWN><<<2 * p.num_sms, kSThreads, SCfg<DOWN>::kSmem, s>>>(mb, g);
+  return cudaGetLastError();
+}
+
+// Small-T dense GEMM (T <= kDNB): split-K streaming kernel + ordered reduce.
+cudaError_t umma_dense_small(const UmmaPlan& p, const uint16_t* W, int M, int K, const uint16_t* X, int T, int split,
+                             float* out_f32, uint16_t* out_bf16, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  if (T > kDNB) return cudaErrorInvalidValue;
+  UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, W, M, K, kBM) || !make_map(&mb, X, T, K, kDNB)) return cudaErrorInvalidValue;
+  DenseStreamParams q{};
+  q.MT = (M + kBM - 1) / kBM;
+  q.KS = K / kBK;
+  const int want = (2 * p.num_sms + q.MT - 1) / q.MT;
+  const int nkc0 = std::max(1, std::min({want, q.KS, kMaxChunks}));
+  q.ks_per_chunk = (q.KS + nkc0 - 1) / nkc0;
+  q.nkc = (q.KS + q.ks_per_chunk - 1) / q.ks_per_chunk;
+  q.M = M;
+  q.T = T;
+  q.part = ws.part;
+  q.status = p.status;
+  q.limit_ns = p.limit_ns;
+  const int items = q.MT * q.nkc;
+  umma_dense_stream_kernel<<<std::min(items, 2 * p.num_sms), kSThreads, DCfg::kSmem, s>>>(ma, mb, q);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long total = (long long)T * M;
+  const int blocks = (int)std::min<long long>((total + 255) / 256, 4LL * p.num_sms);
+  splitk_reduce_kernel<<<blocks, 256, 0, s>>>(ws.part, q.nkc, T, M, split, out_f32, out_bf16);
   return cudaGetLastError();
 }
 

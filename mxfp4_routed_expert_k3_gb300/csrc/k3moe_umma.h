@@ -18,6 +18,7 @@ struct UmmaPlan {
   void* ws = nullptr;
   unsigned* status = nullptr;  // device status word (bounded waits report here)
   int num_sms = 152;
+  Dims dims{};  // the context's layer dimensions (workspace layout)
   uint64_t limit_ns = 2000000000ull;
 };
 
@@ -27,6 +28,9 @@ bool umma_path_enabled(const UmmaPlan& p, const Dims& d, int T);
 cudaError_t umma_dense(const UmmaPlan& p, const uint16_t* W, int M, int K, const uint16_t* X, int T, int split,
                        float* out_f32, uint16_t* out_bf16, cudaStream_t s);
 int umma_dense_launches();
+// T <= 64: split-K streaming dense GEMM over all SMs + ordered reduction (2 launches)
+cudaError_t umma_dense_small(const UmmaPlan& p, const uint16_t* W, int M, int K, const uint16_t* X, int T, int split,
+                             float* out_f32, uint16_t* out_bf16, cudaStream_t s);
 cudaError_t umma_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8_t* d_tiles, const Work& w, int T,
                          const Dims& d, cudaStream_t s);
 int umma_expert_launches();

@@ -70,7 +70,8 @@ def lib():
         L.k3moe_profile_name.argtypes = [vp, i32]
         L.k3moe_profile_name.restype = C.c_char_p
         for f in ("k3moe_create", "k3moe_load_weights", "k3moe_forward", "k3moe_forward_host", "k3moe_status",
-                  "k3moe_mxfp4_dequant", "k3moe_route", "k3moe_fetch", "k3moe_query", "k3moe_profile",
+                  "k3moe_mxfp4_dequant", "k3moe_route", "k3moe_fetch", "k3moe_query",
+                  "k3moe_profile",
                   "k3moe_profile_read"):
             getattr(L, f).restype = C.c_int
         _lib = L

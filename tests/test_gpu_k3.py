@@ -10,7 +10,7 @@ from mxfp4_routed_expert_k3_gb300 import k3moe, synth
 from mxfp4_routed_expert_k3_gb300.dims import K3
 from oracle import oracle as ora
 
-from _cases import assert_routing_equal, assert_y_close, gapped_tokens, y_metrics
+from _cases import assert_routing_equal, assert_y_close, bf16_f64, gapped_tokens, y_metrics
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -68,7 +68,18 @@ def _sampled(layer, w, x, n_sample, seed, label):
     assert_routing_equal(idx, wts, idx_ref, w_ref, label)
     sample = np.sort(np.random.default_rng(seed).choice(T, n_sample, replace=False))
     sample[-1] = T - 1  # always include the ragged tail
-    ref = ora.forward(K3, w, np.ascontiguousarray(x[sample]))
+    ref = ora.forward(K3, w, np.ascontiguousarray(x[sample]), probes=True)
+    # per-step diagnostics on the sampled tokens
+    logits = layer.fetch("logits", (T, K3.n_experts), np.float32)[sample].astype(np.float64)
+    lat = bf16_f64(layer.fetch("lat", (T, K3.latent), np.uint16)[sample])
+    n = bf16_f64(layer.fetch("n", (T, K3.latent), np.uint16)[sample])
+    dl = np.abs(logits - ref["logits"])
+    diag = {"logits_max_abs": float(dl.max()), "logits_rms": float(np.sqrt(np.mean(ref["logits"] ** 2))),
+            "lat_identical": float(np.mean(lat == bf16_f64(ref["lat"]))),
+            "lat_max_rel": float(np.max(np.abs(lat - bf16_f64(ref["lat"])) / np.maximum(np.abs(bf16_f64(ref["lat"])), 1e-3))),
+            "n_identical": float(np.mean(n == bf16_f64(ref["n"]))),
+            "n_rel_rms": float(np.sqrt(np.mean((n - bf16_f64(ref["n"])) ** 2) / np.mean(bf16_f64(ref["n"]) ** 2)))}
+    print(label, "steps", diag)
     m = assert_y_close(y[sample], ref["y"], label)
     # properties that hold for every token
     yf = (y.astype(np.uint32) << 16).view(np.float32)

@@ -77,7 +77,10 @@ def test_tiny_layer_matches_oracle(tiny, T):
         h_ref = bf16_round(situ(xl @ W1.T, xl @ W3.T))
         hg = bf16_f64(h[s_of])
         assert np.mean(hg == h_ref) > 0.995, e
-        assert np.all(np.abs(hg - h_ref) <= bf16_ulp(h_ref) + 1e-30), e
+        # one bf16 ulp, plus an fp32-accumulation floor: where g or u cancel to
+        # near zero, h is small and fp32 vs fp64 sums differ by several of its ulps
+        floor = 1e-4 * np.sqrt(np.mean(h_ref ** 2))
+        assert np.all(np.abs(hg - h_ref) <= bf16_ulp(h_ref) + floor), e
         o_ref = hg @ W2.T
         assert np.max(np.abs(o[s_of] - o_ref)) <= 2e-5 * np.sqrt(np.mean(o_ref ** 2)) + 1e-6, e
     n = layer.fetch("n", (T, d.latent), np.uint16)
