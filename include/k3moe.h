@@ -173,6 +173,25 @@ int k3moe_route(const void* x, int T, const void* router_w, const float* bias, i
                 int norm_topk, float routed_scaling, float* logits, int32_t* topk_idx, float* topk_w,
                 void* cuda_stream);
 
+/* Router step that allocates nothing, for callers that must not allocate
+ * device memory when they route: code running while a CUDA graph is being
+ * captured, code living inside another framework's memory pool or under a
+ * fixed memory budget, services that forbid allocation after start-up.  (The
+ * pages have no counterpart; this is a property of this library's API.)
+ * Same inputs, outputs and results as k3moe_route, but the [T, E] fp32
+ * logits scratch is a file-scope __device__ array of 131072 floats (512 KiB)
+ * that every GPU loading the library holds until the process exits.
+ * T * E > 131072 returns K3MOE_EINVAL.  The first call on a device looks up
+ * the array's device address (with that device current, once per device);
+ * make that first call before any stream capture.  Calls never allocate.
+ * All calls share the one array and it keeps the last call's contents
+ * (nothing here needs it zeroed): calls that overlap on the GPU, from any
+ * stream or thread, race on it.  Errors are reported by
+ * k3moe_last_error(NULL) on the calling thread. */
+int k3moe_route_noalloc(const void* x, int T, const void* router_w, const float* bias, int E, int H, int K,
+                        int norm_topk, float routed_scaling, int32_t* topk_idx, float* topk_w,
+                        void* cuda_stream);
+
 /* ---- inspection (tests and tools) ---- */
 
 enum {

@@ -20,7 +20,7 @@ BUF = dict(logits=0, lat=1, counts=2, offsets=3, perm=4, slot=5, h=6, o=7, n=8, 
 Q = dict(workspace_bytes=0, weight_bytes=1, launches_last=2, path_last=3, device=4)
 EXPORTS = ["k3moe_create", "k3moe_load_weights", "k3moe_forward", "k3moe_forward_host", "k3moe_status",
            "k3moe_last_error", "k3moe_destroy", "k3moe_mxfp4_dequant", "k3moe_route", "k3moe_fetch",
-           "k3moe_query", "k3moe_profile", "k3moe_profile_read", "k3moe_profile_name"]
+           "k3moe_query", "k3moe_profile", "k3moe_profile_read", "k3moe_profile_name", "k3moe_route_noalloc"]
 
 
 class K3Error(RuntimeError):
@@ -63,6 +63,7 @@ def lib():
         L.k3moe_destroy.restype = None
         L.k3moe_mxfp4_dequant.argtypes = [vp, vp, i32, i32, vp, i32, vp]
         L.k3moe_route.argtypes = [vp, i32, vp, vp, i32, i32, i32, i32, C.c_float, vp, vp, vp, vp]
+        L.k3moe_route_noalloc.argtypes = [vp, i32, vp, vp, i32, i32, i32, i32, C.c_float, vp, vp, vp]
         L.k3moe_fetch.argtypes = [vp, i32, vp, C.c_size_t]
         L.k3moe_query.argtypes = [vp, i32, C.POINTER(C.c_longlong)]
         L.k3moe_profile.argtypes = [vp, i32]
@@ -70,7 +71,7 @@ def lib():
         L.k3moe_profile_name.argtypes = [vp, i32]
         L.k3moe_profile_name.restype = C.c_char_p
         for f in ("k3moe_create", "k3moe_load_weights", "k3moe_forward", "k3moe_forward_host", "k3moe_status",
-                  "k3moe_mxfp4_dequant", "k3moe_route", "k3moe_fetch", "k3moe_query",
+                  "k3moe_mxfp4_dequant", "k3moe_route", "k3moe_route_noalloc", "k3moe_fetch", "k3moe_query",
                   "k3moe_profile",
                   "k3moe_profile_read"):
             getattr(L, f).restype = C.c_int
