@@ -77,11 +77,11 @@ typedef struct {
   int norm_topk;   /* 1: topk_w = s / sum of the selected s; 0: topk_w = s */
   int max_tokens;  /* largest T a forward call may pass */
   int spin_timeout_ms; /* limit of any device-side wait; 0 selects 2000 ms */
-  int force_path;  /* 0: by token count (CUDA-core kernels below 128 tokens,
-                      tensor-core kernels from 128); 1: always the CUDA-core
-                      kernels; 2: always the tensor-core GEMM kernels;
-                      3: CUDA-core dense GEMVs with the streaming
-                      tensor-core expert kernels (decode-size batches) */
+  int force_path;  /* 0: by token count (T <= 64: path 3, else path 2);
+                      1: CUDA-core kernels everywhere;
+                      2: tensor-core GEMM kernels (prefill-size batches);
+                      3: streaming tensor-core kernels (decode-size batches;
+                         dense projections by split-K for T <= 64) */
 } k3moe_config;
 
 /* Host arrays in checkpoint layout, experts stacked along dim 0.  Row-major;

@@ -304,20 +304,23 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
   k3::Work& w = c->w;
   // path: 1 CUDA-core kernels, 2 tensor-core GEMMs, 3 CUDA-core dense GEMVs + streaming tensor-core experts
   int path = c->cfg.force_path;
-  if (path == 0) path = k3::umma_path_enabled(c->umma, d, T) ? 2 : 1;
+  if (path == 0) path = T <= 64 ? 3 : 2;
   const bool big = path == 2;
   c->path_last = path;
   long long n = 0;
   cudaError_t e;
   c->prof_n = 0;
-  if (c->prof && (e = cudaEventRecord(c->prof_ev[0], s)) != cudaSuccess) return cuda_fail(c, e, "profile event");
+  // external records, so that events recorded while a graph is captured are
+  // updated by every replay and readable outside the graph
+  if (c->prof && (e = cudaEventRecordWithFlags(c->prof_ev[0], s, cudaEventRecordExternal)) != cudaSuccess)
+    return cuda_fail(c, e, "profile event");
 #define K3_LAUNCH(expr, count, what)                                                    \
   do {                                                                                  \
     if ((e = (expr)) != cudaSuccess) return cuda_fail(c, e, what);                      \
     n += (count);                                                                       \
     if (c->prof && c->prof_n < k3moe_ctx::kMaxProf) {                                   \
       c->prof_name[c->prof_n] = what;                                                   \
-      if ((e = cudaEventRecord(c->prof_ev[++c->prof_n], s)) != cudaSuccess)            \
+      if ((e = cudaEventRecordWithFlags(c->prof_ev[++c->prof_n], s, cudaEventRecordExternal)) != cudaSuccess) \
         return cuda_fail(c, e, "profile event");                                        \
     }                                                                                   \
   } while (0)

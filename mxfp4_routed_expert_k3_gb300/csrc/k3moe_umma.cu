@@ -40,17 +40,25 @@ constexpr int kThreads = 192;
 
 enum Mode { DENSE = 0, GATEUP = 1, DOWN = 2 };
 
+// The tensor cores' fp32 accumulation drifts by about 2^-24 (relative) per
+// accumulation step, so a long K loop into one accumulator loses more than
+// an fp32 FMA chain.  kAcc accumulators take the K steps in turn (each sees
+// K/(16*kAcc) steps) and the epilogue adds them with round-to-nearest fp32.
 template <int MODE>
 struct Cfg {
   static constexpr int kNumA = (MODE == GATEUP) ? 2 : 1;
+  static constexpr int kBN = (MODE == DENSE) ? 128 : kBNMax;    // token rows per tile
   static constexpr int kABytes = kBM * kBK * 2;                 // 16 KB per A tile
-  static constexpr int kBBytes = kBNMax * kBK * 2;              // 24 KB
+  static constexpr int kBBytes = kBN * kBK * 2;
   static constexpr int kStageBytesRaw = (MODE == DENSE) ? 0 : kNumA * kTileBytes;
   static constexpr int kStaging = (kStageBytesRaw + 1023) / 1024 * 1024;
   static constexpr int kStageBytes = kNumA * kABytes + kBBytes + kStaging;
   static constexpr int kStages = (MODE == GATEUP) ? 3 : 4;
-  static constexpr int kTmemCols = (MODE == GATEUP) ? 512 : 256;
+  static constexpr int kAcc = (MODE == DENSE) ? 4 : (MODE == DOWN) ? 2 : 1;
+  static constexpr int kAccStride = (MODE == DENSE) ? 128 : 256;  // TMEM columns between accumulators
+  static constexpr int kTmemCols = 512;
   static constexpr int kSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+  static_assert(kNumA * kAcc * kAccStride <= kTmemCols || MODE == GATEUP, "TMEM budget");
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -307,13 +315,14 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
         if (!ok) break;
         tc_fence_after();
         const uint32_t b0 = smem_u32(stage_b(s));
+        const uint32_t acc_col = (uint32_t)((ks % C::kAcc) * C::kAccStride);
 #pragma unroll
         for (int i = 0; i < C::kNumA; ++i) {
           const uint32_t a0 = smem_u32(stage_a(s, i));
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_bf16(tmem + i * 256, umma_desc_sw128(a0 + kk * 32), umma_desc_sw128(b0 + kk * 32), idesc,
-                      (ks | kk) ? 1u : 0u);
+            umma_bf16(tmem + acc_col + i * 256, umma_desc_sw128(a0 + kk * 32), umma_desc_sw128(b0 + kk * 32), idesc,
+                      (ks >= C::kAcc || kk) ? 1u : 0u);
         }
         umma_commit(empty(s));
       }
@@ -362,9 +371,16 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
       const int m_local = quarter * 32 + lane;
       const int m = mt * kBM + m_local;
       const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+      const int n_acc = min(C::kAcc, p.KS);
       for (int j0 = 0; j0 < n_mma; j0 += 32) {
         float acc[32];
         tmem_ld32(lane_addr + j0, acc);
+        for (int a = 1; a < n_acc; ++a) {
+          float part[32];
+          tmem_ld32(lane_addr + a * C::kAccStride + j0, part);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[j] += part[j];
+        }
         if (MODE == GATEUP) {
           float up[32];
           tmem_ld32(lane_addr + 256 + j0, up);
@@ -987,8 +1003,9 @@ cudaError_t umma_dense(const UmmaPlan& p, const uint16_t* W, int M, int K, const
                        float* out_f32, uint16_t* out_bf16, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   CUtensorMap ma, mb;
-  if (!make_map(&ma, W, M, K, kBM) || !make_map(&mb, X, T, K, kBNMax)) return cudaErrorInvalidValue;
-  const int ntile = (T + kBNMax - 1) / kBNMax;
+  constexpr int BN = Cfg<DENSE>::kBN;
+  if (!make_map(&ma, W, M, K, kBM) || !make_map(&mb, X, T, K, BN)) return cudaErrorInvalidValue;
+  const int ntile = (T + BN - 1) / BN;
   const int per = (T + ntile - 1) / ntile;
   Params prm{};
   prm.MT = (M + kBM - 1) / kBM;

@@ -15,7 +15,11 @@ GAP = 1e-3          # forced margin between the K-th and (K+1)-th router key
 REL_RMS_TOL = 1e-2  # ||y - ref|| / ||ref||
 MEAN_REL_TOL = 2e-3  # mean|y - ref| / mean|ref|
 MAX_TOL = 1e-2      # |y_i - ref_i| <= MAX_TOL * rms(ref) + one bf16 ulp of ref_i
-W_RTOL = 2e-6       # routing weights: a few fp32 ulps (sigmoid, sum, division)
+# routing weights: w = s / sum(s) moves by about (1 - s) * |d logit| for a
+# logit error d logit.  fp32 sums on CUDA cores keep |d logit| ~ 1e-6; the
+# tensor cores' fp32 accumulation drifts by up to ~K/16 * 2^-24 relative
+# (K = 7168: ~3e-5, measured 3.4e-5), hence 5e-5.
+W_RTOL = 5e-5
 
 
 def gapped_tokens(d: LayerDims, w: dict, seed: int, T: int, max_attempts: int = 40) -> np.ndarray:

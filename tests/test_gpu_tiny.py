@@ -84,7 +84,11 @@ def test_tiny_layer_matches_oracle(tiny, T):
         o_ref = hg @ W2.T
         assert np.max(np.abs(o[s_of] - o_ref)) <= 2e-5 * np.sqrt(np.mean(o_ref ** 2)) + 1e-6, e
     n = layer.fetch("n", (T, d.latent), np.uint16)
-    assert np.mean(bf16_f64(n) == bf16_f64(ref["n"])) > 0.98
+    # n is bf16 after two bf16 roundings upstream (lat, h): one-ulp flips there
+    # move c by ~1e-4 relative and flip a few percent of n's roundings
+    nn, nr = bf16_f64(n), bf16_f64(ref["n"])
+    assert np.mean(nn == nr) > 0.95
+    assert np.sqrt(np.mean((nn - nr) ** 2) / np.mean(nr ** 2)) < 2e-3
     m = assert_y_close(y, ref["y"], f"T={T}")
     print(f"T={T}", m)
 
