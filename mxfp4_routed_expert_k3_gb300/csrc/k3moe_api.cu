@@ -310,17 +310,24 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
   long long n = 0;
   cudaError_t e;
   c->prof_n = 0;
-  // external records, so that events recorded while a graph is captured are
-  // updated by every replay and readable outside the graph
-  if (c->prof && (e = cudaEventRecordWithFlags(c->prof_ev[0], s, cudaEventRecordExternal)) != cudaSuccess)
-    return cuda_fail(c, e, "profile event");
+  // While a graph is being captured, event records must be "external" to be
+  // updated by every replay and readable outside the graph; outside capture
+  // that flag is not allowed.
+  unsigned ev_flags = cudaEventRecordDefault;
+  if (c->prof) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if ((e = cudaStreamIsCapturing(s, &cs)) != cudaSuccess) return cuda_fail(c, e, "cudaStreamIsCapturing");
+    if (cs == cudaStreamCaptureStatusActive) ev_flags = cudaEventRecordExternal;
+    if ((e = cudaEventRecordWithFlags(c->prof_ev[0], s, ev_flags)) != cudaSuccess)
+      return cuda_fail(c, e, "profile event");
+  }
 #define K3_LAUNCH(expr, count, what)                                                    \
   do {                                                                                  \
     if ((e = (expr)) != cudaSuccess) return cuda_fail(c, e, what);                      \
     n += (count);                                                                       \
     if (c->prof && c->prof_n < k3moe_ctx::kMaxProf) {                                   \
       c->prof_name[c->prof_n] = what;                                                   \
-      if ((e = cudaEventRecordWithFlags(c->prof_ev[++c->prof_n], s, cudaEventRecordExternal)) != cudaSuccess) \
+      if ((e = cudaEventRecordWithFlags(c->prof_ev[++c->prof_n], s, ev_flags)) != cudaSuccess) \
         return cuda_fail(c, e, "profile event");                                        \
     }                                                                                   \
   } while (0)
@@ -329,20 +336,34 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
               k3::umma_dense_launches(), "router + down_proj (tensor cores)");
   } else if (path == 3 && T <= 64) {
     K3_LAUNCH(k3::umma_dense_small(c->umma, c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, d.E, w.logits, w.lat, s),
-              2, "router + down_proj");
+              1, "router + down_proj");
   } else {
     K3_LAUNCH(k3::launch_dense_gemv(c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, d.E, w.logits, w.lat, s), 1,
               "router + down_proj");
   }
-  K3_LAUNCH(k3::launch_topk(w.logits, T, d.E, d.E, c->bias, d.K, d.norm_topk, d.rsf, idx, wts, s), 1, "top-k");
-  K3_LAUNCH(k3::launch_permute(idx, T, d.K, d.E, w.blk_hist, w.counts, w.offsets, w.active, w.perm, w.slot, s), 3,
-            "permute");
+  const bool fused_route = path == 3 && T * d.K <= 1024;
+  if (fused_route) {
+    int4* tiles;
+    int* tile_count;
+    int bn;
+    k3::umma_tile_list(c->umma, &tiles, &tile_count, &bn);
+    K3_LAUNCH(k3::launch_route_small(w.logits, T, d.E, c->bias, d.K, d.norm_topk, d.rsf, idx, wts, w.counts,
+                                     w.offsets, w.active, w.perm, w.slot, bn, tiles, tile_count, s),
+              1, "top-k + permute");
+  } else {
+    K3_LAUNCH(k3::launch_topk(w.logits, T, d.E, d.E, c->bias, d.K, d.norm_topk, d.rsf, idx, wts, s), 1, "top-k");
+    K3_LAUNCH(k3::launch_permute(idx, T, d.K, d.E, w.blk_hist, w.counts, w.offsets, w.active, w.perm, w.slot, s), 3,
+              "permute");
+  }
   const int max_active = std::min(d.E, T * d.K);
   if (big) {
     K3_LAUNCH(k3::umma_experts(c->umma, c->gu_tiles, c->d_tiles, w, T, d, s), k3::umma_expert_launches(),
               "experts (tensor cores)");
   } else if (path == 3) {
-    K3_LAUNCH(k3::umma_stream_prepare(c->umma, w, T, d, s), 2, "tile list + gather");
+    if (fused_route)
+      K3_LAUNCH(k3::umma_stream_gather(c->umma, w, T, d, s), 1, "gather");
+    else
+      K3_LAUNCH(k3::umma_stream_prepare(c->umma, w, T, d, s), 2, "tile list + gather");
     K3_LAUNCH(k3::umma_stream_gateup(c->umma, c->gu_tiles, w, T, d, s), 1, "gate/up");
     K3_LAUNCH(k3::umma_stream_down(c->umma, c->d_tiles, w, T, d, s), 1, "down");
   } else {
@@ -355,7 +376,7 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
     K3_LAUNCH(k3::umma_dense(c->umma, c->wu, d.H, d.L, w.n, T, 0, nullptr, (uint16_t*)y, s),
               k3::umma_dense_launches(), "up_proj (tensor cores)");
   } else if (path == 3 && T <= 64) {
-    K3_LAUNCH(k3::umma_dense_small(c->umma, c->wu, d.H, d.L, w.n, T, 0, nullptr, (uint16_t*)y, s), 2, "up_proj");
+    K3_LAUNCH(k3::umma_dense_small(c->umma, c->wu, d.H, d.L, w.n, T, 0, nullptr, (uint16_t*)y, s), 1, "up_proj");
   } else {
     K3_LAUNCH(k3::launch_dense_gemv(c->wu, d.H, d.L, w.n, T, 0, nullptr, (uint16_t*)y, s), 1, "up_proj");
   }

@@ -121,31 +121,30 @@ cudaError_t launch_dense_gemv(const uint16_t* W, int M, int K, const uint16_t* X
 //   are taken one at a time, ties to the lower expert id; weights from the
 //   unbiased s, divided by their sum when norm_topk, times rsf.
 // =====================================================================
+// One warp selects the K experts of one token from its fp32 logits row and
+// writes idx[0..K) and w[0..K) (ties to the lower id; weights summed in k
+// order for a fixed rounding sequence).
 template <int EPL>
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int T, int E, int ld,
-                                                   const float* __restrict__ bias, int K, int norm_topk, float rsf,
-                                                   int32_t* __restrict__ idx, float* __restrict__ w) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
-  float key[EPL], sc[EPL];
+__device__ __forceinline__ void topk_warp(const float* __restrict__ logit_row, int E,
+                                          const float* __restrict__ bias, int K, int norm_topk, float rsf,
+                                          int32_t* __restrict__ idx, float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  float key[EPL];
   unsigned long long avail = 0;
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
     if (e < E) {
-      const float z = logits[(size_t)t * ld + e];
-      sc[i] = 1.0f / (1.0f + expf(-z));
-      key[i] = sc[i] + bias[e];
+      const float s = 1.0f / (1.0f + expf(-logit_row[e]));
+      key[i] = s + bias[e];
       avail |= 1ull << i;
     } else {
-      sc[i] = 0.f;
       key[i] = -INFINITY;
     }
   }
   float my_s = 0.f;
   for (int k = 0; k < K; ++k) {
-    float bk = -INFINITY, bs = 0.f;
+    float bk = -INFINITY;
     int be = INT_MAX;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
@@ -154,28 +153,34 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
       if (key[i] > bk || (key[i] == bk && e < be)) {
         bk = key[i];
         be = e;
-        bs = sc[i];
       }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       const float ok = __shfl_xor_sync(0xFFFFFFFFu, bk, off);
       const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
-      const float os = __shfl_xor_sync(0xFFFFFFFFu, bs, off);
       if (ok > bk || (ok == bk && oe < be)) {
         bk = ok;
         be = oe;
-        bs = os;
       }
     }
     if (be != INT_MAX && (be & 31) == lane) avail &= ~(1ull << (be >> 5));
-    if (lane == k) my_s = bs;
-    if (lane == 0) idx[(size_t)t * K + k] = be;
+    // the selected expert's score, recomputed with the same expression
+    if (lane == k) my_s = be < E ? 1.0f / (1.0f + expf(-logit_row[be])) : 0.f;
+    if (lane == 0) idx[k] = be;
   }
   float sum = 0.f;
-  // sum in k order (lane order) for a fixed, documented rounding sequence
   for (int k = 0; k < K; ++k) sum += __shfl_sync(0xFFFFFFFFu, my_s, k);
-  if (lane < K) w[(size_t)t * K + lane] = (norm_topk ? my_s / sum : my_s) * rsf;
+  if (lane < K) w[lane] = (norm_topk ? my_s / sum : my_s) * rsf;
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int T, int E, int ld,
+                                                   const float* __restrict__ bias, int K, int norm_topk, float rsf,
+                                                   int32_t* __restrict__ idx, float* __restrict__ w) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  topk_warp<EPL>(logits + (size_t)t * ld, E, bias, K, norm_topk, rsf, idx + (size_t)t * K, w + (size_t)t * K);
 }
 
 cudaError_t launch_topk(const float* logits, int T, int E, int ld, const float* bias, int K, int norm_topk,
@@ -317,6 +322,122 @@ cudaError_t launch_permute(const int32_t* idx, int T, int K, int E, int* blk_his
   perm_hist_kernel<<<nblk, kPermChunk, sm, s>>>(idx, TK, E, blk_hist);
   perm_scan_kernel<<<1, 1024, 0, s>>>(blk_hist, nblk, E, TK, counts, offsets, active);
   perm_scatter_kernel<<<nblk, kPermChunk, sm, s>>>(idx, TK, E, blk_hist, offsets, perm, slot);
+  return cudaGetLastError();
+}
+
+// =====================================================================
+// Routing for small batches (T*K <= 1024) in ONE CTA: top-K per token, the
+// per-expert histogram, offsets, active list, the stable slot order and its
+// inverse (same results as topk_kernel + the three permutation kernels), and
+// the tile list of the streaming expert kernels (tiles of at most bn_max
+// slots per expert: {expert, first slot, rows, rows rounded up to 16}).
+// =====================================================================
+template <int EPL>
+__global__ void __launch_bounds__(1024) route_small_kernel(const float* __restrict__ logits, int T, int E,
+                                                           const float* __restrict__ bias, int K, int norm_topk,
+                                                           float rsf, int32_t* __restrict__ idx,
+                                                           float* __restrict__ w, int* __restrict__ counts,
+                                                           int* __restrict__ offsets, int* __restrict__ active,
+                                                           int* __restrict__ perm, int* __restrict__ slot,
+                                                           int bn_max, int4* __restrict__ tiles,
+                                                           int* __restrict__ tile_count) {
+  __shared__ int sidx[1024];
+  __shared__ int hist[2048];
+  __shared__ int base[2048];
+  __shared__ int warp_tot[32];
+  __shared__ int total_s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int TK = T * K;
+  for (int e = threadIdx.x; e < E; e += 1024) hist[e] = 0;
+  // top-K, one warp per token
+  for (int t = warp; t < T; t += 32) {
+    topk_warp<EPL>(logits + (size_t)t * E, E, bias, K, norm_topk, rsf, idx + (size_t)t * K, w + (size_t)t * K);
+  }
+  __syncthreads();  // idx written by lane 0 of each warp (global memory, same CTA)
+  const int a = threadIdx.x;
+  const int e_a = a < TK ? idx[a] : -1;
+  if (a < TK) sidx[a] = e_a;
+  __syncthreads();
+  if (a < TK) atomicAdd(&hist[e_a], 1);
+  __syncthreads();
+  // offsets and active list (experts in chunks of 1024)
+  int carry_off = 0, carry_act = 0;
+  for (int e0 = 0; e0 < E; e0 += 1024) {
+    const int e = e0 + threadIdx.x;
+    const int c = e < E ? hist[e] : 0;
+    const int ex = block_exclusive_scan(c, warp_tot, &total_s);
+    if (e < E) {
+      base[e] = carry_off + ex;
+      counts[e] = c;
+      offsets[e] = carry_off + ex;
+    }
+    carry_off += total_s;
+    const int flag = c > 0 ? 1 : 0;
+    const int ax = block_exclusive_scan(flag, warp_tot, &total_s);
+    if (flag) active[1 + carry_act + ax] = e;
+    carry_act += total_s;
+  }
+  if (threadIdx.x == 0) {
+    offsets[E] = TK;
+    active[0] = carry_act;
+  }
+  __syncthreads();
+  // stable scatter: rank among earlier assignments of the same expert
+  const unsigned peers = __match_any_sync(0xFFFFFFFFu, e_a);
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  const bool leader = (__ffs(peers) - 1) == lane;
+  for (int i = threadIdx.x; i < E; i += 1024) hist[i] = 0;  // reused as running counters
+  __syncthreads();
+  int before = 0;
+  for (int wv = 0; wv < 32; ++wv) {
+    if (warp == wv && a < TK) {
+      before = hist[e_a];
+      __syncwarp(peers);
+      if (leader) hist[e_a] = before + __popc(peers);
+    }
+    __syncthreads();
+  }
+  if (a < TK) {
+    const int sl = base[e_a] + before + rank;
+    perm[sl] = a;
+    slot[a] = sl;
+  }
+  // tile list over the active experts (at most TK of them)
+  const int n_act = carry_act;
+  int nsub = 0, e_t = 0, c_t = 0;
+  if (threadIdx.x < n_act) {
+    e_t = active[1 + threadIdx.x];
+    c_t = offsets[e_t + 1] - offsets[e_t];
+    nsub = (c_t + bn_max - 1) / bn_max;
+  }
+  __syncthreads();
+  const int tb = block_exclusive_scan(nsub, warp_tot, &total_s);
+  if (nsub > 0) {
+    const int per = (c_t + nsub - 1) / nsub;
+    const int tn = (per + 15) & ~15;
+    for (int j = 0; j < nsub; ++j) {
+      const int r0 = j * tn;
+      const int rows = min(tn, c_t - r0);
+      tiles[tb + j] = make_int4(e_t, base[e_t] + r0, rows, (rows + 15) & ~15);
+    }
+  }
+  if (threadIdx.x == 0) *tile_count = total_s;
+}
+
+cudaError_t launch_route_small(const float* logits, int T, int E, const float* bias, int K, int norm_topk, float rsf,
+                               int32_t* idx, float* w, int* counts, int* offsets, int* active, int* perm, int* slot,
+                               int bn_max, int4* tiles, int* tile_count, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  if (T * K > 1024 || E > 2048) return cudaErrorInvalidValue;
+  if (E <= 32 * 8)
+    route_small_kernel<8><<<1, 1024, 0, s>>>(logits, T, E, bias, K, norm_topk, rsf, idx, w, counts, offsets, active,
+                                             perm, slot, bn_max, tiles, tile_count);
+  else if (E <= 32 * 32)
+    route_small_kernel<32><<<1, 1024, 0, s>>>(logits, T, E, bias, K, norm_topk, rsf, idx, w, counts, offsets, active,
+                                              perm, slot, bn_max, tiles, tile_count);
+  else
+    route_small_kernel<64><<<1, 1024, 0, s>>>(logits, T, E, bias, K, norm_topk, rsf, idx, w, counts, offsets, active,
+                                              perm, slot, bn_max, tiles, tile_count);
   return cudaGetLastError();
 }
 

@@ -46,6 +46,10 @@ cudaError_t launch_gateup_gemv(const uint8_t* gu_tiles, const uint16_t* lat, con
 cudaError_t launch_down_gemv(const uint8_t* d_tiles, const uint16_t* h, const int* active, const int* offsets,
                              int max_active, const Dims& d, float* o, cudaStream_t s);
 cudaError_t prepare_decode_kernels(const Dims& d);
+// T*K <= 1024: top-K + permutation + streaming tile list in one CTA
+cudaError_t launch_route_small(const float* logits, int T, int E, const float* bias, int K, int norm_topk, float rsf,
+                               int32_t* idx, float* w, int* counts, int* offsets, int* active, int* perm, int* slot,
+                               int bn_max, int4* tiles, int* tile_count, cudaStream_t s);
 cudaError_t launch_combine_rmsnorm(const float* o, const int* slot, const float* topk_w, const uint16_t* gamma,
                                    int T, const Dims& d, uint16_t* n, cudaStream_t s);
 cudaError_t launch_relayout(const uint8_t* packed, const uint8_t* scale, int n_mat, int rows, int cols,

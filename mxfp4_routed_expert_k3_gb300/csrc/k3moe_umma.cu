@@ -434,7 +434,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
 // (k even in the low half) per 32-bit column, 8 columns per K = 16.
 // =====================================================================
 constexpr int kSNB = 32;  // max token rows per streaming tile
-constexpr int kSThreads = 192;
+// producer warp, MMA warp, two decode warpgroups (one per scale group of a K step)
+constexpr int kSThreads = 320;
+constexpr int kDThreads = 192;
 
 template <int MODE>
 struct SCfg {
@@ -462,6 +464,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t v[32]) 
       "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t v[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
 __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
                                                  uint32_t acc) {
   asm volatile(
@@ -472,7 +482,7 @@ __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tme
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kSThreads, 1) umma_stream_kernel(const __grid_constant__ CUtensorMap map_b,
+__global__ void __launch_bounds__(kSThreads, 2) umma_stream_kernel(const __grid_constant__ CUtensorMap map_b,
                                                                    const Params p) {
   using C = SCfg<MODE>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -490,7 +500,7 @@ __global__ void __launch_bounds__(kSThreads, 1) umma_stream_kernel(const __grid_
   if (threadIdx.x == 0) {
     for (int i = 0; i < NB; ++i) {
       const bool is_ready = i >= 2 * C::kStages && i < 2 * C::kStages + C::kSlots;
-      mbar_init(smem_u32(bars + i), is_ready ? 128u : 1u);
+      mbar_init(smem_u32(bars + i), is_ready ? 256u : 1u);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -581,8 +591,11 @@ __global__ void __launch_bounds__(kSThreads, 1) umma_stream_kernel(const __grid_
     }
     __syncwarp();
   } else {
-    // ================= decode to TMEM + epilogue (warps 2..5)
+    // ================= decode to TMEM (warps 2..9) + epilogue (warps 2..5)
+    // warpgroup grp decodes scale group grp (input columns 32 grp .. +31) of
+    // every K step: 16 TMEM columns per matrix.
     const int quarter = warp & 3;
+    const int grp = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;  // tile row == TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     int kg = 0, it = 0;
@@ -598,22 +611,20 @@ __global__ void __launch_bounds__(kSThreads, 1) umma_stream_kernel(const __grid_
 #pragma unroll
         for (int i = 0; i < C::kNumA; ++i) {
           const uint8_t* tl = stg + i * kTileBytes;
-          const uint4 c0 = *reinterpret_cast<const uint4*>(tl + (size_t)r * 16);
-          const uint4 c1 = *reinterpret_cast<const uint4*>(tl + (size_t)(128 + r) * 16);
-          const uint32_t sc = *reinterpret_cast<const uint16_t*>(tl + kTilePackedBytes + 2 * r);
-          const ScaleMul m0 = scale_multipliers(sc & 0xFFu), m1 = scale_multipliers(sc >> 8);
-          const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-          uint32_t v[32];
+          const uint4 c = *reinterpret_cast<const uint4*>(tl + (size_t)(grp * 128 + r) * 16);
+          const ScaleMul m = scale_multipliers(tl[kTilePackedBytes + 2 * r + grp]);
+          const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+          uint32_t v[16];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) tile_word_to_bf16(words[q], q < 4 ? m0 : m1, v + 4 * q);
-          tmem_st32(lane_base + slot_col(t) + i * 32, v);
+          for (int q = 0; q < 4; ++q) tile_word_to_bf16(words[q], m, v + 4 * q);
+          tmem_st16(lane_base + slot_col(t) + i * 32 + grp * 16, v);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         mbar_arrive(a_ready(t));
       }
-      if (!ok) break;
-      // epilogue of this item
+      if (!ok || grp != 0) continue;
+      // epilogue of this item (warpgroup 0)
       ok = mbar_wait(tmem_full, it & 1, g, 16u) && !*abort_flag;
       if (!ok) break;
       tc_fence_after();
@@ -660,13 +671,16 @@ struct DCfg {
 };
 
 struct DenseStreamParams {
-  int MT, KS, nkc, ks_per_chunk, M, T;
-  float* part;  // [nkc][T][M]
+  int MT, KS, nkc, ks_per_chunk, M, T, split;
+  float* part;     // [nkc][T][M] fp32 partial sums
+  int* counters;   // [MT][4] chunks finished per row tile and warp (zero between calls)
+  float* out_f32;  // rows m < split: out_f32[t * split + m]
+  uint16_t* out_bf16;  // rows m >= split: bf16 out_bf16[t * (M - split) + m - split]
   unsigned* status;
   uint64_t limit_ns;
 };
 
-__global__ void __launch_bounds__(kSThreads, 1) umma_dense_stream_kernel(const __grid_constant__ CUtensorMap map_a,
+__global__ void __launch_bounds__(kDThreads, 1) umma_dense_stream_kernel(const __grid_constant__ CUtensorMap map_a,
                                                                          const __grid_constant__ CUtensorMap map_b,
                                                                          const DenseStreamParams p) {
   using C = DCfg;
@@ -787,29 +801,37 @@ __global__ void __launch_bounds__(kSThreads, 1) umma_dense_stream_kernel(const _
       }
       tc_fence_before();
       mbar_arrive(tempty(buf));
+      // The last chunk to finish adds the chunks in order.  Counting is per
+      // warp (32 rows each), so no warp ever waits for another; whoever comes
+      // last does the sum.
+      __threadfence();
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) {
+        int* cnt = p.counters + mt * 4 + quarter;
+        last = (atomicAdd(cnt, 1) == p.nkc - 1) ? 1 : 0;
+        if (last) *cnt = 0;  // ready for the next call
+      }
+      last = __shfl_sync(0xFFFFFFFFu, last, 0);
+      if (last) {
+        __threadfence();
+        if (m < p.M) {
+          for (int t = 0; t < p.T; ++t) {
+            float v = 0.f;
+            for (int c = 0; c < p.nkc; ++c) v += __ldcg(p.part + ((size_t)c * p.T + t) * p.M + m);
+            if (m < p.split)
+              p.out_f32[(size_t)t * p.split + m] = v;
+            else
+              p.out_bf16[(size_t)t * (p.M - p.split) + (m - p.split)] = f32_to_bf16(v);
+          }
+        }
+      }
     }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, 128);
-}
-
-// out[t][m] = sum over chunks (in order) of part[kc][t][m]; rows m < split
-// to out_f32[t*split + m], the others to bf16 out_bf16[t*(M-split) + m-split].
-__global__ void splitk_reduce_kernel(const float* __restrict__ part, int nkc, int T, int M, int split,
-                                     float* __restrict__ out_f32, uint16_t* __restrict__ out_bf16) {
-  const long long total = (long long)T * M;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    float v = 0.f;
-    for (int kc = 0; kc < nkc; ++kc) v += part[(size_t)kc * total + i];
-    const int t = (int)(i / M), m = (int)(i - (long long)t * M);
-    if (m < split)
-      out_f32[(size_t)t * split + m] = v;
-    else
-      out_bf16[(size_t)t * (M - split) + (m - split)] = f32_to_bf16(v);
-  }
 }
 
 // ------------------------------------------------------------------ helpers
@@ -920,6 +942,7 @@ struct UmmaWs {
   int* count;
   uint16_t* lat_perm;
   float* part;
+  int* counters;
 };
 
 constexpr int kMaxChunks = 16;  // split-K chunks of the small-T dense GEMM
@@ -929,7 +952,7 @@ constexpr int kMaxChunks = 16;  // split-K chunks of the small-T dense GEMM
 //          smallest tile height used), lat_perm: T*K rows of L,
 //   part : kMaxChunks * kDNB * max(E + L, H) fp32 partial sums.
 struct WsLayout {
-  size_t tiles_off, count_off, lat_off, part_off, total;
+  size_t tiles_off, count_off, lat_off, part_off, counters_off, total;
 };
 WsLayout ws_layout(const Dims& d, int max_tokens) {
   auto up = [](size_t v) { return (v + 255) / 256 * 256; };
@@ -939,7 +962,8 @@ WsLayout ws_layout(const Dims& d, int max_tokens) {
   l.count_off = up(max_tiles * sizeof(int4));
   l.lat_off = l.count_off + 256;
   l.part_off = l.lat_off + up((size_t)max_tokens * d.K * d.L * 2);
-  l.total = l.part_off + up((size_t)kMaxChunks * kDNB * std::max(d.E + d.L, d.H) * sizeof(float));
+  l.counters_off = l.part_off + up((size_t)kMaxChunks * kDNB * std::max(d.E + d.L, d.H) * sizeof(float));
+  l.total = l.counters_off + up((size_t)(std::max(d.E + d.L, d.H) / kBM + 2) * 4 * sizeof(int));
   return l;
 }
 
@@ -951,6 +975,7 @@ UmmaWs ws_view(const UmmaPlan& p, const Dims& d, int max_tokens) {
   w.count = reinterpret_cast<int*>(b + l.count_off);
   w.lat_perm = reinterpret_cast<uint16_t*>(b + l.lat_off);
   w.part = reinterpret_cast<float*>(b + l.part_off);
+  w.counters = reinterpret_cast<int*>(b + l.counters_off);
   return w;
 }
 
@@ -1072,6 +1097,23 @@ cudaError_t umma_stream_prepare(const UmmaPlan& p, const Work& w, int T, const D
   return cudaGetLastError();
 }
 
+// Only the slot-ordered latent rows (the tile list was built by the fused
+// small-batch routing kernel).
+cudaError_t umma_stream_gather(const UmmaPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s) {
+  const int TK = T * d.K;
+  if (TK <= 0) return cudaSuccess;
+  UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
+  gather_rows_kernel<<<152 * 2, 256, 0, s>>>(w.lat, w.perm, TK, d.K, d.L, ws.lat_perm);
+  return cudaGetLastError();
+}
+
+void umma_tile_list(const UmmaPlan& p, int4** tiles, int** count, int* bn_max) {
+  UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
+  *tiles = ws.tiles;
+  *count = ws.count;
+  *bn_max = kSNB;
+}
+
 static Params stream_params(const UmmaPlan& p, const Dims& d, const UmmaWs& ws) {
   Params g{};
   g.list = TileList{ws.tiles, ws.count};
@@ -1135,16 +1177,15 @@ cudaError_t umma_dense_small(const UmmaPlan& p, const uint16_t* W, int M, int K,
   q.nkc = (q.KS + q.ks_per_chunk - 1) / q.ks_per_chunk;
   q.M = M;
   q.T = T;
+  q.split = split;
   q.part = ws.part;
+  q.counters = ws.counters;
+  q.out_f32 = out_f32;
+  q.out_bf16 = out_bf16;
   q.status = p.status;
   q.limit_ns = p.limit_ns;
   const int items = q.MT * q.nkc;
-  umma_dense_stream_kernel<<<std::min(items, 2 * p.num_sms), kSThreads, DCfg::kSmem, s>>>(ma, mb, q);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const long long total = (long long)T * M;
-  const int blocks = (int)std::min<long long>((total + 255) / 256, 4LL * p.num_sms);
-  splitk_reduce_kernel<<<blocks, 256, 0, s>>>(ws.part, q.nkc, T, M, split, out_f32, out_bf16);
+  umma_dense_stream_kernel<<<std::min(items, 2 * p.num_sms), kDThreads, DCfg::kSmem, s>>>(ma, mb, q);
   return cudaGetLastError();
 }
 

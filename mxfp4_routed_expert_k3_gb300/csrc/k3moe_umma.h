@@ -28,13 +28,17 @@ bool umma_path_enabled(const UmmaPlan& p, const Dims& d, int T);
 cudaError_t umma_dense(const UmmaPlan& p, const uint16_t* W, int M, int K, const uint16_t* X, int T, int split,
                        float* out_f32, uint16_t* out_bf16, cudaStream_t s);
 int umma_dense_launches();
-// T <= 64: split-K streaming dense GEMM over all SMs + ordered reduction (2 launches)
+// T <= 64: split-K streaming dense GEMM over all SMs; the last chunk of each
+// row tile adds the chunks in order (one launch)
 cudaError_t umma_dense_small(const UmmaPlan& p, const uint16_t* W, int M, int K, const uint16_t* X, int T, int split,
                              float* out_f32, uint16_t* out_bf16, cudaStream_t s);
 cudaError_t umma_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8_t* d_tiles, const Work& w, int T,
                          const Dims& d, cudaStream_t s);
 int umma_expert_launches();
 cudaError_t umma_stream_prepare(const UmmaPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s);
+cudaError_t umma_stream_gather(const UmmaPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s);
+// where the streaming kernels read their tile list (and the tile height)
+void umma_tile_list(const UmmaPlan& p, int4** tiles, int** count, int* bn_max);
 cudaError_t umma_stream_gateup(const UmmaPlan& p, const uint8_t* gu_tiles, const Work& w, int T, const Dims& d,
                                cudaStream_t s);
 cudaError_t umma_stream_down(const UmmaPlan& p, const uint8_t* d_tiles, const Work& w, int T, const Dims& d,
