@@ -435,6 +435,8 @@ int k3moe_status(k3moe_ctx* c) {
   if (st) {
     unsigned zero = 0;
     K3_CUDA(c, cudaMemcpy(c->w.status, &zero, 4, cudaMemcpyHostToDevice), "clear status");
+    // an aborted call can leave the split-K completion counters mid-count
+    K3_CUDA(c, k3::umma_reset_counters(c->umma), "reset counters");
     return fail(c, K3MOE_ETIMEOUT, "a device-side wait gave up (status word 0x%08x)", st);
   }
   return K3MOE_OK;

@@ -1107,6 +1107,11 @@ cudaError_t umma_stream_gather(const UmmaPlan& p, const Work& w, int T, const Di
   return cudaGetLastError();
 }
 
+cudaError_t umma_reset_counters(const UmmaPlan& p) {
+  const WsLayout l = ws_layout(p.dims, p.max_tokens);
+  return cudaMemset(static_cast<uint8_t*>(p.ws) + l.counters_off, 0, l.total - l.counters_off);
+}
+
 void umma_tile_list(const UmmaPlan& p, int4** tiles, int** count, int* bn_max) {
   UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
   *tiles = ws.tiles;

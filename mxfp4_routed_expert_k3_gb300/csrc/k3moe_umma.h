@@ -39,6 +39,7 @@ cudaError_t umma_stream_prepare(const UmmaPlan& p, const Work& w, int T, const D
 cudaError_t umma_stream_gather(const UmmaPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s);
 // where the streaming kernels read their tile list (and the tile height)
 void umma_tile_list(const UmmaPlan& p, int4** tiles, int** count, int* bn_max);
+cudaError_t umma_reset_counters(const UmmaPlan& p);
 cudaError_t umma_stream_gateup(const UmmaPlan& p, const uint8_t* gu_tiles, const Work& w, int T, const Dims& d,
                                cudaStream_t s);
 cudaError_t umma_stream_down(const UmmaPlan& p, const uint8_t* d_tiles, const Work& w, int T, const Dims& d,
