@@ -8,6 +8,7 @@
 // instructions), so they are written as streaming kernels: coalesced
 // 16-byte loads, work items sized so the grid covers the 152 SMs several
 // times, activations staged once per CTA in shared memory.
+#include <algorithm>
 #include <cfloat>
 #include <climits>
 
@@ -124,10 +125,14 @@ cudaError_t launch_dense_gemv(const uint16_t* W, int M, int K, const uint16_t* X
 // One warp selects the K experts of one token from its fp32 logits row and
 // writes idx[0..K) and w[0..K) (ties to the lower id; weights summed in k
 // order for a fixed rounding sequence).
+// `scores` (optional, E floats of shared memory for this warp) keeps the
+// sigmoid scores so that the selected ones are read back without a
+// dependent global load per selection.
 template <int EPL>
 __device__ __forceinline__ void topk_warp(const float* __restrict__ logit_row, int E,
                                           const float* __restrict__ bias, int K, int norm_topk, float rsf,
-                                          int32_t* __restrict__ idx, float* __restrict__ w) {
+                                          int32_t* __restrict__ idx, float* __restrict__ w,
+                                          float* scores = nullptr) {
   const int lane = threadIdx.x & 31;
   float key[EPL];
   unsigned long long avail = 0;
@@ -136,12 +141,14 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ logit_row, i
     const int e = lane + 32 * i;
     if (e < E) {
       const float s = 1.0f / (1.0f + expf(-logit_row[e]));
+      if (scores) scores[e] = s;
       key[i] = s + bias[e];
       avail |= 1ull << i;
     } else {
       key[i] = -INFINITY;
     }
   }
+  if (scores) __syncwarp();
   float my_s = 0.f;
   for (int k = 0; k < K; ++k) {
     float bk = -INFINITY;
@@ -166,7 +173,7 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ logit_row, i
     }
     if (be != INT_MAX && (be & 31) == lane) avail &= ~(1ull << (be >> 5));
     // the selected expert's score, recomputed with the same expression
-    if (lane == k) my_s = be < E ? 1.0f / (1.0f + expf(-logit_row[be])) : 0.f;
+    if (lane == k) my_s = be < E ? (scores ? scores[be] : 1.0f / (1.0f + expf(-logit_row[be]))) : 0.f;
     if (lane == 0) idx[k] = be;
   }
   float sum = 0.f;
@@ -341,6 +348,7 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const float* __restri
                                                            int* __restrict__ perm, int* __restrict__ slot,
                                                            int bn_max, int4* __restrict__ tiles,
                                                            int* __restrict__ tile_count) {
+  extern __shared__ float score_cache[];  // [32 warps][E]
   __shared__ int sidx[1024];
   __shared__ int hist[2048];
   __shared__ int base[2048];
@@ -351,7 +359,8 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const float* __restri
   for (int e = threadIdx.x; e < E; e += 1024) hist[e] = 0;
   // top-K, one warp per token
   for (int t = warp; t < T; t += 32) {
-    topk_warp<EPL>(logits + (size_t)t * E, E, bias, K, norm_topk, rsf, idx + (size_t)t * K, w + (size_t)t * K);
+    topk_warp<EPL>(logits + (size_t)t * E, E, bias, K, norm_topk, rsf, idx + (size_t)t * K, w + (size_t)t * K,
+                   score_cache + (size_t)warp * E);
   }
   __syncthreads();  // idx written by lane 0 of each warp (global memory, same CTA)
   const int a = threadIdx.x;
@@ -389,7 +398,8 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const float* __restri
   for (int i = threadIdx.x; i < E; i += 1024) hist[i] = 0;  // reused as running counters
   __syncthreads();
   int before = 0;
-  for (int wv = 0; wv < 32; ++wv) {
+  const int n_warps_used = (TK + 31) / 32;
+  for (int wv = 0; wv < n_warps_used; ++wv) {
     if (warp == wv && a < TK) {
       before = hist[e_a];
       __syncwarp(peers);
@@ -429,15 +439,16 @@ cudaError_t launch_route_small(const float* logits, int T, int E, const float* b
                                int bn_max, int4* tiles, int* tile_count, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   if (T * K > 1024 || E > 2048) return cudaErrorInvalidValue;
+  const size_t sm = sizeof(float) * 32 * (size_t)E;
   if (E <= 32 * 8)
-    route_small_kernel<8><<<1, 1024, 0, s>>>(logits, T, E, bias, K, norm_topk, rsf, idx, w, counts, offsets, active,
-                                             perm, slot, bn_max, tiles, tile_count);
+    route_small_kernel<8><<<1, 1024, sm, s>>>(logits, T, E, bias, K, norm_topk, rsf, idx, w, counts, offsets, active,
+                                              perm, slot, bn_max, tiles, tile_count);
   else if (E <= 32 * 32)
-    route_small_kernel<32><<<1, 1024, 0, s>>>(logits, T, E, bias, K, norm_topk, rsf, idx, w, counts, offsets, active,
-                                              perm, slot, bn_max, tiles, tile_count);
+    route_small_kernel<32><<<1, 1024, sm, s>>>(logits, T, E, bias, K, norm_topk, rsf, idx, w, counts, offsets,
+                                               active, perm, slot, bn_max, tiles, tile_count);
   else
-    route_small_kernel<64><<<1, 1024, 0, s>>>(logits, T, E, bias, K, norm_topk, rsf, idx, w, counts, offsets, active,
-                                              perm, slot, bn_max, tiles, tile_count);
+    route_small_kernel<64><<<1, 1024, sm, s>>>(logits, T, E, bias, K, norm_topk, rsf, idx, w, counts, offsets,
+                                               active, perm, slot, bn_max, tiles, tile_count);
   return cudaGetLastError();
 }
 
@@ -648,15 +659,18 @@ cudaError_t launch_down_gemv(const uint8_t* d_tiles, const uint16_t* h, const in
 // README, REAP section caveat: RMSNorm on the combined expert output,
 // before up_proj).  One CTA per token.
 // =====================================================================
-__global__ void __launch_bounds__(256) combine_rmsnorm_kernel(const float* __restrict__ o,
-                                                              const int* __restrict__ slot,
-                                                              const float* __restrict__ topk_w,
-                                                              const uint16_t* __restrict__ gamma, int K, int L,
-                                                              float eps, uint16_t* __restrict__ n) {
+__global__ void __launch_bounds__(1024) combine_rmsnorm_kernel(const float* __restrict__ o,
+                                                               const int* __restrict__ slot,
+                                                               const float* __restrict__ topk_w,
+                                                               const uint16_t* __restrict__ gamma, int K, int L,
+                                                               float eps, uint16_t* __restrict__ n) {
+  // One CTA per token; thread i owns latent columns 4i..4i+3 (plus further
+  // groups of 4*blockDim.x when L is larger); the K slot rows of a column
+  // group are loaded together so their latencies overlap.
   extern __shared__ float cs[];  // [L]
   __shared__ int sl[32];
   __shared__ float wk[32];
-  __shared__ float red[8];
+  __shared__ float red[32];
   const int t = blockIdx.x;
   if (threadIdx.x < K) {
     sl[threadIdx.x] = slot[(size_t)t * K + threadIdx.x];
@@ -664,11 +678,29 @@ __global__ void __launch_bounds__(256) combine_rmsnorm_kernel(const float* __res
   }
   __syncthreads();
   float ss = 0.f;
-  for (int l = threadIdx.x; l < L; l += blockDim.x) {
-    float c = 0.f;
-    for (int k = 0; k < K; ++k) c = fmaf(wk[k], o[(size_t)sl[k] * L + l], c);
-    cs[l] = c;
-    ss = fmaf(c, c, ss);
+  for (int c4 = threadIdx.x; c4 < L / 4; c4 += blockDim.x) {
+    float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k0 = 0; k0 < K; k0 += 8) {  // eight slot rows in flight at a time, added in k order
+      float4 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (k0 + k < K) v[k] = __ldg(reinterpret_cast<const float4*>(o + (size_t)sl[k0 + k] * L) + c4);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (k0 + k < K) {
+          const float wv = wk[k0 + k];
+          c.x = fmaf(wv, v[k].x, c.x);
+          c.y = fmaf(wv, v[k].y, c.y);
+          c.z = fmaf(wv, v[k].z, c.z);
+          c.w = fmaf(wv, v[k].w, c.w);
+        }
+      }
+    }
+    reinterpret_cast<float4*>(cs)[c4] = c;
+    ss = fmaf(c.x, c.x, ss);
+    ss = fmaf(c.y, c.y, ss);
+    ss = fmaf(c.z, c.z, ss);
+    ss = fmaf(c.w, c.w, ss);
   }
   ss = warp_sum(ss);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
@@ -676,8 +708,15 @@ __global__ void __launch_bounds__(256) combine_rmsnorm_kernel(const float* __res
   float tot = 0.f;
   for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += red[i];
   const float inv = 1.0f / sqrtf(tot / (float)L + eps);
-  for (int l = threadIdx.x; l < L; l += blockDim.x)
-    n[(size_t)t * L + l] = f32_to_bf16(cs[l] * inv * bf16_to_f32(gamma[l]));
+  for (int c4 = threadIdx.x; c4 < L / 4; c4 += blockDim.x) {
+    const float4 c = reinterpret_cast<const float4*>(cs)[c4];
+    const uint2 g = __ldg(reinterpret_cast<const uint2*>(gamma) + c4);
+    const float2 g01 = unpack_bf16x2(g.x), g23 = unpack_bf16x2(g.y);
+    uint2 out;
+    out.x = pack_bf16x2(c.x * inv * g01.x, c.y * inv * g01.y);
+    out.y = pack_bf16x2(c.z * inv * g23.x, c.w * inv * g23.y);
+    reinterpret_cast<uint2*>(n + (size_t)t * L)[c4] = out;
+  }
 }
 
 // One-time kernel attributes (dynamic shared memory above 48 KB), set when a
@@ -691,13 +730,21 @@ cudaError_t prepare_decode_kernels(const Dims& d) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(combine_rmsnorm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(sizeof(float) * d.L));
+  const int rs_smem = (int)(sizeof(float) * 32 * (size_t)d.E);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(route_small_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, rs_smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(route_small_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, rs_smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(route_small_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, rs_smem);
   return e;
 }
 
 cudaError_t launch_combine_rmsnorm(const float* o, const int* slot, const float* topk_w, const uint16_t* gamma,
                                    int T, const Dims& d, uint16_t* n, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  combine_rmsnorm_kernel<<<T, 256, sizeof(float) * d.L, s>>>(o, slot, topk_w, gamma, d.K, d.L, d.rms_eps, n);
+  const int threads = std::min(1024, ((d.L / 4 + 31) / 32) * 32);
+  combine_rmsnorm_kernel<<<T, threads, sizeof(float) * d.L, s>>>(o, slot, topk_w, gamma, d.K, d.L, d.rms_eps, n);
   return cudaGetLastError();
 }
 

@@ -124,6 +124,27 @@ __device__ __forceinline__ void tile_word_to_bf16(uint32_t q, const ScaleMul& m,
   }
 }
 
+// One scale group (a 16-byte chunk, 32 columns) to 16 bf16x2 words, with a
+// single branch on the scale: scale bytes up to 128 (all practical weight
+// scales) take one multiply per pair.
+__device__ __forceinline__ void group_to_bf16(const uint4& c, uint32_t S, uint32_t v[16]) {
+  const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+  if (S <= 128u) {
+    const uint32_t e = (S + 126u) << 7;
+    const uint32_t mul = e | (e << 16);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      tile_word_to_bf16x2_raw(words[q], v + 4 * q);
+#pragma unroll
+      for (int p = 0; p < 4; ++p) v[4 * q + p] = bf16x2_mul(v[4 * q + p], mul);
+    }
+  } else {
+    const ScaleMul m = scale_multipliers(S);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) tile_word_to_bf16(words[q], m, v + 4 * q);
+  }
+}
+
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

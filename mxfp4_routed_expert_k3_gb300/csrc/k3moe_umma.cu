@@ -612,11 +612,8 @@ __global__ void __launch_bounds__(kSThreads, 2) umma_stream_kernel(const __grid_
         for (int i = 0; i < C::kNumA; ++i) {
           const uint8_t* tl = stg + i * kTileBytes;
           const uint4 c = *reinterpret_cast<const uint4*>(tl + (size_t)(grp * 128 + r) * 16);
-          const ScaleMul m = scale_multipliers(tl[kTilePackedBytes + 2 * r + grp]);
-          const uint32_t words[4] = {c.x, c.y, c.z, c.w};
           uint32_t v[16];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) tile_word_to_bf16(words[q], m, v + 4 * q);
+          group_to_bf16(c, tl[kTilePackedBytes + 2 * r + grp], v);
           tmem_st16(lane_base + slot_col(t) + i * 32 + grp * 16, v);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -816,13 +813,27 @@ __global__ void __launch_bounds__(kDThreads, 1) umma_dense_stream_kernel(const _
       if (last) {
         __threadfence();
         if (m < p.M) {
-          for (int t = 0; t < p.T; ++t) {
-            float v = 0.f;
-            for (int c = 0; c < p.nkc; ++c) v += __ldcg(p.part + ((size_t)c * p.T + t) * p.M + m);
-            if (m < p.split)
-              p.out_f32[(size_t)t * p.split + m] = v;
-            else
-              p.out_bf16[(size_t)t * (p.M - p.split) + (m - p.split)] = f32_to_bf16(v);
+          for (int t0 = 0; t0 < p.T; t0 += 8) {  // eight tokens' loads in flight; chunks added in order
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = 0.f;
+            for (int c = 0; c < p.nkc; ++c) {
+              const float* src = p.part + ((size_t)c * p.T + t0) * p.M + m;
+              float x[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) x[i] = (t0 + i < p.T) ? __ldcg(src + (size_t)i * p.M) : 0.f;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v[i] += x[i];
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int t = t0 + i;
+              if (t >= p.T) break;
+              if (m < p.split)
+                p.out_f32[(size_t)t * p.split + m] = v[i];
+              else
+                p.out_bf16[(size_t)t * (p.M - p.split) + (m - p.split)] = f32_to_bf16(v[i]);
+            }
           }
         }
       }
