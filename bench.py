@@ -81,20 +81,39 @@ def barrier(world: int):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms with a
+    timestamp; only the samples taken inside the timed region's wall-clock
+    window [begin(), end()] are kept."""
 
-    def __init__(self, gpu_index: int):
+    QUERY = "timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active"
+
+    def __init__(self, gpu_index: int, settle_s: float = 1.5):
         self.proc = None
+        self.t0 = self.t1 = None
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
-        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,utilization.gpu")
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(settle_s)  # nvidia-smi needs a moment before its first sample
         except Exception:
             self.proc = None
+
+    def begin(self):
+        self.t0 = time.time()
+
+    def end(self):
+        self.t1 = time.time()
+
+    @staticmethod
+    def _stamp(text: str):
+        import datetime
+        try:
+            return datetime.datetime.strptime(text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
 
     def stop(self) -> dict | None:
         if self.proc is None:
@@ -105,26 +124,32 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.fh.close()
-        sm, smax, reasons = [], None, set()
+        return self.parse()
+
+    def parse(self) -> dict:
+        sm, smax, reasons, window = [], None, set(), 0
+        lo = (self.t0 if self.t0 is not None else float("-inf")) - 0.02
+        hi = (self.t1 if self.t1 is not None else float("inf")) + 0.02
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 6:
                 continue
+            ts = self._stamp(parts[0])
             try:
-                clk, mx, util = float(parts[1]), float(parts[2]), float(parts[5])
-                act = int(parts[4], 16)
+                clk, mx = float(parts[2]), float(parts[3])
+                act = int(parts[5], 16)
             except ValueError:
                 continue
             smax = mx
-            if util > 0:
-                sm.append(clk)
-                for bit, name in REASON_BITS.items():
-                    if act & bit and name != "gpu_idle":
-                        reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+            if ts is None or not (lo <= ts <= hi):
+                continue
+            window += 1
+            sm.append(clk)
+            for bit, name in REASON_BITS.items():
+                if act & bit and name != "gpu_idle":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": window, "interval_ms": 20}
 
 
 def source_sha(path: str) -> str:
@@ -133,8 +158,9 @@ def source_sha(path: str) -> str:
 
 
 def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel's
-    source is unchanged since it was taken."""
+    """DRAM bytes per active expert of `kernel` from a committed ncu capture
+    (profiles/traffic.json), if the kernel's source is unchanged since the
+    counters were taken; None otherwise."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -144,7 +170,7 @@ def recorded_traffic(kernel: str, workload: str):
     src = os.path.join(ROOT, "mxfp4_routed_expert_k3_gb300", "csrc", rec["source"])
     if not os.path.exists(src) or source_sha(src) != rec.get("source_sha"):
         return None
-    return rec["dram_bytes_per_launch"]
+    return rec["dram_bytes_per_active_expert"]
 
 
 # ============================================================================ ours
@@ -216,11 +242,13 @@ def run_ours(args, rank, world, local_rank):
     barrier(world)
     clocks = ClockSampler(local_rank)
     torch.cuda.synchronize()
+    clocks.begin()
     t_wall0 = time.perf_counter()
     for i in range(args.warmup, pool):
         one_step(i, True)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
+    clocks.end()
     barrier(world)
     clk = clocks.stop()
     assert layer.status() == 0, k3moe.last_error(layer.ctx)
@@ -250,7 +278,11 @@ def run_ours(args, rank, world, local_rank):
     kernel_desc = {1: "gateup_gemv_kernel (CUDA-core grouped MXFP4 gate/up GEMV + SiTU-GLU)",
                    3: "umma_stream_kernel<GATEUP> (tcgen05, decoded MXFP4 weights in TMEM, SiTU-GLU epilogue)"
                    }.get(path_used, "umma_gemm_kernel<GATEUP> (tcgen05 grouped MXFP4 GEMM)")
-    traffic = recorded_traffic(kernel_id, "k3-decode")
+    # ncu's DRAM bytes per active expert (captured on a smaller case, traffic
+    # grows with the experts touched) times this run's mean active experts
+    per_expert = recorded_traffic(kernel_id, "k3-decode")
+    mean_active = statistics.mean([n for T in batches for n in active_experts[T]])
+    traffic = per_expert * mean_active if per_expert is not None else None
     roofline = {"bound": "hbm", "kernel": kernel_desc, "path": path_used,
                 "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": (achieved / peaks["hbm_gbs"]) if achieved else None,

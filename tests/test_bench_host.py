@@ -54,24 +54,27 @@ def test_single_rank_reduction_is_identity():
     assert bench.reduce_sum_over_ranks(3.5, 1) == 3.5
 
 
-def test_clock_log_parsing(tmp_path, monkeypatch):
+def test_clock_log_parsing(tmp_path):
+    import datetime
     s = bench.ClockSampler.__new__(bench.ClockSampler)
     s.path = str(tmp_path / "c.csv")
-    with open(s.path, "w") as f:
-        f.write("0, 1965, 2070, 900.1, 0x0000000000000000, 95\n")
-        f.write("0, 1980, 2070, 950.2, 0x0000000000000004, 97\n")   # sw_power_cap
-        f.write("0, 345, 2070, 100.0, 0x0000000000000001, 0\n")     # idle sample: ignored
-        f.write("garbage line\n")
-    s.fh = open(os.devnull, "w")
+    base = datetime.datetime(2026, 1, 2, 3, 4, 5)
 
-    class P:
-        def terminate(self): pass
-        def wait(self, timeout=None): return 0
-        def kill(self): pass
-    s.proc = P()
-    c = s.stop()
-    assert c["samples"] == 2 and c["sm_max_mhz"] == 2070
-    assert c["sm_mhz"] == (1965 + 1980) / 2
+    def stamp(dt_s):
+        return (base + datetime.timedelta(seconds=dt_s)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+
+    with open(s.path, "w") as f:
+        f.write(f"{stamp(0.0)}, 0, 345, 2070, 100.0, 0x0000000000000001\n")    # before the region
+        f.write(f"{stamp(1.00)}, 0, 1965, 2070, 900.1, 0x0000000000000000\n")
+        f.write(f"{stamp(1.05)}, 0, 1980, 2070, 950.2, 0x0000000000000004\n")  # sw_power_cap
+        f.write(f"{stamp(1.10)}, 0, 1995, 2070, 950.2, 0x0000000000000000\n")
+        f.write(f"{stamp(3.0)}, 0, 345, 2070, 100.0, 0x0000000000000020\n")    # after: ignored
+        f.write("garbage line\n")
+    s.t0 = base.timestamp() + 0.99
+    s.t1 = base.timestamp() + 1.11
+    c = s.parse()
+    assert c["samples"] == 3 and c["sm_max_mhz"] == 2070
+    assert c["sm_mhz"] == 1980
     assert c["reasons"] == ["sw_power_cap"]
 
 
@@ -82,7 +85,7 @@ def test_traffic_record_requires_same_source(tmp_path, monkeypatch):
     prof = tmp_path / "profiles"
     prof.mkdir()
     rec = {"gateup_gemv_kernel": {"source": "k.cu", "source_sha": bench.source_sha(str(csrc / "k.cu")),
-                                  "workload": "w", "dram_bytes_per_launch": 123.0}}
+                                  "workload": "w", "dram_bytes_per_active_expert": 123.0}}
     (prof / "traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.recorded_traffic("gateup_gemv_kernel", "w") == 123.0
