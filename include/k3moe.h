@@ -81,7 +81,12 @@ typedef struct {
                       1: CUDA-core kernels everywhere;
                       2: tensor-core GEMM kernels (prefill-size batches);
                       3: streaming tensor-core kernels (decode-size batches;
-                         dense projections by split-K for T <= 64) */
+                         dense projections by split-K for T <= 64; expert
+                         weights decoded to bf16 into tensor memory);
+                      4: as 3, with the expert GEMMs on the block-scaled
+                         MXFP4 tensor cores (tcgen05 kind::mxf8f6f4: e2m1
+                         weights and e8m0 scales as stored, activations as
+                         two exact block-scaled e4m3 terms); T <= 256 */
 } k3moe_config;
 
 /* Host arrays in checkpoint layout, experts stacked along dim 0.  Row-major;
@@ -216,7 +221,7 @@ enum {
   K3MOE_Q_WORKSPACE_BYTES = 0, /* device workspace bytes                       */
   K3MOE_Q_WEIGHT_BYTES = 1,    /* device weight bytes                          */
   K3MOE_Q_LAUNCHES_LAST = 2,   /* kernels launched by the last forward          */
-  K3MOE_Q_PATH_LAST = 3,       /* path of the last forward (force_path values 1..3) */
+  K3MOE_Q_PATH_LAST = 3,       /* path of the last forward (force_path values 1..4) */
   K3MOE_Q_DEVICE = 4           /* CUDA device ordinal                          */
 };
 

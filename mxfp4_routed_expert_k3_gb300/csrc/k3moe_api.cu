@@ -10,6 +10,7 @@
 #include "../../include/k3moe.h"
 #include "k3moe_device.cuh"
 #include "k3moe_internal.h"
+#include "k3moe_bs.h"
 #include "k3moe_umma.h"
 
 namespace {
@@ -48,6 +49,8 @@ struct k3moe_ctx {
   int32_t* idx_stage = nullptr;
   float* w_stage = nullptr;
   k3::UmmaPlan umma{};
+  k3::BsPlan bs{};
+  k3::BsWeights bw{};
   long long launches_last = 0;
   int path_last = 0;
   // optional per-step timing: events around each launch group of a forward
@@ -102,7 +105,7 @@ int check_config(const k3moe_config* c) {
   if (!(c->rms_eps >= 0.f) || !(c->beta > 0.f) || !(c->beta_lin > 0.f))
     return fail(nullptr, K3MOE_EINVAL, "beta, beta_lin must be > 0 and rms_eps >= 0");
   if (c->spin_timeout_ms < 0) return fail(nullptr, K3MOE_EINVAL, "spin_timeout_ms must be >= 0");
-  if (c->force_path < 0 || c->force_path > 3) return fail(nullptr, K3MOE_EINVAL, "force_path must be 0..3");
+  if (c->force_path < 0 || c->force_path > 4) return fail(nullptr, K3MOE_EINVAL, "force_path must be 0..4");
   return K3MOE_OK;
 }
 
@@ -149,9 +152,10 @@ int k3moe_create(const k3moe_config* cfg, int cuda_device, k3moe_ctx** out) {
   c->sz_o = Tm * K * L * 4;
   c->sz_n = Tm * L * 2;
   c->umma = k3::umma_plan(c->d, (int)Tm);
+  const size_t bs_bytes = k3::bs_ws_bytes(c->d, (int)Tm);
   const size_t parts[] = {c->sz_logits, c->sz_lat,   c->sz_counts, c->sz_offsets, c->sz_active, c->sz_perm,
                           c->sz_perm,   nblk * E * 4, c->sz_h,     c->sz_o,       c->sz_n,      256,
-                          Tm * H * 2,   Tm * H * 2,   Tm * K * 4,  Tm * K * 4,    c->umma.ws_bytes};
+                          Tm * H * 2,   Tm * H * 2,   Tm * K * 4,  Tm * K * 4,    c->umma.ws_bytes, bs_bytes};
   size_t total = 0;
   for (size_t p : parts) total += align_up(p, 256);
   e = cudaMalloc(&c->ws, total);
@@ -188,9 +192,17 @@ int k3moe_create(const k3moe_config* cfg, int cuda_device, k3moe_ctx** out) {
   c->umma.status = c->w.status;
   c->umma.num_sms = prop.multiProcessorCount;
   c->umma.limit_ns = (uint64_t)c->cfg.spin_timeout_ms * 1000000ull;
+  c->bs.ws = take(parts[17]);
+  c->bs.ws_bytes = bs_bytes;
+  c->bs.max_tokens = std::min((int)Tm, k3::kBsMaxTokens);
+  c->bs.status = c->w.status;
+  c->bs.num_sms = prop.multiProcessorCount;
+  c->bs.limit_ns = c->umma.limit_ns;
+  c->bs.dims = c->d;
   e = cudaMemset(c->ws, 0, total);
   if (e == cudaSuccess) e = k3::prepare_decode_kernels(c->d);
   if (e == cudaSuccess) e = k3::prepare_umma_kernels();
+  if (e == cudaSuccess) e = k3::prepare_bs_kernels();
   if (e != cudaSuccess) {
     fail(nullptr, K3MOE_ECUDA, "workspace / kernel setup: %s", cudaGetErrorString(e));
     cudaFree(c->ws);
@@ -212,6 +224,7 @@ void k3moe_destroy(k3moe_ctx* c) {
   cudaFree(c->wu);
   cudaFree(c->gu_tiles);
   cudaFree(c->d_tiles);
+  cudaFree(c->bw.gu_q);
   for (cudaEvent_t ev : c->prof_ev)
     if (ev) cudaEventDestroy(ev);
   delete c;
@@ -247,7 +260,12 @@ int k3moe_load_weights(k3moe_ctx* c, const k3moe_weights* wt) {
     K3_CUDA(c, cudaMalloc(&c->wu, H * L * 2), "cudaMalloc(up_proj)");
     K3_CUDA(c, cudaMalloc(&c->gu_tiles, gu_bytes), "cudaMalloc(gate/up tiles)");
     K3_CUDA(c, cudaMalloc(&c->d_tiles, d_bytes), "cudaMalloc(down tiles)");
-    c->weight_bytes = (E + L) * H * 2 + E * 4 + L * 2 + H * L * 2 + gu_bytes + d_bytes;
+    // block-scaled layout: one allocation, carved as gu_q | gu_sf | d_q | d_sf
+    K3_CUDA(c, cudaMalloc(&c->bw.gu_q, k3::bs_weight_bytes(c->d)), "cudaMalloc(block-scaled experts)");
+    c->bw.gu_sf = c->bw.gu_q + E * 2 * I * L / 2;
+    c->bw.d_q = c->bw.gu_sf + E * 2 * I * L / 32;
+    c->bw.d_sf = c->bw.d_q + E * L * I / 2;
+    c->weight_bytes = (E + L) * H * 2 + E * 4 + L * 2 + H * L * 2 + gu_bytes + d_bytes + k3::bs_weight_bytes(c->d);
   }
   c->loaded = false;
   K3_CUDA(c, cudaMemcpy(c->wcat, wt->router_w, E * H * 2, cudaMemcpyHostToDevice), "copy router_w");
@@ -291,6 +309,33 @@ int k3moe_load_weights(k3moe_ctx* c, const k3moe_weights* wt) {
         rc = cuda_fail(c, e, "expert re-layout");
     }
   }
+  // block-scaled layout: nibbles as stored (gate and up interleaved per
+  // expert), scales regrouped into 512-byte atoms
+  if (rc == K3MOE_OK) {
+    const size_t per = I * L / 2;
+    if ((e = cudaMemcpy2D(c->bw.gu_q, 2 * per, wt->w1_packed, per, per, E, cudaMemcpyHostToDevice)) ||
+        (e = cudaMemcpy2D(c->bw.gu_q + per, 2 * per, wt->w3_packed, per, per, E, cudaMemcpyHostToDevice)) ||
+        (e = cudaMemcpy(c->bw.d_q, wt->w2_packed, E * per, cudaMemcpyHostToDevice)))
+      rc = cuda_fail(c, e, "block-scaled expert copy");
+  }
+  struct SJob {
+    const uint8_t* s;
+    int rows, cols, n_mat, mat;
+    uint8_t* out;
+  } sjobs[3] = {{wt->w1_scale, (int)I, (int)L, 2, 0, c->bw.gu_sf},
+                {wt->w3_scale, (int)I, (int)L, 2, 1, c->bw.gu_sf},
+                {wt->w2_scale, (int)L, (int)I, 1, 0, c->bw.d_sf}};
+  for (const SJob& j : sjobs) {
+    for (size_t e0 = 0; e0 < E && rc == K3MOE_OK; e0 += chunk) {
+      const size_t ne = std::min(chunk, E - e0);
+      const size_t atoms_per_expert = (size_t)(j.rows / 128) * (j.cols / 128) * j.n_mat;
+      if ((e = cudaMemcpy(st_s, j.s + e0 * per_expert_scale, ne * per_expert_scale, cudaMemcpyHostToDevice)) ||
+          (e = k3::bs_scale_atoms(st_s, (int)ne, j.rows, j.cols, j.n_mat, j.mat,
+                                  j.out + e0 * atoms_per_expert * 512, 0)) ||
+          (e = cudaDeviceSynchronize()))
+        rc = cuda_fail(c, e, "block-scaled scale atoms");
+    }
+  }
   cudaFree(st_p);
   cudaFree(st_s);
   if (rc) return rc;
@@ -302,9 +347,14 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
                         cudaStream_t s) {
   const k3::Dims& d = c->d;
   k3::Work& w = c->w;
-  // path: 1 CUDA-core kernels, 2 tensor-core GEMMs, 3 CUDA-core dense GEMVs + streaming tensor-core experts
+  // path: 1 CUDA-core kernels, 2 tensor-core GEMMs, 3 streaming tensor-core
+  // kernels (experts decoded to bf16 in TMEM), 4 as 3 with the experts on
+  // the block-scaled MXFP4 tensor cores
   int path = c->cfg.force_path;
   if (path == 0) path = T <= 64 ? 3 : 2;
+  if (path == 4 && T > c->bs.max_tokens)
+    return fail(c, K3MOE_EINVAL, "path 4 serves T <= %d (got %d)", c->bs.max_tokens, T);
+  const bool stream = path == 3 || path == 4;
   const bool big = path == 2;
   c->path_last = path;
   long long n = 0;
@@ -334,14 +384,17 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
   if (big) {
     K3_LAUNCH(k3::umma_dense(c->umma, c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, d.E, w.logits, w.lat, s),
               k3::umma_dense_launches(), "router + down_proj (tensor cores)");
-  } else if (path == 3 && T <= 64) {
+  } else if (stream && T <= 64) {
     K3_LAUNCH(k3::umma_dense_small(c->umma, c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, d.E, w.logits, w.lat, s),
               1, "router + down_proj");
+  } else if (path == 4) {
+    K3_LAUNCH(k3::umma_dense(c->umma, c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, d.E, w.logits, w.lat, s),
+              k3::umma_dense_launches(), "router + down_proj");
   } else {
     K3_LAUNCH(k3::launch_dense_gemv(c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, d.E, w.logits, w.lat, s), 1,
               "router + down_proj");
   }
-  const bool fused_route = path == 3 && T * d.K <= 1024;
+  const bool fused_route = stream && T * d.K <= 1024;
   if (fused_route) {
     int4* tiles;
     int* tile_count;
@@ -359,6 +412,15 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
   if (big) {
     K3_LAUNCH(k3::umma_experts(c->umma, c->gu_tiles, c->d_tiles, w, T, d, s), k3::umma_expert_launches(),
               "experts (tensor cores)");
+  } else if (path == 4) {
+    int4* tiles;
+    int* tile_count;
+    int bn;
+    k3::umma_tile_list(c->umma, &tiles, &tile_count, &bn);
+    if (!fused_route) K3_LAUNCH(k3::umma_stream_tiles(c->umma, w, T, d, s), 1, "tile list");
+    K3_LAUNCH(k3::bs_quantize_latent(c->bs, w, T, d, s), 1, "latent rows -> e4m3 terms");
+    K3_LAUNCH(k3::bs_stream_gateup(c->bs, c->bw, tiles, tile_count, w, T, d, s), 1, "gate/up");
+    K3_LAUNCH(k3::bs_stream_down(c->bs, c->bw, tiles, tile_count, w, T, d, s), 1, "down");
   } else if (path == 3) {
     if (fused_route)
       K3_LAUNCH(k3::umma_stream_gather(c->umma, w, T, d, s), 1, "gather");
@@ -375,8 +437,11 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
   if (big) {
     K3_LAUNCH(k3::umma_dense(c->umma, c->wu, d.H, d.L, w.n, T, 0, nullptr, (uint16_t*)y, s),
               k3::umma_dense_launches(), "up_proj (tensor cores)");
-  } else if (path == 3 && T <= 64) {
+  } else if (stream && T <= 64) {
     K3_LAUNCH(k3::umma_dense_small(c->umma, c->wu, d.H, d.L, w.n, T, 0, nullptr, (uint16_t*)y, s), 1, "up_proj");
+  } else if (path == 4) {
+    K3_LAUNCH(k3::umma_dense(c->umma, c->wu, d.H, d.L, w.n, T, 0, nullptr, (uint16_t*)y, s),
+              k3::umma_dense_launches(), "up_proj");
   } else {
     K3_LAUNCH(k3::launch_dense_gemv(c->wu, d.H, d.L, w.n, T, 0, nullptr, (uint16_t*)y, s), 1, "up_proj");
   }

@@ -1,0 +1,55 @@
+// k3moe_bs.h -- block-scaled tensor-core path for the MXFP4 expert GEMMs:
+// tcgen05.mma kind::mxf8f6f4 with the e2m1 weights and their e8m0 scales fed
+// to the tensor cores as they are stored, and the bf16 activations written
+// exactly as the sum of two block-scaled e4m3 terms.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "k3moe_internal.h"
+
+namespace k3 {
+
+// Expert weights in the block-scaled layout (device memory).
+//   gu_q : [E][2][I][L/2]  e2m1 nibbles (checkpoint order), gate then up
+//   gu_sf: [E][I/128][L/128][2][512] e8m0 scale atoms (gate, up)
+//   d_q  : [E][L][I/2]
+//   d_sf : [E][L/128][I/128][512]
+struct BsWeights {
+  uint8_t* gu_q = nullptr;
+  uint8_t* gu_sf = nullptr;
+  uint8_t* d_q = nullptr;
+  uint8_t* d_sf = nullptr;
+};
+size_t bs_weight_bytes(const Dims& d);
+// Scale atoms of n_mat matrices [ne][rows][cols/32] into out (layout above;
+// mat_stride atoms between experts, `mat` selects the slot in an atom pair).
+cudaError_t bs_scale_atoms(const uint8_t* scale, int ne, int rows, int cols, int n_mat, int mat, uint8_t* out,
+                           cudaStream_t s);
+
+struct BsPlan {
+  int max_tokens = 0;     // largest T this path serves (workspace bound)
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  unsigned* status = nullptr;
+  uint64_t limit_ns = 2000000000ull;
+  int num_sms = 152;
+  Dims dims{};
+};
+constexpr int kBsMaxTokens = 256;
+size_t bs_ws_bytes(const Dims& d, int max_tokens);
+cudaError_t prepare_bs_kernels();
+
+// Slot-ordered latent rows (lat[perm[s] / K]) written as two e4m3 terms and
+// their scale records.
+cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s);
+// gate/up over the tile list (tiles of at most 32 rows): h (bf16, slot
+// order) and its two-term e4m3 form for the down GEMM.
+cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* tiles, const int* tile_count,
+                             const Work& w, int T, const Dims& d, cudaStream_t s);
+// down: o (fp32, slot order)
+cudaError_t bs_stream_down(const BsPlan& p, const BsWeights& bw, const int4* tiles, const int* tile_count,
+                           const Work& w, int T, const Dims& d, cudaStream_t s);
+
+}  // namespace k3

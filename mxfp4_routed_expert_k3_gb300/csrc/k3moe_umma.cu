@@ -29,6 +29,7 @@
 #include <cstdio>
 
 #include "k3moe_device.cuh"
+#include "k3moe_tc.cuh"
 #include "k3moe_umma.h"
 
 namespace k3 {
@@ -60,142 +61,6 @@ struct Cfg {
   static constexpr int kSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
   static_assert(kNumA * kAcc * kAccStride <= kTmemCols || MODE == GATEUP, "TMEM budget");
 };
-
-// ------------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-struct Guard {
-  volatile int* abort;   // shared flag
-  unsigned* status;      // device status word
-  uint64_t limit_ns;
-};
-
-// Bounded wait; false if the wait gave up (or another role already did).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Guard& g, unsigned code) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0) {
-      if (*g.abort) return false;
-      if (global_ns() - t0 > g.limit_ns) {
-        *g.abort = 1;
-        atomicOr(g.status, code);
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-               : "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols));
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// UMMA shared-memory descriptor, K-major, 128-byte swizzle: rows of 128 bytes,
-// 8-row groups 1024 bytes apart (stride byte offset), leading offset unused.
-__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-  d |= (uint64_t)1u << 16;                 // leading byte offset (unused for this layout)
-  d |= (uint64_t)(1024u >> 4) << 32;       // stride byte offset
-  d |= (uint64_t)1u << 46;                 // descriptor version
-  d |= (uint64_t)2u << 61;                 // 128-byte swizzle
-  return d;
-}
-// Instruction descriptor: kind::f16, A = B = bf16, D = fp32, both K-major.
-__device__ __forceinline__ uint32_t umma_idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(
-          d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// SiTU-GLU in fp32 from the identities tanh(x/2) = (1 - e^-x)/(1 + e^-x)
-// and sigmoid(g) = 1/(1 + e^-g), one exponential per branch, written for
-// either sign without overflow:
-//   t = e^(-|g|/2):  g >= 0: beta tanh(g/beta) sigma(g) = 4 (1-t) / ((1+t)(1+t^2))   (beta = 4)
-//                    g <  0:                            = -4 (1-t) t^2 / ((1+t)(1+t^2))
-// The general-beta form uses t1 = e^(-2|g|/beta) for the tanh and e^(-|g|)
-// for the sigmoid.
-__device__ __forceinline__ float situ_fast(float g, float u, float beta, float beta_lin) {
-  const float ag = fabsf(g);
-  const float a = __expf(-2.0f * ag / beta);  // tanh(|g|/beta) = (1-a)/(1+a)
-  const float b = __expf(-ag);                 // sigmoid(|g|) = 1/(1+b), sigmoid(-|g|) = b/(1+b)
-  const float th = __fdividef(1.0f - a, 1.0f + a);
-  const float sg = g >= 0.f ? __fdividef(1.0f, 1.0f + b) : __fdividef(b, 1.0f + b);
-  const float gate = beta * copysignf(th, g) * sg;
-  const float au = fabsf(u);
-  const float c = __expf(-2.0f * au / beta_lin);
-  const float tu = copysignf(__fdividef(1.0f - c, 1.0f + c), u);
-  return gate * beta_lin * tu;
-}
 
 // Per-tile description for grouped GEMMs: x = expert, y = first row (slot),
 // z = valid rows, w = MMA N (rows rounded up to 16).
@@ -918,23 +783,6 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int* __restrict
 // ------------------------------------------------------------------ host side
 namespace {
 
-using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeFn encode_fn() {
-  static EncodeFn fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeFn>(ptr);
-  }
-  return fn;
-}
-
 // 2-D bf16 map of a row-major [rows, cols] matrix, box [box_rows, 64], 128-byte swizzle.
 bool make_map(CUtensorMap* map, const void* base, int rows, int cols, int box_rows) {
   EncodeFn fn = encode_fn();
@@ -1105,6 +953,14 @@ cudaError_t umma_stream_prepare(const UmmaPlan& p, const Work& w, int T, const D
   UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
   build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, kSNB, ws.tiles, ws.count);
   gather_rows_kernel<<<152 * 2, 256, 0, s>>>(w.lat, w.perm, TK, d.K, d.L, ws.lat_perm);
+  return cudaGetLastError();
+}
+
+// Only the tile list (tiles of at most kSNB rows).
+cudaError_t umma_stream_tiles(const UmmaPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s) {
+  if (T * d.K <= 0) return cudaSuccess;
+  UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
+  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, kSNB, ws.tiles, ws.count);
   return cudaGetLastError();
 }
 

@@ -106,7 +106,7 @@ def _check(rc: int, ctx=None):
         raise K3Error(rc, last_error(ctx))
 
 
-PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_STREAM = 0, 1, 2, 3
+PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_STREAM, PATH_BLOCK_SCALED = 0, 1, 2, 3, 4
 
 
 def make_config(d: LayerDims, max_tokens: int, spin_timeout_ms: int = 0, force_path: int = 0) -> Config:
@@ -189,6 +189,7 @@ class Layer:
                  force_path: int = PATH_AUTO):
         self.d = d
         self.max_tokens = max_tokens
+        self.force_path = force_path
         self.ctx = create(make_config(d, max_tokens, spin_timeout_ms, force_path), device)
         try:
             load_weights(self.ctx, weights)

@@ -30,7 +30,8 @@ def k3layer(k3weights):
     layer.close()
 
 
-@pytest.fixture(scope="module", params=[k3moe.PATH_CUDA_CORE, k3moe.PATH_STREAM], ids=["cudacore", "stream"])
+@pytest.fixture(scope="module", params=[k3moe.PATH_CUDA_CORE, k3moe.PATH_STREAM, k3moe.PATH_BLOCK_SCALED],
+                ids=["cudacore", "stream", "blockscaled"])
 def k3decode(request, k3weights):
     layer = k3moe.Layer(K3, k3weights, max_tokens=64, force_path=request.param)
     yield k3weights, layer
