@@ -274,9 +274,12 @@ def run_ours(args, rank, world, local_rank):
     launches = sum(len(per_kernel[T]) for T in batches)
     achieved = kern_bytes / (kern_ms / 1e3) / 1e9 if kern_ms > 0 else None
     path_used = layer.query("path_last")
-    kernel_id = {1: "gateup_gemv_kernel", 3: "umma_stream_kernel_gateup"}.get(path_used, "umma_gemm_kernel_gateup")
+    kernel_id = {1: "gateup_gemv_kernel", 3: "umma_stream_kernel_gateup",
+                 4: "bs_stream_kernel_gateup"}.get(path_used, "umma_gemm_kernel_gateup")
     kernel_desc = {1: "gateup_gemv_kernel (CUDA-core grouped MXFP4 gate/up GEMV + SiTU-GLU)",
-                   3: "umma_stream_kernel<GATEUP> (tcgen05, decoded MXFP4 weights in TMEM, SiTU-GLU epilogue)"
+                   3: "umma_stream_kernel<GATEUP> (tcgen05, decoded MXFP4 weights in TMEM, SiTU-GLU epilogue)",
+                   4: "bs_stream_kernel<GATEUP> (tcgen05 kind::mxf8f6f4: e2m1 weights x two e4m3 activation "
+                      "terms, UE8M0 scales in TMEM, SiTU-GLU + requantisation epilogue)"
                    }.get(path_used, "umma_gemm_kernel<GATEUP> (tcgen05 grouped MXFP4 GEMM)")
     # ncu's DRAM bytes per active expert (captured on a smaller case, traffic
     # grows with the experts touched) times this run's mean active experts
@@ -423,7 +426,7 @@ def main():
     ap.add_argument("--cpu-sample", type=int, default=16, help="tokens in the oracle CPU baseline sample")
     ap.add_argument("--ref-tokens-per-step", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2, 3],
+    ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2, 3, 4],
                     help="kernel path (0 = the library's choice by token count; see k3moe_config.force_path)")
     ap.add_argument("--experts", type=int, default=896,
                     help="experts of the K3-dim layer (default 896; fewer only for small profiling captures)")

@@ -309,14 +309,25 @@ int k3moe_load_weights(k3moe_ctx* c, const k3moe_weights* wt) {
         rc = cuda_fail(c, e, "expert re-layout");
     }
   }
-  // block-scaled layout: nibbles as stored (gate and up interleaved per
-  // expert), scales regrouped into 512-byte atoms
-  if (rc == K3MOE_OK) {
-    const size_t per = I * L / 2;
-    if ((e = cudaMemcpy2D(c->bw.gu_q, 2 * per, wt->w1_packed, per, per, E, cudaMemcpyHostToDevice)) ||
-        (e = cudaMemcpy2D(c->bw.gu_q + per, 2 * per, wt->w3_packed, per, per, E, cudaMemcpyHostToDevice)) ||
-        (e = cudaMemcpy(c->bw.d_q, wt->w2_packed, E * per, cudaMemcpyHostToDevice)))
-      rc = cuda_fail(c, e, "block-scaled expert copy");
+  // block-scaled layout: nibbles unchanged, regrouped into contiguous
+  // 128 x 128 boxes (gate and up of an expert adjacent); scales into
+  // 512-byte atoms
+  struct QJob {
+    const uint8_t* p;
+    int rows, cols, n_mat, mat;
+    uint8_t* out;
+  } qjobs[3] = {{wt->w1_packed, (int)I, (int)L, 2, 0, c->bw.gu_q},
+                {wt->w3_packed, (int)I, (int)L, 2, 1, c->bw.gu_q},
+                {wt->w2_packed, (int)L, (int)I, 1, 0, c->bw.d_q}};
+  for (const QJob& j : qjobs) {
+    for (size_t e0 = 0; e0 < E && rc == K3MOE_OK; e0 += chunk) {
+      const size_t ne = std::min(chunk, E - e0);
+      if ((e = cudaMemcpy(st_p, j.p + e0 * per_expert_packed, ne * per_expert_packed, cudaMemcpyHostToDevice)) ||
+          (e = k3::bs_e2m1_boxes(st_p, (int)ne, j.rows, j.cols, j.n_mat, j.mat,
+                                 j.out + e0 * j.n_mat * per_expert_packed, 0)) ||
+          (e = cudaDeviceSynchronize()))
+        rc = cuda_fail(c, e, "block-scaled expert boxes");
+    }
   }
   struct SJob {
     const uint8_t* s;
@@ -351,7 +362,7 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
   // kernels (experts decoded to bf16 in TMEM), 4 as 3 with the experts on
   // the block-scaled MXFP4 tensor cores
   int path = c->cfg.force_path;
-  if (path == 0) path = T <= 64 ? 3 : 2;
+  if (path == 0) path = T <= 64 ? 4 : 2;
   if (path == 4 && T > c->bs.max_tokens)
     return fail(c, K3MOE_EINVAL, "path 4 serves T <= %d (got %d)", c->bs.max_tokens, T);
   const bool stream = path == 3 || path == 4;

@@ -20,11 +20,11 @@
 // block's largest magnitude; smaller elements keep an absolute error below
 // 2^(S0-127-13).  Two MMAs (one per term) accumulate into the same D.
 //
-// Tile scheme (decode sizes): M = 128 weight rows, N = 32 token rows (one
-// tile of the expert's slots), K = 128 input columns per stage (four MMAs of
-// K = 32 per term and matrix).  Warp 0 issues the copies, warp 1 the MMAs,
-// warps 2..5 run the epilogue from a double-buffered accumulator.  Every
-// wait is bounded (status bit + shared abort flag, as in the bf16 kernels).
+// Tile scheme (decode sizes): M = 128 weight rows, N = 16 or 32 token rows
+// (one tile of the expert's slots), MMAs of K = 32 per term and matrix.
+// Warp 0 issues the copies, warp 1 the MMAs, warps 2..5 run the epilogue
+// from a double-buffered accumulator; two CTAs per SM.  Every wait is
+// bounded (status bit + shared abort flag, as in the bf16 kernels).
 #include <cuda.h>
 
 #include <algorithm>
@@ -67,6 +67,26 @@ __global__ void scale_atoms_kernel(const uint8_t* __restrict__ in, int ne, int r
   }
 }
 
+// Packed nibbles [ne][rows][cols/2] -> boxes [ne][rows/128][cols/128][n_mat][128 rows][64 bytes]
+// (mat selects the slot), so that every 128 x 128 tile is one contiguous
+// 8 KB block and the gate and up tiles of one (row tile, column chunk) are
+// adjacent.  Bytes are moved unchanged, 16 at a time.
+__global__ void e2m1_boxes_kernel(const uint8_t* __restrict__ in, int ne, int rows, int cols, int n_mat, int mat,
+                                  uint8_t* __restrict__ out) {
+  const int rb = cols / 2 / 16;  // 16-byte vectors per row
+  const int MT = rows / kQM, KC = cols / kQK;
+  const long long total = (long long)ne * rows * rb;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int v = (int)(i % rb);
+    const long long er = i / rb;
+    const int row = (int)(er % rows);
+    const int e = (int)(er / rows);
+    const size_t box = (((size_t)e * MT + row / kQM) * KC + v / 4) * n_mat + mat;
+    reinterpret_cast<uint4*>(out)[(box * kQM + row % kQM) * 4 + (v & 3)] = reinterpret_cast<const uint4*>(in)[i];
+  }
+}
+
 // ------------------------------------------------------------------ two-term e4m3 split
 __device__ __forceinline__ float exp2i(int n) { return __uint_as_float((uint32_t)(n + 127) << 23); }  // |n| <= 126
 __device__ __forceinline__ uint32_t to_e4m3(float x) {
@@ -92,12 +112,13 @@ __device__ __forceinline__ uint32_t split_e4m3(float x, uint32_t s0, uint32_t s1
   return q0 | (to_e4m3(r) << 8);
 }
 
-// Slot-ordered rows: dst row s = src row (perm ? perm[s] / K : s).  A half
+// Slot-ordered rows: dst row s = src row (perm ? perm[s] / K : s), written
+// as terms q[t][C/128][rows_max][128] and scale records
+// sf[t][C/128][rows_max][16] (bytes 0..3: the four 32-column groups).  A half
 // warp covers 128 columns (8 per lane, 4 lanes per scale block); the loop
 // runs per warp so that both halves always meet at the shuffles.
 __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, const int* __restrict__ perm, int K, int rows,
-                                  int C, uint8_t* __restrict__ q0, uint8_t* __restrict__ q1, uint8_t* __restrict__ sf0,
-                                  uint8_t* __restrict__ sf1) {
+                                  int C, int rows_max, uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
   const int hl = threadIdx.x & 15, half = (threadIdx.x >> 4) & 1;
   const int KC = C / kQK;
   const long long nwork = (long long)rows * KC;
@@ -133,13 +154,13 @@ __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, const int* _
       }
     }
     if (!valid) continue;
-    const size_t off = (size_t)s * C + kc * kQK + hl * 8;
-    *reinterpret_cast<uint2*>(q0 + off) = make_uint2(a0, b0);
-    *reinterpret_cast<uint2*>(q1 + off) = make_uint2(a1, b1);
+    const size_t plane = (size_t)KC * rows_max;  // rows per term
+    const size_t r0 = (size_t)kc * rows_max + s;
+    *reinterpret_cast<uint2*>(q + r0 * kQK + hl * 8) = make_uint2(a0, b0);
+    *reinterpret_cast<uint2*>(q + (plane + r0) * kQK + hl * 8) = make_uint2(a1, b1);
     if ((hl & 3) == 0) {
-      const size_t so = ((size_t)s * KC + kc) * 16 + (hl >> 2);
-      sf0[so] = (uint8_t)s0;
-      sf1[so] = (uint8_t)s1;
+      sf[r0 * 16 + (hl >> 2)] = (uint8_t)s0;
+      sf[(plane + r0) * 16 + (hl >> 2)] = (uint8_t)s1;
     }
   }
 }
@@ -163,10 +184,11 @@ __device__ __forceinline__ void tc_cp_scales(uint32_t taddr, uint64_t desc) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
 // Instruction descriptor: kind::mxf8f6f4, A e2m1, B e4m3, both K-major,
-// UE8M0 scales, M = 128, N = 32, scale-factor ids (byte of the scale column).
-__device__ __forceinline__ uint32_t bs_idesc(uint32_t sfa_id, uint32_t sfb_id) {
-  return (sfb_id << 4) | (5u << 7) | (0u << 10) | ((uint32_t)(kQN >> 3) << 17) | (1u << 23) |
-         ((uint32_t)(kQM >> 4) << 24) | (sfa_id << 29);
+// UE8M0 scales, M = 128, N = n (16 or 32), scale-factor ids (byte of the
+// scale column).
+__device__ __forceinline__ uint32_t bs_idesc(uint32_t sfa_id, uint32_t sfb_id, uint32_t n) {
+  return (sfb_id << 4) | (5u << 7) | (0u << 10) | ((n >> 3) << 17) | (1u << 23) | ((uint32_t)(kQM >> 4) << 24) |
+         (sfa_id << 29);
 }
 __device__ __forceinline__ void umma_bs(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
                                         uint32_t sfb, uint32_t acc) {
@@ -178,34 +200,49 @@ __device__ __forceinline__ void umma_bs(uint32_t d, uint64_t a, uint64_t b, uint
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                            int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+      "[%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+// Per stage four copies: two adjacent e2m1 tiles (GATEUP: gate and up of one
+// 128-column chunk; DOWN: two consecutive chunks), both activation terms of
+// the stage's chunks, the weight scale atoms, the activation scale records.
+// Few large copies per stage keep the HBM stream going; two CTAs per SM.
 template <int MODE>
 struct BsCfg {
-  static constexpr int kNumA = (MODE == BS_GATEUP) ? 2 : 1;
-  static constexpr int kA = kQM * kQK;  // e2m1 tile in 16-byte slots (8 data + 8 padding bytes per 16 codes)
-  static constexpr int kB = kQN * kQK;  // one e4m3 term
-  static constexpr int kOffB = kNumA * kA;
-  static constexpr int kOffSfa = kOffB + 2 * kB;
-  static constexpr int kOffSfb = kOffSfa + kNumA * kAtom;
-  static constexpr int kStageBytes = (kOffSfb + 2 * kAtom + 1023) / 1024 * 1024;
-  static constexpr int kStages = (MODE == BS_GATEUP) ? 5 : 8;
-  static constexpr uint32_t kTx = kNumA * kA + 2 * kB + kNumA * kAtom + 2 * kAtom;
-  static constexpr int kDCols = kNumA * kQN;      // one accumulator buffer (gate, up)
-  static constexpr int kSfCols = 4 * (kNumA + 2); // scale columns per stage: SFA per matrix, SFB per term
+  static constexpr int kNumA = (MODE == BS_GATEUP) ? 2 : 1;  // accumulators
+  static constexpr int kNK = (MODE == BS_GATEUP) ? 1 : 2;    // 128-column chunks per stage
+  static constexpr int kA = kQM * kQK;  // one e2m1 tile in 16-byte slots (8 data + 8 padding bytes per 16 codes)
+  static constexpr int kB = kQN * kQK;  // one e4m3 term of one chunk
+  static constexpr int kOffB = 2 * kA;
+  static constexpr int kOffSfa = kOffB + 2 * kNK * kB;
+  static constexpr int kOffSfb = kOffSfa + 2 * kAtom;
+  static constexpr int kStageBytes = (kOffSfb + 2 * kNK * kAtom + 1023) / 1024 * 1024;
+  static constexpr int kStages = 2;
+  static constexpr int kDCols = kNumA * kQN;   // one accumulator buffer
+  static constexpr int kSfCols = 8 + 8 * kNK;  // SFA: 2 atoms, SFB: 2 terms x kNK chunks (4 columns each)
   static constexpr int kSfBase = 2 * kDCols;
   static constexpr int kTmemCols = 256;
   static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
   static_assert(kSfBase + kStages * kSfCols <= kTmemCols, "TMEM budget");
-  static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(2 * (kSmem + 1024) <= 233472, "two CTAs per SM");
 };
 
 struct BsParams {
   const uint8_t* sfa;  // weight scale atoms
-  int MT, KC;          // weight row tiles, input-column chunks
+  int MT, KC, KS;      // weight row tiles, 128-column chunks, stages per item
   const int4* tiles;   // {expert, first slot, rows, -}
   const int* count;
   int ld_out;          // GATEUP: I, DOWN: L
-  uint16_t* h;         // GATEUP outputs
-  uint8_t *hq0, *hq1, *hsf0, *hsf1;
+  int rows_max;        // slot rows of the activation-term planes
+  uint16_t* h;         // GATEUP outputs: h (bf16) and its terms / scale records
+  uint8_t* hq;
+  uint8_t* hsf;
   float* o;            // DOWN output
   float beta, beta_lin;
   unsigned* status;
@@ -213,10 +250,9 @@ struct BsParams {
 };
 
 template <int MODE>
-__global__ void __launch_bounds__(kBsThreads, 1)
-    bs_stream_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_q0,
-                     const __grid_constant__ CUtensorMap map_q1, const __grid_constant__ CUtensorMap map_s0,
-                     const __grid_constant__ CUtensorMap map_s1, const BsParams p) {
+__global__ void __launch_bounds__(kBsThreads, 2)
+    bs_stream_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                     const __grid_constant__ CUtensorMap map_sfb, const BsParams p) {
   using C = BsCfg<MODE>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -259,23 +295,26 @@ __global__ void __launch_bounds__(kBsThreads, 1)
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const int4 tile = p.tiles[item / p.MT];
         const int mt = item - (item / p.MT) * p.MT;
-        const int z = (MODE == BS_GATEUP) ? 2 * tile.x : tile.x;
-        const uint8_t* sfa = p.sfa + (((size_t)tile.x * p.MT + mt) * p.KC) * C::kNumA * kAtom;
-        for (int kc = 0; kc < p.KC; ++kc, ++kg) {
+        const size_t tile0 = ((size_t)tile.x * p.MT + mt) * p.KC;  // (expert, row tile) chunk 0
+        for (int ks = 0; ks < p.KS; ++ks, ++kg) {
           const int s = kg % C::kStages, u = kg / C::kStages;
           if (u > 0 && !mbar_wait(sfree(s), (u - 1) & 1, g, 1u)) {
             ok = false;
             break;
           }
+          const int kc0 = ks * C::kNK;
+          const int nk = min(C::kNK, p.KC - kc0);
+          // GATEUP: atoms / tiles (kc, gate), (kc, up); DOWN: (kc0), (kc0 + 1)
+          const int n_sfa = (MODE == BS_GATEUP) ? 2 : nk;
+          const size_t first = (MODE == BS_GATEUP) ? (tile0 + kc0) * 2 : tile0 + kc0;
           const uint32_t st = smem_u32(stage(s));
-          mbar_expect_tx(full(s), C::kTx);
-          tma_load_3d(st, &map_a, full(s), kc * kQK, mt * kQM, z);
-          if (MODE == BS_GATEUP) tma_load_3d(st + C::kA, &map_a, full(s), kc * kQK, mt * kQM, z + 1);
-          tma_load_2d(st + C::kOffB, &map_q0, full(s), kc * kQK, tile.y);
-          tma_load_2d(st + C::kOffB + C::kB, &map_q1, full(s), kc * kQK, tile.y);
-          bulk_load(st + C::kOffSfa, sfa + (size_t)kc * C::kNumA * kAtom, C::kNumA * kAtom, full(s));
-          tma_load_2d(st + C::kOffSfb, &map_s0, full(s), kc * 16, tile.y);
-          tma_load_2d(st + C::kOffSfb + kAtom, &map_s1, full(s), kc * 16, tile.y);
+          // the e2m1 copies count their packed bytes; boxes past the end of the
+          // tensor are zero-filled and counted in full
+          mbar_expect_tx(full(s), (uint32_t)(2 * (C::kA / 2) + 2 * C::kNK * C::kB + n_sfa * kAtom + 2 * C::kNK * kAtom));
+          tma_load_3d(st, &map_a, full(s), 0, 0, (int)first);
+          tma_load_4d(st + C::kOffB, &map_b, full(s), 0, tile.y, kc0, 0);
+          bulk_load(st + C::kOffSfa, p.sfa + first * kAtom, n_sfa * kAtom, full(s));
+          tma_load_4d(st + C::kOffSfb, &map_sfb, full(s), 0, tile.y, kc0, 0);
           ++issued;
         }
       }
@@ -290,7 +329,16 @@ __global__ void __launch_bounds__(kBsThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ================= MMA issue
+    // Descriptors are formed once: the start-address field of a shared-memory
+    // descriptor is (address >> 4) in its low bits, so every operand of every
+    // stage is base + (offset >> 4) with compile-time offsets (the stage ring
+    // ends below 256 KB, so the 14-bit field never carries).
     if (lane == 0) {
+      const uint32_t st0 = smem_u32(stage(0));
+      const uint64_t a_base = umma_desc_sw128(st0);
+      const uint64_t b_base = umma_desc_sw128(st0 + C::kOffB);
+      const uint64_t sfa_base = sf_desc(st0 + C::kOffSfa);
+      const uint64_t sfb_base = sf_desc(st0 + C::kOffSfb);
       int kg = 0, it = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
@@ -301,29 +349,39 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         }
         tc_fence_after();
         const uint32_t d0 = tmem + buf * C::kDCols;
-        for (int kc = 0; kc < p.KC; ++kc, ++kg) {
+        // MMA N: 16 when the tile holds at most 16 rows
+        const uint32_t n = p.tiles[item / p.MT].z > 16 ? 32u : 16u;
+        for (int ks = 0; ks < p.KS; ++ks, ++kg) {
           const int s = kg % C::kStages;
           if (!mbar_wait(full(s), (kg / C::kStages) & 1, g, 4u)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t st = smem_u32(stage(s));
+          const int nk = min(C::kNK, p.KC - ks * C::kNK);
+          const uint64_t so = (uint64_t)((uint32_t)(s * C::kStageBytes) >> 4);
+          const uint64_t a_d = a_base + so, b_d = b_base + so;
           const uint32_t sfc = tmem + C::kSfBase + s * C::kSfCols;
 #pragma unroll
-          for (int a = 0; a < C::kNumA; ++a) tc_cp_scales(sfc + 4 * a, sf_desc(st + C::kOffSfa + a * kAtom));
-          tc_cp_scales(sfc + 4 * C::kNumA, sf_desc(st + C::kOffSfb));
-          tc_cp_scales(sfc + 4 * C::kNumA + 4, sf_desc(st + C::kOffSfb + kAtom));
+          for (int j = 0; j < 2; ++j)
+            if (MODE == BS_GATEUP || j < nk) tc_cp_scales(sfc + 4 * j, sfa_base + so + (j * kAtom >> 4));
 #pragma unroll
-          for (int kb = 0; kb < kQK / 32; ++kb) {
-            const uint32_t idesc = bs_idesc(kb, kb);
+          for (int j = 0; j < 2 * C::kNK; ++j) tc_cp_scales(sfc + 8 + 4 * j, sfb_base + so + (j * kAtom >> 4));
+          const uint32_t first = ks ? 1u : 0u;
 #pragma unroll
-            for (int a = 0; a < C::kNumA; ++a)
+          for (int c = 0; c < C::kNK; ++c) {
+            if (c >= nk) break;
 #pragma unroll
-              for (int t = 0; t < 2; ++t)
-                umma_bs(d0 + a * kQN, umma_desc_sw128(st + a * C::kA + kb * 32),
-                        umma_desc_sw128(st + C::kOffB + t * C::kB + kb * 32), idesc, sfc + 4 * a,
-                        sfc + 4 * C::kNumA + 4 * t, (kc | kb | t) ? 1u : 0u);
+            for (int kb = 0; kb < kQK / 32; ++kb)
+#pragma unroll
+              for (int a = 0; a < C::kNumA; ++a)
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                  const int ablk = (MODE == BS_GATEUP) ? a : c;
+                  const int bblk = t * C::kNK + c;
+                  umma_bs(d0 + a * kQN, a_d + ((ablk * C::kA + kb * 32) >> 4), b_d + ((bblk * C::kB + kb * 32) >> 4),
+                          bs_idesc(kb, kb, n), sfc + 4 * ablk, sfc + 8 + 4 * bblk, (c | kb | t) ? 1u : first);
+                }
           }
           umma_commit(sfree(s));
         }
@@ -359,8 +417,11 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         tmem_ld32(lane_base + buf * C::kDCols + kQN, up);
         tc_fence_before();
         mbar_arrive(dempty(buf));
+        // h as bf16 and as the two e4m3 terms of the down GEMM's B operand
         const int KCo = p.ld_out / kQK;
-        const int b = m >> 5;
+        const size_t plane = (size_t)KCo * p.rows_max;
+        const size_t rbase = (size_t)(m >> 7) * p.rows_max;
+        const int grp = (m >> 5) & 3;
 #pragma unroll
         for (int j = 0; j < kQN; ++j) {
           if (j < tile.z) {
@@ -370,12 +431,11 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             const uint32_t emax = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(hb >> 7) & 0xFFu);
             const uint32_t s0 = term0_scale(emax), s1 = term1_scale(s0);
             const uint32_t q = split_e4m3(bf16_to_f32(hb), s0, s1);
-            p.hq0[row * p.ld_out + m] = (uint8_t)q;
-            p.hq1[row * p.ld_out + m] = (uint8_t)(q >> 8);
+            p.hq[(rbase + row) * kQK + (m & 127)] = (uint8_t)q;
+            p.hq[(plane + rbase + row) * kQK + (m & 127)] = (uint8_t)(q >> 8);
             if (lane == 0) {
-              const size_t so = (row * KCo + (b >> 2)) * 16 + (b & 3);
-              p.hsf0[so] = (uint8_t)s0;
-              p.hsf1[so] = (uint8_t)s1;
+              p.hsf[(rbase + row) * 16 + grp] = (uint8_t)s0;
+              p.hsf[(plane + rbase + row) * 16 + grp] = (uint8_t)s1;
             }
           }
         }
@@ -395,72 +455,74 @@ __global__ void __launch_bounds__(kBsThreads, 1)
 }
 
 // ------------------------------------------------------------------ host helpers
-// e2m1 weights [nmat][rows][cols/2] as a 3-D map, box 128 codes x 128 rows,
-// landing in 16-byte slots with a 128-byte swizzle.
-bool map_e2m1(CUtensorMap* map, const void* base, int nmat, int rows, int cols) {
+bool encode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
   EncodeFn fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)nmat};
-  const cuuint64_t strides[2] = {(cuuint64_t)cols / 2, (cuuint64_t)rows * cols / 2};
-  const cuuint32_t box[3] = {(cuuint32_t)kQK, (cuuint32_t)kQM, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(map, dt, rank, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-// bytes [rows][cols], box box_cols x box_rows
-bool map_u8(CUtensorMap* map, const void* base, int rows, int cols, int box_rows, int box_cols,
-            CUtensorMapSwizzle sw) {
-  EncodeFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)cols};
-  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+// e2m1 tiles [nbox][128 rows][64 bytes]; one copy = two adjacent tiles, each
+// landing as 128 rows of 128 bytes (16-byte slots) with a 128-byte swizzle.
+bool map_e2m1(CUtensorMap* map, const void* base, long long nbox) {
+  const cuuint64_t dims[3] = {(cuuint64_t)kQK, (cuuint64_t)kQM, (cuuint64_t)nbox};
+  const cuuint64_t strides[2] = {(cuuint64_t)kQK / 2, (cuuint64_t)kQM * kQK / 2};
+  const cuuint32_t box[3] = {(cuuint32_t)kQK, (cuuint32_t)kQM, 2};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+// Activation terms q[2][KC][rows_max][128] (box: 128 x 32 rows x nk chunks
+// x 2 terms, 128-byte swizzle) or scale records sf[2][KC][rows_max][16]
+// (box 16 x 32 x nk x 2, no swizzle).
+bool map_terms(CUtensorMap* map, const void* base, int KC, int rows_max, int inner, int nk,
+               CUtensorMapSwizzle sw) {
+  const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)rows_max, (cuuint64_t)KC, 2};
+  const cuuint64_t strides[3] = {(cuuint64_t)inner, (cuuint64_t)rows_max * inner, (cuuint64_t)KC * rows_max * inner};
+  const cuuint32_t box[4] = {(cuuint32_t)inner, (cuuint32_t)kQN, (cuuint32_t)nk, 2};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box, sw);
 }
 
 struct BsWs {
-  uint8_t *lq0, *lq1, *lsf0, *lsf1;  // latent rows, slot order [TKmax][L], [TKmax][L/128][16]
-  uint8_t *hq0, *hq1, *hsf0, *hsf1;  // h rows [TKmax][I], [TKmax][I/128][16]
+  int rows_max;
+  uint8_t *lq, *lsf;  // latent rows: terms [2][L/128][rows_max][128], records [2][L/128][rows_max][16]
+  uint8_t *hq, *hsf;  // h rows:      terms [2][I/128][rows_max][128], records [2][I/128][rows_max][16]
   size_t total;
 };
 BsWs bs_ws_view(void* base, const Dims& d, int max_tokens) {
   auto up = [](size_t v) { return (v + 255) / 256 * 256; };
-  const size_t TK = (size_t)std::min(max_tokens, kBsMaxTokens) * d.K;
-  const size_t sizes[8] = {TK * d.L, TK * d.L, TK * d.L / 8, TK * d.L / 8, TK * d.I, TK * d.I, TK * d.I / 8,
-                           TK * d.I / 8};
+  const size_t R = (size_t)std::min(max_tokens, kBsMaxTokens) * d.K;
+  const size_t sizes[4] = {2 * R * d.L, 2 * R * d.L / 8, 2 * R * d.I, 2 * R * d.I / 8};
   uint8_t* b = static_cast<uint8_t*>(base);
-  uint8_t* ptr[8];
+  uint8_t* ptr[4];
   size_t off = 0;
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < 4; ++i) {
     ptr[i] = b ? b + off : nullptr;
     off += up(sizes[i]);
   }
-  return BsWs{ptr[0], ptr[1], ptr[2], ptr[3], ptr[4], ptr[5], ptr[6], ptr[7], off};
+  return BsWs{(int)R, ptr[0], ptr[1], ptr[2], ptr[3], off};
 }
 
 template <int MODE>
-cudaError_t launch_bs(const BsPlan& p, const uint8_t* wq, const uint8_t* sfa, int nmat, int rows, int cols,
-                      const uint8_t* q0, const uint8_t* q1, const uint8_t* sf0, const uint8_t* sf1, int TK,
-                      const int4* tiles, const int* count, BsParams prm, cudaStream_t s) {
-  CUtensorMap ma, m0, m1, s0, s1;
-  const int KC = cols / kQK;
-  if (!map_e2m1(&ma, wq, nmat, rows, cols) || !map_u8(&m0, q0, TK, cols, kQN, kQK, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !map_u8(&m1, q1, TK, cols, kQN, kQK, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !map_u8(&s0, sf0, TK, KC * 16, kQN, 16, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !map_u8(&s1, sf1, TK, KC * 16, kQN, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
+cudaError_t launch_bs(const BsPlan& p, const uint8_t* wq, const uint8_t* sfa, int n_exp, int rows, int cols,
+                      const uint8_t* q, const uint8_t* sf, int rows_max, const int4* tiles, const int* count,
+                      BsParams prm, cudaStream_t s) {
+  using C = BsCfg<MODE>;
+  CUtensorMap ma, mb, msf;
+  const int KC = cols / kQK, MT = rows / kQM;
+  const long long nbox = (long long)n_exp * MT * KC * C::kNumA;
+  if (!map_e2m1(&ma, wq, nbox) || !map_terms(&mb, q, KC, rows_max, kQK, C::kNK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !map_terms(&msf, sf, KC, rows_max, 16, C::kNK, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   prm.sfa = sfa;
-  prm.MT = rows / kQM;
+  prm.MT = MT;
   prm.KC = KC;
+  prm.KS = (KC + C::kNK - 1) / C::kNK;
   prm.tiles = tiles;
   prm.count = count;
+  prm.rows_max = rows_max;
   prm.status = p.status;
   prm.limit_ns = p.limit_ns;
-  bs_stream_kernel<MODE><<<p.num_sms, kBsThreads, BsCfg<MODE>::kSmem, s>>>(ma, m0, m1, s0, s1, prm);
+  bs_stream_kernel<MODE><<<2 * p.num_sms, kBsThreads, C::kSmem, s>>>(ma, mb, msf, prm);
   return cudaGetLastError();
 }
 
@@ -469,6 +531,12 @@ cudaError_t launch_bs(const BsPlan& p, const uint8_t* wq, const uint8_t* sfa, in
 size_t bs_weight_bytes(const Dims& d) {
   const size_t E = d.E, I = d.I, L = d.L;
   return E * 2 * I * L / 2 + E * 2 * I * L / 32 + E * L * I / 2 + E * L * I / 32;
+}
+
+cudaError_t bs_e2m1_boxes(const uint8_t* packed, int ne, int rows, int cols, int n_mat, int mat, uint8_t* out,
+                          cudaStream_t s) {
+  e2m1_boxes_kernel<<<1024, 256, 0, s>>>(packed, ne, rows, cols, n_mat, mat, out);
+  return cudaGetLastError();
 }
 
 cudaError_t bs_scale_atoms(const uint8_t* scale, int ne, int rows, int cols, int n_mat, int mat, uint8_t* out,
@@ -495,7 +563,7 @@ cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims
   const BsWs ws = bs_ws_view(p.ws, d, p.max_tokens);
   const long long halves = (long long)TK * (d.L / kQK);
   const int blocks = (int)std::min<long long>((halves * 16 + 255) / 256, 4LL * p.num_sms);
-  quant_rows_kernel<<<blocks, 256, 0, s>>>(w.lat, w.perm, d.K, TK, d.L, ws.lq0, ws.lq1, ws.lsf0, ws.lsf1);
+  quant_rows_kernel<<<blocks, 256, 0, s>>>(w.lat, w.perm, d.K, TK, d.L, ws.rows_max, ws.lq, ws.lsf);
   return cudaGetLastError();
 }
 
@@ -508,14 +576,12 @@ cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* t
   BsParams prm{};
   prm.ld_out = d.I;
   prm.h = w.h;
-  prm.hq0 = ws.hq0;
-  prm.hq1 = ws.hq1;
-  prm.hsf0 = ws.hsf0;
-  prm.hsf1 = ws.hsf1;
+  prm.hq = ws.hq;
+  prm.hsf = ws.hsf;
   prm.beta = d.beta;
   prm.beta_lin = d.beta_lin;
-  return launch_bs<BS_GATEUP>(p, bw.gu_q, bw.gu_sf, 2 * d.E, d.I, d.L, ws.lq0, ws.lq1, ws.lsf0, ws.lsf1, TK, tiles,
-                              tile_count, prm, s);
+  return launch_bs<BS_GATEUP>(p, bw.gu_q, bw.gu_sf, d.E, d.I, d.L, ws.lq, ws.lsf, ws.rows_max, tiles, tile_count,
+                              prm, s);
 }
 
 cudaError_t bs_stream_down(const BsPlan& p, const BsWeights& bw, const int4* tiles, const int* tile_count,
@@ -527,8 +593,8 @@ cudaError_t bs_stream_down(const BsPlan& p, const BsWeights& bw, const int4* til
   BsParams prm{};
   prm.ld_out = d.L;
   prm.o = w.o;
-  return launch_bs<BS_DOWN>(p, bw.d_q, bw.d_sf, d.E, d.L, d.I, ws.hq0, ws.hq1, ws.hsf0, ws.hsf1, TK, tiles,
-                            tile_count, prm, s);
+  return launch_bs<BS_DOWN>(p, bw.d_q, bw.d_sf, d.E, d.L, d.I, ws.hq, ws.hsf, ws.rows_max, tiles, tile_count, prm,
+                            s);
 }
 
 }  // namespace k3

@@ -12,9 +12,10 @@
 namespace k3 {
 
 // Expert weights in the block-scaled layout (device memory).
-//   gu_q : [E][2][I][L/2]  e2m1 nibbles (checkpoint order), gate then up
+//   gu_q : [E][I/128][L/128][2][128][64] e2m1 nibbles in checkpoint order,
+//          one contiguous 8 KB block per 128 x 128 tile, gate then up
 //   gu_sf: [E][I/128][L/128][2][512] e8m0 scale atoms (gate, up)
-//   d_q  : [E][L][I/2]
+//   d_q  : [E][L/128][I/128][128][64]
 //   d_sf : [E][L/128][I/128][512]
 struct BsWeights {
   uint8_t* gu_q = nullptr;
@@ -23,6 +24,10 @@ struct BsWeights {
   uint8_t* d_sf = nullptr;
 };
 size_t bs_weight_bytes(const Dims& d);
+// Packed nibbles [ne][rows][cols/2] into the box layout above (slot `mat`
+// of n_mat matrices per expert).
+cudaError_t bs_e2m1_boxes(const uint8_t* packed, int ne, int rows, int cols, int n_mat, int mat, uint8_t* out,
+                          cudaStream_t s);
 // Scale atoms of n_mat matrices [ne][rows][cols/32] into out (layout above;
 // mat_stride atoms between experts, `mat` selects the slot in an atom pair).
 cudaError_t bs_scale_atoms(const uint8_t* scale, int ne, int rows, int cols, int n_mat, int mat, uint8_t* out,
