@@ -413,7 +413,7 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
     k3::umma_tile_list(c->umma, &tiles, &tile_count, &bn);
     K3_LAUNCH(k3::launch_route_small(w.logits, T, d.E, c->bias, d.K, d.norm_topk, d.rsf, idx, wts, w.counts,
                                      w.offsets, w.active, w.perm, w.slot, bn, tiles, tile_count, s),
-              1, "top-k + permute");
+              2, "top-k + permute");
   } else {
     K3_LAUNCH(k3::launch_topk(w.logits, T, d.E, d.E, c->bias, d.K, d.norm_topk, d.rsf, idx, wts, s), 1, "top-k");
     K3_LAUNCH(k3::launch_permute(idx, T, d.K, d.E, w.blk_hist, w.counts, w.offsets, w.active, w.perm, w.slot, s), 3,

@@ -122,84 +122,168 @@ cudaError_t launch_dense_gemv(const uint16_t* W, int M, int K, const uint16_t* X
 //   are taken one at a time, ties to the lower expert id; weights from the
 //   unbiased s, divided by their sum when norm_topk, times rsf.
 // =====================================================================
-// One warp selects the K experts of one token from its fp32 logits row and
-// writes idx[0..K) and w[0..K) (ties to the lower id; weights summed in k
-// order for a fixed rounding sequence).
-// `scores` (optional, E floats of shared memory for this warp) keeps the
-// sigmoid scores so that the selected ones are read back without a
-// dependent global load per selection.
-template <int EPL>
-__device__ __forceinline__ void topk_warp(const float* __restrict__ logit_row, int E,
-                                          const float* __restrict__ bias, int K, int norm_topk, float rsf,
-                                          int32_t* __restrict__ idx, float* __restrict__ w,
-                                          float* scores = nullptr) {
-  const int lane = threadIdx.x & 31;
-  float key[EPL];
-  unsigned long long avail = 0;
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E) {
-      const float s = 1.0f / (1.0f + expf(-logit_row[e]));
-      if (scores) scores[e] = s;
-      key[i] = s + bias[e];
-      avail |= 1ull << i;
-    } else {
-      key[i] = -INFINITY;
-    }
-  }
-  if (scores) __syncwarp();
-  float my_s = 0.f;
-  for (int k = 0; k < K; ++k) {
-    float bk = -INFINITY;
-    int be = INT_MAX;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      if (!((avail >> i) & 1ull)) continue;
-      const int e = lane + 32 * i;
-      if (key[i] > bk || (key[i] == bk && e < be)) {
-        bk = key[i];
-        be = e;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ok = __shfl_xor_sync(0xFFFFFFFFu, bk, off);
-      const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
-      if (ok > bk || (ok == bk && oe < be)) {
-        bk = ok;
-        be = oe;
-      }
-    }
-    if (be != INT_MAX && (be & 31) == lane) avail &= ~(1ull << (be >> 5));
-    // the selected expert's score, recomputed with the same expression
-    if (lane == k) my_s = be < E ? (scores ? scores[be] : 1.0f / (1.0f + expf(-logit_row[be]))) : 0.f;
-    if (lane == 0) idx[k] = be;
-  }
-  float sum = 0.f;
-  for (int k = 0; k < K; ++k) sum += __shfl_sync(0xFFFFFFFFu, my_s, k);
-  if (lane < K) w[lane] = (norm_topk ? my_s / sum : my_s) * rsf;
+// Router top-K (kimi-k3-mlx README, "Architecture" table: sigmoid router,
+// e_score_correction_bias added for selection only).  One CTA per token:
+//   s[e] = 1 / (1 + exp(-logit[e])),  key[e] = s[e] + bias[e] (fp32);
+//   the K largest keys (ties -> lower expert id), in descending key order;
+//   w[k] = s[idx[k]] / sum_k s[idx[k]] * rsf (sum in k order, fp32), or
+//   s * rsf without renormalisation.
+// The K-th largest key is found exactly by a most-significant-digit-first
+// radix select (four 8-bit digits) over an order-preserving integer image of
+// the fp32 keys; keys above it are taken, keys equal to it by ascending id.
+// The K winners are then ordered by (key desc, id asc) with a warp bitonic
+// sort.  256 threads, ceil(E / 256) keys per thread.
+// =====================================================================
+__device__ __forceinline__ uint32_t ordered_bits(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-template <int EPL>
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int T, int E, int ld,
-                                                   const float* __restrict__ bias, int K, int norm_topk, float rsf,
-                                                   int32_t* __restrict__ idx, float* __restrict__ w) {
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t >= T) return;
-  topk_warp<EPL>(logits + (size_t)t * ld, E, bias, K, norm_topk, rsf, idx + (size_t)t * K, w + (size_t)t * K);
+template <int EPT>
+__global__ void __launch_bounds__(256) topk_cta_kernel(const float* __restrict__ logits, int E, int ld,
+                                                       const float* __restrict__ bias, int K, int norm_topk,
+                                                       float rsf, int32_t* __restrict__ idx,
+                                                       float* __restrict__ w) {
+  __shared__ int hist[256];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_need, n_cand, n_eq;
+  __shared__ unsigned long long cand[32];
+  __shared__ float cand_s[32];
+  __shared__ int eq_e[2048];
+  __shared__ float eq_s[2048];
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float* row = logits + (size_t)t * ld;
+  uint32_t u[EPT];
+  float sc[EPT];
+#pragma unroll
+  for (int j = 0; j < EPT; ++j) {
+    const int e = tid + 256 * j;
+    u[j] = 0u;  // below every key's image (the image of -inf is 0x007FFFFF)
+    sc[j] = 0.f;
+    if (e < E) {
+      const float sg = 1.0f / (1.0f + expf(-row[e]));
+      sc[j] = sg;
+      u[j] = ordered_bits(sg + bias[e]);
+    }
+  }
+  // ---- radix select of the K-th largest image
+  uint32_t prefix = 0u;
+  int need = K;
+#pragma unroll 1
+  for (int pass = 3; pass >= 0; --pass) {
+    const int shift = 8 * pass;
+    const uint32_t hmask = pass == 3 ? 0u : (0xFFFFFFFFu << (shift + 8));
+    hist[tid] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < EPT; ++j)
+      if (u[j] != 0u && (u[j] & hmask) == prefix) atomicAdd(&hist[(u[j] >> shift) & 255u], 1);
+    __syncthreads();
+    if (warp == 0) {
+      // lane l holds digits 255-8l .. 248-8l (descending)
+      int c[8], tot = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c[i] = hist[255 - 8 * lane - i];
+        tot += c[i];
+      }
+      int incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      const int excl = incl - tot;
+      const unsigned owner = __ballot_sync(0xFFFFFFFFu, excl < need && need <= incl);
+      if (lane == __ffs(owner) - 1) {
+        int acc = excl;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (acc + c[i] >= need) {
+            s_prefix = prefix | ((uint32_t)(255 - 8 * lane - i) << shift);
+            s_need = need - acc;
+            break;
+          }
+          acc += c[i];
+        }
+      }
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    need = s_need;
+  }
+  // ---- the K winners: images above the K-th, then `need` of the equal ones by ascending id
+  if (tid == 0) {
+    n_cand = 0;
+    n_eq = 0;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < EPT; ++j) {
+    const int e = tid + 256 * j;
+    if (u[j] > prefix) {
+      const int k = atomicAdd(&n_cand, 1);
+      cand[k] = ((unsigned long long)u[j] << 32) | (0xFFFFFFFFu - (uint32_t)e);
+      cand_s[k] = sc[j];
+    } else if (u[j] == prefix && u[j] != 0u) {
+      const int k = atomicAdd(&n_eq, 1);
+      eq_e[k] = e;
+      eq_s[k] = sc[j];
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int k = n_cand;
+    // the `need` lowest ids among the equal keys (all of them in the usual case need == n_eq)
+    for (int r = 0; r < need; ++r) {
+      int best = -1;
+      for (int i = 0; i < n_eq; ++i)
+        if (eq_e[i] >= 0 && (best < 0 || eq_e[i] < eq_e[best])) best = i;
+      cand[k] = ((unsigned long long)prefix << 32) | (0xFFFFFFFFu - (uint32_t)eq_e[best]);
+      cand_s[k] = eq_s[best];
+      eq_e[best] = -1;
+      ++k;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // bitonic sort of the K (<= 32) winners, descending; lanes >= K hold 0
+    unsigned long long v = lane < K ? cand[lane] : 0ull;
+    float sv = lane < K ? cand_s[lane] : 0.f;
+#pragma unroll
+    for (int k2 = 2; k2 <= 32; k2 <<= 1) {
+#pragma unroll
+      for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
+        const unsigned long long ov = __shfl_xor_sync(0xFFFFFFFFu, v, j2);
+        const float os = __shfl_xor_sync(0xFFFFFFFFu, sv, j2);
+        const bool up = (lane & k2) == 0;      // this block sorts descending when up
+        const bool lower = (lane & j2) == 0;   // this lane keeps the larger value when lower == up
+        const bool take = (lower == up) ? (ov > v) : (ov < v);
+        if (take) {
+          v = ov;
+          sv = os;
+        }
+      }
+    }
+    float sum = 0.f;
+    for (int k = 0; k < K; ++k) sum += __shfl_sync(0xFFFFFFFFu, sv, k);
+    if (lane < K) {
+      idx[(size_t)t * K + lane] = (int32_t)(0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFull));
+      w[(size_t)t * K + lane] = (norm_topk ? sv / sum : sv) * rsf;
+    }
+  }
 }
 
 cudaError_t launch_topk(const float* logits, int T, int E, int ld, const float* bias, int K, int norm_topk,
                         float rsf, int32_t* idx, float* w, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  const int blocks = (T + 7) / 8;
-  if (E <= 32 * 8)
-    topk_kernel<8><<<blocks, 256, 0, s>>>(logits, T, E, ld, bias, K, norm_topk, rsf, idx, w);
-  else if (E <= 32 * 32)
-    topk_kernel<32><<<blocks, 256, 0, s>>>(logits, T, E, ld, bias, K, norm_topk, rsf, idx, w);
+  if (K > 32 || E > 2048 || K > E) return cudaErrorInvalidValue;
+  if (E <= 256)
+    topk_cta_kernel<1><<<T, 256, 0, s>>>(logits, E, ld, bias, K, norm_topk, rsf, idx, w);
+  else if (E <= 1024)
+    topk_cta_kernel<4><<<T, 256, 0, s>>>(logits, E, ld, bias, K, norm_topk, rsf, idx, w);
   else
-    topk_kernel<64><<<blocks, 256, 0, s>>>(logits, T, E, ld, bias, K, norm_topk, rsf, idx, w);
+    topk_cta_kernel<8><<<T, 256, 0, s>>>(logits, E, ld, bias, K, norm_topk, rsf, idx, w);
   return cudaGetLastError();
 }
 
@@ -333,23 +417,18 @@ cudaError_t launch_permute(const int32_t* idx, int T, int K, int E, int* blk_his
 }
 
 // =====================================================================
-// Routing for small batches (T*K <= 1024) in ONE CTA: top-K per token, the
-// per-expert histogram, offsets, active list, the stable slot order and its
-// inverse (same results as topk_kernel + the three permutation kernels), and
-// the tile list of the streaming expert kernels (tiles of at most bn_max
-// slots per expert: {expert, first slot, rows, rows rounded up to 16}).
+// Permutation for small batches (T*K <= 1024) in ONE CTA, from the top-K
+// of topk_cta_kernel: the per-expert histogram, offsets, active list, the
+// stable slot order and its inverse (same results as the three
+// permutation kernels), and the tile list of the streaming expert kernels
+// (tiles of at most bn_max slots per expert: {expert, first slot, rows,
+// rows rounded up to 16}).
 // =====================================================================
-template <int EPL>
-__global__ void __launch_bounds__(1024) route_small_kernel(const float* __restrict__ logits, int T, int E,
-                                                           const float* __restrict__ bias, int K, int norm_topk,
-                                                           float rsf, int32_t* __restrict__ idx,
-                                                           float* __restrict__ w, int* __restrict__ counts,
-                                                           int* __restrict__ offsets, int* __restrict__ active,
-                                                           int* __restrict__ perm, int* __restrict__ slot,
-                                                           int bn_max, int4* __restrict__ tiles,
-                                                           int* __restrict__ tile_count) {
-  extern __shared__ float score_cache[];  // [32 warps][E]
-  __shared__ int sidx[1024];
+__global__ void __launch_bounds__(1024) perm_small_kernel(const int32_t* __restrict__ idx, int T, int E, int K,
+                                                          int* __restrict__ counts, int* __restrict__ offsets,
+                                                          int* __restrict__ active, int* __restrict__ perm,
+                                                          int* __restrict__ slot, int bn_max,
+                                                          int4* __restrict__ tiles, int* __restrict__ tile_count) {
   __shared__ int hist[2048];
   __shared__ int base[2048];
   __shared__ int warp_tot[32];
@@ -357,16 +436,9 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const float* __restri
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int TK = T * K;
   for (int e = threadIdx.x; e < E; e += 1024) hist[e] = 0;
-  // top-K, one warp per token
-  for (int t = warp; t < T; t += 32) {
-    topk_warp<EPL>(logits + (size_t)t * E, E, bias, K, norm_topk, rsf, idx + (size_t)t * K, w + (size_t)t * K,
-                   score_cache + (size_t)warp * E);
-  }
-  __syncthreads();  // idx written by lane 0 of each warp (global memory, same CTA)
+  __syncthreads();
   const int a = threadIdx.x;
   const int e_a = a < TK ? idx[a] : -1;
-  if (a < TK) sidx[a] = e_a;
-  __syncthreads();
   if (a < TK) atomicAdd(&hist[e_a], 1);
   __syncthreads();
   // offsets and active list (experts in chunks of 1024)
@@ -439,16 +511,9 @@ cudaError_t launch_route_small(const float* logits, int T, int E, const float* b
                                int bn_max, int4* tiles, int* tile_count, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   if (T * K > 1024 || E > 2048) return cudaErrorInvalidValue;
-  const size_t sm = sizeof(float) * 32 * (size_t)E;
-  if (E <= 32 * 8)
-    route_small_kernel<8><<<1, 1024, sm, s>>>(logits, T, E, bias, K, norm_topk, rsf, idx, w, counts, offsets, active,
-                                              perm, slot, bn_max, tiles, tile_count);
-  else if (E <= 32 * 32)
-    route_small_kernel<32><<<1, 1024, sm, s>>>(logits, T, E, bias, K, norm_topk, rsf, idx, w, counts, offsets,
-                                               active, perm, slot, bn_max, tiles, tile_count);
-  else
-    route_small_kernel<64><<<1, 1024, sm, s>>>(logits, T, E, bias, K, norm_topk, rsf, idx, w, counts, offsets,
-                                               active, perm, slot, bn_max, tiles, tile_count);
+  cudaError_t e = launch_topk(logits, T, E, E, bias, K, norm_topk, rsf, idx, w, s);
+  if (e != cudaSuccess) return e;
+  perm_small_kernel<<<1, 1024, 0, s>>>(idx, T, E, K, counts, offsets, active, perm, slot, bn_max, tiles, tile_count);
   return cudaGetLastError();
 }
 
@@ -730,13 +795,6 @@ cudaError_t prepare_decode_kernels(const Dims& d) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(combine_rmsnorm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(sizeof(float) * d.L));
-  const int rs_smem = (int)(sizeof(float) * 32 * (size_t)d.E);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(route_small_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, rs_smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(route_small_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, rs_smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(route_small_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, rs_smem);
   return e;
 }
 

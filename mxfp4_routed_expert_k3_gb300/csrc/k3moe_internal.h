@@ -46,7 +46,8 @@ cudaError_t launch_gateup_gemv(const uint8_t* gu_tiles, const uint16_t* lat, con
 cudaError_t launch_down_gemv(const uint8_t* d_tiles, const uint16_t* h, const int* active, const int* offsets,
                              int max_active, const Dims& d, float* o, cudaStream_t s);
 cudaError_t prepare_decode_kernels(const Dims& d);
-// T*K <= 1024: top-K + permutation + streaming tile list in one CTA
+// T*K <= 1024: top-K (one CTA per token) + permutation and streaming tile
+// list in one CTA
 cudaError_t launch_route_small(const float* logits, int T, int E, const float* bias, int K, int norm_topk, float rsf,
                                int32_t* idx, float* w, int* counts, int* offsets, int* active, int* perm, int* slot,
                                int bn_max, int4* tiles, int* tile_count, cudaStream_t s);

@@ -534,6 +534,7 @@ struct DCfg {
 
 struct DenseStreamParams {
   int MT, KS, nkc, ks_per_chunk, M, T, split;
+  uint32_t b_bytes;  // bytes of one token-row box: 128 x (T rounded up to 16)
   float* part;     // [nkc][T][M] fp32 partial sums
   int* counters;   // [MT][4] chunks finished per row tile and warp (zero between calls)
   float* out_f32;  // rows m < split: out_f32[t * split + m]
@@ -588,7 +589,7 @@ __global__ void __launch_bounds__(kDThreads, 1) umma_dense_stream_kernel(const _
             ok = false;
             break;
           }
-          mbar_expect_tx(full(s), C::kABytes + C::kBBytes);
+          mbar_expect_tx(full(s), C::kABytes + p.b_bytes);
           tma_load_2d(smem_u32(stage_a(s)), &map_a, full(s), ks * kBK, mt * kBM);
           tma_load_2d(smem_u32(stage_b(s)), &map_b, full(s), ks * kBK, 0);
           ++issued;
@@ -1039,12 +1040,16 @@ cudaError_t umma_dense_small(const UmmaPlan& p, const uint16_t* W, int M, int K,
   if (T > kDNB) return cudaErrorInvalidValue;
   UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
   CUtensorMap ma, mb;
-  if (!make_map(&ma, W, M, K, kBM) || !make_map(&mb, X, T, K, kDNB)) return cudaErrorInvalidValue;
+  const int n_mma = (T + 15) & ~15;  // token rows per box (the MMA's N)
+  if (!make_map(&ma, W, M, K, kBM) || !make_map(&mb, X, T, K, n_mma)) return cudaErrorInvalidValue;
   DenseStreamParams q{};
   q.MT = (M + kBM - 1) / kBM;
   q.KS = K / kBK;
-  const int want = (2 * p.num_sms + q.MT - 1) / q.MT;
-  const int nkc0 = std::max(1, std::min({want, q.KS, kMaxChunks}));
+  q.b_bytes = (uint32_t)(n_mma * kBK * 2);
+  // K chunks per row tile: as many as keep every (row tile, chunk) item in
+  // one wave of the grid (a second wave for a few items doubles the time)
+  const int fit = (2 * p.num_sms) / q.MT;
+  const int nkc0 = std::max(1, std::min({fit, q.KS, kMaxChunks}));
   q.ks_per_chunk = (q.KS + nkc0 - 1) / nkc0;
   q.nkc = (q.KS + q.ks_per_chunk - 1) / q.ks_per_chunk;
   q.M = M;

@@ -201,3 +201,47 @@ def test_route_entry_point_matches_oracle():
     torch.cuda.synchronize()
     assert np.allclose(logits.cpu().numpy(), logits_r, rtol=1e-5, atol=1e-5)
     assert_routing_equal(idx.cpu().numpy(), wt.cpu().numpy(), idx_r, w_r)
+
+
+@pytest.mark.parametrize("n_experts", [64, 896])
+def test_route_exact_ties_go_to_lower_ids(n_experts):
+    """Duplicated router rows with equal bias give bit-identical keys: the
+    selection must take the lower expert ids, in the oracle's order
+    (kimi-k3-mlx README, "Architecture": top-k by score + bias; ties are
+    this implementation's reading, lower id first)."""
+    d = TINY.with_(n_experts=n_experts)
+    w = synth.layer_weights(d, seed=5)
+    rw = w["router_w"].copy()
+    bias = w["router_bias"].copy()
+    # experts 3, 17, 40, 41, 60 (and more when E is large) copy expert 9
+    dups = [3, 17, 40, 41, 60] + ([100, 333, 700, 701, 895] if n_experts > 64 else [])
+    for e in dups:
+        rw[e] = rw[9]
+        bias[e] = bias[9]
+    bias[9] += np.float32(0.5)  # push the tied group into the top-K
+    for e in dups:
+        bias[e] = bias[9]
+    T = 16
+    x = synth.token_rows(d, 77, T)
+    idx_r, w_r, logits_r = ora.route(d, x, rw, bias)
+    xd = torch.from_numpy(x.view(np.int16)).cuda()
+    rwd = torch.from_numpy(rw.view(np.int16)).cuda()
+    b = torch.from_numpy(bias).cuda()
+    logits = torch.empty((T, d.n_experts), dtype=torch.float32, device="cuda")
+    idx = torch.empty((T, d.top_k), dtype=torch.int32, device="cuda")
+    wt = torch.empty((T, d.top_k), dtype=torch.float32, device="cuda")
+    k3moe.route(xd, T, rwd, b, d.n_experts, d.hidden, d.top_k, 1, 1.0, logits, idx, wt,
+                torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    lg = logits.cpu().numpy()
+    # the duplicated rows produce identical logits on the device, so the keys tie exactly there
+    for e in dups:
+        assert np.array_equal(lg[:, e], lg[:, 9])
+    # selection from the device's own logits by the oracle's rule
+    idx_dev_rule, w_dev_rule = ora.route_from_logits(d, lg, bias)
+    assert np.array_equal(idx.cpu().numpy(), idx_dev_rule)
+    assert np.allclose(wt.cpu().numpy(), w_dev_rule, rtol=1e-6, atol=0)
+    # at least one token has a tie crossing the K-th position or inside the top-K
+    sel = idx.cpu().numpy()
+    tied = [e for e in [9] + dups]
+    assert any(len(set(sel[t]) & set(tied)) >= 2 for t in range(T))
