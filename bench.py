@@ -32,6 +32,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 DECODE_BATCHES = (1, 8, 64)
+PREFILL_T = 8192
 METRIC = "LatentMoE MXFP4 layer tokens/s (K3 dims); decode HBM GB/s vs ~8 TB/s"
 FLUSH_BYTES = 512 << 20
 REASON_BITS = {
@@ -185,7 +186,8 @@ def run_ours(args, rank, world, local_rank):
     batches = DECODE_BATCHES
     maxT = max(batches)
     w = synth.layer_weights(d, seed=1)
-    layer = k3moe.Layer(d, w, max_tokens=maxT, device=local_rank, force_path=args.path)
+    prefill_T = 0 if args.no_prefill else PREFILL_T
+    layer = k3moe.Layer(d, w, max_tokens=max(maxT, prefill_T), device=local_rank, force_path=args.path)
     stream = torch.cuda.Stream(device=dev)
     pool = args.warmup + args.steps
     # fresh token batches for every step, resident in HBM before timing
@@ -312,6 +314,7 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- e2e: through the public C-ABI call with HOST buffers (pinned), copies timed
     e2e = run_e2e(layer, d, batches, args, rank, dev, stream)
+    prefill = run_prefill(layer, d, prefill_T, rank, dev, stream, peaks) if prefill_T else None
     e2e_value = reduce_sum_over_ranks(e2e["tokens_per_s_rank"], world, dev)
 
     cpu = None
@@ -336,12 +339,53 @@ def run_ours(args, rank, world, local_rank):
         "decode_sweep": sweep,
         "wall_s_timed_region": t_wall,
     }
+    if prefill is not None:
+        out["prefill"] = prefill
     if clk is not None:
         out["clocks"] = clk
     if cpu is not None:
         out["cpu_baseline"] = cpu
     layer.close()
     return out
+
+
+def run_prefill(layer, d, T, rank, dev, stream, peaks, reps: int = 5):
+    """Prefill-size forward (T tokens, near-uniform routing): device time per
+    forward with CUDA events, FLOP rate against the bf16 dense tensor peak.
+    The forward touches every expert (15.8 GB of weights, far above L2), so
+    no flush is needed between forwards."""
+    import torch
+    from mxfp4_routed_expert_k3_gb300 import k3moe, synth
+    x = torch.from_numpy(synth.token_rows(d, 7000 + rank, T).view(np.int16)).to(dev)
+    y = torch.empty((T, d.hidden), dtype=torch.int16, device=dev)
+    idx = torch.empty((T, d.top_k), dtype=torch.int32, device=dev)
+    wt = torch.empty((T, d.top_k), dtype=torch.float32, device=dev)
+    k3moe.profile(layer.ctx, True)
+    for _ in range(2):
+        layer.forward(x, y, idx, wt, stream=stream)
+    stream.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    kms = {}
+    for i in range(reps):
+        ev[i][0].record(stream)
+        layer.forward(x, y, idx, wt, stream=stream)
+        ev[i][1].record(stream)
+        stream.synchronize()
+        for name, ms in k3moe.profile_read(layer.ctx):
+            kms.setdefault(name, []).append(ms)
+    assert layer.status() == 0, k3moe.last_error(layer.ctx)
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+    flop = d.flop_per_token() * T
+    tflops = flop / (ms / 1e3) / 1e12
+    peak = peaks.get("bf16_tflops") if isinstance(peaks, dict) else None
+    return {"T": T, "ms_per_forward": ms, "tokens_per_s": T / (ms / 1e3), "algorithmic_tflop": flop / 1e12,
+            "tflops": tflops, "bound": "tensor", "peak_bf16_tflops": peak,
+            "frac": tflops / peak if peak else None,
+            "peak_bf16_tflops_sustained": peaks.get("bf16_tflops_sustained") if isinstance(peaks, dict) else None,
+            "path": layer.query("path_last"),
+            "kernel_ms": {k: statistics.mean(v) for k, v in kms.items()},
+            "how": f"CUDA events around each of {reps} forwards after 2 warm-up forwards; "
+                   "FLOP = 2*(E*H + 2*L*H) + top_k*(2*2*I*L + 2*L*I) per token"}
 
 
 def run_e2e(layer, d, batches, args, rank, dev, stream):
@@ -426,6 +470,7 @@ def main():
     ap.add_argument("--cpu-sample", type=int, default=16, help="tokens in the oracle CPU baseline sample")
     ap.add_argument("--ref-tokens-per-step", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the T=8192 prefill measurement")
     ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2, 3, 4],
                     help="kernel path (0 = the library's choice by token count; see k3moe_config.force_path)")
     ap.add_argument("--experts", type=int, default=896,
