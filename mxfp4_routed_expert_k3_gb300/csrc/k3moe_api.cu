@@ -194,7 +194,7 @@ int k3moe_create(const k3moe_config* cfg, int cuda_device, k3moe_ctx** out) {
   c->umma.limit_ns = (uint64_t)c->cfg.spin_timeout_ms * 1000000ull;
   c->bs.ws = take(parts[17]);
   c->bs.ws_bytes = bs_bytes;
-  c->bs.max_tokens = std::min((int)Tm, k3::kBsMaxTokens);
+  c->bs.max_tokens = (int)Tm;
   c->bs.status = c->w.status;
   c->bs.num_sms = prop.multiProcessorCount;
   c->bs.limit_ns = c->umma.limit_ns;
@@ -363,8 +363,6 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
   // the block-scaled MXFP4 tensor cores
   int path = c->cfg.force_path;
   if (path == 0) path = T <= 64 ? 4 : 2;
-  if (path == 4 && T > c->bs.max_tokens)
-    return fail(c, K3MOE_EINVAL, "path 4 serves T <= %d (got %d)", c->bs.max_tokens, T);
   const bool stream = path == 3 || path == 4;
   const bool big = path == 2;
   c->path_last = path;
@@ -411,8 +409,11 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
     int* tile_count;
     int bn;
     k3::umma_tile_list(c->umma, &tiles, &tile_count, &bn);
+    // path 4 also needs the slot -> tile map (its tiles have bs_tile_rows(T) <= bn rows)
+    int* slot_tile = path == 4 ? k3::bs_slot_tile(c->bs) : nullptr;
+    if (path == 4) bn = k3::bs_tile_rows(T);
     K3_LAUNCH(k3::launch_route_small(w.logits, T, d.E, c->bias, d.K, d.norm_topk, d.rsf, idx, wts, w.counts,
-                                     w.offsets, w.active, w.perm, w.slot, bn, tiles, tile_count, s),
+                                     w.offsets, w.active, w.perm, w.slot, bn, tiles, tile_count, slot_tile, s),
               2, "top-k + permute");
   } else {
     K3_LAUNCH(k3::launch_topk(w.logits, T, d.E, d.E, c->bias, d.K, d.norm_topk, d.rsf, idx, wts, s), 1, "top-k");
@@ -428,10 +429,12 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
     int* tile_count;
     int bn;
     k3::umma_tile_list(c->umma, &tiles, &tile_count, &bn);
-    if (!fused_route) K3_LAUNCH(k3::umma_stream_tiles(c->umma, w, T, d, s), 1, "tile list");
+    bn = k3::bs_tile_rows(T);
+    if (!fused_route)
+      K3_LAUNCH(k3::umma_stream_tiles(c->umma, w, T, d, bn, k3::bs_slot_tile(c->bs), s), 1, "tile list");
     K3_LAUNCH(k3::bs_quantize_latent(c->bs, w, T, d, s), 1, "latent rows -> e4m3 terms");
-    K3_LAUNCH(k3::bs_stream_gateup(c->bs, c->bw, tiles, tile_count, w, T, d, s), 1, "gate/up");
-    K3_LAUNCH(k3::bs_stream_down(c->bs, c->bw, tiles, tile_count, w, T, d, s), 1, "down");
+    K3_LAUNCH(k3::bs_stream_gateup(c->bs, c->bw, tiles, tile_count, w, T, d, bn, s), 1, "gate/up");
+    K3_LAUNCH(k3::bs_stream_down(c->bs, c->bw, tiles, tile_count, w, T, d, bn, s), 1, "down");
   } else if (path == 3) {
     if (fused_route)
       K3_LAUNCH(k3::umma_stream_gather(c->umma, w, T, d, s), 1, "gather");

@@ -38,7 +38,6 @@ namespace k3 {
 namespace {
 
 constexpr int kQM = 128;   // weight rows per tile (MMA M)
-constexpr int kQN = 32;    // token rows per tile (MMA N)
 constexpr int kQK = 128;   // input columns per stage
 constexpr int kAtom = 512; // scale bytes per 128 rows x 128 columns
 constexpr int kBsThreads = 192;
@@ -113,12 +112,15 @@ __device__ __forceinline__ uint32_t split_e4m3(float x, uint32_t s0, uint32_t s1
 }
 
 // Slot-ordered rows: dst row s = src row (perm ? perm[s] / K : s), written
-// as terms q[t][C/128][rows_max][128] and scale records
-// sf[t][C/128][rows_max][16] (bytes 0..3: the four 32-column groups).  A half
-// warp covers 128 columns (8 per lane, 4 lanes per scale block); the loop
+// as terms q[t][C/128][rows_max][128]; the scales go to the tile atoms
+// sf[tile][C/128][t][512] at byte (n%32)*16 + (n/32)*4 + g for row n of the
+// tile (slot_tile[s] = tile << 8 | n), the order in which tcgen05.cp and
+// the MMA read per-row scales (row n in lane n%32 of column n/32).  A half
+// warp covers 128 columns (8 per lane, 4 lanes per scale group); the loop
 // runs per warp so that both halves always meet at the shuffles.
 __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, const int* __restrict__ perm, int K, int rows,
-                                  int C, int rows_max, uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+                                  int C, int rows_max, const int* __restrict__ slot_tile, uint8_t* __restrict__ q,
+                                  uint8_t* __restrict__ sf) {
   const int hl = threadIdx.x & 15, half = (threadIdx.x >> 4) & 1;
   const int KC = C / kQK;
   const long long nwork = (long long)rows * KC;
@@ -159,8 +161,11 @@ __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, const int* _
     *reinterpret_cast<uint2*>(q + r0 * kQK + hl * 8) = make_uint2(a0, b0);
     *reinterpret_cast<uint2*>(q + (plane + r0) * kQK + hl * 8) = make_uint2(a1, b1);
     if ((hl & 3) == 0) {
-      sf[r0 * 16 + (hl >> 2)] = (uint8_t)s0;
-      sf[(plane + r0) * 16 + (hl >> 2)] = (uint8_t)s1;
+      const int tn = slot_tile[s];
+      const int n = tn & 0xFF;
+      uint8_t* atom = sf + (((size_t)(tn >> 8) * KC + kc) * 2) * kAtom + (n & 31) * 16 + (n >> 5) * 4 + (hl >> 2);
+      atom[0] = (uint8_t)s0;
+      atom[kAtom] = (uint8_t)s1;
     }
   }
 }
@@ -209,38 +214,47 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Per stage four copies: two adjacent e2m1 tiles (GATEUP: gate and up of one
-// 128-column chunk; DOWN: two consecutive chunks), both activation terms of
-// the stage's chunks, the weight scale atoms, the activation scale records.
-// Few large copies per stage keep the HBM stream going; two CTAs per SM.
-template <int MODE>
+// Per stage four copies: the e2m1 tiles (GATEUP: gate and up of one
+// 128-column chunk; DOWN: kNK consecutive chunks), both activation terms of
+// the stage's chunks (one 4-D box), the weight scale atoms and the
+// activation scale atoms (bulk copies).  Few large copies per stage keep the
+// HBM stream going; two CTAs per SM.  NQ is the tile height (MMA N <= NQ):
+// 32 for decode-size batches, 80 for larger ones (fewer weight re-reads per
+// token; gate/up then keeps a single accumulator buffer).
+template <int MODE, int NQ>
 struct BsCfg {
-  static constexpr int kNumA = (MODE == BS_GATEUP) ? 2 : 1;  // accumulators
-  static constexpr int kNK = (MODE == BS_GATEUP) ? 1 : 2;    // 128-column chunks per stage
+  static constexpr bool kBig = NQ > 32;
+  static constexpr int kNumA = (MODE == BS_GATEUP) ? 2 : 1;                 // accumulators (matrices)
+  static constexpr int kNK = (MODE == BS_GATEUP || kBig) ? 1 : 2;           // 128-column chunks per stage
+  static constexpr int kNA = (MODE == BS_GATEUP) ? 2 : kNK;                 // e2m1 tiles per stage
   static constexpr int kA = kQM * kQK;  // one e2m1 tile in 16-byte slots (8 data + 8 padding bytes per 16 codes)
-  static constexpr int kB = kQN * kQK;  // one e4m3 term of one chunk
-  static constexpr int kOffB = 2 * kA;
+  static constexpr int kB = NQ * kQK;   // one e4m3 term of one chunk
+  static constexpr int kOffB = kNA * kA;
   static constexpr int kOffSfa = kOffB + 2 * kNK * kB;
-  static constexpr int kOffSfb = kOffSfa + 2 * kAtom;
+  static constexpr int kOffSfb = kOffSfa + kNA * kAtom;
   static constexpr int kStageBytes = (kOffSfb + 2 * kNK * kAtom + 1023) / 1024 * 1024;
   static constexpr int kStages = 2;
-  static constexpr int kDCols = kNumA * kQN;   // one accumulator buffer
-  static constexpr int kSfCols = 8 + 8 * kNK;  // SFA: 2 atoms, SFB: 2 terms x kNK chunks (4 columns each)
-  static constexpr int kSfBase = 2 * kDCols;
+  static constexpr int kDBuf = (MODE == BS_GATEUP && kBig) ? 1 : 2;       // accumulator buffers
+  static constexpr int kAccStride = kBig ? 128 : 32;                       // TMEM columns between matrices
+  static constexpr int kBufStride = kNumA * kAccStride;                    // TMEM columns between buffers
+  static constexpr int kSfBase = (kDBuf - 1) * kBufStride + (kNumA - 1) * kAccStride + (NQ + 15) / 16 * 16;
+  static constexpr int kSfCols = 4 * kNA + 8 * kNK;  // weight atoms, then term x chunk activation atoms
   static constexpr int kTmemCols = 256;
   static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
-  static_assert(kSfBase + kStages * kSfCols <= kTmemCols, "TMEM budget");
+  static_assert(kSfBase % 4 == 0 && kSfBase + kStages * kSfCols <= kTmemCols, "TMEM budget");
+  static_assert(kB % 1024 == 0, "term blocks must keep the 1024-byte swizzle alignment");
   static_assert(2 * (kSmem + 1024) <= 233472, "two CTAs per SM");
 };
 
 struct BsParams {
   const uint8_t* sfa;  // weight scale atoms
+  const uint8_t* sfb;  // activation scale atoms [tile][KC][2][512]
   int MT, KC, KS;      // weight row tiles, 128-column chunks, stages per item
-  const int4* tiles;   // {expert, first slot, rows, -}
+  const int4* tiles;   // {expert, first slot, rows, rows rounded up to 16}
   const int* count;
   int ld_out;          // GATEUP: I, DOWN: L
   int rows_max;        // slot rows of the activation-term planes
-  uint16_t* h;         // GATEUP outputs: h (bf16) and its terms / scale records
+  uint16_t* h;         // GATEUP outputs: h (bf16), its terms and scale atoms
   uint8_t* hq;
   uint8_t* hsf;
   float* o;            // DOWN output
@@ -249,11 +263,11 @@ struct BsParams {
   uint64_t limit_ns;
 };
 
-template <int MODE>
+template <int MODE, int NQ>
 __global__ void __launch_bounds__(kBsThreads, 2)
     bs_stream_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                     const __grid_constant__ CUtensorMap map_sfb, const BsParams p) {
-  using C = BsCfg<MODE>;
+                     const BsParams p) {
+  using C = BsCfg<MODE, NQ>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
@@ -293,8 +307,9 @@ __global__ void __launch_bounds__(kBsThreads, 2)
       int kg = 0, issued = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const int4 tile = p.tiles[item / p.MT];
-        const int mt = item - (item / p.MT) * p.MT;
+        const int ti = item / p.MT;
+        const int4 tile = p.tiles[ti];
+        const int mt = item - ti * p.MT;
         const size_t tile0 = ((size_t)tile.x * p.MT + mt) * p.KC;  // (expert, row tile) chunk 0
         for (int ks = 0; ks < p.KS; ++ks, ++kg) {
           const int s = kg % C::kStages, u = kg / C::kStages;
@@ -304,17 +319,18 @@ __global__ void __launch_bounds__(kBsThreads, 2)
           }
           const int kc0 = ks * C::kNK;
           const int nk = min(C::kNK, p.KC - kc0);
-          // GATEUP: atoms / tiles (kc, gate), (kc, up); DOWN: (kc0), (kc0 + 1)
+          // GATEUP: tiles / atoms (kc, gate), (kc, up); DOWN: (kc0) .. (kc0 + kNK - 1)
           const int n_sfa = (MODE == BS_GATEUP) ? 2 : nk;
           const size_t first = (MODE == BS_GATEUP) ? (tile0 + kc0) * 2 : tile0 + kc0;
           const uint32_t st = smem_u32(stage(s));
-          // the e2m1 copies count their packed bytes; boxes past the end of the
+          // the e2m1 copies count their packed bytes; boxes past the end of a
           // tensor are zero-filled and counted in full
-          mbar_expect_tx(full(s), (uint32_t)(2 * (C::kA / 2) + 2 * C::kNK * C::kB + n_sfa * kAtom + 2 * C::kNK * kAtom));
+          mbar_expect_tx(full(s), (uint32_t)(C::kNA * (C::kA / 2) + 2 * C::kNK * C::kB + n_sfa * kAtom +
+                                             2 * nk * kAtom));
           tma_load_3d(st, &map_a, full(s), 0, 0, (int)first);
           tma_load_4d(st + C::kOffB, &map_b, full(s), 0, tile.y, kc0, 0);
           bulk_load(st + C::kOffSfa, p.sfa + first * kAtom, n_sfa * kAtom, full(s));
-          tma_load_4d(st + C::kOffSfb, &map_sfb, full(s), 0, tile.y, kc0, 0);
+          bulk_load(st + C::kOffSfb, p.sfb + ((size_t)ti * p.KC + kc0) * 2 * kAtom, 2 * nk * kAtom, full(s));
           ++issued;
         }
       }
@@ -342,15 +358,16 @@ __global__ void __launch_bounds__(kBsThreads, 2)
       int kg = 0, it = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
-        const int buf = it & 1;
-        if (it >= 2 && !mbar_wait(dempty(buf), ((it >> 1) - 1) & 1, g, 2u)) {
+        const int buf = (C::kDBuf == 2) ? (it & 1) : 0;
+        const int use = (C::kDBuf == 2) ? (it >> 1) : it;  // earlier uses of this buffer
+        if (use > 0 && !mbar_wait(dempty(buf), (use - 1) & 1, g, 2u)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d0 = tmem + buf * C::kDCols;
-        // MMA N: 16 when the tile holds at most 16 rows
-        const uint32_t n = p.tiles[item / p.MT].z > 16 ? 32u : 16u;
+        const uint32_t d0 = tmem + buf * C::kBufStride;
+        // MMA N: the tile's rows rounded up to 16
+        const uint32_t n = (uint32_t)p.tiles[item / p.MT].w;
         for (int ks = 0; ks < p.KS; ++ks, ++kg) {
           const int s = kg % C::kStages;
           if (!mbar_wait(full(s), (kg / C::kStages) & 1, g, 4u)) {
@@ -363,10 +380,11 @@ __global__ void __launch_bounds__(kBsThreads, 2)
           const uint64_t a_d = a_base + so, b_d = b_base + so;
           const uint32_t sfc = tmem + C::kSfBase + s * C::kSfCols;
 #pragma unroll
-          for (int j = 0; j < 2; ++j)
+          for (int j = 0; j < C::kNA; ++j)
             if (MODE == BS_GATEUP || j < nk) tc_cp_scales(sfc + 4 * j, sfa_base + so + (j * kAtom >> 4));
 #pragma unroll
-          for (int j = 0; j < 2 * C::kNK; ++j) tc_cp_scales(sfc + 8 + 4 * j, sfb_base + so + (j * kAtom >> 4));
+          for (int j = 0; j < 2 * C::kNK; ++j)
+            if (j < 2 * nk) tc_cp_scales(sfc + 4 * C::kNA + 4 * j, sfb_base + so + (j * kAtom >> 4));
           const uint32_t first = ks ? 1u : 0u;
 #pragma unroll
           for (int c = 0; c < C::kNK; ++c) {
@@ -378,9 +396,11 @@ __global__ void __launch_bounds__(kBsThreads, 2)
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                   const int ablk = (MODE == BS_GATEUP) ? a : c;
-                  const int bblk = t * C::kNK + c;
-                  umma_bs(d0 + a * kQN, a_d + ((ablk * C::kA + kb * 32) >> 4), b_d + ((bblk * C::kB + kb * 32) >> 4),
-                          bs_idesc(kb, kb, n), sfc + 4 * ablk, sfc + 8 + 4 * bblk, (c | kb | t) ? 1u : first);
+                  const int bblk = t * C::kNK + c;  // term block of the 4-D box ([term][chunk])
+                  const int sfbj = c * 2 + t;       // activation atom ([chunk][term])
+                  umma_bs(d0 + a * C::kAccStride, a_d + ((ablk * C::kA + kb * 32) >> 4),
+                          b_d + ((bblk * C::kB + kb * 32) >> 4), bs_idesc(kb, kb, n), sfc + 4 * ablk,
+                          sfc + 4 * C::kNA + 4 * sfbj, (c | kb | t) ? 1u : first);
                 }
           }
           umma_commit(sfree(s));
@@ -404,47 +424,64 @@ __global__ void __launch_bounds__(kBsThreads, 2)
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     int it = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
-      const int buf = it & 1;
-      if (!mbar_wait(dfull(buf), (it >> 1) & 1, g, 8u)) break;
+      const int buf = (C::kDBuf == 2) ? (it & 1) : 0;
+      const int use = (C::kDBuf == 2) ? (it >> 1) : it;
+      if (!mbar_wait(dfull(buf), use & 1, g, 8u)) break;
       tc_fence_after();
-      const int4 tile = p.tiles[item / p.MT];
-      const int mt = item - (item / p.MT) * p.MT;
+      const int ti = item / p.MT;
+      const int4 tile = p.tiles[ti];
+      const int mt = item - ti * p.MT;
       const int m = mt * kQM + r;
-      float acc[32];
-      tmem_ld32(lane_base + buf * C::kDCols, acc);
+      const uint32_t dbase = lane_base + buf * C::kBufStride;
       if (MODE == BS_GATEUP) {
-        float up[32];
-        tmem_ld32(lane_base + buf * C::kDCols + kQN, up);
-        tc_fence_before();
-        mbar_arrive(dempty(buf));
-        // h as bf16 and as the two e4m3 terms of the down GEMM's B operand
+        // h as bf16 and as the two e4m3 terms (and scale atoms) of the down GEMM's B operand
         const int KCo = p.ld_out / kQK;
         const size_t plane = (size_t)KCo * p.rows_max;
         const size_t rbase = (size_t)(m >> 7) * p.rows_max;
         const int grp = (m >> 5) & 3;
+        uint8_t* atoms = p.hsf + (((size_t)ti * KCo + (m >> 7)) * 2) * kAtom + grp;
+#pragma unroll 1
+        for (int j0 = 0; j0 < NQ; j0 += 32) {
+          float acc[32], up[32];
+          tmem_ld32(dbase + j0, acc);
+          tmem_ld32(dbase + C::kAccStride + j0, up);
+          if (j0 + 32 >= NQ) {
+            tc_fence_before();
+            mbar_arrive(dempty(buf));
+          }
 #pragma unroll
-        for (int j = 0; j < kQN; ++j) {
-          if (j < tile.z) {
-            const size_t row = (size_t)(tile.y + j);
-            const uint16_t hb = f32_to_bf16(situ_fast(acc[j], up[j], p.beta, p.beta_lin));
-            p.h[row * p.ld_out + m] = hb;
-            const uint32_t emax = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(hb >> 7) & 0xFFu);
-            const uint32_t s0 = term0_scale(emax), s1 = term1_scale(s0);
-            const uint32_t q = split_e4m3(bf16_to_f32(hb), s0, s1);
-            p.hq[(rbase + row) * kQK + (m & 127)] = (uint8_t)q;
-            p.hq[(plane + rbase + row) * kQK + (m & 127)] = (uint8_t)(q >> 8);
-            if (lane == 0) {
-              p.hsf[(rbase + row) * 16 + grp] = (uint8_t)s0;
-              p.hsf[(plane + rbase + row) * 16 + grp] = (uint8_t)s1;
+          for (int j = 0; j < 32; ++j) {
+            const int jj = j0 + j;
+            if (jj < tile.z) {
+              const size_t row = (size_t)(tile.y + jj);
+              const uint16_t hb = f32_to_bf16(situ_fast(acc[j], up[j], p.beta, p.beta_lin));
+              p.h[row * p.ld_out + m] = hb;
+              const uint32_t emax = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(hb >> 7) & 0xFFu);
+              const uint32_t s0 = term0_scale(emax), s1 = term1_scale(s0);
+              const uint32_t q = split_e4m3(bf16_to_f32(hb), s0, s1);
+              p.hq[(rbase + row) * kQK + (m & 127)] = (uint8_t)q;
+              p.hq[(plane + rbase + row) * kQK + (m & 127)] = (uint8_t)(q >> 8);
+              if (lane == 0) {
+                const int ab = (jj & 31) * 16 + (jj >> 5) * 4;
+                atoms[ab] = (uint8_t)s0;
+                atoms[kAtom + ab] = (uint8_t)s1;
+              }
             }
           }
         }
       } else {
-        tc_fence_before();
-        mbar_arrive(dempty(buf));
+#pragma unroll 1
+        for (int j0 = 0; j0 < NQ; j0 += 32) {
+          float acc[32];
+          tmem_ld32(dbase + j0, acc);
+          if (j0 + 32 >= NQ) {
+            tc_fence_before();
+            mbar_arrive(dempty(buf));
+          }
 #pragma unroll
-        for (int j = 0; j < kQN; ++j)
-          if (j < tile.z) p.o[(size_t)(tile.y + j) * p.ld_out + m] = acc[j];
+          for (int j = 0; j < 32; ++j)
+            if (j0 + j < tile.z) p.o[(size_t)(tile.y + j0 + j) * p.ld_out + m] = acc[j];
+        }
       }
     }
   }
@@ -463,57 +500,59 @@ bool encode(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base
   return fn(map, dt, rank, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-// e2m1 tiles [nbox][128 rows][64 bytes]; one copy = two adjacent tiles, each
-// landing as 128 rows of 128 bytes (16-byte slots) with a 128-byte swizzle.
-bool map_e2m1(CUtensorMap* map, const void* base, long long nbox) {
+// e2m1 tiles [nbox][128 rows][64 bytes]; one copy = `depth` adjacent tiles,
+// each landing as 128 rows of 128 bytes (16-byte slots) with a 128-byte swizzle.
+bool map_e2m1(CUtensorMap* map, const void* base, long long nbox, int depth) {
   const cuuint64_t dims[3] = {(cuuint64_t)kQK, (cuuint64_t)kQM, (cuuint64_t)nbox};
   const cuuint64_t strides[2] = {(cuuint64_t)kQK / 2, (cuuint64_t)kQM * kQK / 2};
-  const cuuint32_t box[3] = {(cuuint32_t)kQK, (cuuint32_t)kQM, 2};
+  const cuuint32_t box[3] = {(cuuint32_t)kQK, (cuuint32_t)kQM, (cuuint32_t)depth};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
-// Activation terms q[2][KC][rows_max][128] (box: 128 x 32 rows x nk chunks
-// x 2 terms, 128-byte swizzle) or scale records sf[2][KC][rows_max][16]
-// (box 16 x 32 x nk x 2, no swizzle).
-bool map_terms(CUtensorMap* map, const void* base, int KC, int rows_max, int inner, int nk,
-               CUtensorMapSwizzle sw) {
-  const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)rows_max, (cuuint64_t)KC, 2};
-  const cuuint64_t strides[3] = {(cuuint64_t)inner, (cuuint64_t)rows_max * inner, (cuuint64_t)KC * rows_max * inner};
-  const cuuint32_t box[4] = {(cuuint32_t)inner, (cuuint32_t)kQN, (cuuint32_t)nk, 2};
-  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box, sw);
+// Activation terms q[2][KC][rows_max][128]: box 128 x box_rows x nk chunks x
+// 2 terms, 128-byte swizzle.
+bool map_terms(CUtensorMap* map, const void* base, int KC, int rows_max, int box_rows, int nk) {
+  const cuuint64_t dims[4] = {(cuuint64_t)kQK, (cuuint64_t)rows_max, (cuuint64_t)KC, 2};
+  const cuuint64_t strides[3] = {(cuuint64_t)kQK, (cuuint64_t)rows_max * kQK, (cuuint64_t)KC * rows_max * kQK};
+  const cuuint32_t box[4] = {(cuuint32_t)kQK, (cuuint32_t)box_rows, (cuuint32_t)nk, 2};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 struct BsWs {
-  int rows_max;
-  uint8_t *lq, *lsf;  // latent rows: terms [2][L/128][rows_max][128], records [2][L/128][rows_max][16]
-  uint8_t *hq, *hsf;  // h rows:      terms [2][I/128][rows_max][128], records [2][I/128][rows_max][16]
+  int rows_max;       // slots: max_tokens * K
+  int max_tiles;      // bound on the tile list length
+  uint8_t *lq, *lsf;  // latent rows: terms [2][L/128][rows_max][128], atoms [max_tiles][L/128][2][512]
+  uint8_t *hq, *hsf;  // h rows:      terms [2][I/128][rows_max][128], atoms [max_tiles][I/128][2][512]
+  int* slot_tile;     // [rows_max]: tile << 8 | row within the tile
   size_t total;
 };
 BsWs bs_ws_view(void* base, const Dims& d, int max_tokens) {
   auto up = [](size_t v) { return (v + 255) / 256 * 256; };
-  const size_t R = (size_t)std::min(max_tokens, kBsMaxTokens) * d.K;
-  const size_t sizes[4] = {2 * R * d.L, 2 * R * d.L / 8, 2 * R * d.I, 2 * R * d.I / 8};
+  const size_t R = (size_t)max_tokens * d.K;
+  // tiles hold at least one slot and at most one expert: <= E + R / 16 whatever the tile height
+  const size_t MT = (size_t)d.E + R / 16 + 1;
+  const size_t sizes[5] = {2 * R * d.L, MT * (d.L / kQK) * 2 * kAtom, 2 * R * d.I, MT * (d.I / kQK) * 2 * kAtom,
+                           R * sizeof(int)};
   uint8_t* b = static_cast<uint8_t*>(base);
-  uint8_t* ptr[4];
+  uint8_t* ptr[5];
   size_t off = 0;
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < 5; ++i) {
     ptr[i] = b ? b + off : nullptr;
     off += up(sizes[i]);
   }
-  return BsWs{(int)R, ptr[0], ptr[1], ptr[2], ptr[3], off};
+  return BsWs{(int)R, (int)MT, ptr[0], ptr[1], ptr[2], ptr[3], reinterpret_cast<int*>(ptr[4]), off};
 }
 
-template <int MODE>
+template <int MODE, int NQ>
 cudaError_t launch_bs(const BsPlan& p, const uint8_t* wq, const uint8_t* sfa, int n_exp, int rows, int cols,
-                      const uint8_t* q, const uint8_t* sf, int rows_max, const int4* tiles, const int* count,
+                      const uint8_t* q, const uint8_t* sfb, int rows_max, const int4* tiles, const int* count,
                       BsParams prm, cudaStream_t s) {
-  using C = BsCfg<MODE>;
-  CUtensorMap ma, mb, msf;
+  using C = BsCfg<MODE, NQ>;
+  CUtensorMap ma, mb;
   const int KC = cols / kQK, MT = rows / kQM;
   const long long nbox = (long long)n_exp * MT * KC * C::kNumA;
-  if (!map_e2m1(&ma, wq, nbox) || !map_terms(&mb, q, KC, rows_max, kQK, C::kNK, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !map_terms(&msf, sf, KC, rows_max, 16, C::kNK, CU_TENSOR_MAP_SWIZZLE_NONE))
-    return cudaErrorInvalidValue;
+  if (!map_e2m1(&ma, wq, nbox, C::kNA) || !map_terms(&mb, q, KC, rows_max, NQ, C::kNK)) return cudaErrorInvalidValue;
   prm.sfa = sfa;
+  prm.sfb = sfb;
   prm.MT = MT;
   prm.KC = KC;
   prm.KS = (KC + C::kNK - 1) / C::kNK;
@@ -522,7 +561,7 @@ cudaError_t launch_bs(const BsPlan& p, const uint8_t* wq, const uint8_t* sfa, in
   prm.rows_max = rows_max;
   prm.status = p.status;
   prm.limit_ns = p.limit_ns;
-  bs_stream_kernel<MODE><<<2 * p.num_sms, kBsThreads, C::kSmem, s>>>(ma, mb, msf, prm);
+  bs_stream_kernel<MODE, NQ><<<2 * p.num_sms, kBsThreads, C::kSmem, s>>>(ma, mb, prm);
   return cudaGetLastError();
 }
 
@@ -547,31 +586,36 @@ cudaError_t bs_scale_atoms(const uint8_t* scale, int ne, int rows, int cols, int
 
 size_t bs_ws_bytes(const Dims& d, int max_tokens) { return bs_ws_view(nullptr, d, max_tokens).total; }
 
+int* bs_slot_tile(const BsPlan& p) { return bs_ws_view(p.ws, p.dims, p.max_tokens).slot_tile; }
+
 cudaError_t prepare_bs_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(bs_stream_kernel<BS_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       BsCfg<BS_GATEUP>::kSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(bs_stream_kernel<BS_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             BsCfg<BS_DOWN>::kSmem);
+  cudaError_t e = cudaSuccess;
+  auto set = [&](const void* f, int bytes) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  };
+  set((const void*)bs_stream_kernel<BS_GATEUP, kBsDecodeRows>, BsCfg<BS_GATEUP, kBsDecodeRows>::kSmem);
+  set((const void*)bs_stream_kernel<BS_DOWN, kBsDecodeRows>, BsCfg<BS_DOWN, kBsDecodeRows>::kSmem);
+  set((const void*)bs_stream_kernel<BS_GATEUP, kBsPrefillRows>, BsCfg<BS_GATEUP, kBsPrefillRows>::kSmem);
+  set((const void*)bs_stream_kernel<BS_DOWN, kBsPrefillRows>, BsCfg<BS_DOWN, kBsPrefillRows>::kSmem);
   return e;
 }
 
 cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s) {
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
-  if (T > std::min(p.max_tokens, kBsMaxTokens)) return cudaErrorInvalidValue;
+  if (T > p.max_tokens) return cudaErrorInvalidValue;
   const BsWs ws = bs_ws_view(p.ws, d, p.max_tokens);
   const long long halves = (long long)TK * (d.L / kQK);
-  const int blocks = (int)std::min<long long>((halves * 16 + 255) / 256, 4LL * p.num_sms);
-  quant_rows_kernel<<<blocks, 256, 0, s>>>(w.lat, w.perm, d.K, TK, d.L, ws.rows_max, ws.lq, ws.lsf);
+  const int blocks = (int)std::min<long long>((halves * 16 + 255) / 256, 8LL * p.num_sms);
+  quant_rows_kernel<<<blocks, 256, 0, s>>>(w.lat, w.perm, d.K, TK, d.L, ws.rows_max, ws.slot_tile, ws.lq, ws.lsf);
   return cudaGetLastError();
 }
 
 cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* tiles, const int* tile_count,
-                             const Work& w, int T, const Dims& d, cudaStream_t s) {
+                             const Work& w, int T, const Dims& d, int tile_rows, cudaStream_t s) {
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
-  if (T > std::min(p.max_tokens, kBsMaxTokens)) return cudaErrorInvalidValue;
+  if (T > p.max_tokens) return cudaErrorInvalidValue;
   const BsWs ws = bs_ws_view(p.ws, d, p.max_tokens);
   BsParams prm{};
   prm.ld_out = d.I;
@@ -580,21 +624,31 @@ cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* t
   prm.hsf = ws.hsf;
   prm.beta = d.beta;
   prm.beta_lin = d.beta_lin;
-  return launch_bs<BS_GATEUP>(p, bw.gu_q, bw.gu_sf, d.E, d.I, d.L, ws.lq, ws.lsf, ws.rows_max, tiles, tile_count,
-                              prm, s);
+  if (tile_rows == kBsDecodeRows)
+    return launch_bs<BS_GATEUP, kBsDecodeRows>(p, bw.gu_q, bw.gu_sf, d.E, d.I, d.L, ws.lq, ws.lsf, ws.rows_max,
+                                               tiles, tile_count, prm, s);
+  if (tile_rows == kBsPrefillRows)
+    return launch_bs<BS_GATEUP, kBsPrefillRows>(p, bw.gu_q, bw.gu_sf, d.E, d.I, d.L, ws.lq, ws.lsf, ws.rows_max,
+                                                tiles, tile_count, prm, s);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t bs_stream_down(const BsPlan& p, const BsWeights& bw, const int4* tiles, const int* tile_count,
-                           const Work& w, int T, const Dims& d, cudaStream_t s) {
+                           const Work& w, int T, const Dims& d, int tile_rows, cudaStream_t s) {
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
-  if (T > std::min(p.max_tokens, kBsMaxTokens)) return cudaErrorInvalidValue;
+  if (T > p.max_tokens) return cudaErrorInvalidValue;
   const BsWs ws = bs_ws_view(p.ws, d, p.max_tokens);
   BsParams prm{};
   prm.ld_out = d.L;
   prm.o = w.o;
-  return launch_bs<BS_DOWN>(p, bw.d_q, bw.d_sf, d.E, d.L, d.I, ws.hq, ws.hsf, ws.rows_max, tiles, tile_count, prm,
-                            s);
+  if (tile_rows == kBsDecodeRows)
+    return launch_bs<BS_DOWN, kBsDecodeRows>(p, bw.d_q, bw.d_sf, d.E, d.L, d.I, ws.hq, ws.hsf, ws.rows_max, tiles,
+                                             tile_count, prm, s);
+  if (tile_rows == kBsPrefillRows)
+    return launch_bs<BS_DOWN, kBsPrefillRows>(p, bw.d_q, bw.d_sf, d.E, d.L, d.I, ws.hq, ws.hsf, ws.rows_max, tiles,
+                                              tile_count, prm, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace k3

@@ -34,7 +34,7 @@ cudaError_t bs_scale_atoms(const uint8_t* scale, int ne, int rows, int cols, int
                            cudaStream_t s);
 
 struct BsPlan {
-  int max_tokens = 0;     // largest T this path serves (workspace bound)
+  int max_tokens = 0;     // largest T (workspace bound)
   void* ws = nullptr;
   size_t ws_bytes = 0;
   unsigned* status = nullptr;
@@ -42,19 +42,26 @@ struct BsPlan {
   int num_sms = 152;
   Dims dims{};
 };
-constexpr int kBsMaxTokens = 256;
+// Tile heights (token rows per tile, the MMA's N bound): decode-size batches
+// use short tiles (every weight byte streamed once per forward), larger
+// batches taller ones (fewer weight re-reads per token).
+constexpr int kBsDecodeRows = 32;
+constexpr int kBsPrefillRows = 80;
+inline int bs_tile_rows(int T) { return T <= 128 ? kBsDecodeRows : kBsPrefillRows; }
 size_t bs_ws_bytes(const Dims& d, int max_tokens);
+// slot -> (tile << 8 | row in tile), written by the tile-list builders
+int* bs_slot_tile(const BsPlan& p);
 cudaError_t prepare_bs_kernels();
 
-// Slot-ordered latent rows (lat[perm[s] / K]) written as two e4m3 terms and
-// their scale records.
+// Slot-ordered latent rows (lat[perm[s] / K]) written as two e4m3 terms, and
+// their scales as per-tile atoms (needs the tile list's slot map).
 cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s);
-// gate/up over the tile list (tiles of at most 32 rows): h (bf16, slot
-// order) and its two-term e4m3 form for the down GEMM.
+// gate/up over the tile list (tiles of at most tile_rows rows): h (bf16,
+// slot order) and its two-term e4m3 form for the down GEMM.
 cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* tiles, const int* tile_count,
-                             const Work& w, int T, const Dims& d, cudaStream_t s);
+                             const Work& w, int T, const Dims& d, int tile_rows, cudaStream_t s);
 // down: o (fp32, slot order)
 cudaError_t bs_stream_down(const BsPlan& p, const BsWeights& bw, const int4* tiles, const int* tile_count,
-                           const Work& w, int T, const Dims& d, cudaStream_t s);
+                           const Work& w, int T, const Dims& d, int tile_rows, cudaStream_t s);
 
 }  // namespace k3

@@ -428,7 +428,8 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(const int32_t* __restr
                                                           int* __restrict__ counts, int* __restrict__ offsets,
                                                           int* __restrict__ active, int* __restrict__ perm,
                                                           int* __restrict__ slot, int bn_max,
-                                                          int4* __restrict__ tiles, int* __restrict__ tile_count) {
+                                                          int4* __restrict__ tiles, int* __restrict__ tile_count,
+                                                          int* __restrict__ slot_tile) {
   __shared__ int hist[2048];
   __shared__ int base[2048];
   __shared__ int warp_tot[32];
@@ -501,6 +502,8 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(const int32_t* __restr
       const int r0 = j * tn;
       const int rows = min(tn, c_t - r0);
       tiles[tb + j] = make_int4(e_t, base[e_t] + r0, rows, (rows + 15) & ~15);
+      if (slot_tile)
+        for (int n = 0; n < rows; ++n) slot_tile[base[e_t] + r0 + n] = ((tb + j) << 8) | n;
     }
   }
   if (threadIdx.x == 0) *tile_count = total_s;
@@ -508,12 +511,13 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(const int32_t* __restr
 
 cudaError_t launch_route_small(const float* logits, int T, int E, const float* bias, int K, int norm_topk, float rsf,
                                int32_t* idx, float* w, int* counts, int* offsets, int* active, int* perm, int* slot,
-                               int bn_max, int4* tiles, int* tile_count, cudaStream_t s) {
+                               int bn_max, int4* tiles, int* tile_count, int* slot_tile, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  if (T * K > 1024 || E > 2048) return cudaErrorInvalidValue;
+  if (T * K > 1024 || E > 2048 || bn_max > 255) return cudaErrorInvalidValue;
   cudaError_t e = launch_topk(logits, T, E, E, bias, K, norm_topk, rsf, idx, w, s);
   if (e != cudaSuccess) return e;
-  perm_small_kernel<<<1, 1024, 0, s>>>(idx, T, E, K, counts, offsets, active, perm, slot, bn_max, tiles, tile_count);
+  perm_small_kernel<<<1, 1024, 0, s>>>(idx, T, E, K, counts, offsets, active, perm, slot, bn_max, tiles, tile_count,
+                                       slot_tile);
   return cudaGetLastError();
 }
 

@@ -50,7 +50,7 @@ cudaError_t prepare_decode_kernels(const Dims& d);
 // list in one CTA
 cudaError_t launch_route_small(const float* logits, int T, int E, const float* bias, int K, int norm_topk, float rsf,
                                int32_t* idx, float* w, int* counts, int* offsets, int* active, int* perm, int* slot,
-                               int bn_max, int4* tiles, int* tile_count, cudaStream_t s);
+                               int bn_max, int4* tiles, int* tile_count, int* slot_tile, cudaStream_t s);
 cudaError_t launch_combine_rmsnorm(const float* o, const int* slot, const float* topk_w, const uint16_t* gamma,
                                    int T, const Dims& d, uint16_t* n, cudaStream_t s);
 cudaError_t launch_relayout(const uint8_t* packed, const uint8_t* scale, int n_mat, int rows, int cols,

@@ -729,7 +729,8 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ lat, const int* 
 // rounded up to 16: tiles[i] = {expert, first slot, rows, MMA N}.
 __global__ void __launch_bounds__(1024) build_tiles_kernel(const int* __restrict__ active,
                                                            const int* __restrict__ offsets, int bn_max,
-                                                           int4* __restrict__ tiles, int* __restrict__ count) {
+                                                           int4* __restrict__ tiles, int* __restrict__ count,
+                                                           int* __restrict__ slot_tile) {
   __shared__ int warp_tot[32];
   __shared__ int carry;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -772,6 +773,8 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int* __restrict
         const int r0 = j * tn;
         const int rows = min(tn, c - r0);
         tiles[base + j] = make_int4(e, offsets[e] + r0, rows, (rows + 15) & ~15);
+        if (slot_tile)
+          for (int n = 0; n < rows; ++n) slot_tile[offsets[e] + r0 + n] = ((base + j) << 8) | n;
       }
     }
     __syncthreads();
@@ -913,7 +916,7 @@ cudaError_t umma_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8
   if (TK <= 0) return cudaSuccess;
   UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
   const int max_tiles = TK / kBNMax + std::min(d.E, TK) + 1;
-  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, kBNMax, ws.tiles, ws.count);
+  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, kBNMax, ws.tiles, ws.count, nullptr);
   gather_rows_kernel<<<152 * 8, 256, 0, s>>>(w.lat, w.perm, TK, d.K, d.L, ws.lat_perm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -952,16 +955,18 @@ cudaError_t umma_stream_prepare(const UmmaPlan& p, const Work& w, int T, const D
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
   UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
-  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, kSNB, ws.tiles, ws.count);
+  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, kSNB, ws.tiles, ws.count, nullptr);
   gather_rows_kernel<<<152 * 2, 256, 0, s>>>(w.lat, w.perm, TK, d.K, d.L, ws.lat_perm);
   return cudaGetLastError();
 }
 
-// Only the tile list (tiles of at most kSNB rows).
-cudaError_t umma_stream_tiles(const UmmaPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s) {
+// Only the tile list (tiles of at most bn_max rows) and the slot -> tile map.
+cudaError_t umma_stream_tiles(const UmmaPlan& p, const Work& w, int T, const Dims& d, int bn_max, int* slot_tile,
+                              cudaStream_t s) {
   if (T * d.K <= 0) return cudaSuccess;
+  if (bn_max < kSNB || bn_max > 255) return cudaErrorInvalidValue;  // the tile list holds E + T*K/kSNB tiles
   UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
-  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, kSNB, ws.tiles, ws.count);
+  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, bn_max, ws.tiles, ws.count, slot_tile);
   return cudaGetLastError();
 }
 

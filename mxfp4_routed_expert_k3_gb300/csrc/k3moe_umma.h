@@ -36,7 +36,8 @@ cudaError_t umma_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8
                          const Dims& d, cudaStream_t s);
 int umma_expert_launches();
 cudaError_t umma_stream_prepare(const UmmaPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s);
-cudaError_t umma_stream_tiles(const UmmaPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s);
+cudaError_t umma_stream_tiles(const UmmaPlan& p, const Work& w, int T, const Dims& d, int bn_max, int* slot_tile,
+                              cudaStream_t s);
 cudaError_t umma_stream_gather(const UmmaPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s);
 // where the streaming kernels read their tile list (and the tile height)
 void umma_tile_list(const UmmaPlan& p, int4** tiles, int** count, int* bn_max);

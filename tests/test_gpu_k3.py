@@ -23,9 +23,9 @@ def k3weights():
     return synth.layer_weights(K3, seed=1)
 
 
-@pytest.fixture(scope="module")
-def k3layer(k3weights):
-    layer = k3moe.Layer(K3, k3weights, max_tokens=MAXT)
+@pytest.fixture(scope="module", params=[k3moe.PATH_AUTO, k3moe.PATH_BLOCK_SCALED], ids=["auto", "blockscaled"])
+def k3layer(request, k3weights):
+    layer = k3moe.Layer(K3, k3weights, max_tokens=MAXT, force_path=request.param)
     yield k3weights, layer
     layer.close()
 
@@ -96,10 +96,11 @@ def test_k3_prefill_8192(k3layer):
     _sampled(layer, w, x, 24, 1, "prefill T=8192")
 
 
-def test_k3_skewed_4096():
+@pytest.mark.parametrize("path", [k3moe.PATH_AUTO, k3moe.PATH_BLOCK_SCALED], ids=["auto", "blockscaled"])
+def test_k3_skewed_4096(path):
     w = synth.layer_weights(K3, seed=3, n_hot=32)
     hot = synth.hot_experts(K3, 3, 32)
-    layer = k3moe.Layer(K3, w, max_tokens=4096)
+    layer = k3moe.Layer(K3, w, max_tokens=4096, force_path=path)
     try:
         x = gapped_tokens(K3, w, seed=301, T=4096)
         idx = _sampled(layer, w, x, 16, 2, "skew T=4096")
