@@ -366,8 +366,8 @@ __global__ void __launch_bounds__(kBsThreads, 2)
         }
         tc_fence_after();
         const uint32_t d0 = tmem + buf * C::kBufStride;
-        // MMA N: the tile's rows rounded up to 16
-        const uint32_t n = (uint32_t)p.tiles[item / p.MT].w;
+        // MMA N: the tile's rows rounded up to 16 (never beyond the accumulator's NQ columns)
+        const uint32_t n = (uint32_t)min(p.tiles[item / p.MT].w, (NQ + 15) / 16 * 16);
         for (int ks = 0; ks < p.KS; ++ks, ++kg) {
           const int s = kg % C::kStages;
           if (!mbar_wait(full(s), (kg / C::kStages) & 1, g, 4u)) {
