@@ -40,7 +40,6 @@ namespace {
 constexpr int kQM = 128;   // weight rows per tile (MMA M)
 constexpr int kQK = 128;   // input columns per stage
 constexpr int kAtom = 512; // scale bytes per 128 rows x 128 columns
-constexpr int kBsThreads = 192;
 enum BsMode { BS_GATEUP = 0, BS_DOWN = 1 };
 
 // Position of the scale of row r (0..127), group g (0..3) inside an atom:
@@ -218,12 +217,21 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
 // 128-column chunk; DOWN: kNK consecutive chunks), both activation terms of
 // the stage's chunks (one 4-D box), the weight scale atoms and the
 // activation scale atoms (bulk copies).  Few large copies per stage keep the
-// HBM stream going; two CTAs per SM.  NQ is the tile height (MMA N <= NQ):
-// 32 for decode-size batches, 80 for larger ones (fewer weight re-reads per
-// token; gate/up then keeps a single accumulator buffer).
+// HBM stream going.  NQ is the tile height (MMA N <= NQ):
+//   32 (decode-size batches): two CTAs per SM, two stages each, one
+//      epilogue warpgroup; the kernel streams weights;
+//   80 (larger batches): also two CTAs per SM with two stages (a single CTA
+//      per SM with deeper rings and both accumulator buffers measured
+//      slower: the copies a CTA keeps in flight bound the rate); gate/up
+//      then keeps one accumulator buffer per CTA (gate + up need 208 of the
+//      CTA's 256 TMEM columns), and the other CTA on the SM covers its
+//      epilogue.
 template <int MODE, int NQ>
 struct BsCfg {
   static constexpr bool kBig = NQ > 32;
+  static constexpr int kCtas = 2;                                           // CTAs per SM
+  static constexpr int kEpiWarps = 4;                                       // epilogue warps
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int kNumA = (MODE == BS_GATEUP) ? 2 : 1;                 // accumulators (matrices)
   static constexpr int kNK = (MODE == BS_GATEUP || kBig) ? 1 : 2;           // 128-column chunks per stage
   static constexpr int kNA = (MODE == BS_GATEUP) ? 2 : kNK;                 // e2m1 tiles per stage
@@ -234,16 +242,17 @@ struct BsCfg {
   static constexpr int kOffSfb = kOffSfa + kNA * kAtom;
   static constexpr int kStageBytes = (kOffSfb + 2 * kNK * kAtom + 1023) / 1024 * 1024;
   static constexpr int kStages = 2;
-  static constexpr int kDBuf = (MODE == BS_GATEUP && kBig) ? 1 : 2;       // accumulator buffers
-  static constexpr int kAccStride = kBig ? 128 : 32;                       // TMEM columns between matrices
-  static constexpr int kBufStride = kNumA * kAccStride;                    // TMEM columns between buffers
+  static constexpr int kDBuf = (MODE == BS_GATEUP && kBig) ? 1 : 2;        // accumulator buffers
+  static constexpr int kAccStride = kBig ? 128 : 32;                        // TMEM columns between matrices
+  static constexpr int kBufStride = kNumA * kAccStride;                     // TMEM columns between buffers
   static constexpr int kSfBase = (kDBuf - 1) * kBufStride + (kNumA - 1) * kAccStride + (NQ + 15) / 16 * 16;
   static constexpr int kSfCols = 4 * kNA + 8 * kNK;  // weight atoms, then term x chunk activation atoms
   static constexpr int kTmemCols = 256;
   static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
   static_assert(kSfBase % 4 == 0 && kSfBase + kStages * kSfCols <= kTmemCols, "TMEM budget");
+  static_assert(kCtas * kTmemCols <= 512, "TMEM per SM");
   static_assert(kB % 1024 == 0, "term blocks must keep the 1024-byte swizzle alignment");
-  static_assert(2 * (kSmem + 1024) <= 233472, "two CTAs per SM");
+  static_assert(kCtas * (kSmem + 1024) <= 233472, "shared memory per SM");
 };
 
 struct BsParams {
@@ -264,7 +273,7 @@ struct BsParams {
 };
 
 template <int MODE, int NQ>
-__global__ void __launch_bounds__(kBsThreads, 2)
+__global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kCtas)
     bs_stream_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                      const BsParams p) {
   using C = BsCfg<MODE, NQ>;
@@ -283,7 +292,7 @@ __global__ void __launch_bounds__(kBsThreads, 2)
   if (threadIdx.x == 0) {
     for (int i = 0; i < NB; ++i) {
       const bool is_empty = i >= 2 * C::kStages + 2 && i < 2 * C::kStages + 4;
-      mbar_init(smem_u32(bars + i), is_empty ? 128u : 1u);
+      mbar_init(smem_u32(bars + i), is_empty ? 32u * C::kEpiWarps : 1u);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -418,8 +427,11 @@ __global__ void __launch_bounds__(kBsThreads, 2)
     }
     __syncwarp();
   } else {
-    // ================= epilogue (warps 2..5: lane quarter warp % 4)
+    // ================= epilogue (warps 2..: lane quarter warp % 4; warpgroup
+    // wg takes every kEpiWarps/4-th group of 32 token columns)
     const int quarter = warp & 3;
+    const int wg = (warp - 2) >> 2;
+    constexpr int kWG = C::kEpiWarps / 4;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     int it = 0;
@@ -441,11 +453,11 @@ __global__ void __launch_bounds__(kBsThreads, 2)
         const int grp = (m >> 5) & 3;
         uint8_t* atoms = p.hsf + (((size_t)ti * KCo + (m >> 7)) * 2) * kAtom + grp;
 #pragma unroll 1
-        for (int j0 = 0; j0 < NQ; j0 += 32) {
+        for (int j0 = 32 * wg; j0 < NQ; j0 += 32 * kWG) {
           float acc[32], up[32];
           tmem_ld32(dbase + j0, acc);
           tmem_ld32(dbase + C::kAccStride + j0, up);
-          if (j0 + 32 >= NQ) {
+          if (j0 + 32 * kWG >= NQ) {
             tc_fence_before();
             mbar_arrive(dempty(buf));
           }
@@ -471,10 +483,10 @@ __global__ void __launch_bounds__(kBsThreads, 2)
         }
       } else {
 #pragma unroll 1
-        for (int j0 = 0; j0 < NQ; j0 += 32) {
+        for (int j0 = 32 * wg; j0 < NQ; j0 += 32 * kWG) {
           float acc[32];
           tmem_ld32(dbase + j0, acc);
-          if (j0 + 32 >= NQ) {
+          if (j0 + 32 * kWG >= NQ) {
             tc_fence_before();
             mbar_arrive(dempty(buf));
           }
@@ -561,7 +573,7 @@ cudaError_t launch_bs(const BsPlan& p, const uint8_t* wq, const uint8_t* sfa, in
   prm.rows_max = rows_max;
   prm.status = p.status;
   prm.limit_ns = p.limit_ns;
-  bs_stream_kernel<MODE, NQ><<<2 * p.num_sms, kBsThreads, C::kSmem, s>>>(ma, mb, prm);
+  bs_stream_kernel<MODE, NQ><<<C::kCtas * p.num_sms, C::kThreads, C::kSmem, s>>>(ma, mb, prm);
   return cudaGetLastError();
 }
 
