@@ -77,7 +77,7 @@ typedef struct {
   int norm_topk;   /* 1: topk_w = s / sum of the selected s; 0: topk_w = s */
   int max_tokens;  /* largest T a forward call may pass */
   int spin_timeout_ms; /* limit of any device-side wait; 0 selects 2000 ms */
-  int force_path;  /* 0: by token count (T <= 64: path 4, else path 2);
+  int force_path;  /* 0: the library's choice (path 4 for every T);
                       1: CUDA-core kernels everywhere;
                       2: tensor-core GEMM kernels (prefill-size batches);
                       3: streaming tensor-core kernels (decode-size batches;

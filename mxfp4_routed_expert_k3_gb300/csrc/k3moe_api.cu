@@ -362,7 +362,7 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
   // kernels (experts decoded to bf16 in TMEM), 4 as 3 with the experts on
   // the block-scaled MXFP4 tensor cores
   int path = c->cfg.force_path;
-  if (path == 0) path = T <= 64 ? 4 : 2;
+  if (path == 0) path = 4;
   const bool stream = path == 3 || path == 4;
   const bool big = path == 2;
   c->path_last = path;

@@ -115,56 +115,81 @@ __device__ __forceinline__ uint32_t split_e4m3(float x, uint32_t s0, uint32_t s1
 // sf[tile][C/128][t][512] at byte (n%32)*16 + (n/32)*4 + g for row n of the
 // tile (slot_tile[s] = tile << 8 | n), the order in which tcgen05.cp and
 // the MMA read per-row scales (row n in lane n%32 of column n/32).  A half
-// warp covers 128 columns (8 per lane, 4 lanes per scale group); the loop
-// runs per warp so that both halves always meet at the shuffles.
+// warp covers 128 columns per chunk (8 per lane, 4 lanes per scale group)
+// and four chunks of one slot per pass, their loads issued together; the
+// loop runs per warp so that both halves always meet at the shuffles.
+constexpr int kQuantChunks = 4;
 __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, const int* __restrict__ perm, int K, int rows,
                                   int C, int rows_max, const int* __restrict__ slot_tile, uint8_t* __restrict__ q,
                                   uint8_t* __restrict__ sf) {
   const int hl = threadIdx.x & 15, half = (threadIdx.x >> 4) & 1;
   const int KC = C / kQK;
-  const long long nwork = (long long)rows * KC;
+  const int KG = (KC + kQuantChunks - 1) / kQuantChunks;  // chunk groups per row
+  const long long nwork = (long long)rows * KG;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const size_t plane = (size_t)KC * rows_max;  // rows per term
   for (long long wi = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; 2 * wi < nwork; wi += nwarps) {
     const long long i = 2 * wi + half;
     const bool valid = i < nwork;
-    const int s = valid ? (int)(i / KC) : 0, kc = valid ? (int)(i - (long long)s * KC) : 0;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    const int s = valid ? (int)(i / KG) : 0, kg = valid ? (int)(i - (long long)s * KG) : 0;
+    uint4 v[kQuantChunks];
+    int tn = 0;
     if (valid) {
       const int t = perm ? perm[s] / K : s;
-      v = *reinterpret_cast<const uint4*>(src + (size_t)t * C + kc * kQK + hl * 8);
-    }
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t e = 0;
+      tn = slot_tile[s];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) e = max(e, max((w[j] >> 7) & 0xFFu, (w[j] >> 23) & 0xFFu));
-    e = max(e, __shfl_xor_sync(0xFFFFFFFFu, e, 1));
-    e = max(e, __shfl_xor_sync(0xFFFFFFFFu, e, 2));
-    const uint32_t s0 = term0_scale(e), s1 = term1_scale(s0);
-    uint32_t a0 = 0, a1 = 0, b0 = 0, b1 = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t lo = split_e4m3(__uint_as_float(w[j] << 16), s0, s1);
-      const uint32_t hi = split_e4m3(__uint_as_float(w[j] & 0xFFFF0000u), s0, s1);
-      const uint32_t p0 = (lo & 0xFFu) | ((hi & 0xFFu) << 8), p1 = (lo >> 8) | (hi & 0xFF00u);
-      if (j < 2) {
-        a0 |= p0 << (16 * j);
-        a1 |= p1 << (16 * j);
-      } else {
-        b0 |= p0 << (16 * (j - 2));
-        b1 |= p1 << (16 * (j - 2));
+      for (int c = 0; c < kQuantChunks; ++c) {
+        const int kc = kg * kQuantChunks + c;
+        v[c] = kc < KC ? *reinterpret_cast<const uint4*>(src + (size_t)t * C + kc * kQK + hl * 8)
+                       : make_uint4(0u, 0u, 0u, 0u);
       }
+    } else {
+#pragma unroll
+      for (int c = 0; c < kQuantChunks; ++c) v[c] = make_uint4(0u, 0u, 0u, 0u);
     }
-    if (!valid) continue;
-    const size_t plane = (size_t)KC * rows_max;  // rows per term
-    const size_t r0 = (size_t)kc * rows_max + s;
-    *reinterpret_cast<uint2*>(q + r0 * kQK + hl * 8) = make_uint2(a0, b0);
-    *reinterpret_cast<uint2*>(q + (plane + r0) * kQK + hl * 8) = make_uint2(a1, b1);
-    if ((hl & 3) == 0) {
-      const int tn = slot_tile[s];
-      const int n = tn & 0xFF;
-      uint8_t* atom = sf + (((size_t)(tn >> 8) * KC + kc) * 2) * kAtom + (n & 31) * 16 + (n >> 5) * 4 + (hl >> 2);
-      atom[0] = (uint8_t)s0;
-      atom[kAtom] = (uint8_t)s1;
+#pragma unroll
+    for (int c = 0; c < kQuantChunks; ++c) {
+      const int kc = kg * kQuantChunks + c;
+      const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+      uint32_t e = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) e = max(e, max((w[j] >> 7) & 0xFFu, (w[j] >> 23) & 0xFFu));
+      e = max(e, __shfl_xor_sync(0xFFFFFFFFu, e, 1));
+      e = max(e, __shfl_xor_sync(0xFFFFFFFFu, e, 2));
+      const uint32_t s0 = term0_scale(e), s1 = term1_scale(s0);
+      uint32_t a0 = 0, a1 = 0, b0 = 0, b1 = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = split_e4m3(__uint_as_float(w[j] << 16), s0, s1);
+        const uint32_t hi = split_e4m3(__uint_as_float(w[j] & 0xFFFF0000u), s0, s1);
+        const uint32_t p0 = (lo & 0xFFu) | ((hi & 0xFFu) << 8), p1 = (lo >> 8) | (hi & 0xFF00u);
+        if (j < 2) {
+          a0 |= p0 << (16 * j);
+          a1 |= p1 << (16 * j);
+        } else {
+          b0 |= p0 << (16 * (j - 2));
+          b1 |= p1 << (16 * (j - 2));
+        }
+      }
+      // the four groups' scales of this (slot, chunk) are adjacent bytes of
+      // the atom: gather them to lane 0 of the half warp, one 4-byte store per term
+      const uint32_t base_lane = threadIdx.x & 16;
+      uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        w0 |= __shfl_sync(0xFFFFFFFFu, s0, base_lane + 4 * g) << (8 * g);
+        w1 |= __shfl_sync(0xFFFFFFFFu, s1, base_lane + 4 * g) << (8 * g);
+      }
+      if (!valid || kc >= KC) continue;
+      const size_t r0 = (size_t)kc * rows_max + s;
+      *reinterpret_cast<uint2*>(q + r0 * kQK + hl * 8) = make_uint2(a0, b0);
+      *reinterpret_cast<uint2*>(q + (plane + r0) * kQK + hl * 8) = make_uint2(a1, b1);
+      if (hl == 0) {
+        const int n = tn & 0xFF;
+        uint8_t* atom = sf + (((size_t)(tn >> 8) * KC + kc) * 2) * kAtom + (n & 31) * 16 + (n >> 5) * 4;
+        *reinterpret_cast<uint32_t*>(atom) = w0;
+        *reinterpret_cast<uint32_t*>(atom + kAtom) = w1;
+      }
     }
   }
 }
@@ -461,6 +486,7 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
             tc_fence_before();
             mbar_arrive(dempty(buf));
           }
+          uint32_t my_sc = 0;  // lane l keeps the scales of token j0 + l
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int jj = j0 + j;
@@ -473,12 +499,14 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
               const uint32_t q = split_e4m3(bf16_to_f32(hb), s0, s1);
               p.hq[(rbase + row) * kQK + (m & 127)] = (uint8_t)q;
               p.hq[(plane + rbase + row) * kQK + (m & 127)] = (uint8_t)(q >> 8);
-              if (lane == 0) {
-                const int ab = (jj & 31) * 16 + (jj >> 5) * 4;
-                atoms[ab] = (uint8_t)s0;
-                atoms[kAtom + ab] = (uint8_t)s1;
-              }
+              if (lane == j) my_sc = s0 | (s1 << 8);
             }
+          }
+          // one store per term for the 32 tokens: token j0 + l at byte l*16 + (j0/32)*4 (+ group)
+          if (j0 + lane < tile.z) {
+            const int ab = lane * 16 + (j0 >> 5) * 4;
+            atoms[ab] = (uint8_t)my_sc;
+            atoms[kAtom + ab] = (uint8_t)(my_sc >> 8);
           }
         }
       } else {
@@ -617,7 +645,7 @@ cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims
   if (TK <= 0) return cudaSuccess;
   if (T > p.max_tokens) return cudaErrorInvalidValue;
   const BsWs ws = bs_ws_view(p.ws, d, p.max_tokens);
-  const long long halves = (long long)TK * (d.L / kQK);
+  const long long halves = (long long)TK * ((d.L / kQK + kQuantChunks - 1) / kQuantChunks);
   const int blocks = (int)std::min<long long>((halves * 16 + 255) / 256, 8LL * p.num_sms);
   quant_rows_kernel<<<blocks, 256, 0, s>>>(w.lat, w.perm, d.K, TK, d.L, ws.rows_max, ws.slot_tile, ws.lq, ws.lsf);
   return cudaGetLastError();
