@@ -186,7 +186,7 @@ def run_ours(args, rank, world, local_rank):
     batches = DECODE_BATCHES
     maxT = max(batches)
     w = synth.layer_weights(d, seed=1)
-    prefill_T = 0 if args.no_prefill else PREFILL_T
+    prefill_T = 0 if args.no_prefill else args.prefill_tokens
     layer = k3moe.Layer(d, w, max_tokens=max(maxT, prefill_T), device=local_rank, force_path=args.path)
     stream = torch.cuda.Stream(device=dev)
     pool = args.warmup + args.steps
@@ -471,6 +471,9 @@ def main():
     ap.add_argument("--ref-tokens-per-step", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the T=8192 prefill measurement")
+    ap.add_argument("--prefill-tokens", type=int, default=PREFILL_T,
+                    help="tokens of the prefill measurement (default 8192; with --experts E, 8192*E/896 keeps "
+                         "the tokens per expert of the full layer, for small profiling captures)")
     ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2, 3, 4],
                     help="kernel path (0 = the library's choice by token count; see k3moe_config.force_path)")
     ap.add_argument("--experts", type=int, default=896,
