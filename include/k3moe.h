@@ -113,10 +113,12 @@ typedef struct {
 int k3moe_create(const k3moe_config* cfg, int cuda_device, k3moe_ctx** out);
 
 /* Copies the weights (host memory, checkpoint layout) to the device.  The
- * MXFP4 tensors are re-laid into 128-row x 64-column tiles (packed nibbles
- * followed by their scales) for the expert kernels; values are unchanged.
- * Any scale byte equal to 0xFF is rejected with EBADSCALE before anything
- * is copied.  May be called again to replace the weights.  Synchronous. */
+ * MXFP4 tensors are regrouped (values unchanged) into 128 x 128 blocks of
+ * nibbles and 512-byte scale atoms for the block-scaled expert kernels
+ * (path 4); contexts created with force_path 1, 2 or 3 also keep a copy in
+ * 128-row x 64-column tiles for those paths' kernels.  Any scale byte equal
+ * to 0xFF is rejected with EBADSCALE before anything is copied.  May be
+ * called again to replace the weights.  Synchronous. */
 int k3moe_load_weights(k3moe_ctx* ctx, const k3moe_weights* w);
 
 /* One layer forward for T tokens, enqueued on `cuda_stream` (a

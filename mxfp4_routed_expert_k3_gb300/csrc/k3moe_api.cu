@@ -253,19 +253,25 @@ int k3moe_load_weights(k3moe_ctx* c, const k3moe_weights* wt) {
   K3_CUDA(c, cudaSetDevice(c->device), "cudaSetDevice");
   const size_t gu_bytes = E * (I / 128) * (L / 64) * 2 * (size_t)k3::kTileBytes;
   const size_t d_bytes = E * (L / 128) * (I / 64) * (size_t)k3::kTileBytes;
+  // The bf16-decode tile copy of the experts serves paths 1-3 only; the
+  // default (path 4) reads the block-scaled copy alone.
+  const bool want_tiles = c->cfg.force_path >= 1 && c->cfg.force_path <= 3;
   if (!c->wcat) {
     K3_CUDA(c, cudaMalloc(&c->wcat, (E + L) * H * 2), "cudaMalloc(router+down_proj)");
     K3_CUDA(c, cudaMalloc(&c->bias, E * 4), "cudaMalloc(bias)");
     K3_CUDA(c, cudaMalloc(&c->gamma, L * 2), "cudaMalloc(gamma)");
     K3_CUDA(c, cudaMalloc(&c->wu, H * L * 2), "cudaMalloc(up_proj)");
-    K3_CUDA(c, cudaMalloc(&c->gu_tiles, gu_bytes), "cudaMalloc(gate/up tiles)");
-    K3_CUDA(c, cudaMalloc(&c->d_tiles, d_bytes), "cudaMalloc(down tiles)");
+    if (want_tiles) {
+      K3_CUDA(c, cudaMalloc(&c->gu_tiles, gu_bytes), "cudaMalloc(gate/up tiles)");
+      K3_CUDA(c, cudaMalloc(&c->d_tiles, d_bytes), "cudaMalloc(down tiles)");
+    }
     // block-scaled layout: one allocation, carved as gu_q | gu_sf | d_q | d_sf
     K3_CUDA(c, cudaMalloc(&c->bw.gu_q, k3::bs_weight_bytes(c->d)), "cudaMalloc(block-scaled experts)");
     c->bw.gu_sf = c->bw.gu_q + E * 2 * I * L / 2;
     c->bw.d_q = c->bw.gu_sf + E * 2 * I * L / 32;
     c->bw.d_sf = c->bw.d_q + E * L * I / 2;
-    c->weight_bytes = (E + L) * H * 2 + E * 4 + L * 2 + H * L * 2 + gu_bytes + d_bytes + k3::bs_weight_bytes(c->d);
+    c->weight_bytes = (E + L) * H * 2 + E * 4 + L * 2 + H * L * 2 + (want_tiles ? gu_bytes + d_bytes : 0) +
+                      k3::bs_weight_bytes(c->d);
   }
   c->loaded = false;
   K3_CUDA(c, cudaMemcpy(c->wcat, wt->router_w, E * H * 2, cudaMemcpyHostToDevice), "copy router_w");
@@ -298,6 +304,7 @@ int k3moe_load_weights(k3moe_ctx* c, const k3moe_weights* wt) {
   };
   int rc = K3MOE_OK;
   for (const Job& j : jobs) {
+    if (!want_tiles) break;
     for (size_t e0 = 0; e0 < E && rc == K3MOE_OK; e0 += chunk) {
       const size_t ne = std::min(chunk, E - e0);
       if ((e = cudaMemcpy(st_p, j.p + e0 * per_expert_packed, ne * per_expert_packed, cudaMemcpyHostToDevice)) ||

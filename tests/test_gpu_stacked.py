@@ -1,0 +1,117 @@
+"""Four stacked K3-dim routed layers on one GPU: independent seeded weights
+(about 63 GB of MXFP4 experts resident at once), each layer's output
+rescaled per token into the next layer's input, x_{l+1} = bf16(y_l / rms(y_l)).
+A T = 32768 prefill and a T = 1 decode captured in one CUDA graph run
+through all four layers.
+
+Every layer is checked against the CPU oracle teacher-forced: the oracle
+gets the GPU's own input of that layer for a seeded sample of tokens, so a
+difference cannot compound across layers.  Layer 2..4 inputs are not
+resampled, so some tokens have a K-th/(K+1)-th router-key gap below the
+1e-3 margin the other tests force; for those the routing may legitimately
+differ, they are counted and reported, and the routing and output checks
+run on the other tokens (kimi-k3-mlx README, "Architecture": the layer is
+the routed path of every MoE block; the stacking and rescale only feed
+realistic inputs into layers 2..4)."""
+import numpy as np
+import pytest
+import torch
+
+from _cases import GAP, assert_routing_equal, assert_y_close
+from mxfp4_routed_expert_k3_gb300 import k3moe, synth
+from mxfp4_routed_expert_k3_gb300.dims import K3
+from oracle import oracle as ora
+
+pytestmark = pytest.mark.gpu
+
+N_LAYERS = 4
+T_PREFILL = 32768
+N_SAMPLE = 8
+
+
+def rescale(y_bits: torch.Tensor) -> torch.Tensor:
+    """x = bf16(y / rms(y)) per token (fp32 arithmetic, round to nearest even)."""
+    f = y_bits.view(torch.bfloat16).float()
+    r = torch.sqrt(torch.mean(f * f, dim=1, keepdim=True))
+    return (f / r).to(torch.bfloat16).view(torch.int16)
+
+
+@pytest.fixture(scope="module")
+def stack():
+    torch.cuda.empty_cache()
+    layers = []
+    try:
+        for l in range(N_LAYERS):
+            w = synth.layer_weights(K3, seed=4 + l)
+            layers.append(k3moe.Layer(K3, w, max_tokens=T_PREFILL))
+            del w
+        yield layers
+    finally:
+        for layer in layers:
+            layer.close()
+
+
+def _check_layer(l: int, x_bits: np.ndarray, y_bits: np.ndarray, idx: np.ndarray, wts: np.ndarray, label: str):
+    """Teacher-forced oracle check of layer l on the given tokens (inputs x_bits)."""
+    w = synth.layer_weights(K3, seed=4 + l)
+    _, _, _, keys = ora.route(K3, x_bits, w["router_w"], w["router_bias"], want_keys=True)
+    gap = keys[:, K3.top_k - 1].astype(np.float64) - keys[:, K3.top_k].astype(np.float64)
+    clear = np.flatnonzero(gap > GAP)
+    print(f"{label} layer {l}: {x_bits.shape[0] - clear.size} of {x_bits.shape[0]} tokens within the "
+          f"{GAP} key band (routing not compared for them)")
+    if clear.size == 0:
+        return
+    ref = ora.forward(K3, w, np.ascontiguousarray(x_bits[clear]))
+    assert_routing_equal(idx[clear], wts[clear], ref["idx"], ref["w"], f"{label} layer {l}")
+    m = assert_y_close(y_bits[clear], ref["y"], f"{label} layer {l}")
+    print(f"{label} layer {l}", m)
+
+
+def test_stacked_prefill_32768(stack):
+    s = torch.cuda.current_stream()
+    x = torch.from_numpy(synth.token_rows(K3, 400, T_PREFILL).view(np.int16)).cuda()
+    sample = np.sort(np.random.default_rng(4).choice(T_PREFILL, N_SAMPLE, replace=False))
+    sample[-1] = T_PREFILL - 1
+    per_layer = []
+    for layer in stack:
+        y, idx, wts = layer.forward_torch(x, stream=s)
+        torch.cuda.synchronize()
+        assert layer.status() == 0, k3moe.last_error(layer.ctx)
+        assert layer.query("path_last") == k3moe.PATH_BLOCK_SCALED
+        yf = y.view(torch.bfloat16).float()
+        assert bool(torch.isfinite(yf).all())
+        per_layer.append(tuple(a.cpu().numpy()[sample] for a in (x, y, idx, wts)))
+        x = rescale(y)
+    for l, (xs, ys, idx, wts) in enumerate(per_layer):
+        _check_layer(l, xs.view(np.uint16), ys.view(np.uint16), idx, wts, "stacked prefill")
+
+
+def test_stacked_decode_graph(stack):
+    s = torch.cuda.Stream()
+    x0 = torch.from_numpy(synth.token_rows(K3, 401, 1).view(np.int16)).cuda()
+    xs = [torch.empty((1, K3.hidden), dtype=torch.int16, device="cuda") for _ in range(N_LAYERS)]
+    ys = [torch.empty((1, K3.hidden), dtype=torch.int16, device="cuda") for _ in range(N_LAYERS)]
+    ids = [torch.empty((1, K3.top_k), dtype=torch.int32, device="cuda") for _ in range(N_LAYERS)]
+    ws = [torch.empty((1, K3.top_k), dtype=torch.float32, device="cuda") for _ in range(N_LAYERS)]
+
+    def chain():
+        for l, layer in enumerate(stack):
+            if l > 0:
+                xs[l].copy_(rescale(ys[l - 1]))
+            layer.forward(xs[l], ys[l], ids[l], ws[l], stream=s)
+
+    xs[0].copy_(x0)
+    with torch.cuda.stream(s):
+        chain()  # eager warm-up of every layer before capture
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        chain()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    for layer in stack:
+        assert layer.status() == 0, k3moe.last_error(layer.ctx)
+    for l in range(N_LAYERS):
+        _check_layer(l, xs[l].cpu().numpy().view(np.uint16), ys[l].cpu().numpy().view(np.uint16),
+                     ids[l].cpu().numpy(), ws[l].cpu().numpy(), "stacked decode")
