@@ -214,15 +214,16 @@ def run_ours(args, rank, world, local_rank):
             with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
                 layer.forward(x_in[T], y[T], idx[T], wt[T], stream=stream)
             out[T] = g
-        k3moe.profile(layer.ctx, False)
         return out
     graphs = capture(False)
-    graphs_prof = capture(True)
     launches_per_forward = {}
     for T in batches:
         layer.forward(x_in[T], y[T], idx[T], wt[T], stream=stream)
         launches_per_forward[T] = layer.query("launches_last")
     stream.synchronize()
+    # captured last and left enabled until read: an eager forward or
+    # disabling the profile resets the context's record of the event slots
+    graphs_prof = capture(True)
 
     ev = {T: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(pool)]
           for T in batches}
@@ -269,6 +270,7 @@ def run_ours(args, rank, world, local_rank):
                 graphs_prof[T].replay()
             stream.synchronize()
             per_kernel[T].append(k3moe.profile_read(layer.ctx))
+    k3moe.profile(layer.ctx, False)
 
     fwd_ms = {T: [ev[T][i][0].elapsed_time(ev[T][i][1]) for i in range(args.warmup, pool)] for T in batches}
     step_ms = sum(statistics.mean(fwd_ms[T]) for T in batches)

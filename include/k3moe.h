@@ -86,8 +86,9 @@ typedef struct {
                       4: as 3, with the expert GEMMs on the block-scaled
                          MXFP4 tensor cores (tcgen05 kind::mxf8f6f4: e2m1
                          weights and e8m0 scales as stored, activations as
-                         two exact block-scaled e4m3 terms; tiles of 32
-                         token rows up to T = 128, 80 above) */
+                         two exact block-scaled e4m3 terms; tiles of 16
+                         token rows up to T = 128, both terms in one MMA,
+                         80 rows above) */
 } k3moe_config;
 
 /* Host arrays in checkpoint layout, experts stacked along dim 0.  Row-major;

@@ -111,23 +111,26 @@ __device__ __forceinline__ uint32_t split_e4m3(float x, uint32_t s0, uint32_t s1
 }
 
 // Slot-ordered rows: dst row s = src row (perm ? perm[s] / K : s), written
-// as terms q[t][C/128][rows_max][128]; the scales go to the tile atoms
+// as terms q[C/128][t][rows_max][128]; the scales go to the tile atoms
 // sf[tile][C/128][t][512] at byte (n%32)*16 + (n/32)*4 + g for row n of the
 // tile (slot_tile[s] = tile << 8 | n), the order in which tcgen05.cp and
-// the MMA read per-row scales (row n in lane n%32 of column n/32).  A half
+// the MMA read per-row scales (row n in lane n%32 of column n/32).  With
+// stack > 0 (tiles of `stack` rows whose two terms form one MMA operand)
+// term 1 of row n is row stack + n of the term-0 atom.  A half
 // warp covers 128 columns per chunk (8 per lane, 4 lanes per scale group)
 // and four chunks of one slot per pass, their loads issued together; the
 // loop runs per warp so that both halves always meet at the shuffles.
 constexpr int kQuantChunks = 4;
 __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, const int* __restrict__ perm, int K, int rows,
-                                  int C, int rows_max, const int* __restrict__ slot_tile, uint8_t* __restrict__ q,
-                                  uint8_t* __restrict__ sf) {
+                                  int C, int rows_max, const int* __restrict__ slot_tile, int stack,
+                                  uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+  pdl_trigger();
+  pdl_wait();
   const int hl = threadIdx.x & 15, half = (threadIdx.x >> 4) & 1;
   const int KC = C / kQK;
   const int KG = (KC + kQuantChunks - 1) / kQuantChunks;  // chunk groups per row
   const long long nwork = (long long)rows * KG;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-  const size_t plane = (size_t)KC * rows_max;  // rows per term
   for (long long wi = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; 2 * wi < nwork; wi += nwarps) {
     const long long i = 2 * wi + half;
     const bool valid = i < nwork;
@@ -181,14 +184,14 @@ __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, const int* _
         w1 |= __shfl_sync(0xFFFFFFFFu, s1, base_lane + 4 * g) << (8 * g);
       }
       if (!valid || kc >= KC) continue;
-      const size_t r0 = (size_t)kc * rows_max + s;
+      const size_t r0 = (size_t)kc * 2 * rows_max + s;
       *reinterpret_cast<uint2*>(q + r0 * kQK + hl * 8) = make_uint2(a0, b0);
-      *reinterpret_cast<uint2*>(q + (plane + r0) * kQK + hl * 8) = make_uint2(a1, b1);
+      *reinterpret_cast<uint2*>(q + (r0 + rows_max) * kQK + hl * 8) = make_uint2(a1, b1);
       if (hl == 0) {
-        const int n = tn & 0xFF;
-        uint8_t* atom = sf + (((size_t)(tn >> 8) * KC + kc) * 2) * kAtom + (n & 31) * 16 + (n >> 5) * 4;
-        *reinterpret_cast<uint32_t*>(atom) = w0;
-        *reinterpret_cast<uint32_t*>(atom + kAtom) = w1;
+        const int n = tn & 0xFF, n1 = stack ? stack + n : n;
+        uint8_t* atom = sf + (((size_t)(tn >> 8) * KC + kc) * 2) * kAtom;
+        *reinterpret_cast<uint32_t*>(atom + (n & 31) * 16 + (n >> 5) * 4) = w0;
+        *reinterpret_cast<uint32_t*>(atom + (stack ? 0 : kAtom) + (n1 & 31) * 16 + (n1 >> 5) * 4) = w1;
       }
     }
   }
@@ -254,6 +257,12 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
 template <int MODE, int NQ>
 struct BsCfg {
   static constexpr bool kBig = NQ > 32;
+  // Decode tiles put both activation terms in one MMA: B rows [term 0 of the
+  // NQ tokens; term 1 of the same tokens], N = 2 * NQ, and the epilogue adds
+  // accumulator columns j and NQ + j.  An MMA of N <= 32 costs about as much
+  // tensor-pipe time as one of N = 16, so this halves the pipe time per
+  // weight byte, which bounds the decode stream otherwise.
+  static constexpr bool kStack = !kBig;
   static constexpr int kCtas = 2;                                           // CTAs per SM
   static constexpr int kEpiWarps = 4;                                       // epilogue warps
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
@@ -268,13 +277,19 @@ struct BsCfg {
   static constexpr int kStageBytes = (kOffSfb + 2 * kNK * kAtom + 1023) / 1024 * 1024;
   static constexpr int kStages = 2;
   static constexpr int kDBuf = (MODE == BS_GATEUP && kBig) ? 1 : 2;        // accumulator buffers
+  static constexpr int kAccW = kStack ? 2 * NQ : (NQ + 15) / 16 * 16;     // accumulator columns (MMA N)
   static constexpr int kAccStride = kBig ? 128 : 32;                        // TMEM columns between matrices
   static constexpr int kBufStride = kNumA * kAccStride;                     // TMEM columns between buffers
-  static constexpr int kSfBase = (kDBuf - 1) * kBufStride + (kNumA - 1) * kAccStride + (NQ + 15) / 16 * 16;
-  static constexpr int kSfCols = 4 * kNA + 8 * kNK;  // weight atoms, then term x chunk activation atoms
+  static constexpr int kSfBase = (kDBuf - 1) * kBufStride + (kNumA - 1) * kAccStride + kAccW;
+  // weight atoms, then the activation atoms: one per chunk holding both
+  // terms' rows (stacked), else one per chunk and term
+  static constexpr int kSfbAtoms = kStack ? 1 : 2;
+  static constexpr int kSfCols = 4 * kNA + 4 * kSfbAtoms * kNK;
   static constexpr int kTmemCols = 256;
   static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
   static_assert(kSfBase % 4 == 0 && kSfBase + kStages * kSfCols <= kTmemCols, "TMEM budget");
+  static_assert(kAccW <= kAccStride && kAccW % 16 == 0, "accumulator width");
+  static_assert(!kStack || 2 * NQ <= 32, "stacked rows share one 32-lane scale column");
   static_assert(kCtas * kTmemCols <= 512, "TMEM per SM");
   static_assert(kB % 1024 == 0, "term blocks must keep the 1024-byte swizzle alignment");
   static_assert(kCtas * (kSmem + 1024) <= 233472, "shared memory per SM");
@@ -311,6 +326,8 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  pdl_trigger();
+  pdl_wait();
   const int n_items = *p.count * p.MT;
   if ((int)blockIdx.x >= n_items) return;
 
@@ -362,7 +379,7 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
           mbar_expect_tx(full(s), (uint32_t)(C::kNA * (C::kA / 2) + 2 * C::kNK * C::kB + n_sfa * kAtom +
                                              2 * nk * kAtom));
           tma_load_3d(st, &map_a, full(s), 0, 0, (int)first);
-          tma_load_4d(st + C::kOffB, &map_b, full(s), 0, tile.y, kc0, 0);
+          tma_load_4d(st + C::kOffB, &map_b, full(s), 0, tile.y, 0, kc0);
           bulk_load(st + C::kOffSfa, p.sfa + first * kAtom, n_sfa * kAtom, full(s));
           bulk_load(st + C::kOffSfb, p.sfb + ((size_t)ti * p.KC + kc0) * 2 * kAtom, 2 * nk * kAtom, full(s));
           ++issued;
@@ -400,8 +417,9 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
         }
         tc_fence_after();
         const uint32_t d0 = tmem + buf * C::kBufStride;
-        // MMA N: the tile's rows rounded up to 16 (never beyond the accumulator's NQ columns)
-        const uint32_t n = (uint32_t)min(p.tiles[item / p.MT].w, (NQ + 15) / 16 * 16);
+        // MMA N: stacked, both terms of the NQ rows; else the tile's rows
+        // rounded up to 16 (never beyond the accumulator's columns)
+        const uint32_t n = C::kStack ? (uint32_t)C::kAccW : (uint32_t)min(p.tiles[item / p.MT].w, C::kAccW);
         for (int ks = 0; ks < p.KS; ++ks, ++kg) {
           const int s = kg % C::kStages;
           if (!mbar_wait(full(s), (kg / C::kStages) & 1, g, 4u)) {
@@ -416,9 +434,13 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
 #pragma unroll
           for (int j = 0; j < C::kNA; ++j)
             if (MODE == BS_GATEUP || j < nk) tc_cp_scales(sfc + 4 * j, sfa_base + so + (j * kAtom >> 4));
+          // activation atoms in smem: [chunk][term][512] (stacked: term slot 0 holds both)
 #pragma unroll
-          for (int j = 0; j < 2 * C::kNK; ++j)
-            if (j < 2 * nk) tc_cp_scales(sfc + 4 * C::kNA + 4 * j, sfb_base + so + (j * kAtom >> 4));
+          for (int c = 0; c < C::kNK; ++c)
+#pragma unroll
+            for (int t = 0; t < C::kSfbAtoms; ++t)
+              if (c < nk)
+                tc_cp_scales(sfc + 4 * C::kNA + 4 * (c * C::kSfbAtoms + t), sfb_base + so + ((c * 2 + t) * kAtom >> 4));
           const uint32_t first = ks ? 1u : 0u;
 #pragma unroll
           for (int c = 0; c < C::kNK; ++c) {
@@ -428,13 +450,14 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
 #pragma unroll
               for (int a = 0; a < C::kNumA; ++a)
 #pragma unroll
-                for (int t = 0; t < 2; ++t) {
+                for (int t = 0; t < (C::kStack ? 1 : 2); ++t) {
+                  // B blocks of the 4-D box are [chunk][term]; stacked, the
+                  // two terms' rows are one 2*NQ-row operand
                   const int ablk = (MODE == BS_GATEUP) ? a : c;
-                  const int bblk = t * C::kNK + c;  // term block of the 4-D box ([term][chunk])
-                  const int sfbj = c * 2 + t;       // activation atom ([chunk][term])
+                  const int bblk = c * 2 + t;
                   umma_bs(d0 + a * C::kAccStride, a_d + ((ablk * C::kA + kb * 32) >> 4),
                           b_d + ((bblk * C::kB + kb * 32) >> 4), bs_idesc(kb, kb, n), sfc + 4 * ablk,
-                          sfc + 4 * C::kNA + 4 * sfbj, (c | kb | t) ? 1u : first);
+                          sfc + 4 * C::kNA + 4 * (c * C::kSfbAtoms + t), (c | kb | t) ? 1u : first);
                 }
           }
           umma_commit(sfree(s));
@@ -470,25 +493,34 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
       const int mt = item - ti * p.MT;
       const int m = mt * kQM + r;
       const uint32_t dbase = lane_base + buf * C::kBufStride;
+      // token columns per group of the accumulator: 32, or NQ when the two
+      // terms' partial sums sit in columns j and NQ + j
+      constexpr int JW = C::kStack ? NQ : 32;
       if (MODE == BS_GATEUP) {
         // h as bf16 and as the two e4m3 terms (and scale atoms) of the down GEMM's B operand
         const int KCo = p.ld_out / kQK;
-        const size_t plane = (size_t)KCo * p.rows_max;
-        const size_t rbase = (size_t)(m >> 7) * p.rows_max;
+        const size_t rb0 = (size_t)((m >> 7) * 2) * p.rows_max, rb1 = rb0 + p.rows_max;  // [KC][2][rows_max]
         const int grp = (m >> 5) & 3;
         uint8_t* atoms = p.hsf + (((size_t)ti * KCo + (m >> 7)) * 2) * kAtom + grp;
 #pragma unroll 1
-        for (int j0 = 32 * wg; j0 < NQ; j0 += 32 * kWG) {
+        for (int j0 = JW * wg; j0 < NQ; j0 += JW * kWG) {
           float acc[32], up[32];
-          tmem_ld32(dbase + j0, acc);
-          tmem_ld32(dbase + C::kAccStride + j0, up);
-          if (j0 + 32 * kWG >= NQ) {
+          tmem_ld32(dbase + (C::kStack ? 0 : j0), acc);
+          tmem_ld32(dbase + C::kAccStride + (C::kStack ? 0 : j0), up);
+          if (j0 + JW * kWG >= NQ) {
             tc_fence_before();
             mbar_arrive(dempty(buf));
           }
+          if (C::kStack) {
+#pragma unroll
+            for (int j = 0; j < JW; ++j) {
+              acc[j] += acc[j + JW];
+              up[j] += up[j + JW];
+            }
+          }
           uint32_t my_sc = 0;  // lane l keeps the scales of token j0 + l
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
+          for (int j = 0; j < JW; ++j) {
             const int jj = j0 + j;
             if (jj < tile.z) {
               const size_t row = (size_t)(tile.y + jj);
@@ -497,30 +529,33 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
               const uint32_t emax = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(hb >> 7) & 0xFFu);
               const uint32_t s0 = term0_scale(emax), s1 = term1_scale(s0);
               const uint32_t q = split_e4m3(bf16_to_f32(hb), s0, s1);
-              p.hq[(rbase + row) * kQK + (m & 127)] = (uint8_t)q;
-              p.hq[(plane + rbase + row) * kQK + (m & 127)] = (uint8_t)(q >> 8);
+              p.hq[(rb0 + row) * kQK + (m & 127)] = (uint8_t)q;
+              p.hq[(rb1 + row) * kQK + (m & 127)] = (uint8_t)(q >> 8);
               if (lane == j) my_sc = s0 | (s1 << 8);
             }
           }
-          // one store per term for the 32 tokens: token j0 + l at byte l*16 + (j0/32)*4 (+ group)
-          if (j0 + lane < tile.z) {
-            const int ab = lane * 16 + (j0 >> 5) * 4;
-            atoms[ab] = (uint8_t)my_sc;
-            atoms[kAtom + ab] = (uint8_t)(my_sc >> 8);
+          // one store per term for the group's tokens: token row jj at byte
+          // (jj%32)*16 + (jj/32)*4 (+ group) of the term's atom; stacked, term
+          // 1 is row NQ + jj of the first atom
+          const int jj = j0 + lane;
+          if (lane < JW && jj < tile.z) {
+            const int r1 = C::kStack ? NQ + jj : jj;
+            atoms[(jj & 31) * 16 + (jj >> 5) * 4] = (uint8_t)my_sc;
+            atoms[(C::kStack ? 0 : kAtom) + (r1 & 31) * 16 + (r1 >> 5) * 4] = (uint8_t)(my_sc >> 8);
           }
         }
       } else {
 #pragma unroll 1
-        for (int j0 = 32 * wg; j0 < NQ; j0 += 32 * kWG) {
+        for (int j0 = JW * wg; j0 < NQ; j0 += JW * kWG) {
           float acc[32];
-          tmem_ld32(dbase + j0, acc);
-          if (j0 + 32 * kWG >= NQ) {
+          tmem_ld32(dbase + (C::kStack ? 0 : j0), acc);
+          if (j0 + JW * kWG >= NQ) {
             tc_fence_before();
             mbar_arrive(dempty(buf));
           }
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j0 + j < tile.z) p.o[(size_t)(tile.y + j0 + j) * p.ld_out + m] = acc[j];
+          for (int j = 0; j < JW; ++j)
+            if (j0 + j < tile.z) p.o[(size_t)(tile.y + j0 + j) * p.ld_out + m] = C::kStack ? acc[j] + acc[j + JW] : acc[j];
         }
       }
     }
@@ -548,20 +583,20 @@ bool map_e2m1(CUtensorMap* map, const void* base, long long nbox, int depth) {
   const cuuint32_t box[3] = {(cuuint32_t)kQK, (cuuint32_t)kQM, (cuuint32_t)depth};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
-// Activation terms q[2][KC][rows_max][128]: box 128 x box_rows x nk chunks x
-// 2 terms, 128-byte swizzle.
+// Activation terms q[KC][2][rows_max][128]: box 128 x box_rows x 2 terms x
+// nk chunks, 128-byte swizzle; in shared memory [chunk][term][row][128].
 bool map_terms(CUtensorMap* map, const void* base, int KC, int rows_max, int box_rows, int nk) {
-  const cuuint64_t dims[4] = {(cuuint64_t)kQK, (cuuint64_t)rows_max, (cuuint64_t)KC, 2};
-  const cuuint64_t strides[3] = {(cuuint64_t)kQK, (cuuint64_t)rows_max * kQK, (cuuint64_t)KC * rows_max * kQK};
-  const cuuint32_t box[4] = {(cuuint32_t)kQK, (cuuint32_t)box_rows, (cuuint32_t)nk, 2};
+  const cuuint64_t dims[4] = {(cuuint64_t)kQK, (cuuint64_t)rows_max, 2, (cuuint64_t)KC};
+  const cuuint64_t strides[3] = {(cuuint64_t)kQK, (cuuint64_t)rows_max * kQK, (cuuint64_t)2 * rows_max * kQK};
+  const cuuint32_t box[4] = {(cuuint32_t)kQK, (cuuint32_t)box_rows, 2, (cuuint32_t)nk};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 struct BsWs {
   int rows_max;       // slots: max_tokens * K
   int max_tiles;      // bound on the tile list length
-  uint8_t *lq, *lsf;  // latent rows: terms [2][L/128][rows_max][128], atoms [max_tiles][L/128][2][512]
-  uint8_t *hq, *hsf;  // h rows:      terms [2][I/128][rows_max][128], atoms [max_tiles][I/128][2][512]
+  uint8_t *lq, *lsf;  // latent rows: terms [L/128][2][rows_max][128], atoms [max_tiles][L/128][2][512]
+  uint8_t *hq, *hsf;  // h rows:      terms [I/128][2][rows_max][128], atoms [max_tiles][I/128][2][512]
   int* slot_tile;     // [rows_max]: tile << 8 | row within the tile
   size_t total;
 };
@@ -601,8 +636,7 @@ cudaError_t launch_bs(const BsPlan& p, const uint8_t* wq, const uint8_t* sfa, in
   prm.rows_max = rows_max;
   prm.status = p.status;
   prm.limit_ns = p.limit_ns;
-  bs_stream_kernel<MODE, NQ><<<C::kCtas * p.num_sms, C::kThreads, C::kSmem, s>>>(ma, mb, prm);
-  return cudaGetLastError();
+  return launch_pdl(bs_stream_kernel<MODE, NQ>, C::kCtas * p.num_sms, C::kThreads, C::kSmem, s, ma, mb, prm);
 }
 
 }  // namespace
@@ -640,15 +674,16 @@ cudaError_t prepare_bs_kernels() {
   return e;
 }
 
-cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s) {
+cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims& d, int tile_rows, cudaStream_t s) {
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
-  if (T > p.max_tokens) return cudaErrorInvalidValue;
+  if (T > p.max_tokens || (tile_rows != kBsDecodeRows && tile_rows != kBsPrefillRows)) return cudaErrorInvalidValue;
+  const int stack = BsCfg<BS_GATEUP, kBsDecodeRows>::kStack && tile_rows == kBsDecodeRows ? kBsDecodeRows : 0;
   const BsWs ws = bs_ws_view(p.ws, d, p.max_tokens);
   const long long halves = (long long)TK * ((d.L / kQK + kQuantChunks - 1) / kQuantChunks);
   const int blocks = (int)std::min<long long>((halves * 16 + 255) / 256, 8LL * p.num_sms);
-  quant_rows_kernel<<<blocks, 256, 0, s>>>(w.lat, w.perm, d.K, TK, d.L, ws.rows_max, ws.slot_tile, ws.lq, ws.lsf);
-  return cudaGetLastError();
+  return launch_pdl(quant_rows_kernel, blocks, 256, 0, s, w.lat, w.perm, d.K, TK, d.L, ws.rows_max, ws.slot_tile,
+                    stack, ws.lq, ws.lsf);
 }
 
 cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* tiles, const int* tile_count,

@@ -43,9 +43,10 @@ struct BsPlan {
   Dims dims{};
 };
 // Tile heights (token rows per tile, the MMA's N bound): decode-size batches
-// use short tiles (every weight byte streamed once per forward), larger
+// use short tiles (every weight byte streamed once per forward; the two
+// activation terms of the 16 rows form one 32-row MMA operand), larger
 // batches taller ones (fewer weight re-reads per token).
-constexpr int kBsDecodeRows = 32;
+constexpr int kBsDecodeRows = 16;
 constexpr int kBsPrefillRows = 80;
 inline int bs_tile_rows(int T) { return T <= 128 ? kBsDecodeRows : kBsPrefillRows; }
 size_t bs_ws_bytes(const Dims& d, int max_tokens);
@@ -54,8 +55,9 @@ int* bs_slot_tile(const BsPlan& p);
 cudaError_t prepare_bs_kernels();
 
 // Slot-ordered latent rows (lat[perm[s] / K]) written as two e4m3 terms, and
-// their scales as per-tile atoms (needs the tile list's slot map).
-cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s);
+// their scales as per-tile atoms (needs the tile list's slot map; tile_rows
+// is the tile height the expert kernels will use).
+cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims& d, int tile_rows, cudaStream_t s);
 // gate/up over the tile list (tiles of at most tile_rows rows): h (bf16,
 // slot order) and its two-term e4m3 form for the down GEMM.
 cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* tiles, const int* tile_count,

@@ -151,6 +151,8 @@ __global__ void __launch_bounds__(256) topk_cta_kernel(const float* __restrict__
   __shared__ float cand_s[32];
   __shared__ int eq_e[2048];
   __shared__ float eq_s[2048];
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* row = logits + (size_t)t * ld;
   uint32_t u[EPT];
@@ -278,13 +280,8 @@ cudaError_t launch_topk(const float* logits, int T, int E, int ld, const float* 
                         float rsf, int32_t* idx, float* w, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   if (K > 32 || E > 2048 || K > E) return cudaErrorInvalidValue;
-  if (E <= 256)
-    topk_cta_kernel<1><<<T, 256, 0, s>>>(logits, E, ld, bias, K, norm_topk, rsf, idx, w);
-  else if (E <= 1024)
-    topk_cta_kernel<4><<<T, 256, 0, s>>>(logits, E, ld, bias, K, norm_topk, rsf, idx, w);
-  else
-    topk_cta_kernel<8><<<T, 256, 0, s>>>(logits, E, ld, bias, K, norm_topk, rsf, idx, w);
-  return cudaGetLastError();
+  auto kernel = E <= 256 ? topk_cta_kernel<1> : E <= 1024 ? topk_cta_kernel<4> : topk_cta_kernel<8>;
+  return launch_pdl(kernel, T, 256, 0, s, logits, E, ld, bias, K, norm_topk, rsf, idx, w);
 }
 
 // =====================================================================
@@ -434,6 +431,8 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(const int32_t* __restr
   __shared__ int base[2048];
   __shared__ int warp_tot[32];
   __shared__ int total_s;
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int TK = T * K;
   for (int e = threadIdx.x; e < E; e += 1024) hist[e] = 0;
@@ -513,12 +512,12 @@ cudaError_t launch_route_small(const float* logits, int T, int E, const float* b
                                int32_t* idx, float* w, int* counts, int* offsets, int* active, int* perm, int* slot,
                                int bn_max, int4* tiles, int* tile_count, int* slot_tile, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  if (T * K > 1024 || E > 2048 || bn_max > 255) return cudaErrorInvalidValue;
+  // tiles of at least 16 rows (the tile list's capacity), row field of 8 bits
+  if (T * K > 1024 || E > 2048 || bn_max < 16 || bn_max > 255) return cudaErrorInvalidValue;
   cudaError_t e = launch_topk(logits, T, E, E, bias, K, norm_topk, rsf, idx, w, s);
   if (e != cudaSuccess) return e;
-  perm_small_kernel<<<1, 1024, 0, s>>>(idx, T, E, K, counts, offsets, active, perm, slot, bn_max, tiles, tile_count,
-                                       slot_tile);
-  return cudaGetLastError();
+  return launch_pdl(perm_small_kernel, 1, 1024, 0, s, idx, T, E, K, counts, offsets, active, perm, slot, bn_max, tiles,
+                    tile_count, slot_tile);
 }
 
 // =====================================================================
@@ -740,6 +739,8 @@ __global__ void __launch_bounds__(1024) combine_rmsnorm_kernel(const float* __re
   __shared__ int sl[32];
   __shared__ float wk[32];
   __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x;
   if (threadIdx.x < K) {
     sl[threadIdx.x] = slot[(size_t)t * K + threadIdx.x];
@@ -806,8 +807,8 @@ cudaError_t launch_combine_rmsnorm(const float* o, const int* slot, const float*
                                    int T, const Dims& d, uint16_t* n, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const int threads = std::min(1024, ((d.L / 4 + 31) / 32) * 32);
-  combine_rmsnorm_kernel<<<T, threads, sizeof(float) * d.L, s>>>(o, slot, topk_w, gamma, d.K, d.L, d.rms_eps, n);
-  return cudaGetLastError();
+  return launch_pdl(combine_rmsnorm_kernel, T, threads, sizeof(float) * d.L, s, o, slot, topk_w, gamma, d.K, d.L,
+                    d.rms_eps, n);
 }
 
 // =====================================================================

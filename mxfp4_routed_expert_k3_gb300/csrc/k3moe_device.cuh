@@ -29,6 +29,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 namespace k3 {
 
 constexpr int kTileRows = 128;
@@ -163,6 +165,38 @@ __device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
 }
 __device__ __forceinline__ float2 unpack_f32x2(unsigned long long v) {
   return make_float2(__uint_as_float((uint32_t)v), __uint_as_float((uint32_t)(v >> 32)));
+}
+
+// ------------------------------------------------------------------ programmatic dependent launch
+// The kernels of a forward after the first are launched with programmatic
+// stream serialization, so a kernel's launch and its CTAs' start overlap the
+// tail of its predecessor.  pdl_trigger() lets the next kernel launch;
+// pdl_wait() blocks until the preceding kernel has completed and its memory
+// is visible.  Every CTA of such a kernel calls pdl_wait() before its first
+// access to a buffer that another kernel writes or reads, before any early
+// exit (so that a kernel never completes ahead of its predecessor, which
+// makes the wait cover every earlier kernel) and before allocating TMEM (an
+// early-launched CTA holding columns while it waits could starve a CTA of
+// the kernel it waits for).  Only static data (weights) may be touched
+// before it.  Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch with programmatic stream serialization (see pdl_wait above).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace k3

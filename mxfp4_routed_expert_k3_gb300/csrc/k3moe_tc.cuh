@@ -146,6 +146,7 @@ __device__ __forceinline__ float situ_fast(float g, float u, float beta, float b
   return gate * beta_lin * tu;
 }
 
+
 // ------------------------------------------------------------------ host side
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,

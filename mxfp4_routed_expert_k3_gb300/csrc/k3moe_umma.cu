@@ -299,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
 // (k even in the low half) per 32-bit column, 8 columns per K = 16.
 // =====================================================================
 constexpr int kSNB = 32;  // max token rows per streaming tile
+constexpr int kMinTileRows = 16;  // the shortest tile height any tile list uses
 // producer warp, MMA warp, two decode warpgroups (one per scale group of a K step)
 constexpr int kSThreads = 320;
 constexpr int kDThreads = 192;
@@ -556,6 +557,8 @@ __global__ void __launch_bounds__(kDThreads, 1) umma_dense_stream_kernel(const _
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = p.MT * p.nkc;
+  pdl_trigger();
+  pdl_wait();
   if ((int)blockIdx.x >= n_items) return;
   if (threadIdx.x == 0) {
     for (int i = 0; i < NB; ++i) mbar_init(smem_u32(bars + i), i >= 2 * C::kStages + 2 ? 128u : 1u);
@@ -819,7 +822,9 @@ struct WsLayout {
 };
 WsLayout ws_layout(const Dims& d, int max_tokens) {
   auto up = [](size_t v) { return (v + 255) / 256 * 256; };
-  const size_t max_tiles = (size_t)max_tokens * d.K / kSNB + d.E + 1;
+  // every tile list holds tiles of at least kMinTileRows rows (one expert
+  // each): at most E + T*K / kMinTileRows of them
+  const size_t max_tiles = (size_t)max_tokens * d.K / kMinTileRows + d.E + 1;
   WsLayout l;
   l.tiles_off = 0;
   l.count_off = up(max_tiles * sizeof(int4));
@@ -964,7 +969,7 @@ cudaError_t umma_stream_prepare(const UmmaPlan& p, const Work& w, int T, const D
 cudaError_t umma_stream_tiles(const UmmaPlan& p, const Work& w, int T, const Dims& d, int bn_max, int* slot_tile,
                               cudaStream_t s) {
   if (T * d.K <= 0) return cudaSuccess;
-  if (bn_max < kSNB || bn_max > 255) return cudaErrorInvalidValue;  // the tile list holds E + T*K/kSNB tiles
+  if (bn_max < kMinTileRows || bn_max > 255) return cudaErrorInvalidValue;  // list capacity, slot map row field
   UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
   build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, bn_max, ws.tiles, ws.count, slot_tile);
   return cudaGetLastError();
@@ -1067,8 +1072,7 @@ cudaError_t umma_dense_small(const UmmaPlan& p, const uint16_t* W, int M, int K,
   q.status = p.status;
   q.limit_ns = p.limit_ns;
   const int items = q.MT * q.nkc;
-  umma_dense_stream_kernel<<<std::min(items, 2 * p.num_sms), kDThreads, DCfg::kSmem, s>>>(ma, mb, q);
-  return cudaGetLastError();
+  return launch_pdl(umma_dense_stream_kernel, std::min(items, 2 * p.num_sms), kDThreads, DCfg::kSmem, s, ma, mb, q);
 }
 
 }  // namespace k3
