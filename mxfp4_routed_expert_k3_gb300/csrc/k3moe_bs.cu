@@ -110,13 +110,23 @@ __device__ __forceinline__ uint32_t split_e4m3(float x, uint32_t s0, uint32_t s1
   return q0 | (to_e4m3(r) << 8);
 }
 
+// Byte of operand row R's scales (group g added by the caller) among the
+// activation atoms of one chunk: rows 0..127 in the first 512-byte atom,
+// 128..255 in the second, each at (R%32)*16 + ((R%128)/32)*4 -- row R is
+// read from TMEM lane R%32 of column R/32 once the atoms sit in consecutive
+// 4-column groups.
+__device__ __forceinline__ int act_atom_byte(int R) { return (R >> 7) * kAtom + (R & 31) * 16 + ((R & 127) >> 5) * 4; }
+// Term t of tile row n: stacked tiles (`stack` rows, both terms one operand
+// of 2*stack rows) use operand row t*stack + n; otherwise term t has its own
+// atom and the operand row is n.
+__device__ __forceinline__ int act_scale_byte(int t, int n, int stack) {
+  return stack ? act_atom_byte(t * stack + n) : t * kAtom + act_atom_byte(n);
+}
+
 // Slot-ordered rows: dst row s = src row (perm ? perm[s] / K : s), written
 // as terms q[C/128][t][rows_max][128]; the scales go to the tile atoms
-// sf[tile][C/128][t][512] at byte (n%32)*16 + (n/32)*4 + g for row n of the
-// tile (slot_tile[s] = tile << 8 | n), the order in which tcgen05.cp and
-// the MMA read per-row scales (row n in lane n%32 of column n/32).  With
-// stack > 0 (tiles of `stack` rows whose two terms form one MMA operand)
-// term 1 of row n is row stack + n of the term-0 atom.  A half
+// sf[tile][C/128][2][512] at act_scale_byte(t, n, stack) + g for row n of
+// the tile (slot_tile[s] = tile << 8 | n).  A half
 // warp covers 128 columns per chunk (8 per lane, 4 lanes per scale group)
 // and four chunks of one slot per pass, their loads issued together; the
 // loop runs per warp so that both halves always meet at the shuffles.
@@ -188,24 +198,16 @@ __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, const int* _
       *reinterpret_cast<uint2*>(q + r0 * kQK + hl * 8) = make_uint2(a0, b0);
       *reinterpret_cast<uint2*>(q + (r0 + rows_max) * kQK + hl * 8) = make_uint2(a1, b1);
       if (hl == 0) {
-        const int n = tn & 0xFF, n1 = stack ? stack + n : n;
+        const int n = tn & 0xFF;
         uint8_t* atom = sf + (((size_t)(tn >> 8) * KC + kc) * 2) * kAtom;
-        *reinterpret_cast<uint32_t*>(atom + (n & 31) * 16 + (n >> 5) * 4) = w0;
-        *reinterpret_cast<uint32_t*>(atom + (stack ? 0 : kAtom) + (n1 & 31) * 16 + (n1 >> 5) * 4) = w1;
+        *reinterpret_cast<uint32_t*>(atom + act_scale_byte(0, n, stack)) = w0;
+        *reinterpret_cast<uint32_t*>(atom + act_scale_byte(1, n, stack)) = w1;
       }
     }
   }
 }
 
 // ------------------------------------------------------------------ tcgen05 block-scaled pieces
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
-                                            int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
 // Shared-memory descriptor of a 32-row x 16-byte scale block (no swizzle,
 // 8-row core matrices 128 bytes apart).
 __device__ __forceinline__ uint64_t sf_desc(uint32_t saddr) {
@@ -257,14 +259,18 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
 template <int MODE, int NQ>
 struct BsCfg {
   static constexpr bool kBig = NQ > 32;
-  // Decode tiles put both activation terms in one MMA: B rows [term 0 of the
-  // NQ tokens; term 1 of the same tokens], N = 2 * NQ, and the epilogue adds
-  // accumulator columns j and NQ + j.  An MMA of N <= 32 costs about as much
-  // tensor-pipe time as one of N = 16, so this halves the pipe time per
-  // weight byte, which bounds the decode stream otherwise.
-  static constexpr bool kStack = !kBig;
-  static constexpr int kCtas = 2;                                           // CTAs per SM
-  static constexpr int kEpiWarps = 4;                                       // epilogue warps
+  // Both activation terms go into one MMA: B rows [term 0 of the NQ tokens;
+  // term 1 of the same tokens], N = 2 * NQ, and the epilogue adds
+  // accumulator columns j and NQ + j.  A block-scaled MMA instruction takes
+  // about the tensor-pipe time of an N = 256 one whatever its N, so this
+  // halves the pipe time, which bounds both the decode stream and prefill.
+  static constexpr bool kStack = true;
+  // Prefill gate/up: its two stacked accumulators (2 x 160 columns) need
+  // all of an SM's tensor memory, so one CTA per SM with a deeper ring and
+  // two epilogue warpgroups; the other kernels run two CTAs per SM.
+  static constexpr bool kWide = kBig && MODE == BS_GATEUP;
+  static constexpr int kCtas = kWide ? 1 : 2;                               // CTAs per SM
+  static constexpr int kEpiWarps = kWide ? 8 : 4;                           // epilogue warps
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int kNumA = (MODE == BS_GATEUP) ? 2 : 1;                 // accumulators (matrices)
   static constexpr int kNK = (MODE == BS_GATEUP || kBig) ? 1 : 2;           // 128-column chunks per stage
@@ -275,21 +281,20 @@ struct BsCfg {
   static constexpr int kOffSfa = kOffB + 2 * kNK * kB;
   static constexpr int kOffSfb = kOffSfa + kNA * kAtom;
   static constexpr int kStageBytes = (kOffSfb + 2 * kNK * kAtom + 1023) / 1024 * 1024;
-  static constexpr int kStages = 2;
-  static constexpr int kDBuf = (MODE == BS_GATEUP && kBig) ? 1 : 2;        // accumulator buffers
+  static constexpr int kStages = kWide ? 4 : 2;
+  static constexpr int kDBuf = kBig ? 1 : 2;                                // accumulator buffers
   static constexpr int kAccW = kStack ? 2 * NQ : (NQ + 15) / 16 * 16;     // accumulator columns (MMA N)
-  static constexpr int kAccStride = kBig ? 128 : 32;                        // TMEM columns between matrices
+  static constexpr int kAccStride = kWide ? kAccW : kBig ? 128 : 32;       // TMEM columns between matrices
   static constexpr int kBufStride = kNumA * kAccStride;                     // TMEM columns between buffers
   static constexpr int kSfBase = (kDBuf - 1) * kBufStride + (kNumA - 1) * kAccStride + kAccW;
   // weight atoms, then the activation atoms: one per chunk holding both
   // terms' rows (stacked), else one per chunk and term
-  static constexpr int kSfbAtoms = kStack ? 1 : 2;
+  static constexpr int kSfbAtoms = kStack ? (2 * NQ + 127) / 128 : 2;
   static constexpr int kSfCols = 4 * kNA + 4 * kSfbAtoms * kNK;
-  static constexpr int kTmemCols = 256;
+  static constexpr int kTmemCols = kWide ? 512 : 256;
   static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
   static_assert(kSfBase % 4 == 0 && kSfBase + kStages * kSfCols <= kTmemCols, "TMEM budget");
-  static_assert(kAccW <= kAccStride && kAccW % 16 == 0, "accumulator width");
-  static_assert(!kStack || 2 * NQ <= 32, "stacked rows share one 32-lane scale column");
+  static_assert((kNumA == 1 || kAccW <= kAccStride) && kAccW % 16 == 0 && kAccW <= 256, "accumulator width");
   static_assert(kCtas * kTmemCols <= 512, "TMEM per SM");
   static_assert(kB % 1024 == 0, "term blocks must keep the 1024-byte swizzle alignment");
   static_assert(kCtas * (kSmem + 1024) <= 233472, "shared memory per SM");
@@ -493,30 +498,99 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
       const int mt = item - ti * p.MT;
       const int m = mt * kQM + r;
       const uint32_t dbase = lane_base + buf * C::kBufStride;
-      // token columns per group of the accumulator: 32, or NQ when the two
-      // terms' partial sums sit in columns j and NQ + j
-      constexpr int JW = C::kStack ? NQ : 32;
+      // Token columns per group: 32, or NQ when both terms' columns of the
+      // NQ tokens fit one 32-column load.  Stacked, token j's two partial
+      // sums sit in columns j and NQ + j and are added here.
+      constexpr bool kPair = C::kStack && 2 * NQ <= 32;
+      constexpr int JW = kPair ? NQ : 32;
+      auto load_acc = [&](uint32_t base, int j0, float* v) {
+        if (kPair) {
+          tmem_ld32(base, v);
+#pragma unroll
+          for (int j = 0; j < JW; ++j) v[j] += v[j + JW];
+        } else if (C::kStack) {
+          float w2[32];
+          tmem_ld32(base + j0, v);
+          tmem_ld32(base + NQ + j0, w2);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] += w2[j];
+        } else {
+          tmem_ld32(base + j0, v);
+        }
+      };
       if (MODE == BS_GATEUP) {
-        // h as bf16 and as the two e4m3 terms (and scale atoms) of the down GEMM's B operand
+        // h as bf16 and as the two e4m3 terms (and scale atoms) of the down
+        // GEMM's B operand, laid out for the down kernel's tiles
+        constexpr int kHStack = BsCfg<BS_DOWN, NQ>::kStack ? NQ : 0;
         const int KCo = p.ld_out / kQK;
         const size_t rb0 = (size_t)((m >> 7) * 2) * p.rows_max, rb1 = rb0 + p.rows_max;  // [KC][2][rows_max]
         const int grp = (m >> 5) & 3;
         uint8_t* atoms = p.hsf + (((size_t)ti * KCo + (m >> 7)) * 2) * kAtom + grp;
+        if constexpr (C::kWide) {
+          // Each warpgroup takes NQ / kWG consecutive tokens: all their
+          // gate and up sums go to registers and the accumulators back to
+          // the MMA at once, so the epilogue math overlaps the next item.
+          constexpr int TPW = NQ / kWG;
+          static_assert(TPW % 8 == 0 && NQ % kWG == 0, "token split");
+          const int t_lo = wg * TPW;
+          float gs[TPW], us[TPW];
+          auto load_sum = [&](uint32_t col, float* v) {  // columns col.. (term 0) plus NQ + col.. (term 1)
+            float t[32];
+#pragma unroll
+            for (int c = 0; c < TPW; c += 32) {
+              if (c + 32 <= TPW) {
+                tmem_ld32(col + c, v + c);
+                tmem_ld32(col + NQ + c, t);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[c + i] += t[i];
+              } else {
+#pragma unroll
+                for (int c8 = c; c8 < TPW; c8 += 8) {
+                  tmem_ld8(col + c8, v + c8);
+                  tmem_ld8(col + NQ + c8, t);
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) v[c8 + i] += t[i];
+                }
+              }
+            }
+          };
+          load_sum(dbase + t_lo, gs);
+          load_sum(dbase + C::kAccStride + t_lo, us);
+          tc_fence_before();
+          mbar_arrive(dempty(buf));
+          uint32_t my_sc[(TPW + 31) / 32] = {};  // lane l keeps the scales of tokens t_lo + 32 i + l
+#pragma unroll
+          for (int j = 0; j < TPW; ++j) {
+            const int jj = t_lo + j;
+            if (jj < tile.z) {
+              const size_t row = (size_t)(tile.y + jj);
+              const uint16_t hb = f32_to_bf16(situ_fast(gs[j], us[j], p.beta, p.beta_lin));
+              p.h[row * p.ld_out + m] = hb;
+              const uint32_t emax = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(hb >> 7) & 0xFFu);
+              const uint32_t s0 = term0_scale(emax), s1 = term1_scale(s0);
+              const uint32_t q = split_e4m3(bf16_to_f32(hb), s0, s1);
+              p.hq[(rb0 + row) * kQK + (m & 127)] = (uint8_t)q;
+              p.hq[(rb1 + row) * kQK + (m & 127)] = (uint8_t)(q >> 8);
+              if (lane == (j & 31)) my_sc[j >> 5] = s0 | (s1 << 8);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < (TPW + 31) / 32; ++i) {
+            const int jl = 32 * i + lane, jj = t_lo + jl;
+            if (jl < TPW && jj < tile.z) {
+              atoms[act_scale_byte(0, jj, kHStack)] = (uint8_t)my_sc[i];
+              atoms[act_scale_byte(1, jj, kHStack)] = (uint8_t)(my_sc[i] >> 8);
+            }
+          }
+        } else
 #pragma unroll 1
         for (int j0 = JW * wg; j0 < NQ; j0 += JW * kWG) {
           float acc[32], up[32];
-          tmem_ld32(dbase + (C::kStack ? 0 : j0), acc);
-          tmem_ld32(dbase + C::kAccStride + (C::kStack ? 0 : j0), up);
+          load_acc(dbase, j0, acc);
+          load_acc(dbase + C::kAccStride, j0, up);
           if (j0 + JW * kWG >= NQ) {
             tc_fence_before();
             mbar_arrive(dempty(buf));
-          }
-          if (C::kStack) {
-#pragma unroll
-            for (int j = 0; j < JW; ++j) {
-              acc[j] += acc[j + JW];
-              up[j] += up[j + JW];
-            }
           }
           uint32_t my_sc = 0;  // lane l keeps the scales of token j0 + l
 #pragma unroll
@@ -534,28 +608,26 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
               if (lane == j) my_sc = s0 | (s1 << 8);
             }
           }
-          // one store per term for the group's tokens: token row jj at byte
-          // (jj%32)*16 + (jj/32)*4 (+ group) of the term's atom; stacked, term
-          // 1 is row NQ + jj of the first atom
+          // lane l stores the two scale bytes of token j0 + l (one byte of
+          // the group's word per warp)
           const int jj = j0 + lane;
           if (lane < JW && jj < tile.z) {
-            const int r1 = C::kStack ? NQ + jj : jj;
-            atoms[(jj & 31) * 16 + (jj >> 5) * 4] = (uint8_t)my_sc;
-            atoms[(C::kStack ? 0 : kAtom) + (r1 & 31) * 16 + (r1 >> 5) * 4] = (uint8_t)(my_sc >> 8);
+            atoms[act_scale_byte(0, jj, kHStack)] = (uint8_t)my_sc;
+            atoms[act_scale_byte(1, jj, kHStack)] = (uint8_t)(my_sc >> 8);
           }
         }
       } else {
 #pragma unroll 1
         for (int j0 = JW * wg; j0 < NQ; j0 += JW * kWG) {
           float acc[32];
-          tmem_ld32(dbase + (C::kStack ? 0 : j0), acc);
+          load_acc(dbase, j0, acc);
           if (j0 + JW * kWG >= NQ) {
             tc_fence_before();
             mbar_arrive(dempty(buf));
           }
 #pragma unroll
           for (int j = 0; j < JW; ++j)
-            if (j0 + j < tile.z) p.o[(size_t)(tile.y + j0 + j) * p.ld_out + m] = C::kStack ? acc[j] + acc[j + JW] : acc[j];
+            if (j0 + j < tile.z) p.o[(size_t)(tile.y + j0 + j) * p.ld_out + m] = acc[j];
         }
       }
     }
@@ -678,7 +750,8 @@ cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
   if (T > p.max_tokens || (tile_rows != kBsDecodeRows && tile_rows != kBsPrefillRows)) return cudaErrorInvalidValue;
-  const int stack = BsCfg<BS_GATEUP, kBsDecodeRows>::kStack && tile_rows == kBsDecodeRows ? kBsDecodeRows : 0;
+  const int stack = tile_rows == kBsDecodeRows ? (BsCfg<BS_GATEUP, kBsDecodeRows>::kStack ? kBsDecodeRows : 0)
+                                                : (BsCfg<BS_GATEUP, kBsPrefillRows>::kStack ? kBsPrefillRows : 0);
   const BsWs ws = bs_ws_view(p.ws, d, p.max_tokens);
   const long long halves = (long long)TK * ((d.L / kQK + kQuantChunks - 1) / kQuantChunks);
   const int blocks = (int)std::min<long long>((halves * 16 + 255) / 256, 8LL * p.num_sms);

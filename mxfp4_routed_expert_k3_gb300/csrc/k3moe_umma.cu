@@ -682,17 +682,27 @@ __global__ void __launch_bounds__(kDThreads, 1) umma_dense_stream_kernel(const _
       if (last) {
         __threadfence();
         if (m < p.M) {
-          for (int t0 = 0; t0 < p.T; t0 += 8) {  // eight tokens' loads in flight; chunks added in order
+          for (int t0 = 0; t0 < p.T; t0 += 8) {
+            // eight tokens x eight chunks of loads in flight (the sum is
+            // latency-bound otherwise); chunks added in order
             float v[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) v[i] = 0.f;
-            for (int c = 0; c < p.nkc; ++c) {
-              const float* src = p.part + ((size_t)c * p.T + t0) * p.M + m;
-              float x[8];
+            for (int c0 = 0; c0 < p.nkc; c0 += 8) {
+              float x[8][8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) x[i] = (t0 + i < p.T) ? __ldcg(src + (size_t)i * p.M) : 0.f;
+              for (int cc = 0; cc < 8; ++cc) {
+                const float* src = p.part + ((size_t)(c0 + cc) * p.T + t0) * p.M + m;
 #pragma unroll
-              for (int i = 0; i < 8; ++i) v[i] += x[i];
+                for (int i = 0; i < 8; ++i)
+                  x[cc][i] = (c0 + cc < p.nkc && t0 + i < p.T) ? __ldcg(src + (size_t)i * p.M) : 0.f;
+              }
+#pragma unroll
+              for (int cc = 0; cc < 8; ++cc)
+                if (c0 + cc < p.nkc) {
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) v[i] += x[cc][i];
+                }
             }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
