@@ -266,8 +266,10 @@ struct BsCfg {
   // halves the pipe time, which bounds both the decode stream and prefill.
   static constexpr bool kStack = true;
   // Prefill gate/up: its two stacked accumulators (2 x 160 columns) need
-  // all of an SM's tensor memory, so one CTA per SM with a deeper ring and
-  // two epilogue warpgroups; the other kernels run two CTAs per SM.
+  // more than a CTA's share of a two-CTA split, so one CTA per SM owns all
+  // 512 columns, with a deeper ring and two epilogue warpgroups.  The other
+  // kernels run two CTAs per SM (prefill down measured slower as one CTA
+  // per SM with two accumulator buffers).
   static constexpr bool kWide = kBig && MODE == BS_GATEUP;
   static constexpr int kCtas = kWide ? 1 : 2;                               // CTAs per SM
   static constexpr int kEpiWarps = kWide ? 8 : 4;                           // epilogue warps
@@ -518,6 +520,28 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
           tmem_ld32(base + j0, v);
         }
       };
+      // Prefill tiles: the sums of a warpgroup's NQ / kWG consecutive tokens
+      // (term 0 in columns c, term 1 in NQ + c) go to registers, then the
+      // accumulator is released before any store.
+      constexpr int TPW = NQ / kWG;
+      static_assert(!C::kBig || (TPW % 8 == 0 && NQ % kWG == 0), "token split");
+      auto load_sum = [&](uint32_t col, float* v) {
+        float t[8];
+#pragma unroll
+        for (int c = 0; c < TPW; c += 32) {
+          if (c + 32 <= TPW)
+            tmem_ld32(col + c, v + c);
+          else
+#pragma unroll
+            for (int c8 = c; c8 < TPW; c8 += 8) tmem_ld8(col + c8, v + c8);
+        }
+#pragma unroll
+        for (int c8 = 0; c8 < TPW; c8 += 8) {
+          tmem_ld8(col + NQ + c8, t);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[c8 + i] += t[i];
+        }
+      };
       if (MODE == BS_GATEUP) {
         // h as bf16 and as the two e4m3 terms (and scale atoms) of the down
         // GEMM's B operand, laid out for the down kernel's tiles
@@ -526,34 +550,13 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
         const size_t rb0 = (size_t)((m >> 7) * 2) * p.rows_max, rb1 = rb0 + p.rows_max;  // [KC][2][rows_max]
         const int grp = (m >> 5) & 3;
         uint8_t* atoms = p.hsf + (((size_t)ti * KCo + (m >> 7)) * 2) * kAtom + grp;
-        if constexpr (C::kWide) {
+        if constexpr (C::kBig) {
           // Each warpgroup takes NQ / kWG consecutive tokens: all their
           // gate and up sums go to registers and the accumulators back to
           // the MMA at once, so the epilogue math overlaps the next item.
           constexpr int TPW = NQ / kWG;
-          static_assert(TPW % 8 == 0 && NQ % kWG == 0, "token split");
           const int t_lo = wg * TPW;
           float gs[TPW], us[TPW];
-          auto load_sum = [&](uint32_t col, float* v) {  // columns col.. (term 0) plus NQ + col.. (term 1)
-            float t[32];
-#pragma unroll
-            for (int c = 0; c < TPW; c += 32) {
-              if (c + 32 <= TPW) {
-                tmem_ld32(col + c, v + c);
-                tmem_ld32(col + NQ + c, t);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[c + i] += t[i];
-              } else {
-#pragma unroll
-                for (int c8 = c; c8 < TPW; c8 += 8) {
-                  tmem_ld8(col + c8, v + c8);
-                  tmem_ld8(col + NQ + c8, t);
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) v[c8 + i] += t[i];
-                }
-              }
-            }
-          };
           load_sum(dbase + t_lo, gs);
           load_sum(dbase + C::kAccStride + t_lo, us);
           tc_fence_before();
@@ -616,6 +619,15 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
             atoms[act_scale_byte(1, jj, kHStack)] = (uint8_t)(my_sc >> 8);
           }
         }
+      } else if constexpr (C::kBig) {
+        const int t_lo = wg * TPW;
+        float os[TPW];
+        load_sum(dbase + t_lo, os);
+        tc_fence_before();
+        mbar_arrive(dempty(buf));
+#pragma unroll
+        for (int j = 0; j < TPW; ++j)
+          if (t_lo + j < tile.z) p.o[(size_t)(tile.y + t_lo + j) * p.ld_out + m] = os[j];
       } else {
 #pragma unroll 1
         for (int j0 = JW * wg; j0 < NQ; j0 += JW * kWG) {
