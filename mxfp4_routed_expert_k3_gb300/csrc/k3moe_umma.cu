@@ -48,15 +48,17 @@ enum Mode { DENSE = 0, GATEUP = 1, DOWN = 2 };
 template <int MODE>
 struct Cfg {
   static constexpr int kNumA = (MODE == GATEUP) ? 2 : 1;
-  static constexpr int kBN = (MODE == DENSE) ? 128 : kBNMax;    // token rows per tile
+  // Dense: 256 token rows per tile (an MMA instruction costs about the pipe
+  // time of an N = 256 one whatever its N), K split over two accumulators.
+  static constexpr int kBN = (MODE == DENSE) ? 256 : kBNMax;    // token rows per tile
   static constexpr int kABytes = kBM * kBK * 2;                 // 16 KB per A tile
   static constexpr int kBBytes = kBN * kBK * 2;
   static constexpr int kStageBytesRaw = (MODE == DENSE) ? 0 : kNumA * kTileBytes;
   static constexpr int kStaging = (kStageBytesRaw + 1023) / 1024 * 1024;
   static constexpr int kStageBytes = kNumA * kABytes + kBBytes + kStaging;
   static constexpr int kStages = (MODE == GATEUP) ? 3 : 4;
-  static constexpr int kAcc = (MODE == DENSE) ? 4 : (MODE == DOWN) ? 2 : 1;
-  static constexpr int kAccStride = (MODE == DENSE) ? 128 : 256;  // TMEM columns between accumulators
+  static constexpr int kAcc = (MODE == DENSE || MODE == DOWN) ? 2 : 1;
+  static constexpr int kAccStride = 256;  // TMEM columns between accumulators
   static constexpr int kTmemCols = 512;
   static constexpr int kSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
   static_assert(kNumA * kAcc * kAccStride <= kTmemCols || MODE == GATEUP, "TMEM budget");
