@@ -110,6 +110,44 @@ __device__ __forceinline__ uint32_t split_e4m3(float x, uint32_t s0, uint32_t s1
   return q0 | (to_e4m3(r) << 8);
 }
 
+// ------------------------------------------------------------------ e2m1 term split
+// Decode-size tiles carry each activation as kFp4Terms e2m1 terms with their
+// own UE8M0 scale per 32-column group: term t quantises what the earlier
+// terms left, x = sum_t q_t * 2^(S_t - 127).  The scale puts the group's
+// largest remaining magnitude at or below 6 (the largest e2m1 value); each
+// term leaves at most about a quarter of it, so six terms keep an activation
+// within about 2.5e-7 of its group's largest magnitude (four measured 1e-4:
+// enough for the layer's output, not for the per-step checks that hold h
+// and o to one bf16 ulp and 2e-5).  2^n for n in [-127, 127] (2^-127 is
+// subnormal).
+constexpr int kFp4Terms = 6;
+__device__ __forceinline__ float exp2_any(int n) {
+  return n >= -126 ? __uint_as_float((uint32_t)(n + 127) << 23) : __uint_as_float(0x00400000u);
+}
+// UE8M0 byte of the group whose largest magnitude has the float bits mb
+// (255 for Inf/NaN: the MMA then yields NaN).
+__device__ __forceinline__ uint32_t e2m1_scale_byte(uint32_t mb) {
+  const uint32_t eb = (mb >> 23) & 0xFFu;
+  if (eb == 0xFFu) return 255u;
+  const int S = (int)eb - 129 + ((mb & 0x7FFFFFu) > 0x400000u ? 1 : 0);  // m 2^e <= 6 * 2^S
+  return (uint32_t)(max(S, -127) + 127);
+}
+// Two e2m1 codes in one byte: lo in bits 0..3, hi in bits 4..7 (round to
+// nearest even, saturating at 6).
+__device__ __forceinline__ uint32_t to_e2m1x2(float hi, float lo) {
+  uint32_t r;
+  asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// The two values of an e2m1x2 byte (lo nibble -> .x).
+__device__ __forceinline__ float2 from_e2m1x2(uint32_t b) {
+  uint32_t h2;
+  asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(h2) : "r"(b));
+  float lo, hi;
+  asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; cvt.f32.f16 %0, l; cvt.f32.f16 %1, h; }" : "=f"(lo), "=f"(hi) : "r"(h2));
+  return make_float2(lo, hi);
+}
+
 // Byte of operand row R's scales (group g added by the caller) among the
 // activation atoms of one chunk: rows 0..127 in the first 512-byte atom,
 // 128..255 in the second, each at (R%32)*16 + ((R%128)/32)*4 -- row R is
@@ -207,6 +245,96 @@ __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, const int* _
   }
 }
 
+// The same for decode-size tiles (`stack` rows): kFp4Terms e2m1 terms
+// q[C/128][kFp4Terms][rows_max][64] (two codes per byte, low nibble first)
+// and their scales at act_scale_byte(t, n, stack) + g of the tile's first
+// atom.
+__global__ void quant_rows_fp4_kernel(const uint16_t* __restrict__ src, const int* __restrict__ perm, int K, int rows,
+                                      int C, int rows_max, const int* __restrict__ slot_tile, int stack,
+                                      uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+  pdl_trigger();
+  pdl_wait();
+  const int hl = threadIdx.x & 15, half = (threadIdx.x >> 4) & 1;
+  const int KC = C / kQK;
+  const int KG = (KC + kQuantChunks - 1) / kQuantChunks;  // chunk groups per row
+  const long long nwork = (long long)rows * KG;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long wi = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; 2 * wi < nwork; wi += nwarps) {
+    const long long i = 2 * wi + half;
+    const bool valid = i < nwork;
+    const int s = valid ? (int)(i / KG) : 0, kg = valid ? (int)(i - (long long)s * KG) : 0;
+    uint4 v[kQuantChunks];
+    int tn = 0;
+    if (valid) {
+      const int t = perm ? perm[s] / K : s;
+      tn = slot_tile[s];
+#pragma unroll
+      for (int c = 0; c < kQuantChunks; ++c) {
+        const int kc = kg * kQuantChunks + c;
+        v[c] = kc < KC ? *reinterpret_cast<const uint4*>(src + (size_t)t * C + kc * kQK + hl * 8)
+                       : make_uint4(0u, 0u, 0u, 0u);
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < kQuantChunks; ++c) v[c] = make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int c = 0; c < kQuantChunks; ++c) {
+      const int kc = kg * kQuantChunks + c;
+      const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+      float x[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        x[2 * j] = __uint_as_float(w[j] << 16);
+        x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+      }
+      uint32_t words[kFp4Terms], scw[kFp4Terms];
+      const uint32_t base_lane = threadIdx.x & 16;
+#pragma unroll
+      for (int t = 0; t < kFp4Terms; ++t) {
+        uint32_t mb = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mb = max(mb, __float_as_uint(fabsf(x[j])));
+        mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
+        mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
+        const uint32_t sb = e2m1_scale_byte(mb);
+        uint32_t word = 0;
+        if (sb == 255u) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) x[j] = 0.f;
+        } else {
+          const float inv = exp2_any(127 - (int)sb), scl = exp2_any((int)sb - 127);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t b = to_e2m1x2(x[2 * j + 1] * inv, x[2 * j] * inv);
+            const float2 d = from_e2m1x2(b);
+            x[2 * j] = fmaf(-d.x, scl, x[2 * j]);
+            x[2 * j + 1] = fmaf(-d.y, scl, x[2 * j + 1]);
+            word |= b << (8 * j);
+          }
+        }
+        words[t] = word;
+        // the four groups' scale bytes of this (slot, chunk) and term: one word at lane 0 of the half warp
+        uint32_t ws = 0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) ws |= __shfl_sync(0xFFFFFFFFu, sb, base_lane + 4 * g) << (8 * g);
+        scw[t] = ws;
+      }
+      if (!valid || kc >= KC) continue;
+#pragma unroll
+      for (int t = 0; t < kFp4Terms; ++t)
+        *reinterpret_cast<uint32_t*>(q + (((size_t)kc * kFp4Terms + t) * rows_max + s) * 64 + hl * 4) = words[t];
+      if (hl == 0) {
+        const int n = tn & 0xFF;
+        uint8_t* atom = sf + (((size_t)(tn >> 8) * KC + kc) * 2) * kAtom;
+#pragma unroll
+        for (int t = 0; t < kFp4Terms; ++t)
+          *reinterpret_cast<uint32_t*>(atom + act_atom_byte(t * stack + n)) = scw[t];
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ tcgen05 block-scaled pieces
 // Shared-memory descriptor of a 32-row x 16-byte scale block (no swizzle,
 // 8-row core matrices 128 bytes apart).
@@ -230,6 +358,21 @@ __device__ __forceinline__ void umma_bs(uint32_t d, uint64_t a, uint64_t b, uint
       "{ .reg .pred p; setp.ne.b32 p, %6, 0; "
       "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p; }" ::"r"(
           d),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+      : "memory");
+}
+
+// kind::mxf4: A and B e2m1 (type code 1), UE8M0 scales per 32 columns
+// (two per row and MMA, K = 64), M = 128, N = n.
+__device__ __forceinline__ uint32_t fp4_idesc(uint32_t sfa_id, uint32_t sfb_id, uint32_t n) {
+  return (sfb_id << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | (1u << 23) | ((uint32_t)(kQM >> 4) << 24) |
+         (sfa_id << 29);
+}
+__device__ __forceinline__ void umma_fp4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                         uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %6, 0; "
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p; }" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
       : "memory");
 }
@@ -271,34 +414,47 @@ struct BsCfg {
   // kernels run two CTAs per SM (prefill down measured slower as one CTA
   // per SM with two accumulator buffers).
   static constexpr bool kWide = kBig && MODE == BS_GATEUP;
+  // Decode tiles use tcgen05.mma kind::mxf4: the e2m1 weights sit in shared
+  // memory as stored (64-byte rows, half the room of the 16-byte-slot
+  // layout kind::mxf8f6f4 reads), so a CTA keeps four stages in flight; the
+  // activations are kFp4Terms e2m1 terms (N = 6 * 16 = 96).  Prefill tiles
+  // keep kind::mxf8f6f4 with two e4m3 terms (N = 160: more terms would not
+  // fit an MMA of N <= 256).
+  static constexpr bool kFp4 = !kBig;
+  static constexpr int kTerms = kFp4 ? kFp4Terms : 2;
+  static constexpr int kRowB = kFp4 ? 64 : 128;  // shared-memory bytes per operand row of a 128-column chunk
   static constexpr int kCtas = kWide ? 1 : 2;                               // CTAs per SM
   static constexpr int kEpiWarps = kWide ? 8 : 4;                           // epilogue warps
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int kNumA = (MODE == BS_GATEUP) ? 2 : 1;                 // accumulators (matrices)
   static constexpr int kNK = (MODE == BS_GATEUP || kBig) ? 1 : 2;           // 128-column chunks per stage
   static constexpr int kNA = (MODE == BS_GATEUP) ? 2 : kNK;                 // e2m1 tiles per stage
-  static constexpr int kA = kQM * kQK;  // one e2m1 tile in 16-byte slots (8 data + 8 padding bytes per 16 codes)
-  static constexpr int kB = NQ * kQK;   // one e4m3 term of one chunk
+  // one e2m1 tile: dense, or in 16-byte slots (8 data + 8 padding bytes per 16 codes)
+  static constexpr int kA = kQM * kRowB;
+  static constexpr int kATx = kQM * kQK / 2;  // bytes a tile's copy brings (the packed codes)
+  static constexpr int kB = NQ * kRowB;       // one activation term of one chunk
   static constexpr int kOffB = kNA * kA;
-  static constexpr int kOffSfa = kOffB + 2 * kNK * kB;
+  static constexpr int kOffSfa = kOffB + kTerms * kNK * kB;
   static constexpr int kOffSfb = kOffSfa + kNA * kAtom;
   static constexpr int kStageBytes = (kOffSfb + 2 * kNK * kAtom + 1023) / 1024 * 1024;
-  static constexpr int kStages = kWide ? 4 : 2;
-  static constexpr int kDBuf = kBig ? 1 : 2;                                // accumulator buffers
-  static constexpr int kAccW = kStack ? 2 * NQ : (NQ + 15) / 16 * 16;     // accumulator columns (MMA N)
-  static constexpr int kAccStride = kWide ? kAccW : kBig ? 128 : 32;       // TMEM columns between matrices
+  static constexpr int kStages = kWide ? 4 : !kFp4 ? 2 : MODE == BS_GATEUP ? 4 : 3;
+  // accumulator buffers: one where the stacked accumulators fill the CTA's
+  // columns (the epilogue then releases the buffer as soon as it has read it)
+  static constexpr int kDBuf = (kBig || MODE == BS_GATEUP) ? 1 : 2;
+  static constexpr int kAccW = kStack ? kTerms * NQ : (NQ + 15) / 16 * 16;  // accumulator columns (MMA N)
+  static constexpr int kAccStride = (kWide || kFp4) ? kAccW : 128;          // TMEM columns between matrices
   static constexpr int kBufStride = kNumA * kAccStride;                     // TMEM columns between buffers
   static constexpr int kSfBase = (kDBuf - 1) * kBufStride + (kNumA - 1) * kAccStride + kAccW;
   // weight atoms, then the activation atoms: one per chunk holding both
   // terms' rows (stacked), else one per chunk and term
-  static constexpr int kSfbAtoms = kStack ? (2 * NQ + 127) / 128 : 2;
+  static constexpr int kSfbAtoms = kStack ? (kTerms * NQ + 127) / 128 : 2;
   static constexpr int kSfCols = 4 * kNA + 4 * kSfbAtoms * kNK;
   static constexpr int kTmemCols = kWide ? 512 : 256;
   static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
   static_assert(kSfBase % 4 == 0 && kSfBase + kStages * kSfCols <= kTmemCols, "TMEM budget");
   static_assert((kNumA == 1 || kAccW <= kAccStride) && kAccW % 16 == 0 && kAccW <= 256, "accumulator width");
   static_assert(kCtas * kTmemCols <= 512, "TMEM per SM");
-  static_assert(kB % 1024 == 0, "term blocks must keep the 1024-byte swizzle alignment");
+  static_assert(kB % (8 * kRowB) == 0 && kA % 1024 == 0, "operand blocks must keep their swizzle atoms aligned");
   static_assert(kCtas * (kSmem + 1024) <= 233472, "shared memory per SM");
 };
 
@@ -383,7 +539,7 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
           const uint32_t st = smem_u32(stage(s));
           // the e2m1 copies count their packed bytes; boxes past the end of a
           // tensor are zero-filled and counted in full
-          mbar_expect_tx(full(s), (uint32_t)(C::kNA * (C::kA / 2) + 2 * C::kNK * C::kB + n_sfa * kAtom +
+          mbar_expect_tx(full(s), (uint32_t)(C::kNA * C::kATx + C::kTerms * C::kNK * C::kB + n_sfa * kAtom +
                                              2 * nk * kAtom));
           tma_load_3d(st, &map_a, full(s), 0, 0, (int)first);
           tma_load_4d(st + C::kOffB, &map_b, full(s), 0, tile.y, 0, kc0);
@@ -409,8 +565,8 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
     // ends below 256 KB, so the 14-bit field never carries).
     if (lane == 0) {
       const uint32_t st0 = smem_u32(stage(0));
-      const uint64_t a_base = umma_desc_sw128(st0);
-      const uint64_t b_base = umma_desc_sw128(st0 + C::kOffB);
+      const uint64_t a_base = C::kFp4 ? umma_desc_sw64(st0) : umma_desc_sw128(st0);
+      const uint64_t b_base = C::kFp4 ? umma_desc_sw64(st0 + C::kOffB) : umma_desc_sw128(st0 + C::kOffB);
       const uint64_t sfa_base = sf_desc(st0 + C::kOffSfa);
       const uint64_t sfb_base = sf_desc(st0 + C::kOffSfb);
       int kg = 0, it = 0;
@@ -449,6 +605,23 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
               if (c < nk)
                 tc_cp_scales(sfc + 4 * C::kNA + 4 * (c * C::kSfbAtoms + t), sfb_base + so + ((c * 2 + t) * kAtom >> 4));
           const uint32_t first = ks ? 1u : 0u;
+          if constexpr (C::kFp4) {
+            // kind::mxf4: K = 64 per MMA (32 bytes of each 64-byte row), two
+            // scale bytes per row and MMA (scale ids 0 and 2)
+#pragma unroll
+            for (int c = 0; c < C::kNK; ++c) {
+              if (c >= nk) break;
+#pragma unroll
+              for (int kb = 0; kb < kQK / 64; ++kb)
+#pragma unroll
+                for (int a = 0; a < C::kNumA; ++a) {
+                  const int ablk = (MODE == BS_GATEUP) ? a : c;
+                  umma_fp4(d0 + a * C::kAccStride, a_d + ((ablk * C::kA + kb * 32) >> 4),
+                           b_d + ((c * C::kTerms * C::kB + kb * 32) >> 4), fp4_idesc(2 * kb, 2 * kb, n),
+                           sfc + 4 * ablk, sfc + 4 * C::kNA + 4 * c, (c | kb) ? 1u : first);
+                }
+            }
+          } else
 #pragma unroll
           for (int c = 0; c < C::kNK; ++c) {
             if (c >= nk) break;
@@ -500,16 +673,25 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
       const int mt = item - ti * p.MT;
       const int m = mt * kQM + r;
       const uint32_t dbase = lane_base + buf * C::kBufStride;
-      // Token columns per group: 32, or NQ when both terms' columns of the
-      // NQ tokens fit one 32-column load.  Stacked, token j's two partial
-      // sums sit in columns j and NQ + j and are added here.
-      constexpr bool kPair = C::kStack && 2 * NQ <= 32;
+      // Token columns per group: 32, or NQ for decode tiles, whose terms'
+      // columns (term t of token j in column t*NQ + j) fit one or two
+      // 32-column loads.  Stacked, token j's partial sums are added here.
+      constexpr bool kPair = C::kStack && !C::kBig;
       constexpr int JW = kPair ? NQ : 32;
+      static_assert(!kPair || (2 * NQ == 32 && C::kTerms % 2 == 0), "decode accumulator layout");
       auto load_acc = [&](uint32_t base, int j0, float* v) {
         if (kPair) {
+          // 32-column block b holds terms 2b and 2b + 1 of the NQ tokens
           tmem_ld32(base, v);
 #pragma unroll
           for (int j = 0; j < JW; ++j) v[j] += v[j + JW];
+#pragma unroll
+          for (int b = 1; b < C::kTerms / 2; ++b) {
+            float w2[32];
+            tmem_ld32(base + 32 * b, w2);
+#pragma unroll
+            for (int j = 0; j < JW; ++j) v[j] += w2[j] + w2[j + JW];
+          }
         } else if (C::kStack) {
           float w2[32];
           tmem_ld32(base + j0, v);
@@ -546,6 +728,8 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
         // h as bf16 and as the two e4m3 terms (and scale atoms) of the down
         // GEMM's B operand, laid out for the down kernel's tiles
         constexpr int kHStack = BsCfg<BS_DOWN, NQ>::kStack ? NQ : 0;
+        constexpr bool kHFp4 = BsCfg<BS_DOWN, NQ>::kFp4;
+        constexpr int kHTerms = BsCfg<BS_DOWN, NQ>::kTerms;
         const int KCo = p.ld_out / kQK;
         const size_t rb0 = (size_t)((m >> 7) * 2) * p.rows_max, rb1 = rb0 + p.rows_max;  // [KC][2][rows_max]
         const int grp = (m >> 5) & 3;
@@ -595,7 +779,7 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
             tc_fence_before();
             mbar_arrive(dempty(buf));
           }
-          uint32_t my_sc = 0;  // lane l keeps the scales of token j0 + l
+          unsigned long long my_sc = 0;  // lane l keeps the scales of token j0 + l (term t in byte t)
 #pragma unroll
           for (int j = 0; j < JW; ++j) {
             const int jj = j0 + j;
@@ -603,20 +787,48 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
               const size_t row = (size_t)(tile.y + jj);
               const uint16_t hb = f32_to_bf16(situ_fast(acc[j], up[j], p.beta, p.beta_lin));
               p.h[row * p.ld_out + m] = hb;
-              const uint32_t emax = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(hb >> 7) & 0xFFu);
-              const uint32_t s0 = term0_scale(emax), s1 = term1_scale(s0);
-              const uint32_t q = split_e4m3(bf16_to_f32(hb), s0, s1);
-              p.hq[(rb0 + row) * kQK + (m & 127)] = (uint8_t)q;
-              p.hq[(rb1 + row) * kQK + (m & 127)] = (uint8_t)(q >> 8);
-              if (lane == j) my_sc = s0 | (s1 << 8);
+              if constexpr (kHFp4) {
+                // kHTerms e2m1 terms, [KC][kHTerms][rows_max][64]: lane pairs share a byte
+                float rr = bf16_to_f32(hb);
+                uint32_t qn = 0;
+                unsigned long long sc = 0;
+#pragma unroll
+                for (int t = 0; t < kHTerms; ++t) {
+                  const uint32_t sb = e2m1_scale_byte(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(rr))));
+                  uint32_t qb = 0;
+                  if (sb != 255u) {
+                    qb = to_e2m1x2(0.f, rr * exp2_any(127 - (int)sb)) & 0xFu;
+                    rr = fmaf(-from_e2m1x2(qb).x, exp2_any((int)sb - 127), rr);
+                  } else {
+                    rr = 0.f;
+                  }
+                  qn |= qb << (4 * t);
+                  sc |= (unsigned long long)sb << (8 * t);
+                }
+                const uint32_t qo = __shfl_down_sync(0xFFFFFFFFu, qn, 1);
+                if (!(lane & 1)) {
+#pragma unroll
+                  for (int t = 0; t < kHTerms; ++t)
+                    p.hq[(((size_t)(m >> 7) * kHTerms + t) * p.rows_max + row) * 64 + ((m & 127) >> 1)] =
+                        (uint8_t)(((qn >> (4 * t)) & 0xFu) | (((qo >> (4 * t)) & 0xFu) << 4));
+                }
+                if (lane == j) my_sc = sc;
+              } else {
+                const uint32_t emax = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(hb >> 7) & 0xFFu);
+                const uint32_t s0 = term0_scale(emax), s1 = term1_scale(s0);
+                const uint32_t q = split_e4m3(bf16_to_f32(hb), s0, s1);
+                p.hq[(rb0 + row) * kQK + (m & 127)] = (uint8_t)q;
+                p.hq[(rb1 + row) * kQK + (m & 127)] = (uint8_t)(q >> 8);
+                if (lane == j) my_sc = s0 | (s1 << 8);
+              }
             }
           }
-          // lane l stores the two scale bytes of token j0 + l (one byte of
-          // the group's word per warp)
+          // lane l stores the scale bytes of token j0 + l (one byte of the
+          // group's word per warp and term)
           const int jj = j0 + lane;
           if (lane < JW && jj < tile.z) {
-            atoms[act_scale_byte(0, jj, kHStack)] = (uint8_t)my_sc;
-            atoms[act_scale_byte(1, jj, kHStack)] = (uint8_t)(my_sc >> 8);
+#pragma unroll
+            for (int t = 0; t < kHTerms; ++t) atoms[act_scale_byte(t, jj, kHStack)] = (uint8_t)(my_sc >> (8 * t));
           }
         }
       } else if constexpr (C::kBig) {
@@ -667,6 +879,23 @@ bool map_e2m1(CUtensorMap* map, const void* base, long long nbox, int depth) {
   const cuuint32_t box[3] = {(cuuint32_t)kQK, (cuuint32_t)kQM, (cuuint32_t)depth};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
+// The same tiles as bytes: each lands dense, 128 rows of 64 bytes with the
+// 64-byte swizzle (the layout kind::mxf4 reads).
+bool map_e2m1_dense(CUtensorMap* map, const void* base, long long nbox, int depth) {
+  const cuuint64_t dims[3] = {(cuuint64_t)kQK / 2, (cuuint64_t)kQM, (cuuint64_t)nbox};
+  const cuuint64_t strides[2] = {(cuuint64_t)kQK / 2, (cuuint64_t)kQM * kQK / 2};
+  const cuuint32_t box[3] = {(cuuint32_t)kQK / 2, (cuuint32_t)kQM, (cuuint32_t)depth};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+// e2m1 activation terms q[KC][kFp4Terms][rows_max][64]: box 64 x box_rows x
+// all terms x nk chunks, 64-byte swizzle; in shared memory
+// [chunk][term][row][64].
+bool map_terms_fp4(CUtensorMap* map, const void* base, int KC, int rows_max, int box_rows, int nk) {
+  const cuuint64_t dims[4] = {64, (cuuint64_t)rows_max, kFp4Terms, (cuuint64_t)KC};
+  const cuuint64_t strides[3] = {64, (cuuint64_t)rows_max * 64, (cuuint64_t)kFp4Terms * rows_max * 64};
+  const cuuint32_t box[4] = {64, (cuuint32_t)box_rows, kFp4Terms, (cuuint32_t)nk};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
+}
 // Activation terms q[KC][2][rows_max][128]: box 128 x box_rows x 2 terms x
 // nk chunks, 128-byte swizzle; in shared memory [chunk][term][row][128].
 bool map_terms(CUtensorMap* map, const void* base, int KC, int rows_max, int box_rows, int nk) {
@@ -678,18 +907,24 @@ bool map_terms(CUtensorMap* map, const void* base, int KC, int rows_max, int box
 
 struct BsWs {
   int rows_max;       // slots: max_tokens * K
+  int rows_fp4;       // slots of the decode-size layout: min(max_tokens, kBsDecodeMaxT) * K
   int max_tiles;      // bound on the tile list length
-  uint8_t *lq, *lsf;  // latent rows: terms [L/128][2][rows_max][128], atoms [max_tiles][L/128][2][512]
-  uint8_t *hq, *hsf;  // h rows:      terms [I/128][2][rows_max][128], atoms [max_tiles][I/128][2][512]
+  // latent rows: terms [L/128][2][rows_max][128] e4m3 (prefill tiles) or
+  // [L/128][kFp4Terms][rows_fp4][64] e2m1 (decode tiles); atoms
+  // [max_tiles][L/128][2][512]
+  uint8_t *lq, *lsf;
+  uint8_t *hq, *hsf;  // h rows: the same over I
   int* slot_tile;     // [rows_max]: tile << 8 | row within the tile
   size_t total;
 };
 BsWs bs_ws_view(void* base, const Dims& d, int max_tokens) {
   auto up = [](size_t v) { return (v + 255) / 256 * 256; };
   const size_t R = (size_t)max_tokens * d.K;
+  const size_t Rf = (size_t)std::min(max_tokens, kBsDecodeMaxT) * d.K;
   // tiles hold at least one slot and at most one expert: <= E + R / 16 whatever the tile height
   const size_t MT = (size_t)d.E + R / 16 + 1;
-  const size_t sizes[5] = {2 * R * d.L, MT * (d.L / kQK) * 2 * kAtom, 2 * R * d.I, MT * (d.I / kQK) * 2 * kAtom,
+  auto terms = [&](size_t C) { return std::max(2 * R * C, (size_t)kFp4Terms * Rf * C / 2); };
+  const size_t sizes[5] = {terms(d.L), MT * (d.L / kQK) * 2 * kAtom, terms(d.I), MT * (d.I / kQK) * 2 * kAtom,
                            R * sizeof(int)};
   uint8_t* b = static_cast<uint8_t*>(base);
   uint8_t* ptr[5];
@@ -698,7 +933,7 @@ BsWs bs_ws_view(void* base, const Dims& d, int max_tokens) {
     ptr[i] = b ? b + off : nullptr;
     off += up(sizes[i]);
   }
-  return BsWs{(int)R, (int)MT, ptr[0], ptr[1], ptr[2], ptr[3], reinterpret_cast<int*>(ptr[4]), off};
+  return BsWs{(int)R, (int)Rf, (int)MT, ptr[0], ptr[1], ptr[2], ptr[3], reinterpret_cast<int*>(ptr[4]), off};
 }
 
 template <int MODE, int NQ>
@@ -709,7 +944,9 @@ cudaError_t launch_bs(const BsPlan& p, const uint8_t* wq, const uint8_t* sfa, in
   CUtensorMap ma, mb;
   const int KC = cols / kQK, MT = rows / kQM;
   const long long nbox = (long long)n_exp * MT * KC * C::kNumA;
-  if (!map_e2m1(&ma, wq, nbox, C::kNA) || !map_terms(&mb, q, KC, rows_max, NQ, C::kNK)) return cudaErrorInvalidValue;
+  const bool mapped = C::kFp4 ? map_e2m1_dense(&ma, wq, nbox, C::kNA) && map_terms_fp4(&mb, q, KC, rows_max, NQ, C::kNK)
+                              : map_e2m1(&ma, wq, nbox, C::kNA) && map_terms(&mb, q, KC, rows_max, NQ, C::kNK);
+  if (!mapped) return cudaErrorInvalidValue;
   prm.sfa = sfa;
   prm.sfb = sfb;
   prm.MT = MT;
@@ -767,8 +1004,11 @@ cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims
   const BsWs ws = bs_ws_view(p.ws, d, p.max_tokens);
   const long long halves = (long long)TK * ((d.L / kQK + kQuantChunks - 1) / kQuantChunks);
   const int blocks = (int)std::min<long long>((halves * 16 + 255) / 256, 8LL * p.num_sms);
-  return launch_pdl(quant_rows_kernel, blocks, 256, 0, s, w.lat, w.perm, d.K, TK, d.L, ws.rows_max, ws.slot_tile,
-                    stack, ws.lq, ws.lsf);
+  auto kernel = (tile_rows == kBsDecodeRows && BsCfg<BS_GATEUP, kBsDecodeRows>::kFp4) ? quant_rows_fp4_kernel
+                                                                                     : quant_rows_kernel;
+  const int rows = tile_rows == kBsDecodeRows ? ws.rows_fp4 : ws.rows_max;
+  return launch_pdl(kernel, blocks, 256, 0, s, w.lat, w.perm, d.K, TK, d.L, rows, ws.slot_tile, stack, ws.lq,
+                    ws.lsf);
 }
 
 cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* tiles, const int* tile_count,
@@ -785,7 +1025,7 @@ cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* t
   prm.beta = d.beta;
   prm.beta_lin = d.beta_lin;
   if (tile_rows == kBsDecodeRows)
-    return launch_bs<BS_GATEUP, kBsDecodeRows>(p, bw.gu_q, bw.gu_sf, d.E, d.I, d.L, ws.lq, ws.lsf, ws.rows_max,
+    return launch_bs<BS_GATEUP, kBsDecodeRows>(p, bw.gu_q, bw.gu_sf, d.E, d.I, d.L, ws.lq, ws.lsf, ws.rows_fp4,
                                                tiles, tile_count, prm, s);
   if (tile_rows == kBsPrefillRows)
     return launch_bs<BS_GATEUP, kBsPrefillRows>(p, bw.gu_q, bw.gu_sf, d.E, d.I, d.L, ws.lq, ws.lsf, ws.rows_max,
@@ -803,7 +1043,7 @@ cudaError_t bs_stream_down(const BsPlan& p, const BsWeights& bw, const int4* til
   prm.ld_out = d.L;
   prm.o = w.o;
   if (tile_rows == kBsDecodeRows)
-    return launch_bs<BS_DOWN, kBsDecodeRows>(p, bw.d_q, bw.d_sf, d.E, d.L, d.I, ws.hq, ws.hsf, ws.rows_max, tiles,
+    return launch_bs<BS_DOWN, kBsDecodeRows>(p, bw.d_q, bw.d_sf, d.E, d.L, d.I, ws.hq, ws.hsf, ws.rows_fp4, tiles,
                                              tile_count, prm, s);
   if (tile_rows == kBsPrefillRows)
     return launch_bs<BS_DOWN, kBsPrefillRows>(p, bw.d_q, bw.d_sf, d.E, d.L, d.I, ws.hq, ws.hsf, ws.rows_max, tiles,

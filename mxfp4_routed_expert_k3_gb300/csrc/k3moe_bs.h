@@ -48,7 +48,8 @@ struct BsPlan {
 // batches taller ones (fewer weight re-reads per token).
 constexpr int kBsDecodeRows = 16;
 constexpr int kBsPrefillRows = 80;
-inline int bs_tile_rows(int T) { return T <= 128 ? kBsDecodeRows : kBsPrefillRows; }
+constexpr int kBsDecodeMaxT = 128;  // largest T run on decode tiles
+inline int bs_tile_rows(int T) { return T <= kBsDecodeMaxT ? kBsDecodeRows : kBsPrefillRows; }
 size_t bs_ws_bytes(const Dims& d, int max_tokens);
 // slot -> (tile << 8 | row in tile), written by the tile-list builders
 int* bs_slot_tile(const BsPlan& p);

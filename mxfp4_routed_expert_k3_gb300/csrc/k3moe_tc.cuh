@@ -94,6 +94,17 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 
 // UMMA shared-memory descriptor, K-major, 128-byte swizzle: rows of 128 bytes,
 // 8-row groups 1024 bytes apart (stride byte offset), leading offset unused.
+// K-major operand in 64-byte rows with the 64-byte swizzle (8-row atoms of
+// 512 bytes): dense e2m1 tiles of 128 columns.
+__device__ __forceinline__ uint64_t umma_desc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1u << 16;                 // leading byte offset (unused for this layout)
+  d |= (uint64_t)(512u >> 4) << 32;        // stride byte offset
+  d |= (uint64_t)1u << 46;                 // descriptor version
+  d |= (uint64_t)4u << 61;                 // 64-byte swizzle
+  return d;
+}
 __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
