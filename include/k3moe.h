@@ -84,11 +84,13 @@ typedef struct {
                          dense projections by split-K for T <= 64; expert
                          weights decoded to bf16 into tensor memory);
                       4: as 3, with the expert GEMMs on the block-scaled
-                         MXFP4 tensor cores (tcgen05 kind::mxf8f6f4: e2m1
-                         weights and e8m0 scales as stored, activations as
-                         two exact block-scaled e4m3 terms; tiles of 16
-                         token rows up to T = 128, both terms in one MMA,
-                         80 rows above) */
+                         MXFP4 tensor cores (e2m1 weights and e8m0 scales
+                         as stored; up to T = 128 tcgen05 kind::mxf4 on
+                         tiles of 16 token rows with the activations as six
+                         block-scaled e2m1 terms, above that
+                         kind::mxf8f6f4 on tiles of 80 rows with two exact
+                         e4m3 terms; the terms of a tile form one MMA
+                         operand) */
 } k3moe_config;
 
 /* Host arrays in checkpoint layout, experts stacked along dim 0.  Row-major;
