@@ -297,8 +297,8 @@ def run_ours(args, rank, world, local_rank):
                  4: "bs_stream_kernel_gateup"}.get(path_used, "umma_gemm_kernel_gateup")
     kernel_desc = {1: "gateup_gemv_kernel (CUDA-core grouped MXFP4 gate/up GEMV + SiTU-GLU)",
                    3: "umma_stream_kernel<GATEUP> (tcgen05, decoded MXFP4 weights in TMEM, SiTU-GLU epilogue)",
-                   4: "bs_stream_kernel<GATEUP> (tcgen05 kind::mxf8f6f4: e2m1 weights x two e4m3 activation "
-                      "terms, UE8M0 scales in TMEM, SiTU-GLU + requantisation epilogue)"
+                   4: "bs_stream_kernel<GATEUP> (tcgen05 kind::mxf4: e2m1 weights as stored x six e2m1 "
+                      "activation terms, UE8M0 scales in TMEM, SiTU-GLU + requantisation epilogue)"
                    }.get(path_used, "umma_gemm_kernel<GATEUP> (tcgen05 grouped MXFP4 GEMM)")
     # ncu's DRAM bytes per active expert (captured on a smaller case, traffic
     # grows with the experts touched) times this run's mean active experts
