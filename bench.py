@@ -452,8 +452,13 @@ def run_reference(args, rank, world):
     from oracle import oracle as ora
     d = K3
     w = synth.layer_weights(d, seed=1)
-    per_step = args.ref_tokens_per_step
-    xs = [synth.token_rows(d, 5000 + i, per_step) for i in range(args.warmup + args.steps)]
+    # Bounded sample per step: one token per oracle thread by default.  The
+    # oracle spreads tokens over its threads and a token's layer runs on one
+    # thread, so a step costs about one token's time whatever its size up to
+    # the thread count (about 13 s per step on 8-16 host cores).
+    per_step = args.ref_tokens_per_step if args.ref_tokens_per_step > 0 else ora.num_threads()
+    n_steps = args.warmup + args.steps
+    xs = [synth.token_rows(d, 5000 + i, per_step) for i in range(n_steps)]
     for i in range(args.warmup):
         ora.forward(d, w, xs[i])
     times = []
@@ -481,11 +486,12 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-sample", type=int, default=16, help="tokens in the oracle CPU baseline sample")
-    ap.add_argument("--ref-tokens-per-step", type=int, default=8)
+    ap.add_argument("--ref-tokens-per-step", type=int, default=0,
+                    help="tokens per step of the reference arm (0: one per oracle thread)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the T=8192 prefill measurement")
     ap.add_argument("--prefill-tokens", type=int, default=PREFILL_T,
