@@ -154,12 +154,9 @@ __device__ __forceinline__ float2 from_e2m1x2(uint32_t b) {
 // read from TMEM lane R%32 of column R/32 once the atoms sit in consecutive
 // 4-column groups.
 __device__ __forceinline__ int act_atom_byte(int R) { return (R >> 7) * kAtom + (R & 31) * 16 + ((R & 127) >> 5) * 4; }
-// Term t of tile row n: stacked tiles (`stack` rows, both terms one operand
-// of 2*stack rows) use operand row t*stack + n; otherwise term t has its own
-// atom and the operand row is n.
-__device__ __forceinline__ int act_scale_byte(int t, int n, int stack) {
-  return stack ? act_atom_byte(t * stack + n) : t * kAtom + act_atom_byte(n);
-}
+// Term t of row n of a tile of `stack` rows: the terms of a tile form one
+// MMA operand, term t of row n being operand row t*stack + n.
+__device__ __forceinline__ int act_scale_byte(int t, int n, int stack) { return act_atom_byte(t * stack + n); }
 
 // Slot-ordered rows: dst row s = src row (perm ? perm[s] / K : s), written
 // as terms q[C/128][t][rows_max][128]; the scales go to the tile atoms
@@ -248,7 +245,9 @@ __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, const int* _
 // The same for decode-size tiles (`stack` rows): kFp4Terms e2m1 terms
 // q[C/128][kFp4Terms][rows_max][64] (two codes per byte, low nibble first)
 // and their scales at act_scale_byte(t, n, stack) + g of the tile's first
-// atom.
+// atom.  CH chunks per half warp: one for the few rows of the smallest
+// batches (more warps, shorter chains), four otherwise.
+template <int CH>
 __global__ void quant_rows_fp4_kernel(const uint16_t* __restrict__ src, const int* __restrict__ perm, int K, int rows,
                                       int C, int rows_max, const int* __restrict__ slot_tile, int stack,
                                       uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
@@ -256,31 +255,31 @@ __global__ void quant_rows_fp4_kernel(const uint16_t* __restrict__ src, const in
   pdl_wait();
   const int hl = threadIdx.x & 15, half = (threadIdx.x >> 4) & 1;
   const int KC = C / kQK;
-  const int KG = (KC + kQuantChunks - 1) / kQuantChunks;  // chunk groups per row
+  const int KG = (KC + CH - 1) / CH;  // chunk groups per row
   const long long nwork = (long long)rows * KG;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
   for (long long wi = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; 2 * wi < nwork; wi += nwarps) {
     const long long i = 2 * wi + half;
     const bool valid = i < nwork;
     const int s = valid ? (int)(i / KG) : 0, kg = valid ? (int)(i - (long long)s * KG) : 0;
-    uint4 v[kQuantChunks];
+    uint4 v[CH];
     int tn = 0;
     if (valid) {
       const int t = perm ? perm[s] / K : s;
       tn = slot_tile[s];
 #pragma unroll
-      for (int c = 0; c < kQuantChunks; ++c) {
-        const int kc = kg * kQuantChunks + c;
+      for (int c = 0; c < CH; ++c) {
+        const int kc = kg * CH + c;
         v[c] = kc < KC ? *reinterpret_cast<const uint4*>(src + (size_t)t * C + kc * kQK + hl * 8)
                        : make_uint4(0u, 0u, 0u, 0u);
       }
     } else {
 #pragma unroll
-      for (int c = 0; c < kQuantChunks; ++c) v[c] = make_uint4(0u, 0u, 0u, 0u);
+      for (int c = 0; c < CH; ++c) v[c] = make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
-    for (int c = 0; c < kQuantChunks; ++c) {
-      const int kc = kg * kQuantChunks + c;
+    for (int c = 0; c < CH; ++c) {
+      const int kc = kg * CH + c;
       const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
       float x[8];
 #pragma unroll
@@ -387,27 +386,24 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
 }
 
 // Per stage four copies: the e2m1 tiles (GATEUP: gate and up of one
-// 128-column chunk; DOWN: kNK consecutive chunks), both activation terms of
+// 128-column chunk; DOWN: kNK consecutive chunks), all activation terms of
 // the stage's chunks (one 4-D box), the weight scale atoms and the
 // activation scale atoms (bulk copies).  Few large copies per stage keep the
-// HBM stream going.  NQ is the tile height (MMA N <= NQ):
-//   32 (decode-size batches): two CTAs per SM, two stages each, one
-//      epilogue warpgroup; the kernel streams weights;
-//   80 (larger batches): also two CTAs per SM with two stages (a single CTA
-//      per SM with deeper rings and both accumulator buffers measured
-//      slower: the copies a CTA keeps in flight bound the rate); gate/up
-//      then keeps one accumulator buffer per CTA (gate + up need 208 of the
-//      CTA's 256 TMEM columns), and the other CTA on the SM covers its
-//      epilogue.
+// HBM stream going.  NQ is the tile height:
+//   16 (T <= 128): kind::mxf4, six e2m1 activation terms (N = 96), two CTAs
+//      per SM with four (gate/up) or three (down) stages; the kernel
+//      streams weights;
+//   80 (larger batches): kind::mxf8f6f4, two e4m3 terms (N = 160); gate/up
+//      runs one CTA per SM (its accumulators take 320 TMEM columns), down
+//      two CTAs per SM with two stages and one accumulator buffer each.
 template <int MODE, int NQ>
 struct BsCfg {
   static constexpr bool kBig = NQ > 32;
-  // Both activation terms go into one MMA: B rows [term 0 of the NQ tokens;
-  // term 1 of the same tokens], N = 2 * NQ, and the epilogue adds
-  // accumulator columns j and NQ + j.  A block-scaled MMA instruction takes
-  // about the tensor-pipe time of an N = 256 one whatever its N, so this
-  // halves the pipe time, which bounds both the decode stream and prefill.
-  static constexpr bool kStack = true;
+  // All activation terms go into one MMA: B rows [term 0 of the NQ tokens;
+  // term 1 of the same tokens; ...], N = terms * NQ, and the epilogue adds
+  // accumulator columns t * NQ + j.  A block-scaled MMA instruction takes
+  // about the tensor-pipe time of an N = 256 one whatever its N, so one MMA
+  // per k step and matrix keeps the tensor pipe's share of a stage small.
   // Prefill gate/up: its two stacked accumulators (2 x 160 columns) need
   // more than a CTA's share of a two-CTA split, so one CTA per SM owns all
   // 512 columns, with a deeper ring and two epilogue warpgroups.  The other
@@ -441,13 +437,13 @@ struct BsCfg {
   // accumulator buffers: one where the stacked accumulators fill the CTA's
   // columns (the epilogue then releases the buffer as soon as it has read it)
   static constexpr int kDBuf = (kBig || MODE == BS_GATEUP) ? 1 : 2;
-  static constexpr int kAccW = kStack ? kTerms * NQ : (NQ + 15) / 16 * 16;  // accumulator columns (MMA N)
+  static constexpr int kAccW = kTerms * NQ;  // accumulator columns (MMA N)
   static constexpr int kAccStride = (kWide || kFp4) ? kAccW : 128;          // TMEM columns between matrices
   static constexpr int kBufStride = kNumA * kAccStride;                     // TMEM columns between buffers
   static constexpr int kSfBase = (kDBuf - 1) * kBufStride + (kNumA - 1) * kAccStride + kAccW;
   // weight atoms, then the activation atoms: one per chunk holding both
   // terms' rows (stacked), else one per chunk and term
-  static constexpr int kSfbAtoms = kStack ? (kTerms * NQ + 127) / 128 : 2;
+  static constexpr int kSfbAtoms = (kTerms * NQ + 127) / 128;
   static constexpr int kSfCols = 4 * kNA + 4 * kSfbAtoms * kNK;
   static constexpr int kTmemCols = kWide ? 512 : 256;
   static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
@@ -580,9 +576,7 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
         }
         tc_fence_after();
         const uint32_t d0 = tmem + buf * C::kBufStride;
-        // MMA N: stacked, both terms of the NQ rows; else the tile's rows
-        // rounded up to 16 (never beyond the accumulator's columns)
-        const uint32_t n = C::kStack ? (uint32_t)C::kAccW : (uint32_t)min(p.tiles[item / p.MT].w, C::kAccW);
+        const uint32_t n = (uint32_t)C::kAccW;  // MMA N: every term of the tile's NQ rows
         for (int ks = 0; ks < p.KS; ++ks, ++kg) {
           const int s = kg % C::kStages;
           if (!mbar_wait(full(s), (kg / C::kStages) & 1, g, 4u)) {
@@ -628,17 +622,14 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
 #pragma unroll
             for (int kb = 0; kb < kQK / 32; ++kb)
 #pragma unroll
-              for (int a = 0; a < C::kNumA; ++a)
-#pragma unroll
-                for (int t = 0; t < (C::kStack ? 1 : 2); ++t) {
-                  // B blocks of the 4-D box are [chunk][term]; stacked, the
-                  // two terms' rows are one 2*NQ-row operand
-                  const int ablk = (MODE == BS_GATEUP) ? a : c;
-                  const int bblk = c * 2 + t;
-                  umma_bs(d0 + a * C::kAccStride, a_d + ((ablk * C::kA + kb * 32) >> 4),
-                          b_d + ((bblk * C::kB + kb * 32) >> 4), bs_idesc(kb, kb, n), sfc + 4 * ablk,
-                          sfc + 4 * C::kNA + 4 * (c * C::kSfbAtoms + t), (c | kb | t) ? 1u : first);
-                }
+              for (int a = 0; a < C::kNumA; ++a) {
+                // B blocks of the 4-D box are [chunk][term]: a chunk's terms
+                // are one terms*NQ-row operand
+                const int ablk = (MODE == BS_GATEUP) ? a : c;
+                umma_bs(d0 + a * C::kAccStride, a_d + ((ablk * C::kA + kb * 32) >> 4),
+                        b_d + ((c * C::kTerms * C::kB + kb * 32) >> 4), bs_idesc(kb, kb, n), sfc + 4 * ablk,
+                        sfc + 4 * C::kNA + 4 * c * C::kSfbAtoms, (c | kb) ? 1u : first);
+              }
           }
           umma_commit(sfree(s));
         }
@@ -676,7 +667,7 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
       // Token columns per group: 32, or NQ for decode tiles, whose terms'
       // columns (term t of token j in column t*NQ + j) fit one or two
       // 32-column loads.  Stacked, token j's partial sums are added here.
-      constexpr bool kPair = C::kStack && !C::kBig;
+      constexpr bool kPair = !C::kBig;
       constexpr int JW = kPair ? NQ : 32;
       static_assert(!kPair || (2 * NQ == 32 && C::kTerms % 2 == 0), "decode accumulator layout");
       auto load_acc = [&](uint32_t base, int j0, float* v) {
@@ -692,14 +683,12 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
 #pragma unroll
             for (int j = 0; j < JW; ++j) v[j] += w2[j] + w2[j + JW];
           }
-        } else if (C::kStack) {
+        } else {
           float w2[32];
           tmem_ld32(base + j0, v);
           tmem_ld32(base + NQ + j0, w2);
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] += w2[j];
-        } else {
-          tmem_ld32(base + j0, v);
         }
       };
       // Prefill tiles: the sums of a warpgroup's NQ / kWG consecutive tokens
@@ -727,7 +716,7 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
       if (MODE == BS_GATEUP) {
         // h as bf16 and as the two e4m3 terms (and scale atoms) of the down
         // GEMM's B operand, laid out for the down kernel's tiles
-        constexpr int kHStack = BsCfg<BS_DOWN, NQ>::kStack ? NQ : 0;
+        constexpr int kHStack = NQ;  // the down kernel's tiles have the same height
         constexpr bool kHFp4 = BsCfg<BS_DOWN, NQ>::kFp4;
         constexpr int kHTerms = BsCfg<BS_DOWN, NQ>::kTerms;
         const int KCo = p.ld_out / kQK;
@@ -999,13 +988,13 @@ cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
   if (T > p.max_tokens || (tile_rows != kBsDecodeRows && tile_rows != kBsPrefillRows)) return cudaErrorInvalidValue;
-  const int stack = tile_rows == kBsDecodeRows ? (BsCfg<BS_GATEUP, kBsDecodeRows>::kStack ? kBsDecodeRows : 0)
-                                                : (BsCfg<BS_GATEUP, kBsPrefillRows>::kStack ? kBsPrefillRows : 0);
+  const int stack = tile_rows;
   const BsWs ws = bs_ws_view(p.ws, d, p.max_tokens);
-  const long long halves = (long long)TK * ((d.L / kQK + kQuantChunks - 1) / kQuantChunks);
+  const bool fp4 = tile_rows == kBsDecodeRows && BsCfg<BS_GATEUP, kBsDecodeRows>::kFp4;
+  const int ch = (fp4 && TK <= 8 * d.K) ? 1 : kQuantChunks;  // chunks per half warp
+  const long long halves = (long long)TK * ((d.L / kQK + ch - 1) / ch);
   const int blocks = (int)std::min<long long>((halves * 16 + 255) / 256, 8LL * p.num_sms);
-  auto kernel = (tile_rows == kBsDecodeRows && BsCfg<BS_GATEUP, kBsDecodeRows>::kFp4) ? quant_rows_fp4_kernel
-                                                                                     : quant_rows_kernel;
+  auto kernel = !fp4 ? quant_rows_kernel : ch == 1 ? quant_rows_fp4_kernel<1> : quant_rows_fp4_kernel<kQuantChunks>;
   const int rows = tile_rows == kBsDecodeRows ? ws.rows_fp4 : ws.rows_max;
   return launch_pdl(kernel, blocks, 256, 0, s, w.lat, w.perm, d.K, TK, d.L, rows, ws.slot_tile, stack, ws.lq,
                     ws.lsf);
