@@ -114,12 +114,12 @@ __device__ __forceinline__ uint32_t split_e4m3(float x, uint32_t s0, uint32_t s1
 // Decode-size tiles carry each activation as kFp4Terms e2m1 terms with their
 // own UE8M0 scale per 32-column group: term t quantises what the earlier
 // terms left, x = sum_t q_t * 2^(S_t - 127).  The scale puts the group's
-// largest remaining magnitude at or below 6 (the largest e2m1 value); each
-// term leaves at most about a quarter of it, so six terms keep an activation
-// within about 2.5e-7 of its group's largest magnitude (four measured 1e-4:
-// enough for the layer's output, not for the per-step checks that hold h
-// and o to one bf16 ulp and 2e-5).  2^n for n in [-127, 127] (2^-127 is
-// subnormal).
+// largest remaining magnitude in (3, 6] (6 is the largest e2m1 value), so
+// each term shrinks the group's largest residual at least 3x; on the layer's
+// activations six terms leave an RMS error near 1e-7 of theirs (four leave
+// 1e-4: enough for the layer's output, not for the per-step checks that
+// hold h and o to one bf16 ulp and 2e-5).  2^n for n in [-127, 127]
+// (2^-127 is subnormal).
 constexpr int kFp4Terms = 6;
 __device__ __forceinline__ float exp2_any(int n) {
   return n >= -126 ? __uint_as_float((uint32_t)(n + 127) << 23) : __uint_as_float(0x00400000u);
