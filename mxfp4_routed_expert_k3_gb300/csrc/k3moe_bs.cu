@@ -1,30 +1,32 @@
 // k3moe_bs.cu -- MXFP4 expert GEMMs on the block-scaled tensor cores.
 //
-// tcgen05.mma kind::mxf8f6f4 multiplies e2m1 (A) by e4m3 (B) with one
-// UE8M0 scale per 32 elements of K on each side and accumulates in fp32:
+// tcgen05.mma with block scaling multiplies two MX operands with one UE8M0
+// scale per 32 elements of K on each side and accumulates in fp32:
 //   D[m, n] += sum_k (a[m, k] 2^(SA[m, k/32]-127)) (b[n, k] 2^(SB[n, k/32]-127)).
 // A is an expert weight exactly as the checkpoint stores it (e2m1 nibbles,
 // low nibble first; e8m0 scale per 32 along the input dimension: kimi-k3-mlx
 // README, "Tiers"; K3_ARTIFACT_AUDIT section 4.3), so no CUDA-core work
-// touches the weights: TMA moves the packed nibbles into shared memory in
-// the 16-byte-slot layout the tensor core reads (16U4_ALIGN16B), and the
-// scales go to tensor memory with tcgen05.cp.
+// touches the weights: TMA moves the packed nibbles into shared memory and
+// the scales go to tensor memory with tcgen05.cp.
 //
-// B carries the bf16 activations (latent rows, then h) as two e4m3 terms
-// per element with per-32 scales:  x = q0 2^(S0-127) + q1 2^(S1-127),
-//   S0 = max(E - 7, 0) for the block's largest biased bf16 exponent E, so
-//        |x| 2^(127-S0) < 2^8 (inside e4m3's range), q0 = RN_e4m3 of that;
-//   S1 = max(S0 - 4, 0), q1 = RN_e4m3((x 2^(127-S0) - q0) 2^(S0-S1)).
-// The first term keeps the top 4 significant bits, the remainder has at
-// most 4 more, so the split is exact for every element within 2^13 of its
-// block's largest magnitude; smaller elements keep an absolute error below
-// 2^(S0-127-13).  Two MMAs (one per term) accumulate into the same D.
+// B carries the bf16 activations (latent rows, then h) as block-scaled
+// terms with per-32 scales, all terms of a tile stacked into one operand:
+//  * prefill tiles (kind::mxf8f6f4, e2m1 A in the 16-byte-slot layout
+//    16U4_ALIGN16B): two e4m3 terms, x = q0 2^(S0-127) + q1 2^(S1-127),
+//      S0 = max(E - 7, 0) for the block's largest biased bf16 exponent E, so
+//           |x| 2^(127-S0) < 2^8 (inside e4m3's range), q0 = RN_e4m3 of that;
+//      S1 = max(S0 - 4, 0), q1 = RN_e4m3((x 2^(127-S0) - q0) 2^(S0-S1)).
+//    The first term keeps the top 4 significant bits, the remainder has at
+//    most 4 more, so the split is exact for every element within 2^13 of
+//    its block's largest magnitude; smaller elements keep an absolute error
+//    below 2^(S0-127-13).
+//  * decode tiles (kind::mxf4, e2m1 A dense with the 64-byte swizzle): six
+//    e2m1 terms (see the split below).
 //
-// Tile scheme (decode sizes): M = 128 weight rows, N = 16 or 32 token rows
-// (one tile of the expert's slots), MMAs of K = 32 per term and matrix.
-// Warp 0 issues the copies, warp 1 the MMAs, warps 2..5 run the epilogue
-// from a double-buffered accumulator; two CTAs per SM.  Every wait is
-// bounded (status bit + shared abort flag, as in the bf16 kernels).
+// Tile scheme: M = 128 weight rows, N = terms x tile rows (one tile of an
+// expert's slots: 16 rows at decode, 80 at prefill).  Warp 0 issues the
+// copies, warp 1 the MMAs, the remaining warps run the epilogue.  Every wait
+// is bounded (status bit + shared abort flag, as in the bf16 kernels).
 #include <cuda.h>
 
 #include <algorithm>
@@ -714,7 +716,7 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
         }
       };
       if (MODE == BS_GATEUP) {
-        // h as bf16 and as the two e4m3 terms (and scale atoms) of the down
+        // h as bf16 and as the block-scaled terms (and scale atoms) of the down
         // GEMM's B operand, laid out for the down kernel's tiles
         constexpr int kHStack = NQ;  // the down kernel's tiles have the same height
         constexpr bool kHFp4 = BsCfg<BS_DOWN, NQ>::kFp4;

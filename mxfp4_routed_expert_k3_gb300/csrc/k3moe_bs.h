@@ -55,12 +55,14 @@ size_t bs_ws_bytes(const Dims& d, int max_tokens);
 int* bs_slot_tile(const BsPlan& p);
 cudaError_t prepare_bs_kernels();
 
-// Slot-ordered latent rows (lat[perm[s] / K]) written as two e4m3 terms, and
-// their scales as per-tile atoms (needs the tile list's slot map; tile_rows
-// is the tile height the expert kernels will use).
+// Slot-ordered latent rows (lat[perm[s] / K]) written as the block-scaled
+// terms of the expert kernels' B operand (six e2m1 terms for decode tiles,
+// two e4m3 terms for prefill tiles) and their scales as per-tile atoms
+// (needs the tile list's slot map; tile_rows is the tile height the expert
+// kernels will use).
 cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims& d, int tile_rows, cudaStream_t s);
 // gate/up over the tile list (tiles of at most tile_rows rows): h (bf16,
-// slot order) and its two-term e4m3 form for the down GEMM.
+// slot order) and its block-scaled terms for the down GEMM.
 cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* tiles, const int* tile_count,
                              const Work& w, int T, const Dims& d, int tile_rows, cudaStream_t s);
 // down: o (fp32, slot order)
