@@ -63,6 +63,23 @@ def test_k3_decode_all_tokens(k3decode, T):
     print(f"decode T={T} path={layer.query('path_last')}", m)
 
 
+def test_k3_decode_tiles_unfused_route_t96(k3weights):
+    """T = 96: decode tiles (T <= 128) with T*K = 1536 > 1024 slots, so the
+    routing runs the multi-kernel top-k / permute / tile-list chain instead
+    of the fused small-batch kernel; every token against the oracle."""
+    layer = k3moe.Layer(K3, k3weights, max_tokens=128)
+    try:
+        x = gapped_tokens(K3, k3weights, seed=296, T=96)
+        ref = ora.forward(K3, k3weights, x)
+        y, idx, wts = run(layer, x)
+        assert layer.query("path_last") == k3moe.PATH_BLOCK_SCALED
+        assert_routing_equal(idx, wts, ref["idx"], ref["w"], "decode tiles T=96")
+        m = assert_y_close(y, ref["y"], "decode tiles T=96")
+        print("decode tiles T=96", m)
+    finally:
+        layer.close()
+
+
 def _sampled(layer, w, x, n_sample, seed, label):
     T = x.shape[0]
     idx_ref, w_ref, _ = ora.route(K3, x, w["router_w"], w["router_bias"])
