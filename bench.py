@@ -91,10 +91,10 @@ class ClockSampler:
     def __init__(self, gpu_index: int, settle_s: float = 1.5):
         self.proc = None
         self.t0 = self.t1 = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        import tempfile
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.fh = open(self.path, "w")
+            fd, self.path = tempfile.mkstemp(prefix="k3moe_clocks_", suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.QUERY}",
                                           "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
@@ -125,7 +125,13 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.fh.close()
-        return self.parse()
+        try:
+            return self.parse()
+        finally:
+            try:
+                os.unlink(self.path)
+            except OSError:
+                pass
 
     def parse(self) -> dict:
         sm, smax, reasons, window = [], None, set(), 0

@@ -176,8 +176,10 @@ int k3moe_mxfp4_dequant(const uint8_t* packed, const uint8_t* scale, int rows, i
                         void* out, int kind, void* cuda_stream);
 
 /* Router step on its own: logits = x . Wr^T into the caller's scratch
- * `logits` [T, E] fp32 (device), then top-K selection and weights exactly
- * as in k3moe_forward (same kernels).  Device pointers: x [T,H] bf16,
+ * `logits` [T, E] fp32 (device), then top-K selection and weights with the
+ * forward's top-K kernel.  The logits come from a CUDA-core GEMV with fp32
+ * FMA chains (k3moe_forward computes them on the tensor cores, fused with
+ * down_proj), so the two can differ in the last bits of a logit.  Device pointers: x [T,H] bf16,
  * router_w [E,H] bf16, bias [E] f32, topk_idx [T,K], topk_w [T,K].
  * Requires H % 128 == 0, 1 <= K <= 32, K <= E <= 2048.  Asynchronous. */
 int k3moe_route(const void* x, int T, const void* router_w, const float* bias, int E, int H, int K,
@@ -192,9 +194,14 @@ int k3moe_route(const void* x, int T, const void* router_w, const float* bias, i
  * Same inputs, outputs and results as k3moe_route, but the [T, E] fp32
  * logits scratch is a file-scope __device__ array of 131072 floats (512 KiB)
  * that every GPU loading the library holds until the process exits.
- * T * E > 131072 returns K3MOE_EINVAL.  The first call on a device looks up
- * the array's device address (with that device current, once per device);
- * make that first call before any stream capture.  Calls never allocate.
+ * T * E > 131072 returns K3MOE_EINVAL.  The array's device address is
+ * looked up with the calling thread's current device and CUDA context, and
+ * cached per context: outside stream capture every call looks it up again
+ * (so a context rebuilt after cudaDeviceReset gets a fresh address), while
+ * a call made during stream capture uses the cached address of its
+ * context.  So the first call on a device (and the first one after a
+ * device reset) must come before any stream capture; a first call made
+ * during capture returns K3MOE_ESTATE.  Calls never allocate.
  * All calls share the one array and it keeps the last call's contents
  * (nothing here needs it zeroed): calls that overlap on the GPU, from any
  * stream or thread, race on it.  Errors are reported by

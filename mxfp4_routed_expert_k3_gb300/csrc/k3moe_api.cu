@@ -439,7 +439,8 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
     bn = k3::bs_tile_rows(T);
     if (!fused_route)
       K3_LAUNCH(k3::umma_stream_tiles(c->umma, w, T, d, bn, k3::bs_slot_tile(c->bs), s), 1, "tile list");
-    K3_LAUNCH(k3::bs_quantize_latent(c->bs, w, T, d, bn, s), 1, "latent rows -> e4m3 terms");
+    K3_LAUNCH(k3::bs_quantize_latent(c->bs, w, T, d, bn, s), 1,
+              bn <= 16 ? "latent rows -> e2m1 terms" : "latent rows -> e4m3 terms");
     K3_LAUNCH(k3::bs_stream_gateup(c->bs, c->bw, tiles, tile_count, w, T, d, bn, s), 1, "gate/up");
     K3_LAUNCH(k3::bs_stream_down(c->bs, c->bw, tiles, tile_count, w, T, d, bn, s), 1, "down");
   } else if (path == 3) {

@@ -1,7 +1,10 @@
 // k3moe_bs.h -- block-scaled tensor-core path for the MXFP4 expert GEMMs:
-// tcgen05.mma kind::mxf8f6f4 with the e2m1 weights and their e8m0 scales fed
-// to the tensor cores as they are stored, and the bf16 activations written
-// exactly as the sum of two block-scaled e4m3 terms.
+// the e2m1 weights and their e8m0 scales go to the tensor cores as they are
+// stored.  Two tile kinds: decode tiles (16 token rows, up to T = 128) use
+// tcgen05.mma kind::mxf4 with the bf16 activations carried as six
+// block-scaled e2m1 terms; prefill tiles (80 token rows) use
+// kind::mxf8f6f4 with the activations written exactly as the sum of two
+// block-scaled e4m3 terms.
 #pragma once
 #include <cstddef>
 #include <cstdint>

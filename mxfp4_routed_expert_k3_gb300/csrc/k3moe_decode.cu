@@ -117,11 +117,6 @@ cudaError_t launch_dense_gemv(const uint16_t* W, int M, int K, const uint16_t* X
 }
 
 // =====================================================================
-// Router top-K (one warp per token).
-//   s = sigmoid(logit) in fp32; key = s + bias (fp32); the K largest keys
-//   are taken one at a time, ties to the lower expert id; weights from the
-//   unbiased s, divided by their sum when norm_topk, times rsf.
-// =====================================================================
 // Router top-K (kimi-k3-mlx README, "Architecture" table: sigmoid router,
 // e_score_correction_bias added for selection only).  One CTA per token:
 //   s[e] = 1 / (1 + exp(-logit[e])),  key[e] = s[e] + bias[e] (fp32);

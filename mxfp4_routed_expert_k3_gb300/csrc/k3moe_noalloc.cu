@@ -10,6 +10,8 @@
 // They pass inputs and outputs only; the scratch comes from a file-scope
 // __device__ array that every GPU loading this library holds until the
 // process exits.
+#include <cuda.h>
+
 #include <cstdio>
 #include <mutex>
 
@@ -23,9 +25,37 @@ namespace {
 constexpr size_t kNoAllocLogits = 131072;
 __device__ __align__(256) float g_noalloc_logits[kNoAllocLogits];
 
-constexpr int kMaxDevices = 64;
-float* g_scratch_ptr[kMaxDevices] = {};
+// The array's device address belongs to one CUDA context (the module is
+// loaded per context), so the cache is keyed by the current context, not
+// by the device ordinal: a primary context rebuilt after cudaDeviceReset,
+// or a second context on the same device, gets its own entry.  Outside
+// stream capture every call asks the runtime again and refreshes the entry;
+// during capture the entry of the current context is used as it stands.
+constexpr int kMaxContexts = 64;
+struct ScratchEntry {
+  CUcontext ctx;
+  float* ptr;
+};
+ScratchEntry g_scratch[kMaxContexts] = {};
+int g_scratch_n = 0;
 std::mutex g_scratch_mu;
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+// cuCtxGetCurrent from the driver, through the runtime's entry-point query
+// (the library does not link libcuda directly).
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
 
 int noalloc_fail(int code, const char* msg) {
   k3::set_thread_error(msg);  // reported by k3moe_last_error(NULL)
@@ -48,23 +78,42 @@ int k3moe_route_noalloc(const void* x, int T, const void* router_w, const float*
     return noalloc_fail(K3MOE_EINVAL, "T * E exceeds the static scratch (131072 router logits)");
   if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(router_w) & 15u))
     return noalloc_fail(K3MOE_EINVAL, "x and router_w must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  // Make the current device's primary context current (cudaSetDevice
+  // initialises it; a no-op when it already is), then identify it.
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-    return noalloc_fail(K3MOE_ECUDA, "cudaGetDevice failed or device ordinal too large");
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess)
+    return noalloc_fail(K3MOE_ECUDA, "no usable CUDA device");
+  CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+  CUcontext ctx = nullptr;
+  if (!get_ctx || get_ctx(&ctx) != CUDA_SUCCESS || !ctx)
+    return noalloc_fail(K3MOE_ECUDA, "cuCtxGetCurrent failed");
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return noalloc_fail(K3MOE_ECUDA, "cudaStreamIsCapturing failed");
   float* scratch = nullptr;
   {
-    // Set-up, once per device, with that device current: the host-side
-    // name of the array is not a device address, so ask the runtime.
+    // Set-up with the device current: the host-side name of the array is
+    // not a device address, so ask the runtime for this context's copy.
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+    ScratchEntry* ent = nullptr;
+    for (int i = 0; i < g_scratch_n; ++i)
+      if (g_scratch[i].ctx == ctx) ent = &g_scratch[i];
+    if (!ent || cs == cudaStreamCaptureStatusNone) {
+      if (cs != cudaStreamCaptureStatusNone)
+        return noalloc_fail(K3MOE_ESTATE, "first call on this CUDA context made during stream capture; "
+                                          "call once outside capture first");
       void* p = nullptr;
       cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_logits);
       if (e != cudaSuccess || !p) return noalloc_fail(K3MOE_ECUDA, "cudaGetSymbolAddress of the scratch failed");
-      g_scratch_ptr[dev] = static_cast<float*>(p);
+      if (!ent) {
+        if (g_scratch_n == kMaxContexts) return noalloc_fail(K3MOE_ECUDA, "too many CUDA contexts");
+        ent = &g_scratch[g_scratch_n++];
+        ent->ctx = ctx;
+      }
+      ent->ptr = static_cast<float*>(p);
     }
-    scratch = g_scratch_ptr[dev];
+    scratch = ent->ptr;
   }
-  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   cudaError_t e = k3::launch_dense_gemv(static_cast<const uint16_t*>(router_w), E, H, static_cast<const uint16_t*>(x),
                                         T, E, scratch, nullptr, s);
   if (e == cudaSuccess)

@@ -318,8 +318,9 @@ void ora_forward(const ora_dims* d, const ora_weights* W, const uint16_t* x, int
 }
 
 /* Router only, for T tokens (used to measure the K-th/(K+1)-th key gap of
- * candidate inputs).  keys_sorted receives, per token, the K+1 largest
- * keys in descending order. */
+ * candidate inputs).  keys_top_out receives, per token, the K+1 largest
+ * keys (s + bias, fp32) in descending order; when K == E there is no
+ * (K+1)-th key and its slot holds -inf, so the gap is +inf. */
 void ora_route(const ora_dims* d, const uint16_t* x, int T, const uint16_t* router_w,
                const float* bias, int32_t* idx, float* w, float* logits_out,
                float* keys_top_out) {
@@ -334,7 +335,11 @@ void ora_route(const ora_dims* d, const uint16_t* x, int T, const uint16_t* rout
     if (keys_top_out) {
       /* K+1 largest keys, descending (selection again, ties to lower id) */
       char* taken = (char*)calloc(E, 1);
-      for (int k = 0; k <= K && k < E; ++k) {
+      for (int k = 0; k <= K; ++k) {
+        if (k >= E) {
+          keys_top_out[(size_t)t * (K + 1) + k] = -INFINITY;
+          continue;
+        }
         int best = -1;
         for (int e = 0; e < E; ++e) {
           if (taken[e]) continue;

@@ -6,7 +6,9 @@ written for that part of the oracle rejects the mutant while the original
 passes.  The mistakes are the ones a reader could make from the pages:
 the wrong nibble first, the wrong exponent bias, swapped SiTU temperatures,
 the bias leaking into the weights, ties to the higher id, a dropped RMSNorm
-epsilon, a transposed down projection.
+epsilon, a transposed down projection, and two slips in the K+1 routing
+keys that guard the parity inputs' routing gap (only K keys written,
+ranking by the unbiased score).
 """
 import ctypes as C
 import math
@@ -35,6 +37,10 @@ MUTATIONS = {
     "ties_to_higher_id": ("if (best < 0 || key[e] > key[best]) best = e;",
                           "if (best < 0 || key[e] >= key[best]) best = e;"),
     "rmsnorm_no_eps": ("double inv = 1.0 / sqrt(ms + d->rms_eps);", "double inv = 1.0 / sqrt(ms);"),
+    "keys_top_only_k": ("for (int k = 0; k <= K; ++k) {\n        if (k >= E) {",
+                        "for (int k = 0; k < K; ++k) {\n        if (k >= E) {"),
+    "keys_top_by_score": ("float ke = s[e] + bias[e], kb = best < 0 ? 0.f : s[best] + bias[best];",
+                          "float ke = s[e], kb = best < 0 ? 0.f : s[best];"),
     "down_proj_transposed": ("acc += ora_bf16_to_double(W->down_proj[(size_t)l * H + j]) * ora_bf16_to_double(x[j]);",
                              "acc += ora_bf16_to_double(W->down_proj[(size_t)j * L + l]) * ora_bf16_to_double(x[j]);"),
 }
@@ -57,6 +63,7 @@ def build_variant(tmp, name):
     L.ora_situ_glu.argtypes = [C.c_double] * 4
     L.ora_mxfp4_dequant_bf16.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p]
     L.ora_route_from_logits.argtypes = [C.POINTER(ora.OraDims)] + [C.c_void_p] * 5
+    L.ora_route.argtypes = [C.POINTER(ora.OraDims), C.c_void_p, C.c_int] + [C.c_void_p] * 6
     L.ora_forward.argtypes = [C.POINTER(ora.OraDims), C.POINTER(ora.OraWeights)] + [C.c_void_p, C.c_int] + \
         [C.c_void_p] * 9
     return L
@@ -100,6 +107,28 @@ def pin_router(L):
     return bool(np.allclose(w, 1 / 3, rtol=1e-6))
 
 
+def pin_keys(L):
+    """The K+1 routing keys (the parity tests' gap guard) against a numpy
+    sort of s + bias; the output is pre-filled with NaN so that a slot the
+    oracle leaves unwritten fails."""
+    d = LayerDims(hidden=128, latent=128, n_experts=16, top_k=4, inter=128)
+    w = synth.layer_weights(d, seed=23)
+    # a bias wide enough to reorder the sigmoid scores
+    w["router_bias"] = np.random.default_rng(5).uniform(-0.3, 0.3, d.n_experts).astype(np.float32)
+    x = synth.token_rows(d, 24, 64)
+    T, E, K = 64, d.n_experts, d.top_k
+    idx = np.empty((T, K), np.int32)
+    wt = np.empty((T, K), np.float32)
+    logits = np.empty((T, E), np.float32)
+    keys = np.full((T, K + 1), np.nan, np.float32)
+    ds = ora.dims_struct(d)
+    L.ora_route(C.byref(ds), x.ctypes.data, T, w["router_w"].ctypes.data, w["router_bias"].ctypes.data,
+                idx.ctypes.data, wt.ctypes.data, logits.ctypes.data, keys.ctypes.data)
+    s = (1.0 / (1.0 + np.exp(-logits.astype(np.float64)))).astype(np.float32)
+    key = (s + w["router_bias"]).astype(np.float32)
+    return bool(np.array_equal(keys, -np.sort(-key, axis=1)[:, : K + 1]))
+
+
 def pin_layer(L):
     """Against the independent numpy formulation in test_oracle_pins."""
     from test_oracle_pins import np_layer
@@ -128,6 +157,7 @@ PIN_OF = {
     "high_nibble_first": pin_dequant, "e2m1_bias_0": pin_dequant, "e8m0_bias_128": pin_dequant,
     "situ_betas_swapped": pin_situ, "bias_in_weights": pin_router, "ties_to_higher_id": pin_router,
     "rmsnorm_no_eps": pin_layer, "down_proj_transposed": pin_layer,
+    "keys_top_only_k": pin_keys, "keys_top_by_score": pin_keys,
 }
 
 

@@ -235,6 +235,38 @@ def test_router_hot_set_and_scaling_options():
     assert np.allclose(w0, s.astype(np.float64) * 2.5, rtol=1e-6)
 
 
+def _keys_top_by_sort(d, logits, bias):
+    """The K+1 largest keys per token by a numpy sort of s + bias (fp32),
+    -inf padded when the layer has only K experts."""
+    _, key = _keys_from_logits(logits, bias)
+    top = -np.sort(-key, axis=1)[:, : d.top_k + 1]
+    if top.shape[1] < d.top_k + 1:
+        top = np.concatenate([top, np.full((top.shape[0], d.top_k + 1 - top.shape[1]), -np.inf, np.float32)], 1)
+    return top
+
+
+@pytest.mark.parametrize("dims", [TINY, LayerDims(hidden=128, latent=128, n_experts=8, top_k=8, inter=128),
+                                  LayerDims(hidden=128, latent=128, n_experts=9, top_k=8, inter=128)],
+                         ids=["tiny", "k_equals_e", "k_plus_one_equals_e"])
+def test_route_keys_top_match_sort(dims):
+    """The K+1 keys the parity tests use as the routing-gap guard are the
+    K+1 largest of s + bias, descending, exactly (selection uses the biased
+    key, the (K+1)-th slot is filled, and -inf stands in when K == E)."""
+    d = dims
+    w = synth.layer_weights(d, seed=21)
+    x = synth.token_rows(d, 22, 300)
+    idx, _, logits, keys = ora.route(d, x, w["router_w"], w["router_bias"], want_keys=True)
+    ref = _keys_top_by_sort(d, logits, w["router_bias"])
+    assert np.array_equal(keys, ref)
+    # the first K keys are those of the selected experts, in the selection order
+    _, key = _keys_from_logits(logits, w["router_bias"])
+    assert np.array_equal(keys[:, : d.top_k], np.take_along_axis(key, idx, 1))
+    gap = keys[:, d.top_k - 1].astype(np.float64) - keys[:, d.top_k].astype(np.float64)
+    assert np.all(gap >= 0)
+    if d.top_k == d.n_experts:
+        assert np.all(np.isinf(gap))
+
+
 def test_router_logits_match_library_matmul():
     d = TINY
     w = synth.layer_weights(d, seed=1)
