@@ -23,6 +23,12 @@ class LayerDims:
     rms_eps: float = 1e-6
     routed_scaling: float = 1.0
     norm_topk: int = 1
+    # shared experts on the residual (0 = the routed path alone); K3 has 2,
+    # each with intermediate 3072 (kimi-k3-mlx README, "Architecture" table
+    # and "Parameter budget": 12.2 B shared-expert parameters over 92 MoE
+    # layers = 3 x 7168 x 6144 per layer)
+    n_shared: int = 0
+    shared_inter: int = 0
 
     def with_(self, **kw) -> "LayerDims":
         return replace(self, **kw)
@@ -40,6 +46,15 @@ class LayerDims:
     def expert_down_bytes(self) -> int:
         return self.latent * self.inter // 2 + self.latent * self.inter // self.group
 
+    @property
+    def shared_total(self) -> int:
+        """Concatenated intermediate of the shared experts."""
+        return self.n_shared * self.shared_inter
+
+    def shared_bytes(self) -> int:
+        """bf16 gate, up and down weights of the shared experts."""
+        return 3 * self.hidden * self.shared_total * 2
+
     def dense_bytes(self) -> int:
         """Router weight + bias, down_proj, up_proj and the RMSNorm weight."""
         return (self.n_experts * self.hidden * 2 + self.n_experts * 4 + self.latent * self.hidden * 2
@@ -49,11 +64,17 @@ class LayerDims:
     def expert_flop_per_token(self) -> int:
         return self.top_k * (2 * self.latent * 2 * self.inter + 2 * self.inter * self.latent)
 
+    def shared_flop_per_token(self) -> int:
+        return 3 * 2 * self.hidden * self.shared_total
+
     def flop_per_token(self) -> int:
         router = 2 * self.n_experts * self.hidden
         proj = 2 * 2 * self.latent * self.hidden
-        return router + proj + self.expert_flop_per_token()
+        return router + proj + self.expert_flop_per_token() + self.shared_flop_per_token()
 
 
 TINY = LayerDims(hidden=1024, latent=512, n_experts=64, top_k=8, inter=384)
 K3 = LayerDims(hidden=7168, latent=3584, n_experts=896, top_k=16, inter=3072)
+# the K3 MoE block: the routed layer plus its two shared experts
+K3_SHARED = K3.with_(n_shared=2, shared_inter=3072)
+TINY_SHARED = TINY.with_(n_shared=2, shared_inter=384)

@@ -9,6 +9,8 @@ seed; every tensor has its own counter stream):
   up_proj      ~ N(0, 1/L) bf16                     [H, L]
   norm_w       ~ 1 + N(0, 0.02) bf16                [L]
   w1/w3/w2 packed bytes uniform over 0..255; e8m0 scale bytes uniform in 118..124.
+  shared experts (when the dims have them; Is = n_shared * shared_inter):
+  shared_w1, shared_w3 ~ N(0, 1/H) bf16 [Is, H]; shared_w2 ~ N(0, 1/Is) bf16 [H, Is].
 """
 from __future__ import annotations
 
@@ -32,6 +34,7 @@ SYNTH_GCC_FLAGS = ["-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off", "
 S_ROUTER_W, S_BIAS, S_DOWN, S_UP, S_GAMMA = 1, 2, 3, 4, 5
 S_W1P, S_W1S, S_W3P, S_W3S, S_W2P, S_W2S = 6, 7, 8, 9, 10, 11
 S_HOT = 12
+S_SW1, S_SW3, S_SW2 = 13, 14, 15
 S_X = 1000
 SCALE_LO, SCALE_HI = 118, 124
 
@@ -116,6 +119,11 @@ def layer_weights(d: LayerDims, seed: int, n_hot: int = 0, hot_bias: float = 2.0
     }
     if n_hot:
         w["router_bias"][hot_experts(d, seed, n_hot)] = np.float32(hot_bias)
+    if d.n_shared:
+        Is = d.shared_total
+        w["shared_w1"] = bf16_normal(seed, S_SW1, (Is, H), 0.0, 1.0 / np.sqrt(H))
+        w["shared_w3"] = bf16_normal(seed, S_SW3, (Is, H), 0.0, 1.0 / np.sqrt(H))
+        w["shared_w2"] = bf16_normal(seed, S_SW2, (H, Is), 0.0, 1.0 / np.sqrt(Is))
     return w
 
 

@@ -33,6 +33,13 @@
  *       [3072,112]; w2 packed [3584,1536] with scale [3584,96]; group 32.
  *   [K3_ARTIFACT_AUDIT] section 6: router weight [896,7168] bf16 and an fp32
  *       correction bias [896] per MoE layer.
+ *   [kimi-k3-mlx README] "Architecture" table: 2 shared experts on every
+ *       token; "Porting notes" item 3: the shared experts act on the residual,
+ *       not the latent; "Parameter budget": 12.2 B shared-expert parameters
+ *       (92 MoE layers x 3 x 7168 x 6144, i.e. two experts of intermediate
+ *       3072).  Reading: each shared expert is a bf16 SiTU-GLU MLP; the two
+ *       are summed (one MLP over their concatenated intermediate), rounded
+ *       to bf16 once, and added to the routed branch's bf16 output.
  * Readings where the pages are silent (w1 = gate, w3 = up; bias used for
  * selection only; optional renormalisation and routed scaling factor; ties
  * to the lower expert id; OCP e2m1/e8m0 value tables) are the ones listed
@@ -53,6 +60,7 @@ typedef struct {
   int hidden, latent, n_experts, top_k, inter, group;
   double beta, beta_lin, rms_eps, routed_scaling;
   int norm_topk;
+  int n_shared, shared_inter; /* shared experts (0 = none) and each one's intermediate */
 } ora_dims;
 
 /* Host arrays in checkpoint layout (experts stacked along dim 0). */
@@ -68,6 +76,11 @@ typedef struct {
   const uint8_t* w2_scale;    /* [E,L,I/32] */
   const uint16_t* norm_w;     /* [L] bf16 */
   const uint16_t* up_proj;    /* [H,L] bf16 */
+  /* shared experts, bf16, Is = n_shared * shared_inter (expert s owns
+   * intermediate rows [s*shared_inter, (s+1)*shared_inter)) */
+  const uint16_t* shared_w1;  /* [Is,H] gate */
+  const uint16_t* shared_w3;  /* [Is,H] up */
+  const uint16_t* shared_w2;  /* [H,Is] down */
 } ora_weights;
 
 /* ------------------------------------------------------------------ */
@@ -214,6 +227,8 @@ typedef struct {
   double* o;         /* [K, L]   optional */
   double* c;         /* [L]      optional */
   uint16_t* n;       /* [L]      optional */
+  uint16_t* hs;      /* [Is]     optional, shared experts' SiTU-GLU output */
+  uint16_t* z;       /* [H]      optional, shared experts' output */
 } ora_token_probe;
 
 static void ora_forward_token(const ora_dims* d, const ora_weights* W, const uint16_t* x,
@@ -282,6 +297,34 @@ static void ora_forward_token(const ora_dims* d, const ora_weights* W, const uin
     y[j] = ora_bf16_from_double(acc);
   }
 
+  /* 6. shared experts, on the 7168-d residual x itself (not the latent):
+   *    each is a SiTU-GLU MLP; their sum is one MLP over the concatenated
+   *    intermediate, gs = W1s . x, us = W3s . x, hs = bf16(SiTU(gs, us)),
+   *    z = bf16(W2s . hs); the block output is y = bf16(y_routed + z). */
+  if (d->n_shared > 0) {
+    const int Is = d->n_shared * d->shared_inter;
+    uint16_t* hs = (uint16_t*)malloc(sizeof(uint16_t) * Is);
+    for (int j = 0; j < Is; ++j) {
+      double gs = 0.0, us = 0.0;
+      for (int i = 0; i < H; ++i) {
+        double a = ora_bf16_to_double(x[i]);
+        gs += ora_bf16_to_double(W->shared_w1[(size_t)j * H + i]) * a;
+        us += ora_bf16_to_double(W->shared_w3[(size_t)j * H + i]) * a;
+      }
+      hs[j] = ora_bf16_from_double(ora_situ_glu(gs, us, d->beta, d->beta_lin));
+    }
+    for (int i = 0; i < H; ++i) {
+      double acc = 0.0;
+      for (int j = 0; j < Is; ++j)
+        acc += ora_bf16_to_double(W->shared_w2[(size_t)i * Is + j]) * ora_bf16_to_double(hs[j]);
+      uint16_t z = ora_bf16_from_double(acc);
+      if (p && p->z) p->z[i] = z;
+      y[i] = ora_bf16_from_double(ora_bf16_to_double(y[i]) + ora_bf16_to_double(z));
+    }
+    if (p && p->hs) memcpy(p->hs, hs, sizeof(uint16_t) * Is);
+    free(hs);
+  }
+
   if (p) {
     if (p->logits) memcpy(p->logits, logits, sizeof(float) * E);
     if (p->lat) memcpy(p->lat, lat, sizeof(uint16_t) * L);
@@ -298,11 +341,12 @@ static void ora_forward_token(const ora_dims* d, const ora_weights* W, const uin
 /* T tokens; tokens are independent, so they are spread over threads.
  * Optional per-token outputs are strided by token (NULL to skip):
  *   logits [T,E] f32, lat [T,L] bf16, h [T,K,I] bf16, o [T,K,L] f64,
- *   c [T,L] f64, n [T,L] bf16. */
+ *   c [T,L] f64, n [T,L] bf16, hs [T,Is] bf16, z [T,H] bf16. */
 void ora_forward(const ora_dims* d, const ora_weights* W, const uint16_t* x, int T, uint16_t* y,
                  int32_t* idx, float* w, float* logits, uint16_t* lat, uint16_t* h, double* o,
-                 double* c, uint16_t* n) {
+                 double* c, uint16_t* n, uint16_t* hs, uint16_t* z) {
   const int H = d->hidden, L = d->latent, E = d->n_experts, K = d->top_k, I = d->inter;
+  const int Is = d->n_shared * d->shared_inter;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int t = 0; t < T; ++t) {
     ora_token_probe p;
@@ -312,6 +356,8 @@ void ora_forward(const ora_dims* d, const ora_weights* W, const uint16_t* x, int
     p.o = o ? o + (size_t)t * K * L : NULL;
     p.c = c ? c + (size_t)t * L : NULL;
     p.n = n ? n + (size_t)t * L : NULL;
+    p.hs = hs ? hs + (size_t)t * Is : NULL;
+    p.z = z ? z + (size_t)t * H : NULL;
     ora_forward_token(d, W, x + (size_t)t * H, y + (size_t)t * H, idx + (size_t)t * K,
                       w + (size_t)t * K, &p);
   }

@@ -36,13 +36,14 @@ class OraDims(C.Structure):
         ("inter", C.c_int), ("group", C.c_int),
         ("beta", C.c_double), ("beta_lin", C.c_double), ("rms_eps", C.c_double),
         ("routed_scaling", C.c_double), ("norm_topk", C.c_int),
+        ("n_shared", C.c_int), ("shared_inter", C.c_int),
     ]
 
 
 class OraWeights(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in (
         "router_w", "router_bias", "down_proj", "w1_packed", "w1_scale", "w3_packed", "w3_scale",
-        "w2_packed", "w2_scale", "norm_w", "up_proj")]
+        "w2_packed", "w2_scale", "norm_w", "up_proj", "shared_w1", "shared_w3", "shared_w2")]
 
 
 def lib():
@@ -69,7 +70,7 @@ def lib():
             L.ora_mxfp4_dequant_bf16.argtypes = [vp, vp, i32, i32, vp]
             L.ora_forward.restype = None
             L.ora_forward.argtypes = [C.POINTER(OraDims), C.POINTER(OraWeights), vp, i32, vp, vp, vp,
-                                      vp, vp, vp, vp, vp, vp]
+                                      vp, vp, vp, vp, vp, vp, vp, vp]
             L.ora_route.restype = None
             L.ora_route.argtypes = [C.POINTER(OraDims), vp, i32, vp, vp, vp, vp, vp, vp]
             L.ora_route_from_logits.restype = None
@@ -88,19 +89,25 @@ def _p(a):
 def dims_struct(d) -> OraDims:
     """`d` is any object with the LayerDims attribute names."""
     return OraDims(d.hidden, d.latent, d.n_experts, d.top_k, d.inter, d.group, float(d.beta),
-                   float(d.beta_lin), float(d.rms_eps), float(d.routed_scaling), int(d.norm_topk))
+                   float(d.beta_lin), float(d.rms_eps), float(d.routed_scaling), int(d.norm_topk),
+                   int(getattr(d, "n_shared", 0)), int(getattr(d, "shared_inter", 0)))
 
 
 _WEIGHT_DTYPES = {
     "router_w": np.uint16, "router_bias": np.float32, "down_proj": np.uint16,
     "w1_packed": np.uint8, "w1_scale": np.uint8, "w3_packed": np.uint8, "w3_scale": np.uint8,
     "w2_packed": np.uint8, "w2_scale": np.uint8, "norm_w": np.uint16, "up_proj": np.uint16,
+    "shared_w1": np.uint16, "shared_w3": np.uint16, "shared_w2": np.uint16,
 }
+_OPTIONAL = ("shared_w1", "shared_w3", "shared_w2")
 
 
 def weights_struct(w: dict) -> OraWeights:
     s = OraWeights()
     for name, dt in _WEIGHT_DTYPES.items():
+        if name in _OPTIONAL and name not in w:
+            setattr(s, name, None)
+            continue
         a = w[name]
         assert a.dtype == dt and a.flags.c_contiguous, name
         setattr(s, name, a.ctypes.data)
@@ -175,7 +182,8 @@ def route_from_logits(dims, logits: np.ndarray, bias: np.ndarray):
 
 def forward(dims, weights: dict, x: np.ndarray, probes: bool = False) -> dict:
     """The whole layer for every row of x.  Returns y, idx, w and, with
-    probes=True, the intermediates logits, lat, h [T,K,I], o [T,K,L], c, n."""
+    probes=True, the intermediates logits, lat, h [T,K,I], o [T,K,L], c, n
+    and, for dims with shared experts, hs [T,Is] and z [T,H]."""
     x = np.ascontiguousarray(x, dtype=np.uint16)
     T = x.shape[0]
     H, L, E, K, I = dims.hidden, dims.latent, dims.n_experts, dims.top_k, dims.inter
@@ -188,10 +196,16 @@ def forward(dims, weights: dict, x: np.ndarray, probes: bool = False) -> dict:
         out.update(logits=np.empty((T, E), np.float32), lat=np.empty((T, L), np.uint16),
                    h=np.empty((T, K, I), np.uint16), o=np.empty((T, K, L), np.float64),
                    c=np.empty((T, L), np.float64), n=np.empty((T, L), np.uint16))
+        Is = getattr(dims, "n_shared", 0) * getattr(dims, "shared_inter", 0)
+        if Is:
+            out.update(hs=np.empty((T, Is), np.uint16), z=np.empty((T, H), np.uint16))
+    if getattr(dims, "n_shared", 0):
+        assert all(n in weights for n in _OPTIONAL), "dims with shared experts need shared_w1/w3/w2"
     ds, ws = dims_struct(dims), weights_struct(weights)
     g = out.get
     lib().ora_forward(C.byref(ds), C.byref(ws), _p(x), T, _p(out["y"]), _p(out["idx"]), _p(out["w"]),
-                      _p(g("logits")), _p(g("lat")), _p(g("h")), _p(g("o")), _p(g("c")), _p(g("n")))
+                      _p(g("logits")), _p(g("lat")), _p(g("h")), _p(g("o")), _p(g("c")), _p(g("n")),
+                      _p(g("hs")), _p(g("z")))
     return out
 
 

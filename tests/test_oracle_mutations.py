@@ -8,7 +8,8 @@ the wrong nibble first, the wrong exponent bias, swapped SiTU temperatures,
 the bias leaking into the weights, ties to the higher id, a dropped RMSNorm
 epsilon, a transposed down projection, and two slips in the K+1 routing
 keys that guard the parity inputs' routing gap (only K keys written,
-ranking by the unbiased score).
+ranking by the unbiased score), and two in the shared experts (fed the
+latent instead of the residual, gate and up weights swapped).
 """
 import ctypes as C
 import math
@@ -41,6 +42,10 @@ MUTATIONS = {
                         "for (int k = 0; k < K; ++k) {\n        if (k >= E) {"),
     "keys_top_by_score": ("float ke = s[e] + bias[e], kb = best < 0 ? 0.f : s[best] + bias[best];",
                           "float ke = s[e], kb = best < 0 ? 0.f : s[best];"),
+    "shared_on_latent": ("        double a = ora_bf16_to_double(x[i]);\n        gs +=",
+                         "        double a = ora_bf16_to_double(lat[i % L]);\n        gs +="),
+    "shared_gate_up_swapped": ("        gs += ora_bf16_to_double(W->shared_w1[",
+                               "        gs += ora_bf16_to_double(W->shared_w3["),
     "down_proj_transposed": ("acc += ora_bf16_to_double(W->down_proj[(size_t)l * H + j]) * ora_bf16_to_double(x[j]);",
                              "acc += ora_bf16_to_double(W->down_proj[(size_t)j * L + l]) * ora_bf16_to_double(x[j]);"),
 }
@@ -65,7 +70,7 @@ def build_variant(tmp, name):
     L.ora_route_from_logits.argtypes = [C.POINTER(ora.OraDims)] + [C.c_void_p] * 5
     L.ora_route.argtypes = [C.POINTER(ora.OraDims), C.c_void_p, C.c_int] + [C.c_void_p] * 6
     L.ora_forward.argtypes = [C.POINTER(ora.OraDims), C.POINTER(ora.OraWeights)] + [C.c_void_p, C.c_int] + \
-        [C.c_void_p] * 9
+        [C.c_void_p] * 11
     return L
 
 
@@ -129,6 +134,25 @@ def pin_keys(L):
     return bool(np.array_equal(keys, -np.sort(-key, axis=1)[:, : K + 1]))
 
 
+def pin_shared(L):
+    """The shared experts against the numpy per-expert formulation."""
+    from test_oracle_pins import np_shared
+    d = LayerDims(hidden=128, latent=128, n_experts=8, top_k=2, inter=128, n_shared=2, shared_inter=64)
+    w = synth.layer_weights(d, seed=14)
+    x = synth.token_rows(d, 15, 3)
+    T = 3
+    y = np.empty((T, d.hidden), np.uint16)
+    idx = np.empty((T, d.top_k), np.int32)
+    wt = np.empty((T, d.top_k), np.float32)
+    z = np.empty((T, d.hidden), np.uint16)
+    ds, ws = ora.dims_struct(d), ora.weights_struct(w)
+    L.ora_forward(C.byref(ds), C.byref(ws), x.ctypes.data, T, y.ctypes.data, idx.ctypes.data, wt.ctypes.data,
+                  None, None, None, None, None, None, None, z.ctypes.data)
+    _, zr = np_shared(d, w, x)
+    zo = ora.bf16_to_float(z)
+    return bool(np.max(np.abs(zo - zr)) <= 2 ** -7 * np.abs(zr).max())
+
+
 def pin_layer(L):
     """Against the independent numpy formulation in test_oracle_pins."""
     from test_oracle_pins import np_layer
@@ -145,7 +169,7 @@ def pin_layer(L):
     n = np.empty((T, d.latent), np.uint16)
     ds, ws = ora.dims_struct(d), ora.weights_struct(w)
     L.ora_forward(C.byref(ds), C.byref(ws), x.ctypes.data, T, y.ctypes.data, idx.ctypes.data, wt.ctypes.data,
-                  None, None, None, None, c.ctypes.data, n.ctypes.data)
+                  None, None, None, None, c.ctypes.data, n.ctypes.data, None, None)
     assert 0.1 < d.rms_eps / np.mean(ref["c"] ** 2) < 10
     yf, nf = ora.bf16_to_float(y), ora.bf16_to_float(n)
     return bool(np.abs(c - ref["c"]).max() < 1e-9 * np.abs(ref["c"]).max()
@@ -158,6 +182,7 @@ PIN_OF = {
     "situ_betas_swapped": pin_situ, "bias_in_weights": pin_router, "ties_to_higher_id": pin_router,
     "rmsnorm_no_eps": pin_layer, "down_proj_transposed": pin_layer,
     "keys_top_only_k": pin_keys, "keys_top_by_score": pin_keys,
+    "shared_on_latent": pin_shared, "shared_gate_up_swapped": pin_shared,
 }
 
 

@@ -401,6 +401,77 @@ def test_brute_force_tiny_layer_pure_python():
         assert np.allclose(bits_to_f64(out["y"][t]), y, rtol=1e-2, atol=1e-2)
 
 
+# ----------------------------------------------------------------------------- shared experts
+def np_shared(d, w, x):
+    """The shared experts in numpy fp64, one expert at a time, their outputs
+    summed before the single bf16 rounding of the block's shared branch."""
+    xf = bits_to_f64(x)
+    Ie = d.shared_inter
+    zsum = np.zeros((x.shape[0], d.hidden))
+    hs = []
+    for e in range(d.n_shared):
+        rows = slice(e * Ie, (e + 1) * Ie)
+        g = xf @ bits_to_f64(w["shared_w1"][rows]).T
+        u = xf @ bits_to_f64(w["shared_w3"][rows]).T
+        h = np_bf16(4 * np.tanh(g / 4) / (1 + np.exp(-g)) * 25 * np.tanh(u / 25))
+        hs.append(h)
+        zsum += h @ bits_to_f64(w["shared_w2"][:, rows]).T
+    return np.concatenate(hs, axis=1), np_bf16(zsum)
+
+
+@pytest.fixture(scope="module")
+def shared_case():
+    from mxfp4_routed_expert_k3_gb300.dims import TINY_SHARED
+    d = TINY_SHARED
+    w = synth.layer_weights(d, seed=3)
+    x = synth.token_rows(d, 30, 6)
+    return d, w, x, ora.forward(d, w, x, probes=True)
+
+
+def test_shared_experts_match_numpy_per_expert_sum(shared_case):
+    """Shared experts act on the residual x (not the latent), each a SiTU-GLU
+    MLP; z = bf16(sum of the experts' outputs) and y = bf16(y_routed + z)."""
+    d, w, x, out = shared_case
+    hs, z = np_shared(d, w, x)
+    assert np.mean(bits_to_f64(out["hs"]) == hs) > 0.999
+    zo = bits_to_f64(out["z"])
+    assert np.mean(zo == z) > 0.999
+    assert np.max(np.abs(zo - z)) <= 2 ** -7 * np.abs(z).max()
+    routed = ora.forward(d.with_(n_shared=0, shared_inter=0), w, x)
+    y = np_bf16(bits_to_f64(routed["y"]) + zo)
+    assert np.array_equal(bits_to_f64(out["y"]), y)
+    # the shared branch is a sizeable part of the output on these inputs
+    assert np.sqrt(np.mean(zo ** 2)) > 0.1 * np.sqrt(np.mean(bits_to_f64(routed["y"]) ** 2))
+
+
+def test_shared_experts_zero_weights_leave_routed_output(shared_case):
+    d, w, x, _ = shared_case
+    w0 = dict(w)
+    for n in ("shared_w1", "shared_w3", "shared_w2"):
+        w0[n] = np.zeros_like(w[n])
+    a = ora.forward(d, w0, x)
+    b = ora.forward(d.with_(n_shared=0, shared_inter=0), w, x)
+    assert np.array_equal(a["y"], b["y"])
+    assert np.array_equal(a["idx"], b["idx"])
+
+
+def test_shared_experts_brute_force_pure_python():
+    d = LayerDims(hidden=64, latent=64, n_experts=4, top_k=2, inter=64, n_shared=2, shared_inter=32)
+    w = synth.layer_weights(d, seed=6)
+    x = synth.token_rows(d, 66, 1)
+    out = ora.forward(d, w, x, probes=True)
+    f = lambda b: float(bits_to_f64(np.uint16(b)))
+    xs = [f(v) for v in x[0]]
+    hs = []
+    for j in range(64):
+        g = math.fsum(f(w["shared_w1"][j, i]) * xs[i] for i in range(64))
+        u = math.fsum(f(w["shared_w3"][j, i]) * xs[i] for i in range(64))
+        hs.append(bf16_rne_py(4 * math.tanh(g / 4) / (1 + math.exp(-g)) * 25 * math.tanh(u / 25)))
+    assert [bits_to_f64(v) for v in out["hs"][0]] == hs
+    z = [bf16_rne_py(math.fsum(f(w["shared_w2"][i, j]) * hs[j] for j in range(64))) for i in range(64)]
+    assert [bits_to_f64(v) for v in out["z"][0]] == z
+
+
 # ----------------------------------------------------------------------------- work counts
 def test_page_byte_figures(golden):
     g = golden["expert_tensors"]
