@@ -64,6 +64,30 @@ struct Cfg {
   static_assert(kNumA * kAcc * kAccStride <= kTmemCols || MODE == GATEUP, "TMEM budget");
 };
 
+// One output element of a dense projection (DenseOut, glu == 0).
+__device__ __forceinline__ void dense_store1(const DenseOut& o, int M, int t, int m, float v) {
+  if (m < o.split) {
+    o.out_f32[(size_t)t * o.split + m] = v;
+  } else {
+    const size_t i = (size_t)t * (M - o.split) + (m - o.split);
+    uint16_t b = f32_to_bf16(v);
+    if (o.add_bf16) b = f32_to_bf16(bf16_to_f32(b) + bf16_to_f32(o.add_bf16[i]));
+    o.out_bf16[i] = b;
+  }
+}
+// Rows m..m+3 (m % 4 == 0) of token t.
+__device__ __forceinline__ void dense_store4(const DenseOut& o, int M, int t, int m, float4 a) {
+  if (o.glu) {
+    const uint32_t h = pack_bf16x2(situ_fast(a.x, a.y, o.beta, o.beta_lin), situ_fast(a.z, a.w, o.beta, o.beta_lin));
+    *reinterpret_cast<uint32_t*>(o.out_bf16 + (size_t)t * (M >> 1) + (m >> 1)) = h;
+    return;
+  }
+  dense_store1(o, M, t, m, a.x);
+  dense_store1(o, M, t, m + 1, a.y);
+  dense_store1(o, M, t, m + 2, a.z);
+  dense_store1(o, M, t, m + 3, a.w);
+}
+
 // Per-tile description for grouped GEMMs: x = expert, y = first row (slot),
 // z = valid rows, w = MMA N (rows rounded up to 16).
 struct TileList {
@@ -81,9 +105,9 @@ struct Params {
   TileList list;           // GATEUP / DOWN
   int T, tn;               // DENSE: tokens and rows per tile
   // epilogue
-  int split;               // DENSE: rows below -> fp32 out_f32, others -> bf16 out_bf16
-  float* out_f32;
-  uint16_t* out_bf16;
+  DenseOut dout;           // DENSE
+  float* out_f32;          // DOWN: o per slot
+  uint16_t* out_bf16;      // GATEUP: h per slot
   int ld_out;              // GATEUP: I, DOWN: L (row length of h / o)
   float beta, beta_lin;
   unsigned* status;
@@ -260,18 +284,20 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (j0 + j < rows) p.out_f32[(size_t)(row0 + j0 + j) * p.ld_out + m] = acc[j];
+        } else if (p.dout.glu) {
+          // gate/up row pairs sit in neighbouring lanes of this warp
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float partner = __shfl_xor_sync(0xFFFFFFFFu, acc[j], 1);
+            if (!(m & 1) && m < p.M && j0 + j < rows)
+              p.dout.out_bf16[(size_t)(row0 + j0 + j) * (p.M >> 1) + (m >> 1)] =
+                  f32_to_bf16(situ_fast(acc[j], partner, p.dout.beta, p.dout.beta_lin));
+          }
         } else {
           if (m < p.M) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (j0 + j < rows) {
-                const size_t t = (size_t)(row0 + j0 + j);
-                if (m < p.split)
-                  p.out_f32[t * p.split + m] = acc[j];
-                else
-                  p.out_bf16[t * (p.M - p.split) + (m - p.split)] = f32_to_bf16(acc[j]);
-              }
-            }
+            for (int j = 0; j < 32; ++j)
+              if (j0 + j < rows) dense_store1(p.dout, p.M, row0 + j0 + j, m, acc[j]);
           }
         }
       }
@@ -522,9 +548,10 @@ __global__ void __launch_bounds__(kSThreads, 2) umma_stream_kernel(const __grid_
 // [M, K] (the weights, M side) and X bf16 [T <= 64, K] (N side).  Work items
 // are (128-row tile, K chunk) so that every SM streams weights even though
 // M / 128 is small (35 tiles for router + down_proj); each item writes its
-// fp32 partial sums to part[chunk][t][m] and splitk_reduce_kernel adds the
-// chunks in order.  A and B come by 2-D TMA (128-byte swizzle); D is double
-// buffered in TMEM so the epilogue of one item overlaps the next item's MMAs.
+// fp32 partial sums to part[chunk][t][m], and dense_reduce_kernel (launched
+// right after, programmatic dependent launch) adds the chunks in order over
+// all SMs.  A and B come by 2-D TMA (128-byte swizzle); D is double buffered
+// in TMEM so the epilogue of one item overlaps the next item's MMAs.
 // =====================================================================
 constexpr int kDNB = 64;  // max tokens
 struct DCfg {
@@ -536,12 +563,9 @@ struct DCfg {
 };
 
 struct DenseStreamParams {
-  int MT, KS, nkc, ks_per_chunk, M, T, split;
+  int MT, KS, nkc, ks_per_chunk, M, T;
   uint32_t b_bytes;  // bytes of one token-row box: 128 x (T rounded up to 16)
-  float* part;     // [nkc][T][M] fp32 partial sums
-  int* counters;   // [MT][4] chunks finished per row tile and warp (zero between calls)
-  float* out_f32;  // rows m < split: out_f32[t * split + m]
-  uint16_t* out_bf16;  // rows m >= split: bf16 out_bf16[t * (M - split) + m - split]
+  float* part;       // [nkc][T][M] fp32 partial sums
   unsigned* status;
   uint64_t limit_ns;
 };
@@ -669,61 +693,44 @@ __global__ void __launch_bounds__(kDThreads, 1) umma_dense_stream_kernel(const _
       }
       tc_fence_before();
       mbar_arrive(tempty(buf));
-      // The last chunk to finish adds the chunks in order.  Counting is per
-      // warp (32 rows each), so no warp ever waits for another; whoever comes
-      // last does the sum.
-      __threadfence();
-      __syncwarp();
-      int last = 0;
-      if (lane == 0) {
-        int* cnt = p.counters + mt * 4 + quarter;
-        last = (atomicAdd(cnt, 1) == p.nkc - 1) ? 1 : 0;
-        if (last) *cnt = 0;  // ready for the next call
-      }
-      last = __shfl_sync(0xFFFFFFFFu, last, 0);
-      if (last) {
-        __threadfence();
-        if (m < p.M) {
-          for (int t0 = 0; t0 < p.T; t0 += 8) {
-            // eight tokens x eight chunks of loads in flight (the sum is
-            // latency-bound otherwise); chunks added in order
-            float v[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = 0.f;
-            for (int c0 = 0; c0 < p.nkc; c0 += 8) {
-              float x[8][8];
-#pragma unroll
-              for (int cc = 0; cc < 8; ++cc) {
-                const float* src = p.part + ((size_t)(c0 + cc) * p.T + t0) * p.M + m;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                  x[cc][i] = (c0 + cc < p.nkc && t0 + i < p.T) ? __ldcg(src + (size_t)i * p.M) : 0.f;
-              }
-#pragma unroll
-              for (int cc = 0; cc < 8; ++cc)
-                if (c0 + cc < p.nkc) {
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) v[i] += x[cc][i];
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int t = t0 + i;
-              if (t >= p.T) break;
-              if (m < p.split)
-                p.out_f32[(size_t)t * p.split + m] = v[i];
-              else
-                p.out_bf16[(size_t)t * (p.M - p.split) + (m - p.split)] = f32_to_bf16(v[i]);
-            }
-          }
-        }
-      }
     }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+// Ordered split-K reduction: D[t, m] = sum over chunks c = 0, 1, ... of
+// part[c][t][m] (fp32, chunk order fixed, so results do not depend on
+// scheduling), then the dense output rule (DenseOut).  One thread per four
+// consecutive rows of one token; all chunk loads of a thread are issued
+// before the sum.
+constexpr int kReduceMaxChunks = 16;
+__global__ void __launch_bounds__(256) dense_reduce_kernel(const float* __restrict__ part, int nkc, int T, int M,
+                                                           DenseOut o) {
+  pdl_trigger();
+  pdl_wait();
+  const int M4 = M >> 2;
+  const long long total = (long long)T * M4;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(i / M4), m = (int)(i % M4) * 4;
+    float4 v[kReduceMaxChunks];
+#pragma unroll
+    for (int c = 0; c < kReduceMaxChunks; ++c)
+      if (c < nkc) v[c] = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)c * T + t) * M + m));
+    float4 a = v[0];
+#pragma unroll
+    for (int c = 1; c < kReduceMaxChunks; ++c)
+      if (c < nkc) {
+        a.x += v[c].x;
+        a.y += v[c].y;
+        a.z += v[c].z;
+        a.w += v[c].w;
+      }
+    dense_store4(o, M, t, m, a);
+  }
 }
 
 // ------------------------------------------------------------------ helpers
@@ -820,17 +827,16 @@ struct UmmaWs {
   int* count;
   uint16_t* lat_perm;
   float* part;
-  int* counters;
 };
 
-constexpr int kMaxChunks = 16;  // split-K chunks of the small-T dense GEMM
+constexpr int kMaxChunks = kReduceMaxChunks;  // split-K chunks of the small-T dense GEMM
 
 // Workspace carve-up; sizes are bounds for any T <= max_tokens:
 //   tiles: at most T*K/kSNB + (experts with work) entries (kSNB is the
 //          smallest tile height used), lat_perm: T*K rows of L,
 //   part : kMaxChunks * kDNB * max(E + L, H) fp32 partial sums.
 struct WsLayout {
-  size_t tiles_off, count_off, lat_off, part_off, counters_off, total;
+  size_t tiles_off, count_off, lat_off, part_off, total;
 };
 WsLayout ws_layout(const Dims& d, int max_tokens) {
   auto up = [](size_t v) { return (v + 255) / 256 * 256; };
@@ -842,8 +848,7 @@ WsLayout ws_layout(const Dims& d, int max_tokens) {
   l.count_off = up(max_tiles * sizeof(int4));
   l.lat_off = l.count_off + 256;
   l.part_off = l.lat_off + up((size_t)max_tokens * d.K * d.L * 2);
-  l.counters_off = l.part_off + up((size_t)kMaxChunks * kDNB * std::max(d.E + d.L, d.H) * sizeof(float));
-  l.total = l.counters_off + up((size_t)(std::max(d.E + d.L, d.H) / kBM + 2) * 4 * sizeof(int));
+  l.total = l.part_off + up(dense_small_part_floats(std::max(d.E + d.L, d.H)) * sizeof(float));
   return l;
 }
 
@@ -855,7 +860,6 @@ UmmaWs ws_view(const UmmaPlan& p, const Dims& d, int max_tokens) {
   w.count = reinterpret_cast<int*>(b + l.count_off);
   w.lat_perm = reinterpret_cast<uint16_t*>(b + l.lat_off);
   w.part = reinterpret_cast<float*>(b + l.part_off);
-  w.counters = reinterpret_cast<int*>(b + l.counters_off);
   return w;
 }
 
@@ -904,9 +908,10 @@ bool umma_path_enabled(const UmmaPlan& p, const Dims&, int T) { return p.enabled
 int umma_dense_launches() { return 1; }
 int umma_expert_launches() { return 4; }
 
-cudaError_t umma_dense(const UmmaPlan& p, const uint16_t* W, int M, int K, const uint16_t* X, int T, int split,
-                       float* out_f32, uint16_t* out_bf16, cudaStream_t s) {
+cudaError_t umma_dense(const UmmaPlan& p, const uint16_t* W, int M, int K, const uint16_t* X, int T,
+                       const DenseOut& o, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
+  if (o.glu && (M % 2 || !o.out_bf16)) return cudaErrorInvalidValue;
   CUtensorMap ma, mb;
   constexpr int BN = Cfg<DENSE>::kBN;
   if (!make_map(&ma, W, M, K, kBM) || !make_map(&mb, X, T, K, BN)) return cudaErrorInvalidValue;
@@ -918,9 +923,7 @@ cudaError_t umma_dense(const UmmaPlan& p, const uint16_t* W, int M, int K, const
   prm.M = M;
   prm.T = T;
   prm.tn = (per + 15) & ~15;
-  prm.split = split;
-  prm.out_f32 = out_f32;
-  prm.out_bf16 = out_bf16;
+  prm.dout = o;
   prm.status = p.status;
   prm.limit_ns = p.limit_ns;
   const int ny = (T + prm.tn - 1) / prm.tn;
@@ -997,11 +1000,6 @@ cudaError_t umma_stream_gather(const UmmaPlan& p, const Work& w, int T, const Di
   return cudaGetLastError();
 }
 
-cudaError_t umma_reset_counters(const UmmaPlan& p) {
-  const WsLayout l = ws_layout(p.dims, p.max_tokens);
-  return cudaMemset(static_cast<uint8_t*>(p.ws) + l.counters_off, 0, l.total - l.counters_off);
-}
-
 void umma_tile_list(const UmmaPlan& p, int4** tiles, int** count, int* bn_max) {
   UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
   *tiles = ws.tiles;
@@ -1056,11 +1054,17 @@ cudaError_t umma_stream_down(const UmmaPlan& p, const uint8_t* d_tiles, const Wo
 }
 
 // Small-T dense GEMM (T <= kDNB): split-K streaming kernel + ordered reduce.
-cudaError_t umma_dense_small(const UmmaPlan& p, const uint16_t* W, int M, int K, const uint16_t* X, int T, int split,
-                             float* out_f32, uint16_t* out_bf16, cudaStream_t s) {
+size_t dense_small_part_floats(int M) { return (size_t)kMaxChunks * kDNB * (size_t)M; }
+int umma_dense_small_launches() { return 2; }
+
+cudaError_t umma_dense_small(const UmmaPlan& p, const uint16_t* W, int M, int K, const uint16_t* X, int T,
+                             const DenseOut& o, float* part, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  if (T > kDNB) return cudaErrorInvalidValue;
-  UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
+  if (T > kDNB || M % 4 || (o.glu && !o.out_bf16)) return cudaErrorInvalidValue;
+  if (!part) {
+    if ((size_t)M > (size_t)std::max(p.dims.E + p.dims.L, p.dims.H)) return cudaErrorInvalidValue;
+    part = ws_view(p, p.dims, p.max_tokens).part;
+  }
   CUtensorMap ma, mb;
   const int n_mma = (T + 15) & ~15;  // token rows per box (the MMA's N)
   if (!make_map(&ma, W, M, K, kBM) || !make_map(&mb, X, T, K, n_mma)) return cudaErrorInvalidValue;
@@ -1076,15 +1080,16 @@ cudaError_t umma_dense_small(const UmmaPlan& p, const uint16_t* W, int M, int K,
   q.nkc = (q.KS + q.ks_per_chunk - 1) / q.ks_per_chunk;
   q.M = M;
   q.T = T;
-  q.split = split;
-  q.part = ws.part;
-  q.counters = ws.counters;
-  q.out_f32 = out_f32;
-  q.out_bf16 = out_bf16;
+  q.part = part;
   q.status = p.status;
   q.limit_ns = p.limit_ns;
   const int items = q.MT * q.nkc;
-  return launch_pdl(umma_dense_stream_kernel, std::min(items, 2 * p.num_sms), kDThreads, DCfg::kSmem, s, ma, mb, q);
+  cudaError_t e =
+      launch_pdl(umma_dense_stream_kernel, std::min(items, 2 * p.num_sms), kDThreads, DCfg::kSmem, s, ma, mb, q);
+  if (e != cudaSuccess) return e;
+  const long long threads = (long long)T * (M / 4);
+  const int blocks = (int)std::min<long long>((threads + 255) / 256, 8LL * p.num_sms);
+  return launch_pdl(dense_reduce_kernel, blocks, 256, 0, s, (const float*)part, q.nkc, T, M, o);
 }
 
 }  // namespace k3

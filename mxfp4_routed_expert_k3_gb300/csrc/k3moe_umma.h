@@ -10,6 +10,23 @@
 
 namespace k3 {
 
+// Where a dense projection's fp32 sums D[t, m] (t < T tokens, m < M weight
+// rows) go:
+//   glu == 0: rows m < split -> out_f32[t * split + m] (fp32);
+//             rows m >= split -> out_bf16[t * (M - split) + m - split] =
+//             bf16(D), or, with add_bf16, bf16(bf16(D) + add_bf16[same index]);
+//   glu == 1: the weight rows are gate/up pairs (row 2j gate, 2j + 1 up) and
+//             out_bf16[t * (M / 2) + j] = bf16(SiTU-GLU(D[t, 2j], D[t, 2j + 1]))
+//             with temperatures beta, beta_lin.
+struct DenseOut {
+  int split = 0;
+  float* out_f32 = nullptr;
+  uint16_t* out_bf16 = nullptr;
+  const uint16_t* add_bf16 = nullptr;
+  int glu = 0;
+  float beta = 4.f, beta_lin = 25.f;
+};
+
 struct UmmaPlan {
   bool enabled = false;   // false: every forward uses the CUDA-core kernels
   int min_tokens = 1 << 30;
@@ -25,13 +42,16 @@ struct UmmaPlan {
 cudaError_t prepare_umma_kernels();
 UmmaPlan umma_plan(const Dims& d, int max_tokens);
 bool umma_path_enabled(const UmmaPlan& p, const Dims& d, int T);
-cudaError_t umma_dense(const UmmaPlan& p, const uint16_t* W, int M, int K, const uint16_t* X, int T, int split,
-                       float* out_f32, uint16_t* out_bf16, cudaStream_t s);
+cudaError_t umma_dense(const UmmaPlan& p, const uint16_t* W, int M, int K, const uint16_t* X, int T,
+                       const DenseOut& o, cudaStream_t s);
 int umma_dense_launches();
-// T <= 64: split-K streaming dense GEMM over all SMs; the last chunk of each
-// row tile adds the chunks in order (one launch)
-cudaError_t umma_dense_small(const UmmaPlan& p, const uint16_t* W, int M, int K, const uint16_t* X, int T, int split,
-                             float* out_f32, uint16_t* out_bf16, cudaStream_t s);
+// T <= 64: split-K streaming dense GEMM over all SMs writing fp32 partials
+// to `part` (at least dense_small_part_floats(M) floats; a context's own
+// buffer when null), then an ordered reduction of the chunks (two launches)
+cudaError_t umma_dense_small(const UmmaPlan& p, const uint16_t* W, int M, int K, const uint16_t* X, int T,
+                             const DenseOut& o, float* part, cudaStream_t s);
+int umma_dense_small_launches();
+size_t dense_small_part_floats(int M);
 cudaError_t umma_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8_t* d_tiles, const Work& w, int T,
                          const Dims& d, cudaStream_t s);
 int umma_expert_launches();
@@ -41,7 +61,6 @@ cudaError_t umma_stream_tiles(const UmmaPlan& p, const Work& w, int T, const Dim
 cudaError_t umma_stream_gather(const UmmaPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s);
 // where the streaming kernels read their tile list (and the tile height)
 void umma_tile_list(const UmmaPlan& p, int4** tiles, int** count, int* bn_max);
-cudaError_t umma_reset_counters(const UmmaPlan& p);
 cudaError_t umma_stream_gateup(const UmmaPlan& p, const uint8_t* gu_tiles, const Work& w, int T, const Dims& d,
                                cudaStream_t s);
 cudaError_t umma_stream_down(const UmmaPlan& p, const uint8_t* d_tiles, const Work& w, int T, const Dims& d,
