@@ -402,6 +402,124 @@ void ora_route(const ora_dims* d, const uint16_t* x, int T, const uint16_t* rout
   }
 }
 
+/* Expert parallelism (Kimi-K3-Alis-MLX-Dynamic model card, "Performance"
+ * and "Usage": dense weights replicated, routed experts split between two
+ * machines).  Rank r holds experts [e_begin, e_begin + e_count); for every
+ * token it routes over all experts (the router is replicated) and forms the
+ * partial combine
+ *   c_r = sum over k in k order, for selected experts in its range, of w_k o_k
+ * (fp64 here).  The ranks' partials are summed (one all-reduce of [T, L];
+ * RMSNorm needs the whole combine), and ora_finish applies the rest of the
+ * block to the sum: RMSNorm, up_proj and the shared experts on x. */
+void ora_forward_partial(const ora_dims* d, const ora_weights* W, const uint16_t* x, int T, int e_begin,
+                         int e_count, double* c_out) {
+  const int H = d->hidden, L = d->latent, K = d->top_k;
+  double* o = (double*)malloc(sizeof(double) * (size_t)K * L);
+  uint16_t* y = (uint16_t*)malloc(sizeof(uint16_t) * H);
+  int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * K);
+  float* w = (float*)malloc(sizeof(float) * K);
+  for (int t = 0; t < T; ++t) {
+    ora_token_probe p;
+    memset(&p, 0, sizeof(p));
+    p.o = o;
+    ora_forward_token(d, W, x + (size_t)t * H, y, idx, w, &p);
+    double* c = c_out + (size_t)t * L;
+    for (int l = 0; l < L; ++l) c[l] = 0.0;
+    for (int k = 0; k < K; ++k) {
+      if (idx[k] < e_begin || idx[k] >= e_begin + e_count) continue;
+      for (int l = 0; l < L; ++l) c[l] += (double)w[k] * o[(size_t)k * L + l];
+    }
+  }
+  free(o);
+  free(y);
+  free(idx);
+  free(w);
+}
+
+/* The block after the combine, for a given combine c [T, L]: n = bf16(c /
+ * sqrt(mean(c^2) + eps) * gamma), y = bf16(Wu . n), plus the shared experts
+ * of x when the dims have them (steps 4-6 of the forward, restated here
+ * for a c from outside). */
+void ora_finish(const ora_dims* d, const ora_weights* W, const uint16_t* x, const double* c_in, int T,
+                uint16_t* y_out) {
+  const int H = d->hidden, L = d->latent;
+  uint16_t* n = (uint16_t*)malloc(sizeof(uint16_t) * L);
+  for (int t = 0; t < T; ++t) {
+    const double* c = c_in + (size_t)t * L;
+    uint16_t* y = y_out + (size_t)t * H;
+    double ms = 0.0;
+    for (int l = 0; l < L; ++l) ms += c[l] * c[l];
+    ms /= (double)L;
+    double inv = 1.0 / sqrt(ms + d->rms_eps);
+    for (int l = 0; l < L; ++l) n[l] = ora_bf16_from_double(c[l] * inv * ora_bf16_to_double(W->norm_w[l]));
+    for (int j = 0; j < H; ++j) {
+      double acc = 0.0;
+      for (int l = 0; l < L; ++l)
+        acc += ora_bf16_to_double(W->up_proj[(size_t)j * L + l]) * ora_bf16_to_double(n[l]);
+      y[j] = ora_bf16_from_double(acc);
+    }
+    if (d->n_shared > 0) {
+      const int Is = d->n_shared * d->shared_inter;
+      const uint16_t* xt = x + (size_t)t * H;
+      uint16_t* hs = (uint16_t*)malloc(sizeof(uint16_t) * Is);
+      for (int j = 0; j < Is; ++j) {
+        double gs = 0.0, us = 0.0;
+        for (int i = 0; i < H; ++i) {
+          double a = ora_bf16_to_double(xt[i]);
+          gs += ora_bf16_to_double(W->shared_w1[(size_t)j * H + i]) * a;
+          us += ora_bf16_to_double(W->shared_w3[(size_t)j * H + i]) * a;
+        }
+        hs[j] = ora_bf16_from_double(ora_situ_glu(gs, us, d->beta, d->beta_lin));
+      }
+      for (int i = 0; i < H; ++i) {
+        double acc = 0.0;
+        for (int j = 0; j < Is; ++j)
+          acc += ora_bf16_to_double(W->shared_w2[(size_t)i * Is + j]) * ora_bf16_to_double(hs[j]);
+        y[i] = ora_bf16_from_double(ora_bf16_to_double(y[i]) + ora_bf16_to_double(ora_bf16_from_double(acc)));
+      }
+      free(hs);
+    }
+  }
+  free(n);
+}
+
+/* REAP saliency over a calibration set of T tokens (kimi-k3-mlx README,
+ * "REAP expert pruning": S_j = (1/|C|) sum over x in C of g_j(x) ||e_j(x)||_2,
+ * g_j the router's gate value of expert j for token x -- zero when j is not
+ * selected -- and e_j(x) the expert's output).  Reading: g_j is the routing
+ * weight the combine uses (topk_w) and e_j(x) is the expert output o in the
+ * 3584-d latent, before the combine; |C| = T.  S [E] receives the saliency
+ * and S_sum [E] (optional) the undivided sums. */
+void ora_reap_saliency(const ora_dims* d, const ora_weights* W, const uint16_t* x, int T, double* S,
+                       double* S_sum) {
+  const int H = d->hidden, L = d->latent, E = d->n_experts, K = d->top_k;
+  double* acc = (double*)calloc(E, sizeof(double));
+  double* o = (double*)malloc(sizeof(double) * (size_t)K * L);
+  uint16_t* y = (uint16_t*)malloc(sizeof(uint16_t) * H);
+  int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * K);
+  float* w = (float*)malloc(sizeof(float) * K);
+  for (int t = 0; t < T; ++t) {
+    ora_token_probe p;
+    memset(&p, 0, sizeof(p));
+    p.o = o;
+    ora_forward_token(d, W, x + (size_t)t * H, y, idx, w, &p);
+    for (int k = 0; k < K; ++k) {
+      double ss = 0.0;
+      for (int l = 0; l < L; ++l) ss += o[(size_t)k * L + l] * o[(size_t)k * L + l];
+      acc[idx[k]] += (double)w[k] * sqrt(ss);
+    }
+  }
+  for (int e = 0; e < E; ++e) {
+    if (S_sum) S_sum[e] = acc[e];
+    S[e] = T > 0 ? acc[e] / (double)T : 0.0;
+  }
+  free(acc);
+  free(o);
+  free(y);
+  free(idx);
+  free(w);
+}
+
 /* Dense all-expert masked sum: the same layer written with every expert
  * evaluated for every token and a zero weight for unselected ones.  Used
  * only as an independent formulation in the oracle's own tests. */

@@ -77,6 +77,12 @@ def lib():
             L.ora_route_from_logits.argtypes = [C.POINTER(OraDims), vp, vp, vp, vp, vp]
             L.ora_forward_dense_masked.restype = None
             L.ora_forward_dense_masked.argtypes = [C.POINTER(OraDims), C.POINTER(OraWeights), vp, i32, vp]
+            L.ora_reap_saliency.restype = None
+            L.ora_reap_saliency.argtypes = [C.POINTER(OraDims), C.POINTER(OraWeights), vp, i32, vp, vp]
+            L.ora_forward_partial.restype = None
+            L.ora_forward_partial.argtypes = [C.POINTER(OraDims), C.POINTER(OraWeights), vp, i32, i32, i32, vp]
+            L.ora_finish.restype = None
+            L.ora_finish.argtypes = [C.POINTER(OraDims), C.POINTER(OraWeights), vp, vp, i32, vp]
             L.ora_num_threads.restype = C.c_int
             _lib = L
     return _lib
@@ -216,6 +222,35 @@ def forward_dense_masked_c(dims, weights: dict, x: np.ndarray) -> np.ndarray:
     ds, ws = dims_struct(dims), weights_struct(weights)
     lib().ora_forward_dense_masked(C.byref(ds), C.byref(ws), _p(x), T, _p(c))
     return c
+
+
+def reap_saliency(dims, weights: dict, x: np.ndarray):
+    """REAP saliency S [E] of the calibration tokens x and the undivided sums."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    S = np.empty(dims.n_experts, np.float64)
+    S_sum = np.empty(dims.n_experts, np.float64)
+    ds, ws = dims_struct(dims), weights_struct(weights)
+    lib().ora_reap_saliency(C.byref(ds), C.byref(ws), _p(x), x.shape[0], _p(S), _p(S_sum))
+    return S, S_sum
+
+
+def forward_partial(dims, weights: dict, x: np.ndarray, e_begin: int, e_count: int) -> np.ndarray:
+    """Partial combine c_r [T, L] (fp64) of the experts [e_begin, e_begin + e_count)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    c = np.empty((x.shape[0], dims.latent), np.float64)
+    ds, ws = dims_struct(dims), weights_struct(weights)
+    lib().ora_forward_partial(C.byref(ds), C.byref(ws), _p(x), x.shape[0], int(e_begin), int(e_count), _p(c))
+    return c
+
+
+def finish(dims, weights: dict, x: np.ndarray, c: np.ndarray) -> np.ndarray:
+    """y [T, H] bf16 bits from a combine c [T, L]: RMSNorm, up_proj, shared experts."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    c = np.ascontiguousarray(c, dtype=np.float64)
+    y = np.empty((x.shape[0], dims.hidden), np.uint16)
+    ds, ws = dims_struct(dims), weights_struct(weights)
+    lib().ora_finish(C.byref(ds), C.byref(ws), _p(x), _p(c), x.shape[0], _p(y))
+    return y
 
 
 def num_threads() -> int:

@@ -472,6 +472,80 @@ def test_shared_experts_brute_force_pure_python():
     assert [bits_to_f64(v) for v in out["z"][0]] == z
 
 
+# ----------------------------------------------------------------------------- REAP saliency
+def test_reap_saliency_matches_dense_numpy(tiny_case):
+    """S_j = mean over tokens of g_j(x) ||e_j(x)||_2 with g_j = 0 for
+    unselected experts, from the dense all-expert numpy formulation."""
+    d, w, x, _ = tiny_case
+    ref = np_layer(d, w, x)
+    xf = bits_to_f64(x)
+    lat = ref["lat"]
+    S_ref = np.zeros(d.n_experts)
+    for e in range(d.n_experts):
+        W1 = np_dequant(w["w1_packed"][e], w["w1_scale"][e])
+        W3 = np_dequant(w["w3_packed"][e], w["w3_scale"][e])
+        W2 = np_dequant(w["w2_packed"][e], w["w2_scale"][e])
+        g, u = lat @ W1.T, lat @ W3.T
+        h = np_bf16(4 * np.tanh(g / 4) / (1 + np.exp(-g)) * 25 * np.tanh(u / 25))
+        o = h @ W2.T
+        S_ref[e] = np.mean(ref["gate"][:, e] * np.linalg.norm(o, axis=1))
+    S, S_sum = ora.reap_saliency(d, w, x)
+    assert np.allclose(S, S_ref, rtol=1e-9, atol=0)
+    assert np.allclose(S_sum, S * x.shape[0], rtol=1e-15)
+    assert xf.shape[0] == x.shape[0]
+    # experts no token selected score exactly zero
+    assert np.array_equal(S == 0, np.all(ref["gate"] == 0, axis=0))
+
+
+def test_reap_saliency_streams_over_the_calibration_set(tiny_case):
+    """The score of a set is the token-weighted mean of its parts' scores
+    (the calibration streams batches through the layer) and does not depend
+    on the token order."""
+    d, w, x, _ = tiny_case
+    S, _ = ora.reap_saliency(d, w, x)
+    S1, _ = ora.reap_saliency(d, w, x[:5])
+    S2, _ = ora.reap_saliency(d, w, x[5:])
+    assert np.allclose(S, (5 * S1 + (x.shape[0] - 5) * S2) / x.shape[0], rtol=1e-12, atol=1e-300)
+    perm = np.random.default_rng(0).permutation(x.shape[0])
+    Sp, _ = ora.reap_saliency(d, w, np.ascontiguousarray(x[perm]))
+    assert np.allclose(Sp, S, rtol=1e-12, atol=1e-300)
+
+
+def test_reap_saliency_of_a_pruned_expert_is_zero(tiny_case):
+    """An expert removed by a -inf correction bias (the pruning identity)
+    is never selected, so it scores zero."""
+    d, w, x, _ = tiny_case
+    S, _ = ora.reap_saliency(d, w, x)
+    top = int(np.argmax(S))
+    w2 = dict(w)
+    w2["router_bias"] = w["router_bias"].copy()
+    w2["router_bias"][top] = -np.inf
+    S2, _ = ora.reap_saliency(d, w2, x)
+    assert S[top] > 0 and S2[top] == 0.0
+
+
+# ----------------------------------------------------------------------------- expert parallelism
+def test_expert_shards_sum_to_the_combine(shared_case):
+    """The two ranks' partial combines add up to the whole combine, and the
+    finish step on that sum gives the block's output exactly."""
+    d, w, x, out = shared_case
+    h = d.n_experts // 2
+    c0 = ora.forward_partial(d, w, x, 0, h)
+    c1 = ora.forward_partial(d, w, x, h, d.n_experts - h)
+    assert np.allclose(c0 + c1, out["c"], rtol=1e-12, atol=1e-12 * np.abs(out["c"]).max())
+    assert np.array_equal(ora.finish(d, w, x, out["c"]), out["y"])
+    # a rank whose experts no token selected contributes zero
+    sel = np.unique(out["idx"])
+    unused = [e for e in range(d.n_experts) if e not in sel]
+    if unused:
+        assert not np.any(ora.forward_partial(d, w, x, unused[0], 1))
+    # uneven shards and one shard of everything
+    c_all = ora.forward_partial(d, w, x, 0, d.n_experts)
+    assert np.array_equal(c_all, out["c"])
+    parts = sum(ora.forward_partial(d, w, x, b, n) for b, n in ((0, 5), (5, 40), (45, d.n_experts - 45)))
+    assert np.allclose(parts, out["c"], rtol=1e-12, atol=1e-12 * np.abs(out["c"]).max())
+
+
 # ----------------------------------------------------------------------------- work counts
 def test_page_byte_figures(golden):
     g = golden["expert_tensors"]
