@@ -29,6 +29,10 @@ class LayerDims:
     # layers = 3 x 7168 x 6144 per layer)
     n_shared: int = 0
     shared_inter: int = 0
+    # two-bank graded experts (kimi-k3-mlx README, "REAP expert pruning"):
+    # 0 = one MXFP4 bank; else experts >= bank2_begin are stored as 2-bit
+    # affine weights (group 64, bf16 scale and bias: 2.5 bits per weight)
+    bank2_begin: int = 0
 
     def with_(self, **kw) -> "LayerDims":
         return replace(self, **kw)
@@ -54,6 +58,16 @@ class LayerDims:
     def shared_bytes(self) -> int:
         """bf16 gate, up and down weights of the shared experts."""
         return 3 * self.hidden * self.shared_total * 2
+
+    @property
+    def n_bank1(self) -> int:
+        """Experts in the MXFP4 bank."""
+        return self.bank2_begin if self.bank2_begin else self.n_experts
+
+    def expert_bytes_bank2(self) -> int:
+        """2-bit codes + bf16 scale and bias of one second-bank expert."""
+        per = lambda rows, cols: rows * cols // 4 + 2 * 2 * rows * (cols // 64)
+        return 2 * per(self.inter, self.latent) + per(self.latent, self.inter)
 
     def dense_bytes(self) -> int:
         """Router weight + bias, down_proj, up_proj and the RMSNorm weight."""

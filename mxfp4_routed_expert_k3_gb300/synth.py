@@ -9,6 +9,10 @@ seed; every tensor has its own counter stream):
   up_proj      ~ N(0, 1/L) bf16                     [H, L]
   norm_w       ~ 1 + N(0, 0.02) bf16                [L]
   w1/w3/w2 packed bytes uniform over 0..255; e8m0 scale bytes uniform in 118..124.
+  second bank (dims with bank2_begin > 0): the MXFP4 tensors hold experts
+  [0, bank2_begin); experts from there are 2-bit affine: code bytes uniform
+  over 0..255, per 64-element group scale s = bf16(0.14 * U(0.7, 1.3)) and
+  bias b = bf16(-1.5 s * U(0.9, 1.1)) (weights of RMS ~0.16, like the MXFP4 ones).
   shared experts (when the dims have them; Is = n_shared * shared_inter):
   shared_w1, shared_w3 ~ N(0, 1/H) bf16 [Is, H]; shared_w2 ~ N(0, 1/Is) bf16 [H, Is].
 """
@@ -35,6 +39,7 @@ S_ROUTER_W, S_BIAS, S_DOWN, S_UP, S_GAMMA = 1, 2, 3, 4, 5
 S_W1P, S_W1S, S_W3P, S_W3S, S_W2P, S_W2S = 6, 7, 8, 9, 10, 11
 S_HOT = 12
 S_SW1, S_SW3, S_SW2 = 13, 14, 15
+S_B2 = 16  # second-bank streams: 16 + 3 * matrix + {0 codes, 1 scale, 2 bias}
 S_X = 1000
 SCALE_LO, SCALE_HI = 118, 124
 
@@ -103,10 +108,10 @@ def hot_experts(d: LayerDims, seed: int, n_hot: int) -> np.ndarray:
 
 
 def layer_weights(d: LayerDims, seed: int, n_hot: int = 0, hot_bias: float = 2.0) -> dict:
-    H, L, E, I = d.hidden, d.latent, d.n_experts, d.inter
+    H, L, I = d.hidden, d.latent, d.inter
+    E = d.n_bank1  # MXFP4 experts (all of them with one bank)
     w = {
-        "router_w": bf16_normal(seed, S_ROUTER_W, (E, H), 0.0, 1.0 / np.sqrt(H)),
-        "router_bias": f32_uniform(seed, S_BIAS, (E,), -0.1, 0.1),
+        "router_w": bf16_normal(seed, S_ROUTER_W, (d.n_experts, H), 0.0, 1.0 / np.sqrt(H)),
         "down_proj": bf16_normal(seed, S_DOWN, (L, H), 0.0, 1.0 / np.sqrt(H)),
         "w1_packed": u8_full(seed, S_W1P, (E, I, L // 2)),
         "w1_scale": u8_range(seed, S_W1S, (E, I, L // 32), SCALE_LO, SCALE_HI),
@@ -117,14 +122,45 @@ def layer_weights(d: LayerDims, seed: int, n_hot: int = 0, hot_bias: float = 2.0
         "norm_w": bf16_normal(seed, S_GAMMA, (L,), 1.0, 0.02),
         "up_proj": bf16_normal(seed, S_UP, (H, L), 0.0, 1.0 / np.sqrt(L)),
     }
+    w["router_bias"] = f32_uniform(seed, S_BIAS, (d.n_experts,), -0.1, 0.1)
     if n_hot:
         w["router_bias"][hot_experts(d, seed, n_hot)] = np.float32(hot_bias)
+    if d.bank2_begin:
+        w.update(bank2_weights(d, seed))
     if d.n_shared:
-        Is = d.shared_total
-        w["shared_w1"] = bf16_normal(seed, S_SW1, (Is, H), 0.0, 1.0 / np.sqrt(H))
-        w["shared_w3"] = bf16_normal(seed, S_SW3, (Is, H), 0.0, 1.0 / np.sqrt(H))
-        w["shared_w2"] = bf16_normal(seed, S_SW2, (H, Is), 0.0, 1.0 / np.sqrt(Is))
+        w.update(shared_weights(d, seed))
     return w
+
+
+def bank2_weights(d: LayerDims, seed: int) -> dict:
+    """The second bank's 2-bit affine tensors (experts bank2_begin..E-1)."""
+    E2, L, I = d.n_experts - d.bank2_begin, d.latent, d.inter
+    out = {}
+    for m, (name, rows, cols) in enumerate((("w1", I, L), ("w3", I, L), ("w2", L, I))):
+        st = S_B2 + 3 * m
+        out[f"b2_{name}q"] = u8_full(seed, st, (E2, rows, cols // 4))
+        sc = f32_uniform(seed, st + 1, (E2, rows, cols // 64), 0.7, 1.3).astype(np.float64) * 0.14
+        bi = -1.5 * sc * f32_uniform(seed, st + 2, (E2, rows, cols // 64), 0.9, 1.1).astype(np.float64)
+        out[f"b2_{name}s"] = f32_to_bf16_bits(sc)
+        out[f"b2_{name}b"] = f32_to_bf16_bits(bi)
+    return out
+
+
+def f32_to_bf16_bits(v: np.ndarray) -> np.ndarray:
+    """Round to bf16 (nearest, ties to even) through float32; inputs here are
+    ordinary finite numbers."""
+    u = np.asarray(v, np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
+def shared_weights(d: LayerDims, seed: int) -> dict:
+    """The shared experts' bf16 weights alone (the same values layer_weights
+    gives dims with shared experts)."""
+    H, Is = d.hidden, d.shared_total
+    return {"shared_w1": bf16_normal(seed, S_SW1, (Is, H), 0.0, 1.0 / np.sqrt(H)),
+            "shared_w3": bf16_normal(seed, S_SW3, (Is, H), 0.0, 1.0 / np.sqrt(H)),
+            "shared_w2": bf16_normal(seed, S_SW2, (H, Is), 0.0, 1.0 / np.sqrt(Is))}
 
 
 def token_rows(d: LayerDims, seed: int, T: int, attempts: np.ndarray | None = None) -> np.ndarray:

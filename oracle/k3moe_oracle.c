@@ -61,6 +61,7 @@ typedef struct {
   double beta, beta_lin, rms_eps, routed_scaling;
   int norm_topk;
   int n_shared, shared_inter; /* shared experts (0 = none) and each one's intermediate */
+  int bank2_begin;            /* 0: one bank; else experts >= bank2_begin are 2-bit affine */
 } ora_dims;
 
 /* Host arrays in checkpoint layout (experts stacked along dim 0). */
@@ -81,6 +82,19 @@ typedef struct {
   const uint16_t* shared_w1;  /* [Is,H] gate */
   const uint16_t* shared_w3;  /* [Is,H] up */
   const uint16_t* shared_w2;  /* [H,Is] down */
+  /* second bank (experts e >= bank2_begin, stored at index e - bank2_begin;
+   * the MXFP4 tensors above then hold experts [0, bank2_begin) only):
+   * 2-bit codes, four per byte, element j in bits 2(j%4)..2(j%4)+1 of byte
+   * j/4; one bf16 scale and one bf16 bias per 64 elements of a row */
+  const uint8_t* b2_w1q;      /* [E2,I,L/4] */
+  const uint16_t* b2_w1s;     /* [E2,I,L/64] */
+  const uint16_t* b2_w1b;     /* [E2,I,L/64] */
+  const uint8_t* b2_w3q;
+  const uint16_t* b2_w3s;
+  const uint16_t* b2_w3b;
+  const uint8_t* b2_w2q;      /* [E2,L,I/4] */
+  const uint16_t* b2_w2s;     /* [E2,L,I/64] */
+  const uint16_t* b2_w2b;
 } ora_weights;
 
 /* ------------------------------------------------------------------ */
@@ -143,6 +157,18 @@ double ora_mxfp4_element(const uint8_t* packed_row, const uint8_t* scale_row, in
   uint8_t byte = packed_row[j / 2];
   unsigned code = (j % 2 == 0) ? (byte & 0x0Fu) : (byte >> 4);
   return ora_e2m1_value(code) * ora_e8m0_value(scale_row[j / 32]);
+}
+
+/* Second-bank weights (kimi-k3-mlx README, "REAP expert pruning", graded
+ * mode: the top experts keep MXFP4, the middle ones go to a lower bit
+ * width, in a second bank of the two-bank SwitchGLU; "Tiers": the 2-bit
+ * tier stores experts at 2.50 bits per weight).  Reading: MLX affine 2-bit
+ * quantisation with group 64 and a bf16 scale and bias per group (2 + 32/64
+ * bits per weight), w = scale * q + bias, q in {0, 1, 2, 3}, codes packed
+ * low bits first. */
+double ora_affine2_element(const uint8_t* q_row, const uint16_t* s_row, const uint16_t* b_row, int j) {
+  unsigned q = (q_row[j / 4] >> (2 * (j % 4))) & 3u;
+  return ora_bf16_to_double(s_row[j / 64]) * (double)q + ora_bf16_to_double(b_row[j / 64]);
 }
 
 /* Dequantise a [rows, cols] MXFP4 matrix to bf16 bits (IEEE rounding of
@@ -255,6 +281,40 @@ static void ora_forward_token(const ora_dims* d, const ora_weights* W, const uin
   /* 3. experts, combined in k order */
   for (int k = 0; k < K; ++k) {
     int e = idx[k];
+    if (d->bank2_begin > 0 && e >= d->bank2_begin) {
+      /* the second bank: 2-bit affine weights, the same arithmetic */
+      const int e2 = e - d->bank2_begin;
+      const uint8_t* w1q = W->b2_w1q + (size_t)e2 * I * (L / 4);
+      const uint16_t* w1s = W->b2_w1s + (size_t)e2 * I * (L / 64);
+      const uint16_t* w1b = W->b2_w1b + (size_t)e2 * I * (L / 64);
+      const uint8_t* w3q = W->b2_w3q + (size_t)e2 * I * (L / 4);
+      const uint16_t* w3s = W->b2_w3s + (size_t)e2 * I * (L / 64);
+      const uint16_t* w3b = W->b2_w3b + (size_t)e2 * I * (L / 64);
+      const uint8_t* w2q = W->b2_w2q + (size_t)e2 * L * (I / 4);
+      const uint16_t* w2s = W->b2_w2s + (size_t)e2 * L * (I / 64);
+      const uint16_t* w2b = W->b2_w2b + (size_t)e2 * L * (I / 64);
+      for (int j = 0; j < I; ++j) {
+        double g = 0.0, u = 0.0;
+        for (int l = 0; l < L; ++l) {
+          double a = ora_bf16_to_double(lat[l]);
+          g += ora_affine2_element(w1q + (size_t)j * (L / 4), w1s + (size_t)j * (L / 64),
+                                   w1b + (size_t)j * (L / 64), l) * a;
+          u += ora_affine2_element(w3q + (size_t)j * (L / 4), w3s + (size_t)j * (L / 64),
+                                   w3b + (size_t)j * (L / 64), l) * a;
+        }
+        h[j] = ora_bf16_from_double(ora_situ_glu(g, u, d->beta, d->beta_lin));
+        if (p && p->h) p->h[(size_t)k * I + j] = h[j];
+      }
+      for (int l = 0; l < L; ++l) {
+        double o = 0.0;
+        for (int j = 0; j < I; ++j)
+          o += ora_affine2_element(w2q + (size_t)l * (I / 4), w2s + (size_t)l * (I / 64),
+                                   w2b + (size_t)l * (I / 64), j) * ora_bf16_to_double(h[j]);
+        if (p && p->o) p->o[(size_t)k * L + l] = o;
+        c[l] += (double)w[k] * o;
+      }
+      continue;
+    }
     const uint8_t* w1p = W->w1_packed + (size_t)e * I * (L / 2);
     const uint8_t* w1s = W->w1_scale + (size_t)e * I * (L / 32);
     const uint8_t* w3p = W->w3_packed + (size_t)e * I * (L / 2);

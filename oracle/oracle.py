@@ -36,14 +36,15 @@ class OraDims(C.Structure):
         ("inter", C.c_int), ("group", C.c_int),
         ("beta", C.c_double), ("beta_lin", C.c_double), ("rms_eps", C.c_double),
         ("routed_scaling", C.c_double), ("norm_topk", C.c_int),
-        ("n_shared", C.c_int), ("shared_inter", C.c_int),
+        ("n_shared", C.c_int), ("shared_inter", C.c_int), ("bank2_begin", C.c_int),
     ]
 
 
 class OraWeights(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in (
         "router_w", "router_bias", "down_proj", "w1_packed", "w1_scale", "w3_packed", "w3_scale",
-        "w2_packed", "w2_scale", "norm_w", "up_proj", "shared_w1", "shared_w3", "shared_w2")]
+        "w2_packed", "w2_scale", "norm_w", "up_proj", "shared_w1", "shared_w3", "shared_w2",
+        "b2_w1q", "b2_w1s", "b2_w1b", "b2_w3q", "b2_w3s", "b2_w3b", "b2_w2q", "b2_w2s", "b2_w2b")]
 
 
 def lib():
@@ -83,6 +84,8 @@ def lib():
             L.ora_forward_partial.argtypes = [C.POINTER(OraDims), C.POINTER(OraWeights), vp, i32, i32, i32, vp]
             L.ora_finish.restype = None
             L.ora_finish.argtypes = [C.POINTER(OraDims), C.POINTER(OraWeights), vp, vp, i32, vp]
+            L.ora_affine2_element.restype = C.c_double
+            L.ora_affine2_element.argtypes = [vp, vp, vp, i32]
             L.ora_num_threads.restype = C.c_int
             _lib = L
     return _lib
@@ -96,7 +99,8 @@ def dims_struct(d) -> OraDims:
     """`d` is any object with the LayerDims attribute names."""
     return OraDims(d.hidden, d.latent, d.n_experts, d.top_k, d.inter, d.group, float(d.beta),
                    float(d.beta_lin), float(d.rms_eps), float(d.routed_scaling), int(d.norm_topk),
-                   int(getattr(d, "n_shared", 0)), int(getattr(d, "shared_inter", 0)))
+                   int(getattr(d, "n_shared", 0)), int(getattr(d, "shared_inter", 0)),
+                   int(getattr(d, "bank2_begin", 0)))
 
 
 _WEIGHT_DTYPES = {
@@ -104,8 +108,11 @@ _WEIGHT_DTYPES = {
     "w1_packed": np.uint8, "w1_scale": np.uint8, "w3_packed": np.uint8, "w3_scale": np.uint8,
     "w2_packed": np.uint8, "w2_scale": np.uint8, "norm_w": np.uint16, "up_proj": np.uint16,
     "shared_w1": np.uint16, "shared_w3": np.uint16, "shared_w2": np.uint16,
+    "b2_w1q": np.uint8, "b2_w1s": np.uint16, "b2_w1b": np.uint16, "b2_w3q": np.uint8, "b2_w3s": np.uint16,
+    "b2_w3b": np.uint16, "b2_w2q": np.uint8, "b2_w2s": np.uint16, "b2_w2b": np.uint16,
 }
-_OPTIONAL = ("shared_w1", "shared_w3", "shared_w2")
+_OPTIONAL = ("shared_w1", "shared_w3", "shared_w2", "b2_w1q", "b2_w1s", "b2_w1b", "b2_w3q", "b2_w3s", "b2_w3b",
+             "b2_w2q", "b2_w2s", "b2_w2b")
 
 
 def weights_struct(w: dict) -> OraWeights:
@@ -206,7 +213,9 @@ def forward(dims, weights: dict, x: np.ndarray, probes: bool = False) -> dict:
         if Is:
             out.update(hs=np.empty((T, Is), np.uint16), z=np.empty((T, H), np.uint16))
     if getattr(dims, "n_shared", 0):
-        assert all(n in weights for n in _OPTIONAL), "dims with shared experts need shared_w1/w3/w2"
+        assert all(n in weights for n in _OPTIONAL[:3]), "dims with shared experts need shared_w1/w3/w2"
+    if getattr(dims, "bank2_begin", 0):
+        assert all(n in weights for n in _OPTIONAL[3:]), "two-bank dims need the b2_* tensors"
     ds, ws = dims_struct(dims), weights_struct(weights)
     g = out.get
     lib().ora_forward(C.byref(ds), C.byref(ws), _p(x), T, _p(out["y"]), _p(out["idx"]), _p(out["w"]),
@@ -251,6 +260,13 @@ def finish(dims, weights: dict, x: np.ndarray, c: np.ndarray) -> np.ndarray:
     ds, ws = dims_struct(dims), weights_struct(weights)
     lib().ora_finish(C.byref(ds), C.byref(ws), _p(x), _p(c), x.shape[0], _p(y))
     return y
+
+
+def affine2_element(q_row: np.ndarray, s_row: np.ndarray, b_row: np.ndarray, j: int) -> float:
+    q_row = np.ascontiguousarray(q_row, np.uint8)
+    s_row = np.ascontiguousarray(s_row, np.uint16)
+    b_row = np.ascontiguousarray(b_row, np.uint16)
+    return float(lib().ora_affine2_element(_p(q_row), _p(s_row), _p(b_row), int(j)))
 
 
 def num_threads() -> int:

@@ -9,7 +9,8 @@ the bias leaking into the weights, ties to the higher id, a dropped RMSNorm
 epsilon, a transposed down projection, and two slips in the K+1 routing
 keys that guard the parity inputs' routing gap (only K keys written,
 ranking by the unbiased score), and two in the shared experts (fed the
-latent instead of the residual, gate and up weights swapped).
+latent instead of the residual, gate and up weights swapped), and two in the
+second bank's 2-bit decode (high bits first, bias dropped).
 """
 import ctypes as C
 import math
@@ -46,6 +47,10 @@ MUTATIONS = {
                          "        double a = ora_bf16_to_double(lat[i % L]);\n        gs +="),
     "shared_gate_up_swapped": ("        gs += ora_bf16_to_double(W->shared_w1[",
                                "        gs += ora_bf16_to_double(W->shared_w3["),
+    "bank2_high_bits_first": ("unsigned q = (q_row[j / 4] >> (2 * (j % 4))) & 3u;",
+                              "unsigned q = (q_row[j / 4] >> (6 - 2 * (j % 4))) & 3u;"),
+    "bank2_bias_dropped": ("return ora_bf16_to_double(s_row[j / 64]) * (double)q + ora_bf16_to_double(b_row[j / 64]);",
+                           "return ora_bf16_to_double(s_row[j / 64]) * (double)q;"),
     "down_proj_transposed": ("acc += ora_bf16_to_double(W->down_proj[(size_t)l * H + j]) * ora_bf16_to_double(x[j]);",
                              "acc += ora_bf16_to_double(W->down_proj[(size_t)j * L + l]) * ora_bf16_to_double(x[j]);"),
 }
@@ -153,6 +158,21 @@ def pin_shared(L):
     return bool(np.max(np.abs(zo - zr)) <= 2 ** -7 * np.abs(zr).max())
 
 
+def pin_bank2(L):
+    """Second-bank decode against the integer formula on every code byte."""
+    L.ora_affine2_element.restype = C.c_double
+    L.ora_affine2_element.argtypes = [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int]
+    sc = np.array([0x3E00], np.uint16)  # 0.125
+    bi = np.array([0xBE40], np.uint16)  # -0.1875
+    for byte in range(256):
+        row = np.full(16, byte, np.uint8)
+        for j in range(4):
+            v = L.ora_affine2_element(row.ctypes.data, sc.ctypes.data, bi.ctypes.data, j)
+            if v != 0.125 * ((byte >> (2 * j)) & 3) - 0.1875:
+                return False
+    return True
+
+
 def pin_layer(L):
     """Against the independent numpy formulation in test_oracle_pins."""
     from test_oracle_pins import np_layer
@@ -183,6 +203,7 @@ PIN_OF = {
     "rmsnorm_no_eps": pin_layer, "down_proj_transposed": pin_layer,
     "keys_top_only_k": pin_keys, "keys_top_by_score": pin_keys,
     "shared_on_latent": pin_shared, "shared_gate_up_swapped": pin_shared,
+    "bank2_high_bits_first": pin_bank2, "bank2_bias_dropped": pin_bank2,
 }
 
 

@@ -546,6 +546,98 @@ def test_expert_shards_sum_to_the_combine(shared_case):
     assert np.allclose(parts, out["c"], rtol=1e-12, atol=1e-12 * np.abs(out["c"]).max())
 
 
+# ----------------------------------------------------------------------------- two-bank experts
+def np_affine2(q, sc, bi):
+    """Independent numpy dequant of 2-bit affine rows: codes low bits first,
+    scale and bias per 64."""
+    codes = np.stack([(q >> (2 * i)) & 3 for i in range(4)], axis=-1).reshape(*q.shape[:-1], q.shape[-1] * 4)
+    return codes * np.repeat(bits_to_f64(sc), 64, axis=-1) + np.repeat(bits_to_f64(bi), 64, axis=-1)
+
+
+def test_affine2_decode_every_byte():
+    q = np.arange(256, dtype=np.uint8)
+    rng = np.random.default_rng(9)
+    for _ in range(6):
+        sc = f64_to_bits_torch(rng.uniform(-2, 2, 1) * 2.0 ** rng.integers(-20, 10))
+        bi = f64_to_bits_torch(rng.uniform(-2, 2, 1) * 2.0 ** rng.integers(-20, 10))
+        s, b = float(bits_to_f64(sc[0])), float(bits_to_f64(bi[0]))
+        for byte in range(256):
+            row = np.full(16, byte, np.uint8)
+            for j in range(4):
+                code = (byte >> (2 * j)) & 3
+                assert ora.affine2_element(row, sc, bi, j) == s * code + b
+        ref = np_affine2(q[None, :16], sc[None, :], bi[None, :])
+        got = [ora.affine2_element(q[:16], sc, bi, j) for j in range(64)]
+        assert np.array_equal(ref[0], got)
+
+
+def mxfp4_twin_of_bank2(d, w, seed):
+    """Second-bank tensors holding exactly the values of MXFP4 experts:
+    scales 2^k and biases -2^k make every weight one of {-1, 0, 1, 2} 2^k,
+    which e2m1 codes {0xA, 0x0, 0x2, 0x4} with e8m0 byte 127 + k store
+    exactly.  Returns (two-bank weights, the equivalent one-bank weights)."""
+    rng = np.random.default_rng(seed)
+    E2 = d.n_experts - d.bank2_begin
+    two = dict(w)
+    one = dict(w)
+    e2m1_of = np.array([0xA, 0x0, 0x2, 0x4], np.uint8)
+    for name, rows, cols in (("w1", d.inter, d.latent), ("w3", d.inter, d.latent), ("w2", d.latent, d.inter)):
+        q = rng.integers(0, 256, (E2, rows, cols // 4), dtype=np.uint8)
+        k = rng.integers(-9, -3, (E2, rows, cols // 64))
+        two[f"b2_{name}q"] = q
+        two[f"b2_{name}s"] = f64_to_bits_torch(np.ldexp(1.0, k)).reshape(k.shape)
+        two[f"b2_{name}b"] = f64_to_bits_torch(-np.ldexp(1.0, k)).reshape(k.shape)
+        codes = np.stack([(q >> (2 * i)) & 3 for i in range(4)], -1).reshape(E2, rows, cols)
+        nib = e2m1_of[codes]
+        packed = (nib[..., 0::2] | (nib[..., 1::2] << 4)).astype(np.uint8)
+        scale = np.repeat((127 + k).astype(np.uint8), 2, axis=-1)
+        one[f"{name}_packed"] = np.ascontiguousarray(np.concatenate([w[f"{name}_packed"], packed]))
+        one[f"{name}_scale"] = np.ascontiguousarray(np.concatenate([w[f"{name}_scale"], scale]))
+    return two, one
+
+
+def test_two_banks_of_identical_values_match_one_bank():
+    """The graded two-bank layer with the second bank holding exactly the
+    values of MXFP4 experts equals the one-bank layer, bit for bit (the
+    page's own correctness test for the two-bank design)."""
+    d2 = TINY.with_(bank2_begin=40)
+    w = synth.layer_weights(d2, seed=7)
+    two, one = mxfp4_twin_of_bank2(d2, w, 8)
+    x = synth.token_rows(TINY, 77, 10)
+    a = ora.forward(d2, two, x, probes=True)
+    b = ora.forward(TINY, one, x, probes=True)
+    assert np.any(a["idx"] >= 40)  # the second bank is used
+    for k in ("y", "idx", "w", "h", "n"):
+        assert np.array_equal(a[k], b[k]), k
+    assert np.array_equal(a["o"], b["o"])
+
+
+def test_two_bank_layer_matches_dense_numpy():
+    d = TINY.with_(bank2_begin=40)
+    w = synth.layer_weights(d, seed=12)
+    x = synth.token_rows(d, 78, 6)
+    out = ora.forward(d, w, x, probes=True)
+    xf = bits_to_f64(x)
+    lat = np_bf16(xf @ bits_to_f64(w["down_proj"]).T)
+    assert np.array_equal(bits_to_f64(out["lat"]), lat)
+    for t in range(x.shape[0]):
+        for k, e in enumerate(out["idx"][t]):
+            if e < 40:
+                W1 = np_dequant(w["w1_packed"][e], w["w1_scale"][e])
+                W3 = np_dequant(w["w3_packed"][e], w["w3_scale"][e])
+                W2 = np_dequant(w["w2_packed"][e], w["w2_scale"][e])
+            else:
+                e2 = e - 40
+                W1 = np_affine2(w["b2_w1q"][e2], w["b2_w1s"][e2], w["b2_w1b"][e2])
+                W3 = np_affine2(w["b2_w3q"][e2], w["b2_w3s"][e2], w["b2_w3b"][e2])
+                W2 = np_affine2(w["b2_w2q"][e2], w["b2_w2s"][e2], w["b2_w2b"][e2])
+            g, u = W1 @ lat[t], W3 @ lat[t]
+            h = np_bf16(4 * np.tanh(g / 4) / (1 + np.exp(-g)) * 25 * np.tanh(u / 25))
+            assert np.mean(bits_to_f64(out["h"][t, k]) == h) > 0.99
+            o = bits_to_f64(out["h"][t, k]) @ W2.T
+            assert np.allclose(out["o"][t, k], o, rtol=1e-12, atol=1e-12 * np.abs(o).max())
+
+
 # ----------------------------------------------------------------------------- work counts
 def test_page_byte_figures(golden):
     g = golden["expert_tensors"]
