@@ -93,6 +93,8 @@ class ClockSampler:
     def __init__(self, gpu_index: int, settle_s: float = 1.5):
         self.proc = None
         self.t0 = self.t1 = None
+        self.windows = {}
+        self.window_summaries = {}
         import tempfile
         try:
             fd, self.path = tempfile.mkstemp(prefix="k3moe_clocks_", suffix=".csv")
@@ -109,6 +111,11 @@ class ClockSampler:
 
     def end(self):
         self.t1 = time.time()
+
+    def mark(self, name: str, t0: float, t1: float):
+        """Record a further wall-clock window (a later leg of the run) to
+        summarise separately."""
+        self.windows[name] = (t0, t1)
 
     @staticmethod
     def _stamp(text: str):
@@ -128,6 +135,7 @@ class ClockSampler:
             self.proc.kill()
         self.fh.close()
         try:
+            self.window_summaries = {k: self.parse(a, b) for k, (a, b) in self.windows.items()}
             return self.parse()
         finally:
             try:
@@ -135,10 +143,12 @@ class ClockSampler:
             except OSError:
                 pass
 
-    def parse(self) -> dict:
+    def parse(self, t0=None, t1=None) -> dict:
+        t0 = self.t0 if t0 is None else t0
+        t1 = self.t1 if t1 is None else t1
         sm, smax, reasons, window = [], None, set(), 0
-        lo = (self.t0 if self.t0 is not None else float("-inf")) - 0.02
-        hi = (self.t1 if self.t1 is not None else float("inf")) + 0.02
+        lo = (t0 if t0 is not None else float("-inf")) - 0.02
+        hi = (t1 if t1 is not None else float("inf")) + 0.02
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 6:
@@ -272,7 +282,6 @@ def run_ours(args, rank, world, local_rank):
     t_wall = time.perf_counter() - t_wall0
     clocks.end()
     barrier(world)
-    clk = clocks.stop()
     assert layer.status() == 0, k3moe.last_error(layer.ctx)
     # per-launch-group split: the profiled graphs on the same inputs
     for i in range(args.warmup, pool):
@@ -343,9 +352,34 @@ def run_ours(args, rank, world, local_rank):
                            "kernel_ms": {k: statistics.mean(v) for k, v in kms.items()}}
 
     # ---- e2e: through the public C-ABI call with HOST buffers (pinned), copies timed
-    e2e = run_e2e(layer, d, batches, args, rank, dev, stream)
+    t_leg = time.time()
+    e2e = run_e2e(layer, d, batches, args, rank, dev, stream, l2_flush)
+    clocks.mark("e2e", t_leg, time.time())
+    t_leg = time.time()
     prefill = run_prefill(layer, d, prefill_T, rank, dev, stream, peaks) if prefill_T else None
+    clocks.mark("prefill", t_leg, time.time())
     e2e_value = reduce_sum_over_ranks(e2e["tokens_per_s_rank"], world, dev)
+    routed_step_ms = step_ms
+    layer.close()
+    torch.cuda.empty_cache()
+    extra = {}
+    if not args.no_extra and d.n_experts == K3.n_experts:
+        t_leg = time.time()
+        extra["shared_block"] = run_shared_block(w, args, rank, dev, stream, l2_flush, peaks, routed_step_ms)
+        clocks.mark("shared_block", t_leg, time.time())
+        t_leg = time.time()
+        extra["two_bank"] = run_two_bank(w, args, rank, dev, stream, l2_flush, peaks, routed_step_ms)
+        clocks.mark("two_bank", t_leg, time.time())
+        torch.cuda.empty_cache()
+        t_leg = time.time()
+        extra["skew_4096"] = run_skew(w, rank, dev, stream, peaks)
+        clocks.mark("skew_4096", t_leg, time.time())
+        torch.cuda.empty_cache()
+        if not args.no_stacked:
+            t_leg = time.time()
+            extra["stacked4"] = run_stacked4(args, rank, dev, l2_flush, peaks)
+            clocks.mark("stacked4", t_leg, time.time())
+    clk = clocks.stop()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -353,7 +387,9 @@ def run_ours(args, rank, world, local_rank):
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms_max, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "mxfp4(e2m1+e8m0) weights, bf16 activations, f32 accumulate",
+        "vs_baseline": None,
+        "dtype": "mxfp4 (e2m1 + e8m0) weights as stored; bf16 activations, carried to the block-scaled tensor "
+                 "cores as six e2m1 terms (T <= 128) or two exact e4m3 terms (larger T); fp32 accumulate",
         "data": "synthetic (seeded generator: x~N(0,1) bf16, uniform MXFP4 bytes, e8m0 scales 118..124)",
         "config": {"workload": "K3 LatentMoE routed layer, decode batches T=1,8,64 per step (73 tokens)"
                    + ("" if d.n_experts == K3.n_experts else f" [reduced to {d.n_experts} experts: profiling case]"),
@@ -371,11 +407,12 @@ def run_ours(args, rank, world, local_rank):
     }
     if prefill is not None:
         out["prefill"] = prefill
+    out.update(extra)
     if clk is not None:
         out["clocks"] = clk
+        out["clocks_by_leg"] = clocks.window_summaries
     if cpu is not None:
         out["cpu_baseline"] = cpu
-    layer.close()
     return out
 
 
@@ -418,27 +455,260 @@ def run_prefill(layer, d, T, rank, dev, stream, peaks, reps: int = 5):
                    "FLOP = 2*(E*H + 2*L*H) + top_k*(2*2*I*L + 2*L*I) per token"}
 
 
-def run_e2e(layer, d, batches, args, rank, dev, stream):
+def run_e2e(layer, d, batches, args, rank, dev, stream, l2_flush):
+    """The public host-buffer call (k3moe_forward_host): pinned host x in,
+    y / topk_idx / topk_w back to pinned host memory, copies inside the
+    timed region; a fresh token batch every iteration and L2 flushed
+    between iterations (outside the timed spans), as for `value`."""
     import torch
     from mxfp4_routed_expert_k3_gb300 import k3moe, synth
     k3moe.profile(layer.ctx, False)
-    xs = {T: torch.from_numpy(synth.token_rows(d, 9000 + 31 * rank + T, T).view(np.int16)).pin_memory()
-          for T in batches}
+    n = max(3, args.steps // 2)
+    xs = {T: [torch.from_numpy(synth.token_rows(d, 9000 + 31 * rank + 7 * i + T, T).view(np.int16)).pin_memory()
+              for i in range(n + 1)] for T in batches}
     ys = {T: torch.empty((T, d.hidden), dtype=torch.int16).pin_memory() for T in batches}
     ids = {T: torch.empty((T, d.top_k), dtype=torch.int32).pin_memory() for T in batches}
     ws = {T: torch.empty((T, d.top_k), dtype=torch.float32).pin_memory() for T in batches}
     for T in batches:
-        k3moe.forward_host(layer.ctx, xs[T], T, ys[T], ids[T], ws[T], stream=stream)
-    n = max(3, args.steps // 2)
-    t0 = time.perf_counter()
-    for _ in range(n):
+        k3moe.forward_host(layer.ctx, xs[T][n], T, ys[T], ids[T], ws[T], stream=stream)
+    dt = 0.0
+    for i in range(n):
         for T in batches:
-            k3moe.forward_host(layer.ctx, xs[T], T, ys[T], ids[T], ws[T], stream=stream)
-    dt = (time.perf_counter() - t0) / n
+            with torch.cuda.stream(stream):
+                l2_flush()
+            stream.synchronize()
+            t0 = time.perf_counter()
+            k3moe.forward_host(layer.ctx, xs[T][i], T, ys[T], ids[T], ws[T], stream=stream)
+            dt += time.perf_counter() - t0
+    dt /= n
     tok = sum(batches)
     h2d = sum(T * d.hidden * 2 for T in batches)
     d2h = sum(T * (d.hidden * 2 + d.top_k * 8) for T in batches)
     return {"tokens_per_s_rank": tok / dt, "h2d": h2d, "d2h": d2h}
+
+
+# ============================================================================ further workloads
+def _graph_decode(layer, d, T, reps, warmup, stream, l2_flush, seed0):
+    """CUDA-graph replays of the C-ABI forward on fresh T-token batches, L2
+    flushed before each (outside the events): (mean ms, mean active experts)."""
+    import torch
+    from mxfp4_routed_expert_k3_gb300 import k3moe, synth
+    dev = stream.device
+    xs = [torch.from_numpy(synth.token_rows(d, seed0 + 13 * i + T, T).view(np.int16)).to(dev)
+          for i in range(warmup + reps)]
+    x_in = torch.empty((T, d.hidden), dtype=torch.int16, device=dev)
+    y = torch.empty((T, d.hidden), dtype=torch.int16, device=dev)
+    idx = torch.empty((T, d.top_k), dtype=torch.int32, device=dev)
+    wt = torch.empty((T, d.top_k), dtype=torch.float32, device=dev)
+    with torch.cuda.stream(stream):
+        x_in.copy_(xs[0])
+        layer.forward(x_in, y, idx, wt, stream=stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+        layer.forward(x_in, y, idx, wt, stream=stream)
+    ms, act = [], []
+    for i in range(warmup + reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            l2_flush()
+            x_in.copy_(xs[i])
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        if i >= warmup:
+            ms.append(e0.elapsed_time(e1))
+            a = np.empty(d.n_experts + 1, np.int32)
+            k3moe.fetch(layer.ctx, "active", a)
+            act.append(int(a[0]))
+    assert layer.status() == 0, k3moe.last_error(layer.ctx)
+    return statistics.mean(ms), statistics.mean(act)
+
+
+def run_shared_block(w, args, rank, dev, stream, l2_flush, peaks, routed_step_ms):
+    """The K3 MoE block with its two shared experts (bf16, 264 MB per layer,
+    on a side stream beside the routed chain): the same decode step
+    (T = 1, 8, 64) and the T = 8192 prefill."""
+    import torch
+    from mxfp4_routed_expert_k3_gb300 import k3moe, synth
+    from mxfp4_routed_expert_k3_gb300.dims import K3_SHARED
+    d = K3_SHARED
+    ws = dict(w)
+    ws.update(synth.shared_weights(d, seed=1))
+    layer = k3moe.Layer(d, ws, max_tokens=PREFILL_T)
+    try:
+        per_T, step_ms, alg_bytes = {}, 0.0, 0.0
+        for T in DECODE_BATCHES:
+            ms, nact = _graph_decode(layer, d, T, max(5, args.steps // 2), args.warmup, stream, l2_flush, 11000)
+            b = nact * d.expert_bytes() + d.dense_bytes() + d.shared_bytes() + T * d.hidden * 4
+            per_T[f"T={T}"] = {"forward_ms": ms, "active_experts": nact, "algorithmic_GB": b / 1e9,
+                               "GB_per_s": b / (ms / 1e3) / 1e9}
+            step_ms += ms
+            alg_bytes += b
+        pf = run_prefill(layer, d, PREFILL_T, rank, dev, stream, peaks, reps=3)
+    finally:
+        layer.close()
+    tok = sum(DECODE_BATCHES)
+    return {"workload": "K3 MoE block: routed layer + 2 shared experts (intermediate 3072 each, bf16, on the "
+                        "residual), decode batches T=1,8,64 per step",
+            "tokens_per_s": tok / (step_ms / 1e3), "ms_per_step": step_ms,
+            "shared_cost_ms_per_step": step_ms - routed_step_ms,
+            "hbm_GB_per_s": alg_bytes / (step_ms / 1e3) / 1e9,
+            "hbm_frac": alg_bytes / (step_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "decode": per_T, "prefill": pf}
+
+
+def run_two_bank(w, args, rank, dev, stream, l2_flush, peaks, routed_step_ms):
+    """Two-bank graded experts: experts 0..447 MXFP4 (as in the main run),
+    448..895 2-bit affine (2.5 bits per weight); the same decode step.  The
+    banks' split of the sorted selections is found on the device."""
+    import torch
+    from mxfp4_routed_expert_k3_gb300 import k3moe, synth
+    from mxfp4_routed_expert_k3_gb300.dims import K3
+    d = K3.with_(bank2_begin=K3.n_experts // 2)
+    w2 = dict(w)
+    for n in ("w1_packed", "w1_scale", "w3_packed", "w3_scale", "w2_packed", "w2_scale"):
+        w2[n] = np.ascontiguousarray(w[n][: d.bank2_begin])
+    w2.update(synth.bank2_weights(d, seed=1))
+    layer = k3moe.Layer(d, w2, max_tokens=max(DECODE_BATCHES))
+    del w2
+    try:
+        per_T, step_ms, alg_bytes = {}, 0.0, 0.0
+        for T in DECODE_BATCHES:
+            ms, _ = _graph_decode(layer, d, T, max(5, args.steps // 2), args.warmup, stream, l2_flush, 13000)
+            a = np.empty(d.n_experts + 1, np.int32)
+            k3moe.fetch(layer.ctx, "active", a)
+            ids = a[1:1 + a[0]]
+            n1, n2 = int(np.sum(ids < d.bank2_begin)), int(np.sum(ids >= d.bank2_begin))
+            b = n1 * d.expert_bytes() + n2 * d.expert_bytes_bank2() + d.dense_bytes() + T * d.hidden * 4
+            per_T[f"T={T}"] = {"forward_ms": ms, "experts_bank1": n1, "experts_bank2": n2,
+                               "algorithmic_GB": b / 1e9, "GB_per_s": b / (ms / 1e3) / 1e9}
+            step_ms += ms
+            alg_bytes += b
+    finally:
+        layer.close()
+    tok = sum(DECODE_BATCHES)
+    return {"workload": "K3 routed layer, experts 0..447 MXFP4 + 448..895 2-bit affine (second bank), decode "
+                        "batches T=1,8,64 per step",
+            "tokens_per_s": tok / (step_ms / 1e3), "ms_per_step": step_ms,
+            "vs_one_bank_time": step_ms / routed_step_ms,
+            "hbm_GB_per_s": alg_bytes / (step_ms / 1e3) / 1e9, "decode": per_T}
+
+
+def run_skew(w, rank, dev, stream, peaks, T: int = 4096, reps: int = 5):
+    """Skewed routing (+2.0 correction bias on 32 hot experts, the first 32
+    of a seeded permutation): every assignment lands on the hot set, about
+    2,048 tokens per hot expert, 864 experts idle."""
+    from mxfp4_routed_expert_k3_gb300 import k3moe, synth
+    from mxfp4_routed_expert_k3_gb300.dims import K3
+    d = K3
+    wk = dict(w)
+    wk["router_bias"] = w["router_bias"].copy()
+    wk["router_bias"][synth.hot_experts(d, 1, 32)] = np.float32(2.0)
+    layer = k3moe.Layer(d, wk, max_tokens=T)
+    try:
+        r = run_prefill(layer, d, T, rank, dev, stream, peaks, reps=reps)
+        counts = np.empty(d.n_experts, np.int32)
+        k3moe.fetch(layer.ctx, "counts", counts)
+    finally:
+        layer.close()
+    busy = counts[counts > 0]
+    r.update({"workload": "K3 routed layer, T=4096, 32 hot experts (+2.0 bias)",
+              "active_experts": int(busy.size), "tokens_per_hot_expert_max": int(busy.max()),
+              "tokens_per_hot_expert_min": int(busy.min())})
+    return r
+
+
+def run_stacked4(args, rank, dev, l2_flush, peaks, n_layers: int = 4, T_pre: int = 32768):
+    """Four stacked K3 routed layers (independent seeded weights, ~63 GB of
+    MXFP4 experts resident), x_{l+1} = bf16(y_l / rms(y_l)) per token between
+    layers: a T = 32768 prefill chain and a T = 1 decode chain, each captured
+    in one CUDA graph and timed with events (decode: L2 flushed first)."""
+    import torch
+    from mxfp4_routed_expert_k3_gb300 import k3moe, synth
+    from mxfp4_routed_expert_k3_gb300.dims import K3
+    d = K3
+    layers = []
+    try:
+        for l in range(n_layers):
+            wl = synth.layer_weights(d, seed=4 + l)
+            layers.append(k3moe.Layer(d, wl, max_tokens=T_pre, device=dev.index or 0))
+            del wl
+        s = torch.cuda.Stream(device=dev)
+
+        def rescale(y):
+            f = y.view(torch.bfloat16).float()
+            return (f / torch.sqrt(torch.mean(f * f, dim=1, keepdim=True))).to(torch.bfloat16).view(torch.int16)
+
+        def chain_graph(T, x0):
+            xs = [torch.empty((T, d.hidden), dtype=torch.int16, device=dev) for _ in range(n_layers)]
+            ys = [torch.empty((T, d.hidden), dtype=torch.int16, device=dev) for _ in range(n_layers)]
+            ids = [torch.empty((T, d.top_k), dtype=torch.int32, device=dev) for _ in range(n_layers)]
+            wts = [torch.empty((T, d.top_k), dtype=torch.float32, device=dev) for _ in range(n_layers)]
+
+            def chain():
+                for l, layer in enumerate(layers):
+                    if l > 0:
+                        xs[l].copy_(rescale(ys[l - 1]))
+                    layer.forward(xs[l], ys[l], ids[l], wts[l], stream=s)
+
+            xs[0].copy_(x0)
+            with torch.cuda.stream(s):
+                chain()
+            s.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s, capture_error_mode="thread_local"):
+                chain()
+            return g, xs
+
+        def timed(g, xs, pool, reps, warmup, flush):
+            ms = []
+            for i in range(warmup + reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(s):
+                    if flush:
+                        l2_flush()
+                    xs[0].copy_(pool[i % len(pool)])
+                    e0.record(s)
+                    g.replay()
+                    e1.record(s)
+                s.synchronize()
+                if i >= warmup:
+                    ms.append(e0.elapsed_time(e1))
+            for layer in layers:
+                assert layer.status() == 0, k3moe.last_error(layer.ctx)
+            return statistics.mean(ms)
+
+        x_pre = torch.from_numpy(synth.token_rows(d, 12000 + rank, T_pre).view(np.int16)).to(dev)
+        g_pre, xs_pre = chain_graph(T_pre, x_pre)
+        pre_ms = timed(g_pre, xs_pre, [x_pre], reps=3, warmup=1, flush=False)
+        del g_pre, xs_pre
+        dec_pool = [torch.from_numpy(synth.token_rows(d, 12100 + 7 * i + rank, 1).view(np.int16)).to(dev)
+                    for i in range(args.warmup + 10)]
+        g_dec, xs_dec = chain_graph(1, dec_pool[0])
+        dec_ms = timed(g_dec, xs_dec, dec_pool, reps=10, warmup=args.warmup, flush=True)
+        act = []
+        for layer in layers:
+            a = np.empty(d.n_experts + 1, np.int32)
+            k3moe.fetch(layer.ctx, "active", a)
+            act.append(int(a[0]))
+    finally:
+        for layer in layers:
+            layer.close()
+        torch.cuda.empty_cache()
+    flop = d.flop_per_token() * T_pre * n_layers
+    dec_bytes = sum(a * d.expert_bytes() + d.dense_bytes() + 4 * d.hidden for a in act)
+    peak = peaks.get("bf16_tflops")
+    return {"workload": f"{n_layers} stacked K3 routed layers (seeds 4..{3 + n_layers}), per-token RMS rescale "
+                        f"between layers, each chain one CUDA graph",
+            "prefill": {"T": T_pre, "ms": pre_ms, "tokens_per_s": T_pre / (pre_ms / 1e3),
+                        "tflops": flop / (pre_ms / 1e3) / 1e12, "frac_bf16_peak": flop / (pre_ms / 1e3) / 1e12 / peak,
+                        "bound": "tensor"},
+            "decode": {"T": 1, "ms": dec_ms, "tokens_per_s": 1 / (dec_ms / 1e3), "algorithmic_GB": dec_bytes / 1e9,
+                       "GB_per_s": dec_bytes / (dec_ms / 1e3) / 1e9,
+                       "hbm_frac": dec_bytes / (dec_ms / 1e3) / 1e9 / peaks["hbm_gbs"], "bound": "hbm",
+                       "l2": "flushed before every replay"}}
 
 
 # ============================================================================ oracle (CPU)
@@ -512,6 +782,9 @@ def main():
                          "the tokens per expert of the full layer, for small profiling captures)")
     ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2, 3, 4],
                     help="kernel path (0 = the library's choice by token count; see k3moe_config.force_path)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the shared-expert block, skewed-routing and stacked-layer measurements")
+    ap.add_argument("--no-stacked", action="store_true", help="skip the four-stacked-layer measurement")
     ap.add_argument("--experts", type=int, default=896,
                     help="experts of the K3-dim layer (default 896; fewer only for small profiling captures)")
     args = ap.parse_args()

@@ -91,6 +91,41 @@ typedef struct {
                          kind::mxf8f6f4 on tiles of 80 rows with two exact
                          e4m3 terms; the terms of a tile form one MMA
                          operand) */
+  /* Shared experts (kimi-k3-mlx README, "Architecture" table: 2 shared
+   * experts on every token; "Porting notes" item 3: they act on the 7168-d
+   * residual, not the latent; "Parameter budget": 12.2 B parameters, i.e.
+   * intermediate 3072 each).  0 = the routed layer alone.  With Is =
+   * n_shared * shared_inter (a multiple of 128), the block output becomes
+   *   y = bf16(y_routed + z),  z = bf16(W2s . bf16(SiTU(W1s . x, W3s . x)))
+   * (the experts summed: one MLP over their concatenated intermediate).
+   * Needs force_path 0, 2 or 4. */
+  int n_shared;
+  int shared_inter;
+  /* Expert shard (expert parallelism: Kimi-K3-Alis-MLX-Dynamic model card,
+   * "Performance" and "Usage" -- dense weights replicated, the routed
+   * experts split between two machines).  expert_count = 0: the context
+   * holds all n_experts experts.  Otherwise it holds experts
+   * [expert_begin, expert_begin + expert_count): load_weights takes the
+   * expert tensors of those experts only, while the router, bias and dense
+   * weights stay whole.  A shard has no whole forward; it runs
+   * k3moe_forward_partial, the callers sum the shards' partial combines
+   * (one all-reduce), and k3moe_finish completes the block.  Needs
+   * force_path 0, 2 or 4. */
+  int expert_begin;
+  int expert_count;
+  /* Two-bank graded experts (kimi-k3-mlx README, "REAP expert pruning",
+   * graded mode and the two-bank SwitchGLU: the most salient experts keep
+   * MXFP4, the next ones a lower bit width, each bank owning a contiguous
+   * range of expert ids).  0: one MXFP4 bank.  Otherwise experts
+   * [0, bank2_begin) are MXFP4 (the w1/w3/w2 tensors hold those only) and
+   * experts [bank2_begin, n_experts) are 2-bit affine (the b2_* tensors):
+   * w = scale * q + bias, q in {0..3} packed four per byte low bits first,
+   * one bf16 scale and bias per 64 inputs of a row (2.5 bits per weight,
+   * the pages' 2-bit tier).  The permutation sorts the selections by expert,
+   * so each bank's slots form one contiguous slice; the slice boundary is
+   * found on the device and each bank's kernels read it there (no host
+   * synchronisation).  Needs force_path 0 or 4 and no expert shard. */
+  int bank2_begin;
 } k3moe_config;
 
 /* Host arrays in checkpoint layout, experts stacked along dim 0.  Row-major;
@@ -107,6 +142,22 @@ typedef struct {
   const uint8_t* w2_scale;     /* [E, L, I/32]                                */
   const uint16_t* norm_w;      /* [L]    bf16   RMSNorm weight (gamma)        */
   const uint16_t* up_proj;     /* [H, L] bf16                                 */
+  /* shared experts (read only when cfg.n_shared > 0; Is = n_shared *
+   * shared_inter, expert s owning intermediate rows [s*shared_inter, ...)) */
+  const uint16_t* shared_w1;   /* [Is, H] bf16  gate                          */
+  const uint16_t* shared_w3;   /* [Is, H] bf16  up                            */
+  const uint16_t* shared_w2;   /* [H, Is] bf16  down                          */
+  /* second bank (read only when cfg.bank2_begin > 0; E2 = n_experts -
+   * bank2_begin experts, expert bank2_begin + i at index i) */
+  const uint8_t* b2_w1q;       /* [E2, I, L/4]  gate codes                    */
+  const uint16_t* b2_w1s;      /* [E2, I, L/64] bf16 scales                   */
+  const uint16_t* b2_w1b;      /* [E2, I, L/64] bf16 biases                   */
+  const uint8_t* b2_w3q;       /* up, as gate                                 */
+  const uint16_t* b2_w3s;
+  const uint16_t* b2_w3b;
+  const uint8_t* b2_w2q;       /* [E2, L, I/4]  down codes                    */
+  const uint16_t* b2_w2s;      /* [E2, L, I/64]                               */
+  const uint16_t* b2_w2b;
 } k3moe_weights;
 
 /* Creates a context on `cuda_device` and allocates its device workspace for
@@ -159,6 +210,29 @@ const char* k3moe_last_error(const k3moe_ctx* ctx);
  * a no-op. */
 void k3moe_destroy(k3moe_ctx* ctx);
 
+/* ---- expert parallelism: the block split at the combine ---- */
+
+/* The routed chain of one forward up to the score-weighted combine, for
+ * this context's experts only: router and top-K over all experts (topk_idx
+ * and topk_w as in k3moe_forward, global expert ids), then
+ *   c_partial[t] = sum over k in k order, for the selected experts this
+ *                  context holds, of topk_w[t,k] * o_k     (fp32, [T, L])
+ * and no RMSNorm.  For a context without a shard c_partial is the whole
+ * combine.  The shards' c_partial are summed by the caller (one fp32
+ * all-reduce of [T, L]; for two shards, c_0 + c_1), because RMSNorm needs
+ * the whole combine.  Device pointers, 16-byte aligned; asynchronous on
+ * `cuda_stream`; no allocation.  The REAP saliency, when enabled, covers
+ * this context's experts (sums indexed by local expert id). */
+int k3moe_forward_partial(k3moe_ctx* ctx, const void* x, int T, float* c_partial, int32_t* topk_idx,
+                          float* topk_w, void* cuda_stream);
+
+/* The rest of the block for a given combine c_sum [T, L] fp32 (device):
+ * n = bf16(c_sum / sqrt(mean(c_sum^2) + eps) * gamma), y = bf16(Wu . n),
+ * plus the shared experts of x when configured (x [T, H] bf16 device; may
+ * be NULL otherwise).  k3moe_finish(k3moe_forward_partial(x)) on a context
+ * without a shard equals k3moe_forward(x).  Asynchronous; no allocation. */
+int k3moe_finish(k3moe_ctx* ctx, const void* x, const float* c_sum, int T, void* y, void* cuda_stream);
+
 /* ---- step entry points (the hot path's steps, callable on their own) ---- */
 
 /* MXFP4 -> bf16 dequantisation of a [rows, cols] matrix in checkpoint
@@ -210,6 +284,26 @@ int k3moe_route_noalloc(const void* x, int T, const void* router_w, const float*
                         int norm_topk, float routed_scaling, int32_t* topk_idx, float* topk_w,
                         void* cuda_stream);
 
+/* ---- REAP saliency (calibration by-product of the forward) ---- */
+
+/* REAP expert saliency (kimi-k3-mlx README, "REAP expert pruning"):
+ *   S_j = (1/|C|) sum over calibration tokens x of g_j(x) ||e_j(x)||_2,
+ * g_j(x) the routing weight of expert j for x (topk_w; zero when j is not
+ * selected) and e_j(x) the expert's output o in the latent (fp32, before
+ * the combine).  With k3moe_saliency(ctx, 1), every later forward (eager
+ * or replayed from a captured graph) also adds, for each expert, the terms
+ * of its selections to a running fp64 sum -- per expert in slot order (the
+ * tokens ascending), so the totals do not depend on scheduling -- and adds
+ * T to a token count; both live on the device and start at zero.
+ * k3moe_saliency_read synchronises the device and copies the E sums
+ * (`sums`, host, may be NULL) and the token count (`tokens`, host, may be
+ * NULL); S_j = sums[j] / tokens.  k3moe_saliency_reset zeroes both
+ * (synchronising first).  Enabling adds two launches' work to a forward
+ * (the per-slot norms in the combine kernel, one accumulation kernel). */
+int k3moe_saliency(k3moe_ctx* ctx, int enable);
+int k3moe_saliency_read(k3moe_ctx* ctx, double* sums, int n_experts, unsigned long long* tokens);
+int k3moe_saliency_reset(k3moe_ctx* ctx);
+
 /* ---- inspection (tests and tools) ---- */
 
 enum {
@@ -222,7 +316,9 @@ enum {
   K3MOE_BUF_H = 6,      /* [T*K, I] bf16 SiTU-GLU output per slot                */
   K3MOE_BUF_O = 7,      /* [T*K, L] f32 expert output per slot                   */
   K3MOE_BUF_N = 8,      /* [T, L] bf16  RMSNorm output                           */
-  K3MOE_BUF_ACTIVE = 9  /* [E+1]  i32   number of experts with work, then their ids */
+  K3MOE_BUF_ACTIVE = 9, /* [E+1]  i32   number of experts with work, then their ids */
+  K3MOE_BUF_SHARED_H = 10, /* [T, Is] bf16 shared experts' SiTU-GLU output      */
+  K3MOE_BUF_SHARED_Z = 11  /* [T, H] bf16  shared experts' output z              */
 };
 
 /* Copies `bytes` bytes of an internal buffer (K3MOE_BUF_*) of the last
@@ -237,6 +333,19 @@ enum {
   K3MOE_Q_PATH_LAST = 3,       /* path of the last forward (force_path values 1..4) */
   K3MOE_Q_DEVICE = 4           /* CUDA device ordinal                          */
 };
+
+/* Failure detection.  k3moe_check_guards synchronises the device and checks
+ * the 256-byte guard bands the library keeps after every workspace buffer
+ * (filled with 0xA5 at create): K3MOE_OK, or K3MOE_ESTATE naming the first
+ * band a kernel wrote into.  k3moe_test_withhold_copies is a test hook: the
+ * next forward's block-scaled gate/up kernel issues no copies for the first
+ * pipeline stage of one work item, so that the CTA's bounded waits run out
+ * (after spin_timeout_ms), it records K3MOE_ETIMEOUT in the status word,
+ * frees its tensor memory and returns; k3moe_status reports it and clears
+ * it, and later forwards are unaffected (the hook acts once).  Only that
+ * forward's outputs are invalid. */
+int k3moe_check_guards(k3moe_ctx* ctx);
+int k3moe_test_withhold_copies(k3moe_ctx* ctx);
 
 /* Reads a counter or size of the context into *value. */
 int k3moe_query(const k3moe_ctx* ctx, int what, long long* value);

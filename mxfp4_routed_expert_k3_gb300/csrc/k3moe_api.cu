@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <cstring>
 #include <string>
+#include <vector>
 
 #include "../../include/k3moe.h"
 #include "k3moe_device.cuh"
@@ -16,6 +17,9 @@
 namespace {
 
 thread_local std::string g_create_error = "no error";
+
+constexpr size_t kGuardBytes = 256;
+constexpr int kGuardByte = 0xA5;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -36,6 +40,35 @@ struct k3moe_ctx {
   uint16_t* wu = nullptr;       // [H, L]
   uint8_t* gu_tiles = nullptr;  // [E][I/128][L/64][2][tile]
   uint8_t* d_tiles = nullptr;   // [E][L/128][I/64][tile]
+  // shared experts: gate/up rows interleaved (2j gate_j, 2j+1 up_j), so a
+  // GEMM epilogue finds both halves of SiTU-GLU in neighbouring rows
+  int Is = 0;                   // n_shared * shared_inter (0: none)
+  uint16_t* wsh_gu = nullptr;   // [2 Is, H]
+  uint16_t* wsh_d = nullptr;    // [H, Is]
+  uint16_t* sh_h = nullptr;     // workspace [Tm, Is]
+  uint16_t* sh_z = nullptr;     // workspace [Tm, H]
+  float* sh_part = nullptr;     // workspace: split-K partials of the side stream
+  cudaStream_t side = nullptr;  // the shared experts run here, beside the routed chain
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  // expert shard: experts [shard.begin, shard.begin + E_local) of the router's E
+  k3::ExpertShard shard{};
+  int E_local = 0;
+  bool sharded = false;
+  // second bank (two-bank graded experts): experts >= bank2_begin in 2-bit tiles
+  int bank2_begin = 0;           // 0: one bank
+  uint8_t* gu2_tiles = nullptr;  // [E2][I/128][L/64][2][2560]
+  uint8_t* d2_tiles = nullptr;   // [E2][L/128][I/64][2560]
+  int* iota = nullptr;   // workspace [Tm]: 0, 1, 2, ... (RMSNorm of a given combine)
+  bool test_withhold = false;  // test hook: the next forward's gate/up kernel withholds one stage's copies
+  // guard bands: 256 bytes of kGuardByte after every workspace buffer, to
+  // catch a kernel writing past the end of its buffer (k3moe_check_guards)
+  std::vector<uint8_t*> guards;
+  float* ones = nullptr; // workspace [Tm]: 1.0
+  // REAP saliency accumulation (off unless enabled)
+  bool sal_on = false;
+  float* sal_tk = nullptr;          // workspace [Tm * K]: w_k ||o_k|| of the last forward
+  double* sal_sum = nullptr;        // [E] running sums (zero at create and reset)
+  unsigned long long* sal_tokens = nullptr;  // calibration tokens accumulated
   size_t weight_bytes = 0;
   bool loaded = false;
   // workspace
@@ -106,6 +139,27 @@ int check_config(const k3moe_config* c) {
     return fail(nullptr, K3MOE_EINVAL, "beta, beta_lin must be > 0 and rms_eps >= 0");
   if (c->spin_timeout_ms < 0) return fail(nullptr, K3MOE_EINVAL, "spin_timeout_ms must be >= 0");
   if (c->force_path < 0 || c->force_path > 4) return fail(nullptr, K3MOE_EINVAL, "force_path must be 0..4");
+  if (c->n_shared < 0 || c->shared_inter < 0 || (c->n_shared > 0) != (c->shared_inter > 0))
+    return fail(nullptr, K3MOE_EINVAL, "n_shared and shared_inter must both be 0 or both positive");
+  if (c->n_shared > 0) {
+    const long long Is = (long long)c->n_shared * c->shared_inter;
+    if (Is % 128 || Is > (1 << 16))
+      return fail(nullptr, K3MOE_EINVAL, "n_shared * shared_inter must be a multiple of 128 and <= 65536");
+    if (c->force_path == 1 || c->force_path == 3)
+      return fail(nullptr, K3MOE_EINVAL, "shared experts need force_path 0, 2 or 4 (tensor-core dense GEMMs)");
+  }
+  if (c->expert_begin < 0 || c->expert_count < 0 || c->expert_begin + c->expert_count > c->n_experts ||
+      (c->expert_count == 0 && c->expert_begin != 0))
+    return fail(nullptr, K3MOE_EINVAL, "expert shard [%d, %d + %d) outside [0, n_experts=%d)", c->expert_begin,
+                c->expert_begin, c->expert_count, c->n_experts);
+  if (c->expert_count > 0 && c->expert_count < c->n_experts && (c->force_path == 1 || c->force_path == 3))
+    return fail(nullptr, K3MOE_EINVAL, "an expert shard needs force_path 0, 2 or 4");
+  if (c->bank2_begin < 0 || c->bank2_begin >= c->n_experts)
+    return fail(nullptr, K3MOE_EINVAL, "bank2_begin must be 0 (one bank) or in [1, n_experts) (got %d)",
+                c->bank2_begin);
+  if (c->bank2_begin > 0 && ((c->expert_count > 0 && c->expert_count < c->n_experts) ||
+                             (c->force_path != 0 && c->force_path != 4)))
+    return fail(nullptr, K3MOE_EINVAL, "a second bank needs force_path 0 or 4 and no expert shard");
   return K3MOE_OK;
 }
 
@@ -144,20 +198,31 @@ int k3moe_create(const k3moe_config* cfg, int cuda_device, k3moe_ctx** out) {
   const size_t nblk = (Tm * K + k3::kPermChunk - 1) / k3::kPermChunk;
   c->sz_logits = Tm * E * 4;
   c->sz_lat = Tm * L * 2;
-  c->sz_counts = E * 4;
-  c->sz_offsets = (E + 1) * 4;
-  c->sz_active = (E + 1) * 4;
+  c->E_local = cfg->expert_count > 0 ? cfg->expert_count : cfg->n_experts;
+  c->sharded = c->E_local < cfg->n_experts;
+  c->shard.begin = c->sharded ? cfg->expert_begin : 0;
+  c->shard.n_listed = c->E_local;
+  c->shard.n_buckets = c->sharded ? c->E_local + 1 : c->E_local;
+  c->bank2_begin = cfg->bank2_begin;
+  // bucket arrays: counts [buckets], offsets and active [buckets + 1]
+  c->sz_counts = (E + 1) * 4;
+  c->sz_offsets = (E + 2) * 4;
+  c->sz_active = (E + 2) * 4;
   c->sz_perm = Tm * K * 4;
   c->sz_h = Tm * K * I * 2;
   c->sz_o = Tm * K * L * 4;
   c->sz_n = Tm * L * 2;
   c->umma = k3::umma_plan(c->d, (int)Tm);
   const size_t bs_bytes = k3::bs_ws_bytes(c->d, (int)Tm);
+  c->Is = cfg->n_shared * cfg->shared_inter;
+  const size_t Is = (size_t)c->Is;
+  const size_t sh_part = Is ? k3::dense_small_part_floats((int)std::max(2 * Is, H)) * 4 : 0;
   const size_t parts[] = {c->sz_logits, c->sz_lat,   c->sz_counts, c->sz_offsets, c->sz_active, c->sz_perm,
-                          c->sz_perm,   nblk * E * 4, c->sz_h,     c->sz_o,       c->sz_n,      256,
-                          Tm * H * 2,   Tm * H * 2,   Tm * K * 4,  Tm * K * 4,    c->umma.ws_bytes, bs_bytes};
+                          c->sz_perm,   nblk * (E + 1) * 4, c->sz_h, c->sz_o,       c->sz_n,      256,
+                          Tm * H * 2,   Tm * H * 2,   Tm * K * 4,  Tm * K * 4,    c->umma.ws_bytes, bs_bytes,
+                          Tm * Is * 2,  Is ? Tm * H * 2 : 0, sh_part,   Tm * K * 4,  E * 8 + 8,  Tm * 4,  Tm * 4};
   size_t total = 0;
-  for (size_t p : parts) total += align_up(p, 256);
+  for (size_t p : parts) total += align_up(p, 256) + kGuardBytes;
   e = cudaMalloc(&c->ws, total);
   if (e != cudaSuccess) {
     fail(nullptr, K3MOE_ENOMEM, "workspace of %zu bytes for max_tokens=%d: %s", total, cfg->max_tokens,
@@ -170,6 +235,8 @@ int k3moe_create(const k3moe_config* cfg, int cuda_device, k3moe_ctx** out) {
   auto take = [&](size_t n) {
     char* r = p;
     p += align_up(n, 256);
+    c->guards.push_back(reinterpret_cast<uint8_t*>(p));
+    p += kGuardBytes;
     return r;
   };
   c->w.logits = (float*)take(parts[0]);
@@ -193,6 +260,14 @@ int k3moe_create(const k3moe_config* cfg, int cuda_device, k3moe_ctx** out) {
   c->umma.num_sms = prop.multiProcessorCount;
   c->umma.limit_ns = (uint64_t)c->cfg.spin_timeout_ms * 1000000ull;
   c->bs.ws = take(parts[17]);
+  c->sh_h = (uint16_t*)take(parts[18]);
+  c->sh_z = (uint16_t*)take(parts[19]);
+  c->sh_part = (float*)take(parts[20]);
+  c->sal_tk = (float*)take(parts[21]);
+  c->sal_sum = (double*)take(parts[22]);
+  c->sal_tokens = (unsigned long long*)(c->sal_sum + E);
+  c->iota = (int*)take(parts[23]);
+  c->ones = (float*)take(parts[24]);
   c->bs.ws_bytes = bs_bytes;
   c->bs.max_tokens = (int)Tm;
   c->bs.status = c->w.status;
@@ -200,9 +275,21 @@ int k3moe_create(const k3moe_config* cfg, int cuda_device, k3moe_ctx** out) {
   c->bs.limit_ns = c->umma.limit_ns;
   c->bs.dims = c->d;
   e = cudaMemset(c->ws, 0, total);
+  for (uint8_t* gp : c->guards)
+    if (e == cudaSuccess) e = cudaMemset(gp, kGuardByte, kGuardBytes);
+  if (e == cudaSuccess) {
+    std::vector<int> iota(Tm);
+    std::vector<float> ones(Tm, 1.0f);
+    for (size_t i = 0; i < Tm; ++i) iota[i] = (int)i;
+    e = cudaMemcpy(c->iota, iota.data(), Tm * 4, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(c->ones, ones.data(), Tm * 4, cudaMemcpyHostToDevice);
+  }
   if (e == cudaSuccess) e = k3::prepare_decode_kernels(c->d);
   if (e == cudaSuccess) e = k3::prepare_umma_kernels();
   if (e == cudaSuccess) e = k3::prepare_bs_kernels();
+  if (e == cudaSuccess && c->Is) e = cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking);
+  if (e == cudaSuccess && c->Is) e = cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess && c->Is) e = cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     fail(nullptr, K3MOE_ECUDA, "workspace / kernel setup: %s", cudaGetErrorString(e));
     cudaFree(c->ws);
@@ -225,6 +312,13 @@ void k3moe_destroy(k3moe_ctx* c) {
   cudaFree(c->gu_tiles);
   cudaFree(c->d_tiles);
   cudaFree(c->bw.gu_q);
+  cudaFree(c->wsh_gu);
+  cudaFree(c->wsh_d);
+  cudaFree(c->gu2_tiles);
+  cudaFree(c->d2_tiles);
+  if (c->side) cudaStreamDestroy(c->side);
+  if (c->ev_fork) cudaEventDestroy(c->ev_fork);
+  if (c->ev_join) cudaEventDestroy(c->ev_join);
   for (cudaEvent_t ev : c->prof_ev)
     if (ev) cudaEventDestroy(ev);
   delete c;
@@ -239,7 +333,21 @@ int k3moe_load_weights(k3moe_ctx* c, const k3moe_weights* wt) {
                         wt->w3_scale,  wt->w2_packed,   wt->w2_scale,  wt->norm_w,    wt->up_proj};
   for (const void* q : ptrs)
     if (!q) return fail(c, K3MOE_EINVAL, "a weight pointer is NULL");
-  const size_t H = c->d.H, L = c->d.L, E = c->d.E, I = c->d.I;
+  if (c->Is && (!wt->shared_w1 || !wt->shared_w3 || !wt->shared_w2))
+    return fail(c, K3MOE_EINVAL, "the context has shared experts but a shared weight pointer is NULL");
+  if (c->bank2_begin) {
+    const void* b2[] = {wt->b2_w1q, wt->b2_w1s, wt->b2_w1b, wt->b2_w3q, wt->b2_w3s,
+                        wt->b2_w3b, wt->b2_w2q, wt->b2_w2s, wt->b2_w2b};
+    for (const void* q : b2)
+      if (!q) return fail(c, K3MOE_EINVAL, "the context has a second bank but a b2_* pointer is NULL");
+  }
+  // the router, bias and dense weights cover all Er experts; the expert
+  // tensors hold this context's E (its shard, or all of them)
+  // (with a second bank the MXFP4 tensors hold its first bank2_begin experts)
+  const size_t H = c->d.H, L = c->d.L, Er = c->d.E, I = c->d.I;
+  const size_t E = c->bank2_begin ? (size_t)c->bank2_begin : (size_t)c->E_local;
+  k3::Dims dx = c->d;
+  dx.E = (int)E;
   const size_t n_gu_scale = E * I * (L / 32), n_d_scale = E * L * (I / 32);
   const uint8_t* scales[] = {wt->w1_scale, wt->w3_scale, wt->w2_scale};
   const size_t nscales[] = {n_gu_scale, n_gu_scale, n_d_scale};
@@ -257,8 +365,8 @@ int k3moe_load_weights(k3moe_ctx* c, const k3moe_weights* wt) {
   // default (path 4) reads the block-scaled copy alone.
   const bool want_tiles = c->cfg.force_path >= 1 && c->cfg.force_path <= 3;
   if (!c->wcat) {
-    K3_CUDA(c, cudaMalloc(&c->wcat, (E + L) * H * 2), "cudaMalloc(router+down_proj)");
-    K3_CUDA(c, cudaMalloc(&c->bias, E * 4), "cudaMalloc(bias)");
+    K3_CUDA(c, cudaMalloc(&c->wcat, (Er + L) * H * 2), "cudaMalloc(router+down_proj)");
+    K3_CUDA(c, cudaMalloc(&c->bias, Er * 4), "cudaMalloc(bias)");
     K3_CUDA(c, cudaMalloc(&c->gamma, L * 2), "cudaMalloc(gamma)");
     K3_CUDA(c, cudaMalloc(&c->wu, H * L * 2), "cudaMalloc(up_proj)");
     if (want_tiles) {
@@ -266,19 +374,34 @@ int k3moe_load_weights(k3moe_ctx* c, const k3moe_weights* wt) {
       K3_CUDA(c, cudaMalloc(&c->d_tiles, d_bytes), "cudaMalloc(down tiles)");
     }
     // block-scaled layout: one allocation, carved as gu_q | gu_sf | d_q | d_sf
-    K3_CUDA(c, cudaMalloc(&c->bw.gu_q, k3::bs_weight_bytes(c->d)), "cudaMalloc(block-scaled experts)");
+    K3_CUDA(c, cudaMalloc(&c->bw.gu_q, k3::bs_weight_bytes(dx)), "cudaMalloc(block-scaled experts)");
+    c->bw.n_exp = (int)E;
     c->bw.gu_sf = c->bw.gu_q + E * 2 * I * L / 2;
     c->bw.d_q = c->bw.gu_sf + E * 2 * I * L / 32;
     c->bw.d_sf = c->bw.d_q + E * L * I / 2;
-    c->weight_bytes = (E + L) * H * 2 + E * 4 + L * 2 + H * L * 2 + (want_tiles ? gu_bytes + d_bytes : 0) +
-                      k3::bs_weight_bytes(c->d);
+    c->weight_bytes = (Er + L) * H * 2 + Er * 4 + L * 2 + H * L * 2 + (want_tiles ? gu_bytes + d_bytes : 0) +
+                      k3::bs_weight_bytes(dx);
   }
   c->loaded = false;
-  K3_CUDA(c, cudaMemcpy(c->wcat, wt->router_w, E * H * 2, cudaMemcpyHostToDevice), "copy router_w");
-  K3_CUDA(c, cudaMemcpy(c->wcat + E * H, wt->down_proj, L * H * 2, cudaMemcpyHostToDevice), "copy down_proj");
-  K3_CUDA(c, cudaMemcpy(c->bias, wt->router_bias, E * 4, cudaMemcpyHostToDevice), "copy bias");
+  K3_CUDA(c, cudaMemcpy(c->wcat, wt->router_w, Er * H * 2, cudaMemcpyHostToDevice), "copy router_w");
+  K3_CUDA(c, cudaMemcpy(c->wcat + Er * H, wt->down_proj, L * H * 2, cudaMemcpyHostToDevice), "copy down_proj");
+  K3_CUDA(c, cudaMemcpy(c->bias, wt->router_bias, Er * 4, cudaMemcpyHostToDevice), "copy bias");
   K3_CUDA(c, cudaMemcpy(c->gamma, wt->norm_w, L * 2, cudaMemcpyHostToDevice), "copy norm_w");
   K3_CUDA(c, cudaMemcpy(c->wu, wt->up_proj, H * L * 2, cudaMemcpyHostToDevice), "copy up_proj");
+  if (c->Is) {
+    const size_t Is = (size_t)c->Is;
+    if (!c->wsh_gu) {
+      K3_CUDA(c, cudaMalloc(&c->wsh_gu, 2 * Is * H * 2), "cudaMalloc(shared gate/up)");
+      K3_CUDA(c, cudaMalloc(&c->wsh_d, H * Is * 2), "cudaMalloc(shared down)");
+      c->weight_bytes += 3 * Is * H * 2;
+    }
+    // gate row j -> row 2j, up row j -> row 2j + 1
+    K3_CUDA(c, cudaMemcpy2D(c->wsh_gu, 2 * H * 2, wt->shared_w1, H * 2, H * 2, Is, cudaMemcpyHostToDevice),
+            "copy shared_w1");
+    K3_CUDA(c, cudaMemcpy2D(c->wsh_gu + H, 2 * H * 2, wt->shared_w3, H * 2, H * 2, Is, cudaMemcpyHostToDevice),
+            "copy shared_w3");
+    K3_CUDA(c, cudaMemcpy(c->wsh_d, wt->shared_w2, H * Is * 2, cudaMemcpyHostToDevice), "copy shared_w2");
+  }
 
   // Experts: stage a chunk of experts of one tensor, re-lay into tiles.
   const size_t per_expert_packed = I * L / 2, per_expert_scale = I * L / 32;  // same for w1/w3/w2
@@ -357,19 +480,68 @@ int k3moe_load_weights(k3moe_ctx* c, const k3moe_weights* wt) {
   cudaFree(st_p);
   cudaFree(st_s);
   if (rc) return rc;
+  if (c->bank2_begin) {
+    // second bank: 2-bit codes + bf16 scale/bias into 2-bit tiles (gate and
+    // up of one (expert, row tile, k step) adjacent); staged per expert
+    const size_t E2 = (size_t)(c->d.E - c->bank2_begin);
+    const size_t gu_t = k3::bank2_tile_bytes((int)I, (int)L), d_t = k3::bank2_tile_bytes((int)L, (int)I);
+    if (!c->gu2_tiles) {
+      K3_CUDA(c, cudaMalloc(&c->gu2_tiles, E2 * 2 * gu_t), "cudaMalloc(second-bank gate/up)");
+      K3_CUDA(c, cudaMalloc(&c->d2_tiles, E2 * d_t), "cudaMalloc(second-bank down)");
+      c->weight_bytes += E2 * (2 * gu_t + d_t);
+    }
+    struct B2Job {
+      const uint8_t* q;
+      const uint16_t *sc, *bi;
+      int rows, cols, step, offset;
+      uint8_t* out;
+      size_t stride_tiles;
+    } b2jobs[3] = {{wt->b2_w1q, wt->b2_w1s, wt->b2_w1b, (int)I, (int)L, 2, 0, c->gu2_tiles, 2 * gu_t / 2560},
+                   {wt->b2_w3q, wt->b2_w3s, wt->b2_w3b, (int)I, (int)L, 2, 1, c->gu2_tiles, 2 * gu_t / 2560},
+                   {wt->b2_w2q, wt->b2_w2s, wt->b2_w2b, (int)L, (int)I, 1, 0, c->d2_tiles, d_t / 2560}};
+    const size_t nq = I * L / 4, ns = I * (L / 64);  // per expert and matrix (same for w2)
+    uint8_t* stage = nullptr;
+    K3_CUDA(c, cudaMalloc(&stage, nq + 2 * ns * 2), "cudaMalloc(staging)");
+    for (const B2Job& j : b2jobs) {
+      for (size_t e2 = 0; e2 < E2 && rc == K3MOE_OK; ++e2) {
+        uint16_t* st_sc = reinterpret_cast<uint16_t*>(stage + nq);
+        uint16_t* st_bi = st_sc + ns;
+        if ((e = cudaMemcpy(stage, j.q + e2 * nq, nq, cudaMemcpyHostToDevice)) ||
+            (e = cudaMemcpy(st_sc, j.sc + e2 * ns, ns * 2, cudaMemcpyHostToDevice)) ||
+            (e = cudaMemcpy(st_bi, j.bi + e2 * ns, ns * 2, cudaMemcpyHostToDevice)) ||
+            (e = k3::bank2_tiles(stage, st_sc, st_bi, 1, j.rows, j.cols, j.out + e2 * j.stride_tiles * 2560,
+                                 j.stride_tiles, j.step, j.offset, 0)) ||
+            (e = cudaDeviceSynchronize()))
+          rc = cuda_fail(c, e, "second-bank tiles");
+      }
+    }
+    cudaFree(stage);
+    if (rc) return rc;
+  }
   c->loaded = true;
   return K3MOE_OK;
 }
 
+// The block for T tokens, in one of three modes:
+//   c_out == c_in == NULL: the whole block, x -> y;
+//   c_out != NULL: the routed chain up to the combine: c_out = the partial
+//                  combine of this context's experts (an expert shard's
+//                  part; all experts without a shard), no RMSNorm;
+//   c_in != NULL:  the rest of the block for a given combine c_in: shared
+//                  experts of x, RMSNorm(c_in), up_proj -> y.
 static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* idx, float* wts,
-                        cudaStream_t s) {
+                        cudaStream_t s, float* c_out = nullptr, const float* c_in = nullptr) {
   const k3::Dims& d = c->d;
+  const bool routed = c_in == nullptr;  // router, permutation, experts, combine
+  const bool tail = c_out == nullptr;   // shared experts, RMSNorm, up_proj
   k3::Work& w = c->w;
   // path: 1 CUDA-core kernels, 2 tensor-core GEMMs, 3 streaming tensor-core
   // kernels (experts decoded to bf16 in TMEM), 4 as 3 with the experts on
   // the block-scaled MXFP4 tensor cores
   int path = c->cfg.force_path;
   if (path == 0) path = 4;
+  c->bs.withhold_item = c->test_withhold ? 0 : -1;
+  c->test_withhold = false;  // one forward only
   const bool stream = path == 3 || path == 4;
   const bool big = path == 2;
   c->path_last = path;
@@ -397,20 +569,62 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
         return cuda_fail(c, e, "profile event");                                        \
     }                                                                                   \
   } while (0)
+  // Shared experts (on the residual x, independent of the routed chain):
+  // gate/up with the SiTU-GLU epilogue -> sh_h, down -> sh_z; up_proj adds
+  // sh_z.  They run on the context's side stream, forked here and joined
+  // before up_proj, so their weight stream overlaps the routing and
+  // expert-permutation latency of the routed chain.  With per-group
+  // profiling they run on `s` instead, as groups of their own.
+  auto shared_launch = [&](cudaStream_t q, float* part) -> cudaError_t {
+    k3::DenseOut o_gu;
+    o_gu.glu = 1;
+    o_gu.out_bf16 = c->sh_h;
+    o_gu.beta = d.beta;
+    o_gu.beta_lin = d.beta_lin;
+    k3::DenseOut o_dn;
+    o_dn.out_bf16 = c->sh_z;
+    cudaError_t r;
+    if (T <= 64) {
+      r = k3::umma_dense_small(c->umma, c->wsh_gu, 2 * c->Is, d.H, (const uint16_t*)x, T, o_gu, part, q);
+      if (r == cudaSuccess) r = k3::umma_dense_small(c->umma, c->wsh_d, d.H, c->Is, c->sh_h, T, o_dn, part, q);
+    } else {
+      r = k3::umma_dense(c->umma, c->wsh_gu, 2 * c->Is, d.H, (const uint16_t*)x, T, o_gu, q);
+      if (r == cudaSuccess) r = k3::umma_dense(c->umma, c->wsh_d, d.H, c->Is, c->sh_h, T, o_dn, q);
+    }
+    return r;
+  };
+  const int shared_launches = c->Is ? 2 * (T <= 64 ? k3::umma_dense_small_launches() : k3::umma_dense_launches()) : 0;
+  const bool shared_side = tail && c->Is && !c->prof;
+  if (shared_side) {
+    if ((e = cudaEventRecord(c->ev_fork, s)) != cudaSuccess) return cuda_fail(c, e, "fork event");
+    if ((e = cudaStreamWaitEvent(c->side, c->ev_fork, 0)) != cudaSuccess) return cuda_fail(c, e, "fork wait");
+    if ((e = shared_launch(c->side, c->sh_part)) != cudaSuccess) return cuda_fail(c, e, "shared experts");
+    if ((e = cudaEventRecord(c->ev_join, c->side)) != cudaSuccess) return cuda_fail(c, e, "join event");
+    n += shared_launches;
+  }
+  // the slots of this context's experts: all of them without a shard
+  const int* n_local = w.offsets + c->shard.n_listed;
+  if (routed) {
+  // router logits (fp32) and the latent (bf16) from one pass over [Wr; Wd]
+  k3::DenseOut o_route;
+  o_route.split = d.E;
+  o_route.out_f32 = w.logits;
+  o_route.out_bf16 = w.lat;
   if (big) {
-    K3_LAUNCH(k3::umma_dense(c->umma, c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, d.E, w.logits, w.lat, s),
+    K3_LAUNCH(k3::umma_dense(c->umma, c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, o_route, s),
               k3::umma_dense_launches(), "router + down_proj (tensor cores)");
   } else if (stream && T <= 64) {
-    K3_LAUNCH(k3::umma_dense_small(c->umma, c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, d.E, w.logits, w.lat, s),
-              1, "router + down_proj");
+    K3_LAUNCH(k3::umma_dense_small(c->umma, c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, o_route, nullptr, s),
+              k3::umma_dense_small_launches(), "router + down_proj");
   } else if (path == 4) {
-    K3_LAUNCH(k3::umma_dense(c->umma, c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, d.E, w.logits, w.lat, s),
+    K3_LAUNCH(k3::umma_dense(c->umma, c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, o_route, s),
               k3::umma_dense_launches(), "router + down_proj");
   } else {
     K3_LAUNCH(k3::launch_dense_gemv(c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, d.E, w.logits, w.lat, s), 1,
               "router + down_proj");
   }
   const bool fused_route = stream && T * d.K <= 1024;
+  const int split_expert = c->bank2_begin ? c->bank2_begin : (1 << 30);
   if (fused_route) {
     int4* tiles;
     int* tile_count;
@@ -419,13 +633,15 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
     // path 4 also needs the slot -> tile map (its tiles have bs_tile_rows(T) <= bn rows)
     int* slot_tile = path == 4 ? k3::bs_slot_tile(c->bs) : nullptr;
     if (path == 4) bn = k3::bs_tile_rows(T);
-    K3_LAUNCH(k3::launch_route_small(w.logits, T, d.E, c->bias, d.K, d.norm_topk, d.rsf, idx, wts, w.counts,
-                                     w.offsets, w.active, w.perm, w.slot, bn, tiles, tile_count, slot_tile, s),
+    K3_LAUNCH(k3::launch_route_small(w.logits, T, d.E, c->bias, d.K, d.norm_topk, d.rsf, c->shard, idx, wts,
+                                     w.counts, w.offsets, w.active, w.perm, w.slot, bn, tiles, tile_count, slot_tile,
+                                     split_expert, s),
               2, "top-k + permute");
   } else {
     K3_LAUNCH(k3::launch_topk(w.logits, T, d.E, d.E, c->bias, d.K, d.norm_topk, d.rsf, idx, wts, s), 1, "top-k");
-    K3_LAUNCH(k3::launch_permute(idx, T, d.K, d.E, w.blk_hist, w.counts, w.offsets, w.active, w.perm, w.slot, s), 3,
-              "permute");
+    K3_LAUNCH(k3::launch_permute(idx, T, d.K, c->shard, w.blk_hist, w.counts, w.offsets, w.active, w.perm, w.slot,
+                                 s),
+              3, "permute");
   }
   const int max_active = std::min(d.E, T * d.K);
   if (big) {
@@ -438,11 +654,20 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
     k3::umma_tile_list(c->umma, &tiles, &tile_count, &bn);
     bn = k3::bs_tile_rows(T);
     if (!fused_route)
-      K3_LAUNCH(k3::umma_stream_tiles(c->umma, w, T, d, bn, k3::bs_slot_tile(c->bs), s), 1, "tile list");
-    K3_LAUNCH(k3::bs_quantize_latent(c->bs, w, T, d, bn, s), 1,
+      K3_LAUNCH(k3::umma_stream_tiles(c->umma, w, T, d, bn, k3::bs_slot_tile(c->bs), split_expert, s), 1,
+                "tile list");
+    K3_LAUNCH(k3::bs_quantize_latent(c->bs, w, T, d, bn, c->sharded ? n_local : nullptr, s), 1,
               bn <= 16 ? "latent rows -> e2m1 terms" : "latent rows -> e4m3 terms");
-    K3_LAUNCH(k3::bs_stream_gateup(c->bs, c->bw, tiles, tile_count, w, T, d, bn, s), 1, "gate/up");
-    K3_LAUNCH(k3::bs_stream_down(c->bs, c->bw, tiles, tile_count, w, T, d, bn, s), 1, "down");
+    // with a second bank the block-scaled kernels take the first bank's
+    // tiles [0, count[1]) and the second bank's kernels the rest: the split
+    // is read on the device, no host synchronisation
+    const int* count_a = c->bank2_begin ? tile_count + 1 : tile_count;
+    K3_LAUNCH(k3::bs_stream_gateup(c->bs, c->bw, tiles, count_a, w, T, d, bn, s), 1, "gate/up");
+    K3_LAUNCH(k3::bs_stream_down(c->bs, c->bw, tiles, count_a, w, T, d, bn, s), 1, "down");
+    if (c->bank2_begin)
+      K3_LAUNCH(k3::umma_bank2_experts(c->umma, c->gu2_tiles, c->d2_tiles, c->bank2_begin, d.E - c->bank2_begin, bn,
+                                       w, T, d, s),
+                3, "second bank (2-bit)");
   } else if (path == 3) {
     if (fused_route)
       K3_LAUNCH(k3::umma_stream_gather(c->umma, w, T, d, s), 1, "gather");
@@ -455,15 +680,37 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
               "gate/up");
     K3_LAUNCH(k3::launch_down_gemv(c->d_tiles, w.h, w.active, w.offsets, max_active, d, w.o, s), 1, "down");
   }
-  K3_LAUNCH(k3::launch_combine_rmsnorm(w.o, w.slot, wts, c->gamma, T, d, w.n, s), 1, "combine + RMSNorm");
+  K3_LAUNCH(k3::launch_combine_rmsnorm(w.o, w.slot, wts, c->gamma, T, d.K, d, w.n, c->sal_on ? c->sal_tk : nullptr,
+                                       n_local, c_out, s),
+            1, c_out ? "partial combine" : "combine + RMSNorm");
+  if (c->sal_on)
+    K3_LAUNCH(k3::launch_saliency_accumulate(c->sal_tk, w.perm, w.offsets, w.active, T, d.E, c->sal_sum,
+                                             c->sal_tokens, s),
+              1, "REAP saliency");
+  } else {
+    // RMSNorm of the given combine: one "slot" per token (slot t = row t of
+    // c_in) with weight 1, so c = c_in exactly
+    K3_LAUNCH(k3::launch_combine_rmsnorm(c_in, c->iota, c->ones, c->gamma, T, 1, d, w.n, nullptr, nullptr, nullptr, s),
+              1, "RMSNorm");
+  }
+  if (!tail) {
+    c->launches_last = n;
+    return K3MOE_OK;
+  }
+  if (c->Is && !shared_side)
+    K3_LAUNCH(shared_launch(s, c->sh_part), shared_launches, "shared experts");
+  if (shared_side && (e = cudaStreamWaitEvent(s, c->ev_join, 0)) != cudaSuccess) return cuda_fail(c, e, "join wait");
+  k3::DenseOut o_up;
+  o_up.out_bf16 = (uint16_t*)y;
+  o_up.add_bf16 = c->Is ? c->sh_z : nullptr;
   if (big) {
-    K3_LAUNCH(k3::umma_dense(c->umma, c->wu, d.H, d.L, w.n, T, 0, nullptr, (uint16_t*)y, s),
-              k3::umma_dense_launches(), "up_proj (tensor cores)");
+    K3_LAUNCH(k3::umma_dense(c->umma, c->wu, d.H, d.L, w.n, T, o_up, s), k3::umma_dense_launches(),
+              "up_proj (tensor cores)");
   } else if (stream && T <= 64) {
-    K3_LAUNCH(k3::umma_dense_small(c->umma, c->wu, d.H, d.L, w.n, T, 0, nullptr, (uint16_t*)y, s), 1, "up_proj");
+    K3_LAUNCH(k3::umma_dense_small(c->umma, c->wu, d.H, d.L, w.n, T, o_up, nullptr, s),
+              k3::umma_dense_small_launches(), "up_proj");
   } else if (path == 4) {
-    K3_LAUNCH(k3::umma_dense(c->umma, c->wu, d.H, d.L, w.n, T, 0, nullptr, (uint16_t*)y, s),
-              k3::umma_dense_launches(), "up_proj");
+    K3_LAUNCH(k3::umma_dense(c->umma, c->wu, d.H, d.L, w.n, T, o_up, s), k3::umma_dense_launches(), "up_proj");
   } else {
     K3_LAUNCH(k3::launch_dense_gemv(c->wu, d.H, d.L, w.n, T, 0, nullptr, (uint16_t*)y, s), 1, "up_proj");
   }
@@ -485,8 +732,43 @@ int k3moe_forward(k3moe_ctx* c, const void* x, int T, void* y, int32_t* topk_idx
   if (!x || !y || !topk_idx || !topk_w) return fail(c, K3MOE_EINVAL, "a device pointer is NULL");
   if (!aligned16(x) || !aligned16(y) || !aligned16(topk_idx) || !aligned16(topk_w))
     return fail(c, K3MOE_EINVAL, "x, y, topk_idx and topk_w must be 16-byte aligned");
+  if (c->sharded)
+    return fail(c, K3MOE_ESTATE, "an expert shard has no whole forward: use k3moe_forward_partial and k3moe_finish");
   K3_CUDA(c, cudaSetDevice(c->device), "cudaSetDevice");
   return forward_impl(c, x, T, y, topk_idx, topk_w, (cudaStream_t)cuda_stream);
+}
+
+int k3moe_forward_partial(k3moe_ctx* c, const void* x, int T, float* c_partial, int32_t* topk_idx, float* topk_w,
+                          void* cuda_stream) {
+  if (!c) return fail(nullptr, K3MOE_EINVAL, "ctx is NULL");
+  if (!c->loaded) return fail(c, K3MOE_ESTATE, "forward before load_weights");
+  if (T < 0 || T > c->cfg.max_tokens)
+    return fail(c, K3MOE_EINVAL, "T=%d outside [0, max_tokens=%d]", T, c->cfg.max_tokens);
+  if (T == 0) {
+    c->launches_last = 0;
+    return K3MOE_OK;
+  }
+  if (!x || !c_partial || !topk_idx || !topk_w) return fail(c, K3MOE_EINVAL, "a device pointer is NULL");
+  if (!aligned16(x) || !aligned16(c_partial) || !aligned16(topk_idx) || !aligned16(topk_w))
+    return fail(c, K3MOE_EINVAL, "x, c_partial, topk_idx and topk_w must be 16-byte aligned");
+  K3_CUDA(c, cudaSetDevice(c->device), "cudaSetDevice");
+  return forward_impl(c, x, T, nullptr, topk_idx, topk_w, (cudaStream_t)cuda_stream, c_partial, nullptr);
+}
+
+int k3moe_finish(k3moe_ctx* c, const void* x, const float* c_sum, int T, void* y, void* cuda_stream) {
+  if (!c) return fail(nullptr, K3MOE_EINVAL, "ctx is NULL");
+  if (!c->loaded) return fail(c, K3MOE_ESTATE, "finish before load_weights");
+  if (T < 0 || T > c->cfg.max_tokens)
+    return fail(c, K3MOE_EINVAL, "T=%d outside [0, max_tokens=%d]", T, c->cfg.max_tokens);
+  if (T == 0) {
+    c->launches_last = 0;
+    return K3MOE_OK;
+  }
+  if (!c_sum || !y || (c->Is && !x)) return fail(c, K3MOE_EINVAL, "a device pointer is NULL");
+  if (!aligned16(c_sum) || !aligned16(y) || (x && !aligned16(x)))
+    return fail(c, K3MOE_EINVAL, "x, c_sum and y must be 16-byte aligned");
+  K3_CUDA(c, cudaSetDevice(c->device), "cudaSetDevice");
+  return forward_impl(c, x, T, y, nullptr, nullptr, (cudaStream_t)cuda_stream, nullptr, c_sum);
 }
 
 int k3moe_forward_host(k3moe_ctx* c, const void* x_host, int T, void* y_host, int32_t* idx_host, float* w_host,
@@ -497,6 +779,8 @@ int k3moe_forward_host(k3moe_ctx* c, const void* x_host, int T, void* y_host, in
     return fail(c, K3MOE_EINVAL, "T=%d outside [0, max_tokens=%d]", T, c->cfg.max_tokens);
   if (T == 0) return K3MOE_OK;
   if (!x_host) return fail(c, K3MOE_EINVAL, "x_host is NULL");
+  if (c->sharded)
+    return fail(c, K3MOE_ESTATE, "an expert shard has no whole forward: use k3moe_forward_partial and k3moe_finish");
   K3_CUDA(c, cudaSetDevice(c->device), "cudaSetDevice");
   cudaStream_t s = (cudaStream_t)cuda_stream;
   const size_t H = c->d.H, K = c->d.K;
@@ -522,8 +806,6 @@ int k3moe_status(k3moe_ctx* c) {
   if (st) {
     unsigned zero = 0;
     K3_CUDA(c, cudaMemcpy(c->w.status, &zero, 4, cudaMemcpyHostToDevice), "clear status");
-    // an aborted call can leave the split-K completion counters mid-count
-    K3_CUDA(c, k3::umma_reset_counters(c->umma), "reset counters");
     return fail(c, K3MOE_ETIMEOUT, "a device-side wait gave up (status word 0x%08x)", st);
   }
   return K3MOE_OK;
@@ -545,6 +827,8 @@ int k3moe_fetch(k3moe_ctx* c, int which, void* dst, size_t bytes) {
     case K3MOE_BUF_O: src = c->w.o; cap = c->sz_o; break;
     case K3MOE_BUF_N: src = c->w.n; cap = c->sz_n; break;
     case K3MOE_BUF_ACTIVE: src = c->w.active; cap = c->sz_active; break;
+    case K3MOE_BUF_SHARED_H: src = c->sh_h; cap = (size_t)c->cfg.max_tokens * c->Is * 2; break;
+    case K3MOE_BUF_SHARED_Z: src = c->sh_z; cap = c->Is ? (size_t)c->cfg.max_tokens * c->d.H * 2 : 0; break;
     default: return fail(c, K3MOE_EINVAL, "unknown buffer %d", which);
   }
   if (bytes > cap) return fail(c, K3MOE_EINVAL, "buffer %d holds %zu bytes, %zu requested", which, cap, bytes);
@@ -564,6 +848,50 @@ int k3moe_query(const k3moe_ctx* c, int what, long long* value) {
     case K3MOE_Q_DEVICE: *value = c->device; return K3MOE_OK;
     default: return fail(nullptr, K3MOE_EINVAL, "unknown query %d", what);
   }
+}
+
+int k3moe_test_withhold_copies(k3moe_ctx* c) {
+  if (!c) return fail(nullptr, K3MOE_EINVAL, "ctx is NULL");
+  c->test_withhold = true;
+  return K3MOE_OK;
+}
+
+int k3moe_check_guards(k3moe_ctx* c) {
+  if (!c) return fail(nullptr, K3MOE_EINVAL, "ctx is NULL");
+  K3_CUDA(c, cudaSetDevice(c->device), "cudaSetDevice");
+  K3_CUDA(c, cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+  std::vector<uint8_t> band(kGuardBytes);
+  for (size_t i = 0; i < c->guards.size(); ++i) {
+    K3_CUDA(c, cudaMemcpy(band.data(), c->guards[i], kGuardBytes, cudaMemcpyDeviceToHost), "read guard band");
+    for (size_t j = 0; j < kGuardBytes; ++j)
+      if (band[j] != (uint8_t)kGuardByte)
+        return fail(c, K3MOE_ESTATE, "guard band after workspace buffer %zu overwritten at byte %zu", i, j);
+  }
+  return K3MOE_OK;
+}
+
+int k3moe_saliency(k3moe_ctx* c, int enable) {
+  if (!c) return fail(nullptr, K3MOE_EINVAL, "ctx is NULL");
+  c->sal_on = enable != 0;
+  return K3MOE_OK;
+}
+
+int k3moe_saliency_read(k3moe_ctx* c, double* sums, int n_experts, unsigned long long* tokens) {
+  if (!c) return fail(nullptr, K3MOE_EINVAL, "ctx is NULL");
+  if (n_experts != c->d.E) return fail(c, K3MOE_EINVAL, "n_experts %d != the context's %d", n_experts, c->d.E);
+  K3_CUDA(c, cudaSetDevice(c->device), "cudaSetDevice");
+  K3_CUDA(c, cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+  if (sums) K3_CUDA(c, cudaMemcpy(sums, c->sal_sum, (size_t)c->d.E * 8, cudaMemcpyDeviceToHost), "read sums");
+  if (tokens) K3_CUDA(c, cudaMemcpy(tokens, c->sal_tokens, 8, cudaMemcpyDeviceToHost), "read token count");
+  return K3MOE_OK;
+}
+
+int k3moe_saliency_reset(k3moe_ctx* c) {
+  if (!c) return fail(nullptr, K3MOE_EINVAL, "ctx is NULL");
+  K3_CUDA(c, cudaSetDevice(c->device), "cudaSetDevice");
+  K3_CUDA(c, cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+  K3_CUDA(c, cudaMemset(c->sal_sum, 0, (size_t)c->d.E * 8 + 8), "clear saliency");
+  return K3MOE_OK;
 }
 
 int k3moe_profile(k3moe_ctx* c, int enable) {

@@ -169,10 +169,12 @@ __device__ __forceinline__ int act_scale_byte(int t, int n, int stack) { return 
 // loop runs per warp so that both halves always meet at the shuffles.
 constexpr int kQuantChunks = 4;
 __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, const int* __restrict__ perm, int K, int rows,
-                                  int C, int rows_max, const int* __restrict__ slot_tile, int stack,
-                                  uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+                                  const int* __restrict__ rows_dev, int C, int rows_max,
+                                  const int* __restrict__ slot_tile, int stack, uint8_t* __restrict__ q,
+                                  uint8_t* __restrict__ sf) {
   pdl_trigger();
   pdl_wait();
+  if (rows_dev) rows = min(rows, *rows_dev);  // an expert shard: its own slots only
   const int hl = threadIdx.x & 15, half = (threadIdx.x >> 4) & 1;
   const int KC = C / kQK;
   const int KG = (KC + kQuantChunks - 1) / kQuantChunks;  // chunk groups per row
@@ -251,10 +253,12 @@ __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, const int* _
 // batches (more warps, shorter chains), four otherwise.
 template <int CH>
 __global__ void quant_rows_fp4_kernel(const uint16_t* __restrict__ src, const int* __restrict__ perm, int K, int rows,
-                                      int C, int rows_max, const int* __restrict__ slot_tile, int stack,
-                                      uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+                                      const int* __restrict__ rows_dev, int C, int rows_max,
+                                      const int* __restrict__ slot_tile, int stack, uint8_t* __restrict__ q,
+                                      uint8_t* __restrict__ sf) {
   pdl_trigger();
   pdl_wait();
+  if (rows_dev) rows = min(rows, *rows_dev);  // an expert shard: its own slots only
   const int hl = threadIdx.x & 15, half = (threadIdx.x >> 4) & 1;
   const int KC = C / kQK;
   const int KG = (KC + CH - 1) / CH;  // chunk groups per row
@@ -471,6 +475,7 @@ struct BsParams {
   float beta, beta_lin;
   unsigned* status;
   uint64_t limit_ns;
+  int withhold_item;   // test hook: the stage of this work item's first k step gets no copies (-1: none)
 };
 
 template <int MODE, int NQ>
@@ -534,6 +539,12 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
           // GATEUP: tiles / atoms (kc, gate), (kc, up); DOWN: (kc0) .. (kc0 + kNK - 1)
           const int n_sfa = (MODE == BS_GATEUP) ? 2 : nk;
           const size_t first = (MODE == BS_GATEUP) ? (tile0 + kc0) * 2 : tile0 + kc0;
+          if (item == p.withhold_item && ks == 0) {
+            // test hook: this stage's full barrier never completes, so the
+            // MMA issuer's bounded wait runs out and the CTA aborts
+            ++issued;
+            continue;
+          }
           const uint32_t st = smem_u32(stage(s));
           // the e2m1 copies count their packed bytes; boxes past the end of a
           // tensor are zero-filled and counted in full
@@ -948,6 +959,7 @@ cudaError_t launch_bs(const BsPlan& p, const uint8_t* wq, const uint8_t* sfa, in
   prm.rows_max = rows_max;
   prm.status = p.status;
   prm.limit_ns = p.limit_ns;
+  prm.withhold_item = MODE == BS_GATEUP ? p.withhold_item : -1;
   return launch_pdl(bs_stream_kernel<MODE, NQ>, C::kCtas * p.num_sms, C::kThreads, C::kSmem, s, ma, mb, prm);
 }
 
@@ -986,7 +998,8 @@ cudaError_t prepare_bs_kernels() {
   return e;
 }
 
-cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims& d, int tile_rows, cudaStream_t s) {
+cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims& d, int tile_rows,
+                               const int* n_local, cudaStream_t s) {
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
   if (T > p.max_tokens || (tile_rows != kBsDecodeRows && tile_rows != kBsPrefillRows)) return cudaErrorInvalidValue;
@@ -998,8 +1011,8 @@ cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims
   const int blocks = (int)std::min<long long>((halves * 16 + 255) / 256, 8LL * p.num_sms);
   auto kernel = !fp4 ? quant_rows_kernel : ch == 1 ? quant_rows_fp4_kernel<1> : quant_rows_fp4_kernel<kQuantChunks>;
   const int rows = tile_rows == kBsDecodeRows ? ws.rows_fp4 : ws.rows_max;
-  return launch_pdl(kernel, blocks, 256, 0, s, w.lat, w.perm, d.K, TK, d.L, rows, ws.slot_tile, stack, ws.lq,
-                    ws.lsf);
+  return launch_pdl(kernel, blocks, 256, 0, s, w.lat, w.perm, d.K, TK, n_local, d.L, rows, ws.slot_tile, stack,
+                    ws.lq, ws.lsf);
 }
 
 cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* tiles, const int* tile_count,
@@ -1016,10 +1029,10 @@ cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* t
   prm.beta = d.beta;
   prm.beta_lin = d.beta_lin;
   if (tile_rows == kBsDecodeRows)
-    return launch_bs<BS_GATEUP, kBsDecodeRows>(p, bw.gu_q, bw.gu_sf, d.E, d.I, d.L, ws.lq, ws.lsf, ws.rows_fp4,
+    return launch_bs<BS_GATEUP, kBsDecodeRows>(p, bw.gu_q, bw.gu_sf, bw.n_exp, d.I, d.L, ws.lq, ws.lsf, ws.rows_fp4,
                                                tiles, tile_count, prm, s);
   if (tile_rows == kBsPrefillRows)
-    return launch_bs<BS_GATEUP, kBsPrefillRows>(p, bw.gu_q, bw.gu_sf, d.E, d.I, d.L, ws.lq, ws.lsf, ws.rows_max,
+    return launch_bs<BS_GATEUP, kBsPrefillRows>(p, bw.gu_q, bw.gu_sf, bw.n_exp, d.I, d.L, ws.lq, ws.lsf, ws.rows_max,
                                                 tiles, tile_count, prm, s);
   return cudaErrorInvalidValue;
 }
@@ -1034,10 +1047,10 @@ cudaError_t bs_stream_down(const BsPlan& p, const BsWeights& bw, const int4* til
   prm.ld_out = d.L;
   prm.o = w.o;
   if (tile_rows == kBsDecodeRows)
-    return launch_bs<BS_DOWN, kBsDecodeRows>(p, bw.d_q, bw.d_sf, d.E, d.L, d.I, ws.hq, ws.hsf, ws.rows_fp4, tiles,
+    return launch_bs<BS_DOWN, kBsDecodeRows>(p, bw.d_q, bw.d_sf, bw.n_exp, d.L, d.I, ws.hq, ws.hsf, ws.rows_fp4, tiles,
                                              tile_count, prm, s);
   if (tile_rows == kBsPrefillRows)
-    return launch_bs<BS_DOWN, kBsPrefillRows>(p, bw.d_q, bw.d_sf, d.E, d.L, d.I, ws.hq, ws.hsf, ws.rows_max, tiles,
+    return launch_bs<BS_DOWN, kBsPrefillRows>(p, bw.d_q, bw.d_sf, bw.n_exp, d.L, d.I, ws.hq, ws.hsf, ws.rows_max, tiles,
                                               tile_count, prm, s);
   return cudaErrorInvalidValue;
 }

@@ -21,12 +21,13 @@ namespace k3 {
 //   d_q  : [E][L/128][I/128][128][64]
 //   d_sf : [E][L/128][I/128][512]
 struct BsWeights {
+  int n_exp = 0;  // experts held (a shard's own count)
   uint8_t* gu_q = nullptr;
   uint8_t* gu_sf = nullptr;
   uint8_t* d_q = nullptr;
   uint8_t* d_sf = nullptr;
 };
-size_t bs_weight_bytes(const Dims& d);
+size_t bs_weight_bytes(const Dims& d);  // for d.E experts
 // Packed nibbles [ne][rows][cols/2] into the box layout above (slot `mat`
 // of n_mat matrices per expert).
 cudaError_t bs_e2m1_boxes(const uint8_t* packed, int ne, int rows, int cols, int n_mat, int mat, uint8_t* out,
@@ -44,6 +45,7 @@ struct BsPlan {
   uint64_t limit_ns = 2000000000ull;
   int num_sms = 152;
   Dims dims{};
+  int withhold_item = -1;  // test hook (see k3moe_test_withhold_copies)
 };
 // Tile heights (token rows per tile, the MMA's N bound): decode-size batches
 // use short tiles (every weight byte streamed once per forward; the two
@@ -63,7 +65,10 @@ cudaError_t prepare_bs_kernels();
 // two e4m3 terms for prefill tiles) and their scales as per-tile atoms
 // (needs the tile list's slot map; tile_rows is the tile height the expert
 // kernels will use).
-cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims& d, int tile_rows, cudaStream_t s);
+// n_local (device, optional): an expert shard's slot count; slots from there
+// on belong to other shards and are skipped.
+cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims& d, int tile_rows,
+                               const int* n_local, cudaStream_t s);
 // gate/up over the tile list (tiles of at most tile_rows rows): h (bf16,
 // slot order) and its block-scaled terms for the down GEMM.
 cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* tiles, const int* tile_count,

@@ -286,12 +286,12 @@ cudaError_t launch_topk(const float* logits, int T, int E, int ld, const float* 
 // list of experts that received work.  Three kernels; deterministic.
 // =====================================================================
 __global__ void __launch_bounds__(kPermChunk) perm_hist_kernel(const int32_t* __restrict__ idx, int TK, int E,
-                                                               int* __restrict__ blk_hist) {
+                                                               ExpertShard sh, int* __restrict__ blk_hist) {
   extern __shared__ int hist[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   const int a = blockIdx.x * kPermChunk + threadIdx.x;
-  if (a < TK) atomicAdd(&hist[idx[a]], 1);
+  if (a < TK) atomicAdd(&hist[sh.bucket(idx[a])], 1);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) blk_hist[(size_t)blockIdx.x * E + e] = hist[e];
 }
@@ -325,8 +325,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* t
 }
 
 __global__ void __launch_bounds__(1024) perm_scan_kernel(int* __restrict__ blk_hist, int nblk, int E, int TK,
-                                                         int* __restrict__ counts, int* __restrict__ offsets,
-                                                         int* __restrict__ active) {
+                                                         ExpertShard sh, int* __restrict__ counts,
+                                                         int* __restrict__ offsets, int* __restrict__ active) {
   __shared__ int warp_tot[32];
   __shared__ int total_s, carry_off, carry_act;
   if (threadIdx.x == 0) {
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int* __restrict__ blk_h
     const int ex = block_exclusive_scan(tot, warp_tot, &total_s);
     const int add_off = carry_off;
     if (e < E) offsets[e] = add_off + ex;
-    const int flag = (e < E && tot > 0) ? 1 : 0;
+    const int flag = (e < sh.n_listed && tot > 0) ? 1 : 0;
     const int add_tot = total_s;
     const int ax = block_exclusive_scan(flag, warp_tot, &total_s);
     if (flag) active[1 + carry_act + ax] = e;
@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int* __restrict__ blk_h
 }
 
 __global__ void __launch_bounds__(kPermChunk) perm_scatter_kernel(const int32_t* __restrict__ idx, int TK, int E,
-                                                                  const int* __restrict__ blk_prefix,
+                                                                  ExpertShard sh, const int* __restrict__ blk_prefix,
                                                                   const int* __restrict__ offsets,
                                                                   int* __restrict__ perm, int* __restrict__ slot) {
   extern __shared__ int run[];
@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(kPermChunk) perm_scatter_kernel(const int32_t*
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int a = blockIdx.x * kPermChunk + threadIdx.x;
   const bool valid = a < TK;
-  const int e = valid ? idx[a] : -1;
+  const int e = valid ? sh.bucket(idx[a]) : -1;
   const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
   const int rank = __popc(peers & ((1u << lane) - 1u));
   const bool leader = (__ffs(peers) - 1) == lane;
@@ -396,15 +396,16 @@ __global__ void __launch_bounds__(kPermChunk) perm_scatter_kernel(const int32_t*
   }
 }
 
-cudaError_t launch_permute(const int32_t* idx, int T, int K, int E, int* blk_hist, int* counts, int* offsets,
-                           int* active, int* perm, int* slot, cudaStream_t s) {
+cudaError_t launch_permute(const int32_t* idx, int T, int K, const ExpertShard& sh, int* blk_hist, int* counts,
+                           int* offsets, int* active, int* perm, int* slot, cudaStream_t s) {
   const int TK = T * K;
   if (TK <= 0) return cudaSuccess;
+  const int E = sh.n_buckets;
   const int nblk = (TK + kPermChunk - 1) / kPermChunk;
   const size_t sm = sizeof(int) * (size_t)E;
-  perm_hist_kernel<<<nblk, kPermChunk, sm, s>>>(idx, TK, E, blk_hist);
-  perm_scan_kernel<<<1, 1024, 0, s>>>(blk_hist, nblk, E, TK, counts, offsets, active);
-  perm_scatter_kernel<<<nblk, kPermChunk, sm, s>>>(idx, TK, E, blk_hist, offsets, perm, slot);
+  perm_hist_kernel<<<nblk, kPermChunk, sm, s>>>(idx, TK, E, sh, blk_hist);
+  perm_scan_kernel<<<1, 1024, 0, s>>>(blk_hist, nblk, E, TK, sh, counts, offsets, active);
+  perm_scatter_kernel<<<nblk, kPermChunk, sm, s>>>(idx, TK, E, sh, blk_hist, offsets, perm, slot);
   return cudaGetLastError();
 }
 
@@ -417,15 +418,16 @@ cudaError_t launch_permute(const int32_t* idx, int T, int K, int E, int* blk_his
 // rows rounded up to 16}).
 // =====================================================================
 __global__ void __launch_bounds__(1024) perm_small_kernel(const int32_t* __restrict__ idx, int T, int E, int K,
-                                                          int* __restrict__ counts, int* __restrict__ offsets,
+                                                          ExpertShard sh, int* __restrict__ counts,
+                                                          int* __restrict__ offsets,
                                                           int* __restrict__ active, int* __restrict__ perm,
                                                           int* __restrict__ slot, int bn_max,
                                                           int4* __restrict__ tiles, int* __restrict__ tile_count,
-                                                          int* __restrict__ slot_tile) {
+                                                          int* __restrict__ slot_tile, int split_expert) {
   __shared__ int hist[2048];
   __shared__ int base[2048];
   __shared__ int warp_tot[32];
-  __shared__ int total_s;
+  __shared__ int total_s, n_first;
   pdl_trigger();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -433,7 +435,7 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(const int32_t* __restr
   for (int e = threadIdx.x; e < E; e += 1024) hist[e] = 0;
   __syncthreads();
   const int a = threadIdx.x;
-  const int e_a = a < TK ? idx[a] : -1;
+  const int e_a = a < TK ? sh.bucket(idx[a]) : -1;
   if (a < TK) atomicAdd(&hist[e_a], 1);
   __syncthreads();
   // offsets and active list (experts in chunks of 1024)
@@ -448,7 +450,7 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(const int32_t* __restr
       offsets[e] = carry_off + ex;
     }
     carry_off += total_s;
-    const int flag = c > 0 ? 1 : 0;
+    const int flag = (c > 0 && e < sh.n_listed) ? 1 : 0;
     const int ax = block_exclusive_scan(flag, warp_tot, &total_s);
     if (flag) active[1 + carry_act + ax] = e;
     carry_act += total_s;
@@ -456,6 +458,7 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(const int32_t* __restr
   if (threadIdx.x == 0) {
     offsets[E] = TK;
     active[0] = carry_act;
+    n_first = 0;
   }
   __syncthreads();
   // stable scatter: rank among earlier assignments of the same expert
@@ -489,6 +492,8 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(const int32_t* __restr
   }
   __syncthreads();
   const int tb = block_exclusive_scan(nsub, warp_tot, &total_s);
+  // tiles of experts below split_expert come first (experts ascend)
+  if (nsub > 0 && e_t < split_expert) atomicAdd(&n_first, nsub);
   if (nsub > 0) {
     const int per = (c_t + nsub - 1) / nsub;
     const int tn = (per + 15) & ~15;
@@ -500,19 +505,24 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(const int32_t* __restr
         for (int n = 0; n < rows; ++n) slot_tile[base[e_t] + r0 + n] = ((tb + j) << 8) | n;
     }
   }
-  if (threadIdx.x == 0) *tile_count = total_s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    tile_count[0] = total_s;
+    tile_count[1] = n_first;
+  }
 }
 
 cudaError_t launch_route_small(const float* logits, int T, int E, const float* bias, int K, int norm_topk, float rsf,
-                               int32_t* idx, float* w, int* counts, int* offsets, int* active, int* perm, int* slot,
-                               int bn_max, int4* tiles, int* tile_count, int* slot_tile, cudaStream_t s) {
+                               const ExpertShard& sh, int32_t* idx, float* w, int* counts, int* offsets, int* active,
+                               int* perm, int* slot, int bn_max, int4* tiles, int* tile_count, int* slot_tile,
+                               int split_expert, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   // tiles of at least 16 rows (the tile list's capacity), row field of 8 bits
-  if (T * K > 1024 || E > 2048 || bn_max < 16 || bn_max > 255) return cudaErrorInvalidValue;
+  if (T * K > 1024 || E > 2048 || sh.n_buckets > 2048 || bn_max < 16 || bn_max > 255) return cudaErrorInvalidValue;
   cudaError_t e = launch_topk(logits, T, E, E, bias, K, norm_topk, rsf, idx, w, s);
   if (e != cudaSuccess) return e;
-  return launch_pdl(perm_small_kernel, 1, 1024, 0, s, idx, T, E, K, counts, offsets, active, perm, slot, bn_max, tiles,
-                    tile_count, slot_tile);
+  return launch_pdl(perm_small_kernel, 1, 1024, 0, s, idx, T, sh.n_buckets, K, sh, counts, offsets, active, perm, slot,
+                    bn_max, tiles, tile_count, slot_tile, split_expert);
 }
 
 // =====================================================================
@@ -721,12 +731,25 @@ cudaError_t launch_down_gemv(const uint8_t* d_tiles, const uint16_t* h, const in
 // Weighted combine (k order, fp32) + RMSNorm over the latent (kimi-k3-mlx
 // README, REAP section caveat: RMSNorm on the combined expert output,
 // before up_proj).  One CTA per token.
+//   SAL: also the REAP saliency term of each (token, k): w_k ||o_k||_2
+//        (kimi-k3-mlx README, "REAP expert pruning": S_j = 1/|C| sum_x
+//        g_j(x) ||e_j(x)||_2), from the o rows the combine reads anyway.
+//   PARTIAL: an expert shard's partial combine: only slots below *n_local
+//        (the shard's own experts) are added, and c itself (fp32) goes to
+//        c_out instead of through RMSNorm.
+// The sum of squares for RMSNorm is taken on c scaled by a power of two
+// whenever the plain sum overflows fp32 (|c| above ~1e17), which gives the
+// same bits as the plain formula wherever that one is finite.
 // =====================================================================
+template <bool SAL, bool PARTIAL>
 __global__ void __launch_bounds__(1024) combine_rmsnorm_kernel(const float* __restrict__ o,
                                                                const int* __restrict__ slot,
                                                                const float* __restrict__ topk_w,
                                                                const uint16_t* __restrict__ gamma, int K, int L,
-                                                               float eps, uint16_t* __restrict__ n) {
+                                                               float eps, uint16_t* __restrict__ n,
+                                                               float* __restrict__ sal_tk,
+                                                               const int* __restrict__ n_local,
+                                                               float* __restrict__ c_out) {
   // One CTA per token; thread i owns latent columns 4i..4i+3 (plus further
   // groups of 4*blockDim.x when L is larger); the K slot rows of a column
   // group are loaded together so their latencies overlap.
@@ -734,32 +757,54 @@ __global__ void __launch_bounds__(1024) combine_rmsnorm_kernel(const float* __re
   __shared__ int sl[32];
   __shared__ float wk[32];
   __shared__ float red[32];
+  __shared__ float red_k[SAL ? 32 : 1][33];
+  __shared__ int kloc[32];
   pdl_trigger();
   pdl_wait();
   const int t = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x < K) {
-    sl[threadIdx.x] = slot[(size_t)t * K + threadIdx.x];
+    const int sv = slot[(size_t)t * K + threadIdx.x];
+    sl[threadIdx.x] = sv;
     wk[threadIdx.x] = topk_w[(size_t)t * K + threadIdx.x];
+    kloc[threadIdx.x] = PARTIAL ? (sv < *n_local) : 1;  // other shards' slots hold no output
   }
   __syncthreads();
   float ss = 0.f;
+  float sq[SAL ? 32 : 1];
+#pragma unroll
+  for (int k = 0; k < (SAL ? 32 : 1); ++k) sq[k] = 0.f;
   for (int c4 = threadIdx.x; c4 < L / 4; c4 += blockDim.x) {
     float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k0 = 0; k0 < K; k0 += 8) {  // eight slot rows in flight at a time, added in k order
+#pragma unroll
+    for (int k0 = 0; k0 < 32; k0 += 8) {  // eight slot rows in flight at a time, added in k order
+      if (k0 >= K) break;
       float4 v[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        if (k0 + k < K) v[k] = __ldg(reinterpret_cast<const float4*>(o + (size_t)sl[k0 + k] * L) + c4);
+        if (k0 + k < K && (!PARTIAL || kloc[k0 + k]))
+          v[k] = __ldg(reinterpret_cast<const float4*>(o + (size_t)sl[k0 + k] * L) + c4);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        if (k0 + k < K) {
+        if (k0 + k < K && (!PARTIAL || kloc[k0 + k])) {
           const float wv = wk[k0 + k];
           c.x = fmaf(wv, v[k].x, c.x);
           c.y = fmaf(wv, v[k].y, c.y);
           c.z = fmaf(wv, v[k].z, c.z);
           c.w = fmaf(wv, v[k].w, c.w);
+          if (SAL) {
+            float& q = sq[SAL ? k0 + k : 0];
+            q = fmaf(v[k].x, v[k].x, q);
+            q = fmaf(v[k].y, v[k].y, q);
+            q = fmaf(v[k].z, v[k].z, q);
+            q = fmaf(v[k].w, v[k].w, q);
+          }
         }
       }
+    }
+    if (PARTIAL) {
+      reinterpret_cast<float4*>(c_out + (size_t)t * L)[c4] = c;
+      continue;
     }
     reinterpret_cast<float4*>(cs)[c4] = c;
     ss = fmaf(c.x, c.x, ss);
@@ -767,14 +812,70 @@ __global__ void __launch_bounds__(1024) combine_rmsnorm_kernel(const float* __re
     ss = fmaf(c.z, c.z, ss);
     ss = fmaf(c.w, c.w, ss);
   }
+  if (SAL) {
+    // ||o_k||^2: per warp in a fixed tree, then over warps in order
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      if (k >= K) break;
+      const float v = warp_sum(sq[SAL ? k : 0]);
+      if (lane == 0) red_k[SAL ? warp : 0][k] = v;
+    }
+  }
   ss = warp_sum(ss);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  if (lane == 0) red[warp] = ss;
   __syncthreads();
+  const int nw = (int)(blockDim.x >> 5);
   float tot = 0.f;
-  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += red[i];
-  const float inv = 1.0f / sqrtf(tot / (float)L + eps);
+  for (int i = 0; i < nw; ++i) tot += red[i];
+  if (SAL && threadIdx.x < K) {
+    float q = 0.f;
+    for (int i = 0; i < nw; ++i) q += red_k[SAL ? i : 0][threadIdx.x];
+    sal_tk[(size_t)t * K + threadIdx.x] = kloc[threadIdx.x] ? wk[threadIdx.x] * sqrtf(q) : 0.f;
+  }
+  if (PARTIAL) return;
+  float scale = 1.f;  // power of two applied to c before squaring
+  if (!(tot <= 3.0e38f)) {
+    // the plain sum of squares overflowed: take it again on c * 2^-e, e
+    // the exponent of max|c| (exact scaling, same rounding)
+    float mx = 0.f;
+    for (int c4 = threadIdx.x; c4 < L / 4; c4 += blockDim.x) {
+      const float4 c = reinterpret_cast<const float4*>(cs)[c4];
+      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(c.x), fabsf(c.y)), fmaxf(fabsf(c.z), fabsf(c.w))));
+    }
+    mx = warp_max(mx);
+    __syncthreads();
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    mx = 0.f;
+    for (int i = 0; i < nw; ++i) mx = fmaxf(mx, red[i]);
+    if (mx <= 3.0e38f) {  // finite c: rescale; an inf or NaN in c stays as it is
+      int ex;
+      frexpf(mx, &ex);
+      scale = ldexpf(1.f, -ex);
+      float s2 = 0.f;
+      for (int c4 = threadIdx.x; c4 < L / 4; c4 += blockDim.x) {
+        const float4 c = reinterpret_cast<const float4*>(cs)[c4];
+        s2 = fmaf(c.x * scale, c.x * scale, s2);
+        s2 = fmaf(c.y * scale, c.y * scale, s2);
+        s2 = fmaf(c.z * scale, c.z * scale, s2);
+        s2 = fmaf(c.w * scale, c.w * scale, s2);
+      }
+      s2 = warp_sum(s2);
+      __syncthreads();
+      if (lane == 0) red[warp] = s2;
+      __syncthreads();
+      tot = 0.f;
+      for (int i = 0; i < nw; ++i) tot += red[i];
+    }
+  }
+  // scale = 2^-e: c / sqrt(mean(c^2) + eps) = (c 2^-e) / sqrt(mean((c 2^-e)^2) + eps 2^-2e)
+  const float inv = 1.0f / sqrtf(tot / (float)L + eps * scale * scale);
   for (int c4 = threadIdx.x; c4 < L / 4; c4 += blockDim.x) {
-    const float4 c = reinterpret_cast<const float4*>(cs)[c4];
+    float4 c = reinterpret_cast<const float4*>(cs)[c4];
+    c.x *= scale;
+    c.y *= scale;
+    c.z *= scale;
+    c.w *= scale;
     const uint2 g = __ldg(reinterpret_cast<const uint2*>(gamma) + c4);
     const float2 g01 = unpack_bf16x2(g.x), g23 = unpack_bf16x2(g.y);
     uint2 out;
@@ -782,6 +883,34 @@ __global__ void __launch_bounds__(1024) combine_rmsnorm_kernel(const float* __re
     out.y = pack_bf16x2(c.z * inv * g23.x, c.w * inv * g23.y);
     reinterpret_cast<uint2*>(n + (size_t)t * L)[c4] = out;
   }
+}
+
+// REAP saliency accumulation: for every expert with work, the terms of its
+// slots (in slot order: tokens ascending) are added in a fixed order and
+// the sum is added to the expert's fp64 running total; the token count of
+// the calibration set grows by T.  One warp per active expert; the launch
+// is ordered on the stream, so no two updates of a total overlap.
+__global__ void __launch_bounds__(256) saliency_accumulate_kernel(const float* __restrict__ sal_tk,
+                                                                  const int* __restrict__ perm,
+                                                                  const int* __restrict__ offsets,
+                                                                  const int* __restrict__ active, int T,
+                                                                  double* __restrict__ sal_sum,
+                                                                  unsigned long long* __restrict__ sal_tokens) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int n_act = active[0];
+  const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int nw = (int)((gridDim.x * blockDim.x) >> 5);
+  for (int i = gw; i < n_act; i += nw) {
+    const int e = active[1 + i];
+    double acc = 0.0;
+    for (int sidx = offsets[e] + lane; sidx < offsets[e + 1]; sidx += 32) acc += (double)sal_tk[perm[sidx]];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+    if (lane == 0) sal_sum[e] += acc;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *sal_tokens += (unsigned long long)T;
 }
 
 // One-time kernel attributes (dynamic shared memory above 48 KB), set when a
@@ -792,18 +921,37 @@ cudaError_t prepare_decode_kernels(const Dims& d) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(down_gemv_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(sizeof(float) * 4 * d.I));
+  const int sm = (int)(sizeof(float) * d.L);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(combine_rmsnorm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(sizeof(float) * d.L));
+    e = cudaFuncSetAttribute(combine_rmsnorm_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(combine_rmsnorm_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(combine_rmsnorm_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(combine_rmsnorm_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
   return e;
 }
 
 cudaError_t launch_combine_rmsnorm(const float* o, const int* slot, const float* topk_w, const uint16_t* gamma,
-                                   int T, const Dims& d, uint16_t* n, cudaStream_t s) {
+                                   int T, int K, const Dims& d, uint16_t* n, float* sal_tk, const int* n_local,
+                                   float* c_out, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
+  if (K < 1 || K > 32 || (c_out && !n_local)) return cudaErrorInvalidValue;
   const int threads = std::min(1024, ((d.L / 4 + 31) / 32) * 32);
-  return launch_pdl(combine_rmsnorm_kernel, T, threads, sizeof(float) * d.L, s, o, slot, topk_w, gamma, d.K, d.L,
-                    d.rms_eps, n);
+  const size_t sm = sizeof(float) * d.L;
+  auto kernel = c_out ? (sal_tk ? combine_rmsnorm_kernel<true, true> : combine_rmsnorm_kernel<false, true>)
+                      : (sal_tk ? combine_rmsnorm_kernel<true, false> : combine_rmsnorm_kernel<false, false>);
+  return launch_pdl(kernel, T, threads, sm, s, o, slot, topk_w, gamma, K, d.L, d.rms_eps, n, sal_tk, n_local, c_out);
+}
+
+cudaError_t launch_saliency_accumulate(const float* sal_tk, const int* perm, const int* offsets, const int* active,
+                                       int T, int E, double* sal_sum, unsigned long long* sal_tokens,
+                                       cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  const int blocks = std::max(1, std::min((E * 32 + 255) / 256, 152));
+  return launch_pdl(saliency_accumulate_kernel, blocks, 256, 0, s, sal_tk, perm, offsets, active, T, sal_sum,
+                    sal_tokens);
 }
 
 // =====================================================================

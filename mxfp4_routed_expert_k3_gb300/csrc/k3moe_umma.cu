@@ -39,7 +39,15 @@ constexpr int kBK = 64;         // input columns per stage (one 128-byte swizzle
 constexpr int kBNMax = 192;     // token rows per tile (MMA N, multiple of 16)
 constexpr int kThreads = 192;
 
-enum Mode { DENSE = 0, GATEUP = 1, DOWN = 2 };
+enum Mode { DENSE = 0, GATEUP = 1, DOWN = 2, GATEUP2 = 3, DOWN2 = 4 };
+
+// Second-bank (2-bit affine) tile: 128 weight rows x 64 input columns of
+// one matrix -- row r's 64 codes (four per byte, low bits first) at
+// [16 r, 16 r + 16), then the rows' bf16 scales at 2048 + 2 r and bf16
+// biases at 2304 + 2 r (one group of 64 per row per tile: the tile is one
+// quantisation group wide).
+constexpr int kTile2Bytes = 2560;
+constexpr int kTile2MaxRows = 80;  // token rows of the tiles the 2-bit modes take
 
 // The tensor cores' fp32 accumulation drifts by about 2^-24 (relative) per
 // accumulation step, so a long K loop into one accumulator loses more than
@@ -47,21 +55,37 @@ enum Mode { DENSE = 0, GATEUP = 1, DOWN = 2 };
 // K/(16*kAcc) steps) and the epilogue adds them with round-to-nearest fp32.
 template <int MODE>
 struct Cfg {
-  static constexpr int kNumA = (MODE == GATEUP) ? 2 : 1;
+  static constexpr bool kTwoBit = MODE == GATEUP2 || MODE == DOWN2;  // second-bank weights
+  static constexpr bool kGU = MODE == GATEUP || MODE == GATEUP2;     // gate and up: two accumulators
+  static constexpr bool kDown = MODE == DOWN || MODE == DOWN2;
+  static constexpr int kNumMat = kGU ? 2 : 1;
+  // 2-bit affine weights decode exactly to fp32 and enter the MMA as two
+  // bf16 terms (hi + lo, 16 significant bits): two A tiles per matrix
+  static constexpr int kParts = kTwoBit ? 2 : 1;
+  static constexpr int kNumA = kNumMat * kParts;
   // Dense: 256 token rows per tile (an MMA instruction costs about the pipe
   // time of an N = 256 one whatever its N), K split over two accumulators.
-  static constexpr int kBN = (MODE == DENSE) ? 256 : kBNMax;    // token rows per tile
+  // token rows per tile; the 2-bit modes run on the block-scaled path's
+  // tile lists (at most 80 rows), so their token box is 80 rows high
+  static constexpr int kBN = (MODE == DENSE) ? 256 : kTwoBit ? kTile2MaxRows : kBNMax;
   static constexpr int kABytes = kBM * kBK * 2;                 // 16 KB per A tile
   static constexpr int kBBytes = kBN * kBK * 2;
-  static constexpr int kStageBytesRaw = (MODE == DENSE) ? 0 : kNumA * kTileBytes;
+  static constexpr int kSrcTile = kTwoBit ? kTile2Bytes : kTileBytes;  // stored tile of one matrix
+  static constexpr int kStageBytesRaw = (MODE == DENSE) ? 0 : kNumMat * kSrcTile;
   static constexpr int kStaging = (kStageBytesRaw + 1023) / 1024 * 1024;
   static constexpr int kStageBytes = kNumA * kABytes + kBBytes + kStaging;
-  static constexpr int kStages = (MODE == GATEUP) ? 3 : 4;
-  static constexpr int kAcc = (MODE == DENSE || MODE == DOWN) ? 2 : 1;
-  static constexpr int kAccStride = 256;  // TMEM columns between accumulators
+  static constexpr int kStages = (MODE == GATEUP2) ? 2 : (MODE == DOWN2) ? 5 : kGU ? 3 : 4;
+  static constexpr int kAcc = (MODE == DENSE || kDown) ? 2 : 1;
+  // TMEM columns between accumulators.  The 2-bit modes (tiles of at most
+  // 128 token rows) give the hi and lo terms accumulators of their own
+  // (fewer fp32 accumulation steps each), added in the epilogue.
+  static constexpr int kAccStride = kTwoBit ? 128 : 256;
+  static constexpr int kAccPerMat = kAcc * kParts;  // accumulators summed per matrix
+  static constexpr int kMatStride = 256;            // TMEM columns between gate and up
   static constexpr int kTmemCols = 512;
   static constexpr int kSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
-  static_assert(kNumA * kAcc * kAccStride <= kTmemCols || MODE == GATEUP, "TMEM budget");
+  static_assert(kNumMat * kAccPerMat * kAccStride <= kTmemCols || (kGU && !kTwoBit), "TMEM budget");
+  static_assert(!kTwoBit || kAccPerMat * kAccStride <= kMatStride || !kGU, "gate and up accumulators overlap");
 };
 
 // One output element of a dense projection (DenseOut, glu == 0).
@@ -89,15 +113,18 @@ __device__ __forceinline__ void dense_store4(const DenseOut& o, int M, int t, in
 }
 
 // Per-tile description for grouped GEMMs: x = expert, y = first row (slot),
-// z = valid rows, w = MMA N (rows rounded up to 16).
+// z = valid rows, w = MMA N (rows rounded up to 16).  The kernel takes
+// tiles [*begin, *count) (begin NULL: from 0), both read on the device.
 struct TileList {
   const int4* tiles;
   const int* count;
+  const int* begin = nullptr;
 };
 
 struct Params {
   // operand sources
-  const uint8_t* a_tiles;  // MXFP4 tiles (GATEUP / DOWN)
+  const uint8_t* a_tiles;  // MXFP4 tiles (GATEUP / DOWN) or 2-bit tiles (GATEUP2 / DOWN2)
+  int expert_base;         // weight index of a tile = its expert id - expert_base
   int MT;                  // weight row tiles per matrix
   int KS;                  // K / 64
   int M;                   // weight rows (DENSE edge masking)
@@ -136,9 +163,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
     rows = min(p.tn, p.T - row0);
     n_mma = (rows + 15) & ~15;
   } else {
-    if ((int)blockIdx.y >= *p.list.count) return;
-    const int4 t = p.list.tiles[blockIdx.y];
-    e = t.x;
+    const int ti = (int)blockIdx.y + (p.list.begin ? *p.list.begin : 0);
+    if (ti >= *p.list.count) return;
+    const int4 t = p.list.tiles[ti];
+    e = t.x - p.expert_base;
     row0 = t.y;
     rows = t.z;
     n_mma = t.w;
@@ -169,9 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
     // ================= TMA producer
     int issued = 0;
     if (lane == 0) {
-      const uint32_t tx = C::kBBytes + (MODE == DENSE ? C::kABytes : C::kNumA * kTileBytes);
-      const uint8_t* a_src = (MODE == DENSE) ? nullptr
-                                             : p.a_tiles + ((size_t)(e * p.MT + mt) * p.KS) * C::kNumA * kTileBytes;
+      const uint32_t tx = C::kBBytes + (MODE == DENSE ? C::kABytes : C::kNumMat * C::kSrcTile);
+      const uint8_t* a_src =
+          (MODE == DENSE) ? nullptr : p.a_tiles + ((size_t)(e * p.MT + mt) * p.KS) * C::kNumMat * C::kSrcTile;
       for (int ks = 0; ks < p.KS; ++ks) {
         const int s = ks % C::kStages, u = ks / C::kStages;
         if (u > 0 && !mbar_wait(empty(s), (u - 1) & 1, g, 1u)) break;
@@ -180,8 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
         if (MODE == DENSE)
           tma_load_2d(smem_u32(stage_a(s, 0)), &map_a, full_tma(s), ks * kBK, mt * kBM);
         else
-          bulk_load(smem_u32(stage_stg(s)), a_src + (size_t)ks * C::kNumA * kTileBytes, C::kNumA * kTileBytes,
-                    full_tma(s));
+          bulk_load(smem_u32(stage_stg(s)), a_src + (size_t)ks * C::kNumMat * C::kSrcTile,
+                    C::kNumMat * C::kSrcTile, full_tma(s));
         ++issued;
       }
       if (*abort_flag) {
@@ -206,13 +234,16 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
         if (!ok) break;
         tc_fence_after();
         const uint32_t b0 = smem_u32(stage_b(s));
-        const uint32_t acc_col = (uint32_t)((ks % C::kAcc) * C::kAccStride);
+        const int acc_k = ks % C::kAcc;
 #pragma unroll
         for (int i = 0; i < C::kNumA; ++i) {
           const uint32_t a0 = smem_u32(stage_a(s, i));
+          const int part = i % C::kParts;  // hi and lo terms: accumulators of their own
+          const uint32_t acc_col =
+              (uint32_t)((i / C::kParts) * C::kMatStride + (acc_k * C::kParts + part) * C::kAccStride);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_bf16(tmem + acc_col + i * 256, umma_desc_sw128(a0 + kk * 32), umma_desc_sw128(b0 + kk * 32), idesc,
+            umma_bf16(tmem + acc_col, umma_desc_sw128(a0 + kk * 32), umma_desc_sw128(b0 + kk * 32), idesc,
                       (ks >= C::kAcc || kk) ? 1u : 0u);
         }
         umma_commit(empty(s));
@@ -229,7 +260,44 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
   } else {
     // ================= decode (MXFP4) + epilogue warpgroup
     const int wg_t = threadIdx.x - 64;  // 0..127
-    if (MODE != DENSE) {
+    if (C::kTwoBit) {
+      // w = scale * q + bias, exact in fp32 (an 8-bit scale times a 2-bit
+      // code plus an 8-bit bias), written as hi = bf16(w), lo = bf16(w - hi)
+      const int r = wg_t;
+      for (int ks = 0; ks < p.KS; ++ks) {
+        const int s = ks % C::kStages, par = (ks / C::kStages) & 1;
+        if (!mbar_wait(full_tma(s), par, g, 8u)) break;
+        const uint8_t* stg = stage_stg(s);
+#pragma unroll
+        for (int m = 0; m < C::kNumMat; ++m) {
+          const uint8_t* tile = stg + m * kTile2Bytes;
+          const uint4 q = *reinterpret_cast<const uint4*>(tile + (size_t)r * 16);
+          const float sc = bf16_to_f32(*reinterpret_cast<const uint16_t*>(tile + 2048 + 2 * r));
+          const float bi = bf16_to_f32(*reinterpret_cast<const uint16_t*>(tile + 2304 + 2 * r));
+          uint8_t* row_hi = stage_a(s, m * 2) + (size_t)r * 128;
+          uint8_t* row_lo = stage_a(s, m * 2 + 1) + (size_t)r * 128;
+          const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) {  // columns 8 c8 .. 8 c8 + 7: 16 bits of word c8 / 2
+            const uint32_t bits = words[c8 >> 1] >> (16 * (c8 & 1));
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float w0 = fmaf(sc, (float)((bits >> (4 * k)) & 3u), bi);
+              const float w1 = fmaf(sc, (float)((bits >> (4 * k + 2)) & 3u), bi);
+              hi[k] = pack_bf16x2(w0, w1);
+              const float2 h2 = unpack_bf16x2(hi[k]);
+              lo[k] = pack_bf16x2(w0 - h2.x, w1 - h2.y);
+            }
+            const int sw = (c8 ^ (r & 7)) << 4;
+            *reinterpret_cast<uint4*>(row_hi + sw) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(row_lo + sw) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(full_a(s));
+      }
+    } else if (MODE != DENSE) {
       const int r = wg_t;  // row of the 128-row tile this thread decodes
       for (int ks = 0; ks < p.KS; ++ks) {
         const int s = ks % C::kStages, par = (ks / C::kStages) & 1;
@@ -262,7 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
       const int m_local = quarter * 32 + lane;
       const int m = mt * kBM + m_local;
       const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-      const int n_acc = min(C::kAcc, p.KS);
+      // accumulators that hold a part of the sum: every (K accumulator, term)
+      // pair that received at least one k step
+      const int n_acc = min(C::kAcc, p.KS) * C::kParts;
       for (int j0 = 0; j0 < n_mma; j0 += 32) {
         float acc[32];
         tmem_ld32(lane_addr + j0, acc);
@@ -272,15 +342,21 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
 #pragma unroll
           for (int j = 0; j < 32; ++j) acc[j] += part[j];
         }
-        if (MODE == GATEUP) {
+        if (C::kGU) {
           float up[32];
-          tmem_ld32(lane_addr + 256 + j0, up);
+          tmem_ld32(lane_addr + C::kMatStride + j0, up);
+          for (int a = 1; a < n_acc; ++a) {
+            float part[32];
+            tmem_ld32(lane_addr + C::kMatStride + a * C::kAccStride + j0, part);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) up[j] += part[j];
+          }
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (j0 + j < rows)
               p.out_bf16[(size_t)(row0 + j0 + j) * p.ld_out + m] =
                   f32_to_bf16(situ_fast(acc[j], up[j], p.beta, p.beta_lin));
-        } else if (MODE == DOWN) {
+        } else if (C::kDown) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (j0 + j < rows) p.out_f32[(size_t)(row0 + j0 + j) * p.ld_out + m] = acc[j];
@@ -584,25 +660,44 @@ __global__ void __launch_bounds__(kDThreads, 1) umma_dense_stream_kernel(const _
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = p.MT * p.nkc;
   pdl_trigger();
-  pdl_wait();
-  if ((int)blockIdx.x >= n_items) return;
+  if ((int)blockIdx.x >= n_items) {
+    pdl_wait();
+    return;
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < NB; ++i) mbar_init(smem_u32(bars + i), i >= 2 * C::kStages + 2 ? 128u : 1u);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 128);
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const Guard g{abort_flag, p.status, p.limit_ns};
   auto full = [&](int s) { return smem_u32(bars + s); };
   auto sfree = [&](int s) { return smem_u32(bars + C::kStages + s); };
   auto tfull = [&](int b) { return smem_u32(bars + 2 * C::kStages + b); };
   auto tempty = [&](int b) { return smem_u32(bars + 2 * C::kStages + 2 + b); };
   auto stage_a = [&](int s) { return smem + (size_t)s * C::kStageBytes; };
   auto stage_b = [&](int s) { return smem + (size_t)s * C::kStageBytes + C::kABytes; };
+  // The weights are static: the first ring of weight tiles is requested
+  // before the preceding kernel has finished (only the token rows, which
+  // that kernel may write, wait for it).  Each stage's barrier expects the
+  // weight and the token bytes at once; the token copy completes it later.
+  int n_pre = 0;
+  if (warp == 0 && lane == 0) {
+    for (int item = blockIdx.x; item < n_items && n_pre < C::kStages; item += gridDim.x) {
+      const int mt = item % p.MT, kc = item / p.MT;
+      const int k0 = kc * p.ks_per_chunk, k1 = min(p.KS, k0 + p.ks_per_chunk);
+      for (int ks = k0; ks < k1 && n_pre < C::kStages; ++ks, ++n_pre) {
+        mbar_expect_tx(full(n_pre), C::kABytes + p.b_bytes);
+        tma_load_2d(smem_u32(stage_a(n_pre)), &map_a, full(n_pre), ks * kBK, mt * kBM);
+      }
+    }
+  }
+  pdl_wait();
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 128);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Guard g{abort_flag, p.status, p.limit_ns};
   const int n_mma = (p.T + 15) & ~15;
 
   if (warp == 0) {
@@ -614,6 +709,11 @@ __global__ void __launch_bounds__(kDThreads, 1) umma_dense_stream_kernel(const _
         const int k0 = kc * p.ks_per_chunk, k1 = min(p.KS, k0 + p.ks_per_chunk);
         for (int ks = k0; ks < k1; ++ks, ++kg) {
           const int s = kg % C::kStages, u = kg / C::kStages;
+          if (kg < n_pre) {  // weights already requested: the token rows only
+            tma_load_2d(smem_u32(stage_b(s)), &map_b, full(s), ks * kBK, 0);
+            ++issued;
+            continue;
+          }
           if (u > 0 && !mbar_wait(sfree(s), (u - 1) & 1, g, 1u)) {
             ok = false;
             break;
@@ -752,12 +852,15 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ lat, const int* 
 __global__ void __launch_bounds__(1024) build_tiles_kernel(const int* __restrict__ active,
                                                            const int* __restrict__ offsets, int bn_max,
                                                            int4* __restrict__ tiles, int* __restrict__ count,
-                                                           int* __restrict__ slot_tile) {
+                                                           int* __restrict__ slot_tile, int split_expert) {
   __shared__ int warp_tot[32];
-  __shared__ int carry;
+  __shared__ int carry, n_first;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n_act = active[0];
-  if (threadIdx.x == 0) carry = 0;
+  if (threadIdx.x == 0) {
+    carry = 0;
+    n_first = 0;
+  }
   __syncthreads();
   for (int a0 = 0; a0 < n_act; a0 += 1024) {
     const int a = a0 + threadIdx.x;
@@ -788,6 +891,9 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int* __restrict
     }
     __syncthreads();
     const int base = carry + warp_tot[warp] + incl - nsub;
+    // tiles of experts below split_expert come first (experts ascend): their
+    // number is where the second bank's tiles begin
+    if (a < n_act && nsub > 0 && e < split_expert) atomicAdd(&n_first, nsub);
     if (a < n_act && nsub > 0) {
       const int per = (c + nsub - 1) / nsub;
       const int tn = (per + 15) & ~15;
@@ -803,7 +909,40 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int* __restrict
     if (threadIdx.x == 1023) carry = base + nsub;
     __syncthreads();
   }
-  if (threadIdx.x == 0) *count = carry;
+  if (threadIdx.x == 0) {
+    count[0] = carry;
+    count[1] = n_first;
+  }
+}
+
+// Second-bank weights into 2-bit tiles: n_mat matrices [rows, cols] per
+// expert (codes [rows, cols/4] u8, scale and bias [rows, cols/64] bf16);
+// tile (m, mt, ks) of expert e at out + ((e * n_mat_stride + (mt * KS + ks)
+// * step + offset) * kTile2Bytes, one thread per 16-byte row of codes or
+// per row's scale / bias pair.
+__global__ void bank2_tiles_kernel(const uint8_t* __restrict__ q, const uint16_t* __restrict__ sc,
+                                   const uint16_t* __restrict__ bi, int ne, int rows, int cols,
+                                   uint8_t* __restrict__ out, size_t mat_stride_tiles, int step, int offset) {
+  const int KS = cols / 64, MT = rows / kBM;
+  const long long per_tile = 2 * kBM;  // 128 code rows + 128 scale/bias rows
+  const long long total = (long long)ne * MT * KS * per_tile;
+  for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < total;
+       g += (long long)gridDim.x * blockDim.x) {
+    const int w = (int)(g % per_tile);
+    const long long tl = g / per_tile;
+    const int ks = (int)(tl % KS), mt = (int)((tl / KS) % MT);
+    const int e = (int)(tl / ((long long)KS * MT));
+    uint8_t* tile = out + ((size_t)e * mat_stride_tiles + ((size_t)mt * KS + ks) * step + offset) * kTile2Bytes;
+    const int r = w % kBM;
+    const size_t row = (size_t)e * rows + (size_t)mt * kBM + r;
+    if (w < kBM) {
+      *reinterpret_cast<uint4*>(tile + (size_t)r * 16) =
+          *reinterpret_cast<const uint4*>(q + row * (cols / 4) + (size_t)ks * 16);
+    } else {
+      reinterpret_cast<uint16_t*>(tile + 2048)[r] = sc[row * (cols / 64) + ks];
+      reinterpret_cast<uint16_t*>(tile + 2304)[r] = bi[row * (cols / 64) + ks];
+    }
+  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -890,6 +1029,12 @@ cudaError_t prepare_umma_kernels() {
                              Cfg<GATEUP>::kSmem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(umma_gemm_kernel<DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<DOWN>::kSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(umma_gemm_kernel<GATEUP2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<GATEUP2>::kSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(umma_gemm_kernel<DOWN2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<DOWN2>::kSmem);
   return e;
 }
 
@@ -936,7 +1081,7 @@ cudaError_t umma_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8
   if (TK <= 0) return cudaSuccess;
   UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
   const int max_tiles = TK / kBNMax + std::min(d.E, TK) + 1;
-  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, kBNMax, ws.tiles, ws.count, nullptr);
+  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, kBNMax, ws.tiles, ws.count, nullptr, 1 << 30);
   gather_rows_kernel<<<152 * 8, 256, 0, s>>>(w.lat, w.perm, TK, d.K, d.L, ws.lat_perm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -975,19 +1120,71 @@ cudaError_t umma_stream_prepare(const UmmaPlan& p, const Work& w, int T, const D
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
   UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
-  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, kSNB, ws.tiles, ws.count, nullptr);
+  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, kSNB, ws.tiles, ws.count, nullptr, 1 << 30);
   gather_rows_kernel<<<152 * 2, 256, 0, s>>>(w.lat, w.perm, TK, d.K, d.L, ws.lat_perm);
   return cudaGetLastError();
 }
 
 // Only the tile list (tiles of at most bn_max rows) and the slot -> tile map.
 cudaError_t umma_stream_tiles(const UmmaPlan& p, const Work& w, int T, const Dims& d, int bn_max, int* slot_tile,
-                              cudaStream_t s) {
+                              int split_expert, cudaStream_t s) {
   if (T * d.K <= 0) return cudaSuccess;
   if (bn_max < kMinTileRows || bn_max > 255) return cudaErrorInvalidValue;  // list capacity, slot map row field
   UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
-  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, bn_max, ws.tiles, ws.count, slot_tile);
+  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, bn_max, ws.tiles, ws.count, slot_tile, split_expert);
   return cudaGetLastError();
+}
+
+cudaError_t bank2_tiles(const uint8_t* q, const uint16_t* sc, const uint16_t* bi, int ne, int rows, int cols,
+                        uint8_t* out, size_t mat_stride_tiles, int step, int offset, cudaStream_t s) {
+  if (rows % kBM || cols % 64) return cudaErrorInvalidValue;
+  bank2_tiles_kernel<<<152 * 8, 256, 0, s>>>(q, sc, bi, ne, rows, cols, out, mat_stride_tiles, step, offset);
+  return cudaGetLastError();
+}
+
+size_t bank2_tile_bytes(int rows, int cols) { return (size_t)(rows / kBM) * (cols / 64) * kTile2Bytes; }
+
+// The second bank's experts: tiles [count[1], count[0]) of the tile list
+// (experts >= bank2_begin, whose weights sit at index expert - bank2_begin),
+// slot-ordered bf16 latent rows, gate/up with SiTU-GLU -> h, down -> o.
+cudaError_t umma_bank2_experts(const UmmaPlan& p, const uint8_t* gu2_tiles, const uint8_t* d2_tiles, int bank2_begin,
+                               int n_bank2, int tile_rows, const Work& w, int T, const Dims& d, cudaStream_t s) {
+  const int TK = T * d.K;
+  if (TK <= 0) return cudaSuccess;
+  if (tile_rows > kTile2MaxRows) return cudaErrorInvalidValue;  // token box height and TMEM layout
+  UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
+  gather_rows_kernel<<<152 * 8, 256, 0, s>>>(w.lat, w.perm, TK, d.K, d.L, ws.lat_perm);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap mb1, mb2;
+  if (!make_map(&mb1, ws.lat_perm, TK, d.L, kTile2MaxRows) || !make_map(&mb2, w.h, TK, d.I, kTile2MaxRows))
+    return cudaErrorInvalidValue;
+  // at most one tile per second-bank expert with work plus one per 16 slots
+  const int max_tiles = std::min(n_bank2, TK) + TK / kMinTileRows + 1;
+  Params g{};
+  g.a_tiles = gu2_tiles;
+  g.expert_base = bank2_begin;
+  g.MT = d.I / kBM;
+  g.KS = d.L / kBK;
+  g.M = d.I;
+  g.list = TileList{ws.tiles, ws.count, ws.count + 1};
+  g.out_bf16 = w.h;
+  g.ld_out = d.I;
+  g.beta = d.beta;
+  g.beta_lin = d.beta_lin;
+  g.status = p.status;
+  g.limit_ns = p.limit_ns;
+  e = launch_gemm<GATEUP2>(mb1, mb1, g, dim3(g.MT, max_tiles), s);
+  if (e != cudaSuccess) return e;
+  Params dn = g;
+  dn.a_tiles = d2_tiles;
+  dn.MT = d.L / kBM;
+  dn.KS = d.I / kBK;
+  dn.M = d.L;
+  dn.out_bf16 = nullptr;
+  dn.out_f32 = w.o;
+  dn.ld_out = d.L;
+  return launch_gemm<DOWN2>(mb2, mb2, dn, dim3(dn.MT, max_tiles), s);
 }
 
 // Only the slot-ordered latent rows (the tile list was built by the fused

@@ -56,8 +56,18 @@ cudaError_t umma_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8
                          const Dims& d, cudaStream_t s);
 int umma_expert_launches();
 cudaError_t umma_stream_prepare(const UmmaPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s);
+// Tile list over the experts with work (tiles of at most bn_max slots),
+// slot -> tile map, and count[1] = the tiles of experts below split_expert
+// (they come first).
 cudaError_t umma_stream_tiles(const UmmaPlan& p, const Work& w, int T, const Dims& d, int bn_max, int* slot_tile,
-                              cudaStream_t s);
+                              int split_expert, cudaStream_t s);
+// Second bank (2-bit affine experts): re-layout into 2-bit tiles at load,
+// and the bank's gate/up + down over tiles [count[1], count[0]).
+cudaError_t bank2_tiles(const uint8_t* q, const uint16_t* sc, const uint16_t* bi, int ne, int rows, int cols,
+                        uint8_t* out, size_t mat_stride_tiles, int step, int offset, cudaStream_t s);
+size_t bank2_tile_bytes(int rows, int cols);  // one matrix of one expert
+cudaError_t umma_bank2_experts(const UmmaPlan& p, const uint8_t* gu2_tiles, const uint8_t* d2_tiles, int bank2_begin,
+                               int n_bank2, int tile_rows, const Work& w, int T, const Dims& d, cudaStream_t s);
 cudaError_t umma_stream_gather(const UmmaPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s);
 // where the streaming kernels read their tile list (and the tile height)
 void umma_tile_list(const UmmaPlan& p, int4** tiles, int** count, int* bn_max);

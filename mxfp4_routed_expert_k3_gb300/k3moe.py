@@ -16,11 +16,14 @@ from .dims import LayerDims
 from .native import LIB
 
 OK, EINVAL, ENOMEM, ECUDA, ETIMEOUT, EBADSCALE, ESTATE = 0, -1, -2, -3, -4, -5, -6
-BUF = dict(logits=0, lat=1, counts=2, offsets=3, perm=4, slot=5, h=6, o=7, n=8, active=9)
+BUF = dict(logits=0, lat=1, counts=2, offsets=3, perm=4, slot=5, h=6, o=7, n=8, active=9, shared_h=10,
+           shared_z=11)
 Q = dict(workspace_bytes=0, weight_bytes=1, launches_last=2, path_last=3, device=4)
 EXPORTS = ["k3moe_create", "k3moe_load_weights", "k3moe_forward", "k3moe_forward_host", "k3moe_status",
            "k3moe_last_error", "k3moe_destroy", "k3moe_mxfp4_dequant", "k3moe_route", "k3moe_fetch",
-           "k3moe_query", "k3moe_profile", "k3moe_profile_read", "k3moe_profile_name", "k3moe_route_noalloc"]
+           "k3moe_query", "k3moe_profile", "k3moe_profile_read", "k3moe_profile_name", "k3moe_route_noalloc",
+           "k3moe_saliency", "k3moe_saliency_read", "k3moe_saliency_reset", "k3moe_forward_partial",
+           "k3moe_finish", "k3moe_check_guards", "k3moe_test_withhold_copies"]
 
 
 class K3Error(RuntimeError):
@@ -33,12 +36,20 @@ class Config(C.Structure):
     _fields_ = [("hidden", C.c_int), ("latent", C.c_int), ("n_experts", C.c_int), ("top_k", C.c_int),
                 ("inter", C.c_int), ("group", C.c_int), ("beta", C.c_float), ("beta_lin", C.c_float),
                 ("rms_eps", C.c_float), ("routed_scaling", C.c_float), ("norm_topk", C.c_int),
-                ("max_tokens", C.c_int), ("spin_timeout_ms", C.c_int), ("force_path", C.c_int)]
+                ("max_tokens", C.c_int), ("spin_timeout_ms", C.c_int), ("force_path", C.c_int),
+                ("n_shared", C.c_int), ("shared_inter", C.c_int), ("expert_begin", C.c_int),
+                ("expert_count", C.c_int), ("bank2_begin", C.c_int)]
 
 
 class Weights(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in ("router_w", "router_bias", "down_proj", "w1_packed", "w1_scale",
-                                          "w3_packed", "w3_scale", "w2_packed", "w2_scale", "norm_w", "up_proj")]
+                                          "w3_packed", "w3_scale", "w2_packed", "w2_scale", "norm_w", "up_proj",
+                                          "shared_w1", "shared_w3", "shared_w2", "b2_w1q", "b2_w1s", "b2_w1b",
+                                          "b2_w3q", "b2_w3s", "b2_w3b", "b2_w2q", "b2_w2s", "b2_w2b")]
+
+
+OPTIONAL_WEIGHTS = ("shared_w1", "shared_w3", "shared_w2", "b2_w1q", "b2_w1s", "b2_w1b", "b2_w3q", "b2_w3s",
+                    "b2_w3b", "b2_w2q", "b2_w2s", "b2_w2b")
 
 
 _lib = None
@@ -70,10 +81,18 @@ def lib():
         L.k3moe_profile_read.argtypes = [vp, C.POINTER(C.c_float), i32, C.POINTER(C.c_int)]
         L.k3moe_profile_name.argtypes = [vp, i32]
         L.k3moe_profile_name.restype = C.c_char_p
+        L.k3moe_saliency.argtypes = [vp, i32]
+        L.k3moe_forward_partial.argtypes = [vp, vp, i32, vp, vp, vp, vp]
+        L.k3moe_check_guards.argtypes = [vp]
+        L.k3moe_test_withhold_copies.argtypes = [vp]
+        L.k3moe_finish.argtypes = [vp, vp, vp, i32, vp, vp]
+        L.k3moe_saliency_read.argtypes = [vp, vp, i32, C.POINTER(C.c_ulonglong)]
+        L.k3moe_saliency_reset.argtypes = [vp]
         for f in ("k3moe_create", "k3moe_load_weights", "k3moe_forward", "k3moe_forward_host", "k3moe_status",
                   "k3moe_mxfp4_dequant", "k3moe_route", "k3moe_route_noalloc", "k3moe_fetch", "k3moe_query",
-                  "k3moe_profile",
-                  "k3moe_profile_read"):
+                  "k3moe_profile", "k3moe_profile_read", "k3moe_saliency", "k3moe_saliency_read",
+                  "k3moe_saliency_reset", "k3moe_forward_partial", "k3moe_finish", "k3moe_check_guards",
+                  "k3moe_test_withhold_copies"):
             getattr(L, f).restype = C.c_int
         _lib = L
     return _lib
@@ -109,9 +128,12 @@ def _check(rc: int, ctx=None):
 PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_STREAM, PATH_BLOCK_SCALED = 0, 1, 2, 3, 4
 
 
-def make_config(d: LayerDims, max_tokens: int, spin_timeout_ms: int = 0, force_path: int = 0) -> Config:
+def make_config(d: LayerDims, max_tokens: int, spin_timeout_ms: int = 0, force_path: int = 0,
+                expert_begin: int = 0, expert_count: int = 0) -> Config:
     return Config(d.hidden, d.latent, d.n_experts, d.top_k, d.inter, d.group, d.beta, d.beta_lin, d.rms_eps,
-                  d.routed_scaling, int(d.norm_topk), int(max_tokens), int(spin_timeout_ms), int(force_path))
+                  d.routed_scaling, int(d.norm_topk), int(max_tokens), int(spin_timeout_ms), int(force_path),
+                  int(d.n_shared), int(d.shared_inter), int(expert_begin), int(expert_count),
+                  int(d.bank2_begin))
 
 
 # ------------------------------------------------------------------ raw calls
@@ -125,6 +147,9 @@ def load_weights(ctx, w: dict):
     s = Weights()
     keep = {}
     for name, _ in Weights._fields_:
+        if name in OPTIONAL_WEIGHTS and name not in w:
+            setattr(s, name, None)
+            continue
         a = np.ascontiguousarray(w[name])
         keep[name] = a
         setattr(s, name, a.ctypes.data)
@@ -138,6 +163,15 @@ def forward(ctx, x, T: int, y, topk_idx, topk_w, stream=None):
 def forward_host(ctx, x_host, T: int, y_host, idx_host=None, w_host=None, stream=None):
     _check(lib().k3moe_forward_host(ctx, _ptr(x_host), int(T), _ptr(y_host), _ptr(idx_host), _ptr(w_host),
                                     _stream(stream)), ctx)
+
+
+def forward_partial(ctx, x, T: int, c_partial, topk_idx, topk_w, stream=None):
+    _check(lib().k3moe_forward_partial(ctx, _ptr(x), int(T), _ptr(c_partial), _ptr(topk_idx), _ptr(topk_w),
+                                       _stream(stream)), ctx)
+
+
+def finish(ctx, x, c_sum, T: int, y, stream=None):
+    _check(lib().k3moe_finish(ctx, _ptr(x), _ptr(c_sum), int(T), _ptr(y), _stream(stream)), ctx)
 
 
 def status(ctx) -> int:
@@ -181,16 +215,35 @@ def profile_read(ctx) -> list:
     return [(lib().k3moe_profile_name(ctx, i).decode(), float(buf[i])) for i in range(min(n.value, 16))]
 
 
+def saliency(ctx, enable: bool = True):
+    _check(lib().k3moe_saliency(ctx, int(enable)), ctx)
+
+
+def saliency_read(ctx, n_experts: int):
+    """(sums [E] float64, tokens): REAP saliency S = sums / tokens."""
+    sums = np.empty(n_experts, np.float64)
+    tok = C.c_ulonglong()
+    _check(lib().k3moe_saliency_read(ctx, sums.ctypes.data, int(n_experts), C.byref(tok)), ctx)
+    return sums, int(tok.value)
+
+
+def saliency_reset(ctx):
+    _check(lib().k3moe_saliency_reset(ctx), ctx)
+
+
 # ------------------------------------------------------------------ convenience
 class Layer:
     """One context: create + load_weights on construction, destroy on close."""
 
     def __init__(self, d: LayerDims, weights: dict, max_tokens: int, device: int = 0, spin_timeout_ms: int = 0,
-                 force_path: int = PATH_AUTO):
+                 force_path: int = PATH_AUTO, expert_begin: int = 0, expert_count: int = 0):
+        """`weights` holds the expert tensors of experts [expert_begin,
+        expert_begin + expert_count) only when expert_count > 0 (a shard)."""
         self.d = d
         self.max_tokens = max_tokens
         self.force_path = force_path
-        self.ctx = create(make_config(d, max_tokens, spin_timeout_ms, force_path), device)
+        self.ctx = create(make_config(d, max_tokens, spin_timeout_ms, force_path, expert_begin, expert_count),
+                          device)
         try:
             load_weights(self.ctx, weights)
         except Exception:
@@ -220,6 +273,9 @@ class Layer:
 
     def status(self) -> int:
         return status(self.ctx)
+
+    def check_guards(self) -> int:
+        return int(lib().k3moe_check_guards(self.ctx))
 
     def close(self):
         if self.ctx is not None:

@@ -54,6 +54,14 @@ def test_create_rejects_bad_config(L):
     h = C.c_void_p()
     rc = L.k3moe_create(C.byref(k3moe.make_config(TINY, 0)), 0, C.byref(h))
     assert rc == k3moe.EINVAL and "max_tokens" in k3moe.last_error()
+    # shared experts: both fields or neither, a 128-multiple total, tensor-core paths only
+    for d, path, word in [(TINY.with_(n_shared=2, shared_inter=100), 0, "multiple of 128"),
+                          (TINY.with_(n_shared=2, shared_inter=0), 0, "both"),
+                          (TINY.with_(n_shared=2, shared_inter=384), 1, "force_path"),
+                          (TINY.with_(n_shared=2, shared_inter=384), 3, "force_path")]:
+        h = C.c_void_p()
+        rc = L.k3moe_create(C.byref(k3moe.make_config(d, 16, force_path=path)), 0, C.byref(h))
+        assert rc == k3moe.EINVAL and word in k3moe.last_error(), (d, path, k3moe.last_error())
 
 
 def test_create_without_gpu_reports_cuda_error(L):

@@ -111,7 +111,7 @@ def _sampled(layer, w, x, n_sample, seed, label):
 def test_k3_prefill_8192(k3layer):
     w, layer = k3layer
     x = gapped_tokens(K3, w, seed=300, T=8192)
-    _sampled(layer, w, x, 24, 1, "prefill T=8192")
+    _sampled(layer, w, x, 128, 1, "prefill T=8192")
 
 
 @pytest.mark.parametrize("path", [k3moe.PATH_TENSOR_CORE, k3moe.PATH_BLOCK_SCALED], ids=["tensorcore", "blockscaled"])
@@ -121,7 +121,7 @@ def test_k3_skewed_4096(path):
     layer = k3moe.Layer(K3, w, max_tokens=4096, force_path=path)
     try:
         x = gapped_tokens(K3, w, seed=301, T=4096)
-        idx = _sampled(layer, w, x, 16, 2, "skew T=4096")
+        idx = _sampled(layer, w, x, 128, 2, "skew T=4096")
         assert np.isin(idx, hot).all()
         counts = layer.fetch("counts", (K3.n_experts,), np.int32)
         assert np.count_nonzero(counts) == 32 and counts.sum() == 4096 * 16

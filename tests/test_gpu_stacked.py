@@ -26,7 +26,7 @@ pytestmark = pytest.mark.gpu
 
 N_LAYERS = 4
 T_PREFILL = 32768
-N_SAMPLE = 8
+N_SAMPLE = 64  # per layer: leaves well over 30 tokens outside the near-tie band
 
 
 def rescale(y_bits: torch.Tensor) -> torch.Tensor:
