@@ -86,6 +86,8 @@ struct k3moe_ctx {
   k3::BsWeights bw{};
   long long launches_last = 0;
   int path_last = 0;
+  int split_dn_last = 1;  // K parts of the last forward's down GEMM (o lives in part planes when > 1)
+  int T_last = 0;
   // optional per-step timing: events around each launch group of a forward
   static constexpr int kMaxProf = 16;
   bool prof = false;
@@ -644,6 +646,7 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
               3, "permute");
   }
   const int max_active = std::min(d.E, T * d.K);
+  int split_gu = 1, split_dn = 1;  // K parts of the T = 1 expert kernels
   if (big) {
     K3_LAUNCH(k3::umma_experts(c->umma, c->gu_tiles, c->d_tiles, w, T, d, s), k3::umma_expert_launches(),
               "experts (tensor cores)");
@@ -662,8 +665,13 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
     // tiles [0, count[1]) and the second bank's kernels the rest: the split
     // is read on the device, no host synchronisation
     const int* count_a = c->bank2_begin ? tile_count + 1 : tile_count;
-    K3_LAUNCH(k3::bs_stream_gateup(c->bs, c->bw, tiles, count_a, w, T, d, bn, s), 1, "gate/up");
-    K3_LAUNCH(k3::bs_stream_down(c->bs, c->bw, tiles, count_a, w, T, d, bn, s), 1, "down");
+    // T = 1: the K experts' work items are split along K (both kernels)
+    split_gu = c->bank2_begin ? 1 : k3::bs_split_gateup(c->bs, d, T);
+    split_dn = c->bank2_begin ? 1 : k3::bs_split_down(c->bs, d, T);
+    K3_LAUNCH(k3::bs_stream_gateup(c->bs, c->bw, tiles, count_a, w, T, d, bn, s, split_gu,
+                                                c->sharded ? n_local : nullptr), split_gu > 1 ? 2 : 1,
+              "gate/up");
+    K3_LAUNCH(k3::bs_stream_down(c->bs, c->bw, tiles, count_a, w, T, d, bn, s, split_dn), 1, "down");
     if (c->bank2_begin)
       K3_LAUNCH(k3::umma_bank2_experts(c->umma, c->gu2_tiles, c->d2_tiles, c->bank2_begin, d.E - c->bank2_begin, bn,
                                        w, T, d, s),
@@ -680,8 +688,12 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
               "gate/up");
     K3_LAUNCH(k3::launch_down_gemv(c->d_tiles, w.h, w.active, w.offsets, max_active, d, w.o, s), 1, "down");
   }
-  K3_LAUNCH(k3::launch_combine_rmsnorm(w.o, w.slot, wts, c->gamma, T, d.K, d, w.n, c->sal_on ? c->sal_tk : nullptr,
-                                       n_local, c_out, s),
+  // with a K-split down GEMM the combine reads o as the sum of its parts
+  const float* o_src = split_dn > 1 ? k3::bs_down_parts(c->bs, d) : w.o;
+  c->split_dn_last = split_dn;
+  c->T_last = T;
+  K3_LAUNCH(k3::launch_combine_rmsnorm(o_src, w.slot, wts, c->gamma, T, d.K, d, w.n, c->sal_on ? c->sal_tk : nullptr,
+                                       n_local, c_out, s, split_dn, (size_t)T * d.K * d.L),
             1, c_out ? "partial combine" : "combine + RMSNorm");
   if (c->sal_on)
     K3_LAUNCH(k3::launch_saliency_accumulate(c->sal_tk, w.perm, w.offsets, w.active, T, d.E, c->sal_sum,
@@ -834,6 +846,22 @@ int k3moe_fetch(k3moe_ctx* c, int which, void* dst, size_t bytes) {
   if (bytes > cap) return fail(c, K3MOE_EINVAL, "buffer %d holds %zu bytes, %zu requested", which, cap, bytes);
   K3_CUDA(c, cudaSetDevice(c->device), "cudaSetDevice");
   K3_CUDA(c, cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+  if (which == K3MOE_BUF_O && c->split_dn_last > 1) {
+    // the down GEMM ran in K parts: o is their sum, in part order, as the
+    // combine formed it
+    const size_t plane = (size_t)c->T_last * c->d.K * c->d.L;
+    std::vector<float> parts(plane * c->split_dn_last);
+    K3_CUDA(c, cudaMemcpy(parts.data(), k3::bs_down_parts(c->bs, c->d), parts.size() * 4, cudaMemcpyDeviceToHost),
+            "fetch");
+    std::vector<float> o(plane);
+    for (size_t i = 0; i < plane; ++i) {
+      float v = parts[i];
+      for (int pp = 1; pp < c->split_dn_last; ++pp) v += parts[pp * plane + i];
+      o[i] = v;
+    }
+    memcpy(dst, o.data(), std::min(bytes, plane * 4));
+    return K3MOE_OK;
+  }
   K3_CUDA(c, cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost), "fetch");
   return K3MOE_OK;
 }

@@ -476,7 +476,32 @@ struct BsParams {
   unsigned* status;
   uint64_t limit_ns;
   int withhold_item;   // test hook: the stage of this work item's first k step gets no copies (-1: none)
+  // K split (decode tiles): each (tile, row block) is n_split work items over
+  // consecutive ranges of the K steps; with n_split > 1 the epilogue writes
+  // fp32 partial sums (GATEUP: gate to part_a, up to part_b; DOWN: o to
+  // part_a), [n_split][rows_max][ld_out], and a later kernel adds them in
+  // part order
+  int n_split;
+  int part_rows;       // rows of a part plane (the slots: T * K)
+  float* part_a;
+  float* part_b;
 };
+
+// Work item -> (tile, row block, K part) and the part's K-step range.
+struct BsItem {
+  int ti, mt, part, k0, k1;
+};
+__device__ __forceinline__ BsItem bs_item(const BsParams& p, int item) {
+  BsItem it;
+  const int per_tile = p.MT * p.n_split;
+  it.ti = item / per_tile;
+  const int rem = item - it.ti * per_tile;
+  it.mt = rem / p.n_split;
+  it.part = rem - it.mt * p.n_split;
+  it.k0 = it.part * p.KS / p.n_split;
+  it.k1 = (it.part + 1) * p.KS / p.n_split;
+  return it;
+}
 
 template <int MODE, int NQ>
 __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kCtas)
@@ -494,7 +519,7 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
 
   pdl_trigger();
   pdl_wait();
-  const int n_items = *p.count * p.MT;
+  const int n_items = *p.count * p.MT * p.n_split;
   if ((int)blockIdx.x >= n_items) return;
 
   if (threadIdx.x == 0) {
@@ -524,11 +549,11 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
       int kg = 0, issued = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const int ti = item / p.MT;
+        const BsItem bi = bs_item(p, item);
+        const int ti = bi.ti, mt = bi.mt;
         const int4 tile = p.tiles[ti];
-        const int mt = item - ti * p.MT;
         const size_t tile0 = ((size_t)tile.x * p.MT + mt) * p.KC;  // (expert, row tile) chunk 0
-        for (int ks = 0; ks < p.KS; ++ks, ++kg) {
+        for (int ks = bi.k0; ks < bi.k1; ++ks, ++kg) {
           const int s = kg % C::kStages, u = kg / C::kStages;
           if (u > 0 && !mbar_wait(sfree(s), (u - 1) & 1, g, 1u)) {
             ok = false;
@@ -539,7 +564,7 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
           // GATEUP: tiles / atoms (kc, gate), (kc, up); DOWN: (kc0) .. (kc0 + kNK - 1)
           const int n_sfa = (MODE == BS_GATEUP) ? 2 : nk;
           const size_t first = (MODE == BS_GATEUP) ? (tile0 + kc0) * 2 : tile0 + kc0;
-          if (item == p.withhold_item && ks == 0) {
+          if (item == p.withhold_item && ks == bi.k0) {
             // test hook: this stage's full barrier never completes, so the
             // MMA issuer's bounded wait runs out and the CTA aborts
             ++issued;
@@ -590,7 +615,8 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
         tc_fence_after();
         const uint32_t d0 = tmem + buf * C::kBufStride;
         const uint32_t n = (uint32_t)C::kAccW;  // MMA N: every term of the tile's NQ rows
-        for (int ks = 0; ks < p.KS; ++ks, ++kg) {
+        const BsItem bi = bs_item(p, item);
+        for (int ks = bi.k0; ks < bi.k1; ++ks, ++kg) {
           const int s = kg % C::kStages;
           if (!mbar_wait(full(s), (kg / C::kStages) & 1, g, 4u)) {
             ok = false;
@@ -611,7 +637,7 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
             for (int t = 0; t < C::kSfbAtoms; ++t)
               if (c < nk)
                 tc_cp_scales(sfc + 4 * C::kNA + 4 * (c * C::kSfbAtoms + t), sfb_base + so + ((c * 2 + t) * kAtom >> 4));
-          const uint32_t first = ks ? 1u : 0u;
+          const uint32_t first = ks > bi.k0 ? 1u : 0u;
           if constexpr (C::kFp4) {
             // kind::mxf4: K = 64 per MMA (32 bytes of each 64-byte row), two
             // scale bytes per row and MMA (scale ids 0 and 2)
@@ -672,9 +698,9 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
       const int use = (C::kDBuf == 2) ? (it >> 1) : it;
       if (!mbar_wait(dfull(buf), use & 1, g, 8u)) break;
       tc_fence_after();
-      const int ti = item / p.MT;
+      const BsItem bi = bs_item(p, item);
+      const int ti = bi.ti, mt = bi.mt;
       const int4 tile = p.tiles[ti];
-      const int mt = item - ti * p.MT;
       const int m = mt * kQM + r;
       const uint32_t dbase = lane_base + buf * C::kBufStride;
       // Token columns per group: 32, or NQ for decode tiles, whose terms'
@@ -726,7 +752,27 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
           for (int i = 0; i < 8; ++i) v[c8 + i] += t[i];
         }
       };
-      if (MODE == BS_GATEUP) {
+      if (!C::kBig && p.n_split > 1) {
+        // a K part: fp32 partial sums of the tile's tokens, [part][slot][row]
+#pragma unroll 1
+        for (int j0 = JW * wg; j0 < NQ; j0 += JW * kWG) {
+          float acc[32], up[32];
+          load_acc(dbase, j0, acc);
+          if (MODE == BS_GATEUP) load_acc(dbase + C::kAccStride, j0, up);
+          if (j0 + JW * kWG >= NQ) {
+            tc_fence_before();
+            mbar_arrive(dempty(buf));
+          }
+#pragma unroll
+          for (int j = 0; j < JW; ++j) {
+            if (j0 + j < tile.z) {
+              const size_t at = ((size_t)bi.part * p.part_rows + tile.y + j0 + j) * p.ld_out + m;
+              p.part_a[at] = acc[j];
+              if (MODE == BS_GATEUP) p.part_b[at] = up[j];
+            }
+          }
+        }
+      } else if (MODE == BS_GATEUP) {
         // h as bf16 and as the block-scaled terms (and scale atoms) of the down
         // GEMM's B operand, laid out for the down kernel's tiles
         constexpr int kHStack = NQ;  // the down kernel's tiles have the same height
@@ -917,6 +963,7 @@ struct BsWs {
   uint8_t *lq, *lsf;
   uint8_t *hq, *hsf;  // h rows: the same over I
   int* slot_tile;     // [rows_max]: tile << 8 | row within the tile
+  float* part;        // K-split partial sums (T = 1): kBsMaxSplit planes of K rows of I (gate), I (up), L (down)
   size_t total;
 };
 BsWs bs_ws_view(void* base, const Dims& d, int max_tokens) {
@@ -926,16 +973,17 @@ BsWs bs_ws_view(void* base, const Dims& d, int max_tokens) {
   // tiles hold at least one slot and at most one expert: <= E + R / 16 whatever the tile height
   const size_t MT = (size_t)d.E + R / 16 + 1;
   auto terms = [&](size_t C) { return std::max(2 * R * C, (size_t)kFp4Terms * Rf * C / 2); };
-  const size_t sizes[5] = {terms(d.L), MT * (d.L / kQK) * 2 * kAtom, terms(d.I), MT * (d.I / kQK) * 2 * kAtom,
-                           R * sizeof(int)};
+  const size_t sizes[6] = {terms(d.L), MT * (d.L / kQK) * 2 * kAtom, terms(d.I), MT * (d.I / kQK) * 2 * kAtom,
+                           R * sizeof(int), (size_t)kBsMaxSplit * d.K * (2 * d.I + d.L) * sizeof(float)};
   uint8_t* b = static_cast<uint8_t*>(base);
-  uint8_t* ptr[5];
+  uint8_t* ptr[6];
   size_t off = 0;
-  for (int i = 0; i < 5; ++i) {
+  for (int i = 0; i < 6; ++i) {
     ptr[i] = b ? b + off : nullptr;
     off += up(sizes[i]);
   }
-  return BsWs{(int)R, (int)Rf, (int)MT, ptr[0], ptr[1], ptr[2], ptr[3], reinterpret_cast<int*>(ptr[4]), off};
+  return BsWs{(int)R,  (int)Rf, (int)MT, ptr[0], ptr[1], ptr[2], ptr[3], reinterpret_cast<int*>(ptr[4]),
+              reinterpret_cast<float*>(ptr[5]), off};
 }
 
 template <int MODE, int NQ>
@@ -1015,11 +1063,102 @@ cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims
                     ws.lq, ws.lsf);
 }
 
+// Best K split for `items` decode work items of `ks` K steps over `ctas`
+// persistent CTAs: the one with the fewest item-times on the busiest CTA
+// (every part keeps at least one K step).
+int bs_best_split(int items, int ks, int ctas) {
+  int best = 1;
+  double best_t = 1e30;
+  for (int sp = 1; sp <= std::min(kBsMaxSplit, ks); ++sp) {
+    const double t = (double)((items * sp + ctas - 1) / ctas) / sp;
+    if (t < best_t - 1e-9) {
+      best_t = t;
+      best = sp;
+    }
+  }
+  return best;
+}
+
+int bs_split_gateup(const BsPlan& p, const Dims& d, int T) {
+  using C = BsCfg<BS_GATEUP, kBsDecodeRows>;
+  const int ks = (d.L / kQK + C::kNK - 1) / C::kNK;
+  return T == 1 ? bs_best_split(d.K * (d.I / kQM), ks, C::kCtas * p.num_sms) : 1;
+}
+int bs_split_down(const BsPlan& p, const Dims& d, int T) {
+  using C = BsCfg<BS_DOWN, kBsDecodeRows>;
+  const int ks = (d.I / kQK + C::kNK - 1) / C::kNK;
+  return T == 1 ? bs_best_split(d.K * (d.L / kQM), ks, C::kCtas * p.num_sms) : 1;
+}
+float* bs_down_parts(const BsPlan& p, const Dims& d) {
+  return bs_ws_view(p.ws, d, p.max_tokens).part + (size_t)kBsMaxSplit * d.K * 2 * d.I;
+}
+
+// The gate/up K parts of a T = 1 forward added in part order, then SiTU-GLU
+// and the h outputs of the gate/up epilogue (bf16 h, its e2m1 terms and
+// scale atoms for the down kernel): one warp per (slot, 32 rows of I), a
+// row per lane, the 32 rows one scale group of the down GEMM's K.  With an
+// expert shard only the shard's own slots [0, *rows_dev) are finished: the
+// other slots have no partial sums and no tile this forward.
+__global__ void __launch_bounds__(256) bs_gateup_finish_kernel(const BsParams p, const int* __restrict__ slot_tile,
+                                                               int TK, const int* __restrict__ rows_dev) {
+  pdl_trigger();
+  pdl_wait();
+  if (rows_dev) TK = min(TK, *rows_dev);
+  constexpr int kHTerms = BsCfg<BS_DOWN, kBsDecodeRows>::kTerms;
+  constexpr int kHStack = kBsDecodeRows;
+  const int lane = threadIdx.x & 31;
+  const int G = p.ld_out / 32, KCo = p.ld_out / kQK;
+  const int nw = (int)((gridDim.x * blockDim.x) >> 5);
+  for (int wi = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); wi < TK * G; wi += nw) {
+    const int sl = wi / G, m = (wi - sl * G) * 32 + lane;
+    float gs = 0.f, us = 0.f;
+    for (int part = 0; part < p.n_split; ++part) {
+      const size_t at = ((size_t)part * p.part_rows + sl) * p.ld_out + m;
+      gs += p.part_a[at];
+      us += p.part_b[at];
+    }
+    const uint16_t hb = f32_to_bf16(situ_fast(gs, us, p.beta, p.beta_lin));
+    p.h[(size_t)sl * p.ld_out + m] = hb;
+    float rr = bf16_to_f32(hb);
+    uint32_t qn = 0;
+    unsigned long long sc = 0;
+#pragma unroll
+    for (int t = 0; t < kHTerms; ++t) {
+      const uint32_t sb = e2m1_scale_byte(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(rr))));
+      uint32_t qb = 0;
+      if (sb != 255u) {
+        qb = to_e2m1x2(0.f, rr * exp2_any(127 - (int)sb)) & 0xFu;
+        rr = fmaf(-from_e2m1x2(qb).x, exp2_any((int)sb - 127), rr);
+      } else {
+        rr = 0.f;
+      }
+      qn |= qb << (4 * t);
+      sc |= (unsigned long long)sb << (8 * t);
+    }
+    const uint32_t qo = __shfl_down_sync(0xFFFFFFFFu, qn, 1);
+    if (!(lane & 1)) {
+#pragma unroll
+      for (int t = 0; t < kHTerms; ++t)
+        p.hq[(((size_t)(m >> 7) * kHTerms + t) * p.rows_max + sl) * 64 + ((m & 127) >> 1)] =
+            (uint8_t)(((qn >> (4 * t)) & 0xFu) | (((qo >> (4 * t)) & 0xFu) << 4));
+    }
+    if (lane == 0) {  // the group's scales are the same on every lane
+      const int st = slot_tile[sl];
+      uint8_t* atoms = p.hsf + (((size_t)(st >> 8) * KCo + (m >> 7)) * 2) * kAtom + ((m >> 5) & 3);
+#pragma unroll
+      for (int t = 0; t < kHTerms; ++t) atoms[act_scale_byte(t, st & 0xFF, kHStack)] = (uint8_t)(sc >> (8 * t));
+    }
+  }
+}
+
 cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* tiles, const int* tile_count,
-                             const Work& w, int T, const Dims& d, int tile_rows, cudaStream_t s) {
+                             const Work& w, int T, const Dims& d, int tile_rows, cudaStream_t s, int n_split,
+                             const int* n_local) {
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
-  if (T > p.max_tokens) return cudaErrorInvalidValue;
+  if (T > p.max_tokens || n_split < 1 || n_split > kBsMaxSplit ||
+      (n_split > 1 && (T != 1 || tile_rows != kBsDecodeRows)))
+    return cudaErrorInvalidValue;
   const BsWs ws = bs_ws_view(p.ws, d, p.max_tokens);
   BsParams prm{};
   prm.ld_out = d.I;
@@ -1028,6 +1167,19 @@ cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* t
   prm.hsf = ws.hsf;
   prm.beta = d.beta;
   prm.beta_lin = d.beta_lin;
+  prm.n_split = n_split;
+  prm.part_rows = TK;
+  prm.part_a = ws.part;
+  prm.part_b = ws.part + (size_t)kBsMaxSplit * d.K * d.I;
+  if (tile_rows == kBsDecodeRows && n_split > 1) {
+    cudaError_t e = launch_bs<BS_GATEUP, kBsDecodeRows>(p, bw.gu_q, bw.gu_sf, bw.n_exp, d.I, d.L, ws.lq, ws.lsf,
+                                                        ws.rows_fp4, tiles, tile_count, prm, s);
+    if (e != cudaSuccess) return e;
+    prm.rows_max = ws.rows_fp4;
+    const int warps = TK * (d.I / 32);
+    return launch_pdl(bs_gateup_finish_kernel, (warps + 7) / 8, 256, 0, s, prm, (const int*)ws.slot_tile, TK,
+                      n_local);
+  }
   if (tile_rows == kBsDecodeRows)
     return launch_bs<BS_GATEUP, kBsDecodeRows>(p, bw.gu_q, bw.gu_sf, bw.n_exp, d.I, d.L, ws.lq, ws.lsf, ws.rows_fp4,
                                                tiles, tile_count, prm, s);
@@ -1038,14 +1190,19 @@ cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* t
 }
 
 cudaError_t bs_stream_down(const BsPlan& p, const BsWeights& bw, const int4* tiles, const int* tile_count,
-                           const Work& w, int T, const Dims& d, int tile_rows, cudaStream_t s) {
+                           const Work& w, int T, const Dims& d, int tile_rows, cudaStream_t s, int n_split) {
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
-  if (T > p.max_tokens) return cudaErrorInvalidValue;
+  if (T > p.max_tokens || n_split < 1 || n_split > kBsMaxSplit ||
+      (n_split > 1 && (T != 1 || tile_rows != kBsDecodeRows)))
+    return cudaErrorInvalidValue;
   const BsWs ws = bs_ws_view(p.ws, d, p.max_tokens);
   BsParams prm{};
   prm.ld_out = d.L;
   prm.o = w.o;
+  prm.n_split = n_split;
+  prm.part_rows = TK;
+  prm.part_a = ws.part + (size_t)kBsMaxSplit * d.K * 2 * d.I;  // the combine adds the parts
   if (tile_rows == kBsDecodeRows)
     return launch_bs<BS_DOWN, kBsDecodeRows>(p, bw.d_q, bw.d_sf, bw.n_exp, d.L, d.I, ws.hq, ws.hsf, ws.rows_fp4, tiles,
                                              tile_count, prm, s);

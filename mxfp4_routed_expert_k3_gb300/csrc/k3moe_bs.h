@@ -54,6 +54,7 @@ struct BsPlan {
 constexpr int kBsDecodeRows = 16;
 constexpr int kBsPrefillRows = 80;
 constexpr int kBsDecodeMaxT = 128;  // largest T run on decode tiles
+constexpr int kBsMaxSplit = 4;      // most K parts of a T = 1 work item
 inline int bs_tile_rows(int T) { return T <= kBsDecodeMaxT ? kBsDecodeRows : kBsPrefillRows; }
 size_t bs_ws_bytes(const Dims& d, int max_tokens);
 // slot -> (tile << 8 | row in tile), written by the tile-list builders
@@ -71,10 +72,20 @@ cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims
                                const int* n_local, cudaStream_t s);
 // gate/up over the tile list (tiles of at most tile_rows rows): h (bf16,
 // slot order) and its block-scaled terms for the down GEMM.
+// At T = 1 the K experts give K x (rows / 128) work items, fewer than twice
+// the persistent CTAs, so the busiest CTA would take two items: each item's
+// K range is then split in n_split parts (the bs_split_* choice) whose fp32
+// partial sums are added in part order -- for gate/up by a finish kernel
+// (SiTU-GLU and h's terms), for down by the combine (bs_down_parts, planes
+// of T*K rows of L).
+int bs_split_gateup(const BsPlan& p, const Dims& d, int T);
+int bs_split_down(const BsPlan& p, const Dims& d, int T);
+float* bs_down_parts(const BsPlan& p, const Dims& d);
 cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* tiles, const int* tile_count,
-                             const Work& w, int T, const Dims& d, int tile_rows, cudaStream_t s);
+                             const Work& w, int T, const Dims& d, int tile_rows, cudaStream_t s, int n_split = 1,
+                             const int* n_local = nullptr);
 // down: o (fp32, slot order)
 cudaError_t bs_stream_down(const BsPlan& p, const BsWeights& bw, const int4* tiles, const int* tile_count,
-                           const Work& w, int T, const Dims& d, int tile_rows, cudaStream_t s);
+                           const Work& w, int T, const Dims& d, int tile_rows, cudaStream_t s, int n_split = 1);
 
 }  // namespace k3

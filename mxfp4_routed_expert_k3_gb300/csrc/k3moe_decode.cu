@@ -749,7 +749,8 @@ __global__ void __launch_bounds__(1024) combine_rmsnorm_kernel(const float* __re
                                                                float eps, uint16_t* __restrict__ n,
                                                                float* __restrict__ sal_tk,
                                                                const int* __restrict__ n_local,
-                                                               float* __restrict__ c_out) {
+                                                               float* __restrict__ c_out, int o_parts,
+                                                               size_t o_part_stride) {
   // One CTA per token; thread i owns latent columns 4i..4i+3 (plus further
   // groups of 4*blockDim.x when L is larger); the K slot rows of a column
   // group are loaded together so their latencies overlap.
@@ -784,6 +785,18 @@ __global__ void __launch_bounds__(1024) combine_rmsnorm_kernel(const float* __re
       for (int k = 0; k < 8; ++k)
         if (k0 + k < K && (!PARTIAL || kloc[k0 + k]))
           v[k] = __ldg(reinterpret_cast<const float4*>(o + (size_t)sl[k0 + k] * L) + c4);
+      // o split in K parts (T = 1): the parts are added in part order
+      for (int pp = 1; pp < o_parts; ++pp) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (k0 + k < K && (!PARTIAL || kloc[k0 + k])) {
+            const float4 q = __ldg(reinterpret_cast<const float4*>(o + pp * o_part_stride + (size_t)sl[k0 + k] * L) + c4);
+            v[k].x += q.x;
+            v[k].y += q.y;
+            v[k].z += q.z;
+            v[k].w += q.w;
+          }
+      }
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         if (k0 + k < K && (!PARTIAL || kloc[k0 + k])) {
@@ -935,14 +948,15 @@ cudaError_t prepare_decode_kernels(const Dims& d) {
 
 cudaError_t launch_combine_rmsnorm(const float* o, const int* slot, const float* topk_w, const uint16_t* gamma,
                                    int T, int K, const Dims& d, uint16_t* n, float* sal_tk, const int* n_local,
-                                   float* c_out, cudaStream_t s) {
+                                   float* c_out, cudaStream_t s, int o_parts, size_t o_part_stride) {
   if (T <= 0) return cudaSuccess;
   if (K < 1 || K > 32 || (c_out && !n_local)) return cudaErrorInvalidValue;
   const int threads = std::min(1024, ((d.L / 4 + 31) / 32) * 32);
   const size_t sm = sizeof(float) * d.L;
   auto kernel = c_out ? (sal_tk ? combine_rmsnorm_kernel<true, true> : combine_rmsnorm_kernel<false, true>)
                       : (sal_tk ? combine_rmsnorm_kernel<true, false> : combine_rmsnorm_kernel<false, false>);
-  return launch_pdl(kernel, T, threads, sm, s, o, slot, topk_w, gamma, K, d.L, d.rms_eps, n, sal_tk, n_local, c_out);
+  return launch_pdl(kernel, T, threads, sm, s, o, slot, topk_w, gamma, K, d.L, d.rms_eps, n, sal_tk, n_local, c_out,
+                    o_parts, o_part_stride);
 }
 
 cudaError_t launch_saliency_accumulate(const float* sal_tk, const int* perm, const int* offsets, const int* active,

@@ -69,9 +69,11 @@ cudaError_t launch_route_small(const float* logits, int T, int E, const float* b
 // sal_tk (optional, [T*K]): also w_k ||o_k||_2 per (token, k), the REAP
 // saliency terms.  c_out (optional, [T, L] fp32): write the combine itself
 // instead of n, adding only slots below *n_local (an expert shard's part).
+// o_parts > 1: o is the sum of that many planes o_part_stride floats apart
+// (a K-split down GEMM), added in plane order.
 cudaError_t launch_combine_rmsnorm(const float* o, const int* slot, const float* topk_w, const uint16_t* gamma,
                                    int T, int K, const Dims& d, uint16_t* n, float* sal_tk, const int* n_local,
-                                   float* c_out, cudaStream_t s);
+                                   float* c_out, cudaStream_t s, int o_parts = 1, size_t o_part_stride = 0);
 // sal_sum[e] += the terms of expert e's slots (slot order), *sal_tokens += T
 cudaError_t launch_saliency_accumulate(const float* sal_tk, const int* perm, const int* offsets, const int* active,
                                        int T, int E, double* sal_sum, unsigned long long* sal_tokens,

@@ -130,7 +130,7 @@ struct Params {
   int M;                   // weight rows (DENSE edge masking)
   // token tiling
   TileList list;           // GATEUP / DOWN
-  int T, tn;               // DENSE: tokens and rows per tile
+  int T, tn;               // DENSE: tokens and rows per tile; second bank: token box rows
   // epilogue
   DenseOut dout;           // DENSE
   float* out_f32;          // DOWN: o per slot
@@ -383,6 +383,270 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// =====================================================================
+// Second bank (2-bit affine experts): a persistent kernel over the work
+// items (tile of the tile list's second-bank slice, 128-row weight block),
+// the blocks of one tile consecutive so that CTAs running at the same time
+// share its token rows in L2.  The compressed 2-bit tiles and the token
+// rows stream through a deep ring; eight decode warps expand each k step's
+// weights into bf16 hi and lo tiles (w = scale * q + bias is exact in fp32;
+// hi = bf16(w), lo = bf16(w - hi)) in a two-deep ring; one thread issues
+// the MMAs (hi and lo of each matrix into accumulators of their own); the
+// epilogue adds them and applies SiTU-GLU (gate/up) or stores o (down).
+// Decoded tiles are 8x the size of the compressed ones, so keeping them out
+// of the copy ring lets a CTA keep many compressed stages in flight.
+// =====================================================================
+template <bool GU>
+struct B2Cfg {
+  static constexpr int kNumMat = GU ? 2 : 1;
+  static constexpr int kBN = kTile2MaxRows;                    // token rows per box at most
+  static constexpr int kABytes = kBM * kBK * 2;                // one bf16 tile: 16 KB
+  static constexpr int kBBytes = kBN * kBK * 2;                // room for the largest token box: 10 KB
+  static constexpr int kSrc = kNumMat * kTile2Bytes;           // compressed weights of a k step
+  static constexpr int kRingStage = kBBytes + (kSrc + 1023) / 1024 * 1024;
+  static constexpr int kDecBytes = kNumMat * 2 * kABytes;      // hi and lo of each matrix
+  static constexpr int kRing = GU ? 5 : 10;
+  static constexpr int kAcc = GU ? 1 : 2;                      // K split over accumulators
+  static constexpr int kAccStride = 128, kMatStride = 256;
+  static constexpr int kThreads = 320;                         // TMA, MMA, 8 decode warps (4 of them epilogue)
+  static constexpr int kNB = 2 * kRing + 7;                    // barriers
+  static constexpr int kSmem = 2 * kDecBytes + kRing * kRingStage + 1024 + 512;
+  static_assert(kNumMat * 2 * kAcc * kAccStride <= 512, "TMEM budget");
+  static_assert(kAccStride >= kBN && (kNumMat == 1 || 2 * kAcc * kAccStride <= kMatStride), "accumulator layout");
+  static_assert(8 * kNB + 8 <= 512, "barrier area");
+  static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+template <bool GU>
+__global__ void __launch_bounds__(B2Cfg<GU>::kThreads, 1)
+    bank2_gemm_kernel(const __grid_constant__ CUtensorMap map_b, const Params p) {
+  using C = B2Cfg<GU>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* dec = smem;                           // [2][kNumMat][hi, lo][128 x 64 bf16]
+  uint8_t* ring = smem + 2 * C::kDecBytes;       // [kRing][B | compressed weights]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + C::kRing * C::kRingStage);
+  // bars: full[R], empty[R], dfull[2], dempty[2], tmem_full, tmem_empty, drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNB);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int first = p.list.begin ? *p.list.begin : 0;
+  const int n_items = (*p.list.count - first) * p.MT;
+  if ((int)blockIdx.x >= n_items) return;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kNB; ++i) {
+      const bool dfull_bar = i >= 2 * C::kRing && i < 2 * C::kRing + 2;
+      const bool tmem_empty_bar = i == 2 * C::kRing + 5;
+      mbar_init(smem_u32(bars + i), dfull_bar ? 256u : tmem_empty_bar ? 128u : 1u);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Guard g{abort_flag, p.status, p.limit_ns};
+  auto full = [&](int r) { return smem_u32(bars + r); };
+  auto empty = [&](int r) { return smem_u32(bars + C::kRing + r); };
+  auto dfull = [&](int d) { return smem_u32(bars + 2 * C::kRing + d); };
+  auto dempty = [&](int d) { return smem_u32(bars + 2 * C::kRing + 2 + d); };
+  const uint32_t tmem_full = smem_u32(bars + 2 * C::kRing + 4);
+  const uint32_t tmem_empty = smem_u32(bars + 2 * C::kRing + 5);
+  const uint32_t drain = smem_u32(bars + 2 * C::kRing + 6);
+  auto stage_b = [&](int r) { return ring + (size_t)r * C::kRingStage; };
+  auto stage_w = [&](int r) { return ring + (size_t)r * C::kRingStage + C::kBBytes; };
+  auto dec_tile = [&](int d, int m, int part) { return dec + (size_t)d * C::kDecBytes + (m * 2 + part) * C::kABytes; };
+  const uint32_t b_tx = (uint32_t)(p.tn * kBK * 2);  // one token box
+
+  if (warp == 0) {
+    // ================= TMA producer
+    if (lane == 0) {
+      int kg = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const int4 tile = p.list.tiles[first + item / p.MT];
+        const int mt = item % p.MT, e = tile.x - p.expert_base;
+        const uint8_t* a_src = p.a_tiles + ((size_t)(e * p.MT + mt) * p.KS) * C::kSrc;
+        for (int ks = 0; ks < p.KS; ++ks, ++kg) {
+          const int r = kg % C::kRing, u = kg / C::kRing;
+          if (u > 0 && !mbar_wait(empty(r), (u - 1) & 1, g, 1u)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(full(r), b_tx + C::kSrc);
+          tma_load_2d(smem_u32(stage_b(r)), &map_b, full(r), ks * kBK, tile.y);
+          bulk_load(smem_u32(stage_w(r)), a_src + (size_t)ks * C::kSrc, C::kSrc, full(r));
+        }
+      }
+      if (*abort_flag) {  // copies in flight land before the CTA exits
+        for (int k = max(0, kg - C::kRing); k < kg; ++k) {
+          const uint64_t t0 = global_ns();
+          while (!mbar_try_wait(full(k % C::kRing), (k / C::kRing) & 1))
+            if (global_ns() - t0 > p.limit_ns) break;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================= MMA issuer
+    if (lane == 0) {
+      int kg = 0, it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
+        const int n_mma = p.list.tiles[first + item / p.MT].w;
+        const uint32_t idesc = umma_idesc_bf16(kBM, n_mma);
+        if (it > 0 && !mbar_wait(tmem_empty, (it - 1) & 1, g, 2u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int ks = 0; ks < p.KS; ++ks, ++kg) {
+          const int r = kg % C::kRing, d = kg & 1;
+          if (!mbar_wait(full(r), (kg / C::kRing) & 1, g, 2u) || !mbar_wait(dfull(d), (kg >> 1) & 1, g, 4u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t b0 = smem_u32(stage_b(r));
+          const int acc_k = ks % C::kAcc;
+#pragma unroll
+          for (int m = 0; m < C::kNumMat; ++m)
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+              const uint32_t a0 = smem_u32(dec_tile(d, m, part));
+              const uint32_t acc = (uint32_t)(m * C::kMatStride + (acc_k * 2 + part) * C::kAccStride);
+#pragma unroll
+              for (int kk = 0; kk < kBK / 16; ++kk)
+                umma_bf16(tmem + acc, umma_desc_sw128(a0 + kk * 32), umma_desc_sw128(b0 + kk * 32), idesc,
+                          (ks >= C::kAcc || kk) ? 1u : 0u);
+            }
+          umma_commit(empty(r));
+          umma_commit(dempty(d));
+        }
+        if (ok) umma_commit(tmem_full);
+      }
+      if (!ok) {  // MMAs already issued finish before TMEM is released
+        umma_commit(drain);
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(drain, 0))
+          if (global_ns() - t0 > p.limit_ns) break;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ================= decode (warps 2..9: row dt % 128, columns 32 * (dt / 128) ..),
+    // then the epilogue of each item on warps 2..5 (TMEM lane quarter warp % 4)
+    const int dt = threadIdx.x - 64;
+    const int r = dt & 127, half = dt >> 7;
+    int kg = 0, it = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
+      for (int ks = 0; ks < p.KS; ++ks, ++kg) {
+        const int rr = kg % C::kRing, d = kg & 1;
+        if (!mbar_wait(full(rr), (kg / C::kRing) & 1, g, 8u) ||
+            (kg >= 2 && !mbar_wait(dempty(d), ((kg >> 1) - 1) & 1, g, 32u))) {
+          ok = false;
+          break;
+        }
+        const uint8_t* stg = stage_w(rr);
+#pragma unroll
+        for (int m = 0; m < C::kNumMat; ++m) {
+          const uint8_t* tl = stg + m * kTile2Bytes;
+          const uint2 q = *reinterpret_cast<const uint2*>(tl + (size_t)r * 16 + half * 8);  // 32 codes
+          const float sc = bf16_to_f32(*reinterpret_cast<const uint16_t*>(tl + 2048 + 2 * r));
+          const float bi = bf16_to_f32(*reinterpret_cast<const uint16_t*>(tl + 2304 + 2 * r));
+          // the row's four levels w_q = scale * q + bias (q = 0..3), as bf16
+          // hi = bf16(w_q) and lo = bf16(w_q - hi), packed two per word: level
+          // q occupies bytes 2q, 2q + 1 of the pair {H23:H01} (and {L23:L01})
+          const float w0 = fmaf(sc, 0.f, bi), w1 = fmaf(sc, 1.f, bi);
+          const float w2 = fmaf(sc, 2.f, bi), w3 = fmaf(sc, 3.f, bi);
+          const uint32_t H01 = pack_bf16x2(w0, w1), H23 = pack_bf16x2(w2, w3);
+          const float2 h01 = unpack_bf16x2(H01), h23 = unpack_bf16x2(H23);
+          const uint32_t L01 = pack_bf16x2(w0 - h01.x, w1 - h01.y), L23 = pack_bf16x2(w2 - h23.x, w3 - h23.y);
+          uint8_t* row_hi = dec_tile(d, m, 0) + (size_t)r * 128;
+          uint8_t* row_lo = dec_tile(d, m, 1) + (size_t)r * 128;
+          const uint32_t words[2] = {q.x, q.y};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {  // columns 8 c8 .. 8 c8 + 7, c8 = 4 half + c
+            const int c8 = 4 * half + c;
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+              // four codes c0..c3 (two bits each, low first) -> byte i of sp
+              // holds c_i -> the byte_perm selectors of the pairs (c0, c1)
+              // and (c2, c3): nibbles 2 c_i, 2 c_i + 1 (the bytes of level c_i)
+              const uint32_t x = (words[c >> 1] >> (16 * (c & 1) + 8 * b)) & 0xFFu;
+              const uint32_t ev = x & 0x33u, od = x & 0xCCu;
+              const uint32_t sp = ((ev * 0x1001u) & 0x30003u) | ((od * 0x40040u) & 0x3000300u);
+              const uint32_t z = sp * 0x22u + 0x10101010u;
+              hi[2 * b] = __byte_perm(H01, H23, z & 0xFFFFu);
+              hi[2 * b + 1] = __byte_perm(H01, H23, z >> 16);
+              lo[2 * b] = __byte_perm(L01, L23, z & 0xFFFFu);
+              lo[2 * b + 1] = __byte_perm(L01, L23, z >> 16);
+            }
+            const int sw = (c8 ^ (r & 7)) << 4;
+            *reinterpret_cast<uint4*>(row_hi + sw) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(row_lo + sw) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(dfull(d));
+      }
+      if (!ok || warp >= 6) continue;
+      // ---- epilogue of this item
+      if (!mbar_wait(tmem_full, it & 1, g, 16u) || *abort_flag) {
+        ok = false;
+        continue;
+      }
+      tc_fence_after();
+      const int4 tile = p.list.tiles[first + item / p.MT];
+      const int mt = item % p.MT, row0 = tile.y, rows = tile.z, n_mma = tile.w;
+      const int quarter = warp & 3;
+      const int m = mt * kBM + quarter * 32 + lane;
+      const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+      const int n_acc = min(C::kAcc, p.KS) * 2;
+      for (int j0 = 0; j0 < n_mma; j0 += 16) {
+        float acc[16];
+        tmem_ld16(lane_addr + j0, acc);
+        for (int a = 1; a < n_acc; ++a) {
+          float part[16];
+          tmem_ld16(lane_addr + a * C::kAccStride + j0, part);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[j] += part[j];
+        }
+        if (GU) {
+          float up[16];
+          tmem_ld16(lane_addr + C::kMatStride + j0, up);
+          for (int a = 1; a < n_acc; ++a) {
+            float part[16];
+            tmem_ld16(lane_addr + C::kMatStride + a * C::kAccStride + j0, part);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) up[j] += part[j];
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (j0 + j < rows)
+              p.out_bf16[(size_t)(row0 + j0 + j) * p.ld_out + m] =
+                  f32_to_bf16(situ_fast(acc[j], up[j], p.beta, p.beta_lin));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (j0 + j < rows) p.out_f32[(size_t)(row0 + j0 + j) * p.ld_out + m] = acc[j];
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tmem_empty);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // =====================================================================
@@ -1030,11 +1294,11 @@ cudaError_t prepare_umma_kernels() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(umma_gemm_kernel<DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<DOWN>::kSmem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(umma_gemm_kernel<GATEUP2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<GATEUP2>::kSmem);
+    e = cudaFuncSetAttribute(bank2_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             B2Cfg<true>::kSmem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(umma_gemm_kernel<DOWN2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<DOWN2>::kSmem);
+    e = cudaFuncSetAttribute(bank2_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             B2Cfg<false>::kSmem);
   return e;
 }
 
@@ -1151,13 +1415,14 @@ cudaError_t umma_bank2_experts(const UmmaPlan& p, const uint8_t* gu2_tiles, cons
                                int n_bank2, int tile_rows, const Work& w, int T, const Dims& d, cudaStream_t s) {
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
-  if (tile_rows > kTile2MaxRows) return cudaErrorInvalidValue;  // token box height and TMEM layout
+  if (tile_rows > kTile2MaxRows || tile_rows % 16) return cudaErrorInvalidValue;  // token box and TMEM layout
   UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
   gather_rows_kernel<<<152 * 8, 256, 0, s>>>(w.lat, w.perm, TK, d.K, d.L, ws.lat_perm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CUtensorMap mb1, mb2;
-  if (!make_map(&mb1, ws.lat_perm, TK, d.L, kTile2MaxRows) || !make_map(&mb2, w.h, TK, d.I, kTile2MaxRows))
+  // token boxes as high as the tiles (16 rows at decode sizes, 80 at prefill)
+  if (!make_map(&mb1, ws.lat_perm, TK, d.L, tile_rows) || !make_map(&mb2, w.h, TK, d.I, tile_rows))
     return cudaErrorInvalidValue;
   // at most one tile per second-bank expert with work plus one per 16 slots
   const int max_tiles = std::min(n_bank2, TK) + TK / kMinTileRows + 1;
@@ -1174,8 +1439,11 @@ cudaError_t umma_bank2_experts(const UmmaPlan& p, const uint8_t* gu2_tiles, cons
   g.beta_lin = d.beta_lin;
   g.status = p.status;
   g.limit_ns = p.limit_ns;
-  e = launch_gemm<GATEUP2>(mb1, mb1, g, dim3(g.MT, max_tiles), s);
-  if (e != cudaSuccess) return e;
+  g.tn = tile_rows;
+  // persistent: one CTA per SM at most (the items are counted on the device)
+  bank2_gemm_kernel<true><<<std::min(p.num_sms, g.MT * max_tiles), B2Cfg<true>::kThreads, B2Cfg<true>::kSmem, s>>>(
+      mb1, g);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   Params dn = g;
   dn.a_tiles = d2_tiles;
   dn.MT = d.L / kBM;
@@ -1184,7 +1452,9 @@ cudaError_t umma_bank2_experts(const UmmaPlan& p, const uint8_t* gu2_tiles, cons
   dn.out_bf16 = nullptr;
   dn.out_f32 = w.o;
   dn.ld_out = d.L;
-  return launch_gemm<DOWN2>(mb2, mb2, dn, dim3(dn.MT, max_tiles), s);
+  bank2_gemm_kernel<false><<<std::min(p.num_sms, dn.MT * max_tiles), B2Cfg<false>::kThreads, B2Cfg<false>::kSmem,
+                             s>>>(mb2, dn);
+  return cudaGetLastError();
 }
 
 // Only the slot-ordered latent rows (the tile list was built by the fused
