@@ -24,7 +24,7 @@
 //    e2m1 terms (see the split below).
 //
 // Tile scheme: M = 128 weight rows, N = terms x tile rows (one tile of an
-// expert's slots: 16 rows at decode, 80 at prefill).  Warp 0 issues the
+// expert's slots: 16 rows at decode, 88 at prefill).  Warp 0 issues the
 // copies, warp 1 the MMAs, the remaining warps run the epilogue.  Every wait
 // is bounded (status bit + shared abort flag, as in the bf16 kernels).
 #include <cuda.h>
@@ -163,7 +163,8 @@ __device__ __forceinline__ int act_scale_byte(int t, int n, int stack) { return 
 // Slot-ordered rows: dst row s = src row (perm ? perm[s] / K : s), written
 // as terms q[C/128][t][rows_max][128]; the scales go to the tile atoms
 // sf[tile][C/128][2][512] at act_scale_byte(t, n, stack) + g for row n of
-// the tile (slot_tile[s] = tile << 8 | n).  A half
+// the tile (slot_tile[s] = tile << 8 | n), or, without a slot map, to
+// sf[rows][C/128][2] as one word per term (byte g = group g).  A half
 // warp covers 128 columns per chunk (8 per lane, 4 lanes per scale group)
 // and four chunks of one slot per pass, their loads issued together; the
 // loop runs per warp so that both halves always meet at the shuffles.
@@ -188,7 +189,7 @@ __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, const int* _
     int tn = 0;
     if (valid) {
       const int t = perm ? perm[s] / K : s;
-      tn = slot_tile[s];
+      tn = slot_tile ? slot_tile[s] : 0;
 #pragma unroll
       for (int c = 0; c < kQuantChunks; ++c) {
         const int kc = kg * kQuantChunks + c;
@@ -237,11 +238,49 @@ __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, const int* _
       *reinterpret_cast<uint2*>(q + r0 * kQK + hl * 8) = make_uint2(a0, b0);
       *reinterpret_cast<uint2*>(q + (r0 + rows_max) * kQK + hl * 8) = make_uint2(a1, b1);
       if (hl == 0) {
-        const int n = tn & 0xFF;
-        uint8_t* atom = sf + (((size_t)(tn >> 8) * KC + kc) * 2) * kAtom;
-        *reinterpret_cast<uint32_t*>(atom + act_scale_byte(0, n, stack)) = w0;
-        *reinterpret_cast<uint32_t*>(atom + act_scale_byte(1, n, stack)) = w1;
+        if (slot_tile) {
+          const int n = tn & 0xFF;
+          uint8_t* atom = sf + (((size_t)(tn >> 8) * KC + kc) * 2) * kAtom;
+          *reinterpret_cast<uint32_t*>(atom + act_scale_byte(0, n, stack)) = w0;
+          *reinterpret_cast<uint32_t*>(atom + act_scale_byte(1, n, stack)) = w1;
+        } else {  // row order: [rows][KC][2] words
+          *reinterpret_cast<uint2*>(sf + (((size_t)s * KC + kc) * 2) * 4) = make_uint2(w0, w1);
+        }
       }
+    }
+  }
+}
+
+// Slot-ordered copy of per-token terms (the prefill path splits each token's
+// latent row once, then every slot takes its token's terms): tq
+// [KC][2][T][128] and tsc [T][KC][2] words (byte g = group g's scale) from
+// quant_rows_kernel in row order; slot s copies row perm[s] / K into the
+// planes q[KC][2][rows_max][128] and its scale words into the tile atoms at
+// act_scale_byte(term, n, stack).  One thread per 16 bytes: eight threads
+// move a 128-byte row.
+__global__ void gather_terms_kernel(const uint8_t* __restrict__ tq, const uint8_t* __restrict__ tsc,
+                                    const int* __restrict__ perm, int K, int T, int rows,
+                                    const int* __restrict__ rows_dev, int KC, int rows_max,
+                                    const int* __restrict__ slot_tile, int stack, uint8_t* __restrict__ q,
+                                    uint8_t* __restrict__ sf) {
+  pdl_trigger();
+  pdl_wait();
+  if (rows_dev) rows = min(rows, *rows_dev);  // an expert shard: its own slots only
+  const long long total = (long long)rows * KC * 16;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int piece = (int)(i & 7), term = (int)((i >> 3) & 1);
+    const long long sk = i >> 4;
+    const int kc = (int)(sk % KC), sl = (int)(sk / KC);
+    const int t = perm[sl] / K;
+    const size_t plane = (size_t)kc * 2 + term;
+    *reinterpret_cast<uint4*>(q + (plane * rows_max + sl) * kQK + piece * 16) =
+        *reinterpret_cast<const uint4*>(tq + (plane * T + t) * kQK + piece * 16);
+    if (piece == 0) {
+      const int tn = slot_tile[sl];
+      uint8_t* atom = sf + (((size_t)(tn >> 8) * KC + kc) * 2) * kAtom;
+      *reinterpret_cast<uint32_t*>(atom + act_scale_byte(term, tn & 0xFF, stack)) =
+          *reinterpret_cast<const uint32_t*>(tsc + (((size_t)t * KC + kc) * 2 + term) * 4);
     }
   }
 }
@@ -399,7 +438,7 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
 //   16 (T <= 128): kind::mxf4, six e2m1 activation terms (N = 96), two CTAs
 //      per SM with four (gate/up) or three (down) stages; the kernel
 //      streams weights;
-//   80 (larger batches): kind::mxf8f6f4, two e4m3 terms (N = 160); gate/up
+//   88 (larger batches): kind::mxf8f6f4, two e4m3 terms (N = 176); gate/up
 //      runs one CTA per SM (its accumulators take 320 TMEM columns), down
 //      two CTAs per SM with two stages and one accumulator buffer each.
 template <int MODE, int NQ>
@@ -730,23 +769,29 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
           for (int j = 0; j < 32; ++j) v[j] += w2[j];
         }
       };
-      // Prefill tiles: the sums of a warpgroup's NQ / kWG consecutive tokens
-      // (term 0 in columns c, term 1 in NQ + c) go to registers, then the
-      // accumulator is released before any store.
-      constexpr int TPW = NQ / kWG;
-      static_assert(!C::kBig || (TPW % 8 == 0 && NQ % kWG == 0), "token split");
+      // Prefill tiles: the sums of a warpgroup's consecutive tokens (term 0
+      // in columns c, term 1 in NQ + c) go to registers, then the
+      // accumulator is released before any store.  Warpgroup wg takes
+      // tokens [wg * TPW, wg * TPW + n_wg): TPW = the tokens per warpgroup
+      // rounded up to a multiple of 8 (the TMEM loads' width), the last
+      // warpgroup the rest.
+      constexpr int TPW = ((NQ + kWG - 1) / kWG + 7) / 8 * 8;
+      const int n_wg = min(TPW, NQ - wg * TPW);
+      static_assert(!C::kBig || (NQ % 8 == 0 && (kWG - 1) * TPW < NQ), "token split");
       auto load_sum = [&](uint32_t col, float* v) {
         float t[8];
 #pragma unroll
         for (int c = 0; c < TPW; c += 32) {
-          if (c + 32 <= TPW)
+          if (c + 32 <= TPW && c + 32 <= n_wg)
             tmem_ld32(col + c, v + c);
           else
 #pragma unroll
-            for (int c8 = c; c8 < TPW; c8 += 8) tmem_ld8(col + c8, v + c8);
+            for (int c8 = c; c8 < TPW && c8 < c + 32; c8 += 8)
+              if (c8 < n_wg) tmem_ld8(col + c8, v + c8);
         }
 #pragma unroll
         for (int c8 = 0; c8 < TPW; c8 += 8) {
+          if (c8 >= n_wg) break;
           tmem_ld8(col + NQ + c8, t);
 #pragma unroll
           for (int i = 0; i < 8; ++i) v[c8 + i] += t[i];
@@ -783,10 +828,9 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
         const int grp = (m >> 5) & 3;
         uint8_t* atoms = p.hsf + (((size_t)ti * KCo + (m >> 7)) * 2) * kAtom + grp;
         if constexpr (C::kBig) {
-          // Each warpgroup takes NQ / kWG consecutive tokens: all their
+          // Each warpgroup takes its consecutive tokens: all their
           // gate and up sums go to registers and the accumulators back to
           // the MMA at once, so the epilogue math overlaps the next item.
-          constexpr int TPW = NQ / kWG;
           const int t_lo = wg * TPW;
           float gs[TPW], us[TPW];
           load_sum(dbase + t_lo, gs);
@@ -880,14 +924,35 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
           }
         }
       } else if constexpr (C::kBig) {
-        const int t_lo = wg * TPW;
-        float os[TPW];
-        load_sum(dbase + t_lo, os);
-        tc_fence_before();
-        mbar_arrive(dempty(buf));
+        // o of the tile's tokens in chunks of 32 (registers), the
+        // accumulator released after the last chunk's loads
+        static_assert(MODE == BS_GATEUP || C::kEpiWarps == 4, "one warpgroup: every token of the tile");
 #pragma unroll
-        for (int j = 0; j < TPW; ++j)
-          if (t_lo + j < tile.z) p.o[(size_t)(tile.y + t_lo + j) * p.ld_out + m] = os[j];
+        for (int c0 = 0; c0 < NQ; c0 += 32) {
+          constexpr int kW = 32;
+          float os[kW], t2[8];
+          if (c0 + kW <= NQ) {
+            tmem_ld32(dbase + c0, os);
+          } else {
+#pragma unroll
+            for (int c8 = 0; c8 < kW; c8 += 8)
+              if (c0 + c8 < NQ) tmem_ld8(dbase + c0 + c8, os + c8);
+          }
+#pragma unroll
+          for (int c8 = 0; c8 < kW; c8 += 8) {
+            if (c0 + c8 >= NQ) break;
+            tmem_ld8(dbase + NQ + c0 + c8, t2);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) os[c8 + i] += t2[i];
+          }
+          if (c0 + kW >= NQ) {
+            tc_fence_before();
+            mbar_arrive(dempty(buf));
+          }
+#pragma unroll
+          for (int j = 0; j < kW; ++j)
+            if (c0 + j < tile.z) p.o[(size_t)(tile.y + c0 + j) * p.ld_out + m] = os[j];
+        }
       } else {
 #pragma unroll 1
         for (int j0 = JW * wg; j0 < NQ; j0 += JW * kWG) {
@@ -964,6 +1029,7 @@ struct BsWs {
   uint8_t *hq, *hsf;  // h rows: the same over I
   int* slot_tile;     // [rows_max]: tile << 8 | row within the tile
   float* part;        // K-split partial sums (T = 1): kBsMaxSplit planes of K rows of I (gate), I (up), L (down)
+  uint8_t *tq, *tsc;  // prefill: per-token latent terms [L/128][2][max_tokens][128], scale words [max_tokens][L/128][2]
   size_t total;
 };
 BsWs bs_ws_view(void* base, const Dims& d, int max_tokens) {
@@ -973,17 +1039,24 @@ BsWs bs_ws_view(void* base, const Dims& d, int max_tokens) {
   // tiles hold at least one slot and at most one expert: <= E + R / 16 whatever the tile height
   const size_t MT = (size_t)d.E + R / 16 + 1;
   auto terms = [&](size_t C) { return std::max(2 * R * C, (size_t)kFp4Terms * Rf * C / 2); };
-  const size_t sizes[6] = {terms(d.L), MT * (d.L / kQK) * 2 * kAtom, terms(d.I), MT * (d.I / kQK) * 2 * kAtom,
-                           R * sizeof(int), (size_t)kBsMaxSplit * d.K * (2 * d.I + d.L) * sizeof(float)};
+  const size_t Tp = max_tokens > kBsDecodeMaxT ? (size_t)max_tokens : 0;  // prefill sizes only
+  const size_t sizes[8] = {terms(d.L),
+                           MT * (d.L / kQK) * 2 * kAtom,
+                           terms(d.I),
+                           MT * (d.I / kQK) * 2 * kAtom,
+                           R * sizeof(int),
+                           (size_t)kBsMaxSplit * d.K * (2 * d.I + d.L) * sizeof(float),
+                           Tp * d.L * 2,
+                           Tp * (d.L / kQK) * 2 * 4};
   uint8_t* b = static_cast<uint8_t*>(base);
-  uint8_t* ptr[6];
+  uint8_t* ptr[8];
   size_t off = 0;
-  for (int i = 0; i < 6; ++i) {
+  for (int i = 0; i < 8; ++i) {
     ptr[i] = b ? b + off : nullptr;
     off += up(sizes[i]);
   }
   return BsWs{(int)R,  (int)Rf, (int)MT, ptr[0], ptr[1], ptr[2], ptr[3], reinterpret_cast<int*>(ptr[4]),
-              reinterpret_cast<float*>(ptr[5]), off};
+              reinterpret_cast<float*>(ptr[5]), ptr[6], ptr[7], off};
 }
 
 template <int MODE, int NQ>
@@ -1057,9 +1130,21 @@ cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims
   const int ch = (fp4 && TK <= 8 * d.K) ? 1 : kQuantChunks;  // chunks per half warp
   const long long halves = (long long)TK * ((d.L / kQK + ch - 1) / ch);
   const int blocks = (int)std::min<long long>((halves * 16 + 255) / 256, 8LL * p.num_sms);
-  auto kernel = !fp4 ? quant_rows_kernel : ch == 1 ? quant_rows_fp4_kernel<1> : quant_rows_fp4_kernel<kQuantChunks>;
-  const int rows = tile_rows == kBsDecodeRows ? ws.rows_fp4 : ws.rows_max;
-  return launch_pdl(kernel, blocks, 256, 0, s, w.lat, w.perm, d.K, TK, n_local, d.L, rows, ws.slot_tile, stack,
+  if (!fp4) {
+    // prefill tiles: each token's row split once (token order), then the
+    // slots' copies -- the split is ALU work, the copy a memory stream
+    const long long th = (long long)T * ((d.L / kQK + kQuantChunks - 1) / kQuantChunks);
+    const int tb = (int)std::min<long long>((th * 16 + 255) / 256, 8LL * p.num_sms);
+    cudaError_t e = launch_pdl(quant_rows_kernel, tb, 256, 0, s, w.lat, (const int*)nullptr, 1, T,
+                               (const int*)nullptr, d.L, T, (const int*)nullptr, stack, ws.tq, ws.tsc);
+    if (e != cudaSuccess) return e;
+    const long long pieces = (long long)TK * (d.L / kQK) * 16;
+    const int gb = (int)std::min<long long>((pieces + 255) / 256, 16LL * p.num_sms);
+    return launch_pdl(gather_terms_kernel, gb, 256, 0, s, (const uint8_t*)ws.tq, (const uint8_t*)ws.tsc, w.perm,
+                      d.K, T, TK, n_local, d.L / kQK, ws.rows_max, (const int*)ws.slot_tile, stack, ws.lq, ws.lsf);
+  }
+  auto kernel = ch == 1 ? quant_rows_fp4_kernel<1> : quant_rows_fp4_kernel<kQuantChunks>;
+  return launch_pdl(kernel, blocks, 256, 0, s, w.lat, w.perm, d.K, TK, n_local, d.L, ws.rows_fp4, ws.slot_tile, stack,
                     ws.lq, ws.lsf);
 }
 

@@ -2,7 +2,7 @@
 // the e2m1 weights and their e8m0 scales go to the tensor cores as they are
 // stored.  Two tile kinds: decode tiles (16 token rows, up to T = 128) use
 // tcgen05.mma kind::mxf4 with the bf16 activations carried as six
-// block-scaled e2m1 terms; prefill tiles (80 token rows) use
+// block-scaled e2m1 terms; prefill tiles (88 token rows) use
 // kind::mxf8f6f4 with the activations written exactly as the sum of two
 // block-scaled e4m3 terms.
 #pragma once
@@ -48,11 +48,16 @@ struct BsPlan {
   int withhold_item = -1;  // test hook (see k3moe_test_withhold_copies)
 };
 // Tile heights (token rows per tile, the MMA's N bound): decode-size batches
-// use short tiles (every weight byte streamed once per forward; the two
-// activation terms of the 16 rows form one 32-row MMA operand), larger
-// batches taller ones (fewer weight re-reads per token).
+// use short tiles (every weight byte streamed once per forward; the six
+// activation terms of the 16 rows form one 96-row MMA operand), larger
+// batches taller ones (fewer weight re-reads and MMA instructions per
+// token).  A block-scaled MMA instruction costs about the same pipe time
+// for any N up to 192, so the prefill tile is as tall as the gate/up
+// kernel's four-stage ring allows: 88 rows (N = 176), which keeps an
+// expert of up to 176 slots -- nearly every expert of a uniform T = 8192
+// batch, ~146 +- 12 slots -- at two tiles.
 constexpr int kBsDecodeRows = 16;
-constexpr int kBsPrefillRows = 80;
+constexpr int kBsPrefillRows = 88;
 constexpr int kBsDecodeMaxT = 128;  // largest T run on decode tiles
 constexpr int kBsMaxSplit = 4;      // most K parts of a T = 1 work item
 inline int bs_tile_rows(int T) { return T <= kBsDecodeMaxT ? kBsDecodeRows : kBsPrefillRows; }

@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(const int32_t* __restr
   if (nsub > 0 && e_t < split_expert) atomicAdd(&n_first, nsub);
   if (nsub > 0) {
     const int per = (c_t + nsub - 1) / nsub;
-    const int tn = (per + 15) & ~15;
+    const int tn = min((per + 15) & ~15, bn_max);  // tiles never exceed bn_max rows
     for (int j = 0; j < nsub; ++j) {
       const int r0 = j * tn;
       const int rows = min(tn, c_t - r0);

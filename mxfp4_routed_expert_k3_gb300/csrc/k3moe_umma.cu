@@ -39,7 +39,7 @@ constexpr int kBK = 64;         // input columns per stage (one 128-byte swizzle
 constexpr int kBNMax = 192;     // token rows per tile (MMA N, multiple of 16)
 constexpr int kThreads = 192;
 
-enum Mode { DENSE = 0, GATEUP = 1, DOWN = 2, GATEUP2 = 3, DOWN2 = 4 };
+enum Mode { DENSE = 0, GATEUP = 1, DOWN = 2 };
 
 // Second-bank (2-bit affine) tile: 128 weight rows x 64 input columns of
 // one matrix -- row r's 64 codes (four per byte, low bits first) at
@@ -47,7 +47,7 @@ enum Mode { DENSE = 0, GATEUP = 1, DOWN = 2, GATEUP2 = 3, DOWN2 = 4 };
 // biases at 2304 + 2 r (one group of 64 per row per tile: the tile is one
 // quantisation group wide).
 constexpr int kTile2Bytes = 2560;
-constexpr int kTile2MaxRows = 80;  // token rows of the tiles the 2-bit modes take
+constexpr int kTile2MaxRows = 96;  // token rows of a second-bank tile's box at most
 
 // The tensor cores' fp32 accumulation drifts by about 2^-24 (relative) per
 // accumulation step, so a long K loop into one accumulator loses more than
@@ -55,37 +55,26 @@ constexpr int kTile2MaxRows = 80;  // token rows of the tiles the 2-bit modes ta
 // K/(16*kAcc) steps) and the epilogue adds them with round-to-nearest fp32.
 template <int MODE>
 struct Cfg {
-  static constexpr bool kTwoBit = MODE == GATEUP2 || MODE == DOWN2;  // second-bank weights
-  static constexpr bool kGU = MODE == GATEUP || MODE == GATEUP2;     // gate and up: two accumulators
-  static constexpr bool kDown = MODE == DOWN || MODE == DOWN2;
+  static constexpr bool kGU = MODE == GATEUP;  // gate and up: two accumulators
+  static constexpr bool kDown = MODE == DOWN;
   static constexpr int kNumMat = kGU ? 2 : 1;
-  // 2-bit affine weights decode exactly to fp32 and enter the MMA as two
-  // bf16 terms (hi + lo, 16 significant bits): two A tiles per matrix
-  static constexpr int kParts = kTwoBit ? 2 : 1;
-  static constexpr int kNumA = kNumMat * kParts;
+  static constexpr int kNumA = kNumMat;
   // Dense: 256 token rows per tile (an MMA instruction costs about the pipe
   // time of an N = 256 one whatever its N), K split over two accumulators.
-  // token rows per tile; the 2-bit modes run on the block-scaled path's
-  // tile lists (at most 80 rows), so their token box is 80 rows high
-  static constexpr int kBN = (MODE == DENSE) ? 256 : kTwoBit ? kTile2MaxRows : kBNMax;
+  static constexpr int kBN = (MODE == DENSE) ? 256 : kBNMax;
   static constexpr int kABytes = kBM * kBK * 2;                 // 16 KB per A tile
   static constexpr int kBBytes = kBN * kBK * 2;
-  static constexpr int kSrcTile = kTwoBit ? kTile2Bytes : kTileBytes;  // stored tile of one matrix
+  static constexpr int kSrcTile = kTileBytes;                   // stored tile of one matrix
   static constexpr int kStageBytesRaw = (MODE == DENSE) ? 0 : kNumMat * kSrcTile;
   static constexpr int kStaging = (kStageBytesRaw + 1023) / 1024 * 1024;
   static constexpr int kStageBytes = kNumA * kABytes + kBBytes + kStaging;
-  static constexpr int kStages = (MODE == GATEUP2) ? 2 : (MODE == DOWN2) ? 5 : kGU ? 3 : 4;
+  static constexpr int kStages = kGU ? 3 : 4;
   static constexpr int kAcc = (MODE == DENSE || kDown) ? 2 : 1;
-  // TMEM columns between accumulators.  The 2-bit modes (tiles of at most
-  // 128 token rows) give the hi and lo terms accumulators of their own
-  // (fewer fp32 accumulation steps each), added in the epilogue.
-  static constexpr int kAccStride = kTwoBit ? 128 : 256;
-  static constexpr int kAccPerMat = kAcc * kParts;  // accumulators summed per matrix
-  static constexpr int kMatStride = 256;            // TMEM columns between gate and up
+  static constexpr int kAccStride = 256;  // TMEM columns between accumulators
+  static constexpr int kMatStride = 256;  // TMEM columns between gate and up
   static constexpr int kTmemCols = 512;
   static constexpr int kSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
-  static_assert(kNumMat * kAccPerMat * kAccStride <= kTmemCols || (kGU && !kTwoBit), "TMEM budget");
-  static_assert(!kTwoBit || kAccPerMat * kAccStride <= kMatStride || !kGU, "gate and up accumulators overlap");
+  static_assert(kNumMat * kAcc * kAccStride <= kTmemCols || kGU, "TMEM budget");
 };
 
 // One output element of a dense projection (DenseOut, glu == 0).
@@ -123,7 +112,7 @@ struct TileList {
 
 struct Params {
   // operand sources
-  const uint8_t* a_tiles;  // MXFP4 tiles (GATEUP / DOWN) or 2-bit tiles (GATEUP2 / DOWN2)
+  const uint8_t* a_tiles;  // MXFP4 tiles (GATEUP / DOWN) or 2-bit tiles (second bank)
   int expert_base;         // weight index of a tile = its expert id - expert_base
   int MT;                  // weight row tiles per matrix
   int KS;                  // K / 64
@@ -238,9 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
 #pragma unroll
         for (int i = 0; i < C::kNumA; ++i) {
           const uint32_t a0 = smem_u32(stage_a(s, i));
-          const int part = i % C::kParts;  // hi and lo terms: accumulators of their own
-          const uint32_t acc_col =
-              (uint32_t)((i / C::kParts) * C::kMatStride + (acc_k * C::kParts + part) * C::kAccStride);
+          const uint32_t acc_col = (uint32_t)(i * C::kMatStride + acc_k * C::kAccStride);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             umma_bf16(tmem + acc_col, umma_desc_sw128(a0 + kk * 32), umma_desc_sw128(b0 + kk * 32), idesc,
@@ -260,44 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
   } else {
     // ================= decode (MXFP4) + epilogue warpgroup
     const int wg_t = threadIdx.x - 64;  // 0..127
-    if (C::kTwoBit) {
-      // w = scale * q + bias, exact in fp32 (an 8-bit scale times a 2-bit
-      // code plus an 8-bit bias), written as hi = bf16(w), lo = bf16(w - hi)
-      const int r = wg_t;
-      for (int ks = 0; ks < p.KS; ++ks) {
-        const int s = ks % C::kStages, par = (ks / C::kStages) & 1;
-        if (!mbar_wait(full_tma(s), par, g, 8u)) break;
-        const uint8_t* stg = stage_stg(s);
-#pragma unroll
-        for (int m = 0; m < C::kNumMat; ++m) {
-          const uint8_t* tile = stg + m * kTile2Bytes;
-          const uint4 q = *reinterpret_cast<const uint4*>(tile + (size_t)r * 16);
-          const float sc = bf16_to_f32(*reinterpret_cast<const uint16_t*>(tile + 2048 + 2 * r));
-          const float bi = bf16_to_f32(*reinterpret_cast<const uint16_t*>(tile + 2304 + 2 * r));
-          uint8_t* row_hi = stage_a(s, m * 2) + (size_t)r * 128;
-          uint8_t* row_lo = stage_a(s, m * 2 + 1) + (size_t)r * 128;
-          const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8) {  // columns 8 c8 .. 8 c8 + 7: 16 bits of word c8 / 2
-            const uint32_t bits = words[c8 >> 1] >> (16 * (c8 & 1));
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float w0 = fmaf(sc, (float)((bits >> (4 * k)) & 3u), bi);
-              const float w1 = fmaf(sc, (float)((bits >> (4 * k + 2)) & 3u), bi);
-              hi[k] = pack_bf16x2(w0, w1);
-              const float2 h2 = unpack_bf16x2(hi[k]);
-              lo[k] = pack_bf16x2(w0 - h2.x, w1 - h2.y);
-            }
-            const int sw = (c8 ^ (r & 7)) << 4;
-            *reinterpret_cast<uint4*>(row_hi + sw) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(row_lo + sw) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-          }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(full_a(s));
-      }
-    } else if (MODE != DENSE) {
+    if (MODE != DENSE) {
       const int r = wg_t;  // row of the 128-row tile this thread decodes
       for (int ks = 0; ks < p.KS; ++ks) {
         const int s = ks % C::kStages, par = (ks / C::kStages) & 1;
@@ -330,9 +280,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
       const int m_local = quarter * 32 + lane;
       const int m = mt * kBM + m_local;
       const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-      // accumulators that hold a part of the sum: every (K accumulator, term)
-      // pair that received at least one k step
-      const int n_acc = min(C::kAcc, p.KS) * C::kParts;
+      // accumulators that hold a part of the sum: every K accumulator that
+      // received at least one k step
+      const int n_acc = min(C::kAcc, p.KS);
       for (int j0 = 0; j0 < n_mma; j0 += 32) {
         float acc[32];
         tmem_ld32(lane_addr + j0, acc);
@@ -1160,7 +1110,7 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int* __restrict
     if (a < n_act && nsub > 0 && e < split_expert) atomicAdd(&n_first, nsub);
     if (a < n_act && nsub > 0) {
       const int per = (c + nsub - 1) / nsub;
-      const int tn = (per + 15) & ~15;
+      const int tn = min((per + 15) & ~15, bn_max);  // tiles never exceed bn_max rows
       for (int j = 0; j < nsub; ++j) {
         const int r0 = j * tn;
         const int rows = min(tn, c - r0);
@@ -1415,14 +1365,16 @@ cudaError_t umma_bank2_experts(const UmmaPlan& p, const uint8_t* gu2_tiles, cons
                                int n_bank2, int tile_rows, const Work& w, int T, const Dims& d, cudaStream_t s) {
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
-  if (tile_rows > kTile2MaxRows || tile_rows % 16) return cudaErrorInvalidValue;  // token box and TMEM layout
+  // token boxes as high as the largest MMA N of the tiles (their rows
+  // rounded up to 16): 16 at decode sizes, 96 for 88-row prefill tiles
+  const int box_rows = (tile_rows + 15) & ~15;
+  if (tile_rows <= 0 || box_rows > kTile2MaxRows) return cudaErrorInvalidValue;  // box room and TMEM layout
   UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
   gather_rows_kernel<<<152 * 8, 256, 0, s>>>(w.lat, w.perm, TK, d.K, d.L, ws.lat_perm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CUtensorMap mb1, mb2;
-  // token boxes as high as the tiles (16 rows at decode sizes, 80 at prefill)
-  if (!make_map(&mb1, ws.lat_perm, TK, d.L, tile_rows) || !make_map(&mb2, w.h, TK, d.I, tile_rows))
+  if (!make_map(&mb1, ws.lat_perm, TK, d.L, box_rows) || !make_map(&mb2, w.h, TK, d.I, box_rows))
     return cudaErrorInvalidValue;
   // at most one tile per second-bank expert with work plus one per 16 slots
   const int max_tiles = std::min(n_bank2, TK) + TK / kMinTileRows + 1;
@@ -1439,7 +1391,7 @@ cudaError_t umma_bank2_experts(const UmmaPlan& p, const uint8_t* gu2_tiles, cons
   g.beta_lin = d.beta_lin;
   g.status = p.status;
   g.limit_ns = p.limit_ns;
-  g.tn = tile_rows;
+  g.tn = box_rows;
   // persistent: one CTA per SM at most (the items are counted on the device)
   bank2_gemm_kernel<true><<<std::min(p.num_sms, g.MT * max_tiles), B2Cfg<true>::kThreads, B2Cfg<true>::kSmem, s>>>(
       mb1, g);
