@@ -368,7 +368,7 @@ def run_ours(args, rank, world, local_rank):
         extra["shared_block"] = run_shared_block(w, args, rank, dev, stream, l2_flush, peaks, routed_step_ms)
         clocks.mark("shared_block", t_leg, time.time())
         t_leg = time.time()
-        extra["two_bank"] = run_two_bank(w, args, rank, dev, stream, l2_flush, peaks, routed_step_ms)
+        extra["two_bank"] = run_two_bank(w, d, args, rank, dev, stream, l2_flush, peaks, routed_step_ms)
         clocks.mark("two_bank", t_leg, time.time())
         torch.cuda.empty_cache()
         t_leg = time.time()
@@ -379,6 +379,10 @@ def run_ours(args, rank, world, local_rank):
             t_leg = time.time()
             extra["stacked4"] = run_stacked4(args, rank, dev, l2_flush, peaks)
             clocks.mark("stacked4", t_leg, time.time())
+    elif args.two_bank:  # a reduced-expert profiling case of the two-bank leg
+        t_leg = time.time()
+        extra["two_bank"] = run_two_bank(w, d, args, rank, dev, stream, l2_flush, peaks, routed_step_ms)
+        clocks.mark("two_bank", t_leg, time.time())
     clk = clocks.stop()
 
     cpu = None
@@ -559,14 +563,14 @@ def run_shared_block(w, args, rank, dev, stream, l2_flush, peaks, routed_step_ms
             "decode": per_T, "prefill": pf}
 
 
-def run_two_bank(w, args, rank, dev, stream, l2_flush, peaks, routed_step_ms):
-    """Two-bank graded experts: experts 0..447 MXFP4 (as in the main run),
-    448..895 2-bit affine (2.5 bits per weight); the same decode step.  The
-    banks' split of the sorted selections is found on the device."""
+def run_two_bank(w, d1, args, rank, dev, stream, l2_flush, peaks, routed_step_ms):
+    """Two-bank graded experts: the first half of the experts MXFP4 (as in
+    the main run), the second half 2-bit affine (2.5 bits per weight); the
+    same decode step.  The banks' split of the sorted selections is found on
+    the device."""
     import torch
     from mxfp4_routed_expert_k3_gb300 import k3moe, synth
-    from mxfp4_routed_expert_k3_gb300.dims import K3
-    d = K3.with_(bank2_begin=K3.n_experts // 2)
+    d = d1.with_(bank2_begin=d1.n_experts // 2)
     w2 = dict(w)
     for n in ("w1_packed", "w1_scale", "w3_packed", "w3_scale", "w2_packed", "w2_scale"):
         w2[n] = np.ascontiguousarray(w[n][: d.bank2_begin])
@@ -589,8 +593,8 @@ def run_two_bank(w, args, rank, dev, stream, l2_flush, peaks, routed_step_ms):
     finally:
         layer.close()
     tok = sum(DECODE_BATCHES)
-    return {"workload": "K3 routed layer, experts 0..447 MXFP4 + 448..895 2-bit affine (second bank), decode "
-                        "batches T=1,8,64 per step",
+    return {"workload": f"K3 routed layer, experts 0..{d.bank2_begin - 1} MXFP4 + {d.bank2_begin}.."
+                        f"{d.n_experts - 1} 2-bit affine (second bank), decode batches T=1,8,64 per step",
             "tokens_per_s": tok / (step_ms / 1e3), "ms_per_step": step_ms,
             "vs_one_bank_time": step_ms / routed_step_ms,
             "hbm_GB_per_s": alg_bytes / (step_ms / 1e3) / 1e9, "decode": per_T}
@@ -785,6 +789,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the shared-expert block, skewed-routing and stacked-layer measurements")
     ap.add_argument("--no-stacked", action="store_true", help="skip the four-stacked-layer measurement")
+    ap.add_argument("--two-bank", action="store_true",
+                    help="with --experts below 896: run the two-bank leg at that expert count (profiling case)")
     ap.add_argument("--experts", type=int, default=896,
                     help="experts of the K3-dim layer (default 896; fewer only for small profiling captures)")
     args = ap.parse_args()

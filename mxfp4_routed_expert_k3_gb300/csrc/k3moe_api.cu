@@ -672,7 +672,10 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
                                                 c->sharded ? n_local : nullptr), split_gu > 1 ? 2 : 1,
               "gate/up");
     K3_LAUNCH(k3::bs_stream_down(c->bs, c->bw, tiles, count_a, w, T, d, bn, s, split_dn), 1, "down");
-    if (c->bank2_begin)
+    if (c->bank2_begin && bn == k3::kBsDecodeRows)
+      K3_LAUNCH(k3::bs_bank2_experts(c->bs, c->gu2_tiles, c->d2_tiles, c->bank2_begin, tiles, tile_count, w, T, d, s),
+                3, "second bank (2-bit)");
+    else if (c->bank2_begin)
       K3_LAUNCH(k3::umma_bank2_experts(c->umma, c->gu2_tiles, c->d2_tiles, c->bank2_begin, d.E - c->bank2_begin, bn,
                                        w, T, d, s),
                 3, "second bank (2-bit)");

@@ -431,35 +431,42 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
 }
 
 // Per stage four copies: the e2m1 tiles (GATEUP: gate and up of one
-// 128-column chunk; DOWN: kNK consecutive chunks), all activation terms of
+// 128-column chunk; DOWN: kNK consecutive chunks, or at prefill one chunk of
+// two row blocks -- two copies), all activation terms of
 // the stage's chunks (one 4-D box), the weight scale atoms and the
 // activation scale atoms (bulk copies).  Few large copies per stage keep the
 // HBM stream going.  NQ is the tile height:
 //   16 (T <= 128): kind::mxf4, six e2m1 activation terms (N = 96), two CTAs
 //      per SM with four (gate/up) or three (down) stages; the kernel
 //      streams weights;
-//   88 (larger batches): kind::mxf8f6f4, two e4m3 terms (N = 176); gate/up
-//      runs one CTA per SM (its accumulators take 320 TMEM columns), down
-//      two CTAs per SM with two stages and one accumulator buffer each.
+//   88 (larger batches): kind::mxf8f6f4, two e4m3 terms (N = 176); one
+//      CTA per SM with four stages and two accumulators (gate and up, or
+//      two row blocks of down: 352 TMEM columns).
 template <int MODE, int NQ>
 struct BsCfg {
   static constexpr bool kBig = NQ > 32;
   // All activation terms go into one MMA: B rows [term 0 of the NQ tokens;
   // term 1 of the same tokens; ...], N = terms * NQ, and the epilogue adds
   // accumulator columns t * NQ + j.  A block-scaled MMA instruction takes
-  // about the tensor-pipe time of an N = 256 one whatever its N, so one MMA
-  // per k step and matrix keeps the tensor pipe's share of a stage small.
-  // Prefill gate/up: its two stacked accumulators (2 x 160 columns) need
-  // more than a CTA's share of a two-CTA split, so one CTA per SM owns all
-  // 512 columns, with a deeper ring and two epilogue warpgroups.  The other
-  // kernels run two CTAs per SM (prefill down measured slower as one CTA
-  // per SM with two accumulator buffers).
-  static constexpr bool kWide = kBig && MODE == BS_GATEUP;
+  // about the same tensor-pipe time for any N up to 192 (measured: 152
+  // cycles for kind::mxf8f6f4, 168 for kind::mxf4, one after another on
+  // one accumulator), so one MMA per k step and matrix, N as large as the
+  // tile allows.
+  // Prefill: the two stacked accumulators (2 x 176 columns) need more than
+  // a CTA's share of a two-CTA split, so one CTA per SM owns all 512
+  // columns, with a deeper ring and two epilogue warpgroups.  Down takes
+  // two row blocks of the expert's down matrix per item, two accumulators
+  // sharing the stage's activation terms as gate and up do: eight MMAs per
+  // stage, where one row block gave four and the issuing thread's per-stage
+  // overhead left the pipe idle (one CTA per SM: 4.0 ms; two CTAs of one
+  // row block each: 3.1 ms, at T = 8192).  Decode kernels run two CTAs per SM.
+  static constexpr bool kWide = kBig;
+  static constexpr int kRB = (kBig && MODE == BS_DOWN) ? 2 : 1;  // row blocks per item
   // Decode tiles use tcgen05.mma kind::mxf4: the e2m1 weights sit in shared
   // memory as stored (64-byte rows, half the room of the 16-byte-slot
   // layout kind::mxf8f6f4 reads), so a CTA keeps four stages in flight; the
   // activations are kFp4Terms e2m1 terms (N = 6 * 16 = 96).  Prefill tiles
-  // keep kind::mxf8f6f4 with two e4m3 terms (N = 160: more terms would not
+  // keep kind::mxf8f6f4 with two e4m3 terms (N = 176: more terms would not
   // fit an MMA of N <= 256).
   static constexpr bool kFp4 = !kBig;
   static constexpr int kTerms = kFp4 ? kFp4Terms : 2;
@@ -467,9 +474,14 @@ struct BsCfg {
   static constexpr int kCtas = kWide ? 1 : 2;                               // CTAs per SM
   static constexpr int kEpiWarps = kWide ? 8 : 4;                           // epilogue warps
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
-  static constexpr int kNumA = (MODE == BS_GATEUP) ? 2 : 1;                 // accumulators (matrices)
+  static constexpr int kMats = (MODE == BS_GATEUP) ? 2 : 1;                 // matrices in the weight tensor
+  static constexpr int kNumA = kMats * kRB;                                 // accumulators
   static constexpr int kNK = (MODE == BS_GATEUP || kBig) ? 1 : 2;           // 128-column chunks per stage
-  static constexpr int kNA = (MODE == BS_GATEUP) ? 2 : kNK;                 // e2m1 tiles per stage
+  static constexpr int kNA = (MODE == BS_GATEUP || kRB == 2) ? 2 : kNK;     // e2m1 tiles per stage
+  // tiles per weight copy, adjacent in memory: gate and up, or decode
+  // down's kNK consecutive chunks; prefill down's two row blocks are KC
+  // tiles apart (two copies)
+  static constexpr int kABox = kRB == 2 ? 1 : kNA;
   // one e2m1 tile: dense, or in 16-byte slots (8 data + 8 padding bytes per 16 codes)
   static constexpr int kA = kQM * kRowB;
   static constexpr int kATx = kQM * kQK / 2;  // bytes a tile's copy brings (the packed codes)
@@ -591,7 +603,8 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
         const BsItem bi = bs_item(p, item);
         const int ti = bi.ti, mt = bi.mt;
         const int4 tile = p.tiles[ti];
-        const size_t tile0 = ((size_t)tile.x * p.MT + mt) * p.KC;  // (expert, row tile) chunk 0
+        // (expert, first row block of the item) chunk 0
+        const size_t tile0 = ((size_t)tile.x * p.MT * C::kRB + (size_t)mt * C::kRB) * p.KC;
         for (int ks = bi.k0; ks < bi.k1; ++ks, ++kg) {
           const int s = kg % C::kStages, u = kg / C::kStages;
           if (u > 0 && !mbar_wait(sfree(s), (u - 1) & 1, g, 1u)) {
@@ -600,8 +613,9 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
           }
           const int kc0 = ks * C::kNK;
           const int nk = min(C::kNK, p.KC - kc0);
-          // GATEUP: tiles / atoms (kc, gate), (kc, up); DOWN: (kc0) .. (kc0 + kNK - 1)
-          const int n_sfa = (MODE == BS_GATEUP) ? 2 : nk;
+          // GATEUP: tiles / atoms (kc, gate), (kc, up); DOWN: (kc0) .. (kc0 + kNK - 1),
+          // or at prefill (row block, kc) and (row block + 1, kc), KC tiles apart
+          const int n_sfa = (MODE == BS_GATEUP || C::kRB == 2) ? 2 : nk;
           const size_t first = (MODE == BS_GATEUP) ? (tile0 + kc0) * 2 : tile0 + kc0;
           if (item == p.withhold_item && ks == bi.k0) {
             // test hook: this stage's full barrier never completes, so the
@@ -614,9 +628,17 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
           // tensor are zero-filled and counted in full
           mbar_expect_tx(full(s), (uint32_t)(C::kNA * C::kATx + C::kTerms * C::kNK * C::kB + n_sfa * kAtom +
                                              2 * nk * kAtom));
-          tma_load_3d(st, &map_a, full(s), 0, 0, (int)first);
+          if (C::kRB == 2) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              tma_load_3d(st + j * C::kA, &map_a, full(s), 0, 0, (int)(first + (size_t)j * p.KC));
+              bulk_load(st + C::kOffSfa + j * kAtom, p.sfa + (first + (size_t)j * p.KC) * kAtom, kAtom, full(s));
+            }
+          } else {
+            tma_load_3d(st, &map_a, full(s), 0, 0, (int)first);
+            bulk_load(st + C::kOffSfa, p.sfa + first * kAtom, n_sfa * kAtom, full(s));
+          }
           tma_load_4d(st + C::kOffB, &map_b, full(s), 0, tile.y, 0, kc0);
-          bulk_load(st + C::kOffSfa, p.sfa + first * kAtom, n_sfa * kAtom, full(s));
           bulk_load(st + C::kOffSfb, p.sfb + ((size_t)ti * p.KC + kc0) * 2 * kAtom, 2 * nk * kAtom, full(s));
           ++issued;
         }
@@ -668,7 +690,7 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
           const uint32_t sfc = tmem + C::kSfBase + s * C::kSfCols;
 #pragma unroll
           for (int j = 0; j < C::kNA; ++j)
-            if (MODE == BS_GATEUP || j < nk) tc_cp_scales(sfc + 4 * j, sfa_base + so + (j * kAtom >> 4));
+            if (MODE == BS_GATEUP || C::kRB == 2 || j < nk) tc_cp_scales(sfc + 4 * j, sfa_base + so + (j * kAtom >> 4));
           // activation atoms in smem: [chunk][term][512] (stacked: term slot 0 holds both)
 #pragma unroll
           for (int c = 0; c < C::kNK; ++c)
@@ -687,7 +709,7 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
               for (int kb = 0; kb < kQK / 64; ++kb)
 #pragma unroll
                 for (int a = 0; a < C::kNumA; ++a) {
-                  const int ablk = (MODE == BS_GATEUP) ? a : c;
+                  const int ablk = C::kNumA == 2 ? a : c;
                   umma_fp4(d0 + a * C::kAccStride, a_d + ((ablk * C::kA + kb * 32) >> 4),
                            b_d + ((c * C::kTerms * C::kB + kb * 32) >> 4), fp4_idesc(2 * kb, 2 * kb, n),
                            sfc + 4 * ablk, sfc + 4 * C::kNA + 4 * c, (c | kb) ? 1u : first);
@@ -703,7 +725,7 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
               for (int a = 0; a < C::kNumA; ++a) {
                 // B blocks of the 4-D box are [chunk][term]: a chunk's terms
                 // are one terms*NQ-row operand
-                const int ablk = (MODE == BS_GATEUP) ? a : c;
+                const int ablk = C::kNumA == 2 ? a : c;
                 umma_bs(d0 + a * C::kAccStride, a_d + ((ablk * C::kA + kb * 32) >> 4),
                         b_d + ((c * C::kTerms * C::kB + kb * 32) >> 4), bs_idesc(kb, kb, n), sfc + 4 * ablk,
                         sfc + 4 * C::kNA + 4 * c * C::kSfbAtoms, (c | kb) ? 1u : first);
@@ -740,7 +762,7 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
       const BsItem bi = bs_item(p, item);
       const int ti = bi.ti, mt = bi.mt;
       const int4 tile = p.tiles[ti];
-      const int m = mt * kQM + r;
+      const int m = mt * C::kRB * kQM + r;  // output row (of the item's first row block)
       const uint32_t dbase = lane_base + buf * C::kBufStride;
       // Token columns per group: 32, or NQ for decode tiles, whose terms'
       // columns (term t of token j in column t*NQ + j) fit one or two
@@ -924,34 +946,22 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
           }
         }
       } else if constexpr (C::kBig) {
-        // o of the tile's tokens in chunks of 32 (registers), the
-        // accumulator released after the last chunk's loads
-        static_assert(MODE == BS_GATEUP || C::kEpiWarps == 4, "one warpgroup: every token of the tile");
+        // o of the warpgroup's tokens for both row blocks to registers, the
+        // accumulators released, then the stores
+        static_assert(MODE == BS_GATEUP || (C::kRB == 2 && C::kNumA == 2), "prefill down: two row blocks per item");
+        const int t_lo = wg * TPW;
+        float o0[TPW], o1[TPW];
+        load_sum(dbase + t_lo, o0);
+        load_sum(dbase + C::kAccStride + t_lo, o1);
+        tc_fence_before();
+        mbar_arrive(dempty(buf));
 #pragma unroll
-        for (int c0 = 0; c0 < NQ; c0 += 32) {
-          constexpr int kW = 32;
-          float os[kW], t2[8];
-          if (c0 + kW <= NQ) {
-            tmem_ld32(dbase + c0, os);
-          } else {
-#pragma unroll
-            for (int c8 = 0; c8 < kW; c8 += 8)
-              if (c0 + c8 < NQ) tmem_ld8(dbase + c0 + c8, os + c8);
+        for (int j = 0; j < TPW; ++j) {
+          if (t_lo + j < tile.z) {
+            float* orow = p.o + (size_t)(tile.y + t_lo + j) * p.ld_out;
+            orow[m] = o0[j];
+            orow[m + kQM] = o1[j];
           }
-#pragma unroll
-          for (int c8 = 0; c8 < kW; c8 += 8) {
-            if (c0 + c8 >= NQ) break;
-            tmem_ld8(dbase + NQ + c0 + c8, t2);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) os[c8 + i] += t2[i];
-          }
-          if (c0 + kW >= NQ) {
-            tc_fence_before();
-            mbar_arrive(dempty(buf));
-          }
-#pragma unroll
-          for (int j = 0; j < kW; ++j)
-            if (c0 + j < tile.z) p.o[(size_t)(tile.y + c0 + j) * p.ld_out + m] = os[j];
         }
       } else {
 #pragma unroll 1
@@ -973,6 +983,428 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
   __syncthreads();
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// ------------------------------------------------------------------ second bank at decode sizes
+// Experts of the second bank hold 2-bit affine weights: in every 64-column
+// group g of row r, w = s[r, g] q + b[r, g] with q in {0, 1, 2, 3} and bf16
+// s, b (kimi-k3-mlx README, "REAP expert pruning": graded mode).  So
+//   sum_k w[r, k] x[k] = sum_g ( s[r, g] D[r, g] + b[r, g] X[g] ),
+//   D[r, g] = sum_{k in g} q[r, k] x[k],  X[g] = sum_{k in g} x[k].
+// q is exact in e2m1 (0, 1, 2, 3 are e2m1 values 0b0000, 0b0010, 0b0100,
+// 0b0101), so D is one kind::mxf4 MMA per group (K = 64, the weight scale
+// bytes all 127 = 1.0) against the same six-term activation operand the
+// first bank's decode tiles use; the epilogue adds the terms' columns and
+// applies s and b per group in fp32.  Per 128-column stage: the token terms
+// (one 4-D box), the stage's 2-bit tiles (one bulk copy) and the tile's
+// activation scale atom; eight warps expand the codes to e2m1 nibbles in
+// shared memory (64-byte swizzle, the layout the MMA reads) and run the
+// per-group epilogue; one thread issues the MMAs.  Each group's accumulator
+// alternates between two TMEM buffers, so the epilogue of one group
+// overlaps the MMA of the next.
+constexpr int kB2Tile = 2560;  // one 2-bit tile: 128 rows x 64 codes (16 B a row), then 128 bf16 scales and biases
+template <bool GU>
+struct B2Cfg {
+  static constexpr int kNumMat = GU ? 2 : 1;
+  static constexpr int kN = kFp4Terms * kBsDecodeRows;               // MMA N: six terms x 16 rows
+  static constexpr int kB = kFp4Terms * kBsDecodeRows * 64;          // activation terms of one chunk
+  static constexpr int kSrc = kNumMat * 2 * kB2Tile;                 // the chunk's two groups of 2-bit tiles
+  static constexpr int kStage = (kB + kAtom + kSrc + 1023) / 1024 * 1024;
+  static constexpr int kRing = GU ? 6 : 7;
+  static constexpr int kDec = kNumMat * kQM * 64;                    // e2m1 tiles of one chunk
+  static constexpr int kCtas = GU ? 1 : 2;
+  static constexpr int kExFloats = GU ? kQM * kBsDecodeRows : 0;     // up sums handed to the gate warps
+  static constexpr int kXsFloats = kBsDecodeRows * 64;               // the item's per-group row sums (K/64 <= 64)
+  static constexpr int kSmem = kRing * kStage + 2 * kDec + kAtom + 4 * (kExFloats + kXsFloats) + 1024 + 512;
+  // TMEM: accumulators (matrix, buffer) at (m * 2 + buf) * kN, the weight
+  // scale atom, one activation atom per ring stage
+  static constexpr int kSfa = kNumMat * 2 * kN;
+  static constexpr int kTmemCols = GU ? 512 : 256;
+  static constexpr int kThreads = 320;
+  static_assert(kSfa + 4 + 4 * kRing <= kTmemCols, "TMEM budget");
+  static_assert(kCtas * (kSmem + 1024) <= 233472, "shared memory per SM");
+  static_assert(kN % 16 == 0 && kN <= 256, "MMA N");
+};
+
+struct B2Params {
+  const uint8_t* a_tiles;  // 2-bit tiles [expert][MT][K/64][mats][2560]
+  int expert_base;         // weight index of a tile = its expert id - expert_base
+  int MT, KC;              // row blocks of 128, chunks of 128 columns
+  const int4* tiles;       // tile list; the second bank takes [*begin, *count)
+  const int* count;
+  const int* begin;
+  const uint8_t* sfb;      // activation scale atoms [tile][KC][2][512]
+  // per-group sums of the activation rows: GU: xsum [T][K/64] by token
+  // (slot -> token through perm / K); DOWN: hsum [slots][K/32] by slot, the
+  // two 32-row halves of a group added in order
+  const float* xsum;
+  const int* perm;
+  int K;                   // top-k (slot -> token)
+  const float* hsum_in;
+  // outputs: GU: h (bf16), its e2m1 terms hq [I/128][6][rows][64] and atoms
+  // hsf (the down GEMM's operand), hsum [slots][I/32]; DOWN: o (fp32)
+  uint16_t* h;
+  uint8_t* hq;
+  uint8_t* hsf;
+  float* hsum;
+  float* o;
+  int ld_out, rows_max;
+  float beta, beta_lin;
+  unsigned* status;
+  uint64_t limit_ns;
+};
+
+// Four 2-bit codes per byte (low bits first) of a 32-bit word -> eight e2m1
+// nibbles (low nibble first) per output word, q -> 2q - [q == 3].
+__device__ __forceinline__ uint2 codes_to_e2m1(uint32_t w) {
+  uint32_t r[2];
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    uint32_t t = (w >> (16 * hf)) & 0xFFFFu;
+    t = (t | (t << 8)) & 0x00FF00FFu;
+    t = (t | (t << 4)) & 0x0F0F0F0Fu;
+    t = (t | (t << 2)) & 0x33333333u;  // nibble k holds code k
+    r[hf] = (t << 1) - (t & (t >> 1) & 0x11111111u);
+  }
+  return make_uint2(r[0], r[1]);
+}
+
+template <bool GU>
+__global__ void __launch_bounds__(B2Cfg<GU>::kThreads, B2Cfg<GU>::kCtas)
+    bank2_mxf4_kernel(const __grid_constant__ CUtensorMap map_b, const B2Params p) {
+  using C = B2Cfg<GU>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;                                  // [kRing][B terms | B atom | 2-bit tiles]
+  uint8_t* dec = smem + C::kRing * C::kStage;            // [2][mats][128 rows][64 B] e2m1, 64-byte swizzle
+  uint8_t* sfa_atom = dec + 2 * C::kDec;                 // 512 bytes of 127
+  float* ex = reinterpret_cast<float*>(sfa_atom + kAtom);  // GU: [128 rows][16 tokens] up sums
+  float* xs = ex + C::kExFloats;                           // [16 token rows][64 groups] row sums
+  uint64_t* bars = reinterpret_cast<uint64_t*>(xs + C::kXsFloats);
+  // bars: full[R], empty[R], dfull[2], dempty[2], afull[2], aempty[2], drain, ex_full, ex_empty,
+  // xs_full, xs_empty
+  constexpr int NB = 2 * C::kRing + 13;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NB);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  pdl_trigger();
+  pdl_wait();
+  const int first = *p.begin;
+  const int n_items = (*p.count - first) * p.MT;
+  if ((int)blockIdx.x >= n_items) return;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NB; ++i) {
+      const int k = i - 2 * C::kRing;
+      // dfull, aempty, xs_full and xs_empty: one arrival per expand /
+      // epilogue thread; ex_full and ex_empty: one per thread of a matrix half
+      mbar_init(smem_u32(bars + i),
+                (k == 0 || k == 1 || k == 6 || k == 7 || k == 11 || k == 12) ? 256u : (k == 9 || k == 10) ? 128u : 1u);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  for (int i = threadIdx.x; i < kAtom / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(sfa_atom)[i] = 0x7F7F7F7Fu;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Guard g{abort_flag, p.status, p.limit_ns};
+  auto full = [&](int r) { return smem_u32(bars + r); };
+  auto empty = [&](int r) { return smem_u32(bars + C::kRing + r); };
+  auto dfull = [&](int d) { return smem_u32(bars + 2 * C::kRing + d); };
+  auto dempty = [&](int d) { return smem_u32(bars + 2 * C::kRing + 2 + d); };
+  auto afull = [&](int b) { return smem_u32(bars + 2 * C::kRing + 4 + b); };
+  auto aempty = [&](int b) { return smem_u32(bars + 2 * C::kRing + 6 + b); };
+  const uint32_t drain = smem_u32(bars + 2 * C::kRing + 8);
+  const uint32_t ex_full = smem_u32(bars + 2 * C::kRing + 9), ex_empty = smem_u32(bars + 2 * C::kRing + 10);
+  const uint32_t xs_full = smem_u32(bars + 2 * C::kRing + 11), xs_empty = smem_u32(bars + 2 * C::kRing + 12);
+  auto stage = [&](int r) { return ring + (size_t)r * C::kStage; };
+  const int G = p.KC * 2;  // groups along K
+
+  if (warp == 0) {
+    // ================= copies
+    if (lane == 0) {
+      int kg = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const int ti = first + item / p.MT, mt = item % p.MT;
+        const int4 tile = p.tiles[ti];
+        const uint8_t* a_src =
+            p.a_tiles + ((size_t)(tile.x - p.expert_base) * p.MT + mt) * (size_t)G * C::kNumMat * kB2Tile;
+        for (int kc = 0; kc < p.KC; ++kc, ++kg) {
+          const int r = kg % C::kRing, u = kg / C::kRing;
+          if (u > 0 && !mbar_wait(empty(r), (u - 1) & 1, g, 1u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t st = smem_u32(stage(r));
+          mbar_expect_tx(full(r), (uint32_t)(C::kB + kAtom + C::kSrc));
+          tma_load_4d(st, &map_b, full(r), 0, tile.y, 0, kc);
+          bulk_load(st + C::kB, p.sfb + ((size_t)ti * p.KC + kc) * 2 * kAtom, kAtom, full(r));
+          bulk_load(st + C::kB + kAtom, a_src + (size_t)kc * C::kSrc, C::kSrc, full(r));
+        }
+      }
+      if (*abort_flag) {  // copies in flight land before the CTA exits
+        for (int k = max(0, kg - C::kRing); k < kg; ++k) {
+          const uint64_t t0 = global_ns();
+          while (!mbar_try_wait(full(k % C::kRing), (k / C::kRing) & 1))
+            if (global_ns() - t0 > p.limit_ns) break;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================= MMA issue: per chunk, per group j (the 32-byte half
+    // j of every 64-byte operand row), one MMA per matrix into buffer j
+    if (lane == 0) {
+      const uint32_t sfa_col = tmem + C::kSfa;
+      tc_cp_scales(sfa_col, sf_desc(smem_u32(sfa_atom)));
+      const uint64_t a_base = umma_desc_sw64(smem_u32(dec));
+      const uint64_t b_base = umma_desc_sw64(smem_u32(ring));
+      int kg = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        for (int kc = 0; kc < p.KC; ++kc, ++kg) {
+          const int r = kg % C::kRing, d = kg & 1;
+          if (!mbar_wait(full(r), (kg / C::kRing) & 1, g, 2u) || !mbar_wait(dfull(d), (kg >> 1) & 1, g, 4u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfb_col = tmem + C::kSfa + 4 + 4 * r;
+          tc_cp_scales(sfb_col, sf_desc(smem_u32(stage(r) + C::kB)));
+          const uint64_t so = (uint64_t)((uint32_t)(r * C::kStage) >> 4);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            if (kg > 0 && !mbar_wait(aempty(j), (kg - 1) & 1, g, 8u)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int m = 0; m < C::kNumMat; ++m)
+              umma_fp4(tmem + (uint32_t)((m * 2 + j) * C::kN),
+                       a_base + (uint64_t)((uint32_t)(d * C::kDec + m * kQM * 64 + j * 32) >> 4), b_base + so + (j * 32 >> 4),
+                       fp4_idesc(2 * j, 2 * j, C::kN), sfa_col, sfb_col, 0u);
+            umma_commit(afull(j));
+          }
+          if (!ok) break;
+          umma_commit(empty(r));
+          umma_commit(dempty(d));
+        }
+      }
+      if (!ok) {  // MMAs already issued finish before TMEM is released
+        umma_commit(drain);
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(drain, 0))
+          if (global_ns() - t0 > p.limit_ns) break;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ================= expand + epilogue (warps 2..9)
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // weight row of the block (TMEM lane)
+    const int half = (warp - 2) >> 2;   // GU: the matrix (0 gate, 1 up); DOWN: token half
+    const int mat = GU ? half : 0;
+    constexpr int kTok = GU ? kBsDecodeRows : kBsDecodeRows / 2;  // tokens this thread accumulates
+    const int n0 = GU ? 0 : half * kTok;
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    int kg = 0, it = 0;
+    bool ok = true;
+    float s_cur[2] = {0.f, 0.f}, b_cur[2] = {0.f, 0.f};
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
+      const int ti = first + item / p.MT, mt = item % p.MT;
+      const int4 tile = p.tiles[ti];
+      // the item's per-group sums of its token rows (latent rows by token,
+      // h rows by slot; rows past the tile 0) into shared memory, once
+      if (it > 0 && !__all_sync(0xFFFFFFFFu, mbar_wait(xs_empty, (it - 1) & 1, g, 256u))) break;
+      for (int i = threadIdx.x - 64; i < kBsDecodeRows * G; i += 256) {
+        const int n = i / G, gg = i - n * G;
+        float v = 0.f;
+        if (n < tile.z) {
+          const int sl = tile.y + n;
+          v = GU ? p.xsum[(size_t)(p.perm[sl] / p.K) * G + gg]
+                 : p.hsum_in[(size_t)sl * (2 * G) + 2 * gg] + p.hsum_in[(size_t)sl * (2 * G) + 2 * gg + 1];
+        }
+        xs[n * 64 + gg] = v;
+      }
+      mbar_arrive(xs_full);
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(xs_full, it & 1, g, 512u))) break;
+      float acc[kTok];
+#pragma unroll
+      for (int n = 0; n < kTok; ++n) acc[n] = 0.f;
+      // the epilogue of chunk kc - 1's two groups follows the expansion of chunk kc
+      auto epilogue = [&](int kgp, int kc) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int gg = 2 * kc + j;
+          ok = ok && mbar_wait(afull(j), kgp & 1, g, 16u);
+          if (!__all_sync(0xFFFFFFFFu, ok)) {  // warp-uniform before the TMEM loads
+            ok = false;
+            return;
+          }
+          tc_fence_after();
+          const uint32_t col = lane_base + (uint32_t)((mat * 2 + j) * C::kN);
+          // the six terms' columns of this thread's tokens: all loads issued,
+          // then one wait
+          float v[6 * kTok];
+          if constexpr (GU)
+            tmem_ld3x32(col, v);
+          else
+            tmem_ld6x8_stride16(col + n0, v);
+          tc_fence_before();
+          mbar_arrive(aempty(j));
+#pragma unroll
+          for (int n = 0; n < kTok; ++n) {
+            float dsum;
+            if (GU)  // column 16 t + n for term t
+              dsum = ((v[n] + v[n + 16]) + (v[n + 32] + v[n + 48])) + (v[n + 64] + v[n + 80]);
+            else
+              dsum = ((v[n] + v[n + 8]) + (v[n + 16] + v[n + 24])) + (v[n + 32] + v[n + 40]);
+            acc[n] = fmaf(s_cur[j], dsum, acc[n]);
+            acc[n] = fmaf(b_cur[j], xs[(n0 + n) * 64 + gg], acc[n]);
+          }
+        }
+      };
+      float s_next[2], b_next[2];
+      for (int kc = 0; kc < p.KC && ok; ++kc, ++kg) {
+        const int rr = kg % C::kRing, d = kg & 1;
+        bool w_ok = mbar_wait(full(rr), (kg / C::kRing) & 1, g, 32u);
+        if (w_ok && kg >= 2) w_ok = mbar_wait(dempty(d), ((kg >> 1) - 1) & 1, g, 64u);
+        if (!__all_sync(0xFFFFFFFFu, w_ok)) {  // warp-uniform exits
+          ok = false;
+          break;
+        }
+        // expand: GU thread (matrix half, row r) both groups; DOWN thread
+        // (row r) group `half`
+        const uint8_t* src = stage(rr) + C::kB + kAtom;
+        uint8_t* drow = dec + (size_t)d * C::kDec + (size_t)(mat * kQM + r) * 64;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          if (!GU && j != half) continue;
+          const uint4 q = *reinterpret_cast<const uint4*>(src + (size_t)(j * C::kNumMat + mat) * kB2Tile + r * 16);
+          const uint2 e0 = codes_to_e2m1(q.x), e1 = codes_to_e2m1(q.y), e2 = codes_to_e2m1(q.z),
+                      e3 = codes_to_e2m1(q.w);
+          // row bytes [32 j, 32 j + 32): 16-byte chunks 2j, 2j + 1, swizzled
+          const int sw = (r >> 1) & 3;
+          *reinterpret_cast<uint4*>(drow + (((2 * j) ^ sw) << 4)) = make_uint4(e0.x, e0.y, e1.x, e1.y);
+          *reinterpret_cast<uint4*>(drow + (((2 * j + 1) ^ sw) << 4)) = make_uint4(e2.x, e2.y, e3.x, e3.y);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const uint8_t* tl = src + (size_t)(j * C::kNumMat + mat) * kB2Tile;
+          s_next[j] = bf16_to_f32(*reinterpret_cast<const uint16_t*>(tl + 2048 + 2 * r));
+          b_next[j] = bf16_to_f32(*reinterpret_cast<const uint16_t*>(tl + 2304 + 2 * r));
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(dfull(d));
+        if (kc > 0) epilogue(kg - 1, kc - 1);
+        s_cur[0] = s_next[0];
+        s_cur[1] = s_next[1];
+        b_cur[0] = b_next[0];
+        b_cur[1] = b_next[1];
+      }
+      if (ok) epilogue(kg - 1, p.KC - 1);
+      mbar_arrive(xs_empty);  // the item's row sums are no longer read
+      if (!ok || *abort_flag) break;
+      // ---- outputs of the item
+      const int m = mt * kQM + r;
+      if (GU) {
+        // up sums to the gate warps through shared memory (two barriers:
+        // written / read, one phase per item)
+        if (half == 1) {
+          if (it > 0 && !__all_sync(0xFFFFFFFFu, mbar_wait(ex_empty, (it - 1) & 1, g, 128u))) break;
+#pragma unroll
+          for (int n = 0; n < kTok; ++n) ex[r * kTok + n] = acc[n];
+          mbar_arrive(ex_full);
+        } else {
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(ex_full, it & 1, g, 128u))) break;
+          // h = SiTU-GLU(gate, up) as bf16, its six e2m1 terms over the
+          // warp's 32 rows (one scale group of the down GEMM's K) and the
+          // per-32-row sums of h
+          float up[kTok];
+#pragma unroll
+          for (int n = 0; n < kTok; ++n) up[n] = ex[r * kTok + n];
+          mbar_arrive(ex_empty);
+          const int KCo = p.ld_out / kQK;
+          uint8_t* atoms = p.hsf + (((size_t)ti * KCo + (m >> 7)) * 2) * kAtom + ((m >> 5) & 3);
+          unsigned long long my_sc = 0;
+#pragma unroll
+          for (int n = 0; n < kTok; ++n) {
+            if (n >= tile.z) break;  // warp-uniform
+            const size_t row = (size_t)(tile.y + n);
+            const uint16_t hb = f32_to_bf16(situ_fast(acc[n], up[n], p.beta, p.beta_lin));
+            p.h[row * p.ld_out + m] = hb;
+            float rr = bf16_to_f32(hb);
+            float hsum = rr;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) hsum += __shfl_xor_sync(0xFFFFFFFFu, hsum, o);
+            if (lane == 0) p.hsum[row * (p.ld_out / 32) + (m >> 5)] = hsum;
+            uint32_t qn = 0;
+            unsigned long long sc = 0;
+#pragma unroll
+            for (int t = 0; t < kFp4Terms; ++t) {
+              const uint32_t sb = e2m1_scale_byte(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(rr))));
+              uint32_t qb = 0;
+              if (sb != 255u) {
+                qb = to_e2m1x2(0.f, rr * exp2_any(127 - (int)sb)) & 0xFu;
+                rr = fmaf(-from_e2m1x2(qb).x, exp2_any((int)sb - 127), rr);
+              } else {
+                rr = 0.f;
+              }
+              qn |= qb << (4 * t);
+              sc |= (unsigned long long)sb << (8 * t);
+            }
+            const uint32_t qo = __shfl_down_sync(0xFFFFFFFFu, qn, 1);
+            if (!(lane & 1)) {
+#pragma unroll
+              for (int t = 0; t < kFp4Terms; ++t)
+                p.hq[(((size_t)(m >> 7) * kFp4Terms + t) * p.rows_max + row) * 64 + ((m & 127) >> 1)] =
+                    (uint8_t)(((qn >> (4 * t)) & 0xFu) | (((qo >> (4 * t)) & 0xFu) << 4));
+            }
+            if (lane == n) my_sc = sc;
+          }
+          if (lane < tile.z && lane < kTok) {
+#pragma unroll
+            for (int t = 0; t < kFp4Terms; ++t)
+              atoms[act_scale_byte(t, lane, kBsDecodeRows)] = (uint8_t)(my_sc >> (8 * t));
+          }
+        }
+      } else {
+#pragma unroll
+        for (int n = 0; n < kTok; ++n)
+          if (n0 + n < tile.z) p.o[(size_t)(tile.y + n0 + n) * p.ld_out + m] = acc[n];
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// Per-64-column sums of bf16 rows (fp32, a fixed tree over the warp): one
+// warp per (row, group).
+__global__ void group_sums_kernel(const uint16_t* __restrict__ x, int rows, int cols, float* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
+  const int G = cols / 64;
+  const long long n = (long long)rows * G;
+  const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  for (long long wi = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; wi < n; wi += nw) {
+    const int rw = (int)(wi / G), gg = (int)(wi - (long long)rw * G);
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(x + (size_t)rw * cols + gg * 64 + 2 * lane);
+    float s = __uint_as_float(v << 16) + __uint_as_float(v & 0xFFFF0000u);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    if (lane == 0) out[wi] = s;
+  }
 }
 
 // ------------------------------------------------------------------ host helpers
@@ -1030,6 +1462,7 @@ struct BsWs {
   int* slot_tile;     // [rows_max]: tile << 8 | row within the tile
   float* part;        // K-split partial sums (T = 1): kBsMaxSplit planes of K rows of I (gate), I (up), L (down)
   uint8_t *tq, *tsc;  // prefill: per-token latent terms [L/128][2][max_tokens][128], scale words [max_tokens][L/128][2]
+  float *xsum, *hsum; // second bank at decode sizes: per-64-column latent sums by token, per-32-row h sums by slot
   size_t total;
 };
 BsWs bs_ws_view(void* base, const Dims& d, int max_tokens) {
@@ -1040,23 +1473,26 @@ BsWs bs_ws_view(void* base, const Dims& d, int max_tokens) {
   const size_t MT = (size_t)d.E + R / 16 + 1;
   auto terms = [&](size_t C) { return std::max(2 * R * C, (size_t)kFp4Terms * Rf * C / 2); };
   const size_t Tp = max_tokens > kBsDecodeMaxT ? (size_t)max_tokens : 0;  // prefill sizes only
-  const size_t sizes[8] = {terms(d.L),
+  const size_t sizes[10] = {terms(d.L),
                            MT * (d.L / kQK) * 2 * kAtom,
                            terms(d.I),
                            MT * (d.I / kQK) * 2 * kAtom,
                            R * sizeof(int),
                            (size_t)kBsMaxSplit * d.K * (2 * d.I + d.L) * sizeof(float),
                            Tp * d.L * 2,
-                           Tp * (d.L / kQK) * 2 * 4};
+                           Tp * (d.L / kQK) * 2 * 4,
+                           (size_t)std::min(max_tokens, kBsDecodeMaxT) * (d.L / 64) * sizeof(float),
+                           Rf * (d.I / 32) * sizeof(float)};
   uint8_t* b = static_cast<uint8_t*>(base);
-  uint8_t* ptr[8];
+  uint8_t* ptr[10];
   size_t off = 0;
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < 10; ++i) {
     ptr[i] = b ? b + off : nullptr;
     off += up(sizes[i]);
   }
   return BsWs{(int)R,  (int)Rf, (int)MT, ptr[0], ptr[1], ptr[2], ptr[3], reinterpret_cast<int*>(ptr[4]),
-              reinterpret_cast<float*>(ptr[5]), ptr[6], ptr[7], off};
+              reinterpret_cast<float*>(ptr[5]), ptr[6], ptr[7], reinterpret_cast<float*>(ptr[8]),
+              reinterpret_cast<float*>(ptr[9]), off};
 }
 
 template <int MODE, int NQ>
@@ -1066,13 +1502,14 @@ cudaError_t launch_bs(const BsPlan& p, const uint8_t* wq, const uint8_t* sfa, in
   using C = BsCfg<MODE, NQ>;
   CUtensorMap ma, mb;
   const int KC = cols / kQK, MT = rows / kQM;
-  const long long nbox = (long long)n_exp * MT * KC * C::kNumA;
-  const bool mapped = C::kFp4 ? map_e2m1_dense(&ma, wq, nbox, C::kNA) && map_terms_fp4(&mb, q, KC, rows_max, NQ, C::kNK)
-                              : map_e2m1(&ma, wq, nbox, C::kNA) && map_terms(&mb, q, KC, rows_max, NQ, C::kNK);
+  if (MT % C::kRB) return cudaErrorInvalidValue;
+  const long long nbox = (long long)n_exp * MT * KC * C::kMats;
+  const bool mapped = C::kFp4 ? map_e2m1_dense(&ma, wq, nbox, C::kABox) && map_terms_fp4(&mb, q, KC, rows_max, NQ, C::kNK)
+                              : map_e2m1(&ma, wq, nbox, C::kABox) && map_terms(&mb, q, KC, rows_max, NQ, C::kNK);
   if (!mapped) return cudaErrorInvalidValue;
   prm.sfa = sfa;
   prm.sfb = sfb;
-  prm.MT = MT;
+  prm.MT = MT / C::kRB;  // work items per tile
   prm.KC = KC;
   prm.KS = (KC + C::kNK - 1) / C::kNK;
   prm.tiles = tiles;
@@ -1116,6 +1553,8 @@ cudaError_t prepare_bs_kernels() {
   set((const void*)bs_stream_kernel<BS_DOWN, kBsDecodeRows>, BsCfg<BS_DOWN, kBsDecodeRows>::kSmem);
   set((const void*)bs_stream_kernel<BS_GATEUP, kBsPrefillRows>, BsCfg<BS_GATEUP, kBsPrefillRows>::kSmem);
   set((const void*)bs_stream_kernel<BS_DOWN, kBsPrefillRows>, BsCfg<BS_DOWN, kBsPrefillRows>::kSmem);
+  set((const void*)bank2_mxf4_kernel<true>, B2Cfg<true>::kSmem);
+  set((const void*)bank2_mxf4_kernel<false>, B2Cfg<false>::kSmem);
   return e;
 }
 
@@ -1295,6 +1734,66 @@ cudaError_t bs_stream_down(const BsPlan& p, const BsWeights& bw, const int4* til
     return launch_bs<BS_DOWN, kBsPrefillRows>(p, bw.d_q, bw.d_sf, bw.n_exp, d.L, d.I, ws.hq, ws.hsf, ws.rows_max, tiles,
                                               tile_count, prm, s);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t bs_bank2_experts(const BsPlan& p, const uint8_t* gu2_tiles, const uint8_t* d2_tiles, int bank2_begin,
+                             const int4* tiles, const int* tile_count, const Work& w, int T, const Dims& d,
+                             cudaStream_t s) {
+  const int TK = T * d.K;
+  if (TK <= 0) return cudaSuccess;
+  // (the kernel stages the per-group row sums of a tile: at most 64 groups of 64 along K)
+  if (T > p.max_tokens || T > kBsDecodeMaxT || d.L % kQK || d.I % kQK || d.L > 4096 || d.I > 4096)
+    return cudaErrorInvalidValue;
+  const BsWs ws = bs_ws_view(p.ws, d, p.max_tokens);
+  const int G = d.L / 64;
+  const long long warps = (long long)T * G;
+  cudaError_t e = launch_pdl(group_sums_kernel, (int)std::min<long long>((warps + 7) / 8, 8LL * p.num_sms), 256, 0,
+                             s, (const uint16_t*)w.lat, T, d.L, ws.xsum);
+  if (e != cudaSuccess) return e;
+  CUtensorMap m1, m2;
+  if (!map_terms_fp4(&m1, ws.lq, d.L / kQK, ws.rows_fp4, kBsDecodeRows, 1) ||
+      !map_terms_fp4(&m2, ws.hq, d.I / kQK, ws.rows_fp4, kBsDecodeRows, 1))
+    return cudaErrorInvalidValue;
+  B2Params q{};
+  q.a_tiles = gu2_tiles;
+  q.expert_base = bank2_begin;
+  q.MT = d.I / kQM;
+  q.KC = d.L / kQK;
+  q.tiles = tiles;
+  q.count = tile_count;
+  q.begin = tile_count + 1;
+  q.sfb = ws.lsf;
+  q.xsum = ws.xsum;
+  q.perm = w.perm;
+  q.K = d.K;
+  q.h = w.h;
+  q.hq = ws.hq;
+  q.hsf = ws.hsf;
+  q.hsum = ws.hsum;
+  q.ld_out = d.I;
+  q.rows_max = ws.rows_fp4;
+  q.beta = d.beta;
+  q.beta_lin = d.beta_lin;
+  q.status = p.status;
+  q.limit_ns = p.limit_ns;
+  e = launch_pdl(bank2_mxf4_kernel<true>, B2Cfg<true>::kCtas * p.num_sms, B2Cfg<true>::kThreads,
+                 B2Cfg<true>::kSmem, s, m1, q);
+  if (e != cudaSuccess) return e;
+  B2Params q2 = q;
+  q2.a_tiles = d2_tiles;
+  q2.MT = d.L / kQM;
+  q2.KC = d.I / kQK;
+  q2.sfb = ws.hsf;
+  q2.xsum = nullptr;
+  q2.hsum_in = ws.hsum;
+  q2.h = nullptr;
+  q2.hq = nullptr;
+  q2.hsf = nullptr;
+  q2.hsum = nullptr;
+  q2.o = w.o;
+  q2.ld_out = d.L;
+  return launch_pdl(bank2_mxf4_kernel<false>, B2Cfg<false>::kCtas * p.num_sms, B2Cfg<false>::kThreads,
+                    B2Cfg<false>::kSmem, s, m2, q2);
 }
 
 }  // namespace k3

@@ -92,5 +92,13 @@ cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* t
 // down: o (fp32, slot order)
 cudaError_t bs_stream_down(const BsPlan& p, const BsWeights& bw, const int4* tiles, const int* tile_count,
                            const Work& w, int T, const Dims& d, int tile_rows, cudaStream_t s, int n_split = 1);
+// The second bank's experts at decode sizes (T <= kBsDecodeMaxT): tiles
+// [tile_count[1], tile_count[0]) of the list (experts >= bank2_begin, 2-bit
+// tiles at index expert - bank2_begin), on kind::mxf4 against the same
+// e2m1 activation terms as the first bank: gate/up -> h (and its terms),
+// down -> o.
+cudaError_t bs_bank2_experts(const BsPlan& p, const uint8_t* gu2_tiles, const uint8_t* d2_tiles, int bank2_begin,
+                             const int4* tiles, const int* tile_count, const Work& w, int T, const Dims& d,
+                             cudaStream_t s);
 
 }  // namespace k3
