@@ -657,9 +657,9 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
     k3::umma_tile_list(c->umma, &tiles, &tile_count, &bn);
     bn = k3::bs_tile_rows(T);
     if (!fused_route)
-      K3_LAUNCH(k3::umma_stream_tiles(c->umma, w, T, d, bn, k3::bs_slot_tile(c->bs), split_expert, s), 1,
+      K3_LAUNCH(k3::umma_stream_tiles(c->umma, w, T, d, bn, k3::bs_slot_tile(c->bs), split_expert, s), 2,
                 "tile list");
-    K3_LAUNCH(k3::bs_quantize_latent(c->bs, w, T, d, bn, c->sharded ? n_local : nullptr, s), 1,
+    K3_LAUNCH(k3::bs_quantize_latent(c->bs, w, T, d, bn, c->sharded ? n_local : nullptr, s), bn <= 16 ? 1 : 2,
               bn <= 16 ? "latent rows -> e2m1 terms" : "latent rows -> e4m3 terms");
     // with a second bank the block-scaled kernels take the first bank's
     // tiles [0, count[1]) and the second bank's kernels the rest: the split

@@ -163,8 +163,8 @@ __device__ __forceinline__ int act_scale_byte(int t, int n, int stack) { return 
 // Slot-ordered rows: dst row s = src row (perm ? perm[s] / K : s), written
 // as terms q[C/128][t][rows_max][128]; the scales go to the tile atoms
 // sf[tile][C/128][2][512] at act_scale_byte(t, n, stack) + g for row n of
-// the tile (slot_tile[s] = tile << 8 | n), or, without a slot map, to
-// sf[rows][C/128][2] as one word per term (byte g = group g).  A half
+// the tile (slot_tile[s] = tile << 8 | n).  With slot_of the rows are
+// tokens instead, each split once and written to its K slots.  A half
 // warp covers 128 columns per chunk (8 per lane, 4 lanes per scale group)
 // and four chunks of one slot per pass, their loads issued together; the
 // loop runs per warp so that both halves always meet at the shuffles.
@@ -172,10 +172,13 @@ constexpr int kQuantChunks = 4;
 __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, const int* __restrict__ perm, int K, int rows,
                                   const int* __restrict__ rows_dev, int C, int rows_max,
                                   const int* __restrict__ slot_tile, int stack, uint8_t* __restrict__ q,
-                                  uint8_t* __restrict__ sf) {
+                                  uint8_t* __restrict__ sf, const int* __restrict__ slot_of) {
   pdl_trigger();
   pdl_wait();
-  if (rows_dev) rows = min(rows, *rows_dev);  // an expert shard: its own slots only
+  // slot_of: rows are tokens, each split once and written to its K slots
+  // slot_of[t * K + k] (those below *rows_dev with an expert shard)
+  const int slot_lim = (slot_of && rows_dev) ? *rows_dev : 0x7FFFFFFF;
+  if (rows_dev && !slot_of) rows = min(rows, *rows_dev);  // an expert shard: its own slots only
   const int hl = threadIdx.x & 15, half = (threadIdx.x >> 4) & 1;
   const int KC = C / kQK;
   const int KG = (KC + kQuantChunks - 1) / kQuantChunks;  // chunk groups per row
@@ -189,7 +192,7 @@ __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, const int* _
     int tn = 0;
     if (valid) {
       const int t = perm ? perm[s] / K : s;
-      tn = slot_tile ? slot_tile[s] : 0;
+      tn = slot_of ? 0 : slot_tile[s];
 #pragma unroll
       for (int c = 0; c < kQuantChunks; ++c) {
         const int kc = kg * kQuantChunks + c;
@@ -234,53 +237,20 @@ __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, const int* _
         w1 |= __shfl_sync(0xFFFFFFFFu, s1, base_lane + 4 * g) << (8 * g);
       }
       if (!valid || kc >= KC) continue;
-      const size_t r0 = (size_t)kc * 2 * rows_max + s;
-      *reinterpret_cast<uint2*>(q + r0 * kQK + hl * 8) = make_uint2(a0, b0);
-      *reinterpret_cast<uint2*>(q + (r0 + rows_max) * kQK + hl * 8) = make_uint2(a1, b1);
-      if (hl == 0) {
-        if (slot_tile) {
-          const int n = tn & 0xFF;
-          uint8_t* atom = sf + (((size_t)(tn >> 8) * KC + kc) * 2) * kAtom;
+      for (int k = 0; k < (slot_of ? K : 1); ++k) {
+        const int sl = slot_of ? slot_of[(size_t)s * K + k] : s;
+        if (sl >= slot_lim) continue;
+        const size_t r0 = (size_t)kc * 2 * rows_max + sl;
+        *reinterpret_cast<uint2*>(q + r0 * kQK + hl * 8) = make_uint2(a0, b0);
+        *reinterpret_cast<uint2*>(q + (r0 + rows_max) * kQK + hl * 8) = make_uint2(a1, b1);
+        if (hl == 0) {
+          const int tk = slot_of ? slot_tile[sl] : tn;
+          const int n = tk & 0xFF;
+          uint8_t* atom = sf + (((size_t)(tk >> 8) * KC + kc) * 2) * kAtom;
           *reinterpret_cast<uint32_t*>(atom + act_scale_byte(0, n, stack)) = w0;
           *reinterpret_cast<uint32_t*>(atom + act_scale_byte(1, n, stack)) = w1;
-        } else {  // row order: [rows][KC][2] words
-          *reinterpret_cast<uint2*>(sf + (((size_t)s * KC + kc) * 2) * 4) = make_uint2(w0, w1);
         }
       }
-    }
-  }
-}
-
-// Slot-ordered copy of per-token terms (the prefill path splits each token's
-// latent row once, then every slot takes its token's terms): tq
-// [KC][2][T][128] and tsc [T][KC][2] words (byte g = group g's scale) from
-// quant_rows_kernel in row order; slot s copies row perm[s] / K into the
-// planes q[KC][2][rows_max][128] and its scale words into the tile atoms at
-// act_scale_byte(term, n, stack).  One thread per 16 bytes: eight threads
-// move a 128-byte row.
-__global__ void gather_terms_kernel(const uint8_t* __restrict__ tq, const uint8_t* __restrict__ tsc,
-                                    const int* __restrict__ perm, int K, int T, int rows,
-                                    const int* __restrict__ rows_dev, int KC, int rows_max,
-                                    const int* __restrict__ slot_tile, int stack, uint8_t* __restrict__ q,
-                                    uint8_t* __restrict__ sf) {
-  pdl_trigger();
-  pdl_wait();
-  if (rows_dev) rows = min(rows, *rows_dev);  // an expert shard: its own slots only
-  const long long total = (long long)rows * KC * 16;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int piece = (int)(i & 7), term = (int)((i >> 3) & 1);
-    const long long sk = i >> 4;
-    const int kc = (int)(sk % KC), sl = (int)(sk / KC);
-    const int t = perm[sl] / K;
-    const size_t plane = (size_t)kc * 2 + term;
-    *reinterpret_cast<uint4*>(q + (plane * rows_max + sl) * kQK + piece * 16) =
-        *reinterpret_cast<const uint4*>(tq + (plane * T + t) * kQK + piece * 16);
-    if (piece == 0) {
-      const int tn = slot_tile[sl];
-      uint8_t* atom = sf + (((size_t)(tn >> 8) * KC + kc) * 2) * kAtom;
-      *reinterpret_cast<uint32_t*>(atom + act_scale_byte(term, tn & 0xFF, stack)) =
-          *reinterpret_cast<const uint32_t*>(tsc + (((size_t)t * KC + kc) * 2 + term) * 4);
     }
   }
 }
@@ -997,11 +967,14 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
 // first bank's decode tiles use; the epilogue adds the terms' columns and
 // applies s and b per group in fp32.  Per 128-column stage: the token terms
 // (one 4-D box), the stage's 2-bit tiles (one bulk copy) and the tile's
-// activation scale atom; eight warps expand the codes to e2m1 nibbles in
-// shared memory (64-byte swizzle, the layout the MMA reads) and run the
-// per-group epilogue; one thread issues the MMAs.  Each group's accumulator
-// alternates between two TMEM buffers, so the epilogue of one group
-// overlaps the MMA of the next.
+// activation scale atom.  Warps of their own expand the codes to e2m1
+// nibbles in shared memory (64-byte swizzle, the layout the MMA reads; one
+// thread per weight row, two chunks in flight), one thread issues the
+// MMAs, and four warps (one TMEM lane quarter each, both matrices) run the
+// per-group epilogue.  Each group's accumulator alternates between two
+// TMEM buffers, so the epilogue of one group overlaps the MMA of the next,
+// and expansion, MMAs and epilogue all run at once (with the expansion and
+// the epilogue on the same warps, their instruction latencies added up).
 constexpr int kB2Tile = 2560;  // one 2-bit tile: 128 rows x 64 codes (16 B a row), then 128 bf16 scales and biases
 template <bool GU>
 struct B2Cfg {
@@ -1013,14 +986,15 @@ struct B2Cfg {
   static constexpr int kRing = GU ? 6 : 7;
   static constexpr int kDec = kNumMat * kQM * 64;                    // e2m1 tiles of one chunk
   static constexpr int kCtas = GU ? 1 : 2;
-  static constexpr int kExFloats = GU ? kQM * kBsDecodeRows : 0;     // up sums handed to the gate warps
+  static constexpr int kEpiThreads = 128;                            // one weight row (TMEM lane) each
+  static constexpr int kExpThreads = 128;                            // one row (every matrix) each
   static constexpr int kXsFloats = kBsDecodeRows * 64;               // the item's per-group row sums (K/64 <= 64)
-  static constexpr int kSmem = kRing * kStage + 2 * kDec + kAtom + 4 * (kExFloats + kXsFloats) + 1024 + 512;
+  static constexpr int kSmem = kRing * kStage + 2 * kDec + kAtom + 4 * kXsFloats + 1024 + 512;
   // TMEM: accumulators (matrix, buffer) at (m * 2 + buf) * kN, the weight
   // scale atom, one activation atom per ring stage
   static constexpr int kSfa = kNumMat * 2 * kN;
   static constexpr int kTmemCols = GU ? 512 : 256;
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 64 + kEpiThreads + kExpThreads;   // copies, MMA, epilogue, expand
   static_assert(kSfa + 4 + 4 * kRing <= kTmemCols, "TMEM budget");
   static_assert(kCtas * (kSmem + 1024) <= 233472, "shared memory per SM");
   static_assert(kN % 16 == 0 && kN <= 256, "MMA N");
@@ -1054,19 +1028,15 @@ struct B2Params {
   uint64_t limit_ns;
 };
 
-// Four 2-bit codes per byte (low bits first) of a 32-bit word -> eight e2m1
-// nibbles (low nibble first) per output word, q -> 2q - [q == 3].
+// Sixteen 2-bit codes of a 32-bit word (four per byte, low bits first) ->
+// sixteen e2m1 nibbles (low nibble first; codes 0..7 in .x), q -> 2q - [q == 3].
+// Byte j of a holds codes 4j, 4j+1 as nibbles, byte j of b codes 4j+2,
+// 4j+3; the byte permutes interleave them into code order.
 __device__ __forceinline__ uint2 codes_to_e2m1(uint32_t w) {
-  uint32_t r[2];
-#pragma unroll
-  for (int hf = 0; hf < 2; ++hf) {
-    uint32_t t = (w >> (16 * hf)) & 0xFFFFu;
-    t = (t | (t << 8)) & 0x00FF00FFu;
-    t = (t | (t << 4)) & 0x0F0F0F0Fu;
-    t = (t | (t << 2)) & 0x33333333u;  // nibble k holds code k
-    r[hf] = (t << 1) - (t & (t >> 1) & 0x11111111u);
-  }
-  return make_uint2(r[0], r[1]);
+  const uint32_t a = (w & 0x03030303u) | ((w << 2) & 0x30303030u);
+  const uint32_t b = ((w >> 4) & 0x03030303u) | ((w >> 2) & 0x30303030u);
+  const uint32_t t0 = __byte_perm(a, b, 0x5140), t1 = __byte_perm(a, b, 0x7362);
+  return make_uint2((t0 << 1) - (t0 & (t0 >> 1) & 0x11111111u), (t1 << 1) - (t1 & (t1 >> 1) & 0x11111111u));
 }
 
 template <bool GU>
@@ -1078,12 +1048,10 @@ __global__ void __launch_bounds__(B2Cfg<GU>::kThreads, B2Cfg<GU>::kCtas)
   uint8_t* ring = smem;                                  // [kRing][B terms | B atom | 2-bit tiles]
   uint8_t* dec = smem + C::kRing * C::kStage;            // [2][mats][128 rows][64 B] e2m1, 64-byte swizzle
   uint8_t* sfa_atom = dec + 2 * C::kDec;                 // 512 bytes of 127
-  float* ex = reinterpret_cast<float*>(sfa_atom + kAtom);  // GU: [128 rows][16 tokens] up sums
-  float* xs = ex + C::kExFloats;                           // [16 token rows][64 groups] row sums
+  float* xs = reinterpret_cast<float*>(sfa_atom + kAtom);  // [16 token rows][64 groups] row sums
   uint64_t* bars = reinterpret_cast<uint64_t*>(xs + C::kXsFloats);
-  // bars: full[R], empty[R], dfull[2], dempty[2], afull[2], aempty[2], drain, ex_full, ex_empty,
-  // xs_full, xs_empty
-  constexpr int NB = 2 * C::kRing + 13;
+  // bars: full[R], empty[R], dfull[2], dempty[2], afull[2], aempty[2], drain, xs_full, xs_empty
+  constexpr int NB = 2 * C::kRing + 11;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NB);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1097,10 +1065,14 @@ __global__ void __launch_bounds__(B2Cfg<GU>::kThreads, B2Cfg<GU>::kCtas)
   if (threadIdx.x == 0) {
     for (int i = 0; i < NB; ++i) {
       const int k = i - 2 * C::kRing;
-      // dfull, aempty, xs_full and xs_empty: one arrival per expand /
-      // epilogue thread; ex_full and ex_empty: one per thread of a matrix half
-      mbar_init(smem_u32(bars + i),
-                (k == 0 || k == 1 || k == 6 || k == 7 || k == 11 || k == 12) ? 256u : (k == 9 || k == 10) ? 128u : 1u);
+      // empty: the MMA commit and the epilogue threads (done with the
+      // stage's scales and biases); dfull: the expand threads; aempty,
+      // xs_full, xs_empty: the epilogue threads
+      const uint32_t cnt = (i >= C::kRing && i < 2 * C::kRing) ? 1u + C::kEpiThreads
+                           : (k == 0 || k == 1)                  ? (uint32_t)C::kExpThreads
+                           : (k == 6 || k == 7 || k == 9 || k == 10) ? (uint32_t)C::kEpiThreads
+                                                                     : 1u;
+      mbar_init(smem_u32(bars + i), cnt);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1120,8 +1092,7 @@ __global__ void __launch_bounds__(B2Cfg<GU>::kThreads, B2Cfg<GU>::kCtas)
   auto afull = [&](int b) { return smem_u32(bars + 2 * C::kRing + 4 + b); };
   auto aempty = [&](int b) { return smem_u32(bars + 2 * C::kRing + 6 + b); };
   const uint32_t drain = smem_u32(bars + 2 * C::kRing + 8);
-  const uint32_t ex_full = smem_u32(bars + 2 * C::kRing + 9), ex_empty = smem_u32(bars + 2 * C::kRing + 10);
-  const uint32_t xs_full = smem_u32(bars + 2 * C::kRing + 11), xs_empty = smem_u32(bars + 2 * C::kRing + 12);
+  const uint32_t xs_full = smem_u32(bars + 2 * C::kRing + 9), xs_empty = smem_u32(bars + 2 * C::kRing + 10);
   auto stage = [&](int r) { return ring + (size_t)r * C::kStage; };
   const int G = p.KC * 2;  // groups along K
 
@@ -1205,25 +1176,58 @@ __global__ void __launch_bounds__(B2Cfg<GU>::kThreads, B2Cfg<GU>::kCtas)
       }
     }
     __syncwarp();
+  } else if (warp >= 2 + C::kEpiThreads / 32) {
+    // ================= expand (thread = row, every matrix), both groups of
+    // each chunk, into the two-deep ring of e2m1 tiles
+    const int r = threadIdx.x - 64 - C::kEpiThreads;
+    int kg = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      for (int kc = 0; kc < p.KC; ++kc, ++kg) {
+        const int rr = kg % C::kRing, d = kg & 1;
+        bool w_ok = mbar_wait(full(rr), (kg / C::kRing) & 1, g, 32u);
+        if (w_ok && kg >= 2) w_ok = mbar_wait(dempty(d), ((kg >> 1) - 1) & 1, g, 64u);
+        if (!__all_sync(0xFFFFFFFFu, w_ok)) {  // warp-uniform exits
+          ok = false;
+          break;
+        }
+        const uint8_t* src = stage(rr) + C::kB + kAtom;
+        const int sw = (r >> 1) & 3;  // 64-byte swizzle: 16-byte chunk c of row r at c ^ ((r >> 1) & 3)
+#pragma unroll
+        for (int mat = 0; mat < C::kNumMat; ++mat) {
+          uint8_t* drow = dec + (size_t)d * C::kDec + (size_t)(mat * kQM + r) * 64;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint4 q = *reinterpret_cast<const uint4*>(src + (size_t)(j * C::kNumMat + mat) * kB2Tile + r * 16);
+            const uint2 e0 = codes_to_e2m1(q.x), e1 = codes_to_e2m1(q.y), e2 = codes_to_e2m1(q.z),
+                        e3 = codes_to_e2m1(q.w);
+            // row bytes [32 j, 32 j + 32): 16-byte chunks 2j, 2j + 1
+            *reinterpret_cast<uint4*>(drow + (((2 * j) ^ sw) << 4)) = make_uint4(e0.x, e0.y, e1.x, e1.y);
+            *reinterpret_cast<uint4*>(drow + (((2 * j + 1) ^ sw) << 4)) = make_uint4(e2.x, e2.y, e3.x, e3.y);
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(dfull(d));
+      }
+    }
   } else {
-    // ================= expand + epilogue (warps 2..9)
+    // ================= epilogue (warps 2..5: row r = TMEM lane, both
+    // matrices): per group, acc += s * (sum of the six terms' columns) +
+    // b * (the group's row sum); at the end of an item SiTU-GLU and h's
+    // terms (gate/up) or o (down)
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;  // weight row of the block (TMEM lane)
-    const int half = (warp - 2) >> 2;   // GU: the matrix (0 gate, 1 up); DOWN: token half
-    const int mat = GU ? half : 0;
-    constexpr int kTok = GU ? kBsDecodeRows : kBsDecodeRows / 2;  // tokens this thread accumulates
-    const int n0 = GU ? 0 : half * kTok;
+    const int r = quarter * 32 + lane;
+    const int et = threadIdx.x - 64;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     int kg = 0, it = 0;
     bool ok = true;
-    float s_cur[2] = {0.f, 0.f}, b_cur[2] = {0.f, 0.f};
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
       const int ti = first + item / p.MT, mt = item % p.MT;
       const int4 tile = p.tiles[ti];
       // the item's per-group sums of its token rows (latent rows by token,
       // h rows by slot; rows past the tile 0) into shared memory, once
       if (it > 0 && !__all_sync(0xFFFFFFFFu, mbar_wait(xs_empty, (it - 1) & 1, g, 256u))) break;
-      for (int i = threadIdx.x - 64; i < kBsDecodeRows * G; i += 256) {
+      for (int i = et; i < kBsDecodeRows * G; i += C::kEpiThreads) {
         const int n = i / G, gg = i - n * G;
         float v = 0.f;
         if (n < tile.z) {
@@ -1235,118 +1239,92 @@ __global__ void __launch_bounds__(B2Cfg<GU>::kThreads, B2Cfg<GU>::kCtas)
       }
       mbar_arrive(xs_full);
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(xs_full, it & 1, g, 512u))) break;
-      float acc[kTok];
+      float acc[C::kNumMat][kBsDecodeRows];
 #pragma unroll
-      for (int n = 0; n < kTok; ++n) acc[n] = 0.f;
-      // the epilogue of chunk kc - 1's two groups follows the expansion of chunk kc
-      auto epilogue = [&](int kgp, int kc) {
+      for (int m = 0; m < C::kNumMat; ++m)
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int gg = 2 * kc + j;
-          ok = ok && mbar_wait(afull(j), kgp & 1, g, 16u);
-          if (!__all_sync(0xFFFFFFFFu, ok)) {  // warp-uniform before the TMEM loads
-            ok = false;
-            return;
-          }
-          tc_fence_after();
-          const uint32_t col = lane_base + (uint32_t)((mat * 2 + j) * C::kN);
-          // the six terms' columns of this thread's tokens: all loads issued,
-          // then one wait
-          float v[6 * kTok];
-          if constexpr (GU)
-            tmem_ld3x32(col, v);
-          else
-            tmem_ld6x8_stride16(col + n0, v);
-          tc_fence_before();
-          mbar_arrive(aempty(j));
-#pragma unroll
-          for (int n = 0; n < kTok; ++n) {
-            float dsum;
-            if (GU)  // column 16 t + n for term t
-              dsum = ((v[n] + v[n + 16]) + (v[n + 32] + v[n + 48])) + (v[n + 64] + v[n + 80]);
-            else
-              dsum = ((v[n] + v[n + 8]) + (v[n + 16] + v[n + 24])) + (v[n + 32] + v[n + 40]);
-            acc[n] = fmaf(s_cur[j], dsum, acc[n]);
-            acc[n] = fmaf(b_cur[j], xs[(n0 + n) * 64 + gg], acc[n]);
-          }
-        }
-      };
-      float s_next[2], b_next[2];
+        for (int n = 0; n < kBsDecodeRows; ++n) acc[m][n] = 0.f;
       for (int kc = 0; kc < p.KC && ok; ++kc, ++kg) {
-        const int rr = kg % C::kRing, d = kg & 1;
-        bool w_ok = mbar_wait(full(rr), (kg / C::kRing) & 1, g, 32u);
-        if (w_ok && kg >= 2) w_ok = mbar_wait(dempty(d), ((kg >> 1) - 1) & 1, g, 64u);
-        if (!__all_sync(0xFFFFFFFFu, w_ok)) {  // warp-uniform exits
+        const int rr = kg % C::kRing;
+        // the stage's scales and biases (the wait makes its copies visible here)
+        bool w_ok = mbar_wait(full(rr), (kg / C::kRing) & 1, g, 16u);
+        if (!__all_sync(0xFFFFFFFFu, w_ok)) {
           ok = false;
           break;
         }
-        // expand: GU thread (matrix half, row r) both groups; DOWN thread
-        // (row r) group `half`
         const uint8_t* src = stage(rr) + C::kB + kAtom;
-        uint8_t* drow = dec + (size_t)d * C::kDec + (size_t)(mat * kQM + r) * 64;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          if (!GU && j != half) continue;
-          const uint4 q = *reinterpret_cast<const uint4*>(src + (size_t)(j * C::kNumMat + mat) * kB2Tile + r * 16);
-          const uint2 e0 = codes_to_e2m1(q.x), e1 = codes_to_e2m1(q.y), e2 = codes_to_e2m1(q.z),
-                      e3 = codes_to_e2m1(q.w);
-          // row bytes [32 j, 32 j + 32): 16-byte chunks 2j, 2j + 1, swizzled
-          const int sw = (r >> 1) & 3;
-          *reinterpret_cast<uint4*>(drow + (((2 * j) ^ sw) << 4)) = make_uint4(e0.x, e0.y, e1.x, e1.y);
-          *reinterpret_cast<uint4*>(drow + (((2 * j + 1) ^ sw) << 4)) = make_uint4(e2.x, e2.y, e3.x, e3.y);
-        }
+          float sc[C::kNumMat], bi[C::kNumMat];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const uint8_t* tl = src + (size_t)(j * C::kNumMat + mat) * kB2Tile;
-          s_next[j] = bf16_to_f32(*reinterpret_cast<const uint16_t*>(tl + 2048 + 2 * r));
-          b_next[j] = bf16_to_f32(*reinterpret_cast<const uint16_t*>(tl + 2304 + 2 * r));
+          for (int m = 0; m < C::kNumMat; ++m) {
+            const uint8_t* tl = src + (size_t)(j * C::kNumMat + m) * kB2Tile;
+            sc[m] = bf16_to_f32(*reinterpret_cast<const uint16_t*>(tl + 2048 + 2 * r));
+            bi[m] = bf16_to_f32(*reinterpret_cast<const uint16_t*>(tl + 2304 + 2 * r));
+          }
+          w_ok = mbar_wait(afull(j), kg & 1, g, 16u);
+          if (!__all_sync(0xFFFFFFFFu, w_ok)) {  // warp-uniform before the TMEM loads
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int gg = 2 * kc + j;
+          // eight tokens per pass: the six terms' columns 16 t + n of every
+          // matrix, loaded together (one wait)
+#pragma unroll
+          for (int ps = 0; ps < kBsDecodeRows / 8; ++ps) {
+            if (8 * ps < tile.z) {  // warp-uniform
+              float v[48 * C::kNumMat];
+              const uint32_t col0 = lane_base + (uint32_t)(j * C::kN + 8 * ps);
+              if constexpr (C::kNumMat == 2)
+                tmem_ld2x6x8_stride16(col0, col0 + 2 * C::kN, v);
+              else
+                tmem_ld6x8_stride16(col0, v);
+#pragma unroll
+              for (int m = 0; m < C::kNumMat; ++m) {
+#pragma unroll
+                for (int n = 0; n < 8; ++n) {
+                  if (8 * ps + n < tile.z) {
+                    const float* vm = v + 48 * m;
+                    const float dsum = ((vm[n] + vm[n + 8]) + (vm[n + 16] + vm[n + 24])) + (vm[n + 32] + vm[n + 40]);
+                    float& a = acc[m][8 * ps + n];
+                    a = fmaf(sc[m], dsum, a);
+                    a = fmaf(bi[m], xs[(8 * ps + n) * 64 + gg], a);
+                  }
+                }
+              }
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(aempty(j));
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(dfull(d));
-        if (kc > 0) epilogue(kg - 1, kc - 1);
-        s_cur[0] = s_next[0];
-        s_cur[1] = s_next[1];
-        b_cur[0] = b_next[0];
-        b_cur[1] = b_next[1];
+        if (!ok) break;
+        mbar_arrive(empty(rr));  // done with the stage's scales and biases
       }
-      if (ok) epilogue(kg - 1, p.KC - 1);
       mbar_arrive(xs_empty);  // the item's row sums are no longer read
       if (!ok || *abort_flag) break;
       // ---- outputs of the item
-      const int m = mt * kQM + r;
-      if (GU) {
-        // up sums to the gate warps through shared memory (two barriers:
-        // written / read, one phase per item)
-        if (half == 1) {
-          if (it > 0 && !__all_sync(0xFFFFFFFFu, mbar_wait(ex_empty, (it - 1) & 1, g, 128u))) break;
+      const int m_out = mt * kQM + r;
+      if constexpr (GU) {
+        // h = SiTU-GLU(gate, up) as bf16, its six e2m1 terms over the warp's
+        // 32 rows (one scale group of the down GEMM's K) and the per-32-row
+        // sums of h
+        const int KCo = p.ld_out / kQK;
+        uint8_t* atoms = p.hsf + (((size_t)ti * KCo + (m_out >> 7)) * 2) * kAtom + ((m_out >> 5) & 3);
+        unsigned long long my_sc = 0;
 #pragma unroll
-          for (int n = 0; n < kTok; ++n) ex[r * kTok + n] = acc[n];
-          mbar_arrive(ex_full);
-        } else {
-          if (!__all_sync(0xFFFFFFFFu, mbar_wait(ex_full, it & 1, g, 128u))) break;
-          // h = SiTU-GLU(gate, up) as bf16, its six e2m1 terms over the
-          // warp's 32 rows (one scale group of the down GEMM's K) and the
-          // per-32-row sums of h
-          float up[kTok];
-#pragma unroll
-          for (int n = 0; n < kTok; ++n) up[n] = ex[r * kTok + n];
-          mbar_arrive(ex_empty);
-          const int KCo = p.ld_out / kQK;
-          uint8_t* atoms = p.hsf + (((size_t)ti * KCo + (m >> 7)) * 2) * kAtom + ((m >> 5) & 3);
-          unsigned long long my_sc = 0;
-#pragma unroll
-          for (int n = 0; n < kTok; ++n) {
-            if (n >= tile.z) break;  // warp-uniform
+        for (int n = 0; n < kBsDecodeRows; ++n) {
+          if (n < tile.z) {  // warp-uniform
             const size_t row = (size_t)(tile.y + n);
-            const uint16_t hb = f32_to_bf16(situ_fast(acc[n], up[n], p.beta, p.beta_lin));
-            p.h[row * p.ld_out + m] = hb;
+            const uint16_t hb = f32_to_bf16(situ_fast(acc[0][n], acc[1][n], p.beta, p.beta_lin));
+            p.h[row * p.ld_out + m_out] = hb;
             float rr = bf16_to_f32(hb);
             float hsum = rr;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) hsum += __shfl_xor_sync(0xFFFFFFFFu, hsum, o);
-            if (lane == 0) p.hsum[row * (p.ld_out / 32) + (m >> 5)] = hsum;
+            if (lane == 0) p.hsum[row * (p.ld_out / 32) + (m_out >> 5)] = hsum;
             uint32_t qn = 0;
-            unsigned long long sc = 0;
+            unsigned long long scw = 0;
 #pragma unroll
             for (int t = 0; t < kFp4Terms; ++t) {
               const uint32_t sb = e2m1_scale_byte(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(rr))));
@@ -1358,27 +1336,27 @@ __global__ void __launch_bounds__(B2Cfg<GU>::kThreads, B2Cfg<GU>::kCtas)
                 rr = 0.f;
               }
               qn |= qb << (4 * t);
-              sc |= (unsigned long long)sb << (8 * t);
+              scw |= (unsigned long long)sb << (8 * t);
             }
             const uint32_t qo = __shfl_down_sync(0xFFFFFFFFu, qn, 1);
             if (!(lane & 1)) {
 #pragma unroll
               for (int t = 0; t < kFp4Terms; ++t)
-                p.hq[(((size_t)(m >> 7) * kFp4Terms + t) * p.rows_max + row) * 64 + ((m & 127) >> 1)] =
+                p.hq[(((size_t)(m_out >> 7) * kFp4Terms + t) * p.rows_max + row) * 64 + ((m_out & 127) >> 1)] =
                     (uint8_t)(((qn >> (4 * t)) & 0xFu) | (((qo >> (4 * t)) & 0xFu) << 4));
             }
-            if (lane == n) my_sc = sc;
+            if (lane == n) my_sc = scw;
           }
-          if (lane < tile.z && lane < kTok) {
+        }
+        if (lane < tile.z && lane < kBsDecodeRows) {
 #pragma unroll
-            for (int t = 0; t < kFp4Terms; ++t)
-              atoms[act_scale_byte(t, lane, kBsDecodeRows)] = (uint8_t)(my_sc >> (8 * t));
-          }
+          for (int t = 0; t < kFp4Terms; ++t)
+            atoms[act_scale_byte(t, lane, kBsDecodeRows)] = (uint8_t)(my_sc >> (8 * t));
         }
       } else {
 #pragma unroll
-        for (int n = 0; n < kTok; ++n)
-          if (n0 + n < tile.z) p.o[(size_t)(tile.y + n0 + n) * p.ld_out + m] = acc[n];
+        for (int n = 0; n < kBsDecodeRows; ++n)
+          if (n < tile.z) p.o[(size_t)(tile.y + n) * p.ld_out + m_out] = acc[0][n];
       }
     }
   }
@@ -1461,7 +1439,6 @@ struct BsWs {
   uint8_t *hq, *hsf;  // h rows: the same over I
   int* slot_tile;     // [rows_max]: tile << 8 | row within the tile
   float* part;        // K-split partial sums (T = 1): kBsMaxSplit planes of K rows of I (gate), I (up), L (down)
-  uint8_t *tq, *tsc;  // prefill: per-token latent terms [L/128][2][max_tokens][128], scale words [max_tokens][L/128][2]
   float *xsum, *hsum; // second bank at decode sizes: per-64-column latent sums by token, per-32-row h sums by slot
   size_t total;
 };
@@ -1472,27 +1449,24 @@ BsWs bs_ws_view(void* base, const Dims& d, int max_tokens) {
   // tiles hold at least one slot and at most one expert: <= E + R / 16 whatever the tile height
   const size_t MT = (size_t)d.E + R / 16 + 1;
   auto terms = [&](size_t C) { return std::max(2 * R * C, (size_t)kFp4Terms * Rf * C / 2); };
-  const size_t Tp = max_tokens > kBsDecodeMaxT ? (size_t)max_tokens : 0;  // prefill sizes only
-  const size_t sizes[10] = {terms(d.L),
+  const size_t sizes[8] = {terms(d.L),
                            MT * (d.L / kQK) * 2 * kAtom,
                            terms(d.I),
                            MT * (d.I / kQK) * 2 * kAtom,
                            R * sizeof(int),
                            (size_t)kBsMaxSplit * d.K * (2 * d.I + d.L) * sizeof(float),
-                           Tp * d.L * 2,
-                           Tp * (d.L / kQK) * 2 * 4,
                            (size_t)std::min(max_tokens, kBsDecodeMaxT) * (d.L / 64) * sizeof(float),
                            Rf * (d.I / 32) * sizeof(float)};
   uint8_t* b = static_cast<uint8_t*>(base);
-  uint8_t* ptr[10];
+  uint8_t* ptr[8];
   size_t off = 0;
-  for (int i = 0; i < 10; ++i) {
+  for (int i = 0; i < 8; ++i) {
     ptr[i] = b ? b + off : nullptr;
     off += up(sizes[i]);
   }
   return BsWs{(int)R,  (int)Rf, (int)MT, ptr[0], ptr[1], ptr[2], ptr[3], reinterpret_cast<int*>(ptr[4]),
-              reinterpret_cast<float*>(ptr[5]), ptr[6], ptr[7], reinterpret_cast<float*>(ptr[8]),
-              reinterpret_cast<float*>(ptr[9]), off};
+              reinterpret_cast<float*>(ptr[5]), reinterpret_cast<float*>(ptr[6]), reinterpret_cast<float*>(ptr[7]),
+              off};
 }
 
 template <int MODE, int NQ>
@@ -1570,17 +1544,12 @@ cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims
   const long long halves = (long long)TK * ((d.L / kQK + ch - 1) / ch);
   const int blocks = (int)std::min<long long>((halves * 16 + 255) / 256, 8LL * p.num_sms);
   if (!fp4) {
-    // prefill tiles: each token's row split once (token order), then the
-    // slots' copies -- the split is ALU work, the copy a memory stream
+    // prefill tiles: each token's row split once, its terms written to the
+    // token's K slots (the split is ALU work, the copies a memory stream)
     const long long th = (long long)T * ((d.L / kQK + kQuantChunks - 1) / kQuantChunks);
     const int tb = (int)std::min<long long>((th * 16 + 255) / 256, 8LL * p.num_sms);
-    cudaError_t e = launch_pdl(quant_rows_kernel, tb, 256, 0, s, w.lat, (const int*)nullptr, 1, T,
-                               (const int*)nullptr, d.L, T, (const int*)nullptr, stack, ws.tq, ws.tsc);
-    if (e != cudaSuccess) return e;
-    const long long pieces = (long long)TK * (d.L / kQK) * 16;
-    const int gb = (int)std::min<long long>((pieces + 255) / 256, 16LL * p.num_sms);
-    return launch_pdl(gather_terms_kernel, gb, 256, 0, s, (const uint8_t*)ws.tq, (const uint8_t*)ws.tsc, w.perm,
-                      d.K, T, TK, n_local, d.L / kQK, ws.rows_max, (const int*)ws.slot_tile, stack, ws.lq, ws.lsf);
+    return launch_pdl(quant_rows_kernel, tb, 256, 0, s, w.lat, (const int*)nullptr, d.K, T, n_local, d.L,
+                      ws.rows_max, (const int*)ws.slot_tile, stack, ws.lq, ws.lsf, (const int*)w.slot);
   }
   auto kernel = ch == 1 ? quant_rows_fp4_kernel<1> : quant_rows_fp4_kernel<kQuantChunks>;
   return launch_pdl(kernel, blocks, 256, 0, s, w.lat, w.perm, d.K, TK, n_local, d.L, ws.rows_fp4, ws.slot_tile, stack,

@@ -198,6 +198,31 @@ __device__ __forceinline__ void tmem_ld6x8_stride16(uint32_t taddr, float v[48])
   for (int i = 0; i < 48; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Six blocks of 8 columns, 16 columns apart, at two addresses (one wait):
+// v[0..48) from a, v[48..96) from b.
+__device__ __forceinline__ void tmem_ld2x6x8_stride16(uint32_t a, uint32_t b, float v[96]) {
+  uint32_t r[96];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%96];"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%97];"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16, %17, %18, %19, %20, %21, %22, %23}, [%98];"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%24, %25, %26, %27, %28, %29, %30, %31}, [%99];"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%32, %33, %34, %35, %36, %37, %38, %39}, [%100];"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%40, %41, %42, %43, %44, %45, %46, %47}, [%101];"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%48, %49, %50, %51, %52, %53, %54, %55}, [%102];"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%56, %57, %58, %59, %60, %61, %62, %63}, [%103];"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%64, %65, %66, %67, %68, %69, %70, %71}, [%104];"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%72, %73, %74, %75, %76, %77, %78, %79}, [%105];"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%80, %81, %82, %83, %84, %85, %86, %87}, [%106];"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%88, %89, %90, %91, %92, %93, %94, %95}, [%107];"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95])
+      : "r"(a + 0u), "r"(a + 16u), "r"(a + 32u), "r"(a + 48u), "r"(a + 64u), "r"(a + 80u), "r"(b + 0u), "r"(b + 16u), "r"(b + 32u), "r"(b + 48u), "r"(b + 64u), "r"(b + 80u)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 96; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // SiTU-GLU in fp32 from the identities tanh(x/2) = (1 - e^-x)/(1 + e^-x)
 // and sigmoid(g) = 1/(1 + e^-g), one exponential per branch, written for
 // either sign without overflow:

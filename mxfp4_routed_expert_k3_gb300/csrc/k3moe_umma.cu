@@ -1340,13 +1340,34 @@ cudaError_t umma_stream_prepare(const UmmaPlan& p, const Work& w, int T, const D
 }
 
 // Only the tile list (tiles of at most bn_max rows) and the slot -> tile map.
+// slot -> (tile << 8 | row) for every row of every tile: one warp per tile,
+// its rows' entries written together (consecutive slots).
+__global__ void __launch_bounds__(256) slot_tile_kernel(const int4* __restrict__ tiles, const int* __restrict__ count,
+                                                        int* __restrict__ slot_tile) {
+  pdl_trigger();
+  pdl_wait();
+  const int n_tiles = *count;
+  const int lane = threadIdx.x & 31;
+  const int nw = (int)((gridDim.x * blockDim.x) >> 5);
+  for (int ti = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); ti < n_tiles; ti += nw) {
+    const int4 t = tiles[ti];
+    for (int n = lane; n < t.z; n += 32) slot_tile[t.y + n] = (ti << 8) | n;
+  }
+}
+
 cudaError_t umma_stream_tiles(const UmmaPlan& p, const Work& w, int T, const Dims& d, int bn_max, int* slot_tile,
                               int split_expert, cudaStream_t s) {
   if (T * d.K <= 0) return cudaSuccess;
   if (bn_max < kMinTileRows || bn_max > 255) return cudaErrorInvalidValue;  // list capacity, slot map row field
   UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
-  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, bn_max, ws.tiles, ws.count, slot_tile, split_expert);
-  return cudaGetLastError();
+  // the list in one CTA (a scan over the active experts); the slot map,
+  // T*K scattered entries, by all SMs afterwards
+  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, bn_max, ws.tiles, ws.count, nullptr, split_expert);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !slot_tile) return e;
+  const int max_tiles = std::min(p.dims.E, T * d.K) + T * d.K / kMinTileRows + 1;
+  return launch_pdl(slot_tile_kernel, std::min((max_tiles + 7) / 8, 8 * p.num_sms), 256, 0, s, (const int4*)ws.tiles,
+                    (const int*)ws.count, slot_tile);
 }
 
 cudaError_t bank2_tiles(const uint8_t* q, const uint16_t* sc, const uint16_t* bi, int ne, int rows, int cols,
