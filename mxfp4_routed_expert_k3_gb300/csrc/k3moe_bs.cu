@@ -1108,7 +1108,7 @@ __global__ void __launch_bounds__(B2Cfg<GU>::kThreads, B2Cfg<GU>::kCtas)
             p.a_tiles + ((size_t)(tile.x - p.expert_base) * p.MT + mt) * (size_t)G * C::kNumMat * kB2Tile;
         for (int kc = 0; kc < p.KC; ++kc, ++kg) {
           const int r = kg % C::kRing, u = kg / C::kRing;
-          if (u > 0 && !mbar_wait(empty(r), (u - 1) & 1, g, 1u)) {
+          if (u > 0 && !mbar_wait_sleep(empty(r), (u - 1) & 1, g, 1u)) {
             ok = false;
             break;
           }
@@ -1141,7 +1141,7 @@ __global__ void __launch_bounds__(B2Cfg<GU>::kThreads, B2Cfg<GU>::kCtas)
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         for (int kc = 0; kc < p.KC; ++kc, ++kg) {
           const int r = kg % C::kRing, d = kg & 1;
-          if (!mbar_wait(full(r), (kg / C::kRing) & 1, g, 2u) || !mbar_wait(dfull(d), (kg >> 1) & 1, g, 4u)) {
+          if (!mbar_wait_sleep(full(r), (kg / C::kRing) & 1, g, 2u) || !mbar_wait_sleep(dfull(d), (kg >> 1) & 1, g, 4u)) {
             ok = false;
             break;
           }
@@ -1151,7 +1151,7 @@ __global__ void __launch_bounds__(B2Cfg<GU>::kThreads, B2Cfg<GU>::kCtas)
           const uint64_t so = (uint64_t)((uint32_t)(r * C::kStage) >> 4);
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
-            if (kg > 0 && !mbar_wait(aempty(j), (kg - 1) & 1, g, 8u)) {
+            if (kg > 0 && !mbar_wait_sleep(aempty(j), (kg - 1) & 1, g, 8u)) {
               ok = false;
               break;
             }
@@ -1185,8 +1185,8 @@ __global__ void __launch_bounds__(B2Cfg<GU>::kThreads, B2Cfg<GU>::kCtas)
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       for (int kc = 0; kc < p.KC; ++kc, ++kg) {
         const int rr = kg % C::kRing, d = kg & 1;
-        bool w_ok = mbar_wait(full(rr), (kg / C::kRing) & 1, g, 32u);
-        if (w_ok && kg >= 2) w_ok = mbar_wait(dempty(d), ((kg >> 1) - 1) & 1, g, 64u);
+        bool w_ok = mbar_wait_sleep(full(rr), (kg / C::kRing) & 1, g, 32u);
+        if (w_ok && kg >= 2) w_ok = mbar_wait_sleep(dempty(d), ((kg >> 1) - 1) & 1, g, 64u);
         if (!__all_sync(0xFFFFFFFFu, w_ok)) {  // warp-uniform exits
           ok = false;
           break;
@@ -1226,7 +1226,7 @@ __global__ void __launch_bounds__(B2Cfg<GU>::kThreads, B2Cfg<GU>::kCtas)
       const int4 tile = p.tiles[ti];
       // the item's per-group sums of its token rows (latent rows by token,
       // h rows by slot; rows past the tile 0) into shared memory, once
-      if (it > 0 && !__all_sync(0xFFFFFFFFu, mbar_wait(xs_empty, (it - 1) & 1, g, 256u))) break;
+      if (it > 0 && !__all_sync(0xFFFFFFFFu, mbar_wait_sleep(xs_empty, (it - 1) & 1, g, 256u))) break;
       for (int i = et; i < kBsDecodeRows * G; i += C::kEpiThreads) {
         const int n = i / G, gg = i - n * G;
         float v = 0.f;
@@ -1238,7 +1238,7 @@ __global__ void __launch_bounds__(B2Cfg<GU>::kThreads, B2Cfg<GU>::kCtas)
         xs[n * 64 + gg] = v;
       }
       mbar_arrive(xs_full);
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(xs_full, it & 1, g, 512u))) break;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_sleep(xs_full, it & 1, g, 512u))) break;
       float acc[C::kNumMat][kBsDecodeRows];
 #pragma unroll
       for (int m = 0; m < C::kNumMat; ++m)
@@ -1247,7 +1247,7 @@ __global__ void __launch_bounds__(B2Cfg<GU>::kThreads, B2Cfg<GU>::kCtas)
       for (int kc = 0; kc < p.KC && ok; ++kc, ++kg) {
         const int rr = kg % C::kRing;
         // the stage's scales and biases (the wait makes its copies visible here)
-        bool w_ok = mbar_wait(full(rr), (kg / C::kRing) & 1, g, 16u);
+        bool w_ok = mbar_wait_sleep(full(rr), (kg / C::kRing) & 1, g, 16u);
         if (!__all_sync(0xFFFFFFFFu, w_ok)) {
           ok = false;
           break;
@@ -1262,7 +1262,7 @@ __global__ void __launch_bounds__(B2Cfg<GU>::kThreads, B2Cfg<GU>::kCtas)
             sc[m] = bf16_to_f32(*reinterpret_cast<const uint16_t*>(tl + 2048 + 2 * r));
             bi[m] = bf16_to_f32(*reinterpret_cast<const uint16_t*>(tl + 2304 + 2 * r));
           }
-          w_ok = mbar_wait(afull(j), kg & 1, g, 16u);
+          w_ok = mbar_wait_sleep(afull(j), kg & 1, g, 16u);
           if (!__all_sync(0xFFFFFFFFu, w_ok)) {  // warp-uniform before the TMEM loads
             ok = false;
             break;

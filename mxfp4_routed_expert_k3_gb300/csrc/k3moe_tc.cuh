@@ -61,6 +61,33 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const G
   }
 }
 
+// The same wait with a suspend-time hint (1 ms): a waiting thread sleeps
+// until the phase completes instead of re-issuing try_wait, leaving the
+// issue slots to the warps that work (the bound and the abort check are
+// the same; the abort is seen within 32 hints).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(1000000u)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const Guard& g, unsigned code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (*g.abort) return false;
+    if (global_ns() - t0 > g.limit_ns) {
+      *g.abort = 1;
+      atomicOr(g.status, code);
+      return false;
+    }
+  }
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
