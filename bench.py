@@ -784,7 +784,7 @@ def main():
     ap.add_argument("--prefill-tokens", type=int, default=PREFILL_T,
                     help="tokens of the prefill measurement (default 8192; with --experts E, 8192*E/896 keeps "
                          "the tokens per expert of the full layer, for small profiling captures)")
-    ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2, 3, 4],
+    ap.add_argument("--path", type=int, default=0, choices=[0, 1, 4],
                     help="kernel path (0 = the library's choice by token count; see k3moe_config.force_path)")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the shared-expert block, skewed-routing and stacked-layer measurements")

@@ -78,19 +78,18 @@ typedef struct {
   int max_tokens;  /* largest T a forward call may pass */
   int spin_timeout_ms; /* limit of any device-side wait; 0 selects 2000 ms */
   int force_path;  /* 0: the library's choice (path 4 for every T);
-                      1: CUDA-core kernels everywhere;
-                      2: tensor-core GEMM kernels (prefill-size batches);
-                      3: streaming tensor-core kernels (decode-size batches;
-                         dense projections by split-K for T <= 64; expert
-                         weights decoded to bf16 into tensor memory);
-                      4: as 3, with the expert GEMMs on the block-scaled
+                      1: CUDA-core kernels everywhere (an independent
+                         implementation kept as a cross-check);
+                      4: tensor-core dense projections (split-K for
+                         T <= 64) and the expert GEMMs on the block-scaled
                          MXFP4 tensor cores (e2m1 weights and e8m0 scales
                          as stored; up to T = 128 tcgen05 kind::mxf4 on
                          tiles of 16 token rows with the activations as six
                          block-scaled e2m1 terms, above that
-                         kind::mxf8f6f4 on tiles of 80 rows with two exact
+                         kind::mxf8f6f4 on tiles of 88 rows with two exact
                          e4m3 terms; the terms of a tile form one MMA
-                         operand) */
+                         operand).
+                      Other values: EINVAL. */
   /* Shared experts (kimi-k3-mlx README, "Architecture" table: 2 shared
    * experts on every token; "Porting notes" item 3: they act on the 7168-d
    * residual, not the latent; "Parameter budget": 12.2 B parameters, i.e.
@@ -98,7 +97,7 @@ typedef struct {
    * n_shared * shared_inter (a multiple of 128), the block output becomes
    *   y = bf16(y_routed + z),  z = bf16(W2s . bf16(SiTU(W1s . x, W3s . x)))
    * (the experts summed: one MLP over their concatenated intermediate).
-   * Needs force_path 0, 2 or 4. */
+   * Needs force_path 0 or 4. */
   int n_shared;
   int shared_inter;
   /* Expert shard (expert parallelism: Kimi-K3-Alis-MLX-Dynamic model card,
@@ -110,7 +109,7 @@ typedef struct {
    * weights stay whole.  A shard has no whole forward; it runs
    * k3moe_forward_partial, the callers sum the shards' partial combines
    * (one all-reduce), and k3moe_finish completes the block.  Needs
-   * force_path 0, 2 or 4. */
+   * force_path 0 or 4. */
   int expert_begin;
   int expert_count;
   /* Two-bank graded experts (kimi-k3-mlx README, "REAP expert pruning",
@@ -169,8 +168,8 @@ int k3moe_create(const k3moe_config* cfg, int cuda_device, k3moe_ctx** out);
 /* Copies the weights (host memory, checkpoint layout) to the device.  The
  * MXFP4 tensors are regrouped (values unchanged) into 128 x 128 blocks of
  * nibbles and 512-byte scale atoms for the block-scaled expert kernels
- * (path 4); contexts created with force_path 1, 2 or 3 also keep a copy in
- * 128-row x 64-column tiles for those paths' kernels.  Any scale byte equal
+ * (path 4); contexts created with force_path 1 also keep a copy in
+ * 128-row x 64-column tiles for the CUDA-core kernels.  Any scale byte equal
  * to 0xFF is rejected with EBADSCALE before anything is copied.  May be
  * called again to replace the weights.  Synchronous. */
 int k3moe_load_weights(k3moe_ctx* ctx, const k3moe_weights* w);
@@ -330,7 +329,7 @@ enum {
   K3MOE_Q_WORKSPACE_BYTES = 0, /* device workspace bytes                       */
   K3MOE_Q_WEIGHT_BYTES = 1,    /* device weight bytes                          */
   K3MOE_Q_LAUNCHES_LAST = 2,   /* kernels launched by the last forward          */
-  K3MOE_Q_PATH_LAST = 3,       /* path of the last forward (force_path values 1..4) */
+  K3MOE_Q_PATH_LAST = 3,       /* path of the last forward (1 or 4) */
   K3MOE_Q_DEVICE = 4           /* CUDA device ordinal                          */
 };
 
@@ -352,9 +351,9 @@ int k3moe_query(const k3moe_ctx* ctx, int what, long long* value);
 
 /* Per-step timing.  With profiling enabled, every later forward records a
  * CUDA event on its stream before its first launch and after each launch
- * group (router+down_proj, top-k, permute, gate/up, down, combine+RMSNorm,
- * up_proj; the tensor-core path's expert group also contains its tile-list
- * and gather kernels).  k3moe_profile_read waits for the events of the last
+ * group (router+down_proj, top-k + permute, tile list, latent terms,
+ * gate/up, down, second bank, combine+RMSNorm, up_proj; the groups a
+ * forward runs depend on T and the configuration).  k3moe_profile_read waits for the events of the last
  * forward and writes the elapsed milliseconds of each group to ms[0..max)
  * and the number of groups to *count; k3moe_profile_name gives the group's
  * name (a static string, "" out of range).  The events are also recorded

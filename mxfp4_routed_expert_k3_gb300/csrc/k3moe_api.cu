@@ -140,22 +140,23 @@ int check_config(const k3moe_config* c) {
   if (!(c->rms_eps >= 0.f) || !(c->beta > 0.f) || !(c->beta_lin > 0.f))
     return fail(nullptr, K3MOE_EINVAL, "beta, beta_lin must be > 0 and rms_eps >= 0");
   if (c->spin_timeout_ms < 0) return fail(nullptr, K3MOE_EINVAL, "spin_timeout_ms must be >= 0");
-  if (c->force_path < 0 || c->force_path > 4) return fail(nullptr, K3MOE_EINVAL, "force_path must be 0..4");
+  if (c->force_path != 0 && c->force_path != 1 && c->force_path != 4)
+    return fail(nullptr, K3MOE_EINVAL, "force_path must be 0, 1 or 4 (got %d)", c->force_path);
   if (c->n_shared < 0 || c->shared_inter < 0 || (c->n_shared > 0) != (c->shared_inter > 0))
     return fail(nullptr, K3MOE_EINVAL, "n_shared and shared_inter must both be 0 or both positive");
   if (c->n_shared > 0) {
     const long long Is = (long long)c->n_shared * c->shared_inter;
     if (Is % 128 || Is > (1 << 16))
       return fail(nullptr, K3MOE_EINVAL, "n_shared * shared_inter must be a multiple of 128 and <= 65536");
-    if (c->force_path == 1 || c->force_path == 3)
-      return fail(nullptr, K3MOE_EINVAL, "shared experts need force_path 0, 2 or 4 (tensor-core dense GEMMs)");
+    if (c->force_path == 1)
+      return fail(nullptr, K3MOE_EINVAL, "shared experts need force_path 0 or 4 (tensor-core dense GEMMs)");
   }
   if (c->expert_begin < 0 || c->expert_count < 0 || c->expert_begin + c->expert_count > c->n_experts ||
       (c->expert_count == 0 && c->expert_begin != 0))
     return fail(nullptr, K3MOE_EINVAL, "expert shard [%d, %d + %d) outside [0, n_experts=%d)", c->expert_begin,
                 c->expert_begin, c->expert_count, c->n_experts);
-  if (c->expert_count > 0 && c->expert_count < c->n_experts && (c->force_path == 1 || c->force_path == 3))
-    return fail(nullptr, K3MOE_EINVAL, "an expert shard needs force_path 0, 2 or 4");
+  if (c->expert_count > 0 && c->expert_count < c->n_experts && c->force_path == 1)
+    return fail(nullptr, K3MOE_EINVAL, "an expert shard needs force_path 0 or 4");
   if (c->bank2_begin < 0 || c->bank2_begin >= c->n_experts)
     return fail(nullptr, K3MOE_EINVAL, "bank2_begin must be 0 (one bank) or in [1, n_experts) (got %d)",
                 c->bank2_begin);
@@ -363,9 +364,9 @@ int k3moe_load_weights(k3moe_ctx* c, const k3moe_weights* wt) {
   K3_CUDA(c, cudaSetDevice(c->device), "cudaSetDevice");
   const size_t gu_bytes = E * (I / 128) * (L / 64) * 2 * (size_t)k3::kTileBytes;
   const size_t d_bytes = E * (L / 128) * (I / 64) * (size_t)k3::kTileBytes;
-  // The bf16-decode tile copy of the experts serves paths 1-3 only; the
+  // The tile copy of the experts serves the CUDA-core path (1) only; the
   // default (path 4) reads the block-scaled copy alone.
-  const bool want_tiles = c->cfg.force_path >= 1 && c->cfg.force_path <= 3;
+  const bool want_tiles = c->cfg.force_path == 1;
   if (!c->wcat) {
     K3_CUDA(c, cudaMalloc(&c->wcat, (Er + L) * H * 2), "cudaMalloc(router+down_proj)");
     K3_CUDA(c, cudaMalloc(&c->bias, Er * 4), "cudaMalloc(bias)");
@@ -537,15 +538,13 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
   const bool routed = c_in == nullptr;  // router, permutation, experts, combine
   const bool tail = c_out == nullptr;   // shared experts, RMSNorm, up_proj
   k3::Work& w = c->w;
-  // path: 1 CUDA-core kernels, 2 tensor-core GEMMs, 3 streaming tensor-core
-  // kernels (experts decoded to bf16 in TMEM), 4 as 3 with the experts on
-  // the block-scaled MXFP4 tensor cores
+  // path: 4 (default) tensor-core dense projections and the experts on the
+  // block-scaled MXFP4 tensor cores; 1 CUDA-core kernels everywhere (an
+  // independent implementation kept as a cross-check)
   int path = c->cfg.force_path;
   if (path == 0) path = 4;
   c->bs.withhold_item = c->test_withhold ? 0 : -1;
   c->test_withhold = false;  // one forward only
-  const bool stream = path == 3 || path == 4;
-  const bool big = path == 2;
   c->path_last = path;
   long long n = 0;
   cudaError_t e;
@@ -612,10 +611,7 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
   o_route.split = d.E;
   o_route.out_f32 = w.logits;
   o_route.out_bf16 = w.lat;
-  if (big) {
-    K3_LAUNCH(k3::umma_dense(c->umma, c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, o_route, s),
-              k3::umma_dense_launches(), "router + down_proj (tensor cores)");
-  } else if (stream && T <= 64) {
+  if (path == 4 && T <= 64) {
     K3_LAUNCH(k3::umma_dense_small(c->umma, c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, o_route, nullptr, s),
               k3::umma_dense_small_launches(), "router + down_proj");
   } else if (path == 4) {
@@ -625,16 +621,16 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
     K3_LAUNCH(k3::launch_dense_gemv(c->wcat, d.E + d.L, d.H, (const uint16_t*)x, T, d.E, w.logits, w.lat, s), 1,
               "router + down_proj");
   }
-  const bool fused_route = stream && T * d.K <= 1024;
+  const bool fused_route = path == 4 && T * d.K <= 1024;
   const int split_expert = c->bank2_begin ? c->bank2_begin : (1 << 30);
   if (fused_route) {
     int4* tiles;
     int* tile_count;
     int bn;
     k3::umma_tile_list(c->umma, &tiles, &tile_count, &bn);
-    // path 4 also needs the slot -> tile map (its tiles have bs_tile_rows(T) <= bn rows)
-    int* slot_tile = path == 4 ? k3::bs_slot_tile(c->bs) : nullptr;
-    if (path == 4) bn = k3::bs_tile_rows(T);
+    // with the slot -> tile map (the tiles have bs_tile_rows(T) <= bn rows)
+    int* slot_tile = k3::bs_slot_tile(c->bs);
+    bn = k3::bs_tile_rows(T);
     K3_LAUNCH(k3::launch_route_small(w.logits, T, d.E, c->bias, d.K, d.norm_topk, d.rsf, c->shard, idx, wts,
                                      w.counts, w.offsets, w.active, w.perm, w.slot, bn, tiles, tile_count, slot_tile,
                                      split_expert, s),
@@ -647,10 +643,7 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
   }
   const int max_active = std::min(d.E, T * d.K);
   int split_gu = 1, split_dn = 1;  // K parts of the T = 1 expert kernels
-  if (big) {
-    K3_LAUNCH(k3::umma_experts(c->umma, c->gu_tiles, c->d_tiles, w, T, d, s), k3::umma_expert_launches(),
-              "experts (tensor cores)");
-  } else if (path == 4) {
+  if (path == 4) {
     int4* tiles;
     int* tile_count;
     int bn;
@@ -679,13 +672,6 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
       K3_LAUNCH(k3::umma_bank2_experts(c->umma, c->gu2_tiles, c->d2_tiles, c->bank2_begin, d.E - c->bank2_begin, bn,
                                        w, T, d, s),
                 3, "second bank (2-bit)");
-  } else if (path == 3) {
-    if (fused_route)
-      K3_LAUNCH(k3::umma_stream_gather(c->umma, w, T, d, s), 1, "gather");
-    else
-      K3_LAUNCH(k3::umma_stream_prepare(c->umma, w, T, d, s), 2, "tile list + gather");
-    K3_LAUNCH(k3::umma_stream_gateup(c->umma, c->gu_tiles, w, T, d, s), 1, "gate/up");
-    K3_LAUNCH(k3::umma_stream_down(c->umma, c->d_tiles, w, T, d, s), 1, "down");
   } else {
     K3_LAUNCH(k3::launch_gateup_gemv(c->gu_tiles, w.lat, w.active, w.offsets, w.perm, max_active, d, w.h, s), 1,
               "gate/up");
@@ -718,10 +704,7 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
   k3::DenseOut o_up;
   o_up.out_bf16 = (uint16_t*)y;
   o_up.add_bf16 = c->Is ? c->sh_z : nullptr;
-  if (big) {
-    K3_LAUNCH(k3::umma_dense(c->umma, c->wu, d.H, d.L, w.n, T, o_up, s), k3::umma_dense_launches(),
-              "up_proj (tensor cores)");
-  } else if (stream && T <= 64) {
+  if (path == 4 && T <= 64) {
     K3_LAUNCH(k3::umma_dense_small(c->umma, c->wu, d.H, d.L, w.n, T, o_up, nullptr, s),
               k3::umma_dense_small_launches(), "up_proj");
   } else if (path == 4) {

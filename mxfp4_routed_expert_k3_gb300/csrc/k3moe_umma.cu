@@ -1,28 +1,25 @@
-// k3moe_umma.cu -- tensor-core path: tcgen05 MMA with fp32 accumulators in
-// tensor memory, operands staged in shared memory by TMA.
+// k3moe_umma.cu -- tcgen05 kernels with bf16 operands: MMA with fp32
+// accumulators in tensor memory, operands staged in shared memory by TMA.
 //
-// One kernel template serves three GEMMs, all written "weights x tokens":
-// D[m, n] = sum_k A[m, k] * B[n, k], A = a 128-row tile of a weight matrix
-// (M side of the MMA), B = up to 256 token rows (N side), K = the weight's
-// input dimension, both operands K-major, bf16, D fp32 [128 lanes x N].
-//   DENSE  : A is bf16 (router + down_proj fused, or up_proj), loaded by a
-//            2-D TMA with 128-byte swizzle.  Epilogue: fp32 logits for rows
-//            below `split`, bf16 for the rest, written transposed [n, m].
-//   GATEUP : A is MXFP4 (w1 and w3 tiles of one expert, adjacent in memory),
-//            copied by a 1-D bulk TMA, decoded exactly to bf16 in shared
-//            memory by a warpgroup, two accumulators (gate, up); epilogue
-//            SiTU-GLU -> h (bf16) per expert slot.
-//   DOWN   : A is MXFP4 (w2 tile), one accumulator; epilogue o (fp32).
-// For the grouped GEMMs the token rows of an expert are contiguous (slot
-// order) and a device-built tile list gives, per tile, the expert, the first
-// row and the row count.
+//   umma_gemm_kernel         the dense projections at T > 64 (router +
+//                            down_proj fused, up_proj, the shared experts):
+//                            D[m, n] = sum_k W[m, k] X[n, k], a 128-row
+//                            weight block (M side) x up to 256 token rows (N
+//                            side), both K-major; epilogue by a DenseOut rule
+//                            (fp32 logits / bf16 latent, SiTU-GLU pairs, an
+//                            added term).
+//   umma_dense_stream_kernel the same projections at T <= 64: split-K over
+//   + dense_reduce_kernel    all SMs, fp32 partials, ordered reduction.
+//   bank2_gemm_kernel        the second bank's 2-bit experts above decode
+//                            sizes (decoded exactly to bf16 hi + lo).
+// plus the tile-list builders the grouped expert kernels read.
 //
-// Warp roles (192 threads): warp 0 issues the TMA copies, warp 1 (one lane)
-// issues the MMAs, warps 2..5 (a full warpgroup, so that warp w reads TMEM
-// lanes 32*(w%4)..+31) decode MXFP4 tiles and then run the epilogue.
-// Every wait on an mbarrier is bounded: past the limit the kernel records a
-// status bit, raises a shared abort flag that releases the other roles,
-// waits (bounded) for its own copies in flight, frees TMEM and returns.
+// Warp roles: warp 0 issues the TMA copies, one lane of warp 1 issues the
+// MMAs, a warpgroup (warp w reads TMEM lanes 32*(w%4)..+31) runs the
+// epilogue.  Every wait on an mbarrier is bounded: past the limit the kernel
+// records a status bit, raises a shared abort flag that releases the other
+// roles, waits (bounded) for its own copies in flight, frees TMEM and
+// returns.
 #include <cuda.h>
 
 #include <algorithm>
@@ -36,10 +33,7 @@ namespace k3 {
 
 constexpr int kBM = 128;        // weight rows per tile (MMA M)
 constexpr int kBK = 64;         // input columns per stage (one 128-byte swizzle row of bf16)
-constexpr int kBNMax = 192;     // token rows per tile (MMA N, multiple of 16)
 constexpr int kThreads = 192;
-
-enum Mode { DENSE = 0, GATEUP = 1, DOWN = 2 };
 
 // Second-bank (2-bit affine) tile: 128 weight rows x 64 input columns of
 // one matrix -- row r's 64 codes (four per byte, low bits first) at
@@ -53,28 +47,20 @@ constexpr int kTile2MaxRows = 96;  // token rows of a second-bank tile's box at 
 // accumulation step, so a long K loop into one accumulator loses more than
 // an fp32 FMA chain.  kAcc accumulators take the K steps in turn (each sees
 // K/(16*kAcc) steps) and the epilogue adds them with round-to-nearest fp32.
-template <int MODE>
-struct Cfg {
-  static constexpr bool kGU = MODE == GATEUP;  // gate and up: two accumulators
-  static constexpr bool kDown = MODE == DOWN;
-  static constexpr int kNumMat = kGU ? 2 : 1;
-  static constexpr int kNumA = kNumMat;
-  // Dense: 256 token rows per tile (an MMA instruction costs about the pipe
-  // time of an N = 256 one whatever its N), K split over two accumulators.
-  static constexpr int kBN = (MODE == DENSE) ? 256 : kBNMax;
-  static constexpr int kABytes = kBM * kBK * 2;                 // 16 KB per A tile
-  static constexpr int kBBytes = kBN * kBK * 2;
-  static constexpr int kSrcTile = kTileBytes;                   // stored tile of one matrix
-  static constexpr int kStageBytesRaw = (MODE == DENSE) ? 0 : kNumMat * kSrcTile;
-  static constexpr int kStaging = (kStageBytesRaw + 1023) / 1024 * 1024;
-  static constexpr int kStageBytes = kNumA * kABytes + kBBytes + kStaging;
-  static constexpr int kStages = kGU ? 3 : 4;
-  static constexpr int kAcc = (MODE == DENSE || kDown) ? 2 : 1;
-  static constexpr int kAccStride = 256;  // TMEM columns between accumulators
-  static constexpr int kMatStride = 256;  // TMEM columns between gate and up
+// Tiles of 256 token rows (an MMA instruction costs about the pipe time of
+// an N = 256 one whatever its N).
+struct GCfg {
+  static constexpr int kBN = 256;                  // token rows per tile (MMA N)
+  static constexpr int kABytes = kBM * kBK * 2;    // 16 KB
+  static constexpr int kBBytes = kBN * kBK * 2;    // 32 KB
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = 4;
+  static constexpr int kAcc = 2;
+  static constexpr int kAccStride = 256;           // TMEM columns between accumulators
   static constexpr int kTmemCols = 512;
   static constexpr int kSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
-  static_assert(kNumMat * kAcc * kAccStride <= kTmemCols || kGU, "TMEM budget");
+  static_assert(kAcc * kAccStride <= kTmemCols, "TMEM budget");
+  static_assert(kSmem <= 232448, "shared memory budget");
 };
 
 // One output element of a dense projection (DenseOut, glu == 0).
@@ -112,59 +98,48 @@ struct TileList {
 
 struct Params {
   // operand sources
-  const uint8_t* a_tiles;  // MXFP4 tiles (GATEUP / DOWN) or 2-bit tiles (second bank)
+  const uint8_t* a_tiles;  // second bank: 2-bit tiles
   int expert_base;         // weight index of a tile = its expert id - expert_base
   int MT;                  // weight row tiles per matrix
   int KS;                  // K / 64
   int M;                   // weight rows (DENSE edge masking)
   // token tiling
-  TileList list;           // GATEUP / DOWN
+  TileList list;           // second bank
   int T, tn;               // DENSE: tokens and rows per tile; second bank: token box rows
   // epilogue
   DenseOut dout;           // DENSE
-  float* out_f32;          // DOWN: o per slot
-  uint16_t* out_bf16;      // GATEUP: h per slot
-  int ld_out;              // GATEUP: I, DOWN: L (row length of h / o)
+  float* out_f32;          // second bank down: o per slot
+  uint16_t* out_bf16;      // second bank gate/up: h per slot
+  int ld_out;              // I or L (row length of h / o)
   float beta, beta_lin;
   unsigned* status;
   uint64_t limit_ns;
 };
 
-template <int MODE>
+// Dense projection of a token tile: D = W[mt block] . X[tile]^T over K,
+// one CTA per (128-row block, token tile).  Warp 0 issues the 2-D TMA copies
+// of both operands, one lane of warp 1 the MMAs (K steps alternating over
+// kAcc accumulators), warps 2..5 the epilogue (DenseOut rule).
 __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                                                                 const __grid_constant__ CUtensorMap map_b,
                                                                 const Params p) {
-  using C = Cfg<MODE>;
+  using C = GCfg;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
-  // bars: [0, S) full_tma, [S, 2S) full_a, [2S, 3S) empty, [3S] tmem_full
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * C::kStages + 1);
+  // bars: [0, S) full, [S, 2S) empty, [2S] tmem_full
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.x;
-
-  // ---- which token tile
-  int e = 0, row0 = 0, rows = 0, n_mma = 0;
-  if (MODE == DENSE) {
-    row0 = blockIdx.y * p.tn;
-    rows = min(p.tn, p.T - row0);
-    n_mma = (rows + 15) & ~15;
-  } else {
-    const int ti = (int)blockIdx.y + (p.list.begin ? *p.list.begin : 0);
-    if (ti >= *p.list.count) return;
-    const int4 t = p.list.tiles[ti];
-    e = t.x - p.expert_base;
-    row0 = t.y;
-    rows = t.z;
-    n_mma = t.w;
-  }
+  const int row0 = blockIdx.y * p.tn;
+  const int rows = min(p.tn, p.T - row0);
+  const int n_mma = (rows + 15) & ~15;
   if (rows <= 0) return;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 3 * C::kStages + 1; ++s)
-      mbar_init(smem_u32(bars + s), (s >= C::kStages && s < 2 * C::kStages) ? 128u : 1u);
+    for (int s = 0; s < 2 * C::kStages + 1; ++s) mbar_init(smem_u32(bars + s), 1u);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -174,38 +149,29 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Guard g{abort_flag, p.status, p.limit_ns};
-  auto full_tma = [&](int s) { return smem_u32(bars + s); };
-  auto full_a = [&](int s) { return smem_u32(bars + C::kStages + s); };
-  auto empty = [&](int s) { return smem_u32(bars + 2 * C::kStages + s); };
-  const uint32_t tmem_full = smem_u32(bars + 3 * C::kStages);
-  auto stage_a = [&](int s, int i) { return smem + (size_t)s * C::kStageBytes + i * C::kABytes; };
-  auto stage_b = [&](int s) { return smem + (size_t)s * C::kStageBytes + C::kNumA * C::kABytes; };
-  auto stage_stg = [&](int s) { return smem + (size_t)s * C::kStageBytes + C::kNumA * C::kABytes + C::kBBytes; };
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto empty = [&](int s) { return smem_u32(bars + C::kStages + s); };
+  const uint32_t tmem_full = smem_u32(bars + 2 * C::kStages);
+  auto stage_a = [&](int s) { return smem + (size_t)s * C::kStageBytes; };
+  auto stage_b = [&](int s) { return smem + (size_t)s * C::kStageBytes + C::kABytes; };
 
   if (warp == 0) {
     // ================= TMA producer
     int issued = 0;
     if (lane == 0) {
-      const uint32_t tx = C::kBBytes + (MODE == DENSE ? C::kABytes : C::kNumMat * C::kSrcTile);
-      const uint8_t* a_src =
-          (MODE == DENSE) ? nullptr : p.a_tiles + ((size_t)(e * p.MT + mt) * p.KS) * C::kNumMat * C::kSrcTile;
       for (int ks = 0; ks < p.KS; ++ks) {
         const int s = ks % C::kStages, u = ks / C::kStages;
         if (u > 0 && !mbar_wait(empty(s), (u - 1) & 1, g, 1u)) break;
-        mbar_expect_tx(full_tma(s), tx);
-        tma_load_2d(smem_u32(stage_b(s)), &map_b, full_tma(s), ks * kBK, row0);
-        if (MODE == DENSE)
-          tma_load_2d(smem_u32(stage_a(s, 0)), &map_a, full_tma(s), ks * kBK, mt * kBM);
-        else
-          bulk_load(smem_u32(stage_stg(s)), a_src + (size_t)ks * C::kNumMat * C::kSrcTile,
-                    C::kNumMat * C::kSrcTile, full_tma(s));
+        mbar_expect_tx(full(s), C::kABytes + C::kBBytes);
+        tma_load_2d(smem_u32(stage_b(s)), &map_b, full(s), ks * kBK, row0);
+        tma_load_2d(smem_u32(stage_a(s)), &map_a, full(s), ks * kBK, mt * kBM);
         ++issued;
       }
       if (*abort_flag) {
         // let our own copies land before the CTA's shared memory goes away
         for (int ks = max(0, issued - C::kStages); ks < issued; ++ks) {
           const uint64_t t0 = global_ns();
-          while (!mbar_try_wait(full_tma(ks % C::kStages), (ks / C::kStages) & 1))
+          while (!mbar_try_wait(full(ks % C::kStages), (ks / C::kStages) & 1))
             if (global_ns() - t0 > p.limit_ns) break;
         }
       }
@@ -217,22 +183,15 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
       const uint32_t idesc = umma_idesc_bf16(kBM, n_mma);
       bool ok = true;
       for (int ks = 0; ks < p.KS && ok; ++ks) {
-        const int s = ks % C::kStages, par = (ks / C::kStages) & 1;
-        ok = mbar_wait(full_tma(s), par, g, 2u);
-        if (ok && MODE != DENSE) ok = mbar_wait(full_a(s), par, g, 4u);
-        if (!ok) break;
+        const int s = ks % C::kStages;
+        if (!(ok = mbar_wait(full(s), (ks / C::kStages) & 1, g, 2u))) break;
         tc_fence_after();
-        const uint32_t b0 = smem_u32(stage_b(s));
-        const int acc_k = ks % C::kAcc;
+        const uint32_t a0 = smem_u32(stage_a(s)), b0 = smem_u32(stage_b(s));
+        const uint32_t acc_col = (uint32_t)((ks % C::kAcc) * C::kAccStride);
 #pragma unroll
-        for (int i = 0; i < C::kNumA; ++i) {
-          const uint32_t a0 = smem_u32(stage_a(s, i));
-          const uint32_t acc_col = (uint32_t)(i * C::kMatStride + acc_k * C::kAccStride);
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_bf16(tmem + acc_col, umma_desc_sw128(a0 + kk * 32), umma_desc_sw128(b0 + kk * 32), idesc,
-                      (ks >= C::kAcc || kk) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          umma_bf16(tmem + acc_col, umma_desc_sw128(a0 + kk * 32), umma_desc_sw128(b0 + kk * 32), idesc,
+                    (ks >= C::kAcc || kk) ? 1u : 0u);
         umma_commit(empty(s));
       }
       umma_commit(tmem_full);
@@ -245,40 +204,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
     }
     __syncwarp();
   } else {
-    // ================= decode (MXFP4) + epilogue warpgroup
-    const int wg_t = threadIdx.x - 64;  // 0..127
-    if (MODE != DENSE) {
-      const int r = wg_t;  // row of the 128-row tile this thread decodes
-      for (int ks = 0; ks < p.KS; ++ks) {
-        const int s = ks % C::kStages, par = (ks / C::kStages) & 1;
-        if (!mbar_wait(full_tma(s), par, g, 8u)) break;
-        const uint8_t* stg = stage_stg(s);
-#pragma unroll
-        for (int i = 0; i < C::kNumA; ++i) {
-          const uint8_t* tile = stg + i * kTileBytes;
-          const uint4 c0 = *reinterpret_cast<const uint4*>(tile + (size_t)r * 16);
-          const uint4 c1 = *reinterpret_cast<const uint4*>(tile + (size_t)(128 + r) * 16);
-          const uint32_t sc = *reinterpret_cast<const uint16_t*>(tile + kTilePackedBytes + 2 * r);
-          const ScaleMul m0 = scale_multipliers(sc & 0xFFu), m1 = scale_multipliers(sc >> 8);
-          uint8_t* arow = stage_a(s, i) + (size_t)r * 128;
-          const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            uint32_t o[4];
-            tile_word_to_bf16(words[q], q < 4 ? m0 : m1, o);
-            *reinterpret_cast<uint4*>(arow + ((q ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-          }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(full_a(s));
-      }
-    }
-    // ---- epilogue
+    // ================= epilogue (warps 2..5: TMEM lane quarter warp % 4)
     if (mbar_wait(tmem_full, 0, g, 16u) && !*abort_flag) {
       tc_fence_after();
       const int quarter = warp & 3;
-      const int m_local = quarter * 32 + lane;
-      const int m = mt * kBM + m_local;
+      const int m = mt * kBM + quarter * 32 + lane;
       const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
       // accumulators that hold a part of the sum: every K accumulator that
       // received at least one k step
@@ -292,25 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
 #pragma unroll
           for (int j = 0; j < 32; ++j) acc[j] += part[j];
         }
-        if (C::kGU) {
-          float up[32];
-          tmem_ld32(lane_addr + C::kMatStride + j0, up);
-          for (int a = 1; a < n_acc; ++a) {
-            float part[32];
-            tmem_ld32(lane_addr + C::kMatStride + a * C::kAccStride + j0, part);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) up[j] += part[j];
-          }
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j0 + j < rows)
-              p.out_bf16[(size_t)(row0 + j0 + j) * p.ld_out + m] =
-                  f32_to_bf16(situ_fast(acc[j], up[j], p.beta, p.beta_lin));
-        } else if (C::kDown) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j0 + j < rows) p.out_f32[(size_t)(row0 + j0 + j) * p.ld_out + m] = acc[j];
-        } else if (p.dout.glu) {
+        if (p.dout.glu) {
           // gate/up row pairs sit in neighbouring lanes of this warp
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -319,12 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
               p.dout.out_bf16[(size_t)(row0 + j0 + j) * (p.M >> 1) + (m >> 1)] =
                   f32_to_bf16(situ_fast(acc[j], partner, p.dout.beta, p.dout.beta_lin));
           }
-        } else {
-          if (m < p.M) {
+        } else if (m < p.M) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j0 + j < rows) dense_store1(p.dout, p.M, row0 + j0 + j, m, acc[j]);
-          }
+          for (int j = 0; j < 32; ++j)
+            if (j0 + j < rows) dense_store1(p.dout, p.M, row0 + j0 + j, m, acc[j]);
         }
       }
     }
@@ -599,239 +509,8 @@ __global__ void __launch_bounds__(B2Cfg<GU>::kThreads, 1)
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// =====================================================================
-// Streaming expert kernel for small token counts per expert (decode).
-// Persistent: each CTA walks the work items (tile, 128-row block) with
-// stride gridDim.x; the TMA ring runs across item boundaries, so every SM
-// keeps ~(kSStages-1) stages of weight bytes in flight.  The decoded bf16
-// weights go to TENSOR MEMORY (tcgen05.st) and the MMA reads A from there
-// (tcgen05.mma ... [d], [a_tmem], b_desc): the 4x-expanded weights never
-// touch shared memory, and the decode costs the same per weight whatever
-// the number of tokens (N = 16 or 32).  Tokens: up to kSNB rows of the
-// slot-ordered activation matrix per tile, one 2-D TMA box per stage.
-// TMEM (256 columns per CTA, two CTAs per SM):
-//   GATEUP: D gate [0, 32), D up [32, 64), A slots at 64 + 64 t (t < 3;
-//           gate half then up half, 32 columns each)
-//   DOWN  : D [0, 32), A slots at 32 + 32 t (t < 4)
-// A in TMEM for kind::f16, M = 128: row m in lane m, two consecutive bf16
-// (k even in the low half) per 32-bit column, 8 columns per K = 16.
-// =====================================================================
-constexpr int kSNB = 32;  // max token rows per streaming tile
 constexpr int kMinTileRows = 16;  // the shortest tile height any tile list uses
-// producer warp, MMA warp, two decode warpgroups (one per scale group of a K step)
-constexpr int kSThreads = 320;
 constexpr int kDThreads = 192;
-
-template <int MODE>
-struct SCfg {
-  static constexpr int kNumA = (MODE == GATEUP) ? 2 : 1;
-  static constexpr int kBBytes = kSNB * kBK * 2;  // 4 KB, 1024-aligned
-  static constexpr int kStg = (kNumA * kTileBytes + 1023) / 1024 * 1024;
-  static constexpr int kStageBytes = kBBytes + kStg;
-  static constexpr int kStages = (MODE == GATEUP) ? 7 : 9;
-  static constexpr int kSlots = (MODE == GATEUP) ? 3 : 4;
-  static constexpr int kSlotCols = kNumA * 32;
-  static constexpr int kDCols = kNumA * kSNB;
-  // padded so that at most two CTAs fit on an SM (two x 256 TMEM columns)
-  static constexpr int kSmem = 94 * 1024;
-  static_assert(kStages * kStageBytes + 1024 + 512 <= kSmem, "ring does not fit");
-  static_assert(kDCols + kSlots * kSlotCols <= 256, "TMEM budget");
-};
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t v[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
-      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
-      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t v[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-      : "memory");
-}
-__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
-                                                 uint32_t acc) {
-  asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(
-          d_tmem),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
-template <int MODE>
-__global__ void __launch_bounds__(kSThreads, 2) umma_stream_kernel(const __grid_constant__ CUtensorMap map_b,
-                                                                   const Params p) {
-  using C = SCfg<MODE>;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
-  // bars: full[S], free[S], a_ready[NS], a_free[NS], tmem_full
-  const int NB = 2 * C::kStages + 2 * C::kSlots + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NB);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  const int n_items = *p.list.count * p.MT;
-  if ((int)blockIdx.x >= n_items) return;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < NB; ++i) {
-      const bool is_ready = i >= 2 * C::kStages && i < 2 * C::kStages + C::kSlots;
-      mbar_init(smem_u32(bars + i), is_ready ? 256u : 1u);
-    }
-    *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 256);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const Guard g{abort_flag, p.status, p.limit_ns};
-  auto full = [&](int s) { return smem_u32(bars + s); };
-  auto sfree = [&](int s) { return smem_u32(bars + C::kStages + s); };
-  auto a_ready = [&](int t) { return smem_u32(bars + 2 * C::kStages + t); };
-  auto a_free = [&](int t) { return smem_u32(bars + 2 * C::kStages + C::kSlots + t); };
-  const uint32_t tmem_full = smem_u32(bars + 2 * C::kStages + 2 * C::kSlots);
-  auto stage_b = [&](int s) { return smem + (size_t)s * C::kStageBytes; };
-  auto stage_stg = [&](int s) { return smem + (size_t)s * C::kStageBytes + C::kBBytes; };
-  auto slot_col = [&](int t) { return (uint32_t)(C::kDCols + t * C::kSlotCols); };
-
-  if (warp == 0) {
-    // ================= TMA producer
-    if (lane == 0) {
-      const uint32_t tx = C::kBBytes + C::kNumA * kTileBytes;
-      int kg = 0, issued = 0;
-      bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const int4 tile = p.list.tiles[item / p.MT];
-        const int mt = item - (item / p.MT) * p.MT;
-        const uint8_t* a_src = p.a_tiles + ((size_t)(tile.x * p.MT + mt) * p.KS) * C::kNumA * kTileBytes;
-        for (int ks = 0; ks < p.KS; ++ks, ++kg) {
-          const int s = kg % C::kStages, u = kg / C::kStages;
-          if (u > 0 && !mbar_wait(sfree(s), (u - 1) & 1, g, 1u)) {
-            ok = false;
-            break;
-          }
-          mbar_expect_tx(full(s), tx);
-          tma_load_2d(smem_u32(stage_b(s)), &map_b, full(s), ks * kBK, tile.y);
-          bulk_load(smem_u32(stage_stg(s)), a_src + (size_t)ks * C::kNumA * kTileBytes, C::kNumA * kTileBytes,
-                    full(s));
-          ++issued;
-        }
-      }
-      if (*abort_flag) {
-        for (int k = max(0, issued - C::kStages); k < issued; ++k) {
-          const uint64_t t0 = global_ns();
-          while (!mbar_try_wait(full(k % C::kStages), (k / C::kStages) & 1))
-            if (global_ns() - t0 > p.limit_ns) break;
-        }
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ================= MMA issuer
-    if (lane == 0) {
-      int kg = 0, done = 0;
-      bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const int4 tile = p.list.tiles[item / p.MT];
-        const uint32_t idesc = umma_idesc_bf16(kBM, tile.w);
-        for (int ks = 0; ks < p.KS; ++ks, ++kg) {
-          const int s = kg % C::kStages, t = kg % C::kSlots;
-          ok = mbar_wait(full(s), (kg / C::kStages) & 1, g, 2u) &&
-               mbar_wait(a_ready(t), (kg / C::kSlots) & 1, g, 4u);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t b0 = smem_u32(stage_b(s));
-#pragma unroll
-          for (int i = 0; i < C::kNumA; ++i)
-#pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)
-              umma_bf16_tmem_a(tmem + i * kSNB, tmem + slot_col(t) + i * 32 + kk * 8,
-                               umma_desc_sw128(b0 + kk * 32), idesc, (ks | kk) ? 1u : 0u);
-          umma_commit(sfree(s));
-          umma_commit(a_free(t));
-        }
-        if (ok) {
-          umma_commit(tmem_full);
-          ++done;
-        }
-      }
-      if (!ok) {
-        // MMAs already issued must finish before TMEM is released
-        umma_commit(tmem_full);
-        const uint64_t t0 = global_ns();
-        while (!mbar_try_wait(tmem_full, done & 1))
-          if (global_ns() - t0 > p.limit_ns) break;
-      }
-    }
-    __syncwarp();
-  } else {
-    // ================= decode to TMEM (warps 2..9) + epilogue (warps 2..5)
-    // warpgroup grp decodes scale group grp (input columns 32 grp .. +31) of
-    // every K step: 16 TMEM columns per matrix.
-    const int quarter = warp & 3;
-    const int grp = (warp - 2) >> 2;
-    const int r = quarter * 32 + lane;  // tile row == TMEM lane
-    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    int kg = 0, it = 0;
-    bool ok = true;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
-      const int4 tile = p.list.tiles[item / p.MT];
-      const int mt = item - (item / p.MT) * p.MT;
-      for (int ks = 0; ks < p.KS; ++ks, ++kg) {
-        const int s = kg % C::kStages, t = kg % C::kSlots, ut = kg / C::kSlots;
-        ok = mbar_wait(full(s), (kg / C::kStages) & 1, g, 8u) && (ut == 0 || mbar_wait(a_free(t), (ut - 1) & 1, g, 32u));
-        if (!ok) break;
-        const uint8_t* stg = stage_stg(s);
-#pragma unroll
-        for (int i = 0; i < C::kNumA; ++i) {
-          const uint8_t* tl = stg + i * kTileBytes;
-          const uint4 c = *reinterpret_cast<const uint4*>(tl + (size_t)(grp * 128 + r) * 16);
-          uint32_t v[16];
-          group_to_bf16(c, tl[kTilePackedBytes + 2 * r + grp], v);
-          tmem_st16(lane_base + slot_col(t) + i * 32 + grp * 16, v);
-        }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        tc_fence_before();
-        mbar_arrive(a_ready(t));
-      }
-      if (!ok || grp != 0) continue;
-      // epilogue of this item (warpgroup 0)
-      ok = mbar_wait(tmem_full, it & 1, g, 16u) && !*abort_flag;
-      if (!ok) break;
-      tc_fence_after();
-      const int m = mt * kBM + r;
-      float acc[32];
-      tmem_ld32(lane_base + 0, acc);
-      if (MODE == GATEUP) {
-        float up[32];
-        tmem_ld32(lane_base + kSNB, up);
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < tile.z)
-            p.out_bf16[(size_t)(tile.y + j) * p.ld_out + m] = f32_to_bf16(situ_fast(acc[j], up[j], p.beta, p.beta_lin));
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < tile.z) p.out_f32[(size_t)(tile.y + j) * p.ld_out + m] = acc[j];
-      }
-      tc_fence_before();
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, 256);
-}
 
 // =====================================================================
 // Streaming dense GEMM for small T (decode): D = W . X^T with W bf16
@@ -1185,7 +864,7 @@ struct UmmaWs {
 constexpr int kMaxChunks = kReduceMaxChunks;  // split-K chunks of the small-T dense GEMM
 
 // Workspace carve-up; sizes are bounds for any T <= max_tokens:
-//   tiles: at most T*K/kSNB + (experts with work) entries (kSNB is the
+//   tiles: at most T*K/kMinTileRows + (experts with work) entries (kMinTileRows is the
 //          smallest tile height used), lat_perm: T*K rows of L,
 //   part : kMaxChunks * kDNB * max(E + L, H) fp32 partial sums.
 struct WsLayout {
@@ -1216,33 +895,13 @@ UmmaWs ws_view(const UmmaPlan& p, const Dims& d, int max_tokens) {
   return w;
 }
 
-template <int MODE>
-cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const Params& prm, dim3 grid, cudaStream_t s) {
-  constexpr int smem = Cfg<MODE>::kSmem;
-  static_assert(smem <= 232448, "shared memory budget");
-  umma_gemm_kernel<MODE><<<grid, kThreads, smem, s>>>(ma, mb, prm);
-  return cudaGetLastError();
-}
-
 }  // namespace
 
 cudaError_t prepare_umma_kernels() {
-  cudaError_t e0 = cudaFuncSetAttribute(umma_dense_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        DCfg::kSmem);
-  if (e0 != cudaSuccess) return e0;
-  e0 = cudaFuncSetAttribute(umma_stream_kernel<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        SCfg<GATEUP>::kSmem);
-  if (e0 == cudaSuccess)
-    e0 = cudaFuncSetAttribute(umma_stream_kernel<DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              SCfg<DOWN>::kSmem);
-  if (e0 != cudaSuccess) return e0;
-  cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Cfg<DENSE>::kSmem);
+  cudaError_t e = cudaFuncSetAttribute(umma_dense_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       DCfg::kSmem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(umma_gemm_kernel<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<GATEUP>::kSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(umma_gemm_kernel<DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<DOWN>::kSmem);
+    e = cudaFuncSetAttribute(umma_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GCfg::kSmem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(bank2_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              B2Cfg<true>::kSmem);
@@ -1257,22 +916,18 @@ UmmaPlan umma_plan(const Dims& d, int max_tokens) {
   p.max_tokens = max_tokens;
   p.dims = d;
   p.ws_bytes = ws_layout(d, max_tokens).total;
-  p.enabled = true;
-  p.min_tokens = 128;
   return p;
 }
 
-bool umma_path_enabled(const UmmaPlan& p, const Dims&, int T) { return p.enabled && T >= p.min_tokens; }
 
 int umma_dense_launches() { return 1; }
-int umma_expert_launches() { return 4; }
 
 cudaError_t umma_dense(const UmmaPlan& p, const uint16_t* W, int M, int K, const uint16_t* X, int T,
                        const DenseOut& o, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   if (o.glu && (M % 2 || !o.out_bf16)) return cudaErrorInvalidValue;
   CUtensorMap ma, mb;
-  constexpr int BN = Cfg<DENSE>::kBN;
+  constexpr int BN = GCfg::kBN;
   if (!make_map(&ma, W, M, K, kBM) || !make_map(&mb, X, T, K, BN)) return cudaErrorInvalidValue;
   const int ntile = (T + BN - 1) / BN;
   const int per = (T + ntile - 1) / ntile;
@@ -1286,60 +941,10 @@ cudaError_t umma_dense(const UmmaPlan& p, const uint16_t* W, int M, int K, const
   prm.status = p.status;
   prm.limit_ns = p.limit_ns;
   const int ny = (T + prm.tn - 1) / prm.tn;
-  return launch_gemm<DENSE>(ma, mb, prm, dim3(prm.MT, ny), s);
-}
-
-cudaError_t umma_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8_t* d_tiles, const Work& w, int T,
-                         const Dims& d, cudaStream_t s) {
-  const int TK = T * d.K;
-  if (TK <= 0) return cudaSuccess;
-  UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
-  const int max_tiles = TK / kBNMax + std::min(d.E, TK) + 1;
-  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, kBNMax, ws.tiles, ws.count, nullptr, 1 << 30);
-  gather_rows_kernel<<<152 * 8, 256, 0, s>>>(w.lat, w.perm, TK, d.K, d.L, ws.lat_perm);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  CUtensorMap mb1, mb2;
-  if (!make_map(&mb1, ws.lat_perm, TK, d.L, kBNMax) || !make_map(&mb2, w.h, TK, d.I, kBNMax))
-    return cudaErrorInvalidValue;
-  Params g{};
-  g.a_tiles = gu_tiles;
-  g.MT = d.I / kBM;
-  g.KS = d.L / kBK;
-  g.M = d.I;
-  g.list = TileList{ws.tiles, ws.count};
-  g.out_bf16 = w.h;
-  g.ld_out = d.I;
-  g.beta = d.beta;
-  g.beta_lin = d.beta_lin;
-  g.status = p.status;
-  g.limit_ns = p.limit_ns;
-  e = launch_gemm<GATEUP>(mb1, mb1, g, dim3(g.MT, max_tiles), s);
-  if (e != cudaSuccess) return e;
-  Params dn = g;
-  dn.a_tiles = d_tiles;
-  dn.MT = d.L / kBM;
-  dn.KS = d.I / kBK;
-  dn.M = d.L;
-  dn.out_bf16 = nullptr;
-  dn.out_f32 = w.o;
-  dn.ld_out = d.L;
-  return launch_gemm<DOWN>(mb2, mb2, dn, dim3(dn.MT, max_tiles), s);
-}
-
-// Decode-size experts: tiles of at most kSNB rows, streamed by persistent
-// CTAs (two per SM) with the decoded weights in TMEM.  Three launch groups:
-// the tile list + slot-ordered latent rows, then gate/up, then down.
-cudaError_t umma_stream_prepare(const UmmaPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s) {
-  const int TK = T * d.K;
-  if (TK <= 0) return cudaSuccess;
-  UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
-  build_tiles_kernel<<<1, 1024, 0, s>>>(w.active, w.offsets, kSNB, ws.tiles, ws.count, nullptr, 1 << 30);
-  gather_rows_kernel<<<152 * 2, 256, 0, s>>>(w.lat, w.perm, TK, d.K, d.L, ws.lat_perm);
+  umma_gemm_kernel<<<dim3(prm.MT, ny), kThreads, GCfg::kSmem, s>>>(ma, mb, prm);
   return cudaGetLastError();
 }
 
-// Only the tile list (tiles of at most bn_max rows) and the slot -> tile map.
 // slot -> (tile << 8 | row) for every row of every tile: one warp per tile,
 // its rows' entries written together (consecutive slots).
 __global__ void __launch_bounds__(256) slot_tile_kernel(const int4* __restrict__ tiles, const int* __restrict__ count,
@@ -1430,70 +1035,13 @@ cudaError_t umma_bank2_experts(const UmmaPlan& p, const uint8_t* gu2_tiles, cons
   return cudaGetLastError();
 }
 
-// Only the slot-ordered latent rows (the tile list was built by the fused
-// small-batch routing kernel).
-cudaError_t umma_stream_gather(const UmmaPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s) {
-  const int TK = T * d.K;
-  if (TK <= 0) return cudaSuccess;
-  UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
-  gather_rows_kernel<<<152 * 2, 256, 0, s>>>(w.lat, w.perm, TK, d.K, d.L, ws.lat_perm);
-  return cudaGetLastError();
-}
-
 void umma_tile_list(const UmmaPlan& p, int4** tiles, int** count, int* bn_max) {
   UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
   *tiles = ws.tiles;
   *count = ws.count;
-  *bn_max = kSNB;
+  *bn_max = kMinTileRows;
 }
 
-static Params stream_params(const UmmaPlan& p, const Dims& d, const UmmaWs& ws) {
-  Params g{};
-  g.list = TileList{ws.tiles, ws.count};
-  g.beta = d.beta;
-  g.beta_lin = d.beta_lin;
-  g.status = p.status;
-  g.limit_ns = p.limit_ns;
-  return g;
-}
-
-cudaError_t umma_stream_gateup(const UmmaPlan& p, const uint8_t* gu_tiles, const Work& w, int T, const Dims& d,
-                               cudaStream_t s) {
-  const int TK = T * d.K;
-  if (TK <= 0) return cudaSuccess;
-  UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
-  CUtensorMap mb;
-  if (!make_map(&mb, ws.lat_perm, TK, d.L, kSNB)) return cudaErrorInvalidValue;
-  Params g = stream_params(p, d, ws);
-  g.a_tiles = gu_tiles;
-  g.MT = d.I / kBM;
-  g.KS = d.L / kBK;
-  g.M = d.I;
-  g.out_bf16 = w.h;
-  g.ld_out = d.I;
-  umma_stream_kernel<GATEUP><<<2 * p.num_sms, kSThreads, SCfg<GATEUP>::kSmem, s>>>(mb, g);
-  return cudaGetLastError();
-}
-
-cudaError_t umma_stream_down(const UmmaPlan& p, const uint8_t* d_tiles, const Work& w, int T, const Dims& d,
-                             cudaStream_t s) {
-  const int TK = T * d.K;
-  if (TK <= 0) return cudaSuccess;
-  UmmaWs ws = ws_view(p, p.dims, p.max_tokens);
-  CUtensorMap mb;
-  if (!make_map(&mb, w.h, TK, d.I, kSNB)) return cudaErrorInvalidValue;
-  Params g = stream_params(p, d, ws);
-  g.a_tiles = d_tiles;
-  g.MT = d.L / kBM;
-  g.KS = d.I / kBK;
-  g.M = d.L;
-  g.out_f32 = w.o;
-  g.ld_out = d.L;
-  umma_stream_kernel<DOWN><<<2 * p.num_sms, kSThreads, SCfg<DOWN>::kSmem, s>>>(mb, g);
-  return cudaGetLastError();
-}
-
-// Small-T dense GEMM (T <= kDNB): split-K streaming kernel + ordered reduce.
 size_t dense_small_part_floats(int M) { return (size_t)kMaxChunks * kDNB * (size_t)M; }
 int umma_dense_small_launches() { return 2; }
 

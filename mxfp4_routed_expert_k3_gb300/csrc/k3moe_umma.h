@@ -1,6 +1,6 @@
-// k3moe_umma.h -- the tensor-core (tcgen05 / TMEM / TMA) path used for
-// larger token counts: dense bf16 GEMMs (router + down_proj, up_proj) and
-// the grouped MXFP4 expert GEMMs.
+// k3moe_umma.h -- tcgen05 kernels with bf16 operands: the dense projections
+// (router + down_proj, up_proj, shared experts) at every T, the second
+// bank's 2-bit experts above decode sizes, and the expert tile lists.
 #pragma once
 #include <cstddef>
 #include <cstdint>
@@ -28,8 +28,6 @@ struct DenseOut {
 };
 
 struct UmmaPlan {
-  bool enabled = false;   // false: every forward uses the CUDA-core kernels
-  int min_tokens = 1 << 30;
   int max_tokens = 0;
   size_t ws_bytes = 256;  // workspace this path needs (tile list, slot-ordered latent rows)
   void* ws = nullptr;
@@ -41,7 +39,6 @@ struct UmmaPlan {
 
 cudaError_t prepare_umma_kernels();
 UmmaPlan umma_plan(const Dims& d, int max_tokens);
-bool umma_path_enabled(const UmmaPlan& p, const Dims& d, int T);
 cudaError_t umma_dense(const UmmaPlan& p, const uint16_t* W, int M, int K, const uint16_t* X, int T,
                        const DenseOut& o, cudaStream_t s);
 int umma_dense_launches();
@@ -52,10 +49,6 @@ cudaError_t umma_dense_small(const UmmaPlan& p, const uint16_t* W, int M, int K,
                              const DenseOut& o, float* part, cudaStream_t s);
 int umma_dense_small_launches();
 size_t dense_small_part_floats(int M);
-cudaError_t umma_experts(const UmmaPlan& p, const uint8_t* gu_tiles, const uint8_t* d_tiles, const Work& w, int T,
-                         const Dims& d, cudaStream_t s);
-int umma_expert_launches();
-cudaError_t umma_stream_prepare(const UmmaPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s);
 // Tile list over the experts with work (tiles of at most bn_max slots),
 // slot -> tile map, and count[1] = the tiles of experts below split_expert
 // (they come first).
@@ -68,12 +61,8 @@ cudaError_t bank2_tiles(const uint8_t* q, const uint16_t* sc, const uint16_t* bi
 size_t bank2_tile_bytes(int rows, int cols);  // one matrix of one expert
 cudaError_t umma_bank2_experts(const UmmaPlan& p, const uint8_t* gu2_tiles, const uint8_t* d2_tiles, int bank2_begin,
                                int n_bank2, int tile_rows, const Work& w, int T, const Dims& d, cudaStream_t s);
-cudaError_t umma_stream_gather(const UmmaPlan& p, const Work& w, int T, const Dims& d, cudaStream_t s);
-// where the streaming kernels read their tile list (and the tile height)
+// where the grouped expert kernels read their tile list (and the shortest
+// tile height any list uses)
 void umma_tile_list(const UmmaPlan& p, int4** tiles, int** count, int* bn_max);
-cudaError_t umma_stream_gateup(const UmmaPlan& p, const uint8_t* gu_tiles, const Work& w, int T, const Dims& d,
-                               cudaStream_t s);
-cudaError_t umma_stream_down(const UmmaPlan& p, const uint8_t* d_tiles, const Work& w, int T, const Dims& d,
-                             cudaStream_t s);
 
 }  // namespace k3

@@ -125,7 +125,7 @@ def _check(rc: int, ctx=None):
         raise K3Error(rc, last_error(ctx))
 
 
-PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_STREAM, PATH_BLOCK_SCALED = 0, 1, 2, 3, 4
+PATH_AUTO, PATH_CUDA_CORE, PATH_BLOCK_SCALED = 0, 1, 4
 
 
 def make_config(d: LayerDims, max_tokens: int, spin_timeout_ms: int = 0, force_path: int = 0,

@@ -62,6 +62,12 @@ def test_create_rejects_bad_config(L):
         h = C.c_void_p()
         rc = L.k3moe_create(C.byref(k3moe.make_config(d, 16, force_path=path)), 0, C.byref(h))
         assert rc == k3moe.EINVAL and word in k3moe.last_error(), (d, path, k3moe.last_error())
+    # kernel paths: 0 (the library's choice), 1 (CUDA cores) and 4 only
+    for path in (-1, 2, 3, 5):
+        h = C.c_void_p()
+        rc = L.k3moe_create(C.byref(k3moe.make_config(TINY, 16, force_path=path)), 0, C.byref(h))
+        assert rc == k3moe.EINVAL and "force_path" in k3moe.last_error(), (path, k3moe.last_error())
+        assert h.value is None
 
 
 def test_create_without_gpu_reports_cuda_error(L):

@@ -23,16 +23,15 @@ def k3weights():
     return synth.layer_weights(K3, seed=1)
 
 
-@pytest.fixture(scope="module", params=[k3moe.PATH_TENSOR_CORE, k3moe.PATH_BLOCK_SCALED],
-                ids=["tensorcore", "blockscaled"])
+@pytest.fixture(scope="module", params=[k3moe.PATH_BLOCK_SCALED], ids=["blockscaled"])
 def k3layer(request, k3weights):
     layer = k3moe.Layer(K3, k3weights, max_tokens=MAXT, force_path=request.param)
     yield k3weights, layer
     layer.close()
 
 
-@pytest.fixture(scope="module", params=[k3moe.PATH_CUDA_CORE, k3moe.PATH_STREAM, k3moe.PATH_BLOCK_SCALED],
-                ids=["cudacore", "stream", "blockscaled"])
+@pytest.fixture(scope="module", params=[k3moe.PATH_CUDA_CORE, k3moe.PATH_BLOCK_SCALED],
+                ids=["cudacore", "blockscaled"])
 def k3decode(request, k3weights):
     layer = k3moe.Layer(K3, k3weights, max_tokens=64, force_path=request.param)
     yield k3weights, layer
@@ -114,7 +113,7 @@ def test_k3_prefill_8192(k3layer):
     _sampled(layer, w, x, 128, 1, "prefill T=8192")
 
 
-@pytest.mark.parametrize("path", [k3moe.PATH_TENSOR_CORE, k3moe.PATH_BLOCK_SCALED], ids=["tensorcore", "blockscaled"])
+@pytest.mark.parametrize("path", [k3moe.PATH_BLOCK_SCALED], ids=["blockscaled"])
 def test_k3_skewed_4096(path):
     w = synth.layer_weights(K3, seed=3, n_hot=32)
     hot = synth.hot_experts(K3, 3, 32)

@@ -49,7 +49,7 @@ def check(S_gpu, S_ref, label):
         f"{label}: max rel {np.max(np.abs(S_gpu - S_ref) / np.maximum(S_ref, 1e-30)):.3e}"
 
 
-@pytest.mark.parametrize("path", [k3moe.PATH_AUTO, k3moe.PATH_TENSOR_CORE], ids=["auto", "tensorcore"])
+@pytest.mark.parametrize("path", [k3moe.PATH_AUTO, k3moe.PATH_CUDA_CORE], ids=["auto", "cudacore"])
 def test_tiny_saliency_over_two_batches(path):
     d = TINY
     w = synth.layer_weights(d, seed=10)

@@ -58,7 +58,7 @@ def branch_terms(ref):
     return (z, bf16_f64(ref["y"]) - z)
 
 
-@pytest.fixture(scope="module", params=[k3moe.PATH_AUTO, k3moe.PATH_TENSOR_CORE], ids=["auto", "tensorcore"])
+@pytest.fixture(scope="module", params=[k3moe.PATH_AUTO], ids=["auto"])
 def tiny_shared(request):
     d = TINY_SHARED
     w = synth.layer_weights(d, seed=8)

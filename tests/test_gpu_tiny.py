@@ -18,9 +18,7 @@ MAXT = 320
 
 
 @pytest.fixture(scope="module",
-                params=[k3moe.PATH_AUTO, k3moe.PATH_CUDA_CORE, k3moe.PATH_TENSOR_CORE, k3moe.PATH_STREAM,
-                        k3moe.PATH_BLOCK_SCALED],
-                ids=["auto", "cudacore", "tensorcore", "stream", "blockscaled"])
+                params=[k3moe.PATH_AUTO, k3moe.PATH_CUDA_CORE], ids=["auto", "cudacore"])
 def tiny(request):
     d = TINY
     w = synth.layer_weights(d, seed=0)
