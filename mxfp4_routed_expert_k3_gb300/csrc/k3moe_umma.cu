@@ -81,6 +81,17 @@ __device__ __forceinline__ void dense_store4(const DenseOut& o, int M, int t, in
     *reinterpret_cast<uint32_t*>(o.out_bf16 + (size_t)t * (M >> 1) + (m >> 1)) = h;
     return;
   }
+  if (o.add_bf16 && m >= o.split && !(o.split & 3) && !((M - o.split) & 3)) {
+    // bf16 rows with an added term: its four values in one load, before
+    // the store (four loads behind four stores would run one by one)
+    const size_t i = (size_t)t * (M - o.split) + (m - o.split);
+    const uint2 ad = *reinterpret_cast<const uint2*>(o.add_bf16 + i);
+    const float2 a01 = unpack_bf16x2(ad.x), a23 = unpack_bf16x2(ad.y);
+    auto r = [](float v, float add) { return bf16_to_f32(f32_to_bf16(bf16_to_f32(f32_to_bf16(v)) + add)); };
+    *reinterpret_cast<uint2*>(o.out_bf16 + i) =
+        make_uint2(pack_bf16x2(r(a.x, a01.x), r(a.y, a01.y)), pack_bf16x2(r(a.z, a23.x), r(a.w, a23.y)));
+    return;
+  }
   dense_store1(o, M, t, m, a.x);
   dense_store1(o, M, t, m + 1, a.y);
   dense_store1(o, M, t, m + 2, a.z);
@@ -231,6 +242,22 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gemm_kernel(const __grid_con
               p.dout.out_bf16[(size_t)(row0 + j0 + j) * (p.M >> 1) + (m >> 1)] =
                   f32_to_bf16(situ_fast(acc[j], partner, p.dout.beta, p.dout.beta_lin));
           }
+        } else if (m < p.M && p.dout.add_bf16 && m >= p.dout.split) {
+          // the added term's 32 values loaded before any store (the output
+          // and the added tensor are both bf16 arrays, so loads placed
+          // after stores would wait for them one by one)
+          const int Mb = p.M - p.dout.split;
+          float addv[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            addv[j] = (j0 + j < rows)
+                          ? bf16_to_f32(p.dout.add_bf16[(size_t)(row0 + j0 + j) * Mb + (m - p.dout.split)])
+                          : 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j0 + j < rows)
+              p.dout.out_bf16[(size_t)(row0 + j0 + j) * Mb + (m - p.dout.split)] =
+                  f32_to_bf16(bf16_to_f32(f32_to_bf16(acc[j])) + addv[j]);
         } else if (m < p.M) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
