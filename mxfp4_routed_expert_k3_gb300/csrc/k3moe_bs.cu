@@ -172,9 +172,11 @@ constexpr int kQuantChunks = 4;
 __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, const int* __restrict__ perm, int K, int rows,
                                   const int* __restrict__ rows_dev, int C, int rows_max,
                                   const int* __restrict__ slot_tile, int stack, uint8_t* __restrict__ q,
-                                  uint8_t* __restrict__ sf, const int* __restrict__ slot_of) {
+                                  uint8_t* __restrict__ sf, const int* __restrict__ slot_of,
+                                  int* __restrict__ sched) {
   pdl_trigger();
   pdl_wait();
+  if (sched && blockIdx.x == 0 && threadIdx.x == 0) sched[0] = sched[1] = 0;  // the expert kernels' item counters
   // slot_of: rows are tokens, each split once and written to its K slots
   // slot_of[t * K + k] (those below *rows_dev with an expert shard)
   const int slot_lim = (slot_of && rows_dev) ? *rows_dev : 0x7FFFFFFF;
@@ -264,9 +266,10 @@ template <int CH>
 __global__ void quant_rows_fp4_kernel(const uint16_t* __restrict__ src, const int* __restrict__ perm, int K, int rows,
                                       const int* __restrict__ rows_dev, int C, int rows_max,
                                       const int* __restrict__ slot_tile, int stack, uint8_t* __restrict__ q,
-                                      uint8_t* __restrict__ sf) {
+                                      uint8_t* __restrict__ sf, int* __restrict__ sched) {
   pdl_trigger();
   pdl_wait();
+  if (sched && blockIdx.x == 0 && threadIdx.x == 0) sched[0] = sched[1] = 0;  // the expert kernels' item counters
   if (rows_dev) rows = min(rows, *rows_dev);  // an expert shard: its own slots only
   const int hl = threadIdx.x & 15, half = (threadIdx.x >> 4) & 1;
   const int KC = C / kQK;
@@ -497,6 +500,10 @@ struct BsParams {
   unsigned* status;
   uint64_t limit_ns;
   int withhold_item;   // test hook: the stage of this work item's first k step gets no copies (-1: none)
+  // Work distribution: CTA b takes item b first, then the next unclaimed
+  // item from this counter (zero when the kernel starts); NULL: items b,
+  // b + gridDim.x, ...
+  int* next_item;
   // K split (decode tiles): each (tile, row block) is n_split work items over
   // consecutive ranges of the K steps; with n_split > 1 the epilogue writes
   // fp32 partial sums (GATEUP: gate to part_a, up to part_b; DOWN: o to
@@ -536,6 +543,10 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
   constexpr int NB = 2 * C::kStages + 5;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NB);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // the work item of each ring stage (copy thread -> MMA thread) and of
+  // each accumulator buffer (MMA thread -> epilogue); -1 ends the work
+  volatile int* stage_item = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  volatile int* acc_item = stage_item + C::kStages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   pdl_trigger();
@@ -546,7 +557,10 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
   if (threadIdx.x == 0) {
     for (int i = 0; i < NB; ++i) {
       const bool is_empty = i >= 2 * C::kStages + 2 && i < 2 * C::kStages + 4;
-      mbar_init(smem_u32(bars + i), is_empty ? 32u * C::kEpiWarps : 1u);
+      // dfull: the MMAs' commit and the MMA thread's own arrival (which
+      // publishes the buffer's item id)
+      const bool is_dfull = i >= 2 * C::kStages && i < 2 * C::kStages + 2;
+      mbar_init(smem_u32(bars + i), is_empty ? 32u * C::kEpiWarps : is_dfull ? 2u : 1u);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -569,7 +583,7 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
     if (lane == 0) {
       int kg = 0, issued = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      for (int item = blockIdx.x; item < n_items && ok;) {
         const BsItem bi = bs_item(p, item);
         const int ti = bi.ti, mt = bi.mt;
         const int4 tile = p.tiles[ti];
@@ -587,6 +601,7 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
           // or at prefill (row block, kc) and (row block + 1, kc), KC tiles apart
           const int n_sfa = (MODE == BS_GATEUP || C::kRB == 2) ? 2 : nk;
           const size_t first = (MODE == BS_GATEUP) ? (tile0 + kc0) * 2 : tile0 + kc0;
+          stage_item[s] = item;  // published by the arrival below
           if (item == p.withhold_item && ks == bi.k0) {
             // test hook: this stage's full barrier never completes, so the
             // MMA issuer's bounded wait runs out and the CTA aborts
@@ -612,6 +627,15 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
           bulk_load(st + C::kOffSfb, p.sfb + ((size_t)ti * p.KC + kc0) * 2 * kAtom, 2 * nk * kAtom, full(s));
           ++issued;
         }
+        if (ok) item = p.next_item ? (int)gridDim.x + atomicAdd(p.next_item, 1) : item + (int)gridDim.x;
+      }
+      if (ok) {
+        // the end of the work: a stage without copies whose item is -1
+        const int s = kg % C::kStages, u = kg / C::kStages;
+        if (u == 0 || mbar_wait(sfree(s), (u - 1) & 1, g, 1u)) {
+          stage_item[s] = -1;
+          mbar_arrive(full(s));
+        }
       }
       if (*abort_flag) {
         for (int k = max(0, issued - C::kStages); k < issued; ++k) {
@@ -636,11 +660,24 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
       const uint64_t sfb_base = sf_desc(st0 + C::kOffSfb);
       int kg = 0, it = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
+      for (;; ++it) {
+        // the item's first stage names it
+        if (!mbar_wait(full(kg % C::kStages), (kg / C::kStages) & 1, g, 4u)) {
+          ok = false;
+          break;
+        }
+        const int item = stage_item[kg % C::kStages];
         const int buf = (C::kDBuf == 2) ? (it & 1) : 0;
         const int use = (C::kDBuf == 2) ? (it >> 1) : it;  // earlier uses of this buffer
         if (use > 0 && !mbar_wait(dempty(buf), (use - 1) & 1, g, 2u)) {
           ok = false;
+          break;
+        }
+        if (item < 0) {
+          // no more work: the end goes on to the epilogue
+          acc_item[buf] = -1;
+          mbar_arrive(dfull(buf));
+          mbar_arrive(dfull(buf));
           break;
         }
         tc_fence_after();
@@ -649,7 +686,7 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
         const BsItem bi = bs_item(p, item);
         for (int ks = bi.k0; ks < bi.k1; ++ks, ++kg) {
           const int s = kg % C::kStages;
-          if (!mbar_wait(full(s), (kg / C::kStages) & 1, g, 4u)) {
+          if (ks > bi.k0 && !mbar_wait(full(s), (kg / C::kStages) & 1, g, 4u)) {
             ok = false;
             break;
           }
@@ -704,6 +741,8 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
           umma_commit(sfree(s));
         }
         if (!ok) break;
+        acc_item[buf] = item;
+        mbar_arrive(dfull(buf));
         umma_commit(dfull(buf));
       }
       if (!ok) {
@@ -723,12 +762,13 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
     constexpr int kWG = C::kEpiWarps / 4;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    int it = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+    for (int it = 0;; ++it) {
       const int buf = (C::kDBuf == 2) ? (it & 1) : 0;
       const int use = (C::kDBuf == 2) ? (it >> 1) : it;
       if (!mbar_wait(dfull(buf), use & 1, g, 8u)) break;
       tc_fence_after();
+      const int item = acc_item[buf];
+      if (item < 0) break;
       const BsItem bi = bs_item(p, item);
       const int ti = bi.ti, mt = bi.mt;
       const int4 tile = p.tiles[ti];
@@ -1440,6 +1480,7 @@ struct BsWs {
   int* slot_tile;     // [rows_max]: tile << 8 | row within the tile
   float* part;        // K-split partial sums (T = 1): kBsMaxSplit planes of K rows of I (gate), I (up), L (down)
   float *xsum, *hsum; // second bank at decode sizes: per-64-column latent sums by token, per-32-row h sums by slot
+  int* sched;         // the expert kernels' item counters (gate/up, down), zeroed by the quantiser
   size_t total;
 };
 BsWs bs_ws_view(void* base, const Dims& d, int max_tokens) {
@@ -1449,24 +1490,25 @@ BsWs bs_ws_view(void* base, const Dims& d, int max_tokens) {
   // tiles hold at least one slot and at most one expert: <= E + R / 16 whatever the tile height
   const size_t MT = (size_t)d.E + R / 16 + 1;
   auto terms = [&](size_t C) { return std::max(2 * R * C, (size_t)kFp4Terms * Rf * C / 2); };
-  const size_t sizes[8] = {terms(d.L),
+  const size_t sizes[9] = {terms(d.L),
                            MT * (d.L / kQK) * 2 * kAtom,
                            terms(d.I),
                            MT * (d.I / kQK) * 2 * kAtom,
                            R * sizeof(int),
                            (size_t)kBsMaxSplit * d.K * (2 * d.I + d.L) * sizeof(float),
                            (size_t)std::min(max_tokens, kBsDecodeMaxT) * (d.L / 64) * sizeof(float),
-                           Rf * (d.I / 32) * sizeof(float)};
+                           Rf * (d.I / 32) * sizeof(float),
+                           2 * sizeof(int)};
   uint8_t* b = static_cast<uint8_t*>(base);
-  uint8_t* ptr[8];
+  uint8_t* ptr[9];
   size_t off = 0;
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < 9; ++i) {
     ptr[i] = b ? b + off : nullptr;
     off += up(sizes[i]);
   }
   return BsWs{(int)R,  (int)Rf, (int)MT, ptr[0], ptr[1], ptr[2], ptr[3], reinterpret_cast<int*>(ptr[4]),
               reinterpret_cast<float*>(ptr[5]), reinterpret_cast<float*>(ptr[6]), reinterpret_cast<float*>(ptr[7]),
-              off};
+              reinterpret_cast<int*>(ptr[8]), off};
 }
 
 template <int MODE, int NQ>
@@ -1549,11 +1591,11 @@ cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims
     const long long th = (long long)T * ((d.L / kQK + kQuantChunks - 1) / kQuantChunks);
     const int tb = (int)std::min<long long>((th * 16 + 255) / 256, 8LL * p.num_sms);
     return launch_pdl(quant_rows_kernel, tb, 256, 0, s, w.lat, (const int*)nullptr, d.K, T, n_local, d.L,
-                      ws.rows_max, (const int*)ws.slot_tile, stack, ws.lq, ws.lsf, (const int*)w.slot);
+                      ws.rows_max, (const int*)ws.slot_tile, stack, ws.lq, ws.lsf, (const int*)w.slot, ws.sched);
   }
   auto kernel = ch == 1 ? quant_rows_fp4_kernel<1> : quant_rows_fp4_kernel<kQuantChunks>;
   return launch_pdl(kernel, blocks, 256, 0, s, w.lat, w.perm, d.K, TK, n_local, d.L, ws.rows_fp4, ws.slot_tile, stack,
-                    ws.lq, ws.lsf);
+                    ws.lq, ws.lsf, ws.sched);
 }
 
 // Best K split for `items` decode work items of `ks` K steps over `ctas`
@@ -1664,6 +1706,7 @@ cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* t
   prm.part_rows = TK;
   prm.part_a = ws.part;
   prm.part_b = ws.part + (size_t)kBsMaxSplit * d.K * d.I;
+  prm.next_item = ws.sched;
   if (tile_rows == kBsDecodeRows && n_split > 1) {
     cudaError_t e = launch_bs<BS_GATEUP, kBsDecodeRows>(p, bw.gu_q, bw.gu_sf, bw.n_exp, d.I, d.L, ws.lq, ws.lsf,
                                                         ws.rows_fp4, tiles, tile_count, prm, s);
@@ -1696,6 +1739,7 @@ cudaError_t bs_stream_down(const BsPlan& p, const BsWeights& bw, const int4* til
   prm.n_split = n_split;
   prm.part_rows = TK;
   prm.part_a = ws.part + (size_t)kBsMaxSplit * d.K * 2 * d.I;  // the combine adds the parts
+  prm.next_item = ws.sched + 1;
   if (tile_rows == kBsDecodeRows)
     return launch_bs<BS_DOWN, kBsDecodeRows>(p, bw.d_q, bw.d_sf, bw.n_exp, d.L, d.I, ws.hq, ws.hsf, ws.rows_fp4, tiles,
                                              tile_count, prm, s);
