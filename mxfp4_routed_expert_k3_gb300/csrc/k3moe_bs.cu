@@ -260,94 +260,100 @@ __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, const int* _
 // The same for decode-size tiles (`stack` rows): kFp4Terms e2m1 terms
 // q[C/128][kFp4Terms][rows_max][64] (two codes per byte, low nibble first)
 // and their scales at act_scale_byte(t, n, stack) + g of the tile's first
-// atom.  CH chunks per half warp: one for the few rows of the smallest
-// batches (more warps, shorter chains), four otherwise.
-template <int CH>
-__global__ void quant_rows_fp4_kernel(const uint16_t* __restrict__ src, const int* __restrict__ perm, int K, int rows,
-                                      const int* __restrict__ rows_dev, int C, int rows_max,
-                                      const int* __restrict__ slot_tile, int stack, uint8_t* __restrict__ q,
-                                      uint8_t* __restrict__ sf, int* __restrict__ sched) {
+// atom, for every slot of the token (slot_of[t * K + k], those below
+// *rows_dev with an expert shard).  One CTA per (token, 16 chunks): each
+// half warp of the first 256 threads splits one 128-column chunk (8
+// columns per lane, 4 lanes per scale group) into shared memory; then each
+// of the 384 threads owns one 16-byte piece (chunk, term, quarter of the
+// 64-byte row) and stores it for every slot of the token (K <= 32).
+constexpr int kTokChunks = 16;
+constexpr int kTokThreads = kTokChunks * kFp4Terms * 4;
+__global__ void __launch_bounds__(kTokThreads) quant_tok_fp4_kernel(const uint16_t* __restrict__ src, int K, int C,
+                                                            const int* __restrict__ rows_dev, int rows_max,
+                                                            const int* __restrict__ slot_tile, int stack,
+                                                            uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
+                                                            const int* __restrict__ slot_of,
+                                                            int* __restrict__ sched) {
+  __shared__ __align__(16) uint32_t wq[kTokChunks][kFp4Terms][16];  // term words: [chunk][term][lane]
+  __shared__ uint32_t wsc[kTokChunks][kFp4Terms];                   // the chunk's four scale bytes per term
+  __shared__ int s_sl[32], s_tk[32];
   pdl_trigger();
   pdl_wait();
-  if (sched && blockIdx.x == 0 && threadIdx.x == 0) sched[0] = sched[1] = 0;  // the expert kernels' item counters
-  if (rows_dev) rows = min(rows, *rows_dev);  // an expert shard: its own slots only
-  const int hl = threadIdx.x & 15, half = (threadIdx.x >> 4) & 1;
-  const int KC = C / kQK;
-  const int KG = (KC + CH - 1) / CH;  // chunk groups per row
-  const long long nwork = (long long)rows * KG;
-  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-  for (long long wi = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; 2 * wi < nwork; wi += nwarps) {
-    const long long i = 2 * wi + half;
-    const bool valid = i < nwork;
-    const int s = valid ? (int)(i / KG) : 0, kg = valid ? (int)(i - (long long)s * KG) : 0;
-    uint4 v[CH];
-    int tn = 0;
-    if (valid) {
-      const int t = perm ? perm[s] / K : s;
-      tn = slot_tile[s];
+  if (sched && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+    sched[0] = sched[1] = 0;  // the expert kernels' item counters
+  const int t = blockIdx.x, kc0 = blockIdx.y * kTokChunks;
+  const int KC = C / kQK, nc = min(kTokChunks, KC - kc0);
+  const int slot_lim = rows_dev ? *rows_dev : 0x7FFFFFFF;
+  if (threadIdx.x < K) {
+    const int sl = slot_of[(size_t)t * K + threadIdx.x];
+    s_sl[threadIdx.x] = sl;
+    s_tk[threadIdx.x] = sl < slot_lim ? slot_tile[sl] : 0;
+  }
+  const int hw = threadIdx.x >> 4, hl = threadIdx.x & 15;
+  const uint32_t base_lane = threadIdx.x & 16;
+  const int kc = kc0 + hw;
+  // (warps past the first eight only store)
+  if (threadIdx.x < 256) {
+    const uint4 v = hw < nc ? *reinterpret_cast<const uint4*>(src + (size_t)t * C + kc * kQK + hl * 8)
+                            : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float x[8];
 #pragma unroll
-      for (int c = 0; c < CH; ++c) {
-        const int kc = kg * CH + c;
-        v[c] = kc < KC ? *reinterpret_cast<const uint4*>(src + (size_t)t * C + kc * kQK + hl * 8)
-                       : make_uint4(0u, 0u, 0u, 0u);
-      }
-    } else {
-#pragma unroll
-      for (int c = 0; c < CH; ++c) v[c] = make_uint4(0u, 0u, 0u, 0u);
+    for (int j = 0; j < 4; ++j) {
+      x[2 * j] = __uint_as_float(w[j] << 16);
+      x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
     }
 #pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      const int kc = kg * CH + c;
-      const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
-      float x[8];
+    for (int tt = 0; tt < kFp4Terms; ++tt) {
+      uint32_t mb = 0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        x[2 * j] = __uint_as_float(w[j] << 16);
-        x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-      }
-      uint32_t words[kFp4Terms], scw[kFp4Terms];
-      const uint32_t base_lane = threadIdx.x & 16;
+      for (int j = 0; j < 8; ++j) mb = max(mb, __float_as_uint(fabsf(x[j])));
+      mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
+      mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
+      const uint32_t sb = e2m1_scale_byte(mb);
+      uint32_t word = 0;
+      if (sb == 255u) {
 #pragma unroll
-      for (int t = 0; t < kFp4Terms; ++t) {
-        uint32_t mb = 0;
+        for (int j = 0; j < 8; ++j) x[j] = 0.f;
+      } else {
+        const float inv = exp2_any(127 - (int)sb), scl = exp2_any((int)sb - 127);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) mb = max(mb, __float_as_uint(fabsf(x[j])));
-        mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
-        mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
-        const uint32_t sb = e2m1_scale_byte(mb);
-        uint32_t word = 0;
-        if (sb == 255u) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) x[j] = 0.f;
-        } else {
-          const float inv = exp2_any(127 - (int)sb), scl = exp2_any((int)sb - 127);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t b = to_e2m1x2(x[2 * j + 1] * inv, x[2 * j] * inv);
-            const float2 d = from_e2m1x2(b);
-            x[2 * j] = fmaf(-d.x, scl, x[2 * j]);
-            x[2 * j + 1] = fmaf(-d.y, scl, x[2 * j + 1]);
-            word |= b << (8 * j);
-          }
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t b = to_e2m1x2(x[2 * j + 1] * inv, x[2 * j] * inv);
+          const float2 d = from_e2m1x2(b);
+          x[2 * j] = fmaf(-d.x, scl, x[2 * j]);
+          x[2 * j + 1] = fmaf(-d.y, scl, x[2 * j + 1]);
+          word |= b << (8 * j);
         }
-        words[t] = word;
-        // the four groups' scale bytes of this (slot, chunk) and term: one word at lane 0 of the half warp
-        uint32_t ws = 0;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) ws |= __shfl_sync(0xFFFFFFFFu, sb, base_lane + 4 * g) << (8 * g);
-        scw[t] = ws;
       }
-      if (!valid || kc >= KC) continue;
+      // the four groups' scale bytes of this chunk and term, gathered in one word
+      uint32_t ws = 0;
 #pragma unroll
-      for (int t = 0; t < kFp4Terms; ++t)
-        *reinterpret_cast<uint32_t*>(q + (((size_t)kc * kFp4Terms + t) * rows_max + s) * 64 + hl * 4) = words[t];
-      if (hl == 0) {
-        const int n = tn & 0xFF;
-        uint8_t* atom = sf + (((size_t)(tn >> 8) * KC + kc) * 2) * kAtom;
-#pragma unroll
-        for (int t = 0; t < kFp4Terms; ++t)
-          *reinterpret_cast<uint32_t*>(atom + act_atom_byte(t * stack + n)) = scw[t];
+      for (int g4 = 0; g4 < 4; ++g4) ws |= __shfl_sync(0xFFFFFFFFu, sb, base_lane + 4 * g4) << (8 * g4);
+      if (hw < nc) {
+        wq[hw][tt][hl] = word;
+        if (hl == 0) wsc[hw][tt] = ws;
       }
+    }
+  }
+  __syncthreads();
+  // this thread's piece: chunk c, term tt, bytes 16 part .. 16 part + 15 of the 64-byte row
+  const int part = threadIdx.x & 3, tt = (threadIdx.x >> 2) % kFp4Terms, c = threadIdx.x / (4 * kFp4Terms);
+  if (c >= nc) return;
+  const uint4 piece = *reinterpret_cast<const uint4*>(&wq[c][tt][part * 4]);
+  uint8_t* qrow = q + ((size_t)(kc0 + c) * kFp4Terms + tt) * rows_max * 64 + part * 16;
+  for (int k = 0; k < K; ++k) {
+    const int sl = s_sl[k];
+    if (sl < slot_lim) *reinterpret_cast<uint4*>(qrow + (size_t)sl * 64) = piece;
+  }
+  // the scale words: (chunk c, term tt) of every slot, at the slot's tile atom
+  if (part == 0) {
+    const uint32_t sw = wsc[c][tt];
+    for (int k = 0; k < K; ++k) {
+      if (s_sl[k] >= slot_lim) continue;
+      const int tk = s_tk[k];
+      uint8_t* atom = sf + (((size_t)(tk >> 8) * KC + kc0 + c) * 2) * kAtom;
+      *reinterpret_cast<uint32_t*>(atom + act_atom_byte(tt * stack + (tk & 0xFF))) = sw;
     }
   }
 }
@@ -1582,9 +1588,6 @@ cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims
   const int stack = tile_rows;
   const BsWs ws = bs_ws_view(p.ws, d, p.max_tokens);
   const bool fp4 = tile_rows == kBsDecodeRows && BsCfg<BS_GATEUP, kBsDecodeRows>::kFp4;
-  const int ch = (fp4 && TK <= 8 * d.K) ? 1 : kQuantChunks;  // chunks per half warp
-  const long long halves = (long long)TK * ((d.L / kQK + ch - 1) / ch);
-  const int blocks = (int)std::min<long long>((halves * 16 + 255) / 256, 8LL * p.num_sms);
   if (!fp4) {
     // prefill tiles: each token's row split once, its terms written to the
     // token's K slots (the split is ALU work, the copies a memory stream)
@@ -1593,9 +1596,13 @@ cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims
     return launch_pdl(quant_rows_kernel, tb, 256, 0, s, w.lat, (const int*)nullptr, d.K, T, n_local, d.L,
                       ws.rows_max, (const int*)ws.slot_tile, stack, ws.lq, ws.lsf, (const int*)w.slot, ws.sched);
   }
-  auto kernel = ch == 1 ? quant_rows_fp4_kernel<1> : quant_rows_fp4_kernel<kQuantChunks>;
-  return launch_pdl(kernel, blocks, 256, 0, s, w.lat, w.perm, d.K, TK, n_local, d.L, ws.rows_fp4, ws.slot_tile, stack,
-                    ws.lq, ws.lsf, ws.sched);
+  // decode tiles: each token's row split once, its six terms written to
+  // the token's K slots (K <= 32)
+  if (d.K > 32 || d.L % kQK) return cudaErrorInvalidValue;
+  const dim3 grid(T, (d.L / kQK + kTokChunks - 1) / kTokChunks);
+  return launch_pdl(quant_tok_fp4_kernel, grid, kTokThreads, 0, s, (const uint16_t*)w.lat, d.K, d.L, n_local,
+                    ws.rows_fp4,
+                    (const int*)ws.slot_tile, stack, ws.lq, ws.lsf, (const int*)w.slot, ws.sched);
 }
 
 // Best K split for `items` decode work items of `ks` K steps over `ctas`

@@ -411,7 +411,7 @@ cudaError_t launch_permute(const int32_t* idx, int T, int K, const ExpertShard& 
 
 // =====================================================================
 // Permutation for small batches (T*K <= 1024) in ONE CTA, from the top-K
-// of topk_cta_kernel: the per-expert histogram, offsets, active list, the
+// of the top-K kernel: the per-expert histogram, offsets, active list, the
 // stable slot order and its inverse (same results as the three
 // permutation kernels), and the tile list of the streaming expert kernels
 // (tiles of at most bn_max slots per expert: {expert, first slot, rows,
@@ -424,13 +424,14 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(const int32_t* __restr
                                                           int* __restrict__ slot, int bn_max,
                                                           int4* __restrict__ tiles, int* __restrict__ tile_count,
                                                           int* __restrict__ slot_tile, int split_expert) {
-  __shared__ int hist[2048];
-  __shared__ int base[2048];
+  __shared__ int hist[2048];   // assignments per bucket, then placement cursors, then tile heights
+  __shared__ int base[2048];   // first slot of each bucket, then (for active experts) first tile
+  __shared__ int placed[1024]; // assignment ids, grouped by bucket in arbitrary order within a bucket
+  __shared__ int act_s[1024];  // the active experts
   __shared__ int warp_tot[32];
   __shared__ int total_s, n_first;
   pdl_trigger();
   pdl_wait();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int TK = T * K;
   for (int e = threadIdx.x; e < E; e += 1024) hist[e] = 0;
   __syncthreads();
@@ -452,7 +453,10 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(const int32_t* __restr
     carry_off += total_s;
     const int flag = (c > 0 && e < sh.n_listed) ? 1 : 0;
     const int ax = block_exclusive_scan(flag, warp_tot, &total_s);
-    if (flag) active[1 + carry_act + ax] = e;
+    if (flag) {
+      active[1 + carry_act + ax] = e;
+      act_s[carry_act + ax] = e;
+    }
     carry_act += total_s;
   }
   if (threadIdx.x == 0) {
@@ -460,52 +464,58 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(const int32_t* __restr
     active[0] = carry_act;
     n_first = 0;
   }
+  // The stable slot order: an assignment's rank in its bucket is the number
+  // of smaller assignment ids there.  Expert buckets hold at most T entries
+  // (an expert is chosen at most once per token), so the rank is counted
+  // over the bucket's placed ids; the shard's bucket of other experts (up to
+  // T*K entries) takes an exclusive scan of its membership instead.
+  const bool other = a < TK && e_a == sh.n_listed && sh.n_buckets > sh.n_listed;
+  const int orank = block_exclusive_scan(other ? 1 : 0, warp_tot, &total_s);  // (synchronises)
+  for (int e = threadIdx.x; e < E; e += 1024) hist[e] = 0;  // placement cursors
   __syncthreads();
-  // stable scatter: rank among earlier assignments of the same expert
-  const unsigned peers = __match_any_sync(0xFFFFFFFFu, e_a);
-  const int rank = __popc(peers & ((1u << lane) - 1u));
-  const bool leader = (__ffs(peers) - 1) == lane;
-  for (int i = threadIdx.x; i < E; i += 1024) hist[i] = 0;  // reused as running counters
+  if (a < TK && !other) placed[base[e_a] + atomicAdd(&hist[e_a], 1)] = a;
   __syncthreads();
-  int before = 0;
-  const int n_warps_used = (TK + 31) / 32;
-  for (int wv = 0; wv < n_warps_used; ++wv) {
-    if (warp == wv && a < TK) {
-      before = hist[e_a];
-      __syncwarp(peers);
-      if (leader) hist[e_a] = before + __popc(peers);
-    }
-    __syncthreads();
-  }
+  int rank = 0, sl = 0;
   if (a < TK) {
-    const int sl = base[e_a] + before + rank;
+    rank = orank;
+    if (!other) {
+      rank = 0;
+      const int b0 = base[e_a], n = hist[e_a];
+      for (int j = 0; j < n; ++j) rank += placed[b0 + j] < a ? 1 : 0;
+    }
+    sl = base[e_a] + rank;
     perm[sl] = a;
     slot[a] = sl;
   }
   // tile list over the active experts (at most TK of them)
   const int n_act = carry_act;
-  int nsub = 0, e_t = 0, c_t = 0;
+  int nsub = 0, e_t = 0, c_t = 0, tn = 0;
   if (threadIdx.x < n_act) {
-    e_t = active[1 + threadIdx.x];
-    c_t = offsets[e_t + 1] - offsets[e_t];
+    e_t = act_s[threadIdx.x];
+    c_t = hist[e_t];
     nsub = (c_t + bn_max - 1) / bn_max;
+    const int per = (c_t + nsub - 1) / nsub;
+    tn = min((per + 15) & ~15, bn_max);  // tiles never exceed bn_max rows
   }
-  __syncthreads();
-  const int tb = block_exclusive_scan(nsub, warp_tot, &total_s);
+  const int tb = block_exclusive_scan(nsub, warp_tot, &total_s);  // (synchronises)
   // tiles of experts below split_expert come first (experts ascend)
   if (nsub > 0 && e_t < split_expert) atomicAdd(&n_first, nsub);
-  if (nsub > 0) {
-    const int per = (c_t + nsub - 1) / nsub;
-    const int tn = min((per + 15) & ~15, bn_max);  // tiles never exceed bn_max rows
-    for (int j = 0; j < nsub; ++j) {
-      const int r0 = j * tn;
-      const int rows = min(tn, c_t - r0);
-      tiles[tb + j] = make_int4(e_t, base[e_t] + r0, rows, (rows + 15) & ~15);
-      if (slot_tile)
-        for (int n = 0; n < rows; ++n) slot_tile[base[e_t] + r0 + n] = ((tb + j) << 8) | n;
-    }
+  for (int j = 0; j < nsub; ++j) {
+    const int r0 = j * tn;
+    const int rows = min(tn, c_t - r0);
+    tiles[tb + j] = make_int4(e_t, base[e_t] + r0, rows, (rows + 15) & ~15);
   }
   __syncthreads();
+  if (slot_tile) {
+    // slot -> (tile, row): rank r of an expert's slots is row r % tn of its
+    // tile r / tn (tn = the expert's tile height)
+    if (nsub > 0) {
+      hist[e_t] = tn;
+      base[e_t] = tb;
+    }
+    __syncthreads();
+    if (a < TK && !other) slot_tile[sl] = ((base[e_a] + rank / hist[e_a]) << 8) | (rank % hist[e_a]);
+  }
   if (threadIdx.x == 0) {
     tile_count[0] = total_s;
     tile_count[1] = n_first;
