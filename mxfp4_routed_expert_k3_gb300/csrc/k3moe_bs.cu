@@ -589,10 +589,18 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
     if (lane == 0) {
       int kg = 0, issued = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok;) {
+      // The next item is claimed two K steps before the current one ends
+      // and its tile entry read on the last step, so that the stage after
+      // the item's last has its copies ready (a claim and a dependent read
+      // at the boundary would leave a stage of the ring empty meanwhile;
+      // the copy thread waits for a free stage at those points anyway).
+      int4 next_tile = make_int4(0, 0, 0, 0);
+      bool have_tile = false;
+      for (int item = blockIdx.x, next = -1; item < n_items && ok;) {
         const BsItem bi = bs_item(p, item);
         const int ti = bi.ti, mt = bi.mt;
-        const int4 tile = p.tiles[ti];
+        const int4 tile = have_tile ? next_tile : p.tiles[ti];
+        have_tile = false;
         // (expert, first row block of the item) chunk 0
         const size_t tile0 = ((size_t)tile.x * p.MT * C::kRB + (size_t)mt * C::kRB) * p.KC;
         for (int ks = bi.k0; ks < bi.k1; ++ks, ++kg) {
@@ -600,6 +608,12 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
           if (u > 0 && !mbar_wait(sfree(s), (u - 1) & 1, g, 1u)) {
             ok = false;
             break;
+          }
+          if (ks == max(bi.k0, bi.k1 - 2))
+            next = p.next_item ? (int)gridDim.x + atomicAdd(p.next_item, 1) : item + (int)gridDim.x;
+          if (ks == bi.k1 - 1 && next < n_items) {
+            next_tile = p.tiles[bs_item(p, next).ti];
+            have_tile = true;
           }
           const int kc0 = ks * C::kNK;
           const int nk = min(C::kNK, p.KC - kc0);
@@ -633,7 +647,7 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
           bulk_load(st + C::kOffSfb, p.sfb + ((size_t)ti * p.KC + kc0) * 2 * kAtom, 2 * nk * kAtom, full(s));
           ++issued;
         }
-        if (ok) item = p.next_item ? (int)gridDim.x + atomicAdd(p.next_item, 1) : item + (int)gridDim.x;
+        item = next;
       }
       if (ok) {
         // the end of the work: a stage without copies whose item is -1
