@@ -315,13 +315,11 @@ def run_ours(args, rank, world, local_rank):
     launches = sum(len(per_kernel[T]) for T in batches)
     achieved = kern_bytes / (kern_ms / 1e3) / 1e9 if kern_ms > 0 else None
     path_used = layer.query("path_last")
-    kernel_id = {1: "gateup_gemv_kernel", 3: "umma_stream_kernel_gateup",
-                 4: "bs_stream_kernel_gateup"}.get(path_used, "umma_gemm_kernel_gateup")
+    kernel_id = {1: "gateup_gemv_kernel", 4: "bs_stream_kernel_gateup"}[path_used]
     kernel_desc = {1: "gateup_gemv_kernel (CUDA-core grouped MXFP4 gate/up GEMV + SiTU-GLU)",
-                   3: "umma_stream_kernel<GATEUP> (tcgen05, decoded MXFP4 weights in TMEM, SiTU-GLU epilogue)",
                    4: "bs_stream_kernel<GATEUP> (tcgen05 kind::mxf4: e2m1 weights as stored x six e2m1 "
                       "activation terms, UE8M0 scales in TMEM, SiTU-GLU + requantisation epilogue)"
-                   }.get(path_used, "umma_gemm_kernel<GATEUP> (tcgen05 grouped MXFP4 GEMM)")
+                   }[path_used]
     # ncu's DRAM bytes per active expert (captured on a smaller case, traffic
     # grows with the experts touched) times this run's mean active experts
     per_expert = recorded_traffic(kernel_id, "k3-decode")
