@@ -630,7 +630,7 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
     k3::umma_tile_list(c->umma, &tiles, &tile_count, &bn);
     // with the slot -> tile map (the tiles have bs_tile_rows(T) <= bn rows)
     int* slot_tile = k3::bs_slot_tile(c->bs);
-    bn = k3::bs_tile_rows(T);
+    bn = k3::bs_tile_rows(T, c->bank2_begin != 0);
     K3_LAUNCH(k3::launch_route_small(w.logits, T, d.E, c->bias, d.K, d.norm_topk, d.rsf, c->shard, idx, wts,
                                      w.counts, w.offsets, w.active, w.perm, w.slot, bn, tiles, tile_count, slot_tile,
                                      split_expert, s),
@@ -648,7 +648,7 @@ static int forward_impl(k3moe_ctx* c, const void* x, int T, void* y, int32_t* id
     int* tile_count;
     int bn;
     k3::umma_tile_list(c->umma, &tiles, &tile_count, &bn);
-    bn = k3::bs_tile_rows(T);
+    bn = k3::bs_tile_rows(T, c->bank2_begin != 0);
     if (!fused_route)
       K3_LAUNCH(k3::umma_stream_tiles(c->umma, w, T, d, bn, k3::bs_slot_tile(c->bs), split_expert, s), 2,
                 "tile list");

@@ -418,6 +418,9 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
 //   16 (T <= 128): kind::mxf4, six e2m1 activation terms (N = 96), two CTAs
 //      per SM with four (gate/up) or three (down) stages; the kernel
 //      streams weights;
+//    8 (T <= 8, where no expert has more than 8 slots): the same with
+//      N = 48; the smaller stages leave room for five (gate/up) or four
+//      (down) stages per CTA and two gate/up accumulator buffers;
 //   88 (larger batches): kind::mxf8f6f4, two e4m3 terms (N = 176); one
 //      CTA per SM with four stages and two accumulators (gate and up, or
 //      two row blocks of down: 352 TMEM columns).
@@ -469,10 +472,10 @@ struct BsCfg {
   static constexpr int kOffSfa = kOffB + kTerms * kNK * kB;
   static constexpr int kOffSfb = kOffSfa + kNA * kAtom;
   static constexpr int kStageBytes = (kOffSfb + 2 * kNK * kAtom + 1023) / 1024 * 1024;
-  static constexpr int kStages = kWide ? 4 : !kFp4 ? 2 : MODE == BS_GATEUP ? 4 : 3;
+  static constexpr int kStages = kWide ? 4 : !kFp4 ? 2 : MODE == BS_GATEUP ? (NQ <= 8 ? 5 : 4) : (NQ <= 8 ? 4 : 3);
   // accumulator buffers: one where the stacked accumulators fill the CTA's
   // columns (the epilogue then releases the buffer as soon as it has read it)
-  static constexpr int kDBuf = (kBig || MODE == BS_GATEUP) ? 1 : 2;
+  static constexpr int kDBuf = (kBig || (MODE == BS_GATEUP && NQ > 8)) ? 1 : 2;
   static constexpr int kAccW = kTerms * NQ;  // accumulator columns (MMA N)
   static constexpr int kAccStride = (kWide || kFp4) ? kAccW : 128;          // TMEM columns between matrices
   static constexpr int kBufStride = kNumA * kAccStride;                     // TMEM columns between buffers
@@ -799,9 +802,19 @@ __global__ void __launch_bounds__(BsCfg<MODE, NQ>::kThreads, BsCfg<MODE, NQ>::kC
       // 32-column loads.  Stacked, token j's partial sums are added here.
       constexpr bool kPair = !C::kBig;
       constexpr int JW = kPair ? NQ : 32;
-      static_assert(!kPair || (2 * NQ == 32 && C::kTerms % 2 == 0), "decode accumulator layout");
+      static_assert(!kPair || ((NQ == 16 || NQ == 8) && C::kTerms == 6), "decode accumulator layout");
       auto load_acc = [&](uint32_t base, int j0, float* v) {
-        if (kPair) {
+        if constexpr (kPair && NQ == 8) {
+          // 16-column block b holds terms 2b and 2b + 1 of the 8 tokens (every
+          // load starts at a multiple of its width; the accumulators are 48
+          // columns apart); added in the pairs the 16-row tiles use
+          float a[16], b[16], c[16];
+          tmem_ld16(base, a);
+          tmem_ld16(base + 16, b);
+          tmem_ld16(base + 32, c);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = (a[j] + a[j + 8]) + (b[j] + b[j + 8]) + (c[j] + c[j + 8]);
+        } else if (kPair) {
           // 32-column block b holds terms 2b and 2b + 1 of the NQ tokens
           tmem_ld32(base, v);
 #pragma unroll
@@ -1585,6 +1598,8 @@ cudaError_t prepare_bs_kernels() {
   auto set = [&](const void* f, int bytes) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   };
+  set((const void*)bs_stream_kernel<BS_GATEUP, kBsSmallRows>, BsCfg<BS_GATEUP, kBsSmallRows>::kSmem);
+  set((const void*)bs_stream_kernel<BS_DOWN, kBsSmallRows>, BsCfg<BS_DOWN, kBsSmallRows>::kSmem);
   set((const void*)bs_stream_kernel<BS_GATEUP, kBsDecodeRows>, BsCfg<BS_GATEUP, kBsDecodeRows>::kSmem);
   set((const void*)bs_stream_kernel<BS_DOWN, kBsDecodeRows>, BsCfg<BS_DOWN, kBsDecodeRows>::kSmem);
   set((const void*)bs_stream_kernel<BS_GATEUP, kBsPrefillRows>, BsCfg<BS_GATEUP, kBsPrefillRows>::kSmem);
@@ -1598,10 +1613,12 @@ cudaError_t bs_quantize_latent(const BsPlan& p, const Work& w, int T, const Dims
                                const int* n_local, cudaStream_t s) {
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
-  if (T > p.max_tokens || (tile_rows != kBsDecodeRows && tile_rows != kBsPrefillRows)) return cudaErrorInvalidValue;
+  if (T > p.max_tokens || (tile_rows != kBsSmallRows && tile_rows != kBsDecodeRows && tile_rows != kBsPrefillRows) ||
+      (tile_rows == kBsSmallRows && T > kBsSmallMaxT))
+    return cudaErrorInvalidValue;
   const int stack = tile_rows;
   const BsWs ws = bs_ws_view(p.ws, d, p.max_tokens);
-  const bool fp4 = tile_rows == kBsDecodeRows && BsCfg<BS_GATEUP, kBsDecodeRows>::kFp4;
+  const bool fp4 = tile_rows != kBsPrefillRows;
   if (!fp4) {
     // prefill tiles: each token's row split once, its terms written to the
     // token's K slots (the split is ALU work, the copies a memory stream)
@@ -1655,13 +1672,13 @@ float* bs_down_parts(const BsPlan& p, const Dims& d) {
 // row per lane, the 32 rows one scale group of the down GEMM's K.  With an
 // expert shard only the shard's own slots [0, *rows_dev) are finished: the
 // other slots have no partial sums and no tile this forward.
+template <int kHStack>
 __global__ void __launch_bounds__(256) bs_gateup_finish_kernel(const BsParams p, const int* __restrict__ slot_tile,
                                                                int TK, const int* __restrict__ rows_dev) {
   pdl_trigger();
   pdl_wait();
   if (rows_dev) TK = min(TK, *rows_dev);
-  constexpr int kHTerms = BsCfg<BS_DOWN, kBsDecodeRows>::kTerms;
-  constexpr int kHStack = kBsDecodeRows;
+  constexpr int kHTerms = BsCfg<BS_DOWN, kHStack>::kTerms;
   const int lane = threadIdx.x & 31;
   const int G = p.ld_out / 32, KCo = p.ld_out / kQK;
   const int nw = (int)((gridDim.x * blockDim.x) >> 5);
@@ -1713,7 +1730,7 @@ cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* t
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
   if (T > p.max_tokens || n_split < 1 || n_split > kBsMaxSplit ||
-      (n_split > 1 && (T != 1 || tile_rows != kBsDecodeRows)))
+      (n_split > 1 && (T != 1 || tile_rows > kBsDecodeRows)))
     return cudaErrorInvalidValue;
   const BsWs ws = bs_ws_view(p.ws, d, p.max_tokens);
   BsParams prm{};
@@ -1728,15 +1745,21 @@ cudaError_t bs_stream_gateup(const BsPlan& p, const BsWeights& bw, const int4* t
   prm.part_a = ws.part;
   prm.part_b = ws.part + (size_t)kBsMaxSplit * d.K * d.I;
   prm.next_item = ws.sched;
-  if (tile_rows == kBsDecodeRows && n_split > 1) {
-    cudaError_t e = launch_bs<BS_GATEUP, kBsDecodeRows>(p, bw.gu_q, bw.gu_sf, bw.n_exp, d.I, d.L, ws.lq, ws.lsf,
-                                                        ws.rows_fp4, tiles, tile_count, prm, s);
+  if (n_split > 1) {
+    const bool small = tile_rows == kBsSmallRows;
+    cudaError_t e = small ? launch_bs<BS_GATEUP, kBsSmallRows>(p, bw.gu_q, bw.gu_sf, bw.n_exp, d.I, d.L, ws.lq, ws.lsf,
+                                                                ws.rows_fp4, tiles, tile_count, prm, s)
+                          : launch_bs<BS_GATEUP, kBsDecodeRows>(p, bw.gu_q, bw.gu_sf, bw.n_exp, d.I, d.L, ws.lq,
+                                                                 ws.lsf, ws.rows_fp4, tiles, tile_count, prm, s);
     if (e != cudaSuccess) return e;
     prm.rows_max = ws.rows_fp4;
     const int warps = TK * (d.I / 32);
-    return launch_pdl(bs_gateup_finish_kernel, (warps + 7) / 8, 256, 0, s, prm, (const int*)ws.slot_tile, TK,
-                      n_local);
+    return launch_pdl(small ? bs_gateup_finish_kernel<kBsSmallRows> : bs_gateup_finish_kernel<kBsDecodeRows>,
+                      (warps + 7) / 8, 256, 0, s, prm, (const int*)ws.slot_tile, TK, n_local);
   }
+  if (tile_rows == kBsSmallRows)
+    return launch_bs<BS_GATEUP, kBsSmallRows>(p, bw.gu_q, bw.gu_sf, bw.n_exp, d.I, d.L, ws.lq, ws.lsf, ws.rows_fp4,
+                                              tiles, tile_count, prm, s);
   if (tile_rows == kBsDecodeRows)
     return launch_bs<BS_GATEUP, kBsDecodeRows>(p, bw.gu_q, bw.gu_sf, bw.n_exp, d.I, d.L, ws.lq, ws.lsf, ws.rows_fp4,
                                                tiles, tile_count, prm, s);
@@ -1751,7 +1774,7 @@ cudaError_t bs_stream_down(const BsPlan& p, const BsWeights& bw, const int4* til
   const int TK = T * d.K;
   if (TK <= 0) return cudaSuccess;
   if (T > p.max_tokens || n_split < 1 || n_split > kBsMaxSplit ||
-      (n_split > 1 && (T != 1 || tile_rows != kBsDecodeRows)))
+      (n_split > 1 && (T != 1 || tile_rows > kBsDecodeRows)))
     return cudaErrorInvalidValue;
   const BsWs ws = bs_ws_view(p.ws, d, p.max_tokens);
   BsParams prm{};
@@ -1761,6 +1784,9 @@ cudaError_t bs_stream_down(const BsPlan& p, const BsWeights& bw, const int4* til
   prm.part_rows = TK;
   prm.part_a = ws.part + (size_t)kBsMaxSplit * d.K * 2 * d.I;  // the combine adds the parts
   prm.next_item = ws.sched + 1;
+  if (tile_rows == kBsSmallRows)
+    return launch_bs<BS_DOWN, kBsSmallRows>(p, bw.d_q, bw.d_sf, bw.n_exp, d.L, d.I, ws.hq, ws.hsf, ws.rows_fp4, tiles,
+                                            tile_count, prm, s);
   if (tile_rows == kBsDecodeRows)
     return launch_bs<BS_DOWN, kBsDecodeRows>(p, bw.d_q, bw.d_sf, bw.n_exp, d.L, d.I, ws.hq, ws.hsf, ws.rows_fp4, tiles,
                                              tile_count, prm, s);

@@ -56,11 +56,17 @@ struct BsPlan {
 // kernel's four-stage ring allows: 88 rows (N = 176), which keeps an
 // expert of up to 176 slots -- nearly every expert of a uniform T = 8192
 // batch, ~146 +- 12 slots -- at two tiles.
+constexpr int kBsSmallRows = 8;
+constexpr int kBsSmallMaxT = 8;     // largest T run on 8-row decode tiles (no expert has more slots)
 constexpr int kBsDecodeRows = 16;
 constexpr int kBsPrefillRows = 88;
 constexpr int kBsDecodeMaxT = 128;  // largest T run on decode tiles
 constexpr int kBsMaxSplit = 4;      // most K parts of a T = 1 work item
-inline int bs_tile_rows(int T) { return T <= kBsDecodeMaxT ? kBsDecodeRows : kBsPrefillRows; }
+// The token-tile height of the expert kernels for T tokens; the second
+// bank's decode kernel works on 16-row tiles only.
+inline int bs_tile_rows(int T, bool bank2 = false) {
+  return (T <= kBsSmallMaxT && !bank2) ? kBsSmallRows : T <= kBsDecodeMaxT ? kBsDecodeRows : kBsPrefillRows;
+}
 size_t bs_ws_bytes(const Dims& d, int max_tokens);
 // slot -> (tile << 8 | row in tile), written by the tile-list builders
 int* bs_slot_tile(const BsPlan& p);

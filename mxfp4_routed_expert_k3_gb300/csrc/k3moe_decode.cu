@@ -527,8 +527,11 @@ cudaError_t launch_route_small(const float* logits, int T, int E, const float* b
                                int* perm, int* slot, int bn_max, int4* tiles, int* tile_count, int* slot_tile,
                                int split_expert, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  // tiles of at least 16 rows (the tile list's capacity), row field of 8 bits
-  if (T * K > 1024 || E > 2048 || sh.n_buckets > 2048 || bn_max < 16 || bn_max > 255) return cudaErrorInvalidValue;
+  // tiles of at least 16 rows (the tile list's capacity), or shorter ones
+  // when no expert can have more slots than a tile (T <= bn_max: one tile
+  // per expert); row field of 8 bits
+  if (T * K > 1024 || E > 2048 || sh.n_buckets > 2048 || bn_max < 1 || bn_max > 255 || (bn_max < 16 && T > bn_max))
+    return cudaErrorInvalidValue;
   cudaError_t e = launch_topk(logits, T, E, E, bias, K, norm_topk, rsf, idx, w, s);
   if (e != cudaSuccess) return e;
   return launch_pdl(perm_small_kernel, 1, 1024, 0, s, idx, T, sh.n_buckets, K, sh, counts, offsets, active, perm, slot,
