@@ -84,7 +84,8 @@ typedef struct {
                          T <= 64) and the expert GEMMs on the block-scaled
                          MXFP4 tensor cores (e2m1 weights and e8m0 scales
                          as stored; up to T = 128 tcgen05 kind::mxf4 on
-                         tiles of 16 token rows with the activations as six
+                         tiles of 16 token rows (8 for T <= 8 without a
+                         second bank) with the activations as six
                          block-scaled e2m1 terms, above that
                          kind::mxf8f6f4 on tiles of 88 rows with two exact
                          e4m3 terms; the terms of a tile form one MMA
