@@ -536,7 +536,7 @@ __global__ void __launch_bounds__(B2Cfg<GU>::kThreads, 1)
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-constexpr int kMinTileRows = 16;  // the shortest tile height any tile list uses
+constexpr int kMinTileRows = 16;  // the shortest tile height of a list with more than one tile per expert
 constexpr int kDThreads = 192;
 
 // =====================================================================
@@ -900,7 +900,8 @@ struct WsLayout {
 WsLayout ws_layout(const Dims& d, int max_tokens) {
   auto up = [](size_t v) { return (v + 255) / 256 * 256; };
   // every tile list holds tiles of at least kMinTileRows rows (one expert
-  // each): at most E + T*K / kMinTileRows of them
+  // each), or shorter ones only where no expert has more slots than a tile
+  // holds (one tile per expert): at most E + T*K / kMinTileRows of them
   const size_t max_tiles = (size_t)max_tokens * d.K / kMinTileRows + d.E + 1;
   WsLayout l;
   l.tiles_off = 0;
